@@ -1,0 +1,360 @@
+"""CPU oracle for the tensor-parallel pre-RMSNorm MLP sublayer (numpy, float64).
+
+TEST INFRASTRUCTURE ONLY.  Nothing on the product path imports this module:
+only ``tests/``, ``__graft_entry__.smoke()`` and the CPU-baseline leg of
+``bench.py`` may call it.  It shares no code with the CUDA library.
+
+Sources (web pages, cited by title and section):
+
+* "Megatron tensor-parallel MLP" (synapticradio.com/post/megatron-tensor-
+  parallel-mlp) -- the dense block under test ("Start with the dense block"),
+  the shared FFN interval, the column-parallel expansion ("Split the
+  expansion"), the row-parallel contraction and its forward all-reduce
+  ("Split the contraction"), the backward all-reduce ("Put the other
+  collective in backward"), the one-step training comparison ("Reproduce one
+  dense training step") and the two broken variants ("Remove each
+  collective").
+* "Megatron-LM walkthrough" (stanleyjacob.dev) -- the f and g operators
+  ("Deep dive: tensor parallelism and the f and g operators"), the GeLU MLP
+  built from ColumnParallelLinear/RowParallelLinear (Part II), fp32 master
+  parameters in the optimizer step ("Stage 8").
+* "Megatron-LM Explained" (trishampatil.com) -- the GeLU MLP split A by
+  columns, B by rows ("The MLP block: column-parallel, then row-parallel").
+
+Readings where the pages are silent:
+
+* RMSNorm is called but never defined: y = x * (mean_h x^2 + eps)^(-1/2) * w,
+  eps inside the root, no centring, no bias.
+* The display equations of the dense block are missing from the extracted
+  text; the algebra is that of ``F.linear`` as used by the printed code
+  (``linear(x, W) = x W^T``).
+* GeLU is the exact erf form.
+* Loss is 0.5 * mean((y - target)^2) over all N*H elements.
+* SGD is plain ``w <- w - lr * g`` (no momentum, no weight decay).
+* Backward formulas (never written on the pages) are derived by hand from the
+  forward and pinned by central finite differences in the tests.
+
+Parity pins: every function here is pinned in ``tests/test_oracle_pins.py``
+against closed forms, brute-force loops, finite differences and the page's
+invariants (sharded == dense; the two fault patterns).  No function is
+"parity unpinned".
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+# ---------------------------------------------------------------------------
+# Element-wise pieces
+# ---------------------------------------------------------------------------
+
+
+def rms_norm(x: np.ndarray, w: np.ndarray, eps: float):
+    """Pre-norm of the block ("Start with the dense block": ``rms_norm(x,
+    norm_weight)``).  Returns (normed, rstd [N], xhat)."""
+    x = np.asarray(x, dtype=np.float64)
+    ms = np.mean(x * x, axis=-1)
+    rstd = 1.0 / np.sqrt(ms + eps)
+    xhat = x * rstd[:, None]
+    return xhat * np.asarray(w, dtype=np.float64), rstd, xhat
+
+
+def sigmoid(z):
+    return 1.0 / (1.0 + np.exp(-z))
+
+
+def silu(z):
+    """SiLU(z) = z * sigmoid(z) -- ``F.silu`` in the dense block."""
+    return z * sigmoid(z)
+
+
+def silu_grad(z):
+    """d SiLU / dz = s * (1 + z * (1 - s)), s = sigmoid(z)."""
+    s = sigmoid(z)
+    return s * (1.0 + z * (1.0 - s))
+
+
+_ERF = np.vectorize(math.erf, otypes=[np.float64])
+
+
+def _erf(z):
+    try:
+        from scipy.special import erf  # exact to double rounding
+        return erf(z)
+    except Exception:  # pragma: no cover - scipy absent
+        return _ERF(z)
+
+
+def gelu(z):
+    """Exact GeLU, z * Phi(z) (Megatron-LM walkthrough, Part II ``gelu(y)``)."""
+    return 0.5 * z * (1.0 + _erf(z / math.sqrt(2.0)))
+
+
+def gelu_grad(z):
+    """d GeLU / dz = Phi(z) + z * phi(z)."""
+    return 0.5 * (1.0 + _erf(z / math.sqrt(2.0))) + z * np.exp(-0.5 * z * z) / math.sqrt(2.0 * math.pi)
+
+
+def linear(x, w, b=None):
+    """``F.linear(x, w, b) = x w^T + b`` (weights stored [out, in])."""
+    y = x @ w.T
+    return y if b is None else y + b
+
+
+# ---------------------------------------------------------------------------
+# Dense block (the result the sharded path must reproduce)
+# ---------------------------------------------------------------------------
+
+
+def dense_forward(p: dict, x: np.ndarray, eps: float, act: str = "swiglu"):
+    """Dense pre-RMSNorm MLP ("Start with the dense block").
+
+    SwiGLU: y = x + W_d (SiLU(W_g n) * (W_u n)) + b_d, n = RMSNorm(x).
+    GeLU (walkthrough Part II; "The MLP block"): y = x + W_d GeLU(W_1 n + b_1) + b_d.
+    Returns (y, cache)."""
+    x = np.asarray(x, dtype=np.float64)
+    n, rstd, xhat = rms_norm(x, p["norm_w"], eps)
+    c = {"x": x, "n": n, "rstd": rstd, "xhat": xhat, "act": act}
+    if act == "swiglu":
+        gate = linear(n, p["w_gate_up"][0])
+        up = linear(n, p["w_gate_up"][1])
+        hidden = silu(gate) * up
+        c.update(gate=gate, up=up)
+    else:
+        z = linear(n, p["w_1"], p["b_1"])
+        hidden = gelu(z)
+        c.update(z=z)
+    c["hidden"] = hidden
+    y = x + linear(hidden, p["w_down"], p["b_down"])
+    return y, c
+
+
+def mse_loss(y: np.ndarray, target: np.ndarray):
+    """Loss of the training step: 0.5 * mean((y - target)^2); returns (loss, dy)."""
+    d = np.asarray(y, dtype=np.float64) - np.asarray(target, dtype=np.float64)
+    return 0.5 * float(np.mean(d * d)), d / d.size
+
+
+def rms_norm_backward(dn, xhat, rstd, w):
+    """Gradient through n = xhat * w, xhat = x * rstd.
+
+    Returns (dx_norm, dnorm_w): dx_norm = rstd * (g - xhat * mean_h(g * xhat)),
+    g = dn * w; dnorm_w = sum_tokens dn * xhat."""
+    g = dn * w
+    dxn = rstd[:, None] * (g - xhat * np.mean(g * xhat, axis=-1, keepdims=True))
+    return dxn, np.sum(dn * xhat, axis=0)
+
+
+def dense_backward(p: dict, c: dict, dy: np.ndarray) -> dict:
+    """Backward of ``dense_forward`` (what autograd computes in the dense
+    reference of "Reproduce one dense training step").  Keys of the result:
+    x, norm_w, w_gate_up | (w_1, b_1), w_down, b_down."""
+    g = {"b_down": np.sum(dy, axis=0), "w_down": dy.T @ c["hidden"]}
+    dh = dy @ p["w_down"]
+    if c["act"] == "swiglu":
+        dgate = dh * c["up"] * silu_grad(c["gate"])
+        dup = dh * silu(c["gate"])
+        g["w_gate_up"] = np.stack([dgate.T @ c["n"], dup.T @ c["n"]])
+        dn = dgate @ p["w_gate_up"][0] + dup @ p["w_gate_up"][1]
+    else:
+        dz = dh * gelu_grad(c["z"])
+        g["w_1"] = dz.T @ c["n"]
+        g["b_1"] = np.sum(dz, axis=0)
+        dn = dz @ p["w_1"]
+    dxn, g["norm_w"] = rms_norm_backward(dn, c["xhat"], c["rstd"], p["norm_w"])
+    g["x"] = dy + dxn
+    g["_dn"] = dn
+    return g
+
+
+def sgd(p: dict, g: dict, lr: float) -> dict:
+    """Plain SGD, the update that closes the page's one-step comparison:
+    w <- w - lr * g."""
+    return {k: p[k] - lr * g[k] for k in p}
+
+
+def dense_step(p: dict, x, target, eps: float, lr: float, act: str = "swiglu") -> dict:
+    """Forward, loss, backward and SGD of the dense block."""
+    y, c = dense_forward(p, x, eps, act)
+    loss, dy = mse_loss(y, target)
+    g = dense_backward(p, c, dy)
+    return {"y": y, "loss": loss, "dy": dy, "grads": g, "new_params": sgd(p, {k: g[k] for k in p}, lr),
+            "cache": c}
+
+
+# ---------------------------------------------------------------------------
+# Literal t-rank decomposition
+# ---------------------------------------------------------------------------
+
+
+class ShapeError(ValueError):
+    pass
+
+
+def shard_interval(ffn: int, t: int, rank: int):
+    """Shared FFN interval of one rank ("Start with the dense block", the
+    fixture's slicing): asserts F % t == 0; rank r owns [r F/t, (r+1) F/t)
+    of the gate rows, the up rows and the down columns alike."""
+    if t < 1 or ffn % t != 0:
+        raise ShapeError(f"ffn={ffn} is not divisible by t={t}")
+    local = ffn // t
+    return rank * local, (rank + 1) * local
+
+
+def local_params(p: dict, t: int, rank: int, act: str) -> dict:
+    """Rank-local parameters: FFN-sliced projections, replicated norm_w/b_down."""
+    F = p["w_down"].shape[1]
+    lo, hi = shard_interval(F, t, rank)
+    q = {"norm_w": p["norm_w"], "w_down": p["w_down"][:, lo:hi], "b_down": p["b_down"]}
+    if act == "swiglu":
+        q["w_gate_up"] = p["w_gate_up"][:, lo:hi, :]
+    else:
+        q["w_1"] = p["w_1"][lo:hi]
+        q["b_1"] = p["b_1"][lo:hi]
+    return q
+
+
+def copy_to_tp_region_forward(n):
+    """f forward: identity ("Put the other collective in backward")."""
+    return n
+
+
+def reduce_from_tp_region_forward(partials):
+    """g forward: all-reduce(SUM) of the rank partials, summed in rank order
+    0..t-1 ("Split the contraction")."""
+    acc = np.zeros_like(partials[0])
+    for pr in partials:
+        acc = acc + pr
+    return acc
+
+
+def copy_to_tp_region_backward(local_grads):
+    """f backward: all-reduce(SUM) of the rank-local normed-input gradients."""
+    return reduce_from_tp_region_forward(local_grads)
+
+
+def rank_forward(q: dict, x, eps: float, act: str):
+    """One rank's work up to its partial output ("Split the expansion",
+    "Split the contraction"): partial = local hidden @ W_d_local^T."""
+    n, rstd, xhat = rms_norm(x, q["norm_w"], eps)
+    n_par = copy_to_tp_region_forward(n)
+    c = {"n": n_par, "rstd": rstd, "xhat": xhat, "act": act}
+    if act == "swiglu":
+        gate = linear(n_par, q["w_gate_up"][0])
+        up = linear(n_par, q["w_gate_up"][1])
+        c.update(gate=gate, up=up)
+        hidden = silu(gate) * up
+    else:
+        z = linear(n_par, q["w_1"], q["b_1"])
+        c["z"] = z
+        hidden = gelu(z)
+    c["hidden"] = hidden
+    return linear(hidden, q["w_down"]), c
+
+
+def rank_backward_local(q: dict, c: dict, dy):
+    """Rank-local part of the backward, before the f all-reduce: local weight
+    gradients and the local contribution to the normed-input gradient.
+    g backward is the identity, so every rank starts from the same dy."""
+    g = {"w_down": dy.T @ c["hidden"], "b_down": np.sum(dy, axis=0)}
+    dh = dy @ q["w_down"]
+    if c["act"] == "swiglu":
+        dgate = dh * c["up"] * silu_grad(c["gate"])
+        dup = dh * silu(c["gate"])
+        g["w_gate_up"] = np.stack([dgate.T @ c["n"], dup.T @ c["n"]])
+        dn_local = dgate @ q["w_gate_up"][0] + dup @ q["w_gate_up"][1]
+    else:
+        dz = dh * gelu_grad(c["z"])
+        g["w_1"] = dz.T @ c["n"]
+        g["b_1"] = np.sum(dz, axis=0)
+        dn_local = dz @ q["w_1"]
+    return g, dn_local
+
+
+def sharded_step(p: dict, x, target, eps: float, lr: float, t: int, act: str = "swiglu",
+                 skip_forward_reduce: bool = False, skip_backward_reduce: bool = False,
+                 view_rank: int = 0, backward_dy: str = "own") -> dict:
+    """One training step of the t-rank decomposition, rank by rank.
+
+    ``skip_forward_reduce`` / ``skip_backward_reduce`` reproduce the two broken
+    variants of "Remove each collective": the g (forward) or f (backward)
+    all-reduce replaced by each rank's own local value.
+
+    ``backward_dy``: "own" -- every rank back-propagates the dy of its own
+    loss (the multi-process behaviour); "view" -- every rank uses the dy of
+    ``view_rank`` (a single-process view; identical to "own" unless the forward
+    reduction is skipped).
+
+    Returns the quantities as rank ``view_rank`` sees them, with the sharded
+    weights (gradients and updated values) assembled from all ranks, plus the
+    per-rank records under "ranks"."""
+    x = np.asarray(x, dtype=np.float64)
+    F = p["w_down"].shape[1]
+    shard_interval(F, t, 0)  # divisibility check
+    qs = [local_params(p, t, r, act) for r in range(t)]
+    parts, caches = [], []
+    for r in range(t):
+        pr, c = rank_forward(qs[r], x, eps, act)
+        parts.append(pr)
+        caches.append(c)
+    if skip_forward_reduce:
+        mlp_out = parts
+    else:
+        red = reduce_from_tp_region_forward(parts)
+        mlp_out = [red for _ in range(t)]
+    ys = [x + mlp_out[r] + p["b_down"] for r in range(t)]
+    losses, dys = zip(*[mse_loss(ys[r], target) for r in range(t)])
+    use_dy = list(dys) if backward_dy == "own" else [dys[view_rank]] * t
+    gl, dnl = [], []
+    for r in range(t):
+        g, dn = rank_backward_local(qs[r], caches[r], use_dy[r])
+        gl.append(g)
+        dnl.append(dn)
+    if skip_backward_reduce:
+        dns = dnl
+    else:
+        red = copy_to_tp_region_backward(dnl)
+        dns = [red for _ in range(t)]
+    ranks = []
+    for r in range(t):
+        dxn, dnw = rms_norm_backward(dns[r], caches[r]["xhat"], caches[r]["rstd"], p["norm_w"])
+        gr = dict(gl[r])
+        gr["norm_w"] = dnw
+        gr["x"] = use_dy[r] + dxn
+        gr["_dn"] = dns[r]
+        newq = {k: qs[r][k] - lr * gr[k] for k in qs[r]}
+        ranks.append({"y": ys[r], "loss": losses[r], "dy": use_dy[r], "grads": gr, "new_params": newq})
+    v = ranks[view_rank]
+    grads = {"x": v["grads"]["x"], "norm_w": v["grads"]["norm_w"], "b_down": v["grads"]["b_down"],
+             "_dn": v["grads"]["_dn"]}
+    newp = {"norm_w": v["new_params"]["norm_w"], "b_down": v["new_params"]["b_down"]}
+    grads["w_down"] = np.concatenate([rk["grads"]["w_down"] for rk in ranks], axis=1)
+    newp["w_down"] = np.concatenate([rk["new_params"]["w_down"] for rk in ranks], axis=1)
+    if act == "swiglu":
+        grads["w_gate_up"] = np.concatenate([rk["grads"]["w_gate_up"] for rk in ranks], axis=1)
+        newp["w_gate_up"] = np.concatenate([rk["new_params"]["w_gate_up"] for rk in ranks], axis=1)
+    else:
+        for k, ax in (("w_1", 0), ("b_1", 0)):
+            grads[k] = np.concatenate([rk["grads"][k] for rk in ranks], axis=ax)
+            newp[k] = np.concatenate([rk["new_params"][k] for rk in ranks], axis=ax)
+    return {"y": v["y"], "loss": v["loss"], "dy": v["dy"], "grads": grads, "new_params": newp,
+            "ranks": ranks}
+
+
+# ---------------------------------------------------------------------------
+# Shape trace ("Reproduce one dense training step", the inspect output)
+# ---------------------------------------------------------------------------
+
+
+def shape_trace(S: int, B: int, H: int, F: int, t: int) -> dict:
+    """Dense and rank-local tensor shapes of the block laid out [S, B, H]."""
+    lo, hi = shard_interval(F, t, 0)
+    f = hi - lo
+    return {
+        "dense_shapes": {"x": [S, B, H], "norm_weight": [H], "w_gate_up": [2, F, H],
+                         "w_down": [H, F], "output": [S, B, H]},
+        "rank_local_shapes": {"gate_up_weight": [2, f, H], "gate": [S, B, f], "up": [S, B, f],
+                              "swiglu": [S, B, f], "down_weight": [H, f],
+                              "partial_output": [S, B, H]},
+    }

@@ -1,0 +1,105 @@
+"""The page's own setup, on CPU: two gloo ranks, each holding one FFN shard,
+with real all-reduces where the f and g operators put them ("Split the
+contraction", "Put the other collective in backward").  Each rank runs the
+oracle's rank-local functions; the collective sums come from torch.distributed.
+The result must equal the dense block, and each removed collective must break
+exactly what "Remove each collective" says.
+"""
+import os
+import socket
+
+import numpy as np
+import pytest
+
+torch = pytest.importorskip("torch")
+import torch.distributed as dist  # noqa: E402
+import torch.multiprocessing as mp  # noqa: E402
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _fixture():
+    rng = np.random.default_rng(1234)
+    N, H, F = 6, 8, 12
+    p = {"norm_w": 1.0 + 0.1 * rng.standard_normal(H),
+         "w_gate_up": 0.3 * rng.standard_normal((2, F, H)),
+         "w_down": 0.3 * rng.standard_normal((H, F)),
+         "b_down": 0.05 * rng.standard_normal(H)}
+    return p, rng.standard_normal((N, H)), rng.standard_normal((N, H))
+
+
+def _all_reduce(a):
+    t = torch.from_numpy(np.ascontiguousarray(a))
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return t.numpy()
+
+
+def _rank_main(rank, world, port, mode, out_dir):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import tpmlp_oracle as O
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        p, x, tgt = _fixture()
+        eps, lr = 1e-6, 0.1
+        q = O.local_params(p, world, rank, "swiglu")
+        partial, c = O.rank_forward(q, x, eps, "swiglu")
+        mlp_out = partial if mode == "missing_forward_reduce" else _all_reduce(partial)
+        y = x + mlp_out + p["b_down"]
+        loss, dy = O.mse_loss(y, tgt)
+        g, dn_local = O.rank_backward_local(q, c, dy)
+        dn = dn_local if mode == "missing_backward_reduce" else _all_reduce(dn_local)
+        dxn, g["norm_w"] = O.rms_norm_backward(dn, c["xhat"], c["rstd"], p["norm_w"])
+        g["x"] = dy + dxn
+        newq = {k: q[k] - lr * g[k] for k in q}
+        np.savez(os.path.join(out_dir, f"r{rank}.npz"), y=y, loss=loss, dx=g["x"], dnorm_w=g["norm_w"],
+                 dwgu=g["w_gate_up"], dwd=g["w_down"], dbd=g["b_down"], new_norm_w=newq["norm_w"],
+                 new_wgu=newq["w_gate_up"], new_wd=newq["w_down"])
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("mode", ["equivalence", "missing_forward_reduce", "missing_backward_reduce"])
+def test_two_gloo_ranks(tmp_path, mode):
+    from oracle import tpmlp_oracle as O
+    world = 2
+    mp.start_processes(_rank_main, args=(world, _free_port(), mode, str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    p, x, tgt = _fixture()
+    d = O.dense_step(p, x, tgt, 1e-6, 0.1)
+    s = O.sharded_step(p, x, tgt, 1e-6, 0.1, world,
+                       skip_forward_reduce=(mode == "missing_forward_reduce"),
+                       skip_backward_reduce=(mode == "missing_backward_reduce"))
+    F = p["w_down"].shape[1]
+    for r in range(world):
+        z = np.load(tmp_path / f"r{r}.npz")
+        lo, hi = O.shard_interval(F, world, r)
+        # the real-collective ranks agree with the oracle's in-process decomposition
+        rk = s["ranks"][r]
+        np.testing.assert_allclose(z["y"], rk["y"], rtol=0, atol=1e-14)
+        np.testing.assert_allclose(z["dx"], rk["grads"]["x"], rtol=0, atol=1e-15)
+        np.testing.assert_allclose(z["dwgu"], rk["grads"]["w_gate_up"], rtol=0, atol=1e-15)
+        dense_close = lambda a, b: float(np.max(np.abs(a - b))) < 1e-12
+        fwd_ok = dense_close(z["y"], d["y"])
+        dx_ok = dense_close(z["dx"], d["grads"]["x"])
+        dnw_ok = dense_close(z["dnorm_w"], d["grads"]["norm_w"])
+        dwgu_ok = dense_close(z["dwgu"], d["grads"]["w_gate_up"][:, lo:hi])
+        dwd_ok = dense_close(z["dwd"], d["grads"]["w_down"][:, lo:hi])
+        if mode == "equivalence":
+            assert fwd_ok and dx_ok and dnw_ok and dwgu_ok and dwd_ok
+            assert dense_close(z["dbd"], d["grads"]["b_down"])
+            assert dense_close(z["new_wd"], d["new_params"]["w_down"][:, lo:hi])
+        elif mode == "missing_forward_reduce":
+            assert not fwd_ok and not dx_ok and not dnw_ok and not dwgu_ok and not dwd_ok
+        else:
+            assert fwd_ok and dwgu_ok and dwd_ok
+            assert not dx_ok and not dnw_ok
+            assert not dense_close(z["new_norm_w"], d["new_params"]["norm_w"])
