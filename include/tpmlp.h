@@ -1,0 +1,183 @@
+/*
+ * tpmlp -- the Megatron tensor-parallel MLP sublayer on one GB300 (sm_103a).
+ *
+ * The sublayer (page "Megatron tensor-parallel MLP", synapticradio.com,
+ * section "Start with the dense block"):
+ *
+ *     n  = RMSNorm(x) * norm_w                       (pre-norm)
+ *     G  = n W_g^T, U = n W_u^T                      (column-parallel, W_gate_up [2,F,H])
+ *     A  = SiLU(G) * U                                (per FFN shard, no reduction)
+ *     y  = x + sum_{s=0}^{t-1} A_s W_d,s^T + b_down   (row-parallel + the g reduction)
+ *
+ * or, with TPMLP_GELU (page "Megatron-LM walkthrough", Part II, and page
+ * "Megatron-LM Explained", "The MLP block: column-parallel, then row-parallel"):
+ *
+ *     A  = GeLU(n W_1^T + b_1),  W_1 [F,H], b_1 [F]
+ *
+ * plus the mirrored backward (the f reduction of the normed-input gradient,
+ * section "Put the other collective in backward"), a mean-squared-error loss
+ * and one SGD update.  The tensor-parallel degree t is a logical split of the
+ * FFN axis inside one process: rank r owns channels [r F/t, (r+1) F/t) of the
+ * gate rows, the up rows and the down columns alike (the fixture's shared
+ * interval, "Start with the dense block").  Both reductions are summed on the
+ * device inside the GEMM accumulators, in shard order 0..t-1.
+ *
+ * Conventions for every entry point:
+ *  - All tensors are row-major and contiguous, in device memory owned by the
+ *    caller.  The library never allocates or frees device memory: scratch
+ *    lives in a caller-provided workspace (tpmlp_bind_workspace).
+ *  - Element type: TPMLP_F32 -> every tensor is float.  TPMLP_BF16 -> x, y,
+ *    dy, dx, target and the parameters are bfloat16; all parameter
+ *    gradients and master weights are float (fp32 accumulate everywhere).
+ *  - Calls are asynchronous on the context's CUDA stream.  They return after
+ *    validating arguments and enqueuing kernels.  Device-side failures
+ *    (a bounded wait that gave up) are reported by tpmlp_sync.
+ *  - No call throws; each returns a tpmlp_status.  On error nothing is
+ *    enqueued, and tpmlp_last_error() holds a one-line message.
+ *  - Pointers must be 16-byte aligned.  H and F must be multiples of 8.
+ */
+#ifndef TPMLP_H_
+#define TPMLP_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define TPMLP_API __attribute__((visibility("default")))
+#else
+#define TPMLP_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct tpmlp_ctx tpmlp_ctx;
+
+typedef enum {
+  TPMLP_OK = 0,
+  TPMLP_ERR_ARG = 1,          /* null / misaligned pointer, bad value */
+  TPMLP_ERR_SHAPE = 2,        /* F % t != 0, H or F not a multiple of 8, tokens > max_tokens */
+  TPMLP_ERR_UNSUPPORTED = 3,  /* dtype/activation value, or device is not sm_103 */
+  TPMLP_ERR_ORDER = 4,        /* no workspace; backward before forward; sgd before backward */
+  TPMLP_ERR_CUDA = 5,         /* a CUDA runtime call failed */
+  TPMLP_ERR_TIMEOUT = 6       /* a bounded device-side wait gave up (reported by tpmlp_sync) */
+} tpmlp_status;
+
+typedef enum { TPMLP_F32 = 0, TPMLP_BF16 = 1 } tpmlp_dtype;
+typedef enum { TPMLP_SWIGLU = 0, TPMLP_GELU = 1 } tpmlp_act;
+
+/* Debug flags (tpmlp_set_debug).  The two SKIP flags reproduce the broken
+ * variants of section "Remove each collective" as seen by one rank `shard`:
+ *  SKIP_FWD_REDUCE: the g reduction is replaced by shard `shard`'s own
+ *    partial, y = x + A_s W_d,s^T + b_down; the backward then runs from that
+ *    output's dy for every shard.
+ *  SKIP_BWD_REDUCE: the f reduction is replaced by shard `shard`'s own
+ *    normed-input gradient.
+ *  FORCE_TIMEOUT: the next forward's first GEMM waits on an event that never
+ *    happens, gives up after ~2 ms and records TPMLP_ERR_TIMEOUT (tests the
+ *    bounded-wait path without a hang). */
+enum {
+  TPMLP_DBG_SKIP_FWD_REDUCE = 1u,
+  TPMLP_DBG_SKIP_BWD_REDUCE = 2u,
+  TPMLP_DBG_FORCE_TIMEOUT = 4u
+};
+
+typedef struct {
+  int64_t max_tokens; /* N upper bound (tokens = batch * seq) for workspace sizing */
+  int64_t hidden;     /* H */
+  int64_t ffn;        /* F */
+  int32_t max_t;      /* largest logical TP degree that will be passed to forward */
+  int32_t dtype;      /* tpmlp_dtype */
+  int32_t act;        /* tpmlp_act */
+  int32_t reserved;   /* must be 0 */
+} tpmlp_config;
+
+/* Validate `cfg` and create a context bound to `cuda_stream` (a cudaStream_t,
+ * NULL = legacy default stream) on the current device.  Host-only checks run
+ * first, so a bad config is rejected without touching the GPU. */
+TPMLP_API tpmlp_status tpmlp_create(const tpmlp_config* cfg, void* cuda_stream, tpmlp_ctx** out);
+
+/* Bytes of device workspace a context with `cfg` needs (saved activations
+ * n/rstd/G,U/A, the backward intermediates dGU and dN, reduction partials and
+ * the device status word).  0 if `cfg` is invalid. */
+TPMLP_API size_t tpmlp_workspace_bytes(const tpmlp_config* cfg);
+
+/* Hand the context `bytes` of device memory at `dev` (256-byte aligned).  The
+ * caller owns it and keeps it alive until tpmlp_destroy. Zeroes the status
+ * word (enqueued on the stream). */
+TPMLP_API tpmlp_status tpmlp_bind_workspace(tpmlp_ctx* ctx, void* dev, size_t bytes);
+
+/* Change the stream later calls enqueue on. */
+TPMLP_API tpmlp_status tpmlp_set_stream(tpmlp_ctx* ctx, void* cuda_stream);
+
+/* Forward of the sublayer for `tokens` rows (0 <= tokens <= max_tokens).
+ *  x [tokens,H], norm_w [H], w_gate_up [2,F,H] (SwiGLU; GeLU: W_1 [F,H]),
+ *  b_1 [F] (GeLU only, NULL for SwiGLU), w_down [H,F], b_down [H] -> y [tokens,H].
+ *  eps: RMSNorm epsilon, inside the square root.  t: logical TP degree,
+ *  1 <= t <= max_t and F % t == 0 (the fixture's divisibility assertion).
+ * The pointers of x and of the parameters are remembered: backward reads x,
+ * and sgd_step updates the parameters in place. */
+TPMLP_API tpmlp_status tpmlp_forward(tpmlp_ctx* ctx, int64_t tokens, const void* x, const void* norm_w,
+                           const void* w_gate_up, const void* b_1, const void* w_down,
+                           const void* b_down, float eps, int32_t t, void* y);
+
+/* loss = 0.5 * mean((y - target)^2) over tokens*H elements, written as one
+ * float to device memory `loss_dev`; dy = (y - target) / (tokens*H).
+ * y, target, dy: [tokens,H] in the activation dtype.  tokens from the last forward. */
+TPMLP_API tpmlp_status tpmlp_mse_loss_grad(tpmlp_ctx* ctx, const void* y, const void* target, void* dy,
+                                 float* loss_dev);
+
+/* Backward of the last forward, given dy [tokens,H].  Outputs: dx [tokens,H]
+ * (activation dtype); float gradients dnorm_w [H], dw_gate_up [2,F,H]
+ * (GeLU: dW_1 [F,H]), db_1 [F] (GeLU only, else NULL), dw_down [H,F],
+ * db_down [H].  Gradients are overwritten, not accumulated. */
+TPMLP_API tpmlp_status tpmlp_backward(tpmlp_ctx* ctx, const void* dy, void* dx, float* dnorm_w,
+                            float* dw_gate_up, float* db_1, float* dw_down, float* db_down);
+
+/* Bind float master copies of the parameters (same shapes) for the bf16
+ * dtype.  When bound, sgd_step updates the masters and rewrites the bf16
+ * parameters as their round-to-nearest-even copies.  All or none (b_1 only
+ * for GeLU).  Passing all NULL unbinds. */
+TPMLP_API tpmlp_status tpmlp_bind_master(tpmlp_ctx* ctx, float* norm_w, float* w_gate_up, float* b_1,
+                               float* w_down, float* b_down);
+
+/* One plain SGD update, w <- w - lr * g, of every parameter of the last
+ * forward with the gradients of the last backward.  F32: in place on the
+ * parameters.  BF16 with masters: masters updated, parameters re-rounded.
+ * BF16 without masters: parameters updated through float and re-rounded. */
+TPMLP_API tpmlp_status tpmlp_sgd_step(tpmlp_ctx* ctx, float lr);
+
+/* Debug flags (TPMLP_DBG_*) and the shard whose view the SKIP flags take. */
+TPMLP_API tpmlp_status tpmlp_set_debug(tpmlp_ctx* ctx, uint32_t flags, int32_t shard);
+
+/* Wait for the stream, then report an asynchronous CUDA error or a device
+ * status word set by a bounded wait (TPMLP_ERR_TIMEOUT; the word is cleared). */
+TPMLP_API tpmlp_status tpmlp_sync(tpmlp_ctx* ctx);
+
+/* Per-kernel CUDA-event timing on the context's stream: enable/disable, then
+ * read the summed milliseconds and launch counts per kernel id since the last
+ * read (this call synchronises the stream).  `n` = array capacity; returns
+ * the number of kernel ids written. */
+TPMLP_API tpmlp_status tpmlp_set_timing(tpmlp_ctx* ctx, int32_t enable);
+TPMLP_API int32_t tpmlp_read_kernel_times(tpmlp_ctx* ctx, float* ms, int64_t* launches, int32_t n);
+/* Name of kernel id `id` (0 <= id < tpmlp_num_kernel_ids()), or NULL. */
+TPMLP_API const char* tpmlp_kernel_name(int32_t id);
+TPMLP_API int32_t tpmlp_num_kernel_ids(void);
+
+/* Number of kernels this context has launched since creation. */
+TPMLP_API uint64_t tpmlp_launch_count(const tpmlp_ctx* ctx);
+
+/* Static text for a status code; the last error message of a context
+ * (or of the calling thread when ctx is NULL, e.g. after a failed create). */
+TPMLP_API const char* tpmlp_status_string(tpmlp_status s);
+TPMLP_API const char* tpmlp_last_error(const tpmlp_ctx* ctx);
+
+/* Free the host-side context.  Does not touch caller memory. */
+TPMLP_API void tpmlp_destroy(tpmlp_ctx* ctx);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* TPMLP_H_ */

@@ -1,0 +1,99 @@
+// Element-wise math fused into the GEMM epilogues.
+//
+// Page "Megatron tensor-parallel MLP" ("Split the expansion"): the SwiGLU
+// product SiLU(gate) * up is taken per FFN channel on the shard that owns it,
+// so it needs no communication and sits in the column-parallel GEMM's
+// epilogue.  ("Split the contraction"): bias and residual are added once,
+// after the shard sum, in the row-parallel GEMM's epilogue.  The backward
+// epilogues apply the derivative of the activation to dA = dy W_d.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+namespace tpmlp {
+
+enum EpiKind : int {
+  EPI_GATEUP_SWIGLU = 0,  // acc = [G | U] of 128 channels: store G, U, A = SiLU(G) * U
+  EPI_FC1_GELU = 1,       // Z = acc + b_1: store Z, A = GeLU(Z)
+  EPI_DOWN_RESID = 2,     // y = x + acc + b_down
+  EPI_DGRAD_SWIGLU = 3,   // dA = acc: store dG = dA U SiLU'(G), dU = dA SiLU(G)
+  EPI_DGRAD_GELU = 4,     // dZ = acc * GeLU'(Z)
+  EPI_STORE_F32 = 5       // out = acc (float)
+};
+
+// Pointers and leading dimensions (in elements) of the epilogue's operands.
+//  GATEUP_SWIGLU: out0 = GU [M, 2F] (G in [0,F), U in [F,2F)), out1 = A [M, F]
+//  FC1_GELU     : out0 = Z [M, F], out1 = A [M, F], vec = b_1 [F]
+//  DOWN_RESID   : out0 = y [M, H], in0 = x [M, H], vec = b_down [H]
+//  DGRAD_SWIGLU : in0 = GU [M, 2F], out0 = dGU [M, 2F]
+//  DGRAD_GELU   : in0 = Z [M, F], out0 = dZ [M, F]
+//  STORE_F32    : out0 = float [M, N]
+struct EpiParams {
+  void* out0;
+  void* out1;
+  const void* in0;
+  const void* vec;
+  int64_t ld_out0, ld_out1, ld_in0;
+  int64_t pair_off;  // F: column offset of U / dU in the paired layouts
+  int M, N;          // valid output rows / columns (channels for the paired layouts)
+};
+
+__device__ __forceinline__ float to_f(float v) { return v; }
+__device__ __forceinline__ float to_f(__nv_bfloat16 v) { return __bfloat162float(v); }
+template <typename T>
+__device__ __forceinline__ T from_f(float v);
+template <>
+__device__ __forceinline__ float from_f<float>(float v) { return v; }
+template <>
+__device__ __forceinline__ __nv_bfloat16 from_f<__nv_bfloat16>(float v) { return __float2bfloat16_rn(v); }
+
+__device__ __forceinline__ float sigmoid_f(float z) { return 1.0f / (1.0f + expf(-z)); }
+__device__ __forceinline__ float silu_f(float z) { return z * sigmoid_f(z); }
+// Exact (erf) GeLU and its derivative Phi(z) + z phi(z).
+__device__ __forceinline__ float gelu_f(float z) { return 0.5f * z * (1.0f + erff(z * 0.70710678118654752f)); }
+__device__ __forceinline__ float gelu_grad_f(float z) {
+  return 0.5f * (1.0f + erff(z * 0.70710678118654752f)) + z * expf(-0.5f * z * z) * 0.39894228040143268f;
+}
+// SwiGLU backward for one channel: (dG, dU) from dA, G, U.
+__device__ __forceinline__ void swiglu_bwd(float da, float g, float u, float& dg, float& du) {
+  const float s = sigmoid_f(g);
+  dg = da * u * s * (1.0f + g * (1.0f - s));
+  du = da * g * s;
+}
+
+// One output element (m, n) -- used by the SIMT path and by ragged chunks of
+// the tensor-core path.  For GATEUP_SWIGLU, `acc` is G and `acc2` is U of
+// channel n.
+template <int EPI, typename T>
+__device__ __forceinline__ void epi_elem(const EpiParams& p, int m, int n, float acc, float acc2) {
+  const int64_t mm = m;
+  if (EPI == EPI_GATEUP_SWIGLU) {
+    T* gu = static_cast<T*>(p.out0);
+    gu[mm * p.ld_out0 + n] = from_f<T>(acc);
+    gu[mm * p.ld_out0 + p.pair_off + n] = from_f<T>(acc2);
+    static_cast<T*>(p.out1)[mm * p.ld_out1 + n] = from_f<T>(silu_f(acc) * acc2);
+  } else if (EPI == EPI_FC1_GELU) {
+    const float z = acc + to_f(static_cast<const T*>(p.vec)[n]);
+    static_cast<T*>(p.out0)[mm * p.ld_out0 + n] = from_f<T>(z);
+    static_cast<T*>(p.out1)[mm * p.ld_out1 + n] = from_f<T>(gelu_f(z));
+  } else if (EPI == EPI_DOWN_RESID) {
+    const float x = to_f(static_cast<const T*>(p.in0)[mm * p.ld_in0 + n]);
+    const float b = to_f(static_cast<const T*>(p.vec)[n]);
+    static_cast<T*>(p.out0)[mm * p.ld_out0 + n] = from_f<T>(x + acc + b);
+  } else if (EPI == EPI_DGRAD_SWIGLU) {
+    const T* gu = static_cast<const T*>(p.in0);
+    float dg, du;
+    swiglu_bwd(acc, to_f(gu[mm * p.ld_in0 + n]), to_f(gu[mm * p.ld_in0 + p.pair_off + n]), dg, du);
+    T* o = static_cast<T*>(p.out0);
+    o[mm * p.ld_out0 + n] = from_f<T>(dg);
+    o[mm * p.ld_out0 + p.pair_off + n] = from_f<T>(du);
+  } else if (EPI == EPI_DGRAD_GELU) {
+    const float z = to_f(static_cast<const T*>(p.in0)[mm * p.ld_in0 + n]);
+    static_cast<T*>(p.out0)[mm * p.ld_out0 + n] = from_f<T>(acc * gelu_grad_f(z));
+  } else {
+    static_cast<float*>(p.out0)[mm * p.ld_out0 + n] = acc;
+  }
+}
+
+}  // namespace tpmlp

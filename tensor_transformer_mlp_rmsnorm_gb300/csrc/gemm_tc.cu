@@ -1,0 +1,489 @@
+// Persistent, warp-specialised bf16 GEMM on the sm_103a tensor cores.
+//
+//   warp 0      : TMA producer -- one thread streams 128x64 A and 256x64 B
+//                 tiles (128-byte swizzle) into a 4-stage shared-memory ring.
+//   warp 1      : owns tensor memory (512 columns = two 128x256 f32
+//                 accumulators) and one thread issues tcgen05.mma
+//                 (M=128, N=256, K=16), committing each stage back to the
+//                 producer and each finished tile to the epilogue.
+//   warps 2..5  : epilogue -- tcgen05.ld the accumulator (lane = row), apply
+//                 the fused element-wise step, store to global memory.  The
+//                 two accumulators let tile i's epilogue overlap tile i+1's
+//                 main loop.
+//
+// The contraction runs over up to two K segments in order.  For the
+// row-parallel down projection the K axis is the FFN axis, so shard s's
+// partial product A_s W_d,s^T is accumulated in shard order 0..t-1 into the
+// same tensor-memory tile: that *is* the g all-reduce of the page "Megatron
+// tensor-parallel MLP" ("Split the contraction"), done on-chip.  The normed-
+// input gradient GEMM likewise sums every shard's dN_s (the f all-reduce,
+// "Put the other collective in backward").  Restricting the segments to one
+// shard reproduces the broken variants of "Remove each collective".
+//
+// Every wait is bounded (1 s); a wait that gives up raises a CTA-wide abort
+// flag and a bit in the device status word, in-flight TMA copies and MMAs are
+// drained, tensor memory is released and the CTA exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include <mutex>
+
+#include "epilogue.cuh"
+#include "ptx_sm103.cuh"
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 64;
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
+constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
+constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t TMEM_COLS = 512;
+constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s per wait
+constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s for draining after an abort
+constexpr uint64_t FORCED_LIMIT_NS = 2000000ull;    // 2 ms for the forced-timeout debug wait
+
+struct TcParams {
+  int M, N;
+  int num_m_blk, num_n_blk, num_tiles, group_m;
+  int kb[4];  // two k-block segments [kb0, kb1), [kb2, kb3)
+  int paired;
+  int pair_off;
+  EpiParams ep;
+  uint32_t* status;
+  int force_timeout;
+};
+
+__device__ __forceinline__ void tile_coords(const TcParams& p, int tile, int& mb, int& nb) {
+  const int per_group = p.group_m * p.num_n_blk;
+  const int g = tile / per_group;
+  const int first_m = g * p.group_m;
+  const int gm = min(p.num_m_blk - first_m, p.group_m);
+  const int r = tile - g * per_group;
+  mb = first_m + r % gm;
+  nb = r / gm;
+}
+
+__device__ __forceinline__ uint4 pack8_bf16(const float* f) {
+  uint4 r;
+  __nv_bfloat162 h;
+  h = __floats2bfloat162_rn(f[0], f[1]);
+  r.x = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(f[2], f[3]);
+  r.y = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(f[4], f[5]);
+  r.z = *reinterpret_cast<uint32_t*>(&h);
+  h = __floats2bfloat162_rn(f[6], f[7]);
+  r.w = *reinterpret_cast<uint32_t*>(&h);
+  return r;
+}
+
+__device__ __forceinline__ void unpack8_bf16(uint4 v, float* f) {
+  const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    __nv_bfloat162 h = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+    float2 t = __bfloat1622float2(h);
+    f[2 * i] = t.x;
+    f[2 * i + 1] = t.y;
+  }
+}
+
+// Load 32 consecutive bf16 values as floats.
+__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* f) {
+  const uint4* s = reinterpret_cast<const uint4*>(src);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack8_bf16(s[i], f + 8 * i);
+}
+
+__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* f) {
+  uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 4; ++i) d[i] = pack8_bf16(f + 8 * i);
+}
+
+// Epilogue of 32 consecutive output columns [col, col+32) of one row.
+// v = accumulator values; u = second accumulator half (paired layouts).
+template <int EPI>
+__device__ __forceinline__ void epi_chunk(const EpiParams& ep, int row, int col, const float* v, const float* u) {
+  typedef __nv_bfloat16 T;
+  if (row >= ep.M || col >= ep.N) return;
+  if (col + 32 > ep.N) {
+    const int n = ep.N - col;
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < n) epi_elem<EPI, T>(ep, row, col + i, v[i], EPI == EPI_GATEUP_SWIGLU ? u[i] : 0.0f);
+    return;
+  }
+  const int64_t r = row;
+  float o[32];
+  if (EPI == EPI_GATEUP_SWIGLU) {
+    T* gu = static_cast<T*>(ep.out0) + r * ep.ld_out0 + col;
+    store32_bf16(gu, v);
+    store32_bf16(gu + ep.pair_off, u);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = silu_f(v[i]) * u[i];
+    store32_bf16(static_cast<T*>(ep.out1) + r * ep.ld_out1 + col, o);
+  } else if (EPI == EPI_FC1_GELU) {
+    float b[32];
+    load32_bf16(static_cast<const T*>(ep.vec) + col, b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) b[i] += v[i];
+    store32_bf16(static_cast<T*>(ep.out0) + r * ep.ld_out0 + col, b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = gelu_f(b[i]);
+    store32_bf16(static_cast<T*>(ep.out1) + r * ep.ld_out1 + col, o);
+  } else if (EPI == EPI_DOWN_RESID) {
+    float x[32], b[32];
+    load32_bf16(static_cast<const T*>(ep.in0) + r * ep.ld_in0 + col, x);
+    load32_bf16(static_cast<const T*>(ep.vec) + col, b);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = x[i] + v[i] + b[i];
+    store32_bf16(static_cast<T*>(ep.out0) + r * ep.ld_out0 + col, o);
+  } else if (EPI == EPI_DGRAD_SWIGLU) {
+    float g[32], uu[32];
+    const T* gu = static_cast<const T*>(ep.in0) + r * ep.ld_in0 + col;
+    load32_bf16(gu, g);
+    load32_bf16(gu + ep.pair_off, uu);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) swiglu_bwd(v[i], g[i], uu[i], o[i], uu[i]);
+    T* d = static_cast<T*>(ep.out0) + r * ep.ld_out0 + col;
+    store32_bf16(d, o);
+    store32_bf16(d + ep.pair_off, uu);
+  } else if (EPI == EPI_DGRAD_GELU) {
+    float z[32];
+    load32_bf16(static_cast<const T*>(ep.in0) + r * ep.ld_in0 + col, z);
+#pragma unroll
+    for (int i = 0; i < 32; ++i) o[i] = v[i] * gelu_grad_f(z[i]);
+    store32_bf16(static_cast<T*>(ep.out0) + r * ep.ld_out0 + col, o);
+  } else {
+    float4* d = reinterpret_cast<float4*>(static_cast<float*>(ep.out0) + r * ep.ld_out0 + col);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+  }
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
+                   const TcParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t tfull_bar[2];
+  __shared__ __align__(8) uint64_t tempty_bar[2];
+  __shared__ __align__(8) uint64_t drain_bar;
+  __shared__ __align__(8) uint64_t never_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sA = smem;
+  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
+  volatile int* abort_flag = &abort_sh;
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&full_bar[s], 1);
+      mbar_init(&empty_bar[s], 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(&tfull_bar[b], 1);
+      mbar_init(&tempty_bar[b], 128);
+    }
+    mbar_init(&drain_bar, 1);
+    mbar_init(&never_bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_a);
+    tma_prefetch_desc(&map_b);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, TMEM_COLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t stage = 0, phase = 0;
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        int mb, nb;
+        tile_coords(p, tile, mb, nb);
+        const int m0 = mb * BM;
+        int brow0, brow1;
+        if (p.paired) {
+          brow0 = nb * (BN / 2);
+          brow1 = p.pair_off + nb * (BN / 2);
+        } else {
+          brow0 = nb * BN;
+          brow1 = nb * BN + BN / 2;
+        }
+        for (int seg = 0; ok && seg < 2; ++seg) {
+          for (int kb = p.kb[2 * seg]; kb < p.kb[2 * seg + 1]; ++kb) {
+            if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
+              ok = false;
+              break;
+            }
+            mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+            armed |= 1u << stage;
+            armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
+            const int k0 = kb * BK;
+            uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
+            uint8_t* b_dst = sB + stage * B_STAGE_BYTES;
+            if (!A_MN) {
+              tma_load_2d(a_dst, &map_a, &full_bar[stage], k0, m0);
+            } else {
+              tma_load_2d(a_dst, &map_a, &full_bar[stage], m0, k0);
+              tma_load_2d(a_dst + 8192, &map_a, &full_bar[stage], m0 + 64, k0);
+            }
+            if (!B_MN) {
+              tma_load_2d(b_dst, &map_b, &full_bar[stage], k0, brow0);
+              tma_load_2d(b_dst + B_STAGE_BYTES / 2, &map_b, &full_bar[stage], k0, brow1);
+            } else {
+#pragma unroll
+              for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + j * 8192, &map_b, &full_bar[stage], brow0 + 64 * j, k0);
+            }
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+      }
+      if (!ok || *abort_flag) {
+        // Wait for the copies this thread started before the CTA may exit.
+        int no_abort = 0;
+        for (int s = 0; s < STAGES; ++s)
+          if (armed & (1u << s))
+            mbar_wait(&full_bar[s], (armed_par >> s) & 1u, &no_abort, p.status, STATUS_TIMEOUT, DRAIN_LIMIT_NS);
+      }
+    }
+  } else if (warp == 1) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ MMA issuer
+      uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+      bool ok = true;
+      if (p.force_timeout) ok = mbar_wait(&never_bar, 0, abort_flag, p.status, STATUS_TIMEOUT, FORCED_LIMIT_NS);
+      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t d_tmem = tmem_base + acc * BN;
+        uint32_t accumulate = 0;
+        for (int seg = 0; ok && seg < 2; ++seg) {
+          for (int kb = p.kb[2 * seg]; kb < p.kb[2 * seg + 1]; ++kb) {
+            if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+            const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
+            const uint32_t b_base = smem_u32(sB + stage * B_STAGE_BYTES);
+#pragma unroll
+            for (int k = 0; k < BK / UMMA_K; ++k) {
+              const uint64_t a_desc =
+                  A_MN ? sw128_desc(a_base + k * 2048, 8192, 1024) : sw128_desc(a_base + k * 32, 16, 1024);
+              const uint64_t b_desc =
+                  B_MN ? sw128_desc(b_base + k * 2048, 8192, 1024) : sw128_desc(b_base + k * 32, 16, 1024);
+              tc_mma_f16(d_tmem, a_desc, b_desc, IDESC, accumulate);
+              accumulate = 1;
+            }
+            tc_commit(&empty_bar[stage]);
+            if (++stage == STAGES) {
+              stage = 0;
+              phase ^= 1u;
+            }
+          }
+        }
+        if (!ok) break;
+        tc_commit(&tfull_bar[acc]);
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+      }
+      // No MMA may still be running when tensor memory is released.
+      tc_commit(&drain_bar);
+      int no_abort = 0;
+      mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, DRAIN_LIMIT_NS);
+    }
+  } else {
+    // -------------------------------------------------------------- epilogue
+    const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint32_t acc = 0, acc_phase = 0;
+    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+      int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+      ok = __all_sync(0xffffffffu, ok);
+      if (!ok) break;
+      tc_fence_after();
+      int mb, nb;
+      tile_coords(p, tile, mb, nb);
+      const int row = mb * BM + q * 32 + lane;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      uint32_t r0[32], r1[32];
+      if (EPI == EPI_GATEUP_SWIGLU) {
+#pragma unroll 1
+        for (int c = 0; c < BN / 2 / 32; ++c) {
+          tmem_ld_32x32b_x32(tbase + c * 32, r0);
+          tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, r1);
+          tmem_ld_wait();
+          epi_chunk<EPI>(p.ep, row, nb * (BN / 2) + c * 32, reinterpret_cast<const float*>(r0),
+                         reinterpret_cast<const float*>(r1));
+        }
+      } else {
+#pragma unroll 1
+        for (int c = 0; c < BN / 32; ++c) {
+          tmem_ld_32x32b_x32(tbase + c * 32, r0);
+          tmem_ld_wait();
+          epi_chunk<EPI>(p.ep, row, nb * BN + c * 32, reinterpret_cast<const float*>(r0), nullptr);
+        }
+      }
+      tc_fence_before();
+      mbar_arrive(&tempty_bar[acc]);
+      acc ^= 1u;
+      if (acc == 0) acc_phase ^= 1u;
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                                  const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                                  CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn get_encode_fn() {
+  static EncodeTiledFn fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<EncodeTiledFn>(ptr);
+  });
+  return fn;
+}
+
+// 2-D bf16 tensor [outer, inner] with row pitch `ld` elements; box of
+// box_inner (= 64, one 128-byte swizzle row) x box_outer.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc) return false;
+  cuuint64_t dims[2] = {inner, outer};
+  cuuint64_t strides[1] = {ld * 2};
+  cuuint32_t box[2] = {64, box_outer};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+template <bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_inst(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, int grid, cudaStream_t st) {
+  static std::once_flag once;
+  static cudaError_t attr_err = cudaSuccess;
+  std::call_once(once, [] {
+    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    SMEM_BYTES);
+  });
+  if (attr_err != cudaSuccess) return attr_err;
+  gemm_tc_kernel<A_MN, B_MN, EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  TcParams p{};
+  p.M = g.M;
+  p.N = g.N;
+  p.num_m_blk = (g.M + BM - 1) / BM;
+  p.num_n_blk = g.paired ? (g.N + BN / 2 - 1) / (BN / 2) : (g.N + BN - 1) / BN;
+  p.num_tiles = p.num_m_blk * p.num_n_blk;
+  p.group_m = p.num_m_blk < 16 ? p.num_m_blk : 16;
+  for (int s = 0; s < 2; ++s) {
+    const int64_t k0 = g.kseg[2 * s], k1 = g.kseg[2 * s + 1];
+    if (k1 < k0 || k0 % BK != 0 || (k1 % BK != 0 && k1 != g.k_extent) || k1 > g.k_extent)
+      return cudaErrorInvalidValue;
+    p.kb[2 * s] = (int)(k0 / BK);
+    p.kb[2 * s + 1] = (int)((k1 + BK - 1) / BK);
+  }
+  if (p.kb[1] - p.kb[0] + p.kb[3] - p.kb[2] <= 0) return cudaErrorInvalidValue;
+  p.paired = g.paired ? 1 : 0;
+  p.pair_off = (int)g.pair_off;
+  p.ep = g.ep;
+  p.ep.M = g.M;
+  p.ep.N = g.N;
+  p.status = status;
+  p.force_timeout = force_timeout;
+
+  CUtensorMap ma, mb;
+  bool ok;
+  if (!g.a_mn)
+    ok = make_map(&ma, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, 128);
+  else
+    ok = make_map(&ma, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  if (!g.b_mn)
+    ok = make_map(&mb, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, 128);
+  else
+    ok = make_map(&mb, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, 64);
+  if (!ok) return cudaErrorInvalidValue;
+
+  const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
+  const int key = (g.a_mn ? 100 : 0) + (g.b_mn ? 10 : 0) + g.epi;
+  switch (key) {
+    case 0 + EPI_GATEUP_SWIGLU:
+      if (!g.paired) return cudaErrorInvalidValue;
+      return launch_inst<false, false, EPI_GATEUP_SWIGLU>(ma, mb, p, grid, st);
+    case 0 + EPI_FC1_GELU:
+      return launch_inst<false, false, EPI_FC1_GELU>(ma, mb, p, grid, st);
+    case 0 + EPI_DOWN_RESID:
+      return launch_inst<false, false, EPI_DOWN_RESID>(ma, mb, p, grid, st);
+    case 10 + EPI_DGRAD_SWIGLU:
+      return launch_inst<false, true, EPI_DGRAD_SWIGLU>(ma, mb, p, grid, st);
+    case 10 + EPI_DGRAD_GELU:
+      return launch_inst<false, true, EPI_DGRAD_GELU>(ma, mb, p, grid, st);
+    case 110 + EPI_STORE_F32:
+      return launch_inst<true, true, EPI_STORE_F32>(ma, mb, p, grid, st);
+    case 10 + EPI_STORE_F32:
+      return launch_inst<false, true, EPI_STORE_F32>(ma, mb, p, grid, st);
+    default:
+      return cudaErrorNotSupported;
+  }
+}
+
+}  // namespace tpmlp

@@ -1,0 +1,430 @@
+// Memory-bound kernels of the sublayer step: RMSNorm forward and backward
+// (with the residual gradient and the token-axis sums of the replicated
+// parameters' gradients), the MSE loss and its gradient, column sums, and the
+// SGD update.  All use 16-byte vector accesses and fp32 arithmetic;
+// reductions over tokens go through per-block partials summed in a fixed
+// order, so results are deterministic.
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "epilogue.cuh"
+#include "tpmlp_internal.h"
+
+namespace tpmlp {
+namespace {
+
+// 16-byte vector of T as floats.
+template <typename T>
+struct Vec;
+template <>
+struct Vec<float> {
+  static constexpr int N = 4;
+  __device__ static void load(const float* p, float* f) {
+    const float4 v = *reinterpret_cast<const float4*>(p);
+    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
+  }
+  __device__ static void store(float* p, const float* f) {
+    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
+  }
+};
+template <>
+struct Vec<__nv_bfloat16> {
+  static constexpr int N = 8;
+  __device__ static void load(const __nv_bfloat16* p, float* f) {
+    const uint4 v = *reinterpret_cast<const uint4*>(p);
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
+      f[2 * i] = t.x;
+      f[2 * i + 1] = t.y;
+    }
+  }
+  __device__ static void store(__nv_bfloat16* p, const float* f) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
+      w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+};
+
+// 4 consecutive elements of T as floats (8 bytes for bf16, 16 for float).
+__device__ __forceinline__ void load4(const float* p, float* f) { Vec<float>::load(p, f); }
+__device__ __forceinline__ void store4(float* p, const float* f) { Vec<float>::store(p, f); }
+__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* f) {
+  const uint2 v = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+}
+__device__ __forceinline__ void store4(__nv_bfloat16* p, const float* f) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
+  __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
+  uint2 v;
+  v.x = *reinterpret_cast<uint32_t*>(&a);
+  v.y = *reinterpret_cast<uint32_t*>(&b);
+  *reinterpret_cast<uint2*>(p) = v;
+}
+
+// ------------------------------------------------------------- RMSNorm fwd
+// TPR threads per row, each holding up to MAXV 16-byte vectors of the row in
+// registers: one read of x, one write of the normed row, one float rstd.
+template <typename T, int TPR, int MAXV>
+__global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const T* __restrict__ x, const T* __restrict__ w, float eps,
+                                                          T* __restrict__ nrm, float* __restrict__ rstd, int64_t N,
+                                                          int H) {
+  constexpr int V = Vec<T>::N;
+  constexpr int RPB = 256 / TPR;
+  __shared__ float red[8];
+  const int rib = threadIdx.x / TPR;
+  const int t = threadIdx.x % TPR;
+  const int64_t row = (int64_t)blockIdx.x * RPB + rib;
+  const bool active = row < N;
+  const int nvec = H / V;
+  const T* xr = x + row * H;
+  float xs[MAXV][V];
+  float ss = 0.0f;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int v = t + i * TPR;
+    if (active && v < nvec) {
+      Vec<T>::load(xr + v * V, xs[i]);
+#pragma unroll
+      for (int j = 0; j < V; ++j) ss = fmaf(xs[i][j], xs[i][j], ss);
+    }
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+  if (TPR > 32) {
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    __syncthreads();
+    ss = 0.0f;
+    const int w0 = rib * (TPR / 32);
+#pragma unroll
+    for (int k = 0; k < TPR / 32; ++k) ss += red[w0 + k];
+  }
+  if (!active) return;
+  const float r = 1.0f / sqrtf(ss / (float)H + eps);
+  T* nr = nrm + row * H;
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int v = t + i * TPR;
+    if (v < nvec) {
+      float wv[V], o[V];
+      Vec<T>::load(w + v * V, wv);
+#pragma unroll
+      for (int j = 0; j < V; ++j) o[j] = xs[i][j] * r * wv[j];
+      Vec<T>::store(nr + v * V, o);
+    }
+  }
+  if (t == 0) rstd[row] = r;
+}
+
+template <typename T, int TPR>
+cudaError_t rmsnorm_fwd_tpr(const T* x, const T* w, float eps, T* nrm, float* rstd, int64_t N, int H,
+                            cudaStream_t st) {
+  const int64_t blocks = (N + (256 / TPR) - 1) / (256 / TPR);
+  rmsnorm_fwd_kernel<T, TPR, 8><<<(unsigned)blocks, 256, 0, st>>>(x, w, eps, nrm, rstd, N, H);
+  return cudaGetLastError();
+}
+
+template <typename T>
+cudaError_t rmsnorm_fwd_t(const T* x, const T* w, float eps, T* nrm, float* rstd, int64_t N, int64_t H,
+                          cudaStream_t st) {
+  const int64_t nvec = H / Vec<T>::N;
+  if (nvec <= 32 * 8) return rmsnorm_fwd_tpr<T, 32>(x, w, eps, nrm, rstd, N, (int)H, st);
+  if (nvec <= 64 * 8) return rmsnorm_fwd_tpr<T, 64>(x, w, eps, nrm, rstd, N, (int)H, st);
+  if (nvec <= 128 * 8) return rmsnorm_fwd_tpr<T, 128>(x, w, eps, nrm, rstd, N, (int)H, st);
+  if (nvec <= 256 * 8) return rmsnorm_fwd_tpr<T, 256>(x, w, eps, nrm, rstd, N, (int)H, st);
+  return cudaErrorInvalidValue;
+}
+
+// ------------------------------------------------------------- RMSNorm bwd
+// Block b owns rows [b*R, (b+1)*R).  Per row: g = dN * w, xhat = x * rstd,
+// c = mean_h(g * xhat), dx = dy + rstd * (g - xhat * c).  Each thread also
+// keeps running column sums of dN * xhat (norm weight gradient) and dy (down
+// bias gradient) for its columns; they are written as the block's partials.
+template <typename T, int MAXV>
+__global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restrict__ dnrm, const T* __restrict__ x,
+                                                          const float* __restrict__ rstd, const T* __restrict__ w,
+                                                          const T* __restrict__ dy, T* __restrict__ dx,
+                                                          float* __restrict__ part_dw, float* __restrict__ part_db,
+                                                          int64_t N, int H, int rows_per_block) {
+  __shared__ float red[2][8];
+  const int nv = H / 4;
+  float wv[MAXV][4], adw[MAXV][4], adb[MAXV][4];
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int v = threadIdx.x + 256 * i;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) adw[i][j] = adb[i][j] = wv[i][j] = 0.0f;
+    if (v < nv) load4(w + 4 * v, wv[i]);
+  }
+  const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
+  const int64_t r1 = min(N, r0 + rows_per_block);
+  int par = 0;
+  for (int64_t row = r0; row < r1; ++row, par ^= 1) {
+    const float rs = rstd[row];
+    float g[MAXV][4], xh[MAXV][4], d[MAXV][4];
+    float dot = 0.0f;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      if (v < nv) {
+        float dn[4], xv[4];
+        load4(dnrm + row * H + 4 * v, dn);
+        load4(x + row * H + 4 * v, xv);
+        load4(dy + row * H + 4 * v, d[i]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          xh[i][j] = xv[j] * rs;
+          g[i][j] = dn[j] * wv[i][j];
+          dot = fmaf(g[i][j], xh[i][j], dot);
+          adw[i][j] = fmaf(dn[j], xh[i][j], adw[i][j]);
+          adb[i][j] += d[i][j];
+        }
+      }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) dot += __shfl_xor_sync(0xffffffffu, dot, o);
+    if ((threadIdx.x & 31) == 0) red[par][threadIdx.x >> 5] = dot;
+    __syncthreads();
+    dot = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) dot += red[par][k];
+    const float c = dot / (float)H;
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      if (v < nv) {
+        float o[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) o[j] = d[i][j] + rs * (g[i][j] - xh[i][j] * c);
+        store4(dx + row * H + 4 * v, o);
+      }
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < MAXV; ++i) {
+    const int v = threadIdx.x + 256 * i;
+    if (v < nv) {
+      store4(part_dw + (int64_t)blockIdx.x * H + 4 * v, adw[i]);
+      store4(part_db + (int64_t)blockIdx.x * H + 4 * v, adb[i]);
+    }
+  }
+}
+
+template <typename T>
+cudaError_t rmsnorm_bwd_t(const float* dnrm, const T* x, const float* rstd, const T* w, const T* dy, T* dx,
+                          float* part_dw, float* part_db, int64_t N, int64_t H, int nblocks, cudaStream_t st) {
+  const int rpb = (int)((N + nblocks - 1) / nblocks);
+  const int nv = (int)(H / 4);
+#define TPMLP_BWD(MV) \
+  rmsnorm_bwd_kernel<T, MV><<<nblocks, 256, 0, st>>>(dnrm, x, rstd, w, dy, dx, part_dw, part_db, N, (int)H, rpb)
+  if (nv <= 256) TPMLP_BWD(1);
+  else if (nv <= 512) TPMLP_BWD(2);
+  else if (nv <= 1024) TPMLP_BWD(4);
+  else if (nv <= 2048) TPMLP_BWD(8);
+  else return cudaErrorInvalidValue;
+#undef TPMLP_BWD
+  return cudaGetLastError();
+}
+
+// ------------------------------------------------------------- column sums
+__global__ void colsum_finalize_kernel(const float* __restrict__ part, int nparts, float* __restrict__ out,
+                                       int64_t C) {
+  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  if (c >= C) return;
+  float s = 0.0f;
+  for (int p = 0; p < nparts; ++p) s += part[(int64_t)p * C + c];
+  out[c] = s;
+}
+
+// Block (x, y): columns [1024 x, 1024 x + 1024) (4 per thread), rows of chunk y.
+template <typename T>
+__global__ void colsum_partials_kernel(const T* __restrict__ in, int64_t ld, float* __restrict__ part, int64_t N,
+                                       int64_t C, int rows_per_block) {
+  const int64_t c = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) * 4;
+  if (c >= C) return;
+  const int64_t r0 = (int64_t)blockIdx.y * rows_per_block;
+  const int64_t r1 = min(N, r0 + rows_per_block);
+  float s[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+  for (int64_t r = r0; r < r1; ++r) {
+    float v[4];
+    load4(in + r * ld + c, v);
+#pragma unroll
+    for (int j = 0; j < 4; ++j) s[j] += v[j];
+  }
+  store4(part + (int64_t)blockIdx.y * C + c, s);
+}
+
+// ------------------------------------------------------------- loss
+template <typename T>
+__global__ void __launch_bounds__(256) mse_loss_grad_kernel(const T* __restrict__ y, const T* __restrict__ tg,
+                                                            T* __restrict__ dy, double* __restrict__ part, int64_t n,
+                                                            float inv_count) {
+  constexpr int V = Vec<T>::N;
+  __shared__ double red[8];
+  const int64_t nv = n / V;
+  double acc = 0.0;
+  for (int64_t v = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; v < nv; v += (int64_t)gridDim.x * blockDim.x) {
+    float a[V], b[V], o[V];
+    Vec<T>::load(y + v * V, a);
+    Vec<T>::load(tg + v * V, b);
+    float s = 0.0f;
+#pragma unroll
+    for (int j = 0; j < V; ++j) {
+      const float d = a[j] - b[j];
+      s = fmaf(d, d, s);
+      o[j] = d * inv_count;
+    }
+    Vec<T>::store(dy + v * V, o);
+    acc += (double)s;
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+  if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = acc;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    double s = 0.0;
+    for (int k = 0; k < 8; ++k) s += red[k];
+    part[blockIdx.x] = s;
+  }
+}
+
+__global__ void loss_finalize_kernel(const double* __restrict__ part, int nblocks, double scale,
+                                     float* __restrict__ loss) {
+  __shared__ double red[256];
+  double s = 0.0;
+  for (int i = threadIdx.x; i < nblocks; i += 256) s += part[i];
+  red[threadIdx.x] = s;
+  __syncthreads();
+  for (int w = 128; w > 0; w >>= 1) {
+    if (threadIdx.x < w) red[threadIdx.x] += red[threadIdx.x + w];
+    __syncthreads();
+  }
+  if (threadIdx.x == 0) *loss = (float)(red[0] * scale);
+}
+
+// ------------------------------------------------------------- SGD
+template <typename T>
+__global__ void __launch_bounds__(256) sgd_kernel(const SgdArgs a) {
+  const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+  const int64_t tid = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+  for (int s = 0; s < a.nseg; ++s) {
+    const SgdSeg sg = a.seg[s];
+    const int64_t n4 = sg.n / 4;
+    T* w = static_cast<T*>(sg.w);
+    for (int64_t i = tid; i < n4; i += stride) {
+      float g[4], v[4];
+      load4(sg.grad + 4 * i, g);
+      if (sg.master) {
+        load4(sg.master + 4 * i, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = fmaf(-a.lr, g[j], v[j]);
+        store4(sg.master + 4 * i, v);
+      } else {
+        load4(w + 4 * i, v);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) v[j] = fmaf(-a.lr, g[j], v[j]);
+      }
+      store4(w + 4 * i, v);
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_rmsnorm_fwd(int dtype, const void* x, const void* w, float eps, void* nrm, float* rstd, int64_t N,
+                               int64_t H, cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  if (dtype == 0)
+    return rmsnorm_fwd_t<float>((const float*)x, (const float*)w, eps, (float*)nrm, rstd, N, H, st);
+  return rmsnorm_fwd_t<__nv_bfloat16>((const __nv_bfloat16*)x, (const __nv_bfloat16*)w, eps, (__nv_bfloat16*)nrm,
+                                      rstd, N, H, st);
+}
+
+int rmsnorm_bwd_blocks(int64_t N, int num_sms) {
+  int64_t b = 4LL * num_sms;
+  if (b > 1024) b = 1024;
+  if (b > N) b = N;
+  return (int)(b < 1 ? 1 : b);
+}
+
+cudaError_t launch_rmsnorm_bwd(int dtype, const float* dnrm, const void* x, const float* rstd, const void* w,
+                               const void* dy, void* dx, float* part_dw, float* part_db, int64_t N, int64_t H,
+                               int nblocks, cudaStream_t st) {
+  if (N <= 0) return cudaSuccess;
+  if (dtype == 0)
+    return rmsnorm_bwd_t<float>(dnrm, (const float*)x, rstd, (const float*)w, (const float*)dy, (float*)dx, part_dw,
+                                part_db, N, H, nblocks, st);
+  return rmsnorm_bwd_t<__nv_bfloat16>(dnrm, (const __nv_bfloat16*)x, rstd, (const __nv_bfloat16*)w,
+                                      (const __nv_bfloat16*)dy, (__nv_bfloat16*)dx, part_dw, part_db, N, H, nblocks,
+                                      st);
+}
+
+cudaError_t launch_colsum_finalize(const float* part, int nparts, float* out, int64_t C, cudaStream_t st) {
+  if (C <= 0) return cudaSuccess;
+  colsum_finalize_kernel<<<(unsigned)((C + 255) / 256), 256, 0, st>>>(part, nparts, out, C);
+  return cudaGetLastError();
+}
+
+int colsum_blocks(int64_t N, int num_sms) {
+  int64_t b = num_sms;
+  if (b > 256) b = 256;
+  if (b > N) b = N;
+  return (int)(b < 1 ? 1 : b);
+}
+
+cudaError_t launch_colsum_partials(int dtype, const void* in, int64_t ld, float* part, int64_t N, int64_t C,
+                                   int nblocks, cudaStream_t st) {
+  if (N <= 0 || C <= 0) return cudaSuccess;
+  const int rpb = (int)((N + nblocks - 1) / nblocks);
+  dim3 grid((unsigned)((C / 4 + 255) / 256), (unsigned)nblocks);
+  if (dtype == 0)
+    colsum_partials_kernel<float><<<grid, 256, 0, st>>>((const float*)in, ld, part, N, C, rpb);
+  else
+    colsum_partials_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>((const __nv_bfloat16*)in, ld, part, N, C, rpb);
+  return cudaGetLastError();
+}
+
+int loss_blocks(int64_t n, int num_sms) {
+  int64_t b = (n / 8 + 255) / 256;
+  if (b > 2LL * num_sms) b = 2LL * num_sms;
+  if (b > 1024) b = 1024;
+  return (int)(b < 1 ? 1 : b);
+}
+
+cudaError_t launch_mse_loss_grad(int dtype, const void* y, const void* target, void* dy, double* part, int nblocks,
+                                 int64_t n, float inv_count, cudaStream_t st) {
+  if (dtype == 0)
+    mse_loss_grad_kernel<float><<<nblocks, 256, 0, st>>>((const float*)y, (const float*)target, (float*)dy, part, n,
+                                                        inv_count);
+  else
+    mse_loss_grad_kernel<__nv_bfloat16><<<nblocks, 256, 0, st>>>(
+        (const __nv_bfloat16*)y, (const __nv_bfloat16*)target, (__nv_bfloat16*)dy, part, n, inv_count);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_loss_finalize(const double* part, int nblocks, double scale, float* loss, cudaStream_t st) {
+  loss_finalize_kernel<<<1, 256, 0, st>>>(part, nblocks, scale, loss);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_sgd(int dtype, const SgdArgs& a, int num_sms, cudaStream_t st) {
+  int64_t tot = 0;
+  for (int s = 0; s < a.nseg; ++s) tot += a.seg[s].n / 4;
+  int64_t blocks = (tot + 255) / 256;
+  if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+  if (blocks < 1) blocks = 1;
+  if (dtype == 0)
+    sgd_kernel<float><<<(unsigned)blocks, 256, 0, st>>>(a);
+  else
+    sgd_kernel<__nv_bfloat16><<<(unsigned)blocks, 256, 0, st>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace tpmlp

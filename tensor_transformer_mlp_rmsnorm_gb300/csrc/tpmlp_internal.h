@@ -1,0 +1,79 @@
+// Host-side declarations shared by the library's translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "epilogue.cuh"
+
+namespace tpmlp {
+
+// Device status word bits (written by kernels, read by tpmlp_sync).
+constexpr uint32_t STATUS_TIMEOUT = 1u;
+
+// C[M, N] = sum over the contraction segments of A(m, k) B(k, n).
+//  A K-major : A(m,k) = a[m * lda + k]  (tensor [M, K_extent])
+//  A MN-major: A(m,k) = a[k * lda + m]  (tensor [K_extent, M])
+//  B K-major : B(k,n) = b[n * ldb + k]  (tensor [b_rows, K_extent])
+//  B MN-major: B(k,n) = b[k * ldb + n]  (tensor [K_extent, N])
+// paired (K-major B only): output channel n takes B rows n (gate) and
+// pair_off + n (up); the epilogue receives both sums.
+// Contraction segments [k0, k1) and [k2, k3) (k2 == k3 for one segment).
+struct GemmDesc {
+  int M = 0, N = 0;
+  int64_t k_extent = 0;  // K extent of the A/B tensors
+  const void* a = nullptr;
+  int64_t lda = 0;
+  bool a_mn = false;
+  const void* b = nullptr;
+  int64_t ldb = 0;
+  bool b_mn = false;
+  int64_t b_rows = 0;  // rows of a K-major B tensor
+  bool paired = false;
+  int64_t pair_off = 0;
+  int64_t kseg[4] = {0, 0, 0, 0};
+  int epi = EPI_STORE_F32;
+  EpiParams ep{};
+};
+
+// tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory).
+// Segment boundaries must be multiples of 64, except an end equal to k_extent.
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout);
+
+// fp32 SIMT GEMM (exact fp32 path), any segments.
+cudaError_t launch_gemm_simt_f32(const GemmDesc& g, cudaStream_t st);
+
+// Bounded wait on a flag nothing sets; records STATUS_TIMEOUT (debug aid).
+cudaError_t launch_timeout_probe(uint32_t* status, cudaStream_t st);
+
+// Row-wise and reduction kernels (dtype: 0 = f32, 1 = bf16).
+cudaError_t launch_rmsnorm_fwd(int dtype, const void* x, const void* w, float eps, void* nrm, float* rstd,
+                               int64_t N, int64_t H, cudaStream_t st);
+int rmsnorm_bwd_blocks(int64_t N, int num_sms);
+cudaError_t launch_rmsnorm_bwd(int dtype, const float* dnrm, const void* x, const float* rstd, const void* w,
+                               const void* dy, void* dx, float* part_dw, float* part_db, int64_t N, int64_t H,
+                               int nblocks, cudaStream_t st);
+cudaError_t launch_colsum_finalize(const float* part, int nparts, float* out, int64_t C, cudaStream_t st);
+int colsum_blocks(int64_t N, int num_sms);
+cudaError_t launch_colsum_partials(int dtype, const void* in, int64_t ld, float* part, int64_t N, int64_t C,
+                                   int nblocks, cudaStream_t st);
+int loss_blocks(int64_t n, int num_sms);
+cudaError_t launch_mse_loss_grad(int dtype, const void* y, const void* target, void* dy, double* part,
+                                 int nblocks, int64_t n, float inv_count, cudaStream_t st);
+cudaError_t launch_loss_finalize(const double* part, int nblocks, double scale, float* loss, cudaStream_t st);
+
+struct SgdSeg {
+  float* master;      // float master copy (or nullptr)
+  const float* grad;  // float gradient
+  void* w;            // parameter in the activation dtype
+  int64_t n;          // elements (multiple of 4)
+};
+constexpr int SGD_MAX_SEGS = 6;
+struct SgdArgs {
+  SgdSeg seg[SGD_MAX_SEGS];
+  int nseg;
+  float lr;
+};
+cudaError_t launch_sgd(int dtype, const SgdArgs& a, int num_sms, cudaStream_t st);
+
+}  // namespace tpmlp

@@ -1,0 +1,246 @@
+"""ctypes binding of the tpmlp C ABI (``include/tpmlp.h``).
+
+Argument marshalling only: every step of the sublayer runs in the CUDA
+library.  torch supplies device memory and the stream; nothing here computes.
+The module raises ``TPMLPError`` if the shared library has not been built --
+there is no fallback.
+
+Functions named like the C entry points take torch tensors; ``TPMLP`` wraps a
+context together with its workspace.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libtpmlp.so")
+
+OK, ERR_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ORDER, ERR_CUDA, ERR_TIMEOUT = range(7)
+F32, BF16 = 0, 1
+SWIGLU, GELU = 0, 1
+DBG_SKIP_FWD_REDUCE, DBG_SKIP_BWD_REDUCE, DBG_FORCE_TIMEOUT = 1, 2, 4
+
+_DTYPES = {"f32": F32, "bf16": BF16}
+_ACTS = {"swiglu": SWIGLU, "gelu": GELU}
+_TORCH_DTYPE = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+class TPMLPError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"tpmlp status {status}: {msg}")
+        self.status = status
+
+
+class Config(ctypes.Structure):
+    _fields_ = [("max_tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64),
+                ("max_t", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
+                ("reserved", ctypes.c_int32)]
+
+
+_vp, _i32, _i64, _u32, _f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_uint32, ctypes.c_float
+_fp = ctypes.c_void_p  # float* (device)
+_SIGNATURES = {
+    "tpmlp_create": (_i32, [ctypes.POINTER(Config), _vp, ctypes.POINTER(_vp)]),
+    "tpmlp_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Config)]),
+    "tpmlp_bind_workspace": (_i32, [_vp, _vp, ctypes.c_size_t]),
+    "tpmlp_set_stream": (_i32, [_vp, _vp]),
+    "tpmlp_forward": (_i32, [_vp, _i64, _vp, _vp, _vp, _vp, _vp, _vp, _f32, _i32, _vp]),
+    "tpmlp_mse_loss_grad": (_i32, [_vp, _vp, _vp, _vp, _fp]),
+    "tpmlp_backward": (_i32, [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp]),
+    "tpmlp_bind_master": (_i32, [_vp, _fp, _fp, _fp, _fp, _fp]),
+    "tpmlp_sgd_step": (_i32, [_vp, _f32]),
+    "tpmlp_set_debug": (_i32, [_vp, _u32, _i32]),
+    "tpmlp_sync": (_i32, [_vp]),
+    "tpmlp_set_timing": (_i32, [_vp, _i32]),
+    "tpmlp_read_kernel_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int64), _i32]),
+    "tpmlp_kernel_name": (ctypes.c_char_p, [_i32]),
+    "tpmlp_num_kernel_ids": (_i32, []),
+    "tpmlp_launch_count": (ctypes.c_uint64, [_vp]),
+    "tpmlp_status_string": (ctypes.c_char_p, [_i32]),
+    "tpmlp_last_error": (ctypes.c_char_p, [_vp]),
+    "tpmlp_destroy": (None, [_vp]),
+}
+
+_LIB = None
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library; raises if it has not been built."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise TPMLPError(ERR_UNSUPPORTED, f"{LIB_PATH} is missing: build it with "
+                             "tensor_transformer_mlp_rmsnorm_gb300.build.build()")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int, ctx=None):
+    if status != OK:
+        msg = lib().tpmlp_last_error(ctx).decode(errors="replace")
+        raise TPMLPError(status, msg or lib().tpmlp_status_string(status).decode())
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def kernel_names() -> list:
+    L = lib()
+    return [L.tpmlp_kernel_name(i).decode() for i in range(L.tpmlp_num_kernel_ids())]
+
+
+def make_config(max_tokens: int, hidden: int, ffn: int, max_t: int = 8, dtype: str = "bf16",
+                act: str = "swiglu") -> Config:
+    return Config(max_tokens, hidden, ffn, max_t, _DTYPES[dtype], _ACTS[act], 0)
+
+
+def tpmlp_workspace_bytes(cfg: Config) -> int:
+    return int(lib().tpmlp_workspace_bytes(ctypes.byref(cfg)))
+
+
+def tpmlp_create(cfg: Config, stream=None):
+    out = ctypes.c_void_p()
+    s = None if stream is None else ctypes.c_void_p(stream)
+    _check(lib().tpmlp_create(ctypes.byref(cfg), s, ctypes.byref(out)))
+    return out
+
+
+class TPMLP:
+    """One context of the sublayer with its caller-owned workspace.
+
+    Methods mirror the C entry points: ``forward``, ``mse_loss_grad``,
+    ``backward``, ``bind_master``, ``sgd_step``, ``set_debug``, ``sync``."""
+
+    def __init__(self, max_tokens: int, hidden: int, ffn: int, max_t: int = 8, dtype: str = "bf16",
+                 act: str = "swiglu", device=None, stream: torch.cuda.Stream | None = None):
+        dev = torch.device(device) if device is not None else torch.device("cuda")
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
+        self.cfg = make_config(max_tokens, hidden, ffn, max_t, dtype, act)
+        self.dtype = _TORCH_DTYPE[_DTYPES[dtype]]
+        self.act = act
+        self.H, self.F = hidden, ffn
+        self.stream = stream if stream is not None else torch.cuda.current_stream(self.device)
+        with torch.cuda.device(self.device):
+            self.ctx = tpmlp_create(self.cfg, self.stream.cuda_stream)
+            nbytes = tpmlp_workspace_bytes(self.cfg)
+            self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
+        _check(lib().tpmlp_bind_workspace(self.ctx, _ptr(self.workspace), nbytes), self.ctx)
+        self.tokens = 0
+        self._loss = torch.zeros(1, dtype=torch.float32, device=self.device)
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            lib().tpmlp_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    # -- checks ------------------------------------------------------------
+    def _t(self, t, shape, dtype=None, name="tensor"):
+        if t is None:
+            raise TPMLPError(ERR_ARG, f"{name} is None")
+        want = dtype if dtype is not None else self.dtype
+        if t.device != self.device or t.dtype != want or not t.is_contiguous() or tuple(t.shape) != tuple(shape):
+            raise TPMLPError(ERR_ARG, f"{name}: need contiguous {want} {tuple(shape)} on {self.device}, "
+                                      f"got {t.dtype} {tuple(t.shape)} on {t.device}")
+        return _ptr(t)
+
+    def _gu_shape(self):
+        return (2, self.F, self.H) if self.act == "swiglu" else (self.F, self.H)
+
+    # -- entry points --------------------------------------------------------
+    def forward(self, x, norm_w, w_gate_up, w_down, b_down, eps: float, t: int, y=None, b_1=None):
+        n = x.shape[0]
+        if y is None:
+            y = torch.empty_like(x)
+        args = (self._t(x, (n, self.H), name="x"), self._t(norm_w, (self.H,), name="norm_w"),
+                self._t(w_gate_up, self._gu_shape(), name="w_gate_up"),
+                self._t(b_1, (self.F,), name="b_1") if self.act == "gelu" else None,
+                self._t(w_down, (self.H, self.F), name="w_down"), self._t(b_down, (self.H,), name="b_down"))
+        yp = self._t(y, (n, self.H), name="y")
+        _check(lib().tpmlp_forward(self.ctx, n, *args, float(eps), int(t), yp), self.ctx)
+        self.tokens = n
+        return y
+
+    def mse_loss_grad(self, y, target, dy=None, loss=None):
+        n = self.tokens
+        dy = torch.empty_like(y) if dy is None else dy
+        loss = self._loss if loss is None else loss
+        _check(lib().tpmlp_mse_loss_grad(self.ctx, self._t(y, (n, self.H), name="y"),
+                                         self._t(target, (n, self.H), name="target"),
+                                         self._t(dy, (n, self.H), name="dy"),
+                                         self._t(loss, (1,), torch.float32, "loss")), self.ctx)
+        return loss, dy
+
+    def new_grads(self):
+        f32 = dict(dtype=torch.float32, device=self.device)
+        g = {"norm_w": torch.empty(self.H, **f32), "w_gate_up": torch.empty(self._gu_shape(), **f32),
+             "w_down": torch.empty(self.H, self.F, **f32), "b_down": torch.empty(self.H, **f32)}
+        if self.act == "gelu":
+            g["b_1"] = torch.empty(self.F, **f32)
+        return g
+
+    def backward(self, dy, dx=None, grads=None):
+        n = self.tokens
+        dx = torch.empty_like(dy) if dx is None else dx
+        g = self.new_grads() if grads is None else grads
+        f32 = torch.float32
+        _check(lib().tpmlp_backward(
+            self.ctx, self._t(dy, (n, self.H), name="dy"), self._t(dx, (n, self.H), name="dx"),
+            self._t(g["norm_w"], (self.H,), f32, "dnorm_w"), self._t(g["w_gate_up"], self._gu_shape(), f32, "dw_gate_up"),
+            self._t(g["b_1"], (self.F,), f32, "db_1") if self.act == "gelu" else None,
+            self._t(g["w_down"], (self.H, self.F), f32, "dw_down"), self._t(g["b_down"], (self.H,), f32, "db_down")),
+            self.ctx)
+        return dx, g
+
+    def bind_master(self, masters: dict | None):
+        f32 = torch.float32
+        if masters is None:
+            _check(lib().tpmlp_bind_master(self.ctx, None, None, None, None, None), self.ctx)
+            return
+        _check(lib().tpmlp_bind_master(
+            self.ctx, self._t(masters["norm_w"], (self.H,), f32, "norm_w"),
+            self._t(masters["w_gate_up"], self._gu_shape(), f32, "w_gate_up"),
+            self._t(masters["b_1"], (self.F,), f32, "b_1") if self.act == "gelu" else None,
+            self._t(masters["w_down"], (self.H, self.F), f32, "w_down"),
+            self._t(masters["b_down"], (self.H,), f32, "b_down")), self.ctx)
+
+    def sgd_step(self, lr: float):
+        _check(lib().tpmlp_sgd_step(self.ctx, float(lr)), self.ctx)
+
+    def set_debug(self, flags: int, shard: int = 0):
+        _check(lib().tpmlp_set_debug(self.ctx, int(flags), int(shard)), self.ctx)
+
+    def sync(self):
+        _check(lib().tpmlp_sync(self.ctx), self.ctx)
+
+    def set_timing(self, enable: bool):
+        _check(lib().tpmlp_set_timing(self.ctx, 1 if enable else 0), self.ctx)
+
+    def read_kernel_times(self) -> dict:
+        n = lib().tpmlp_num_kernel_ids()
+        ms = (ctypes.c_float * n)()
+        cnt = (ctypes.c_int64 * n)()
+        m = lib().tpmlp_read_kernel_times(self.ctx, ms, cnt, n)
+        if m < 0:
+            raise TPMLPError(ERR_CUDA, "reading kernel times failed")
+        names = kernel_names()
+        return {names[i]: (float(ms[i]), int(cnt[i])) for i in range(m) if cnt[i] > 0}
+
+    def launch_count(self) -> int:
+        return int(lib().tpmlp_launch_count(self.ctx))

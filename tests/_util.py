@@ -1,0 +1,110 @@
+"""Shared helpers for the GPU tests: move seeded inputs to the device, run one
+step through the C ABI, and compare with the oracle under the stated
+tolerances.
+
+Tolerances (written here, used by every parity test):
+
+* fp32 configuration: |gpu - oracle| <= 1e-5 * |oracle| + 1e-5 * rms(oracle)
+  per element (1e-5 relative, with an absolute floor scaled to the tensor so
+  that elements near zero are judged against the tensor's size).
+* bf16 configuration (fp32 accumulation): |gpu - oracle| <= 2e-2 * |oracle| +
+  1e-2 * max(rms(oracle), tiny) per element, and ||gpu - oracle||_2 <= 2e-2 *
+  ||oracle||_2 per tensor.  The absolute part is scaled by the tensor's rms
+  because gradients of a mean loss are ~1e-8..1e-4, where a fixed 1e-2 would
+  accept anything.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import synth
+
+TOL = {
+    "f32": dict(rtol=1e-5, atol_rms=1e-5, norm=1e-5),
+    "bf16": dict(rtol=2e-2, atol_rms=1e-2, norm=2e-2),
+}
+
+
+def to_dev(a, dtype: str, device="cuda"):
+    t = torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32))
+    t = t.to(torch.bfloat16) if dtype == "bf16" else t
+    return t.to(device)
+
+
+def to_np(t):
+    return t.detach().float().cpu().numpy().astype(np.float64)
+
+
+def compare(name: str, gpu, ora, dtype: str, report: dict | None = None):
+    g = np.asarray(gpu, dtype=np.float64)
+    o = np.asarray(ora, dtype=np.float64)
+    assert g.shape == o.shape, (name, g.shape, o.shape)
+    tol = TOL[dtype]
+    rms = float(np.sqrt(np.mean(o * o))) if o.size else 0.0
+    atol = tol["atol_rms"] * max(rms, 1e-30)
+    err = np.abs(g - o)
+    bound = tol["rtol"] * np.abs(o) + atol
+    bad = err > bound
+    nrm = float(np.linalg.norm(g - o) / max(np.linalg.norm(o), 1e-300)) if o.size else 0.0
+    if report is not None:
+        report[name] = {"max_abs": float(err.max()) if err.size else 0.0, "rel_norm": nrm, "n_bad": int(bad.sum())}
+    assert np.all(np.isfinite(g)), f"{name}: non-finite values"
+    if bad.any():
+        i = np.unravel_index(np.argmax(err - bound), err.shape)
+        raise AssertionError(f"{name}: {int(bad.sum())}/{bad.size} elements out of tolerance; worst at {i}: "
+                             f"gpu={g[i]!r} oracle={o[i]!r} bound={bound[i]!r}; rel_norm={nrm:.3e}")
+    assert nrm <= tol["norm"], f"{name}: normwise relative error {nrm:.3e} > {tol['norm']}"
+
+
+def device_inputs(cfg: synth.Config, inp: dict):
+    d = {k: to_dev(v, cfg.dtype) for k, v in inp.items()}
+    return d
+
+
+def gpu_step(cfg: synth.Config, inp: dict, t: int, lr: float, flags: int = 0, shard: int = 0,
+             masters: bool = True, mod=None):
+    """Forward, loss, backward and SGD through the binding; numpy results."""
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP
+    m = mod or TPMLP(max(cfg.tokens, 1), cfg.hidden, cfg.ffn, max_t=max(8, t), dtype=cfg.dtype, act=cfg.act)
+    d = device_inputs(cfg, inp)
+    gu_key = "w_gate_up" if cfg.act == "swiglu" else "w_1"
+    params = {k: d[k] for k in synth.param_names(cfg.act)}
+    ms = None
+    if cfg.dtype == "bf16" and masters:
+        ms = {("w_gate_up" if k == "w_1" else k): torch.from_numpy(np.asarray(inp[k], dtype=np.float32)).cuda()
+              for k in synth.param_names(cfg.act)}
+        m.bind_master(ms)
+    m.set_debug(flags, shard)
+    y = m.forward(d["x"], d["norm_w"], d[gu_key], d["w_down"], d["b_down"], cfg.eps, t,
+                  b_1=d.get("b_1"))
+    loss, dy = m.mse_loss_grad(y, d["target"])
+    dx, g = m.backward(dy)
+    grads = {k: to_np(v) for k, v in g.items()}
+    out = {"y": to_np(y), "loss": float(loss.item()), "dy": to_np(dy), "dx": to_np(dx), "grads": grads}
+    m.sgd_step(lr)
+    m.sync()
+    if ms is not None:
+        out["new_master"] = {k: to_np(v) for k, v in ms.items()}
+    out["new_params"] = {k: to_np(params[k]) for k in params}
+    if cfg.act == "gelu":
+        out["grads"]["w_1"] = out["grads"].pop("w_gate_up")
+        if ms is not None:
+            out["new_master"]["w_1"] = out["new_master"].pop("w_gate_up")
+    m.set_debug(0, 0)
+    return out
+
+
+def compare_step(cfg: synth.Config, gpu: dict, ora: dict, inp: dict, lr: float, report: dict | None = None,
+                 grad_keys=None):
+    dt = cfg.dtype
+    compare("y", gpu["y"], ora["y"], dt, report)
+    assert abs(gpu["loss"] - ora["loss"]) <= TOL[dt]["rtol"] * abs(ora["loss"]) + 1e-12, (gpu["loss"], ora["loss"])
+    compare("dx", gpu["dx"], ora["grads"]["x"], dt, report)
+    for k in grad_keys or synth.param_names(cfg.act):
+        compare("d" + k, gpu["grads"][k], ora["grads"][k], dt, report)
+    # SGD: the applied update equals -lr * oracle gradient.
+    for k in synth.param_names(cfg.act):
+        new = gpu["new_master"][k] if "new_master" in gpu else gpu["new_params"][k]
+        upd = new - np.asarray(inp[k], dtype=np.float32).astype(np.float64)
+        compare("update_" + k, upd, -lr * ora["grads"][k], dt, report)

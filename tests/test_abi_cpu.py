@@ -1,0 +1,97 @@
+"""The C-ABI library builds, loads and exports every entry point its header
+declares; host-side validation rejects bad configurations without a GPU."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "tpmlp.h")
+
+
+@pytest.fixture(scope="module")
+def T():
+    from tensor_transformer_mlp_rmsnorm_gb300 import build
+    build.build()
+    import tensor_transformer_mlp_rmsnorm_gb300 as T
+    return T
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    return sorted(set(re.findall(r"^TPMLP_API\s+[\w\s\*]+?\b(tpmlp_\w+)\(", text, flags=re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for must in ("tpmlp_forward", "tpmlp_backward", "tpmlp_sgd_step", "tpmlp_mse_loss_grad", "tpmlp_create",
+                 "tpmlp_workspace_bytes", "tpmlp_bind_workspace", "tpmlp_sync", "tpmlp_destroy"):
+        assert must in names
+
+
+def test_library_exports_every_declared_symbol(T):
+    L = ctypes.CDLL(T.LIB_PATH)
+    missing = [n for n in declared_functions() if not hasattr(L, n)]
+    assert not missing, missing
+
+
+def test_binding_covers_every_symbol(T):
+    from tensor_transformer_mlp_rmsnorm_gb300 import tpmlp
+    assert set(declared_functions()) <= set(tpmlp._SIGNATURES)
+
+
+def test_config_validation_without_gpu(T):
+    good = T.make_config(16, 64, 256, 2, "f32", "swiglu")
+    assert T.tpmlp_workspace_bytes(good) > 0
+    cases = [
+        (dict(ffn=12), T.ERR_SHAPE),          # not a multiple of 8
+        (dict(hidden=0), T.ERR_SHAPE),
+        (dict(hidden=16384), T.ERR_SHAPE),    # above the supported hidden size
+        (dict(max_t=0), T.ERR_SHAPE),
+        (dict(max_tokens=-1), T.ERR_SHAPE),
+        (dict(dtype=7), T.ERR_UNSUPPORTED),
+        (dict(act=3), T.ERR_UNSUPPORTED),
+        (dict(reserved=1), T.ERR_ARG),
+    ]
+    for kw, status in cases:
+        c = T.make_config(16, 64, 256, 2, "f32", "swiglu")
+        for k, v in kw.items():
+            setattr(c, k, v)
+        assert T.tpmlp_workspace_bytes(c) == 0, kw
+        with pytest.raises(T.TPMLPError) as e:
+            T.tpmlp_create(c)
+        assert e.value.status == status, (kw, e.value)
+
+
+def test_workspace_layout_grows_with_tokens(T):
+    a = T.tpmlp_workspace_bytes(T.make_config(1024, 512, 1536, 8, "bf16", "swiglu"))
+    b = T.tpmlp_workspace_bytes(T.make_config(2048, 512, 1536, 8, "bf16", "swiglu"))
+    per_token = 512 * 2 + 4 + 2 * 1536 * 2 + 1536 * 2 + 2 * 1536 * 2 + 512 * 4  # n, rstd, GU, A, dGU, dN
+    assert b - a >= 1024 * per_token
+    assert a % 256 == 0 and b % 256 == 0
+
+
+def test_status_strings_and_kernel_names(T):
+    L = T.lib()
+    for s in range(7):
+        assert L.tpmlp_status_string(s)
+    names = T.kernel_names()
+    assert len(names) == L.tpmlp_num_kernel_ids() and "gemm_down_reduce" in names
+    assert L.tpmlp_kernel_name(-1) is None and L.tpmlp_kernel_name(len(names)) is None
+
+
+def test_null_context_is_rejected(T):
+    L = T.lib()
+    assert L.tpmlp_sgd_step(None, 0.1) == T.ERR_ARG
+    assert L.tpmlp_sync(None) == T.ERR_ARG
+    assert L.tpmlp_launch_count(None) == 0
+    L.tpmlp_destroy(None)
+
+
+def test_missing_library_fails_loudly(tmp_path, monkeypatch):
+    from tensor_transformer_mlp_rmsnorm_gb300 import tpmlp
+    monkeypatch.setattr(tpmlp, "LIB_PATH", str(tmp_path / "absent.so"))
+    monkeypatch.setattr(tpmlp, "_LIB", None)
+    with pytest.raises(tpmlp.TPMLPError):
+        tpmlp.lib()
