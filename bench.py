@@ -1,0 +1,368 @@
+"""Benchmark of one training step of the tensor-parallel MLP sublayer:
+forward -> MSE loss -> backward -> SGD, on the Llama-3-8B-shaped bf16 SwiGLU
+block (16384 tokens = 4 x 4096, hidden 4096, ffn 14336, t = 8 logical
+shards), through the library's public API.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints one JSON line (rank 0).  ``value`` is whole-job GEMM TFLOP/s
+(18 N H F algorithmic flops per step) with every input resident in HBM; the
+``e2e`` figure adds the per-step host->device copy of x and the target from
+pinned memory and the device->host read of the loss.  With N > 1 (torchrun)
+every rank runs an independent replica of the step on its own GPU (the path
+has no data exchange between replicas), so scaling is weak.
+
+``--impl reference`` times the CPU oracle (float64 numpy) on the host cores on
+a bounded token sample of the same workload; it is the reference arm here.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import signal
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import synth  # noqa: E402
+
+METRIC = "TP-MLP fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak"
+WORKLOAD = "bf16_llama8b"
+T_SHARDS = 8
+FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+# algorithmic flops per launch of each GEMM, in units of N*H*F
+GEMM_UNITS = {"gemm_gateup_act": 4, "gemm_down_reduce": 2, "gemm_dgrad_act": 2, "gemm_wgrad_down": 2,
+              "gemm_wgrad_gateup": 4, "gemm_dgrad_norm_reduce": 4}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(p))
+        return {k: float(d[k]) for k in FALLBACK}, "measured"
+    except Exception:
+        return dict(FALLBACK), "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.idx = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks_", suffix=".csv")
+            os.close(fd)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.idx), f"--query-gpu={self.Q}",
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.send_signal(signal.SIGTERM)
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        rows = []
+        for line in open(self.path):
+            parts = [s.strip() for s in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                rows.append({"sm": float(parts[1]), "max": float(parts[2]), "power": float(parts[3]),
+                             "hw": parts[5], "hw_thermal": parts[6], "sw_thermal": parts[7], "sw_power": parts[8]})
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return None
+        load = [r for r in rows if r["power"] > 200.0] or rows
+        reasons = set()
+        for r in rows:
+            for key, name in (("hw", "hw_slowdown"), ("hw_thermal", "hw_thermal_slowdown"),
+                              ("sw_thermal", "sw_thermal_slowdown"), ("sw_power", "sw_power_cap")):
+                if r[key].lower().startswith("active"):
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(r["sm"] for r in load), "sm_max_mhz": max(r["max"] for r in rows),
+                "reasons": sorted(reasons), "samples": len(rows)}
+
+
+def cpu_oracle_tflops(cfg, inp, budget_s: float, min_tokens: int = 16, max_tokens: int = 4096):
+    """Time the oracle's dense step on a token sample sized to about budget_s."""
+    from oracle import tpmlp_oracle as O
+    p = {k: inp[k] for k in synth.param_names(cfg.act)}
+
+    def run(n):
+        t0 = time.perf_counter()
+        O.dense_step(p, inp["x"][:n], inp["target"][:n], cfg.eps, cfg.lr, cfg.act)
+        return time.perf_counter() - t0
+
+    n = min_tokens
+    dt = run(n)
+    while dt < budget_s / 4 and n < max_tokens:
+        n = min(max_tokens, n * 2)
+        dt = run(n)
+    flops = 18.0 * n * cfg.hidden * cfg.ffn
+    return flops / dt / 1e12, n, dt
+
+
+def host_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except Exception:
+        return os.cpu_count() or 1
+
+
+def reference_arm(args):
+    world, rank, _ = dist_env()
+    if rank != 0:
+        return 0
+    cfg = synth.CONFIGS[args.workload]
+    # the oracle needs the full weights but only a token sample
+    sample = max(16, args.ref_tokens)
+    inp = synth.make_inputs(cfg.with_tokens(sample), seed=1234)
+    from oracle import tpmlp_oracle as O
+    p = {k: inp[k] for k in synth.param_names(cfg.act)}
+    budget = 150.0  # seconds for warmup + timed steps
+
+    def step(n):
+        O.dense_step(p, inp["x"][:n], inp["target"][:n], cfg.eps, cfg.lr, cfg.act)
+
+    n = sample
+    t0 = time.perf_counter()
+    step(n)
+    one = time.perf_counter() - t0
+    while one * (args.steps + args.warmup) > budget and n > 1:
+        n = max(1, n // 2)
+        t0 = time.perf_counter()
+        step(n)
+        one = time.perf_counter() - t0
+    for _ in range(args.warmup):
+        step(n)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step(n)
+    el = time.perf_counter() - t0
+    flops = 18.0 * n * cfg.hidden * cfg.ffn
+    val = flops * args.steps / el / 1e12
+    cores = host_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: tokens={cfg.tokens} hidden={cfg.hidden} ffn={cfg.ffn} t={T_SHARDS} "
+                               f"act={cfg.act}", "tokens_per_step_sampled": n, "parallelism": "replicas"},
+        "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
+                         "sample": f"first {n} of {cfg.tokens} tokens per step, full weights, float64 numpy"},
+        "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def ours(args):
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP, build
+    build.build()
+    cfg = synth.CONFIGS[args.workload]
+    N, H, F = cfg.tokens, cfg.hidden, cfg.ffn
+    t = args.t
+    inp = synth.make_inputs(cfg, seed=1234 + rank)
+    bf = torch.bfloat16
+
+    def dev_bf16(a):
+        return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(bf)
+
+    params = {k: dev_bf16(inp[k]) for k in synth.param_names(cfg.act)}
+    masters = {k: torch.from_numpy(np.ascontiguousarray(inp[k], dtype=np.float32)).to(dev)
+               for k in synth.param_names(cfg.act)}
+    x_host = torch.from_numpy(np.ascontiguousarray(inp["x"], dtype=np.float32)).to(bf).pin_memory()
+    tg_host = torch.from_numpy(np.ascontiguousarray(inp["target"], dtype=np.float32)).to(bf).pin_memory()
+    cpu_inp = inp if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    del inp
+    x = x_host.to(dev)
+    target = tg_host.to(dev)
+    m = TPMLP(N, H, F, max_t=max(8, t), dtype=cfg.dtype, act=cfg.act, device=dev)
+    m.bind_master(masters)
+    y = torch.empty_like(x)
+    dy = torch.empty_like(x)
+    dx = torch.empty_like(x)
+    grads = m.new_grads()
+    loss = torch.zeros(1, dtype=torch.float32, device=dev)
+    loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
+
+    def step():
+        m.forward(x, params["norm_w"], params["w_gate_up"], params["w_down"], params["b_down"], cfg.eps, t, y=y)
+        m.mse_loss_grad(y, target, dy=dy, loss=loss)
+        m.backward(dy, dx=dx, grads=grads)
+        m.sgd_step(cfg.lr)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    m.sync()
+    stream = m.stream
+    # ---------------------------------------------------------- device-resident timing
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    m.set_timing(True)
+    launches0 = m.launch_count()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    launches = m.launch_count() - launches0
+    ktimes = m.read_kernel_times()
+    m.set_timing(False)
+    clk = clocks.stop()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    m.sync()
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    flops_step = cfg.gemm_flops
+    value = flops_step * args.steps * world / (ms / 1e3) / 1e12
+    # ---------------------------------------------------------- end-to-end through the public API
+    barrier()
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 2)
+    f0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            x.copy_(x_host, non_blocking=True)
+            target.copy_(tg_host, non_blocking=True)
+            step()
+            loss_host.copy_(loss, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ems = f0.elapsed_time(f1)
+    if world > 1:
+        tt = torch.tensor([ems], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ems = float(tt.item())
+    e2e_value = flops_step * e2e_steps * world / (ems / 1e3) / 1e12
+    m.sync()
+
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    pk, pk_src = peaks()
+    # dominant kernel and its roofline
+    ktot = {k: v[0] for k, v in ktimes.items()}
+    top = max(ktot, key=ktot.get)
+    top_ms, top_n = ktimes[top]
+    per_launch_ms = top_ms / max(1, top_n)
+    gemm_ms = sum(ktimes[k][0] for k in ktimes if k in GEMM_UNITS)
+    if top in GEMM_UNITS:
+        achieved = GEMM_UNITS[top] * N * H * F / (per_launch_ms / 1e3) / 1e12
+        roof = {"kernel": top, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
+                "peak_kind": f"bf16_tflops_sustained ({pk_src}); kernel timed inside a long step",
+                "frac_of_burst": achieved / pk["bf16_tflops"], "traffic": None,
+                "flops_per_launch": GEMM_UNITS[top] * N * H * F, "avg_launch_ms": per_launch_ms}
+    else:
+        roof = {"kernel": top, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": None, "traffic": None}
+    cpu = None
+    if cpu_inp is not None:
+        v, n, dt = cpu_oracle_tflops(cfg, cpu_inp, budget_s=args.cpu_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"dense fwd+loss+bwd+SGD of the first {n} of {N} tokens with the full weights, "
+                         f"float64 numpy, {dt:.1f} s"}
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: Llama-3-8B-shaped SwiGLU MLP sublayer, tokens={N} (4x4096), "
+                               f"hidden={H}, ffn={F}, t={t} logical shards, lr={cfg.lr}",
+                   "global_batch": 4 * world, "seq_len": 4096, "tokens_per_gpu": N, "t": t,
+                   "parallelism": f"replicas x{world}",
+                   "l2": "no flush: per-step working set ~4.5 GB >> 129 MB L2 (weights 336 MB, x 128 MB)"},
+        "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
+                             "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"],
+                             "source": pk_src},
+        "gemm_only_tflops": flops_step * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None,
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][0])},
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * N * H * 2,
+                "d2h_bytes_per_step": 4, "steps": e2e_steps},
+        "clocks": clk,
+        "gpu_launches": launches,
+        "loss": float(loss_host.item()),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=100)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--t", type=int, default=T_SHARDS)
+    ap.add_argument("--cpu-budget", type=float, default=20.0)
+    ap.add_argument("--ref-tokens", type=int, default=256)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return reference_arm(args)
+    return ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

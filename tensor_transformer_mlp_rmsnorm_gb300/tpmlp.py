@@ -137,6 +137,7 @@ class TPMLP:
             self.workspace = torch.empty(max(nbytes, 256), dtype=torch.uint8, device=self.device)
         _check(lib().tpmlp_bind_workspace(self.ctx, _ptr(self.workspace), nbytes), self.ctx)
         self.tokens = 0
+        self._fwd = False
         self._loss = torch.zeros(1, dtype=torch.float32, device=self.device)
 
     def close(self):
@@ -173,11 +174,18 @@ class TPMLP:
                 self._t(b_1, (self.F,), name="b_1") if self.act == "gelu" else None,
                 self._t(w_down, (self.H, self.F), name="w_down"), self._t(b_down, (self.H,), name="b_down"))
         yp = self._t(y, (n, self.H), name="y")
+        self._fwd = False
         _check(lib().tpmlp_forward(self.ctx, n, *args, float(eps), int(t), yp), self.ctx)
         self.tokens = n
+        self._fwd = True
         return y
 
+    def _need_forward(self, what):
+        if not self._fwd:
+            raise TPMLPError(ERR_ORDER, f"{what} before forward")
+
     def mse_loss_grad(self, y, target, dy=None, loss=None):
+        self._need_forward("mse_loss_grad")
         n = self.tokens
         dy = torch.empty_like(y) if dy is None else dy
         loss = self._loss if loss is None else loss
@@ -196,6 +204,7 @@ class TPMLP:
         return g
 
     def backward(self, dy, dx=None, grads=None):
+        self._need_forward("backward")
         n = self.tokens
         dx = torch.empty_like(dy) if dx is None else dx
         g = self.new_grads() if grads is None else grads
