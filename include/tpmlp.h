@@ -176,6 +176,31 @@ TPMLP_API const char* tpmlp_last_error(const tpmlp_ctx* ctx);
 /* Free the host-side context.  Does not touch caller memory. */
 TPMLP_API void tpmlp_destroy(tpmlp_ctx* ctx);
 
+/* Loss and loss gradient without any device allocation or workspace.
+ *
+ * The paper has no counterpart: this entry point exists for callers that
+ * cannot call cudaMalloc -- code whose device memory is owned by a host
+ * framework's pool and budget, or a latency-bound loop where an allocation
+ * (which may synchronise the device) is not acceptable.  It computes the same
+ * result as tpmlp_mse_loss_grad, without a context:
+ *   loss = 0.5 * mean((y - target)^2) over n elements -> *loss_dev (float),
+ *   dy   = (y - target) / n,
+ * with y, target, dy of `dtype` (TPMLP_F32 or TPMLP_BF16), n >= 0 a multiple
+ * of 8, pointers 16-byte aligned, enqueued on `cuda_stream`.
+ * Its per-block partial sums live in a fixed array inside the library
+ * (TPMLP_NOALLOC_LOSS_MAX_BLOCKS doubles, 512 KiB, held by every GPU that
+ * loads the library until the process exits), so n is limited to
+ * TPMLP_NOALLOC_LOSS_MAX_BLOCKS * 2048 elements for bf16 and * 1024 for f32;
+ * larger n returns TPMLP_ERR_SHAPE before anything is enqueued.
+ * The first call on a device looks up that array's device address (with the
+ * device current); make that first call before any stream capture.  All
+ * calls share the array: calls whose kernels overlap on the GPU race on it.
+ * Errors: TPMLP_ERR_UNSUPPORTED (dtype), TPMLP_ERR_SHAPE (n), TPMLP_ERR_ARG
+ * (NULL / misaligned), TPMLP_ERR_CUDA; the message is in tpmlp_last_error(NULL). */
+#define TPMLP_NOALLOC_LOSS_MAX_BLOCKS 65536
+TPMLP_API tpmlp_status tpmlp_mse_loss_grad_noalloc(int32_t dtype, int64_t n, const void* y, const void* target,
+                                                   void* dy, float* loss_dev, void* cuda_stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -115,6 +115,8 @@ bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 
 }  // namespace
 
+void tpmlp::set_thread_error(const std::string& msg) { g_thread_err = msg; }
+
 struct tpmlp_ctx {
   tpmlp_config cfg{};
   cudaStream_t stream = nullptr;

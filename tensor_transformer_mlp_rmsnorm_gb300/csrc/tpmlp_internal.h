@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <string>
+
 #include "epilogue.cuh"
 
 namespace tpmlp {
@@ -75,5 +77,8 @@ struct SgdArgs {
   float lr;
 };
 cudaError_t launch_sgd(int dtype, const SgdArgs& a, int num_sms, cudaStream_t st);
+
+// Message returned by tpmlp_last_error(NULL) on this host thread.
+void set_thread_error(const std::string& msg);
 
 }  // namespace tpmlp

@@ -62,7 +62,9 @@ _SIGNATURES = {
     "tpmlp_status_string": (ctypes.c_char_p, [_i32]),
     "tpmlp_last_error": (ctypes.c_char_p, [_vp]),
     "tpmlp_destroy": (None, [_vp]),
+    "tpmlp_mse_loss_grad_noalloc": (_i32, [_i32, _i64, _vp, _vp, _vp, _fp, _vp]),
 }
+NOALLOC_LOSS_MAX_BLOCKS = 65536
 
 _LIB = None
 
@@ -112,6 +114,24 @@ def tpmlp_create(cfg: Config, stream=None):
     s = None if stream is None else ctypes.c_void_p(stream)
     _check(lib().tpmlp_create(ctypes.byref(cfg), s, ctypes.byref(out)))
     return out
+
+
+def tpmlp_mse_loss_grad_noalloc(y, target, dy, loss, stream=None):
+    """Loss and gradient without a context or workspace (no device allocation
+    by the library); y, target, dy: same dtype and size, loss: one float."""
+    dt = {torch.float32: F32, torch.bfloat16: BF16}.get(y.dtype)
+    if dt is None or target.dtype != y.dtype or dy.dtype != y.dtype or loss.dtype != torch.float32:
+        raise TPMLPError(ERR_ARG, "y/target/dy must share dtype float32 or bfloat16; loss must be float32")
+    if target.numel() != y.numel() or dy.numel() != y.numel() or loss.numel() < 1:
+        raise TPMLPError(ERR_ARG, "y, target and dy must have the same number of elements")
+    for t in (y, target, dy, loss):
+        if not t.is_cuda or not t.is_contiguous():
+            raise TPMLPError(ERR_ARG, "tensors must be contiguous CUDA tensors")
+    s = stream if stream is not None else torch.cuda.current_stream(y.device).cuda_stream
+    with torch.cuda.device(y.device):
+        _check(lib().tpmlp_mse_loss_grad_noalloc(dt, y.numel(), _ptr(y), _ptr(target), _ptr(dy), _ptr(loss),
+                                                 ctypes.c_void_p(s)))
+    return loss, dy
 
 
 class TPMLP:
