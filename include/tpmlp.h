@@ -76,11 +76,14 @@ typedef enum { TPMLP_SWIGLU = 0, TPMLP_GELU = 1 } tpmlp_act;
  *    normed-input gradient.
  *  FORCE_TIMEOUT: the next forward's first GEMM waits on an event that never
  *    happens, gives up after ~2 ms and records TPMLP_ERR_TIMEOUT (tests the
- *    bounded-wait path without a hang). */
+ *    bounded-wait path without a hang).
+ *  GEMM_SINGLE_CTA: run the bf16 GEMMs with single-CTA 128x256 tiles instead
+ *    of CTA-pair 256x256 tiles (same results up to rounding; for testing). */
 enum {
   TPMLP_DBG_SKIP_FWD_REDUCE = 1u,
   TPMLP_DBG_SKIP_BWD_REDUCE = 2u,
-  TPMLP_DBG_FORCE_TIMEOUT = 4u
+  TPMLP_DBG_FORCE_TIMEOUT = 4u,
+  TPMLP_DBG_GEMM_SINGLE_CTA = 8u
 };
 
 typedef struct {

@@ -1,15 +1,24 @@
 // Persistent, warp-specialised bf16 GEMM on the sm_103a tensor cores.
 //
-//   warp 0      : TMA producer -- one thread streams 128x64 A and 256x64 B
-//                 tiles (128-byte swizzle) into a 4-stage shared-memory ring.
+//   warp 0      : TMA producer -- one thread streams A and B tiles (128-byte
+//                 swizzle) into a shared-memory ring.
 //   warp 1      : owns tensor memory (512 columns = two 128x256 f32
-//                 accumulators) and one thread issues tcgen05.mma
-//                 (M=128, N=256, K=16), committing each stage back to the
-//                 producer and each finished tile to the epilogue.
+//                 accumulators); one thread issues tcgen05.mma, committing
+//                 each stage back to the producer and each finished tile to
+//                 the epilogue.
 //   warps 2..5  : epilogue -- tcgen05.ld the accumulator (lane = row), apply
 //                 the fused element-wise step, store to global memory.  The
 //                 two accumulators let tile i's epilogue overlap tile i+1's
 //                 main loop.
+//
+// Two tile shapes share the code:
+//   * CTA pair (cluster of 2, cta_group::2): a 256x256 tile per pair.  Each
+//     CTA loads 128 rows of A and 128 of the 256 B columns per 64-deep stage
+//     (32 KB, 6 stages), the even CTA issues M=256 MMAs for both, and each
+//     CTA's tensor memory holds its 128 rows.  Per SM this halves the B bytes
+//     per flop and leaves room for a deeper ring -- the default.
+//   * single CTA (cta_group::1): a 128x256 tile, 4 stages of 48 KB; used when
+//     the problem has a single 128-row block.
 //
 // The contraction runs over up to two K segments in order.  For the
 // row-parallel down projection the K axis is the FFN axis, so shard s's
@@ -36,20 +45,31 @@
 namespace tpmlp {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BN = 256;
-constexpr int BK = 64;
+constexpr int BM = 128;  // accumulator rows per CTA (TMEM lanes)
+constexpr int BN = 256;  // accumulator columns (MMA N)
+constexpr int BK = 64;   // K depth of one stage (one 128-byte swizzle row of bf16)
 constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int A_STAGE_BYTES = BM * BK * 2;  // 16 KB
-constexpr int B_STAGE_BYTES = BN * BK * 2;  // 32 KB
-constexpr int STAGE_BYTES = A_STAGE_BYTES + B_STAGE_BYTES;
-constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024;
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s per wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s for draining after an abort
+constexpr uint64_t PEER_DRAIN_NS = 5000000ull;      // 5 ms: a CTA-pair peer's loads land long before this
 constexpr uint64_t FORCED_LIMIT_NS = 2000000ull;    // 2 ms for the forced-timeout debug wait
+
+template <bool PAIR>
+struct TileCfg {
+  static constexpr int STAGES = PAIR ? 6 : 4;
+  static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns held by this CTA per stage
+  static constexpr int A_BYTES = BM * BK * 2;
+  static constexpr int B_BYTES = B_ROWS * BK * 2;
+  static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+  // + 1 KB for 1024-byte alignment; the pair shape keeps 16 KB of slack after
+  // the ring so that no operand read can leave the allocation.
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + (PAIR ? 16384 : 0);
+  static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // output rows per tile (per pair)
+  static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;
+  static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8 : 4;  // one per epilogue warp, both CTAs
+};
 
 struct TcParams {
   int M, N;
@@ -171,13 +191,14 @@ __device__ __forceinline__ void epi_chunk(const EpiParams& ep, int row, int col,
   }
 }
 
-template <bool A_MN, bool B_MN, int EPI>
+template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const TcParams p) {
+  using C = TileCfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ __align__(8) uint64_t empty_bar[STAGES];
+  __shared__ __align__(8) uint64_t full_bar[C::STAGES];
+  __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
   __shared__ __align__(8) uint64_t tfull_bar[2];
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
@@ -187,21 +208,25 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
-  uint8_t* sB = smem + STAGES * A_STAGE_BYTES;
+  uint8_t* sB = smem + C::STAGES * C::A_BYTES;
   volatile int* abort_flag = &abort_sh;
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
-  constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN, A_MN, B_MN);
+  const uint32_t rank = PAIR ? cluster_ctarank() : 0u;
+  const bool leader = rank == 0;
+  const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
+  const int num_workers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
+  constexpr uint32_t IDESC = idesc_bf16_f32(C::TILE_M, BN, A_MN, B_MN);
 
   if (threadIdx.x == 0) {
-    for (int s = 0; s < STAGES; ++s) {
+    for (int s = 0; s < C::STAGES; ++s) {
       mbar_init(&full_bar[s], 1);
       mbar_init(&empty_bar[s], 1);
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(&tfull_bar[b], 1);
-      mbar_init(&tempty_bar[b], 128);
+      mbar_init(&tempty_bar[b], C::EPI_ARRIVALS);
     }
     mbar_init(&drain_bar, 1);
     mbar_init(&never_bar, 1);
@@ -213,25 +238,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tma_prefetch_desc(&map_b);
   }
   if (warp == 1) {
-    tmem_alloc(&tmem_base_sh, TMEM_COLS);
-    tmem_relinquish();
+    if (PAIR) {
+      tmem_alloc_pair(&tmem_base_sh, TMEM_COLS);
+      tmem_relinquish_pair();
+    } else {
+      tmem_alloc(&tmem_base_sh, TMEM_COLS);
+      tmem_relinquish();
+    }
   }
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // the peer's barriers exist before anything targets them
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
 
+  if (p.force_timeout) {
+    // Debug: a wait on a barrier nobody arrives on gives up and aborts the CTA.
+    if (threadIdx.x == 0) mbar_wait(&never_bar, 0, abort_flag, p.status, STATUS_TIMEOUT, FORCED_LIMIT_NS);
+    __syncthreads();
+  }
+
   if (warp == 0) {
-    if (lane == 0) {
+    if (lane == 0 && !*abort_flag) {
       // ------------------------------------------------------------ producer
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
         int mb, nb;
         tile_coords(p, tile, mb, nb);
-        const int m0 = mb * BM;
-        int brow0, brow1;
+        const int m0 = mb * C::TILE_M + (int)rank * BM;
+        int brow0, brow1;  // first B row (K-major) / column (MN-major) of each 128-wide half
         if (p.paired) {
           brow0 = nb * (BN / 2);
           brow1 = p.pair_off + nb * (BN / 2);
@@ -239,32 +276,50 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           brow0 = nb * BN;
           brow1 = nb * BN + BN / 2;
         }
+        if (PAIR) brow0 = rank ? brow1 : brow0;  // each CTA of the pair holds one half
         for (int seg = 0; ok && seg < 2; ++seg) {
           for (int kb = p.kb[2 * seg]; kb < p.kb[2 * seg + 1]; ++kb) {
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
               ok = false;
               break;
             }
-            mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+            if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
             const int k0 = kb * BK;
-            uint8_t* a_dst = sA + stage * A_STAGE_BYTES;
-            uint8_t* b_dst = sB + stage * B_STAGE_BYTES;
-            if (!A_MN) {
-              tma_load_2d(a_dst, &map_a, &full_bar[stage], k0, m0);
+            uint8_t* a_dst = sA + stage * C::A_BYTES;
+            uint8_t* b_dst = sB + stage * C::B_BYTES;
+            if (PAIR) {
+              const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);  // the leader's barrier
+              if (!A_MN) {
+                tma_load_2d_pair(a_dst, &map_a, fb, k0, m0);
+              } else {
+                tma_load_2d_pair(a_dst, &map_a, fb, m0, k0);
+                tma_load_2d_pair(a_dst + 8192, &map_a, fb, m0 + 64, k0);
+              }
+              if (!B_MN) {
+                tma_load_2d_pair(b_dst, &map_b, fb, k0, brow0);
+              } else {
+                tma_load_2d_pair(b_dst, &map_b, fb, brow0, k0);
+                tma_load_2d_pair(b_dst + 8192, &map_b, fb, brow0 + 64, k0);
+              }
             } else {
-              tma_load_2d(a_dst, &map_a, &full_bar[stage], m0, k0);
-              tma_load_2d(a_dst + 8192, &map_a, &full_bar[stage], m0 + 64, k0);
-            }
-            if (!B_MN) {
-              tma_load_2d(b_dst, &map_b, &full_bar[stage], k0, brow0);
-              tma_load_2d(b_dst + B_STAGE_BYTES / 2, &map_b, &full_bar[stage], k0, brow1);
-            } else {
+              if (!A_MN) {
+                tma_load_2d(a_dst, &map_a, &full_bar[stage], k0, m0);
+              } else {
+                tma_load_2d(a_dst, &map_a, &full_bar[stage], m0, k0);
+                tma_load_2d(a_dst + 8192, &map_a, &full_bar[stage], m0 + 64, k0);
+              }
+              if (!B_MN) {
+                tma_load_2d(b_dst, &map_b, &full_bar[stage], k0, brow0);
+                tma_load_2d(b_dst + C::B_BYTES / 2, &map_b, &full_bar[stage], k0, brow1);
+              } else {
 #pragma unroll
-              for (int j = 0; j < 4; ++j) tma_load_2d(b_dst + j * 8192, &map_b, &full_bar[stage], brow0 + 64 * j, k0);
+                for (int j = 0; j < 4; ++j)
+                  tma_load_2d(b_dst + j * 8192, &map_b, &full_bar[stage], brow0 + 64 * j, k0);
+              }
             }
-            if (++stage == STAGES) {
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
@@ -272,20 +327,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       if (!ok || *abort_flag) {
-        // Wait for the copies this thread started before the CTA may exit.
+        // Let the copies this CTA started land before it may exit.  The
+        // leader sees them (and the peer's) complete on its stage barriers;
+        // the peer waits until its stages are consumed or a short time passes.
         int no_abort = 0;
-        for (int s = 0; s < STAGES; ++s)
-          if (armed & (1u << s))
-            mbar_wait(&full_bar[s], (armed_par >> s) & 1u, &no_abort, p.status, STATUS_TIMEOUT, DRAIN_LIMIT_NS);
+        for (int s = 0; s < C::STAGES; ++s) {
+          if (!(armed & (1u << s))) continue;
+          const uint32_t par = (armed_par >> s) & 1u;
+          if (leader)
+            mbar_wait(&full_bar[s], par, &no_abort, p.status, STATUS_TIMEOUT, DRAIN_LIMIT_NS);
+          else
+            mbar_wait(&empty_bar[s], par, &no_abort, p.status, 0u, PEER_DRAIN_NS);
+        }
       }
     }
   } else if (warp == 1) {
-    if (lane == 0) {
+    if (lane == 0 && leader) {
       // ------------------------------------------------------------ MMA issuer
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool ok = true;
-      if (p.force_timeout) ok = mbar_wait(&never_bar, 0, abort_flag, p.status, STATUS_TIMEOUT, FORCED_LIMIT_NS);
-      for (int tile = blockIdx.x; ok && tile < p.num_tiles; tile += gridDim.x) {
+      bool ok = !*abort_flag;
+      for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
         if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
           ok = false;
           break;
@@ -300,46 +361,63 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               break;
             }
             tc_fence_after();
-            const uint32_t a_base = smem_u32(sA + stage * A_STAGE_BYTES);
-            const uint32_t b_base = smem_u32(sB + stage * B_STAGE_BYTES);
+            const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
+            const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
 #pragma unroll
             for (int k = 0; k < BK / UMMA_K; ++k) {
               const uint64_t a_desc =
                   A_MN ? sw128_desc(a_base + k * 2048, 8192, 1024) : sw128_desc(a_base + k * 32, 16, 1024);
               const uint64_t b_desc =
                   B_MN ? sw128_desc(b_base + k * 2048, 8192, 1024) : sw128_desc(b_base + k * 32, 16, 1024);
-              tc_mma_f16(d_tmem, a_desc, b_desc, IDESC, accumulate);
+              if (PAIR)
+                tc_mma_f16_pair(d_tmem, a_desc, b_desc, IDESC, accumulate);
+              else
+                tc_mma_f16(d_tmem, a_desc, b_desc, IDESC, accumulate);
               accumulate = 1;
             }
-            tc_commit(&empty_bar[stage]);
-            if (++stage == STAGES) {
+            if (PAIR)
+              tc_commit_pair(&empty_bar[stage], 0x3);
+            else
+              tc_commit(&empty_bar[stage]);
+            if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
             }
           }
         }
         if (!ok) break;
-        tc_commit(&tfull_bar[acc]);
+        if (PAIR)
+          tc_commit_pair(&tfull_bar[acc], 0x3);
+        else
+          tc_commit(&tfull_bar[acc]);
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // No MMA may still be running when tensor memory is released.
-      tc_commit(&drain_bar);
+      if (PAIR)
+        tc_commit_pair(&drain_bar, 0x3);
+      else
+        tc_commit(&drain_bar);
       int no_abort = 0;
       mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, DRAIN_LIMIT_NS);
+    } else if (lane == 0 && PAIR) {
+      // Peer CTA: its tensor memory is written by the leader's MMAs; wait for
+      // the leader's final commit (bounded, so an aborted leader cannot hold it).
+      int no_abort = 0;
+      mbar_wait(&drain_bar, 0, &no_abort, p.status, 0u, DRAIN_LIMIT_NS);
     }
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     uint32_t acc = 0, acc_phase = 0;
-    for (int tile = blockIdx.x; tile < p.num_tiles; tile += gridDim.x) {
+    for (int tile = worker; tile < p.num_tiles; tile += num_workers) {
       int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
       int mb, nb;
       tile_coords(p, tile, mb, nb);
-      const int row = mb * BM + q * 32 + lane;
+      const int row = mb * C::TILE_M + (int)rank * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       uint32_t r0[32], r1[32];
       if (EPI == EPI_GATEUP_SWIGLU) {
@@ -360,7 +438,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
       }
       tc_fence_before();
-      mbar_arrive(&tempty_bar[acc]);
+      __syncwarp();
+      if (lane == 0) {
+        if (PAIR)
+          mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+        else
+          mbar_arrive(&tempty_bar[acc]);
+      }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
@@ -368,10 +452,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
   tc_fence_before();
   __syncthreads();
+  if (PAIR) cluster_sync();  // neither CTA leaves while the other may still signal it
   if (warp == 1) {
     __syncwarp();
     tc_fence_after();
-    tmem_dealloc(tmem_base, TMEM_COLS);
+    if (PAIR)
+      tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    else
+      tmem_dealloc(tmem_base, TMEM_COLS);
   }
 }
 
@@ -396,7 +484,7 @@ EncodeTiledFn get_encode_fn() {
 }
 
 // 2-D bf16 tensor [outer, inner] with row pitch `ld` elements; box of
-// box_inner (= 64, one 128-byte swizzle row) x box_outer.
+// 64 (one 128-byte swizzle row) x box_outer.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
@@ -410,30 +498,71 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return r == CUDA_SUCCESS;
 }
 
-template <bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_inst(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, int grid, cudaStream_t st) {
+template <bool PAIR, bool A_MN, bool B_MN, int EPI>
+cudaError_t launch_inst(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, int num_sms,
+                        cudaStream_t st) {
+  using C = TileCfg<PAIR>;
+  auto kfn = gemm_tc_kernel<PAIR, A_MN, B_MN, EPI>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
-  std::call_once(once, [] {
-    attr_err = cudaFuncSetAttribute(gemm_tc_kernel<A_MN, B_MN, EPI>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    SMEM_BYTES);
+  static int max_workers = 0;
+  std::call_once(once, [&] {
+    attr_err = cudaFuncSetAttribute(kfn, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    max_workers = num_sms;
+    if (attr_err == cudaSuccess && PAIR) {
+      cudaLaunchConfig_t cfg = {};
+      cudaLaunchAttribute attr[1];
+      attr[0].id = cudaLaunchAttributeClusterDimension;
+      attr[0].val.clusterDim.x = 2;
+      attr[0].val.clusterDim.y = 1;
+      attr[0].val.clusterDim.z = 1;
+      cfg.gridDim = dim3(2 * (num_sms / 2), 1, 1);
+      cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+      cfg.dynamicSmemBytes = C::SMEM_BYTES;
+      cfg.attrs = attr;
+      cfg.numAttrs = 1;
+      int clusters = 0;
+      attr_err = cudaOccupancyMaxActiveClusters(&clusters, kfn, &cfg);
+      max_workers = clusters;
+    }
   });
   if (attr_err != cudaSuccess) return attr_err;
-  gemm_tc_kernel<A_MN, B_MN, EPI><<<grid, NUM_THREADS, SMEM_BYTES, st>>>(ma, mb, p);
-  return cudaGetLastError();
+  if (max_workers <= 0) return cudaErrorInvalidConfiguration;
+  const int workers = p.num_tiles < max_workers ? p.num_tiles : max_workers;
+  if (!PAIR) {
+    kfn<<<workers, NUM_THREADS, C::SMEM_BYTES, st>>>(ma, mb, p);
+    return cudaGetLastError();
+  }
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * workers, 1, 1);
+  cfg.blockDim = dim3(NUM_THREADS, 1, 1);
+  cfg.dynamicSmemBytes = C::SMEM_BYTES;
+  cfg.stream = st;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kfn, ma, mb, p);
 }
 
-}  // namespace
-
-cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout) {
-  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+template <bool PAIR>
+cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout) {
+  using C = TileCfg<PAIR>;
   TcParams p{};
   p.M = g.M;
   p.N = g.N;
-  p.num_m_blk = (g.M + BM - 1) / BM;
+  p.num_m_blk = (g.M + C::TILE_M - 1) / C::TILE_M;
   p.num_n_blk = g.paired ? (g.N + BN / 2 - 1) / (BN / 2) : (g.N + BN - 1) / BN;
   p.num_tiles = p.num_m_blk * p.num_n_blk;
-  p.group_m = p.num_m_blk < 16 ? p.num_m_blk : 16;
+  // Tiles run in groups of group_m row blocks sweeping every column block, so
+  // a group's A rows (about 32 MB) stay in L2 while B streams past them.
+  const int64_t a_block_bytes = (int64_t)C::TILE_M * g.k_extent * 2;
+  int gm = (int)((32ll << 20) / (a_block_bytes > 0 ? a_block_bytes : 1));
+  gm = gm < 4 ? 4 : (gm > 64 ? 64 : gm);
+  p.group_m = p.num_m_blk < gm ? p.num_m_blk : gm;
   for (int s = 0; s < 2; ++s) {
     const int64_t k0 = g.kseg[2 * s], k1 = g.kseg[2 * s + 1];
     if (k1 < k0 || k0 % BK != 0 || (k1 % BK != 0 && k1 != g.k_extent) || k1 > g.k_extent)
@@ -450,40 +579,51 @@ cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int num_sms, uint
   p.status = status;
   p.force_timeout = force_timeout;
 
+  // Box heights: K-major A = this CTA's 128 rows; K-major B = 128 rows per
+  // box; MN-major operands move in 64 (MN) x 64 (K) boxes.
   CUtensorMap ma, mb;
   bool ok;
   if (!g.a_mn)
-    ok = make_map(&ma, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, 128);
+    ok = make_map(&ma, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
   else
     ok = make_map(&ma, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, 64);
   if (!ok) return cudaErrorInvalidValue;
   if (!g.b_mn)
-    ok = make_map(&mb, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, 128);
+    ok = make_map(&mb, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
   else
     ok = make_map(&mb, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, 64);
   if (!ok) return cudaErrorInvalidValue;
 
-  const int grid = p.num_tiles < num_sms ? p.num_tiles : num_sms;
   const int key = (g.a_mn ? 100 : 0) + (g.b_mn ? 10 : 0) + g.epi;
   switch (key) {
     case 0 + EPI_GATEUP_SWIGLU:
       if (!g.paired) return cudaErrorInvalidValue;
-      return launch_inst<false, false, EPI_GATEUP_SWIGLU>(ma, mb, p, grid, st);
+      return launch_inst<PAIR, false, false, EPI_GATEUP_SWIGLU>(ma, mb, p, num_sms, st);
     case 0 + EPI_FC1_GELU:
-      return launch_inst<false, false, EPI_FC1_GELU>(ma, mb, p, grid, st);
+      return launch_inst<PAIR, false, false, EPI_FC1_GELU>(ma, mb, p, num_sms, st);
     case 0 + EPI_DOWN_RESID:
-      return launch_inst<false, false, EPI_DOWN_RESID>(ma, mb, p, grid, st);
+      return launch_inst<PAIR, false, false, EPI_DOWN_RESID>(ma, mb, p, num_sms, st);
     case 10 + EPI_DGRAD_SWIGLU:
-      return launch_inst<false, true, EPI_DGRAD_SWIGLU>(ma, mb, p, grid, st);
+      return launch_inst<PAIR, false, true, EPI_DGRAD_SWIGLU>(ma, mb, p, num_sms, st);
     case 10 + EPI_DGRAD_GELU:
-      return launch_inst<false, true, EPI_DGRAD_GELU>(ma, mb, p, grid, st);
+      return launch_inst<PAIR, false, true, EPI_DGRAD_GELU>(ma, mb, p, num_sms, st);
     case 110 + EPI_STORE_F32:
-      return launch_inst<true, true, EPI_STORE_F32>(ma, mb, p, grid, st);
+      return launch_inst<PAIR, true, true, EPI_STORE_F32>(ma, mb, p, num_sms, st);
     case 10 + EPI_STORE_F32:
-      return launch_inst<false, true, EPI_STORE_F32>(ma, mb, p, grid, st);
+      return launch_inst<PAIR, false, true, EPI_STORE_F32>(ma, mb, p, num_sms, st);
     default:
       return cudaErrorNotSupported;
   }
+}
+
+}  // namespace
+
+cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout) {
+  if (g.M <= 0 || g.N <= 0) return cudaSuccess;
+  // CTA pairs unless the problem has a single 128-row block (or 1-CTA tiles are forced).
+  const bool pair = g.tile_mode == 2 || (g.tile_mode == 0 && g.M > BM);
+  if (pair) return launch_shape<true>(g, st, num_sms, status, force_timeout);
+  return launch_shape<false>(g, st, num_sms, status, force_timeout);
 }
 
 }  // namespace tpmlp

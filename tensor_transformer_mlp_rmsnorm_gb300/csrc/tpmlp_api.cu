@@ -195,9 +195,13 @@ struct tpmlp_ctx {
 
 namespace {
 
-tpmlp_status run_gemm(tpmlp_ctx* c, int id, const GemmDesc& g, int force_timeout = 0) {
-  if (c->cfg.dtype == TPMLP_BF16)
+tpmlp_status run_gemm(tpmlp_ctx* c, int id, const GemmDesc& desc, int force_timeout = 0) {
+  if (c->cfg.dtype == TPMLP_BF16) {
+    GemmDesc g = desc;
+    if (c->dbg_flags & TPMLP_DBG_GEMM_SINGLE_CTA) g.tile_mode = 1;
     return c->run(id, [&] { return launch_gemm_tc(g, c->stream, c->num_sms, c->status(), force_timeout); });
+  }
+  const GemmDesc& g = desc;
   return c->run(id, [&] { return launch_gemm_simt_f32(g, c->stream); });
 }
 
@@ -288,7 +292,7 @@ tpmlp_status tpmlp_set_stream(tpmlp_ctx* c, void* s) {
 
 tpmlp_status tpmlp_set_debug(tpmlp_ctx* c, uint32_t flags, int32_t shard) {
   if (!c) return TPMLP_ERR_ARG;
-  if (flags & ~7u) return c->fail(TPMLP_ERR_ARG, "unknown debug flag");
+  if (flags & ~15u) return c->fail(TPMLP_ERR_ARG, "unknown debug flag");
   if (shard < 0) return c->fail(TPMLP_ERR_ARG, "shard must be >= 0");
   c->dbg_flags = flags;
   c->dbg_shard = shard;

@@ -36,6 +36,7 @@ struct GemmDesc {
   int64_t kseg[4] = {0, 0, 0, 0};
   int epi = EPI_STORE_F32;
   EpiParams ep{};
+  int tile_mode = 0;  // tensor-core path: 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles
 };
 
 // tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory).

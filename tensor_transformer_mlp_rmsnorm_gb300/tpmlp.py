@@ -21,7 +21,7 @@ LIB_PATH = os.path.join(_HERE, "_build", "libtpmlp.so")
 OK, ERR_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ORDER, ERR_CUDA, ERR_TIMEOUT = range(7)
 F32, BF16 = 0, 1
 SWIGLU, GELU = 0, 1
-DBG_SKIP_FWD_REDUCE, DBG_SKIP_BWD_REDUCE, DBG_FORCE_TIMEOUT = 1, 2, 4
+DBG_SKIP_FWD_REDUCE, DBG_SKIP_BWD_REDUCE, DBG_FORCE_TIMEOUT, DBG_GEMM_SINGLE_CTA = 1, 2, 4, 8
 
 _DTYPES = {"f32": F32, "bf16": BF16}
 _ACTS = {"swiglu": SWIGLU, "gelu": GELU}

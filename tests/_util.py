@@ -72,8 +72,9 @@ def device_inputs(cfg: synth.Config, inp: dict):
 
 
 def gpu_step(cfg: synth.Config, inp: dict, t: int, lr: float, flags: int = 0, shard: int = 0,
-             masters: bool = True, mod=None):
-    """Forward, loss, backward and SGD through the binding; numpy results."""
+             masters: bool = True, mod=None, with_params: bool = True):
+    """Forward, loss, backward and SGD through the binding; numpy results
+    (the updated parameters only when ``with_params``)."""
     from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP
     m = mod or TPMLP(max(cfg.tokens, 1), cfg.hidden, cfg.ffn, max_t=max(8, t), dtype=cfg.dtype, act=cfg.act)
     d = device_inputs(cfg, inp)
@@ -93,12 +94,13 @@ def gpu_step(cfg: synth.Config, inp: dict, t: int, lr: float, flags: int = 0, sh
     out = {"y": to_np(y), "loss": float(loss.item()), "dy": to_np(dy), "dx": to_np(dx), "grads": grads}
     m.sgd_step(lr)
     m.sync()
-    if ms is not None:
-        out["new_master"] = {k: to_np(v) for k, v in ms.items()}
-    out["new_params"] = {k: to_np(params[k]) for k in params}
+    if with_params:
+        if ms is not None:
+            out["new_master"] = {k: to_np(v) for k, v in ms.items()}
+        out["new_params"] = {k: to_np(params[k]) for k in params}
     if cfg.act == "gelu":
         out["grads"]["w_1"] = out["grads"].pop("w_gate_up")
-        if ms is not None:
+        if ms is not None and with_params:
             out["new_master"]["w_1"] = out["new_master"].pop("w_gate_up")
     m.set_debug(0, 0)
     return out

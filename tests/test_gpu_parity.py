@@ -64,6 +64,17 @@ def test_bf16_swiglu_tiles_and_tails(N, H, F, ts):
         compare_step(cfg, gpu, ora, inp, 0.1)
 
 
+@pytest.mark.parametrize("N,H,F,t", [(300, 512, 1536, 4), (77, 328, 1000, 1), (1029, 256, 2048, 2)])
+def test_bf16_single_cta_tiles(N, H, F, t):
+    """The single-CTA 128x256 tile shape (the default is CTA pairs with 256x256 tiles)."""
+    from tensor_transformer_mlp_rmsnorm_gb300 import DBG_GEMM_SINGLE_CTA
+    cfg = synth.CONFIGS["bf16_h2048"].with_shape(N, H, F)
+    inp = synth.make_inputs(cfg, seed=13)
+    ora = oracle_step(cfg, inp, t, 0.1)
+    gpu = gpu_step(cfg, inp, t, 0.1, flags=DBG_GEMM_SINGLE_CTA)
+    compare_step(cfg, gpu, ora, inp, 0.1)
+
+
 def test_bf16_gelu_tiles_and_tails():
     cfg = synth.CONFIGS["bf16_gelu_h4096"].with_shape(333, 384, 1280)
     inp = synth.make_inputs(cfg, seed=12)
