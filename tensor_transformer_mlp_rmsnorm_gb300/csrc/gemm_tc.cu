@@ -63,9 +63,10 @@ struct TileCfg {
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // + 1 KB for 1024-byte alignment; the pair shape keeps 16 KB of slack after
-  // the ring so that no operand read can leave the allocation.
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 + (PAIR ? 16384 : 0);
+  // Epilogue staging: per epilogue warp up to three 32x32 bf16 tiles (or one
+  // 32x32 f32 tile), each 2 KB and 1024-byte aligned.
+  static constexpr int EPI_WARP_BYTES = 6144;
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_WARP_BYTES + 1024;  // + alignment
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // output rows per tile (per pair)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;
   static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8 : 4;  // one per epilogue warp, both CTAs
@@ -117,84 +118,139 @@ __device__ __forceinline__ void unpack8_bf16(uint4 v, float* f) {
   }
 }
 
-// Load 32 consecutive bf16 values as floats.
-__device__ __forceinline__ void load32_bf16(const __nv_bfloat16* src, float* f) {
-  const uint4* s = reinterpret_cast<const uint4*>(src);
-#pragma unroll
-  for (int i = 0; i < 4; ++i) unpack8_bf16(s[i], f + 8 * i);
-}
+// Raw bf16 inputs of one epilogue chunk (32 consecutive values of one row,
+// two tensors at most), loaded ahead of the math that uses them.
+struct EpiIn {
+  uint4 a[4];
+  uint4 b[4];
+};
 
-__device__ __forceinline__ void store32_bf16(__nv_bfloat16* dst, const float* f) {
-  uint4* d = reinterpret_cast<uint4*>(dst);
+// 32 consecutive bf16 values starting at src, of which the first n are read
+// (n <= 0: none); the rest are zero.
+__device__ __forceinline__ void load32_raw(const __nv_bfloat16* src, int n, uint4 (&o)[4]) {
+  if (n >= 32) {
+    const uint4* s4 = reinterpret_cast<const uint4*>(src);
 #pragma unroll
-  for (int i = 0; i < 4; ++i) d[i] = pack8_bf16(f + 8 * i);
-}
-
-// Epilogue of 32 consecutive output columns [col, col+32) of one row.
-// v = accumulator values; u = second accumulator half (paired layouts).
-template <int EPI>
-__device__ __forceinline__ void epi_chunk(const EpiParams& ep, int row, int col, const float* v, const float* u) {
-  typedef __nv_bfloat16 T;
-  if (row >= ep.M || col >= ep.N) return;
-  if (col + 32 > ep.N) {
-    const int n = ep.N - col;
-#pragma unroll
-    for (int i = 0; i < 32; ++i)
-      if (i < n) epi_elem<EPI, T>(ep, row, col + i, v[i], EPI == EPI_GATEUP_SWIGLU ? u[i] : 0.0f);
+    for (int i = 0; i < 4; ++i) o[i] = s4[i];
     return;
   }
-  const int64_t r = row;
+  const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+  uint32_t w[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) {
+    const uint32_t lo = 2 * i < n ? s16[2 * i] : 0u;
+    const uint32_t hi = 2 * i + 1 < n ? s16[2 * i + 1] : 0u;
+    w[i] = lo | (hi << 16);
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) o[i] = make_uint4(w[4 * i], w[4 * i + 1], w[4 * i + 2], w[4 * i + 3]);
+}
+
+__device__ __forceinline__ void unpack32(const uint4 (&v)[4], float* f) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) unpack8_bf16(v[i], f + 8 * i);
+}
+
+// Load n (<= 32) consecutive bf16 values as floats; the rest read as 0.
+__device__ __forceinline__ void load32_bf16_guard(const __nv_bfloat16* src, int n, float* f) {
+  uint4 v[4];
+  load32_raw(src, n, v);
+  unpack32(v, f);
+}
+
+// The per-row global inputs of chunk [col, col+32) (x, or G and U, or Z).
+template <int EPI>
+__device__ __forceinline__ void epi_load(const EpiParams& ep, int row, int col, EpiIn& in) {
+  typedef __nv_bfloat16 T;
+  if (EPI != EPI_DOWN_RESID && EPI != EPI_DGRAD_SWIGLU && EPI != EPI_DGRAD_GELU) return;
+  const int nvalid = (row < ep.M && col < ep.N) ? ep.N - col : 0;
+  const T* base = static_cast<const T*>(ep.in0) + (int64_t)(row < ep.M ? row : 0) * ep.ld_in0 + col;
+  load32_raw(base, nvalid, in.a);
+  if (EPI == EPI_DGRAD_SWIGLU) load32_raw(base + ep.pair_off, nvalid, in.b);
+}
+
+// Row r of a 32x32 staging tile in the layout the TMA store expects:
+// bf16 rows are 64 bytes with the 64-byte swizzle (16-byte chunk c of row r
+// at c ^ ((r >> 1) & 3)); f32 rows are 128 bytes with the 128-byte swizzle
+// (chunk c at c ^ (r & 7)).  Both are free of shared-memory bank conflicts
+// when the 32 lanes of a warp each write their own row.
+__device__ __forceinline__ void stage_row_bf16(uint8_t* tile, int r, const float* v) {
+  uint8_t* rowp = tile + r * 64;
+#pragma unroll
+  for (int c = 0; c < 4; ++c)
+    *reinterpret_cast<uint4*>(rowp + ((c ^ ((r >> 1) & 3)) << 4)) = pack8_bf16(v + 8 * c);
+}
+
+__device__ __forceinline__ void stage_row_f32(uint8_t* tile, int r, const float* v) {
+  uint8_t* rowp = tile + r * 128;
+#pragma unroll
+  for (int c = 0; c < 8; ++c)
+    *reinterpret_cast<float4*>(rowp + ((c ^ (r & 7)) << 4)) =
+        make_float4(v[4 * c], v[4 * c + 1], v[4 * c + 2], v[4 * c + 3]);
+}
+
+// Number of 32x32 output tiles the epilogue of each kind stores per chunk.
+template <int EPI>
+struct EpiOut {
+  static constexpr int N = EPI == EPI_GATEUP_SWIGLU ? 3 : (EPI == EPI_FC1_GELU || EPI == EPI_DGRAD_SWIGLU) ? 2 : 1;
+};
+
+// Epilogue of one thread's row for output columns [col, col+32): fused math
+// on the accumulator values v (and u, the second half, for the paired
+// layouts), results written into the warp's staging tiles (row r).  Inputs
+// outside the matrix read as zero; the TMA store clips the outputs.
+template <int EPI>
+__device__ __forceinline__ void epi_stage(const EpiParams& ep, int col, const float* v, const float* u,
+                                          const EpiIn& in, uint8_t* st, int r) {
+  typedef __nv_bfloat16 T;
+  const int ncols = ep.N - col;  // valid columns of this chunk (may exceed 32)
   float o[32];
   if (EPI == EPI_GATEUP_SWIGLU) {
-    T* gu = static_cast<T*>(ep.out0) + r * ep.ld_out0 + col;
-    store32_bf16(gu, v);
-    store32_bf16(gu + ep.pair_off, u);
+    stage_row_bf16(st, r, v);
+    stage_row_bf16(st + 2048, r, u);
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = silu_f(v[i]) * u[i];
-    store32_bf16(static_cast<T*>(ep.out1) + r * ep.ld_out1 + col, o);
+    stage_row_bf16(st + 4096, r, o);
   } else if (EPI == EPI_FC1_GELU) {
     float b[32];
-    load32_bf16(static_cast<const T*>(ep.vec) + col, b);
+    load32_bf16_guard(static_cast<const T*>(ep.vec) + col, ncols, b);
 #pragma unroll
     for (int i = 0; i < 32; ++i) b[i] += v[i];
-    store32_bf16(static_cast<T*>(ep.out0) + r * ep.ld_out0 + col, b);
+    stage_row_bf16(st, r, b);
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = gelu_f(b[i]);
-    store32_bf16(static_cast<T*>(ep.out1) + r * ep.ld_out1 + col, o);
+    stage_row_bf16(st + 2048, r, o);
   } else if (EPI == EPI_DOWN_RESID) {
     float x[32], b[32];
-    load32_bf16(static_cast<const T*>(ep.in0) + r * ep.ld_in0 + col, x);
-    load32_bf16(static_cast<const T*>(ep.vec) + col, b);
+    unpack32(in.a, x);
+    load32_bf16_guard(static_cast<const T*>(ep.vec) + col, ncols, b);
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = x[i] + v[i] + b[i];
-    store32_bf16(static_cast<T*>(ep.out0) + r * ep.ld_out0 + col, o);
+    stage_row_bf16(st, r, o);
   } else if (EPI == EPI_DGRAD_SWIGLU) {
     float g[32], uu[32];
-    const T* gu = static_cast<const T*>(ep.in0) + r * ep.ld_in0 + col;
-    load32_bf16(gu, g);
-    load32_bf16(gu + ep.pair_off, uu);
+    unpack32(in.a, g);
+    unpack32(in.b, uu);
 #pragma unroll
     for (int i = 0; i < 32; ++i) swiglu_bwd(v[i], g[i], uu[i], o[i], uu[i]);
-    T* d = static_cast<T*>(ep.out0) + r * ep.ld_out0 + col;
-    store32_bf16(d, o);
-    store32_bf16(d + ep.pair_off, uu);
+    stage_row_bf16(st, r, o);
+    stage_row_bf16(st + 2048, r, uu);
   } else if (EPI == EPI_DGRAD_GELU) {
     float z[32];
-    load32_bf16(static_cast<const T*>(ep.in0) + r * ep.ld_in0 + col, z);
+    unpack32(in.a, z);
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = v[i] * gelu_grad_f(z[i]);
-    store32_bf16(static_cast<T*>(ep.out0) + r * ep.ld_out0 + col, o);
+    stage_row_bf16(st, r, o);
   } else {
-    float4* d = reinterpret_cast<float4*>(static_cast<float*>(ep.out0) + r * ep.ld_out0 + col);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) d[i] = make_float4(v[4 * i], v[4 * i + 1], v[4 * i + 2], v[4 * i + 3]);
+    stage_row_f32(st, r, v);
   }
 }
 
 template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
-                   const TcParams p) {
+                   const __grid_constant__ CUtensorMap map_o0, const __grid_constant__ CUtensorMap map_o1,
+                   const __grid_constant__ CUtensorMap map_o2, const TcParams p) {
   using C = TileCfg<PAIR>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
@@ -209,6 +265,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sA = smem;
   uint8_t* sB = smem + C::STAGES * C::A_BYTES;
+  uint8_t* sE = smem + C::STAGES * C::STAGE_BYTES;  // epilogue staging
   volatile int* abort_flag = &abort_sh;
 
   const int warp = threadIdx.x >> 5;
@@ -342,43 +399,49 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
     }
   } else if (warp == 1) {
-    if (lane == 0 && leader) {
+    if (leader) {
       // ------------------------------------------------------------ MMA issuer
+      // The whole warp runs this loop in warp-uniform control flow (waits are
+      // folded with __all_sync) and one elected lane issues the MMAs: that
+      // keeps the descriptors in uniform registers and the issue cost of a
+      // tcgen05.mma well below the 128 cycles it keeps the tensor core busy.
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
-      bool ok = !*abort_flag;
+      int ok = !*abort_flag;
       for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
-        if (!mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
-          ok = false;
-          break;
-        }
+        ok = __all_sync(0xffffffffu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status,
+                                               STATUS_TIMEOUT, WAIT_LIMIT_NS));
+        if (!ok) break;
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         uint32_t accumulate = 0;
         for (int seg = 0; ok && seg < 2; ++seg) {
           for (int kb = p.kb[2 * seg]; kb < p.kb[2 * seg + 1]; ++kb) {
-            if (!mbar_wait(&full_bar[stage], phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
-              ok = false;
-              break;
-            }
+            ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, abort_flag, p.status, STATUS_TIMEOUT,
+                                                   WAIT_LIMIT_NS));
+            if (!ok) break;
             tc_fence_after();
             const uint32_t a_base = smem_u32(sA + stage * C::A_BYTES);
             const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
+            if (elect_one()) {
 #pragma unroll
-            for (int k = 0; k < BK / UMMA_K; ++k) {
-              const uint64_t a_desc =
-                  A_MN ? sw128_desc(a_base + k * 2048, 8192, 1024) : sw128_desc(a_base + k * 32, 16, 1024);
-              const uint64_t b_desc =
-                  B_MN ? sw128_desc(b_base + k * 2048, 8192, 1024) : sw128_desc(b_base + k * 32, 16, 1024);
+              for (int k = 0; k < BK / UMMA_K; ++k) {
+                const uint64_t a_desc =
+                    A_MN ? sw128_desc(a_base + k * 2048, 8192, 1024) : sw128_desc(a_base + k * 32, 16, 1024);
+                const uint64_t b_desc =
+                    B_MN ? sw128_desc(b_base + k * 2048, 8192, 1024) : sw128_desc(b_base + k * 32, 16, 1024);
+                if (PAIR)
+                  tc_mma_f16_pair(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
+                else
+                  tc_mma_f16(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
+              }
+              // Free the stage for the producers once these MMAs complete.
               if (PAIR)
-                tc_mma_f16_pair(d_tmem, a_desc, b_desc, IDESC, accumulate);
+                tc_commit_pair(&empty_bar[stage], 0x3);
               else
-                tc_mma_f16(d_tmem, a_desc, b_desc, IDESC, accumulate);
-              accumulate = 1;
+                tc_commit(&empty_bar[stage]);
             }
-            if (PAIR)
-              tc_commit_pair(&empty_bar[stage], 0x3);
-            else
-              tc_commit(&empty_bar[stage]);
+            __syncwarp();
+            accumulate = 1;
             if (++stage == C::STAGES) {
               stage = 0;
               phase ^= 1u;
@@ -386,18 +449,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           }
         }
         if (!ok) break;
-        if (PAIR)
-          tc_commit_pair(&tfull_bar[acc], 0x3);
-        else
-          tc_commit(&tfull_bar[acc]);
+        if (elect_one()) {
+          if (PAIR)
+            tc_commit_pair(&tfull_bar[acc], 0x3);
+          else
+            tc_commit(&tfull_bar[acc]);
+        }
+        __syncwarp();
         acc ^= 1u;
         if (acc == 0) acc_phase ^= 1u;
       }
       // No MMA may still be running when tensor memory is released.
-      if (PAIR)
-        tc_commit_pair(&drain_bar, 0x3);
-      else
-        tc_commit(&drain_bar);
+      if (elect_one()) {
+        if (PAIR)
+          tc_commit_pair(&drain_bar, 0x3);
+        else
+          tc_commit(&drain_bar);
+      }
+      __syncwarp();
       int no_abort = 0;
       mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, DRAIN_LIMIT_NS);
     } else if (lane == 0 && PAIR) {
@@ -409,32 +478,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
+    uint8_t* st = sE + (warp - 2) * C::EPI_WARP_BYTES;
     uint32_t acc = 0, acc_phase = 0;
     for (int tile = worker; tile < p.num_tiles; tile += num_workers) {
+      int mb, nb;
+      tile_coords(p, tile, mb, nb);
+      const int row0 = mb * C::TILE_M + (int)rank * BM + q * 32;  // first row of this warp
+      const int row = row0 + lane;
+      constexpr int CHUNKS = EPI == EPI_GATEUP_SWIGLU ? BN / 2 / 32 : BN / 32;
+      const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
+      // The first chunk's inputs are fetched while the tile's main loop runs;
+      // each later chunk's while the previous one is computed.
+      EpiIn cur, nxt;
+      epi_load<EPI>(p.ep, row, col_base, cur);
       int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      int mb, nb;
-      tile_coords(p, tile, mb, nb);
-      const int row = mb * C::TILE_M + (int)rank * BM + q * 32 + lane;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       uint32_t r0[32], r1[32];
-      if (EPI == EPI_GATEUP_SWIGLU) {
 #pragma unroll 1
-        for (int c = 0; c < BN / 2 / 32; ++c) {
-          tmem_ld_32x32b_x32(tbase + c * 32, r0);
-          tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, r1);
-          tmem_ld_wait();
-          epi_chunk<EPI>(p.ep, row, nb * (BN / 2) + c * 32, reinterpret_cast<const float*>(r0),
-                         reinterpret_cast<const float*>(r1));
-        }
-      } else {
-#pragma unroll 1
-        for (int c = 0; c < BN / 32; ++c) {
-          tmem_ld_32x32b_x32(tbase + c * 32, r0);
-          tmem_ld_wait();
-          epi_chunk<EPI>(p.ep, row, nb * BN + c * 32, reinterpret_cast<const float*>(r0), nullptr);
+      for (int c = 0; c < CHUNKS; ++c) {
+        const int col = col_base + c * 32;
+        if (c + 1 < CHUNKS) epi_load<EPI>(p.ep, row, col + 32, nxt);
+        tmem_ld_32x32b_x32(tbase + c * 32, r0);
+        if (EPI == EPI_GATEUP_SWIGLU) tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, r1);
+        // The staging tiles are reused chunk after chunk: the previous
+        // chunk's stores must have read them.
+        if (lane == 0) bulk_wait_read_all();
+        __syncwarp();
+        tmem_ld_wait();
+        epi_stage<EPI>(p.ep, col, reinterpret_cast<const float*>(r0), reinterpret_cast<const float*>(r1), cur, st,
+                       lane);
+        cur = nxt;
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0 && col < p.N && row0 < p.M) {
+          tma_store_2d(&map_o0, st, col, row0);
+          if (EpiOut<EPI>::N > 1) tma_store_2d(&map_o1, st + 2048, col, row0);
+          if (EpiOut<EPI>::N > 2) tma_store_2d(&map_o2, st + 4096, col, row0);
+          bulk_commit_group();
         }
       }
       tc_fence_before();
@@ -448,6 +531,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
     }
+    if (lane == 0) bulk_wait_all();  // the stores complete before the CTA may exit
+    __syncwarp();
   }
 
   tc_fence_before();
@@ -483,24 +568,39 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor [outer, inner] with row pitch `ld` elements; box of
-// 64 (one 128-byte swizzle row) x box_outer.
-bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
+// 2-D tensor [outer, inner] with row pitch `ld` elements.
+bool encode_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t inner, uint64_t outer, uint64_t ld,
+                uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
+  const uint64_t esz = f32 ? 4 : 2;
   cuuint64_t dims[2] = {inner, outer};
-  cuuint64_t strides[1] = {ld * 2};
-  cuuint32_t box[2] = {64, box_outer};
+  cuuint64_t strides[1] = {ld * esz};
+  cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+                   const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
 }
 
+// bf16 operand: boxes of 64 (one 128-byte swizzle row) x box_outer.
+bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
+  return encode_map(m, ptr, false, inner, outer, ld, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// Epilogue output [rows, cols] (pitch ld): 32x32 boxes, 64-byte swizzle for
+// bf16 rows, 128-byte swizzle for f32 rows (the staging-tile layouts).
+bool make_out_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t cols, uint64_t rows, uint64_t ld) {
+  return encode_map(m, ptr, f32, cols, rows, ld, 32, 32, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+}
+
+struct Maps {
+  CUtensorMap a, b, o[3];
+};
+
 template <bool PAIR, bool A_MN, bool B_MN, int EPI>
-cudaError_t launch_inst(const CUtensorMap& ma, const CUtensorMap& mb, const TcParams& p, int num_sms,
-                        cudaStream_t st) {
+cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStream_t st) {
   using C = TileCfg<PAIR>;
   auto kfn = gemm_tc_kernel<PAIR, A_MN, B_MN, EPI>;
   static std::once_flag once;
@@ -530,7 +630,7 @@ cudaError_t launch_inst(const CUtensorMap& ma, const CUtensorMap& mb, const TcPa
   if (max_workers <= 0) return cudaErrorInvalidConfiguration;
   const int workers = p.num_tiles < max_workers ? p.num_tiles : max_workers;
   if (!PAIR) {
-    kfn<<<workers, NUM_THREADS, C::SMEM_BYTES, st>>>(ma, mb, p);
+    kfn<<<workers, NUM_THREADS, C::SMEM_BYTES, st>>>(mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -545,7 +645,7 @@ cudaError_t launch_inst(const CUtensorMap& ma, const CUtensorMap& mb, const TcPa
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kfn, ma, mb, p);
+  return cudaLaunchKernelEx(&cfg, kfn, mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], p);
 }
 
 template <bool PAIR>
@@ -581,36 +681,66 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
 
   // Box heights: K-major A = this CTA's 128 rows; K-major B = 128 rows per
   // box; MN-major operands move in 64 (MN) x 64 (K) boxes.
-  CUtensorMap ma, mb;
+  Maps mp;
   bool ok;
   if (!g.a_mn)
-    ok = make_map(&ma, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
+    ok = make_map(&mp.a, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
   else
-    ok = make_map(&ma, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, 64);
+    ok = make_map(&mp.a, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, 64);
   if (!ok) return cudaErrorInvalidValue;
   if (!g.b_mn)
-    ok = make_map(&mb, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
+    ok = make_map(&mp.b, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
   else
-    ok = make_map(&mb, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, 64);
+    ok = make_map(&mp.b, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, 64);
+  if (!ok) return cudaErrorInvalidValue;
+  // Output maps; the paired layouts get one map per half so that stores clip
+  // at the half's last channel (F) rather than at 2F.
+  const uint64_t M = (uint64_t)g.M, N = (uint64_t)g.N;
+  const EpiParams& e = g.ep;
+  const __nv_bfloat16* o0 = static_cast<const __nv_bfloat16*>(e.out0);
+  switch (g.epi) {
+    case EPI_GATEUP_SWIGLU:
+      ok = make_out_map(&mp.o[0], o0, false, N, M, e.ld_out0) &&
+           make_out_map(&mp.o[1], o0 + e.pair_off, false, N, M, e.ld_out0) &&
+           make_out_map(&mp.o[2], e.out1, false, N, M, e.ld_out1);
+      break;
+    case EPI_FC1_GELU:
+      ok = make_out_map(&mp.o[0], o0, false, N, M, e.ld_out0) && make_out_map(&mp.o[1], e.out1, false, N, M, e.ld_out1);
+      mp.o[2] = mp.o[1];
+      break;
+    case EPI_DGRAD_SWIGLU:
+      ok = make_out_map(&mp.o[0], o0, false, N, M, e.ld_out0) &&
+           make_out_map(&mp.o[1], o0 + e.pair_off, false, N, M, e.ld_out0);
+      mp.o[2] = mp.o[1];
+      break;
+    case EPI_STORE_F32:
+      ok = make_out_map(&mp.o[0], e.out0, true, N, M, e.ld_out0);
+      mp.o[1] = mp.o[2] = mp.o[0];
+      break;
+    default:  // DOWN_RESID, DGRAD_GELU
+      ok = make_out_map(&mp.o[0], o0, false, N, M, e.ld_out0);
+      mp.o[1] = mp.o[2] = mp.o[0];
+      break;
+  }
   if (!ok) return cudaErrorInvalidValue;
 
   const int key = (g.a_mn ? 100 : 0) + (g.b_mn ? 10 : 0) + g.epi;
   switch (key) {
     case 0 + EPI_GATEUP_SWIGLU:
       if (!g.paired) return cudaErrorInvalidValue;
-      return launch_inst<PAIR, false, false, EPI_GATEUP_SWIGLU>(ma, mb, p, num_sms, st);
+      return launch_inst<PAIR, false, false, EPI_GATEUP_SWIGLU>(mp, p, num_sms, st);
     case 0 + EPI_FC1_GELU:
-      return launch_inst<PAIR, false, false, EPI_FC1_GELU>(ma, mb, p, num_sms, st);
+      return launch_inst<PAIR, false, false, EPI_FC1_GELU>(mp, p, num_sms, st);
     case 0 + EPI_DOWN_RESID:
-      return launch_inst<PAIR, false, false, EPI_DOWN_RESID>(ma, mb, p, num_sms, st);
+      return launch_inst<PAIR, false, false, EPI_DOWN_RESID>(mp, p, num_sms, st);
     case 10 + EPI_DGRAD_SWIGLU:
-      return launch_inst<PAIR, false, true, EPI_DGRAD_SWIGLU>(ma, mb, p, num_sms, st);
+      return launch_inst<PAIR, false, true, EPI_DGRAD_SWIGLU>(mp, p, num_sms, st);
     case 10 + EPI_DGRAD_GELU:
-      return launch_inst<PAIR, false, true, EPI_DGRAD_GELU>(ma, mb, p, num_sms, st);
+      return launch_inst<PAIR, false, true, EPI_DGRAD_GELU>(mp, p, num_sms, st);
     case 110 + EPI_STORE_F32:
-      return launch_inst<PAIR, true, true, EPI_STORE_F32>(ma, mb, p, num_sms, st);
+      return launch_inst<PAIR, true, true, EPI_STORE_F32>(mp, p, num_sms, st);
     case 10 + EPI_STORE_F32:
-      return launch_inst<PAIR, false, true, EPI_STORE_F32>(ma, mb, p, num_sms, st);
+      return launch_inst<PAIR, false, true, EPI_STORE_F32>(mp, p, num_sms, st);
     default:
       return cudaErrorNotSupported;
   }

@@ -234,13 +234,28 @@ cudaError_t rmsnorm_bwd_t(const float* dnrm, const T* x, const float* rstd, cons
 }
 
 // ------------------------------------------------------------- column sums
-__global__ void colsum_finalize_kernel(const float* __restrict__ part, int nparts, float* __restrict__ out,
-                                       int64_t C) {
-  const int64_t c = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
-  if (c >= C) return;
+// out[c] = sum_p part[p][c] for up to two (part, out) pairs (blockIdx.y).
+// A block covers 32 columns; its 8 warps each sum a strided subset of the
+// partial rows, then the 8 warp sums are added in warp order (deterministic).
+__global__ void __launch_bounds__(256) colsum_finalize_kernel(const float* __restrict__ part0, float* __restrict__ out0,
+                                                              const float* __restrict__ part1, float* __restrict__ out1,
+                                                              int nparts, int64_t C) {
+  __shared__ float red[8][33];
+  const float* part = blockIdx.y ? part1 : part0;
+  float* out = blockIdx.y ? out1 : out0;
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  const int64_t c = (int64_t)blockIdx.x * 32 + lane;
   float s = 0.0f;
-  for (int p = 0; p < nparts; ++p) s += part[(int64_t)p * C + c];
-  out[c] = s;
+  if (c < C)
+    for (int p = wid; p < nparts; p += 8) s += part[(int64_t)p * C + c];
+  red[wid][lane] = s;
+  __syncthreads();
+  if (wid == 0 && c < C) {
+    float t = 0.0f;
+#pragma unroll
+    for (int k = 0; k < 8; ++k) t += red[k][lane];
+    out[c] = t;
+  }
 }
 
 // Block (x, y): columns [1024 x, 1024 x + 1024) (4 per thread), rows of chunk y.
@@ -366,9 +381,11 @@ cudaError_t launch_rmsnorm_bwd(int dtype, const float* dnrm, const void* x, cons
                                       st);
 }
 
-cudaError_t launch_colsum_finalize(const float* part, int nparts, float* out, int64_t C, cudaStream_t st) {
+cudaError_t launch_colsum_finalize(const float* part0, float* out0, const float* part1, float* out1, int nparts,
+                                   int64_t C, cudaStream_t st) {
   if (C <= 0) return cudaSuccess;
-  colsum_finalize_kernel<<<(unsigned)((C + 255) / 256), 256, 0, st>>>(part, nparts, out, C);
+  dim3 grid((unsigned)((C + 31) / 32), part1 ? 2u : 1u);
+  colsum_finalize_kernel<<<grid, 256, 0, st>>>(part0, out0, part1, out1, nparts, C);
   return cudaGetLastError();
 }
 
@@ -393,7 +410,7 @@ cudaError_t launch_colsum_partials(int dtype, const void* in, int64_t ld, float*
 
 int loss_blocks(int64_t n, int num_sms) {
   int64_t b = (n / 8 + 255) / 256;
-  if (b > 2LL * num_sms) b = 2LL * num_sms;
+  if (b > 6LL * num_sms) b = 6LL * num_sms;
   if (b > 1024) b = 1024;
   return (int)(b < 1 ? 1 : b);
 }

@@ -10,7 +10,7 @@
 //   backward: gemm_dgrad_act (g backward is the identity) -> gemm_wgrad_down
 //             -> gemm_wgrad_gateup -> gemm_dgrad_norm_reduce (the f
 //             all-reduce, "Put the other collective in backward") ->
-//             rmsnorm_bwd_residual -> colsum_finalize (x2)
+//             rmsnorm_bwd_residual -> colsum_finalize
 //   sgd     : sgd_update
 #include <cuda_runtime.h>
 
@@ -509,7 +509,7 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
     const int nb = colsum_blocks(N, c->num_sms);
     float* part = c->wsp<float>(c->L.part_b1);
     TPMLP_TRY(c->run(K_COLSUM_B1, [&] { return launch_colsum_partials(dt, dgu, F, part, N, F, nb, c->stream); }));
-    TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(part, nb, db_1, F, c->stream); }));
+    TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(part, db_1, nullptr, nullptr, nb, F, c->stream); }));
   }
 
   // dN = sum over shards of dGU_s W_gu,s -- the f all-reduce, summed on chip.
@@ -543,8 +543,7 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
     return launch_rmsnorm_bwd(dt, dnrm, c->x, c->wsp<float>(c->L.rstd), c->norm_w, dy, dx, pdw, pdb, N, H, nb,
                               c->stream);
   }));
-  TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(pdw, nb, dnorm_w, H, c->stream); }));
-  TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(pdb, nb, db_down, H, c->stream); }));
+  TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(pdw, dnorm_w, pdb, db_down, nb, H, c->stream); }));
   c->bwd_done = true;
   return TPMLP_OK;
 }

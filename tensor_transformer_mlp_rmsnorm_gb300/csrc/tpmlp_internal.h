@@ -56,7 +56,9 @@ int rmsnorm_bwd_blocks(int64_t N, int num_sms);
 cudaError_t launch_rmsnorm_bwd(int dtype, const float* dnrm, const void* x, const float* rstd, const void* w,
                                const void* dy, void* dx, float* part_dw, float* part_db, int64_t N, int64_t H,
                                int nblocks, cudaStream_t st);
-cudaError_t launch_colsum_finalize(const float* part, int nparts, float* out, int64_t C, cudaStream_t st);
+// out0[c] = sum_p part0[p][c] (and the same for part1/out1 when part1 != nullptr).
+cudaError_t launch_colsum_finalize(const float* part0, float* out0, const float* part1, float* out1, int nparts,
+                                   int64_t C, cudaStream_t st);
 int colsum_blocks(int64_t N, int num_sms);
 cudaError_t launch_colsum_partials(int dtype, const void* in, int64_t ld, float* part, int64_t N, int64_t C,
                                    int nblocks, cudaStream_t st);
