@@ -81,6 +81,7 @@ struct TcParams {
   EpiParams ep;
   uint32_t* status;
   int force_timeout;
+  int a3d, b3d;  // MN-major operand loaded as one 3-D box per stage
 };
 
 __device__ __forceinline__ void tile_coords(const TcParams& p, int tile, int& mb, int& nb) {
@@ -350,12 +351,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);  // the leader's barrier
               if (!A_MN) {
                 tma_load_2d_pair(a_dst, &map_a, fb, k0, m0);
+              } else if (p.a3d) {
+                tma_load_3d_pair(a_dst, &map_a, fb, 0, k0, m0 >> 6);
               } else {
                 tma_load_2d_pair(a_dst, &map_a, fb, m0, k0);
                 tma_load_2d_pair(a_dst + 8192, &map_a, fb, m0 + 64, k0);
               }
               if (!B_MN) {
                 tma_load_2d_pair(b_dst, &map_b, fb, k0, brow0);
+              } else if (p.b3d) {
+                tma_load_3d_pair(b_dst, &map_b, fb, 0, k0, brow0 >> 6);
               } else {
                 tma_load_2d_pair(b_dst, &map_b, fb, brow0, k0);
                 tma_load_2d_pair(b_dst + 8192, &map_b, fb, brow0 + 64, k0);
@@ -363,6 +368,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
               if (!A_MN) {
                 tma_load_2d(a_dst, &map_a, &full_bar[stage], k0, m0);
+              } else if (p.a3d) {
+                tma_load_3d(a_dst, &map_a, &full_bar[stage], 0, k0, m0 >> 6);
               } else {
                 tma_load_2d(a_dst, &map_a, &full_bar[stage], m0, k0);
                 tma_load_2d(a_dst + 8192, &map_a, &full_bar[stage], m0 + 64, k0);
@@ -370,6 +377,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               if (!B_MN) {
                 tma_load_2d(b_dst, &map_b, &full_bar[stage], k0, brow0);
                 tma_load_2d(b_dst + C::B_BYTES / 2, &map_b, &full_bar[stage], k0, brow1);
+              } else if (p.b3d) {
+                tma_load_3d(b_dst, &map_b, &full_bar[stage], 0, k0, brow0 >> 6);
               } else {
 #pragma unroll
                 for (int j = 0; j < 4; ++j)
@@ -589,6 +598,23 @@ bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, u
   return encode_map(m, ptr, false, inner, outer, ld, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+// MN-major bf16 operand [k_extent, mn] (pitch ld, mn a multiple of 64) as a
+// 3-D tensor {64, k_extent, mn / 64}: one box of `chunks` 64-element MN
+// chunks x 64 K rows lands in shared memory exactly as `chunks` 2-D boxes
+// placed 8 KB apart would.
+bool make_mn_map3(CUtensorMap* m, const void* ptr, uint64_t mn, uint64_t k_extent, uint64_t ld, uint32_t chunks) {
+  EncodeTiledFn enc = get_encode_fn();
+  if (!enc || mn % 64 != 0) return false;
+  cuuint64_t dims[3] = {64, k_extent, mn / 64};
+  cuuint64_t strides[2] = {ld * 2, 128};
+  cuuint32_t box[3] = {64, 64, chunks};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides, box, estr,
+                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // Epilogue output [rows, cols] (pitch ld): 32x32 boxes, 64-byte swizzle for
 // bf16 rows, 128-byte swizzle for f32 rows (the staging-tile layouts).
 bool make_out_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t cols, uint64_t rows, uint64_t ld) {
@@ -681,15 +707,23 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
 
   // Box heights: K-major A = this CTA's 128 rows; K-major B = 128 rows per
   // box; MN-major operands move in 64 (MN) x 64 (K) boxes.
+  // MN-major operands whose MN extent is a multiple of 64 move as one 3-D box
+  // per stage (fewer TMA instructions); otherwise as 64x64 2-D boxes.
   Maps mp;
   bool ok;
+  p.a3d = g.a_mn && g.M % 64 == 0;
+  p.b3d = g.b_mn && g.N % 64 == 0;
   if (!g.a_mn)
     ok = make_map(&mp.a, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
+  else if (p.a3d)
+    ok = make_mn_map3(&mp.a, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, BM / 64);
   else
     ok = make_map(&mp.a, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, 64);
   if (!ok) return cudaErrorInvalidValue;
   if (!g.b_mn)
     ok = make_map(&mp.b, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
+  else if (p.b3d)
+    ok = make_mn_map3(&mp.b, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, C::B_ROWS / 64);
   else
     ok = make_map(&mp.b, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, 64);
   if (!ok) return cudaErrorInvalidValue;
