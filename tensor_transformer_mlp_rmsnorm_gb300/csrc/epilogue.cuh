@@ -62,6 +62,17 @@ __device__ __forceinline__ void swiglu_bwd(float da, float g, float u, float& dg
   du = da * g * s;
 }
 
+// Fast variants for the bf16 tensor-core epilogues, whose results are stored
+// in bf16 (relative rounding 2^-9): __expf and an approximate reciprocal are
+// far inside that.  The fp32 path keeps expf and IEEE division.
+__device__ __forceinline__ float sigmoid_fast(float z) { return __frcp_rn(1.0f + __expf(-z)); }
+__device__ __forceinline__ float silu_fast(float z) { return z * sigmoid_fast(z); }
+__device__ __forceinline__ void swiglu_bwd_fast(float da, float g, float u, float& dg, float& du) {
+  const float s = sigmoid_fast(g);
+  dg = da * u * s * (1.0f + g * (1.0f - s));
+  du = da * g * s;
+}
+
 // One output element (m, n) -- used by the SIMT path and by ragged chunks of
 // the tensor-core path.  For GATEUP_SWIGLU, `acc` is G and `acc2` is U of
 // channel n.

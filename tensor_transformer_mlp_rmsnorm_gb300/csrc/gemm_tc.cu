@@ -56,16 +56,28 @@ constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s for draining after 
 constexpr uint64_t PEER_DRAIN_NS = 5000000ull;      // 5 ms: a CTA-pair peer's loads land long before this
 constexpr uint64_t FORCED_LIMIT_NS = 2000000ull;    // 2 ms for the forced-timeout debug wait
 
-template <bool PAIR>
+// Epilogues that read global inputs (the residual x, or G and U, or Z) bring
+// them into shared memory with TMA as well.
+template <int EPI>
+__host__ __device__ constexpr bool epi_has_in() {
+  return EPI == EPI_DOWN_RESID || EPI == EPI_DGRAD_SWIGLU || EPI == EPI_DGRAD_GELU;
+}
+
+template <bool PAIR, bool HAS_IN>
 struct TileCfg {
-  static constexpr int STAGES = PAIR ? 6 : 4;
+  // Operand ring depth: the staging of epilogue inputs takes one stage's room.
+  static constexpr int STAGES = PAIR ? (HAS_IN ? 5 : 6) : (HAS_IN ? 3 : 4);
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns held by this CTA per stage
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
   static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-  // Epilogue staging: per epilogue warp up to three 32x32 bf16 tiles (or one
-  // 32x32 f32 tile), each 2 KB and 1024-byte aligned.
-  static constexpr int EPI_WARP_BYTES = 6144;
+  // Epilogue staging per epilogue warp: outputs in two 4 KB buffers used
+  // alternately (each up to two 32x32 bf16 tiles or one 32x32 f32 tile) or,
+  // for the three-output gate/up epilogue, one 6 KB buffer; inputs in two
+  // 4 KB buffers (up to two 32x32 bf16 tiles each).
+  static constexpr int EPI_OUT_BYTES = 8192;
+  static constexpr int EPI_IN_BYTES = HAS_IN ? 8192 : 0;
+  static constexpr int EPI_WARP_BYTES = EPI_OUT_BYTES + EPI_IN_BYTES;
   static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_WARP_BYTES + 1024;  // + alignment
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // output rows per tile (per pair)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;
@@ -159,15 +171,11 @@ __device__ __forceinline__ void load32_bf16_guard(const __nv_bfloat16* src, int 
   unpack32(v, f);
 }
 
-// The per-row global inputs of chunk [col, col+32) (x, or G and U, or Z).
-template <int EPI>
-__device__ __forceinline__ void epi_load(const EpiParams& ep, int row, int col, EpiIn& in) {
-  typedef __nv_bfloat16 T;
-  if (EPI != EPI_DOWN_RESID && EPI != EPI_DGRAD_SWIGLU && EPI != EPI_DGRAD_GELU) return;
-  const int nvalid = (row < ep.M && col < ep.N) ? ep.N - col : 0;
-  const T* base = static_cast<const T*>(ep.in0) + (int64_t)(row < ep.M ? row : 0) * ep.ld_in0 + col;
-  load32_raw(base, nvalid, in.a);
-  if (EPI == EPI_DGRAD_SWIGLU) load32_raw(base + ep.pair_off, nvalid, in.b);
+// Row r of a 32x32 bf16 input tile loaded by TMA with the 64-byte swizzle.
+__device__ __forceinline__ void read_row_bf16(const uint8_t* tile, int r, uint4 (&o)[4]) {
+  const uint8_t* rowp = tile + r * 64;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) o[c] = *reinterpret_cast<const uint4*>(rowp + ((c ^ ((r >> 1) & 3)) << 4));
 }
 
 // Row r of a 32x32 staging tile in the layout the TMA store expects:
@@ -194,6 +202,7 @@ __device__ __forceinline__ void stage_row_f32(uint8_t* tile, int r, const float*
 template <int EPI>
 struct EpiOut {
   static constexpr int N = EPI == EPI_GATEUP_SWIGLU ? 3 : (EPI == EPI_FC1_GELU || EPI == EPI_DGRAD_SWIGLU) ? 2 : 1;
+  static constexpr int NBUF = N == 3 ? 1 : 2;  // staging buffers per warp
 };
 
 // Epilogue of one thread's row for output columns [col, col+32): fused math
@@ -210,7 +219,7 @@ __device__ __forceinline__ void epi_stage(const EpiParams& ep, int col, const fl
     stage_row_bf16(st, r, v);
     stage_row_bf16(st + 2048, r, u);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] = silu_f(v[i]) * u[i];
+    for (int i = 0; i < 32; ++i) o[i] = silu_fast(v[i]) * u[i];
     stage_row_bf16(st + 4096, r, o);
   } else if (EPI == EPI_FC1_GELU) {
     float b[32];
@@ -233,7 +242,7 @@ __device__ __forceinline__ void epi_stage(const EpiParams& ep, int col, const fl
     unpack32(in.a, g);
     unpack32(in.b, uu);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) swiglu_bwd(v[i], g[i], uu[i], o[i], uu[i]);
+    for (int i = 0; i < 32; ++i) swiglu_bwd_fast(v[i], g[i], uu[i], o[i], uu[i]);
     stage_row_bf16(st, r, o);
     stage_row_bf16(st + 2048, r, uu);
   } else if (EPI == EPI_DGRAD_GELU) {
@@ -251,8 +260,10 @@ template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_o0, const __grid_constant__ CUtensorMap map_o1,
-                   const __grid_constant__ CUtensorMap map_o2, const TcParams p) {
-  using C = TileCfg<PAIR>;
+                   const __grid_constant__ CUtensorMap map_o2, const __grid_constant__ CUtensorMap map_i0,
+                   const __grid_constant__ CUtensorMap map_i1, const TcParams p) {
+  constexpr bool HAS_IN = epi_has_in<EPI>();
+  using C = TileCfg<PAIR, HAS_IN>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
   __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
@@ -260,6 +271,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t never_bar;
+  __shared__ __align__(8) uint64_t in_bar[4][2];  // epilogue input tiles, per warp and buffer
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -288,12 +300,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(&drain_bar, 1);
     mbar_init(&never_bar, 1);
+    for (int w = 0; w < 4; ++w)
+      for (int b = 0; b < 2; ++b) mbar_init(&in_bar[w][b], 1);
     abort_sh = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
     tma_prefetch_desc(&map_a);
     tma_prefetch_desc(&map_b);
+    tma_prefetch_desc(&map_o0);
+    if (HAS_IN) tma_prefetch_desc(&map_i0);
   }
   if (warp == 1) {
     if (PAIR) {
@@ -487,19 +503,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   } else {
     // -------------------------------------------------------------- epilogue
     const int q = warp & 3;  // TMEM lane quarter this warp may access
-    uint8_t* st = sE + (warp - 2) * C::EPI_WARP_BYTES;
-    uint32_t acc = 0, acc_phase = 0;
+    const int ew = warp - 2;
+    uint8_t* st = sE + ew * C::EPI_WARP_BYTES;  // output staging
+    uint8_t* si = st + C::EPI_OUT_BYTES;        // input staging
+    constexpr uint32_t IN_BYTES = EPI == EPI_DGRAD_SWIGLU ? 4096u : 2048u;
+    uint32_t acc = 0, acc_phase = 0, n_stored = 0;
+    uint32_t n_in = 0, n_used = 0, in_par = 0;  // input tiles issued / consumed, parity per buffer
+    // Input tiles of chunk [col, col+32) of this warp's 32 rows -> buffer n_in & 1.
+    auto issue_in = [&](int col, int row0) {
+      if (!HAS_IN) return;
+      const uint32_t b = n_in & 1u;
+      if (lane == 0) {
+        mbar_arrive_expect_tx(&in_bar[ew][b], IN_BYTES);
+        tma_load_2d(si + b * 4096, &map_i0, &in_bar[ew][b], col, row0);
+        if (EPI == EPI_DGRAD_SWIGLU) tma_load_2d(si + b * 4096 + 2048, &map_i1, &in_bar[ew][b], col, row0);
+      }
+      ++n_in;
+    };
     for (int tile = worker; tile < p.num_tiles; tile += num_workers) {
       int mb, nb;
       tile_coords(p, tile, mb, nb);
       const int row0 = mb * C::TILE_M + (int)rank * BM + q * 32;  // first row of this warp
-      const int row = row0 + lane;
       constexpr int CHUNKS = EPI == EPI_GATEUP_SWIGLU ? BN / 2 / 32 : BN / 32;
       const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
-      // The first chunk's inputs are fetched while the tile's main loop runs;
+      // The first chunk's inputs are fetched while the tile's main loop runs,
       // each later chunk's while the previous one is computed.
-      EpiIn cur, nxt;
-      epi_load<EPI>(p.ep, row, col_base, cur);
+      if (col_base < p.N && row0 < p.M) issue_in(col_base, row0);
       int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -509,26 +538,51 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll 1
       for (int c = 0; c < CHUNKS; ++c) {
         const int col = col_base + c * 32;
-        if (c + 1 < CHUNKS) epi_load<EPI>(p.ep, row, col + 32, nxt);
+        // Chunks wholly outside the output are skipped by the whole warp.
+        if (col >= p.N || row0 >= p.M) break;
+        if (c + 1 < CHUNKS && col + 32 < p.N) issue_in(col + 32, row0);
         tmem_ld_32x32b_x32(tbase + c * 32, r0);
         if (EPI == EPI_GATEUP_SWIGLU) tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, r1);
-        // The staging tiles are reused chunk after chunk: the previous
-        // chunk's stores must have read them.
-        if (lane == 0) bulk_wait_read_all();
-        __syncwarp();
+        EpiIn in;
+        if (HAS_IN) {
+          const uint32_t b = n_used & 1u;
+          int iok = mbar_wait(&in_bar[ew][b], (in_par >> b) & 1u, abort_flag, p.status, STATUS_TIMEOUT,
+                              WAIT_LIMIT_NS);
+          iok = __all_sync(0xffffffffu, iok);
+          if (!iok) {  // the load stays counted as in flight for the drain below
+            ok = 0;
+            break;
+          }
+          in_par ^= 1u << b;
+          ++n_used;
+          read_row_bf16(si + b * 4096, lane, in.a);
+          if (EPI == EPI_DGRAD_SWIGLU) read_row_bf16(si + b * 4096 + 2048, lane, in.b);
+        }
+        // Stores alternate between the two staging buffers (counting stored
+        // chunks, not chunk indices); a buffer is rewritten once the stores
+        // issued from it two chunks ago have read it.
+        uint8_t* sb = st + (EpiOut<EPI>::NBUF == 2 ? (n_stored & 1u) * 4096 : 0);
+        if (lane == 0) {
+          if (EpiOut<EPI>::NBUF == 2)
+            bulk_wait_read_but_last();
+          else
+            bulk_wait_read_all();
+        }
+        __syncwarp();  // also: every lane has read its input row before the buffer is refilled
         tmem_ld_wait();
-        epi_stage<EPI>(p.ep, col, reinterpret_cast<const float*>(r0), reinterpret_cast<const float*>(r1), cur, st,
+        epi_stage<EPI>(p.ep, col, reinterpret_cast<const float*>(r0), reinterpret_cast<const float*>(r1), in, sb,
                        lane);
-        cur = nxt;
         fence_proxy_async_smem();
         __syncwarp();
-        if (lane == 0 && col < p.N && row0 < p.M) {
-          tma_store_2d(&map_o0, st, col, row0);
-          if (EpiOut<EPI>::N > 1) tma_store_2d(&map_o1, st + 2048, col, row0);
-          if (EpiOut<EPI>::N > 2) tma_store_2d(&map_o2, st + 4096, col, row0);
+        if (lane == 0) {
+          tma_store_2d(&map_o0, sb, col, row0);
+          if (EpiOut<EPI>::N > 1) tma_store_2d(&map_o1, sb + 2048, col, row0);
+          if (EpiOut<EPI>::N > 2) tma_store_2d(&map_o2, sb + 4096, col, row0);
           bulk_commit_group();
         }
+        ++n_stored;
       }
+      if (!ok) break;
       tc_fence_before();
       __syncwarp();
       if (lane == 0) {
@@ -539,6 +593,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       acc ^= 1u;
       if (acc == 0) acc_phase ^= 1u;
+    }
+    // Input tiles still in flight (after an abort) land before the CTA may exit.
+    int no_abort = 0;
+    while (n_used < n_in) {
+      const uint32_t b = n_used & 1u;
+      mbar_wait(&in_bar[ew][b], (in_par >> b) & 1u, &no_abort, p.status, 0u, DRAIN_LIMIT_NS);
+      in_par ^= 1u << b;
+      ++n_used;
     }
     if (lane == 0) bulk_wait_all();  // the stores complete before the CTA may exit
     __syncwarp();
@@ -622,12 +684,12 @@ bool make_out_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t cols, uint
 }
 
 struct Maps {
-  CUtensorMap a, b, o[3];
+  CUtensorMap a, b, o[3], i[2];
 };
 
 template <bool PAIR, bool A_MN, bool B_MN, int EPI>
 cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStream_t st) {
-  using C = TileCfg<PAIR>;
+  using C = TileCfg<PAIR, epi_has_in<EPI>()>;
   auto kfn = gemm_tc_kernel<PAIR, A_MN, B_MN, EPI>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
@@ -656,7 +718,7 @@ cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStre
   if (max_workers <= 0) return cudaErrorInvalidConfiguration;
   const int workers = p.num_tiles < max_workers ? p.num_tiles : max_workers;
   if (!PAIR) {
-    kfn<<<workers, NUM_THREADS, C::SMEM_BYTES, st>>>(mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], p);
+    kfn<<<workers, NUM_THREADS, C::SMEM_BYTES, st>>>(mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], mp.i[0], mp.i[1], p);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -671,12 +733,12 @@ cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStre
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kfn, mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], p);
+  return cudaLaunchKernelEx(&cfg, kfn, mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], mp.i[0], mp.i[1], p);
 }
 
 template <bool PAIR>
 cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout) {
-  using C = TileCfg<PAIR>;
+  using C = TileCfg<PAIR, false>;  // tile shape only (the ring depth does not matter here)
   TcParams p{};
   p.M = g.M;
   p.N = g.N;
@@ -684,10 +746,15 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   p.num_n_blk = g.paired ? (g.N + BN / 2 - 1) / (BN / 2) : (g.N + BN - 1) / BN;
   p.num_tiles = p.num_m_blk * p.num_n_blk;
   // Tiles run in groups of group_m row blocks sweeping every column block, so
-  // a group's A rows (about 32 MB) stay in L2 while B streams past them.
+  // a group's A rows (about 32 MB) stay in L2 while B streams past them.  For
+  // long contractions, where that rule gives few rows, the group is at least
+  // sqrt(concurrent tiles) high: the tiles in flight then form a square and
+  // share the most operand blocks.
   const int64_t a_block_bytes = (int64_t)C::TILE_M * g.k_extent * 2;
   int gm = (int)((32ll << 20) / (a_block_bytes > 0 ? a_block_bytes : 1));
-  gm = gm < 4 ? 4 : (gm > 64 ? 64 : gm);
+  int gmin = 1;
+  while (gmin * gmin < (PAIR ? num_sms / 2 : num_sms)) ++gmin;
+  gm = gm < gmin ? gmin : (gm > 64 ? 64 : gm);
   p.group_m = p.num_m_blk < gm ? p.num_m_blk : gm;
   for (int s = 0; s < 2; ++s) {
     const int64_t k0 = g.kseg[2 * s], k1 = g.kseg[2 * s + 1];
@@ -756,6 +823,15 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
       mp.o[1] = mp.o[2] = mp.o[0];
       break;
   }
+  if (!ok) return cudaErrorInvalidValue;
+  // Epilogue inputs (same 32x32 box format as the outputs).
+  const __nv_bfloat16* i0 = static_cast<const __nv_bfloat16*>(e.in0);
+  mp.i[0] = mp.i[1] = mp.o[0];
+  if (g.epi == EPI_DOWN_RESID || g.epi == EPI_DGRAD_GELU)
+    ok = make_out_map(&mp.i[0], i0, false, N, M, e.ld_in0);
+  else if (g.epi == EPI_DGRAD_SWIGLU)
+    ok = make_out_map(&mp.i[0], i0, false, N, M, e.ld_in0) &&
+         make_out_map(&mp.i[1], i0 + e.pair_off, false, N, M, e.ld_in0);
   if (!ok) return cudaErrorInvalidValue;
 
   const int key = (g.a_mn ? 100 : 0) + (g.b_mn ? 10 : 0) + g.epi;

@@ -51,22 +51,37 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
   return ok != 0;
 }
 
+// As mbar_try_wait, but the thread may sleep up to `hint_ns` in the barrier
+// waiting for the phase (it is woken when the phase completes).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t hint_ns) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(smem_u32(bar)), "r"(parity), "r"(hint_ns)
+      : "memory");
+  return ok != 0;
+}
+
 // Bounded wait.  Returns true when the phase completed.  Gives up (returns
 // false) when *abort becomes non-zero, or after `limit_ns` of wall time, in
 // which case it raises *abort and ORs `code` into the device status word.
+// Waiting threads sleep in the barrier instead of spinning, so they leave
+// issue slots to the warps sharing their scheduler.
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, volatile int* abort,
                                           uint32_t* status, uint32_t code, uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = global_timer_ns();
-  for (uint32_t i = 1;; ++i) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((i & 31u) == 0) {
-      if (*abort) return false;
-      if (global_timer_ns() - t0 > limit_ns) {
-        *abort = 1;
-        atomicOr(status, code);
-        return false;
-      }
+  const uint32_t hint = (uint32_t)(limit_ns / 16 < 200000ull ? limit_ns / 16 : 200000ull);
+  for (;;) {
+    if (mbar_try_wait_sleep(bar, parity, hint)) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      atomicOr(status, code);
+      return false;
     }
   }
 }
@@ -127,6 +142,11 @@ __device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bul
 
 // Wait until the shared-memory sources of all committed bulk stores have been read.
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
+
+// ... of all but the most recently committed group.
+__device__ __forceinline__ void bulk_wait_read_but_last() {
+  asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
 
 // Wait until all committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }

@@ -51,6 +51,7 @@ BF16_SHAPES = [
     (300, 512, 1536, (1, 2, 4, 8)),   # 3 m-tiles (ragged), 2 n-tiles, shards of 192 channels
     (77, 328, 1000, (1, 5)),          # everything ragged, F not a multiple of 64
     (1029, 256, 2048, (4,)),          # 9 m-tiles, K=tokens ragged in the weight gradients
+    (600, 320, 1344, (1, 3)),         # H, F multiples of 64 but not of 256: partial 3-D boxes, skipped chunks
 ]
 
 
