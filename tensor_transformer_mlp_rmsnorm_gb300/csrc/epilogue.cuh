@@ -63,9 +63,10 @@ __device__ __forceinline__ void swiglu_bwd(float da, float g, float u, float& dg
 }
 
 // Fast variants for the bf16 tensor-core epilogues, whose results are stored
-// in bf16 (relative rounding 2^-9): __expf and an approximate reciprocal are
-// far inside that.  The fp32 path keeps expf and IEEE division.
-__device__ __forceinline__ float sigmoid_fast(float z) { return __frcp_rn(1.0f + __expf(-z)); }
+// in bf16 (relative rounding 2^-9): __expf and the approximate division
+// (errors of a few ulp of float) are far inside that; for z -> -inf the
+// sigmoid is 0, not NaN.  The fp32 path keeps expf and IEEE division.
+__device__ __forceinline__ float sigmoid_fast(float z) { return __fdividef(1.0f, 1.0f + __expf(-z)); }
 __device__ __forceinline__ float silu_fast(float z) { return z * sigmoid_fast(z); }
 __device__ __forceinline__ void swiglu_bwd_fast(float da, float g, float u, float& dg, float& du) {
   const float s = sigmoid_fast(g);
@@ -73,9 +74,8 @@ __device__ __forceinline__ void swiglu_bwd_fast(float da, float g, float u, floa
   du = da * g * s;
 }
 
-// One output element (m, n) -- used by the SIMT path and by ragged chunks of
-// the tensor-core path.  For GATEUP_SWIGLU, `acc` is G and `acc2` is U of
-// channel n.
+// One output element (m, n) of the fp32 SIMT path.  For GATEUP_SWIGLU, `acc`
+// is G and `acc2` is U of channel n.
 template <int EPI, typename T>
 __device__ __forceinline__ void epi_elem(const EpiParams& p, int m, int n, float acc, float acc2) {
   const int64_t mm = m;
