@@ -34,13 +34,59 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
+DESCR = {"bf16_llama8b": "Llama-3-8B-shaped MLP sublayer", "bf16_h2048": "H=2048 MLP sublayer",
+         "bf16_gelu_h4096": "GPT-style GeLU MLP sublayer", "bf16_70b_n2048": "Llama-2-70B-shaped MLP sublayer",
+         "fp32_small": "small fp32 MLP sublayer"}
 METRIC = "TP-MLP fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak"
 WORKLOAD = "bf16_llama8b"
 T_SHARDS = 8
 FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-# algorithmic flops per launch of each GEMM, in units of N*H*F
+# algorithmic flops per launch of each GEMM, in units of N*H*F (SwiGLU; the GeLU block has one
+# first-projection matrix, so its gate/up-shaped GEMMs are 2 N H F as well)
 GEMM_UNITS = {"gemm_gateup_act": 4, "gemm_down_reduce": 2, "gemm_dgrad_act": 2, "gemm_wgrad_down": 2,
               "gemm_wgrad_gateup": 4, "gemm_dgrad_norm_reduce": 4}
+GELU_UNITS = dict(GEMM_UNITS, gemm_gateup_act=2, gemm_wgrad_gateup=2, gemm_dgrad_norm_reduce=2)
+# sources whose change invalidates recorded DRAM traffic
+KERNEL_SOURCES = ("gemm_tc.cu", "gemm_simt.cu", "rowwise.cu", "tpmlp_api.cu", "epilogue.cuh", "ptx_sm103.cuh",
+                  "tpmlp_internal.h")
+
+
+def kernel_source_digest() -> str:
+    """sha256 (first 16 hex digits) over the library's kernel sources, in a fixed order."""
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, "tensor_transformer_mlp_rmsnorm_gb300", "csrc", f), "rb") as fh:
+            h.update(f.encode() + b"\0" + fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload: str, t: int, tokens: int, kernel: str):
+    """DRAM bytes (read + write) per launch of `kernel`, from a `traffic-record:` line of an ncu
+    summary under profiles/ taken on the same workload and on the current kernel sources; None if
+    there is none (never measured, or the kernels changed since)."""
+    import glob
+    digest = kernel_source_digest()
+    for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
+        for line in open(path):
+            if not line.startswith("traffic-record:"):
+                continue
+            kv = dict(tok.split("=", 1) for tok in line.split()[1:] if "=" in tok)
+            if (kv.get("workload") == workload and kv.get("t") == str(t) and kv.get("tokens") == str(tokens)
+                    and kv.get("sources") == digest and kernel in kv):
+                return float(kv[kernel]), os.path.relpath(path, ROOT)
+    return None, None
+
+
+def hbm_bytes(kernel: str, cfg, masters: bool):
+    """Algorithmic HBM bytes of one launch of a memory-bound kernel."""
+    N, H, F = cfg.tokens, cfg.hidden, cfg.ffn
+    e = 2 if cfg.dtype == "bf16" else 4
+    P = 3 * F * H + 2 * H if cfg.act == "swiglu" else 2 * F * H + F + 2 * H
+    return {"rmsnorm_fwd": 2 * N * H * e + 4 * N + H * e,
+            "mse_loss_grad": 3 * N * H * e,
+            "rmsnorm_bwd_residual": N * H * 4 + 3 * N * H * e + 4 * N + H * e,
+            "sgd_update": P * (12 + e) if masters else P * (4 + 2 * e)}.get(kernel)
 
 
 def peaks():
@@ -129,7 +175,7 @@ def cpu_oracle_tflops(cfg, inp, budget_s: float, min_tokens: int = 16, max_token
     while dt < budget_s / 4 and n < max_tokens:
         n = min(max_tokens, n * 2)
         dt = run(n)
-    flops = 18.0 * n * cfg.hidden * cfg.ffn
+    flops = cfg.gemm_flops * n / cfg.tokens
     return flops / dt / 1e12, n, dt
 
 
@@ -140,11 +186,22 @@ def host_cores():
         return os.cpu_count() or 1
 
 
+def workload_config(cfg, t: int, world: int) -> dict:
+    return {"workload": f"{cfg.name}: {DESCR.get(cfg.name, 'MLP sublayer')}, "
+                        f"{'SwiGLU' if cfg.act == 'swiglu' else 'GeLU'}, tokens={cfg.tokens} "
+                        f"({cfg.batch}x{cfg.seq}), hidden={cfg.hidden}, ffn={cfg.ffn}, t={t} logical shards, "
+                        f"lr={cfg.lr}",
+            "global_batch": cfg.batch * world, "seq_len": cfg.seq, "tokens_per_gpu": cfg.tokens, "t": t,
+            "parallelism": f"replicas x{world}"}
+
+
 def reference_arm(args):
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
     cfg = synth.CONFIGS[args.workload]
+    if args.tokens:
+        cfg = cfg.with_tokens(args.tokens)
     # the oracle needs the full weights but only a token sample
     sample = max(16, args.ref_tokens)
     inp = synth.make_inputs(cfg.with_tokens(sample), seed=1234)
@@ -170,15 +227,14 @@ def reference_arm(args):
     for _ in range(args.steps):
         step(n)
     el = time.perf_counter() - t0
-    flops = 18.0 * n * cfg.hidden * cfg.ffn
+    flops = cfg.gemm_flops * n / cfg.tokens
     val = flops * args.steps / el / 1e12
     cores = host_cores()
     line = {
         "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: tokens={cfg.tokens} hidden={cfg.hidden} ffn={cfg.ffn} t={T_SHARDS} "
-                               f"act={cfg.act}", "tokens_per_step_sampled": n, "parallelism": "replicas"},
+        "config": dict(workload_config(cfg, args.t, world), tokens_per_step_sampled=n),
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
                          "sample": f"first {n} of {cfg.tokens} tokens per step, full weights, float64 numpy"},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -200,6 +256,8 @@ def ours(args):
     from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP, build
     build.build()
     cfg = synth.CONFIGS[args.workload]
+    if args.tokens:
+        cfg = cfg.with_tokens(args.tokens)
     N, H, F = cfg.tokens, cfg.hidden, cfg.ffn
     t = args.t
     inp = synth.make_inputs(cfg, seed=1234 + rank)
@@ -208,8 +266,10 @@ def ours(args):
     def dev_bf16(a):
         return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(dev).to(bf)
 
-    params = {k: dev_bf16(inp[k]) for k in synth.param_names(cfg.act)}
-    masters = {k: torch.from_numpy(np.ascontiguousarray(inp[k], dtype=np.float32)).to(dev)
+    # the library names the first projection w_gate_up for both activations
+    lib_name = {"w_1": "w_gate_up"}
+    params = {lib_name.get(k, k): dev_bf16(inp[k]) for k in synth.param_names(cfg.act)}
+    masters = {lib_name.get(k, k): torch.from_numpy(np.ascontiguousarray(inp[k], dtype=np.float32)).to(dev)
                for k in synth.param_names(cfg.act)}
     x_host = torch.from_numpy(np.ascontiguousarray(inp["x"], dtype=np.float32)).to(bf).pin_memory()
     tg_host = torch.from_numpy(np.ascontiguousarray(inp["target"], dtype=np.float32)).to(bf).pin_memory()
@@ -227,7 +287,8 @@ def ours(args):
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
 
     def step():
-        m.forward(x, params["norm_w"], params["w_gate_up"], params["w_down"], params["b_down"], cfg.eps, t, y=y)
+        m.forward(x, params["norm_w"], params["w_gate_up"], params["w_down"], params["b_down"], cfg.eps, t, y=y,
+                  b_1=params.get("b_1"))
         m.mse_loss_grad(y, target, dy=dy, loss=loss)
         m.backward(dy, dx=dx, grads=grads)
         m.sgd_step(cfg.lr)
@@ -267,6 +328,11 @@ def ours(args):
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
         ms = float(tt.item())
     flops_step = cfg.gemm_flops
+    e = 2 if cfg.dtype == "bf16" else 4
+    nP = sum(v.numel() for v in params.values())
+    # activations saved and produced per step (x, y, dy, dx, n, G|U, A, dGU, dN) + parameters,
+    # fp32 masters and fp32 gradients
+    ws_gb = (N * H * (5 * e + 4) + N * F * (5 * e if cfg.act == "swiglu" else 3 * e) + nP * (e + 8)) / 1e9
     value = flops_step * args.steps * world / (ms / 1e3) / 1e12
     # ---------------------------------------------------------- end-to-end through the public API
     barrier()
@@ -302,17 +368,24 @@ def ours(args):
     top = max(ktot, key=ktot.get)
     top_ms, top_n = ktimes[top]
     per_launch_ms = top_ms / max(1, top_n)
-    gemm_ms = sum(ktimes[k][0] for k in ktimes if k in GEMM_UNITS)
-    if top in GEMM_UNITS:
-        achieved = GEMM_UNITS[top] * N * H * F / (per_launch_ms / 1e3) / 1e12
+    units = GEMM_UNITS if cfg.act == "swiglu" else GELU_UNITS
+    gemm_ms = sum(ktimes[k][0] for k in ktimes if k in units)
+    traffic, traffic_src = recorded_traffic(cfg.name, t, N, top)
+    if top in units:
+        achieved = units[top] * N * H * F / (per_launch_ms / 1e3) / 1e12
         roof = {"kernel": top, "bound": "tensor", "achieved": achieved, "peak": pk["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": achieved / pk["bf16_tflops_sustained"],
                 "peak_kind": f"bf16_tflops_sustained ({pk_src}); kernel timed inside a long step",
-                "frac_of_burst": achieved / pk["bf16_tflops"], "traffic": None,
-                "flops_per_launch": GEMM_UNITS[top] * N * H * F, "avg_launch_ms": per_launch_ms}
+                "frac_of_burst": achieved / pk["bf16_tflops"], "traffic": traffic,
+                "flops_per_launch": units[top] * N * H * F, "avg_launch_ms": per_launch_ms}
     else:
-        roof = {"kernel": top, "bound": "hbm", "achieved": None, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": None, "traffic": None}
+        nbytes = hbm_bytes(top, cfg, masters=True)
+        achieved = nbytes / (per_launch_ms / 1e3) / 1e9 if nbytes else None
+        roof = {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / pk["hbm_gbs"] if achieved else None, "peak_kind": f"hbm_gbs ({pk_src})",
+                "traffic": traffic, "bytes_per_launch": nbytes, "avg_launch_ms": per_launch_ms}
+    roof["traffic_source"] = traffic_src if traffic is not None else \
+        "null: no ncu DRAM record for this workload on the current kernel sources"
     cpu = None
     if cpu_inp is not None:
         v, n, dt = cpu_oracle_tflops(cfg, cpu_inp, budget_s=args.cpu_budget)
@@ -322,12 +395,9 @@ def ours(args):
     line = {
         "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
-        "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: Llama-3-8B-shaped SwiGLU MLP sublayer, tokens={N} (4x4096), "
-                               f"hidden={H}, ffn={F}, t={t} logical shards, lr={cfg.lr}",
-                   "global_batch": 4 * world, "seq_len": 4096, "tokens_per_gpu": N, "t": t,
-                   "parallelism": f"replicas x{world}",
-                   "l2": "no flush: per-step working set ~4.5 GB >> 129 MB L2 (weights 336 MB, x 128 MB)"},
+        "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
+        "config": dict(workload_config(cfg, t, world),
+                       l2=f"no flush: per-step working set ~{ws_gb:.1f} GB >> 129 MB L2"),
         "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
                              "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"],
                              "source": pk_src},
@@ -335,7 +405,7 @@ def ours(args):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][0])},
         "roofline": roof,
         "cpu_baseline": cpu,
-        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * N * H * 2,
+        "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * N * H * e,
                 "d2h_bytes_per_step": 4, "steps": e2e_steps},
         "clocks": clk,
         "gpu_launches": launches,
@@ -355,6 +425,7 @@ def main():
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.CONFIGS))
     ap.add_argument("--t", type=int, default=T_SHARDS)
+    ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
