@@ -17,7 +17,8 @@ Sources (web pages, cited by title and section):
 * "Megatron-LM walkthrough" (stanleyjacob.dev) -- the f and g operators
   ("Deep dive: tensor parallelism and the f and g operators"), the GeLU MLP
   built from ColumnParallelLinear/RowParallelLinear (Part II), fp32 master
-  parameters in the optimizer step ("Stage 8").
+  parameters and the clipped AdamW step ("Stage 8"), whose hyperparameters
+  come from the launch example near the top of the page.
 * "Megatron-LM Explained" (trishampatil.com) -- the GeLU MLP split A by
   columns, B by rows ("The MLP block: column-parallel, then row-parallel").
 
@@ -31,6 +32,11 @@ Readings where the pages are silent:
 * GeLU is the exact erf form.
 * Loss is 0.5 * mean((y - target)^2) over all N*H elements.
 * SGD is plain ``w <- w - lr * g`` (no momentum, no weight decay).
+* AdamW: Adam's published moment rates and epsilon (0.9, 0.999, 1e-8);
+  decoupled decay in PyTorch's parametrisation, on the projection matrices
+  only; clip coefficient max_norm / (norm + 1e-6) capped at 1; bias
+  correction with a 1-based step count; the global norm counts replicated
+  parameters once.
 * Backward formulas (never written on the pages) are derived by hand from the
   forward and pinned by central finite differences in the tests.
 
@@ -358,3 +364,99 @@ def shape_trace(S: int, B: int, H: int, F: int, t: int) -> dict:
                               "swiglu": [S, B, f], "down_weight": [H, f],
                               "partial_output": [S, B, H]},
     }
+
+
+# ---------------------------------------------------------------------------
+# AdamW with global gradient-norm clipping (the optimizer step of the
+# walkthrough, "Stage 8": the gradient norm is taken over every model-parallel
+# dimension and clipped, then AdamW updates the fp32 master parameters; its
+# launch example sets --weight-decay 0.1, --clip-grad 1.0 and --lr 1.5e-4)
+# ---------------------------------------------------------------------------
+
+# Unstated on the pages: the moment rates and epsilon are Adam's published
+# defaults (Kingma & Ba); the decay follows the decoupled form of Loshchilov &
+# Hutter in PyTorch's parametrisation (w <- w - lr*wd*w - lr*adam); decay
+# applies to the projection matrices only, not to the norm weight or biases;
+# the clip coefficient is max_norm / (norm + 1e-6), capped at 1.
+ADAMW_DEFAULTS = {"lr": 1.5e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.1,
+                  "max_grad_norm": 1.0}
+CLIP_EPS = 1e-6
+DECAYED = ("w_gate_up", "w_1", "w_down")
+REPLICATED = ("norm_w", "b_down")
+
+
+def global_grad_norm(g: dict) -> float:
+    """L2 norm of every parameter gradient taken together: sqrt(sum_k sum g_k^2)."""
+    total = 0.0
+    for k in sorted(g):
+        total += float(np.sum(np.square(np.asarray(g[k], dtype=np.float64))))
+    return math.sqrt(total)
+
+
+def clip_coefficient(norm: float, max_norm: float) -> float:
+    """Factor applied to every gradient so the global norm is at most max_norm;
+    1 when clipping is off (max_norm <= 0) or the norm is already within it."""
+    if max_norm <= 0:
+        return 1.0
+    return min(1.0, max_norm / (norm + CLIP_EPS))
+
+
+def adamw(p: dict, g: dict, m: dict, v: dict, step: int, lr: float, beta1: float, beta2: float,
+          eps: float, weight_decay: float, max_grad_norm: float) -> dict:
+    """One AdamW update of every parameter after global-norm clipping.
+
+    For each parameter, with c the clip coefficient and k = step (1-based):
+        g' = c g;  m <- b1 m + (1 - b1) g';  v <- b2 v + (1 - b2) g'^2
+        w  <- w - lr wd w - lr (m / (1 - b1^k)) / (sqrt(v / (1 - b2^k)) + eps)
+    wd is weight_decay for the projection matrices and 0 for the rest."""
+    if step < 1:
+        raise ValueError("step is 1-based")
+    norm = global_grad_norm(g)
+    c = clip_coefficient(norm, max_grad_norm)
+    bc1 = 1.0 - beta1 ** step
+    bc2 = 1.0 - beta2 ** step
+    new_p, new_m, new_v = {}, {}, {}
+    for k in p:
+        gk = c * np.asarray(g[k], dtype=np.float64)
+        mk = beta1 * m[k] + (1.0 - beta1) * gk
+        vk = beta2 * v[k] + (1.0 - beta2) * gk * gk
+        wd = weight_decay if k in DECAYED else 0.0
+        new_p[k] = p[k] - lr * wd * p[k] - lr * (mk / bc1) / (np.sqrt(vk / bc2) + eps)
+        new_m[k] = mk
+        new_v[k] = vk
+    return {"params": new_p, "m": new_m, "v": new_v, "grad_norm": norm, "clip": c}
+
+
+def dense_step_adamw(p: dict, x, target, eps: float, m: dict, v: dict, step: int, hp: dict,
+                     act: str = "swiglu") -> dict:
+    """Forward, loss, backward and one AdamW update of the dense block."""
+    y, c = dense_forward(p, x, eps, act)
+    loss, dy = mse_loss(y, target)
+    g = dense_backward(p, c, dy)
+    pg = {k: g[k] for k in p}
+    upd = adamw(p, pg, m, v, step, **hp)
+    return {"y": y, "loss": loss, "dy": dy, "grads": g, "new_params": upd["params"], "m": upd["m"],
+            "v": upd["v"], "grad_norm": upd["grad_norm"], "clip": upd["clip"]}
+
+
+def rank_grad_sqnorm(rank_grads: dict, rank: int, count_replicated_once: bool = True) -> float:
+    """One rank's share of the squared global norm: its FFN-sliced gradients,
+    plus the replicated ones (norm_w, b_down), which every rank holds
+    identically and which only rank 0 contributes.  With
+    ``count_replicated_once=False`` every rank adds them (the double-counting
+    mistake)."""
+    total = 0.0
+    for k, gk in rank_grads.items():
+        if k in ("x", "_dn"):
+            continue
+        if k in REPLICATED and count_replicated_once and rank != 0:
+            continue
+        total += float(np.sum(np.square(gk)))
+    return total
+
+
+def sharded_grad_norm(ranks: list, count_replicated_once: bool = True) -> float:
+    """Global norm across the t ranks: each rank's squared share, summed in
+    rank order (the all-reduce), then the square root."""
+    return math.sqrt(reduce_from_tp_region_forward(
+        [np.float64(rank_grad_sqnorm(rk["grads"], r, count_replicated_once)) for r, rk in enumerate(ranks)]))

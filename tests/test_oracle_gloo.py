@@ -103,3 +103,60 @@ def test_two_gloo_ranks(tmp_path, mode):
             assert fwd_ok and dwgu_ok and dwd_ok
             assert not dx_ok and not dnw_ok
             assert not dense_close(z["new_norm_w"], d["new_params"]["norm_w"])
+
+
+def _adamw_rank_main(rank, world, port, out_dir):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import tpmlp_oracle as O
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        p, x, tgt = _fixture()
+        eps = 1e-6
+        q = O.local_params(p, world, rank, "swiglu")
+        partial, c = O.rank_forward(q, x, eps, "swiglu")
+        y = x + _all_reduce(partial) + p["b_down"]
+        loss, dy = O.mse_loss(y, tgt)
+        g, dn_local = O.rank_backward_local(q, c, dy)
+        _, g["norm_w"] = O.rms_norm_backward(_all_reduce(dn_local), c["xhat"], c["rstd"], p["norm_w"])
+        # the global norm: each rank's squared share (replicated grads on rank 0 only), all-reduced
+        sq = _all_reduce(np.array([O.rank_grad_sqnorm(g, rank)]))[0]
+        norm = float(np.sqrt(sq))
+        hp = dict(O.ADAMW_DEFAULTS, lr=0.01, max_grad_norm=0.5 * norm)
+        clip = O.clip_coefficient(norm, hp["max_grad_norm"])
+        z = {k: np.zeros_like(q[k]) for k in q}
+        # each rank updates its own slices with the shared clip factor (clipping off inside)
+        out = O.adamw(q, {k: clip * g[k] for k in q}, z, dict(z), 1, **dict(hp, max_grad_norm=0.0))
+        np.savez(os.path.join(out_dir, f"a{rank}.npz"), norm=norm, wgu=out["params"]["w_gate_up"],
+                 wd=out["params"]["w_down"], nw=out["params"]["norm_w"], bd=out["params"]["b_down"])
+    finally:
+        dist.destroy_process_group()
+
+
+def test_two_gloo_ranks_adamw(tmp_path):
+    """The walkthrough's clipped AdamW step across two ranks ("Stage 8"): the
+    norm all-reduce over the ranks' shares equals the dense norm, and the
+    rank-local updates assemble to the dense update."""
+    from oracle import tpmlp_oracle as O
+    world = 2
+    mp.start_processes(_adamw_rank_main, args=(world, _free_port(), str(tmp_path)), nprocs=world, join=True,
+                       start_method="spawn")
+    p, x, tgt = _fixture()
+    d = O.dense_step(p, x, tgt, 1e-6, 0.0)
+    g = {k: d["grads"][k] for k in p}
+    norm = O.global_grad_norm(g)
+    hp = dict(O.ADAMW_DEFAULTS, lr=0.01, max_grad_norm=0.5 * norm)
+    z = {k: np.zeros_like(p[k]) for k in p}
+    ref = O.adamw(p, g, z, dict(z), 1, **hp)
+    assert ref["clip"] < 1.0
+    F = p["w_down"].shape[1]
+    for r in range(world):
+        a = np.load(tmp_path / f"a{r}.npz")
+        lo, hi = O.shard_interval(F, world, r)
+        assert float(a["norm"]) == pytest.approx(norm, rel=1e-13)
+        np.testing.assert_allclose(a["wgu"], ref["params"]["w_gate_up"][:, lo:hi], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(a["wd"], ref["params"]["w_down"][:, lo:hi], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(a["nw"], ref["params"]["norm_w"], rtol=1e-12, atol=1e-15)
+        np.testing.assert_allclose(a["bd"], ref["params"]["b_down"], rtol=1e-12, atol=1e-15)
