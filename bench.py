@@ -34,6 +34,9 @@ import numpy as np  # noqa: E402
 
 import synth  # noqa: E402
 
+# the walkthrough's launch example ("Stage 8" optimizer): lr 1.5e-4, weight decay 0.1, clip 1.0;
+# Adam's published moment rates and epsilon
+ADAMW = {"lr": 1.5e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.1, "max_grad_norm": 1.0}
 DESCR = {"bf16_llama8b": "Llama-3-8B-shaped MLP sublayer", "bf16_h2048": "H=2048 MLP sublayer",
          "bf16_gelu_h4096": "GPT-style GeLU MLP sublayer", "bf16_70b_n2048": "Llama-2-70B-shaped MLP sublayer",
          "fp32_small": "small fp32 MLP sublayer"}
@@ -46,34 +49,51 @@ FALLBACK = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1
 GEMM_UNITS = {"gemm_gateup_act": 4, "gemm_down_reduce": 2, "gemm_dgrad_act": 2, "gemm_wgrad_down": 2,
               "gemm_wgrad_gateup": 4, "gemm_dgrad_norm_reduce": 4}
 GELU_UNITS = dict(GEMM_UNITS, gemm_gateup_act=2, gemm_wgrad_gateup=2, gemm_dgrad_norm_reduce=2)
-# sources whose change invalidates recorded DRAM traffic
-KERNEL_SOURCES = ("gemm_tc.cu", "gemm_simt.cu", "rowwise.cu", "tpmlp_api.cu", "epilogue.cuh", "ptx_sm103.cuh",
-                  "tpmlp_internal.h")
+# kernel sources per family: a change to any of them invalidates the recorded DRAM traffic of that
+# family's kernels
+KERNEL_FAMILIES = {
+    "gemm": ("gemm_tc.cu", "gemm_simt.cu", "ptx_sm103.cuh", "epilogue.cuh"),
+    "rowwise": ("rowwise.cu", "vec.cuh", "epilogue.cuh"),
+    "optim": ("optim.cu", "vec.cuh"),
+}
 
 
-def kernel_source_digest() -> str:
-    """sha256 (first 16 hex digits) over the library's kernel sources, in a fixed order."""
+def kernel_family(kernel: str) -> str:
+    if kernel.startswith("gemm_"):
+        return "gemm"
+    return "optim" if kernel in ("grad_sqnorm", "adamw_update") else "rowwise"
+
+
+def kernel_source_digest(family: str) -> str:
+    """sha256 (first 16 hex digits) over one kernel family's sources, in a fixed order."""
     import hashlib
     h = hashlib.sha256()
-    for f in KERNEL_SOURCES:
+    for f in KERNEL_FAMILIES[family]:
         with open(os.path.join(ROOT, "tensor_transformer_mlp_rmsnorm_gb300", "csrc", f), "rb") as fh:
             h.update(f.encode() + b"\0" + fh.read())
     return h.hexdigest()[:16]
 
 
+def source_digests() -> str:
+    """The `digest=` field of a traffic record for the current sources."""
+    return ",".join(f"{fam}:{kernel_source_digest(fam)}" for fam in sorted(KERNEL_FAMILIES))
+
+
 def recorded_traffic(workload: str, t: int, tokens: int, kernel: str):
     """DRAM bytes (read + write) per launch of `kernel`, from a `traffic-record:` line of an ncu
-    summary under profiles/ taken on the same workload and on the current kernel sources; None if
-    there is none (never measured, or the kernels changed since)."""
+    summary under profiles/ taken on the same workload and on the current sources of the kernel's
+    family; None if there is none (never measured, or the kernel changed since)."""
     import glob
-    digest = kernel_source_digest()
+    fam = kernel_family(kernel)
+    want = kernel_source_digest(fam)
     for path in sorted(glob.glob(os.path.join(ROOT, "profiles", "*.md"))):
         for line in open(path):
             if not line.startswith("traffic-record:"):
                 continue
             kv = dict(tok.split("=", 1) for tok in line.split()[1:] if "=" in tok)
+            digests = dict(d.split(":", 1) for d in kv.get("digest", "").split(",") if ":" in d)
             if (kv.get("workload") == workload and kv.get("t") == str(t) and kv.get("tokens") == str(tokens)
-                    and kv.get("sources") == digest and kernel in kv):
+                    and digests.get(fam) == want and kernel in kv):
                 return float(kv[kernel]), os.path.relpath(path, ROOT)
     return None, None
 
@@ -86,7 +106,9 @@ def hbm_bytes(kernel: str, cfg, masters: bool):
     return {"rmsnorm_fwd": 2 * N * H * e + 4 * N + H * e,
             "mse_loss_grad": 3 * N * H * e,
             "rmsnorm_bwd_residual": N * H * 4 + 3 * N * H * e + 4 * N + H * e,
-            "sgd_update": P * (12 + e) if masters else P * (4 + 2 * e)}.get(kernel)
+            "sgd_update": P * (12 + e) if masters else P * (4 + 2 * e),
+            "grad_sqnorm": 4 * P,
+            "adamw_update": P * (28 + e) if masters else P * (20 + 2 * e)}.get(kernel)
 
 
 def peaks():
@@ -286,12 +308,21 @@ def ours(args):
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
 
+    adamw = args.optimizer == "adamw"
+    if adamw:
+        m.new_adam_state()
+    nstep = [0]
+
     def step():
         m.forward(x, params["norm_w"], params["w_gate_up"], params["w_down"], params["b_down"], cfg.eps, t, y=y,
                   b_1=params.get("b_1"))
         m.mse_loss_grad(y, target, dy=dy, loss=loss)
         m.backward(dy, dx=dx, grads=grads)
-        m.sgd_step(cfg.lr)
+        if adamw:
+            nstep[0] += 1
+            m.adamw_step(step=nstep[0], **ADAMW)
+        else:
+            m.sgd_step(cfg.lr)
 
     def barrier():
         if world > 1:
@@ -392,11 +423,12 @@ def ours(args):
         cpu = {"value": v, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"dense fwd+loss+bwd+SGD of the first {n} of {N} tokens with the full weights, "
                          f"float64 numpy, {dt:.1f} s"}
+    metric = METRIC if not adamw else METRIC.replace("SGD", "AdamW")
     line = {
-        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+        "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
-        "config": dict(workload_config(cfg, t, world),
+        "config": dict(workload_config(cfg, t, world), optimizer=args.optimizer,
                        l2=f"no flush: per-step working set ~{ws_gb:.1f} GB >> 129 MB L2"),
         "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
                              "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"],
@@ -426,6 +458,7 @@ def main():
     ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.CONFIGS))
     ap.add_argument("--t", type=int, default=T_SHARDS)
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
+    ap.add_argument("--optimizer", choices=["sgd", "adamw"], default="sgd")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")

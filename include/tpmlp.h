@@ -151,6 +151,50 @@ TPMLP_API tpmlp_status tpmlp_bind_master(tpmlp_ctx* ctx, float* norm_w, float* w
  * BF16 without masters: parameters updated through float and re-rounded. */
 TPMLP_API tpmlp_status tpmlp_sgd_step(tpmlp_ctx* ctx, float lr);
 
+/* One fp32 tensor per parameter, each laid out like that parameter
+ * (b_1 is the GeLU first-projection bias; NULL for SwiGLU). */
+typedef struct {
+  float* norm_w;
+  float* w_gate_up;
+  float* b_1;
+  float* w_down;
+  float* b_down;
+} tpmlp_param_set;
+
+/* Hyperparameters of one AdamW step ("Megatron-LM walkthrough", "Stage 8",
+ * whose launch example uses lr 1.5e-4, weight decay 0.1, clip 1.0). */
+typedef struct {
+  float lr;            /* learning rate, finite */
+  float beta1, beta2;  /* moment decay rates, each in [0, 1) */
+  float eps;           /* added to the root of the corrected second moment, >= 0 */
+  float weight_decay;  /* decoupled decay, applied to w_gate_up (or W_1) and w_down only */
+  float max_grad_norm; /* clip the global L2 gradient norm to this; <= 0 turns clipping off */
+  int64_t step;        /* 1-based index of this update, for the bias corrections */
+} tpmlp_adamw_params;
+
+/* Bind the first (m) and second (v) moment estimates of AdamW: device fp32
+ * tensors owned by the caller, zero before the first step and carried from
+ * step to step by the caller.  They must stay valid while adamw_step runs.
+ * Every pointer is 16-byte aligned; b_1 is set exactly for GeLU.  Passing
+ * two NULL sets unbinds.  TPMLP_ERR_ARG on a missing or misaligned tensor. */
+TPMLP_API tpmlp_status tpmlp_bind_adam_state(tpmlp_ctx* ctx, const tpmlp_param_set* m, const tpmlp_param_set* v);
+
+/* One AdamW update of every parameter of the last forward, with the
+ * gradients of the last backward, after clipping them by their global norm
+ * (the walkthrough's optimizer step, "Stage 8"):
+ *   c = min(1, max_grad_norm / (||g|| + 1e-6))   (1 if max_grad_norm <= 0)
+ *   m <- b1 m + (1 - b1) c g;   v <- b2 v + (1 - b2) (c g)^2
+ *   w <- w - lr wd w - lr (m / (1 - b1^step)) / (sqrt(v / (1 - b2^step)) + eps)
+ * ||g|| runs over every parameter gradient; wd is weight_decay for the
+ * projection matrices and 0 for norm_w and the biases.  Parameters follow
+ * sgd_step's rules (f32 in place; bf16 through the bound fp32 masters, bf16
+ * copies re-rounded; bf16 without masters through float).  `grad_norm`, if
+ * not NULL, is a device float that receives ||g|| before clipping.
+ * Two kernels: a norm pass over the gradients, then the update.
+ * TPMLP_ERR_ORDER before a backward; TPMLP_ERR_ARG without bound moments or
+ * with hyperparameters out of range. */
+TPMLP_API tpmlp_status tpmlp_adamw_step(tpmlp_ctx* ctx, const tpmlp_adamw_params* hp, float* grad_norm);
+
 /* Debug flags (TPMLP_DBG_*) and the shard whose view the SKIP flags take. */
 TPMLP_API tpmlp_status tpmlp_set_debug(tpmlp_ctx* ctx, uint32_t flags, int32_t shard);
 

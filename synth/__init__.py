@@ -191,6 +191,25 @@ def make_inputs(cfg: Config, seed: int = 1234) -> dict:
     return d
 
 
+def make_optimizer_state(cfg: Config, seed: int = 1234, grad_std: float = 1e-4, m_std: float = 5e-5,
+                         v_std: float = 1e-4) -> dict:
+    """Seeded stand-ins for one optimizer step's inputs, per parameter, as
+    float64 arrays of fp32-representable values: a gradient g ~ N(0, grad_std),
+    a first moment m ~ N(0, m_std) and a second moment v = |N(0, v_std)|^2
+    (non-negative).  Streams 100 + 3k, 101 + 3k, 102 + 3k for the k-th
+    parameter of ``param_names``."""
+    shapes = {"norm_w": (cfg.hidden,), "w_gate_up": (2, cfg.ffn, cfg.hidden), "w_1": (cfg.ffn, cfg.hidden),
+              "b_1": (cfg.ffn,), "w_down": (cfg.hidden, cfg.ffn), "b_down": (cfg.hidden,)}
+    f32 = lambda a: a.astype(np.float32).astype(np.float64)
+    out = {"grad": {}, "m": {}, "v": {}}
+    for k, name in enumerate(param_names(cfg.act)):
+        shp = shapes[name]
+        out["grad"][name] = f32(normal(seed, 100 + 3 * k, shp, 0.0, grad_std))
+        out["m"][name] = f32(normal(seed, 101 + 3 * k, shp, 0.0, m_std))
+        out["v"][name] = f32(np.square(normal(seed, 102 + 3 * k, shp, 0.0, v_std)))
+    return out
+
+
 def param_names(act: str) -> tuple:
     return ("norm_w", "w_gate_up", "w_down", "b_down") if act == "swiglu" else \
            ("norm_w", "w_1", "b_1", "w_down", "b_down")

@@ -9,65 +9,10 @@
 
 #include "epilogue.cuh"
 #include "tpmlp_internal.h"
+#include "vec.cuh"
 
 namespace tpmlp {
 namespace {
-
-// 16-byte vector of T as floats.
-template <typename T>
-struct Vec;
-template <>
-struct Vec<float> {
-  static constexpr int N = 4;
-  __device__ static void load(const float* p, float* f) {
-    const float4 v = *reinterpret_cast<const float4*>(p);
-    f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w;
-  }
-  __device__ static void store(float* p, const float* f) {
-    *reinterpret_cast<float4*>(p) = make_float4(f[0], f[1], f[2], f[3]);
-  }
-};
-template <>
-struct Vec<__nv_bfloat16> {
-  static constexpr int N = 8;
-  __device__ static void load(const __nv_bfloat16* p, float* f) {
-    const uint4 v = *reinterpret_cast<const uint4*>(p);
-    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[i]));
-      f[2 * i] = t.x;
-      f[2 * i + 1] = t.y;
-    }
-  }
-  __device__ static void store(__nv_bfloat16* p, const float* f) {
-    uint32_t w[4];
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);
-      w[i] = *reinterpret_cast<uint32_t*>(&h);
-    }
-    *reinterpret_cast<uint4*>(p) = make_uint4(w[0], w[1], w[2], w[3]);
-  }
-};
-
-// 4 consecutive elements of T as floats (8 bytes for bf16, 16 for float).
-__device__ __forceinline__ void load4(const float* p, float* f) { Vec<float>::load(p, f); }
-__device__ __forceinline__ void store4(float* p, const float* f) { Vec<float>::store(p, f); }
-__device__ __forceinline__ void load4(const __nv_bfloat16* p, float* f) {
-  const uint2 v = *reinterpret_cast<const uint2*>(p);
-  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
-  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
-  f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
-}
-__device__ __forceinline__ void store4(__nv_bfloat16* p, const float* f) {
-  __nv_bfloat162 a = __floats2bfloat162_rn(f[0], f[1]);
-  __nv_bfloat162 b = __floats2bfloat162_rn(f[2], f[3]);
-  uint2 v;
-  v.x = *reinterpret_cast<uint32_t*>(&a);
-  v.y = *reinterpret_cast<uint32_t*>(&b);
-  *reinterpret_cast<uint2*>(p) = v;
-}
 
 // ------------------------------------------------------------- RMSNorm fwd
 // TPR threads per row, each holding up to MAXV 16-byte vectors of the row in

@@ -12,6 +12,7 @@
 //             all-reduce, "Put the other collective in backward") ->
 //             rmsnorm_bwd_residual -> colsum_finalize
 //   sgd     : sgd_update
+//   adamw   : grad_sqnorm -> adamw_update (walkthrough, "Stage 8")
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -42,6 +43,8 @@ enum KernelId {
   K_COLSUM_FINAL,
   K_COLSUM_B1,
   K_SGD,
+  K_GRAD_NORM,
+  K_ADAMW,
   K_PROBE,
   K_COUNT
 };
@@ -50,7 +53,7 @@ const char* const kKernelNames[K_COUNT] = {
     "rmsnorm_fwd",        "gemm_gateup_act",     "gemm_down_reduce",     "mse_loss_grad",
     "loss_finalize",      "gemm_dgrad_act",      "gemm_wgrad_down",      "gemm_wgrad_gateup",
     "gemm_dgrad_norm_reduce", "rmsnorm_bwd_residual", "colsum_finalize", "colsum_b1",
-    "sgd_update",         "timeout_probe"};
+    "sgd_update",         "grad_sqnorm",         "adamw_update",         "timeout_probe"};
 
 constexpr int MAX_BWD_PARTS = 1024;
 constexpr int MAX_B1_PARTS = 256;
@@ -62,7 +65,7 @@ thread_local std::string g_thread_err;
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status, loss_part, nrm, rstd, gu, act, dgu, dnrm, part_dw, part_db, part_b1, total;
+  size_t status, loss_part, norm_part, nrm, rstd, gu, act, dgu, dnrm, part_dw, part_db, part_b1, total;
 };
 
 bool config_error(const tpmlp_config* c, std::string* why, tpmlp_status* st) {
@@ -98,6 +101,7 @@ Layout make_layout(const tpmlp_config& c) {
   };
   L.status = take(256);
   L.loss_part = take(MAX_LOSS_PARTS * sizeof(double));
+  L.norm_part = take(MAX_NORM_PARTS * sizeof(double));
   L.nrm = take(N * H * E);
   L.rstd = take(N * 4);
   L.gu = take(N * guw * E);
@@ -132,6 +136,8 @@ struct tpmlp_ctx {
              *b_down = nullptr;
   float *g_norm_w = nullptr, *g_w_gu = nullptr, *g_b_1 = nullptr, *g_w_down = nullptr, *g_b_down = nullptr;
   float *m_norm_w = nullptr, *m_w_gu = nullptr, *m_b_1 = nullptr, *m_w_down = nullptr, *m_b_down = nullptr;
+  tpmlp_param_set adam_m{}, adam_v{};
+  bool adam_bound = false;
   uint32_t dbg_flags = 0;
   int dbg_shard = 0;
   // timing
@@ -588,6 +594,70 @@ tpmlp_status tpmlp_sgd_step(tpmlp_ctx* c, float lr) {
   add(c->m_b_down, c->g_b_down, c->b_down, H);
   const int dt = c->cfg.dtype == TPMLP_BF16 ? 1 : 0;
   return c->run(K_SGD, [&] { return launch_sgd(dt, a, c->num_sms, c->stream); });
+}
+
+tpmlp_status tpmlp_bind_adam_state(tpmlp_ctx* c, const tpmlp_param_set* m, const tpmlp_param_set* v) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!m && !v) {
+    c->adam_m = tpmlp_param_set{};
+    c->adam_v = tpmlp_param_set{};
+    c->adam_bound = false;
+    return TPMLP_OK;
+  }
+  if (!m || !v) return c->fail(TPMLP_ERR_ARG, "bind both moment sets or neither");
+  for (const tpmlp_param_set* s : {m, v}) {
+    if (!s->norm_w || !s->w_gate_up || !s->w_down || !s->b_down || (c->swiglu() ? s->b_1 != nullptr : !s->b_1))
+      return c->fail(TPMLP_ERR_ARG, "a moment tensor is missing (b_1 exactly for GeLU)");
+    for (const void* p : {(const void*)s->norm_w, (const void*)s->w_gate_up, (const void*)s->b_1,
+                          (const void*)s->w_down, (const void*)s->b_down})
+      if (p && !aligned16(p)) return c->fail(TPMLP_ERR_ARG, "moment tensor not 16-byte aligned");
+  }
+  c->adam_m = *m;
+  c->adam_v = *v;
+  c->adam_bound = true;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_adamw_step(tpmlp_ctx* c, const tpmlp_adamw_params* hp, float* grad_norm) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!hp) return c->fail(TPMLP_ERR_ARG, "hyperparameters are NULL");
+  if (!c->bwd_done) return c->fail(TPMLP_ERR_ORDER, "adamw_step before backward");
+  if (!c->adam_bound) return c->fail(TPMLP_ERR_ARG, "AdamW moments are not bound");
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay) || !std::isfinite(hp->max_grad_norm) ||
+      !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f) ||
+      !(hp->eps >= 0.f && std::isfinite(hp->eps)) || hp->step < 1)
+    return c->fail(TPMLP_ERR_ARG, "AdamW hyperparameter out of range");
+  if (grad_norm && (reinterpret_cast<uintptr_t>(grad_norm) & 3u))
+    return c->fail(TPMLP_ERR_ARG, "grad_norm not 4-byte aligned");
+  const int64_t H = c->cfg.hidden, F = c->cfg.ffn;
+  const bool sw = c->swiglu();
+  const double bc1 = 1.0 - std::pow((double)hp->beta1, (double)hp->step);
+  const double bc2 = 1.0 - std::pow((double)hp->beta2, (double)hp->step);
+  AdamArgs a{};
+  a.beta1 = hp->beta1;
+  a.beta2 = hp->beta2;
+  a.one_m_beta1 = (float)(1.0 - (double)hp->beta1);
+  a.one_m_beta2 = (float)(1.0 - (double)hp->beta2);
+  a.step_size = (float)((double)hp->lr / bc1);
+  a.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  a.eps = hp->eps;
+  a.max_norm = hp->max_grad_norm;
+  a.part = c->wsp<double>(c->L.norm_part);
+  a.grad_norm = grad_norm;
+  const float lr_wd = (float)((double)hp->lr * (double)hp->weight_decay);
+  auto add = [&](float* master, const float* g, const void* w, float* m, float* v, int64_t n, bool decay) {
+    a.seg[a.nseg++] = AdamSeg{master, g, const_cast<void*>(w), m, v, n, decay ? lr_wd : 0.0f};
+  };
+  const tpmlp_param_set &M = c->adam_m, &V = c->adam_v;
+  add(c->m_norm_w, c->g_norm_w, c->norm_w, M.norm_w, V.norm_w, H, false);
+  add(c->m_w_gu, c->g_w_gu, c->w_gu, M.w_gate_up, V.w_gate_up, (sw ? 2 * F : F) * H, true);
+  if (!sw) add(c->m_b_1, c->g_b_1, c->b_1, M.b_1, V.b_1, F, false);
+  add(c->m_w_down, c->g_w_down, c->w_down, M.w_down, V.w_down, H * F, true);
+  add(c->m_b_down, c->g_b_down, c->b_down, M.b_down, V.b_down, H, false);
+  const int nb = adam_blocks(a, c->num_sms);
+  const int dt = c->cfg.dtype == TPMLP_BF16 ? 1 : 0;
+  TPMLP_TRY(c->run(K_GRAD_NORM, [&] { return launch_grad_sqnorm(a, nb, c->stream); }));
+  return c->run(K_ADAMW, [&] { return launch_adamw(dt, a, nb, c->stream); });
 }
 
 tpmlp_status tpmlp_sync(tpmlp_ctx* c) {

@@ -81,6 +81,35 @@ struct SgdArgs {
 };
 cudaError_t launch_sgd(int dtype, const SgdArgs& a, int num_sms, cudaStream_t st);
 
+// AdamW with global-norm clipping: one segment per parameter.
+struct AdamSeg {
+  float* master;      // float master copy (or nullptr)
+  const float* grad;  // float gradient
+  void* w;            // parameter in the activation dtype
+  float* m;           // first moment
+  float* v;           // second moment
+  int64_t n;          // elements (multiple of 4)
+  float lr_wd;        // lr * weight_decay for this parameter (0: no decay)
+};
+constexpr int ADAM_MAX_SEGS = 6;
+constexpr int MAX_NORM_PARTS = 2048;
+struct AdamArgs {
+  AdamSeg seg[ADAM_MAX_SEGS];
+  int nseg;
+  float beta1, beta2;      // moment rates
+  float one_m_beta1, one_m_beta2;
+  float step_size;         // lr / (1 - beta1^step)
+  float inv_sqrt_bc2;      // 1 / sqrt(1 - beta2^step)
+  float eps;
+  float max_norm;          // <= 0: no clipping
+  double* part;            // per-block partial sums of g^2 (MAX_NORM_PARTS)
+  float* grad_norm;        // optional device output
+};
+// Number of blocks (= norm partials) both AdamW kernels use.
+int adam_blocks(const AdamArgs& a, int num_sms);
+cudaError_t launch_grad_sqnorm(const AdamArgs& a, int nblocks, cudaStream_t st);
+cudaError_t launch_adamw(int dtype, const AdamArgs& a, int nblocks, cudaStream_t st);
+
 // Message returned by tpmlp_last_error(NULL) on this host thread.
 void set_thread_error(const std::string& msg);
 

@@ -34,6 +34,19 @@ class TPMLPError(RuntimeError):
         self.status = status
 
 
+class ParamSet(ctypes.Structure):
+    """tpmlp_param_set: one device float* per parameter (b_1 for GeLU only)."""
+    _fields_ = [("norm_w", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("b_1", ctypes.c_void_p),
+                ("w_down", ctypes.c_void_p), ("b_down", ctypes.c_void_p)]
+
+
+class AdamWParams(ctypes.Structure):
+    """tpmlp_adamw_params."""
+    _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
+                ("eps", ctypes.c_float), ("weight_decay", ctypes.c_float), ("max_grad_norm", ctypes.c_float),
+                ("step", ctypes.c_int64)]
+
+
 class Config(ctypes.Structure):
     _fields_ = [("max_tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("ffn", ctypes.c_int64),
                 ("max_t", ctypes.c_int32), ("dtype", ctypes.c_int32), ("act", ctypes.c_int32),
@@ -52,6 +65,8 @@ _SIGNATURES = {
     "tpmlp_backward": (_i32, [_vp, _vp, _vp, _fp, _fp, _fp, _fp, _fp]),
     "tpmlp_bind_master": (_i32, [_vp, _fp, _fp, _fp, _fp, _fp]),
     "tpmlp_sgd_step": (_i32, [_vp, _f32]),
+    "tpmlp_bind_adam_state": (_i32, [_vp, ctypes.POINTER(ParamSet), ctypes.POINTER(ParamSet)]),
+    "tpmlp_adamw_step": (_i32, [_vp, ctypes.POINTER(AdamWParams), _fp]),
     "tpmlp_set_debug": (_i32, [_vp, _u32, _i32]),
     "tpmlp_sync": (_i32, [_vp]),
     "tpmlp_set_timing": (_i32, [_vp, _i32]),
@@ -159,6 +174,8 @@ class TPMLP:
         self.tokens = 0
         self._fwd = False
         self._loss = torch.zeros(1, dtype=torch.float32, device=self.device)
+        self._gn = torch.zeros(1, dtype=torch.float32, device=self.device)
+        self._adam = None
 
     def close(self):
         if getattr(self, "ctx", None):
@@ -251,6 +268,40 @@ class TPMLP:
 
     def sgd_step(self, lr: float):
         _check(lib().tpmlp_sgd_step(self.ctx, float(lr)), self.ctx)
+
+    def _param_set(self, d: dict, what: str) -> ParamSet:
+        f32 = torch.float32
+        return ParamSet(self._t(d["norm_w"], (self.H,), f32, f"{what}.norm_w"),
+                        self._t(d["w_gate_up"], self._gu_shape(), f32, f"{what}.w_gate_up"),
+                        self._t(d["b_1"], (self.F,), f32, f"{what}.b_1") if self.act == "gelu" else None,
+                        self._t(d["w_down"], (self.H, self.F), f32, f"{what}.w_down"),
+                        self._t(d["b_down"], (self.H,), f32, f"{what}.b_down"))
+
+    def new_adam_state(self):
+        """Zeroed first and second moments shaped like the parameters (fp32), bound to this context."""
+        m = {k: torch.zeros_like(v) for k, v in self.new_grads().items()}
+        v = {k: torch.zeros_like(t) for k, t in m.items()}
+        self.bind_adam_state(m, v)
+        return m, v
+
+    def bind_adam_state(self, m: dict | None, v: dict | None):
+        if m is None and v is None:
+            _check(lib().tpmlp_bind_adam_state(self.ctx, None, None), self.ctx)
+            self._adam = None
+            return
+        ms, vs = self._param_set(m, "m"), self._param_set(v, "v")
+        _check(lib().tpmlp_bind_adam_state(self.ctx, ctypes.byref(ms), ctypes.byref(vs)), self.ctx)
+        self._adam = (m, v)  # keep the tensors alive while bound
+
+    def adamw_step(self, lr: float, step: int, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                   weight_decay: float = 0.1, max_grad_norm: float = 1.0, grad_norm=None):
+        """One clipped AdamW update; returns the device float holding the global gradient norm."""
+        gn = self._gn if grad_norm is None else grad_norm
+        hp = AdamWParams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                         float(max_grad_norm), int(step))
+        _check(lib().tpmlp_adamw_step(self.ctx, ctypes.byref(hp), self._t(gn, (1,), torch.float32, "grad_norm")),
+               self.ctx)
+        return gn
 
     def set_debug(self, flags: int, shard: int = 0):
         _check(lib().tpmlp_set_debug(self.ctx, int(flags), int(shard)), self.ctx)
