@@ -18,7 +18,9 @@ Sources (web pages, cited by title and section):
   ("Deep dive: tensor parallelism and the f and g operators"), the GeLU MLP
   built from ColumnParallelLinear/RowParallelLinear (Part II), fp32 master
   parameters and the clipped AdamW step ("Stage 8"), whose hyperparameters
-  come from the launch example near the top of the page.
+  come from the launch example near the top of the page; the sequence-
+  parallel form ("Deep dive: sequence parallelism, memory for free") and the
+  all-reduce of its norm-weight gradients ("Stage 7: finalize_model_grads").
 * "Megatron-LM Explained" (trishampatil.com) -- the GeLU MLP split A by
   columns, B by rows ("The MLP block: column-parallel, then row-parallel").
 
@@ -37,6 +39,10 @@ Readings where the pages are silent:
   only; clip coefficient max_norm / (norm + 1e-6) capped at 1; bias
   correction with a 1-based step count; the global norm counts replicated
   parameters once.
+* Sequence parallelism: contiguous token slices per rank (N % t == 0); the
+  output bias is added on the slice after the reduce-scatter, so its
+  gradient, like the norm weight's, is a per-slice sum that the all-reduce
+  completes; the loss is the mean over every token.
 * Backward formulas (never written on the pages) are derived by hand from the
   forward and pinned by central finite differences in the tests.
 
@@ -244,8 +250,15 @@ def rank_forward(q: dict, x, eps: float, act: str):
     """One rank's work up to its partial output ("Split the expansion",
     "Split the contraction"): partial = local hidden @ W_d_local^T."""
     n, rstd, xhat = rms_norm(x, q["norm_w"], eps)
-    n_par = copy_to_tp_region_forward(n)
-    c = {"n": n_par, "rstd": rstd, "xhat": xhat, "act": act}
+    partial, c = rank_forward_normed(q, copy_to_tp_region_forward(n), act)
+    c.update(rstd=rstd, xhat=xhat)
+    return partial, c
+
+
+def rank_forward_normed(q: dict, n_par, act: str):
+    """The tensor-parallel region of one rank, from the normed input it
+    receives: column-parallel expansion, activation, row-parallel partial."""
+    c = {"n": n_par, "act": act}
     if act == "swiglu":
         gate = linear(n_par, q["w_gate_up"][0])
         up = linear(n_par, q["w_gate_up"][1])
@@ -460,3 +473,116 @@ def sharded_grad_norm(ranks: list, count_replicated_once: bool = True) -> float:
     rank order (the all-reduce), then the square root."""
     return math.sqrt(reduce_from_tp_region_forward(
         [np.float64(rank_grad_sqnorm(rk["grads"], r, count_replicated_once)) for r, rk in enumerate(ranks)]))
+
+
+# ---------------------------------------------------------------------------
+# Sequence-parallel form (walkthrough, "Deep dive: sequence parallelism,
+# memory for free"; "Stage 7: finalize_model_grads"): the regions outside the
+# tensor-parallel linears (RMSNorm, residual, bias) hold a slice of the tokens
+# per rank; an all-gather enters the tensor-parallel region and a
+# reduce-scatter leaves it; the gradients of the replicated norm weight and
+# output bias, each computed from one rank's tokens, are all-reduced.
+# ---------------------------------------------------------------------------
+
+
+def token_interval(tokens: int, t: int, rank: int):
+    """Rank r's contiguous token slice [r N/t, (r+1) N/t); N % t == 0."""
+    if t < 1 or tokens % t != 0:
+        raise ShapeError(f"tokens={tokens} is not divisible by t={t}")
+    n = tokens // t
+    return rank * n, (rank + 1) * n
+
+
+def gather_from_sequence_parallel_region(shards):
+    """All-gather along the tokens: the rank slices concatenated in rank order."""
+    return np.concatenate(shards, axis=0)
+
+
+def reduce_scatter_to_sequence_parallel_region(partials):
+    """Reduce-scatter along the tokens: rank r receives the sum, in rank order,
+    of every rank's rows [r N/t, (r+1) N/t)."""
+    t = len(partials)
+    out = []
+    for r in range(t):
+        lo, hi = token_interval(partials[0].shape[0], t, r)
+        out.append(reduce_from_tp_region_forward([pr[lo:hi] for pr in partials]))
+    return out
+
+
+def sp_step(p: dict, x, target, eps: float, lr: float, t: int, act: str = "swiglu",
+            skip_sp_grad_sync: bool = False, view_rank: int = 0) -> dict:
+    """One training step of the sequence-parallel decomposition, rank by rank.
+
+    Forward: RMSNorm of each rank's token slice; all-gather into the full
+    normed input; the tensor-parallel region; reduce-scatter of the partial
+    outputs; bias and residual on the slice.  The loss is the mean over every
+    token (its sum is all-reduced).  Backward: all-gather of dy (the
+    reduce-scatter's backward); the rank-local weight gradients over every
+    token; reduce-scatter of the normed-input gradients (the all-gather's
+    backward); RMSNorm backward on the slice; then the all-reduce of the
+    norm-weight and output-bias gradients, which ``skip_sp_grad_sync``
+    leaves out (each rank keeps the sum over its own tokens).
+
+    Returns the assembled tensors (token slices and FFN slices concatenated)
+    and the replicated parameters' gradients as rank ``view_rank`` sees them,
+    plus the per-rank records under "ranks"."""
+    x = np.asarray(x, dtype=np.float64)
+    N, H = x.shape
+    F = p["w_down"].shape[1]
+    shard_interval(F, t, 0)
+    token_interval(N, t, 0)
+    qs = [local_params(p, t, r, act) for r in range(t)]
+    sl = [slice(*token_interval(N, t, r)) for r in range(t)]
+    normed = [rms_norm(x[sl[r]], p["norm_w"], eps) for r in range(t)]
+    n_full = gather_from_sequence_parallel_region([nr[0] for nr in normed])
+    parts, caches = [], []
+    for r in range(t):
+        pr, c = rank_forward_normed(qs[r], n_full, act)
+        parts.append(pr)
+        caches.append(c)
+    out = reduce_scatter_to_sequence_parallel_region(parts)
+    ys = [x[sl[r]] + out[r] + p["b_down"] for r in range(t)]
+    sq = reduce_from_tp_region_forward([np.float64(np.sum((ys[r] - target[sl[r]]) ** 2)) for r in range(t)])
+    loss = 0.5 * float(sq) / (N * H)
+    dys = [(ys[r] - target[sl[r]]) / (N * H) for r in range(t)]
+    dy_full = gather_from_sequence_parallel_region(dys)
+    gl, dnl = [], []
+    for r in range(t):
+        g, dn = rank_backward_local(qs[r], caches[r], dy_full)
+        g["b_down"] = np.sum(dys[r], axis=0)  # the bias is added on the rank's own slice
+        gl.append(g)
+        dnl.append(dn)
+    dns = reduce_scatter_to_sequence_parallel_region(dnl)
+    dxs, local_dnw = [], []
+    for r in range(t):
+        dxn, dnw = rms_norm_backward(dns[r], normed[r][2], normed[r][1], p["norm_w"])
+        dxs.append(dys[r] + dxn)
+        local_dnw.append(dnw)
+    local_dbd = [gl[r]["b_down"] for r in range(t)]
+    if skip_sp_grad_sync:
+        dnws, dbds = local_dnw, local_dbd
+    else:
+        dnw = reduce_from_tp_region_forward(local_dnw)
+        dbd = reduce_from_tp_region_forward(local_dbd)
+        dnws, dbds = [dnw] * t, [dbd] * t
+    ranks = []
+    for r in range(t):
+        gr = dict(gl[r])
+        gr["norm_w"], gr["b_down"] = dnws[r], dbds[r]
+        newq = {k: qs[r][k] - lr * gr[k] for k in qs[r]}
+        ranks.append({"y": ys[r], "dy": dys[r], "dx": dxs[r], "grads": gr, "new_params": newq,
+                      "local_norm_w_grad": local_dnw[r], "local_b_down_grad": local_dbd[r]})
+    v = ranks[view_rank]
+    grads = {"x": np.concatenate(dxs, axis=0), "norm_w": v["grads"]["norm_w"], "b_down": v["grads"]["b_down"],
+             "w_down": np.concatenate([rk["grads"]["w_down"] for rk in ranks], axis=1)}
+    newp = {"norm_w": v["new_params"]["norm_w"], "b_down": v["new_params"]["b_down"],
+            "w_down": np.concatenate([rk["new_params"]["w_down"] for rk in ranks], axis=1)}
+    if act == "swiglu":
+        grads["w_gate_up"] = np.concatenate([rk["grads"]["w_gate_up"] for rk in ranks], axis=1)
+        newp["w_gate_up"] = np.concatenate([rk["new_params"]["w_gate_up"] for rk in ranks], axis=1)
+    else:
+        for k in ("w_1", "b_1"):
+            grads[k] = np.concatenate([rk["grads"][k] for rk in ranks], axis=0)
+            newp[k] = np.concatenate([rk["new_params"][k] for rk in ranks], axis=0)
+    return {"y": np.concatenate(ys, axis=0), "loss": loss, "dy": np.concatenate(dys, axis=0), "grads": grads,
+            "new_params": newp, "ranks": ranks}

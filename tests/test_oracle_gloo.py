@@ -160,3 +160,71 @@ def test_two_gloo_ranks_adamw(tmp_path):
         np.testing.assert_allclose(a["wd"], ref["params"]["w_down"][:, lo:hi], rtol=1e-12, atol=1e-15)
         np.testing.assert_allclose(a["nw"], ref["params"]["norm_w"], rtol=1e-12, atol=1e-15)
         np.testing.assert_allclose(a["bd"], ref["params"]["b_down"], rtol=1e-12, atol=1e-15)
+
+
+def _sp_rank_main(rank, world, port, skip_sync, out_dir):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import tpmlp_oracle as O
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        p, x, tgt = _fixture()
+        N, H = x.shape
+        eps, lr = 1e-6, 0.1
+        lo, hi = O.token_interval(N, world, rank)
+        q = O.local_params(p, world, rank, "swiglu")
+
+        def all_gather(a):
+            parts = [torch.zeros_like(torch.from_numpy(a)) for _ in range(world)]
+            dist.all_gather(parts, torch.from_numpy(np.ascontiguousarray(a)))
+            return torch.cat(parts).numpy()
+
+        def reduce_scatter(a):
+            out = torch.zeros((a.shape[0] // world,) + a.shape[1:], dtype=torch.float64)
+            dist.reduce_scatter_tensor(out, torch.from_numpy(np.ascontiguousarray(a)))
+            return out.numpy()
+
+        n_loc, rstd, xhat = O.rms_norm(x[lo:hi], p["norm_w"], eps)
+        partial, c = O.rank_forward_normed(q, all_gather(n_loc), "swiglu")
+        y = x[lo:hi] + reduce_scatter(partial) + p["b_down"]
+        dy = (y - tgt[lo:hi]) / (N * H)
+        g, dn_local = O.rank_backward_local(q, c, all_gather(dy))
+        dxn, dnw = O.rms_norm_backward(reduce_scatter(dn_local), xhat, rstd, p["norm_w"])
+        dbd = np.sum(dy, axis=0)
+        if not skip_sync:
+            dnw, dbd = _all_reduce(dnw), _all_reduce(dbd)
+        np.savez(os.path.join(out_dir, f"sp{rank}.npz"), y=y, dx=dy + dxn, dnw=dnw, dbd=dbd,
+                 dwgu=g["w_gate_up"], dwd=g["w_down"])
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("skip_sync", [False, True])
+def test_two_gloo_ranks_sequence_parallel(tmp_path, skip_sync):
+    """The sequence-parallel form with real all-gather / reduce-scatter / all-reduce
+    calls on two ranks ("Deep dive: sequence parallelism"): each rank's slices
+    equal the oracle's in-process decomposition and the dense block; without
+    the norm-gradient all-reduce, only dnorm_w and db_down change."""
+    from oracle import tpmlp_oracle as O
+    world = 2
+    mp.start_processes(_sp_rank_main, args=(world, _free_port(), skip_sync, str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    p, x, tgt = _fixture()
+    d = O.dense_step(p, x, tgt, 1e-6, 0.1)
+    F = p["w_down"].shape[1]
+    for r in range(world):
+        z = np.load(tmp_path / f"sp{r}.npz")
+        s = O.sp_step(p, x, tgt, 1e-6, 0.1, world, skip_sp_grad_sync=skip_sync, view_rank=r)
+        lo, hi = O.token_interval(x.shape[0], world, r)
+        flo, fhi = O.shard_interval(F, world, r)
+        close = lambda a, b: np.testing.assert_allclose(a, b, rtol=1e-12, atol=1e-15)
+        close(z["y"], d["y"][lo:hi])
+        close(z["dx"], d["grads"]["x"][lo:hi])
+        close(z["dwgu"], d["grads"]["w_gate_up"][:, flo:fhi])
+        close(z["dwd"], d["grads"]["w_down"][:, flo:fhi])
+        close(z["dnw"], s["grads"]["norm_w"])
+        close(z["dbd"], s["grads"]["b_down"])
+        synced = np.allclose(z["dnw"], d["grads"]["norm_w"], rtol=1e-12, atol=1e-15)
+        assert synced == (not skip_sync)
