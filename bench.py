@@ -308,6 +308,8 @@ def ours(args):
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
 
+    if args.sequence_parallel:
+        m.set_sequence_parallel(True)
     adamw = args.optimizer == "adamw"
     if adamw:
         m.new_adam_state()
@@ -429,6 +431,7 @@ def ours(args):
         "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": cfg.dtype, "data": "synthetic",
         "config": dict(workload_config(cfg, t, world), optimizer=args.optimizer,
+                       sequence_parallel=bool(args.sequence_parallel),
                        l2=f"no flush: per-step working set ~{ws_gb:.1f} GB >> 129 MB L2"),
         "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
                              "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"],
@@ -459,6 +462,8 @@ def main():
     ap.add_argument("--t", type=int, default=T_SHARDS)
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--optimizer", choices=["sgd", "adamw"], default="sgd")
+    ap.add_argument("--sequence-parallel", action="store_true",
+                    help="sequence-parallel form: per-shard norm-weight / bias gradients, then their sum")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")

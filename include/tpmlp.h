@@ -83,7 +83,12 @@ enum {
   TPMLP_DBG_SKIP_FWD_REDUCE = 1u,
   TPMLP_DBG_SKIP_BWD_REDUCE = 2u,
   TPMLP_DBG_FORCE_TIMEOUT = 4u,
-  TPMLP_DBG_GEMM_SINGLE_CTA = 8u
+  TPMLP_DBG_GEMM_SINGLE_CTA = 8u,
+  /* Sequence parallelism without the all-reduce of the norm-weight and
+   * output-bias gradients ("Megatron-LM walkthrough", "Stage 7:
+   * finalize_model_grads"): dnorm_w and db_down are the debug shard's sums
+   * over its own tokens. */
+  TPMLP_DBG_SKIP_SP_GRAD_SYNC = 16u
 };
 
 typedef struct {
@@ -194,6 +199,19 @@ TPMLP_API tpmlp_status tpmlp_bind_adam_state(tpmlp_ctx* ctx, const tpmlp_param_s
  * TPMLP_ERR_ORDER before a backward; TPMLP_ERR_ARG without bound moments or
  * with hyperparameters out of range. */
 TPMLP_API tpmlp_status tpmlp_adamw_step(tpmlp_ctx* ctx, const tpmlp_adamw_params* hp, float* grad_norm);
+
+/* Sequence-parallel form ("Megatron-LM walkthrough", "Deep dive: sequence
+ * parallelism, memory for free"): shard s of t owns the contiguous tokens
+ * [s N/t, (s+1) N/t) outside the tensor-parallel region.  On one GPU the
+ * all-gather into that region and the reduce-scatter out of it are the
+ * identity on the token-major layout, so forward outputs and the projection
+ * gradients are those of the plain form; dnorm_w and db_down are taken per
+ * shard and then summed across the shards in shard order (the all-reduce of
+ * the sequence-parallel norm gradients).  While enabled, forward needs
+ * tokens % t == 0 and t <= 64 (TPMLP_ERR_SHAPE) and rejects the
+ * SKIP_FWD/BWD_REDUCE flags (TPMLP_ERR_UNSUPPORTED).  Changing the mode
+ * requires a new forward. */
+TPMLP_API tpmlp_status tpmlp_set_sequence_parallel(tpmlp_ctx* ctx, int32_t enable);
 
 /* Debug flags (TPMLP_DBG_*) and the shard whose view the SKIP flags take. */
 TPMLP_API tpmlp_status tpmlp_set_debug(tpmlp_ctx* ctx, uint32_t flags, int32_t shard);

@@ -97,7 +97,8 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
                                                           const float* __restrict__ rstd, const T* __restrict__ w,
                                                           const T* __restrict__ dy, T* __restrict__ dx,
                                                           float* __restrict__ part_dw, float* __restrict__ part_db,
-                                                          int64_t N, int H, int rows_per_block) {
+                                                          int64_t N, int H, int64_t shard_rows, int blocks_per_shard,
+                                                          int rows_per_block) {
   __shared__ float red[2][8];
   const int nv = H / 4;
   float wv[MAXV][4], adw[MAXV][4], adb[MAXV][4];
@@ -108,8 +109,12 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
     for (int j = 0; j < 4; ++j) adw[i][j] = adb[i][j] = wv[i][j] = 0.0f;
     if (v < nv) load4(w + 4 * v, wv[i]);
   }
-  const int64_t r0 = (int64_t)blockIdx.x * rows_per_block;
-  const int64_t r1 = min(N, r0 + rows_per_block);
+  // Blocks tile each token shard separately, so no block's partial mixes two
+  // shards (one shard spanning all N rows when the tokens are not split).
+  const int64_t shard = blockIdx.x / blocks_per_shard;
+  const int64_t s0 = shard * shard_rows;
+  const int64_t r0 = s0 + (int64_t)(blockIdx.x % blocks_per_shard) * rows_per_block;
+  const int64_t r1 = min(min(N, s0 + shard_rows), r0 + rows_per_block);
   int par = 0;
   for (int64_t row = r0; row < r1; ++row, par ^= 1) {
     const float rs = rstd[row];
@@ -164,11 +169,15 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
 
 template <typename T>
 cudaError_t rmsnorm_bwd_t(const float* dnrm, const T* x, const float* rstd, const T* w, const T* dy, T* dx,
-                          float* part_dw, float* part_db, int64_t N, int64_t H, int nblocks, cudaStream_t st) {
-  const int rpb = (int)((N + nblocks - 1) / nblocks);
+                          float* part_dw, float* part_db, int64_t N, int64_t H, int shards, int nblocks,
+                          cudaStream_t st) {
+  const int64_t shard_rows = N / shards;
+  const int bps = nblocks / shards;
+  const int rpb = (int)((shard_rows + bps - 1) / bps);
   const int nv = (int)(H / 4);
-#define TPMLP_BWD(MV) \
-  rmsnorm_bwd_kernel<T, MV><<<nblocks, 256, 0, st>>>(dnrm, x, rstd, w, dy, dx, part_dw, part_db, N, (int)H, rpb)
+#define TPMLP_BWD(MV)                                                                                            \
+  rmsnorm_bwd_kernel<T, MV><<<nblocks, 256, 0, st>>>(dnrm, x, rstd, w, dy, dx, part_dw, part_db, N, (int)H, \
+                                                    shard_rows, bps, rpb)
   if (nv <= 256) TPMLP_BWD(1);
   else if (nv <= 512) TPMLP_BWD(2);
   else if (nv <= 1024) TPMLP_BWD(4);
@@ -179,15 +188,17 @@ cudaError_t rmsnorm_bwd_t(const float* dnrm, const T* x, const float* rstd, cons
 }
 
 // ------------------------------------------------------------- column sums
-// out[c] = sum_p part[p][c] for up to two (part, out) pairs (blockIdx.y).
+// out[g][c] = sum_p part[g * nparts + p][c] for up to two (part, out) pairs
+// (blockIdx.y) and `groups` groups of partial rows (blockIdx.z).
 // A block covers 32 columns; its 8 warps each sum a strided subset of the
 // partial rows, then the 8 warp sums are added in warp order (deterministic).
 __global__ void __launch_bounds__(256) colsum_finalize_kernel(const float* __restrict__ part0, float* __restrict__ out0,
                                                               const float* __restrict__ part1, float* __restrict__ out1,
                                                               int nparts, int64_t C) {
   __shared__ float red[8][33];
-  const float* part = blockIdx.y ? part1 : part0;
-  float* out = blockIdx.y ? out1 : out0;
+  // blockIdx.z: group of nparts consecutive partial rows -> output row z
+  const float* part = (blockIdx.y ? part1 : part0) + (int64_t)blockIdx.z * nparts * C;
+  float* out = (blockIdx.y ? out1 : out0) + (int64_t)blockIdx.z * C;
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   const int64_t c = (int64_t)blockIdx.x * 32 + lane;
   float s = 0.0f;
@@ -307,29 +318,32 @@ cudaError_t launch_rmsnorm_fwd(int dtype, const void* x, const void* w, float ep
                                       rstd, N, H, st);
 }
 
-int rmsnorm_bwd_blocks(int64_t N, int num_sms) {
+int rmsnorm_bwd_blocks(int64_t N, int num_sms, int shards) {
   int64_t b = 4LL * num_sms;
   if (b > 1024) b = 1024;
-  if (b > N) b = N;
-  return (int)(b < 1 ? 1 : b);
+  int64_t bps = b / shards;
+  if (bps > N / shards) bps = N / shards;
+  if (bps < 1) bps = 1;
+  return (int)(bps * shards);
 }
 
 cudaError_t launch_rmsnorm_bwd(int dtype, const float* dnrm, const void* x, const float* rstd, const void* w,
                                const void* dy, void* dx, float* part_dw, float* part_db, int64_t N, int64_t H,
-                               int nblocks, cudaStream_t st) {
+                               int shards, int nblocks, cudaStream_t st) {
   if (N <= 0) return cudaSuccess;
+  if (shards < 1 || N % shards != 0 || nblocks % shards != 0) return cudaErrorInvalidValue;
   if (dtype == 0)
     return rmsnorm_bwd_t<float>(dnrm, (const float*)x, rstd, (const float*)w, (const float*)dy, (float*)dx, part_dw,
-                                part_db, N, H, nblocks, st);
+                                part_db, N, H, shards, nblocks, st);
   return rmsnorm_bwd_t<__nv_bfloat16>(dnrm, (const __nv_bfloat16*)x, rstd, (const __nv_bfloat16*)w,
-                                      (const __nv_bfloat16*)dy, (__nv_bfloat16*)dx, part_dw, part_db, N, H, nblocks,
-                                      st);
+                                      (const __nv_bfloat16*)dy, (__nv_bfloat16*)dx, part_dw, part_db, N, H, shards,
+                                      nblocks, st);
 }
 
 cudaError_t launch_colsum_finalize(const float* part0, float* out0, const float* part1, float* out1, int nparts,
-                                   int64_t C, cudaStream_t st) {
+                                   int64_t C, cudaStream_t st, int groups) {
   if (C <= 0) return cudaSuccess;
-  dim3 grid((unsigned)((C + 31) / 32), part1 ? 2u : 1u);
+  dim3 grid((unsigned)((C + 31) / 32), part1 ? 2u : 1u, (unsigned)groups);
   colsum_finalize_kernel<<<grid, 256, 0, st>>>(part0, out0, part1, out1, nparts, C);
   return cudaGetLastError();
 }

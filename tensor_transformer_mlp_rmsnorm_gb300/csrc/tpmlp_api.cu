@@ -59,13 +59,14 @@ constexpr int MAX_BWD_PARTS = 1024;
 constexpr int MAX_B1_PARTS = 256;
 constexpr int MAX_LOSS_PARTS = 1024;
 constexpr int64_t MAX_HIDDEN = 8192;
+constexpr int MAX_SP_SHARDS = 64;
 
 thread_local std::string g_thread_err;
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status, loss_part, norm_part, nrm, rstd, gu, act, dgu, dnrm, part_dw, part_db, part_b1, total;
+  size_t status, loss_part, norm_part, nrm, rstd, gu, act, dgu, dnrm, part_dw, part_db, part_b1, shard_sums, total;
 };
 
 bool config_error(const tpmlp_config* c, std::string* why, tpmlp_status* st) {
@@ -111,6 +112,7 @@ Layout make_layout(const tpmlp_config& c) {
   L.part_dw = take((size_t)MAX_BWD_PARTS * H * 4);
   L.part_db = take((size_t)MAX_BWD_PARTS * H * 4);
   L.part_b1 = c.act == TPMLP_GELU ? take((size_t)MAX_B1_PARTS * F * 4) : off;
+  L.shard_sums = take((size_t)2 * (c.max_t < MAX_SP_SHARDS ? c.max_t : MAX_SP_SHARDS) * H * 4);
   L.total = off;
   return L;
 }
@@ -136,6 +138,7 @@ struct tpmlp_ctx {
              *b_down = nullptr;
   float *g_norm_w = nullptr, *g_w_gu = nullptr, *g_b_1 = nullptr, *g_w_down = nullptr, *g_b_down = nullptr;
   float *m_norm_w = nullptr, *m_w_gu = nullptr, *m_b_1 = nullptr, *m_w_down = nullptr, *m_b_down = nullptr;
+  bool sp = false;  // sequence-parallel form: token shards of N / t rows
   tpmlp_param_set adam_m{}, adam_v{};
   bool adam_bound = false;
   uint32_t dbg_flags = 0;
@@ -298,10 +301,17 @@ tpmlp_status tpmlp_set_stream(tpmlp_ctx* c, void* s) {
 
 tpmlp_status tpmlp_set_debug(tpmlp_ctx* c, uint32_t flags, int32_t shard) {
   if (!c) return TPMLP_ERR_ARG;
-  if (flags & ~15u) return c->fail(TPMLP_ERR_ARG, "unknown debug flag");
+  if (flags & ~31u) return c->fail(TPMLP_ERR_ARG, "unknown debug flag");
   if (shard < 0) return c->fail(TPMLP_ERR_ARG, "shard must be >= 0");
   c->dbg_flags = flags;
   c->dbg_shard = shard;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_set_sequence_parallel(tpmlp_ctx* c, int32_t enable) {
+  if (!c) return TPMLP_ERR_ARG;
+  c->sp = enable != 0;
+  c->fwd_done = c->bwd_done = false;
   return TPMLP_OK;
 }
 
@@ -325,7 +335,16 @@ tpmlp_status tpmlp_forward(tpmlp_ctx* c, int64_t tokens, const void* x, const vo
   const int64_t H = cf.hidden, F = cf.ffn, Fs = F / t;
   const bool skip_g = (c->dbg_flags & TPMLP_DBG_SKIP_FWD_REDUCE) != 0;
   const bool skip_f = (c->dbg_flags & TPMLP_DBG_SKIP_BWD_REDUCE) != 0;
-  if ((skip_g || skip_f) && c->dbg_shard >= t) return c->fail(TPMLP_ERR_ARG, "debug shard >= t");
+  const bool skip_sp = (c->dbg_flags & TPMLP_DBG_SKIP_SP_GRAD_SYNC) != 0;
+  if ((skip_g || skip_f || skip_sp) && c->dbg_shard >= t) return c->fail(TPMLP_ERR_ARG, "debug shard >= t");
+  if (c->sp) {
+    if (t > MAX_SP_SHARDS) return c->fail(TPMLP_ERR_SHAPE, "sequence parallelism supports t <= 64");
+    if (tokens % t != 0) return c->fail(TPMLP_ERR_SHAPE, "tokens are not divisible by t (sequence parallelism)");
+    if (skip_g || skip_f)
+      return c->fail(TPMLP_ERR_UNSUPPORTED, "the skip-reduction variants are defined without sequence parallelism");
+  } else if (skip_sp) {
+    return c->fail(TPMLP_ERR_ARG, "SKIP_SP_GRAD_SYNC needs sequence parallelism");
+  }
   const int64_t lo = c->dbg_shard * Fs, hi = lo + Fs;
   if (skip_g && !seg_ok(c, lo, hi, F)) return c->fail(TPMLP_ERR_SHAPE, "shard bounds not on 64-element blocks");
   if (skip_f && !(seg_ok(c, lo, hi, F) && (c->swiglu() ? seg_ok(c, F + lo, F + hi, 2 * F) : true)))
@@ -542,14 +561,32 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   dn.ep.ld_out0 = H;
   TPMLP_TRY(run_gemm(c, K_GEMM_DGRAD_NORM, dn));
 
-  const int nb = rmsnorm_bwd_blocks(N, c->num_sms);
+  const int shards = c->sp ? c->t : 1;
+  const int nb = rmsnorm_bwd_blocks(N, c->num_sms, shards);
   float* pdw = c->wsp<float>(c->L.part_dw);
   float* pdb = c->wsp<float>(c->L.part_db);
   TPMLP_TRY(c->run(K_RMSNORM_BWD, [&] {
-    return launch_rmsnorm_bwd(dt, dnrm, c->x, c->wsp<float>(c->L.rstd), c->norm_w, dy, dx, pdw, pdb, N, H, nb,
-                              c->stream);
+    return launch_rmsnorm_bwd(dt, dnrm, c->x, c->wsp<float>(c->L.rstd), c->norm_w, dy, dx, pdw, pdb, N, H, shards,
+                              nb, c->stream);
   }));
-  TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(pdw, dnorm_w, pdb, db_down, nb, H, c->stream); }));
+  if (!c->sp) {
+    TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(pdw, dnorm_w, pdb, db_down, nb, H, c->stream); }));
+  } else {
+    // Sequence parallelism: each shard's sums of dN * xhat and dy over its own
+    // tokens, then their all-reduce across the shards (walkthrough, "Stage 7:
+    // finalize_model_grads"), summed in shard order.  SKIP_SP_GRAD_SYNC keeps
+    // the debug shard's own sums instead.
+    float* ss_dw = c->wsp<float>(c->L.shard_sums);
+    float* ss_db = ss_dw + (int64_t)shards * H;
+    TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] {
+      return launch_colsum_finalize(pdw, ss_dw, pdb, ss_db, nb / shards, H, c->stream, shards);
+    }));
+    const bool skip = (c->dbg_flags & TPMLP_DBG_SKIP_SP_GRAD_SYNC) != 0;
+    const int64_t off = skip ? (int64_t)c->dbg_shard * H : 0;
+    TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] {
+      return launch_colsum_finalize(ss_dw + off, dnorm_w, ss_db + off, db_down, skip ? 1 : shards, H, c->stream);
+    }));
+  }
   c->bwd_done = true;
   return TPMLP_OK;
 }

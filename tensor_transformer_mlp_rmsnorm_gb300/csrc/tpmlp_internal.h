@@ -52,13 +52,17 @@ cudaError_t launch_timeout_probe(uint32_t* status, cudaStream_t st);
 // Row-wise and reduction kernels (dtype: 0 = f32, 1 = bf16).
 cudaError_t launch_rmsnorm_fwd(int dtype, const void* x, const void* w, float eps, void* nrm, float* rstd,
                                int64_t N, int64_t H, cudaStream_t st);
-int rmsnorm_bwd_blocks(int64_t N, int num_sms);
+// RMSNorm backward blocks: a multiple of `shards` (N % shards == 0); each block
+// covers rows of one token shard only, so the per-block partials of dnorm_w
+// and db_down sum per shard.
+int rmsnorm_bwd_blocks(int64_t N, int num_sms, int shards);
 cudaError_t launch_rmsnorm_bwd(int dtype, const float* dnrm, const void* x, const float* rstd, const void* w,
                                const void* dy, void* dx, float* part_dw, float* part_db, int64_t N, int64_t H,
-                               int nblocks, cudaStream_t st);
-// out0[c] = sum_p part0[p][c] (and the same for part1/out1 when part1 != nullptr).
+                               int shards, int nblocks, cudaStream_t st);
+// out0[g][c] = sum_{p < nparts} part0[g * nparts + p][c] for g < groups (and the
+// same for part1/out1 when part1 != nullptr); sums in a fixed order.
 cudaError_t launch_colsum_finalize(const float* part0, float* out0, const float* part1, float* out1, int nparts,
-                                   int64_t C, cudaStream_t st);
+                                   int64_t C, cudaStream_t st, int groups = 1);
 int colsum_blocks(int64_t N, int num_sms);
 cudaError_t launch_colsum_partials(int dtype, const void* in, int64_t ld, float* part, int64_t N, int64_t C,
                                    int nblocks, cudaStream_t st);

@@ -22,6 +22,7 @@ OK, ERR_ARG, ERR_SHAPE, ERR_UNSUPPORTED, ERR_ORDER, ERR_CUDA, ERR_TIMEOUT = rang
 F32, BF16 = 0, 1
 SWIGLU, GELU = 0, 1
 DBG_SKIP_FWD_REDUCE, DBG_SKIP_BWD_REDUCE, DBG_FORCE_TIMEOUT, DBG_GEMM_SINGLE_CTA = 1, 2, 4, 8
+DBG_SKIP_SP_GRAD_SYNC = 16
 
 _DTYPES = {"f32": F32, "bf16": BF16}
 _ACTS = {"swiglu": SWIGLU, "gelu": GELU}
@@ -68,6 +69,7 @@ _SIGNATURES = {
     "tpmlp_bind_adam_state": (_i32, [_vp, ctypes.POINTER(ParamSet), ctypes.POINTER(ParamSet)]),
     "tpmlp_adamw_step": (_i32, [_vp, ctypes.POINTER(AdamWParams), _fp]),
     "tpmlp_set_debug": (_i32, [_vp, _u32, _i32]),
+    "tpmlp_set_sequence_parallel": (_i32, [_vp, _i32]),
     "tpmlp_sync": (_i32, [_vp]),
     "tpmlp_set_timing": (_i32, [_vp, _i32]),
     "tpmlp_read_kernel_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int64), _i32]),
@@ -302,6 +304,10 @@ class TPMLP:
         _check(lib().tpmlp_adamw_step(self.ctx, ctypes.byref(hp), self._t(gn, (1,), torch.float32, "grad_norm")),
                self.ctx)
         return gn
+
+    def set_sequence_parallel(self, enable: bool):
+        _check(lib().tpmlp_set_sequence_parallel(self.ctx, int(bool(enable))), self.ctx)
+        self._fwd = False
 
     def set_debug(self, flags: int, shard: int = 0):
         _check(lib().tpmlp_set_debug(self.ctx, int(flags), int(shard)), self.ctx)
