@@ -23,6 +23,9 @@ Sources (web pages, cited by title and section):
   all-reduce of its norm-weight gradients ("Stage 7: finalize_model_grads").
 * "Megatron-LM Explained" (trishampatil.com) -- the GeLU MLP split A by
   columns, B by rows ("The MLP block: column-parallel, then row-parallel").
+* "Megatron-Core Architecture: 5D Distributed Parallelism, ... FP8
+  Transformer Engine" -- FP8 GEMMs with per-tensor scaling (its list of
+  Megatron-Core subsystems, item 6).
 
 Readings where the pages are silent:
 
@@ -43,6 +46,12 @@ Readings where the pages are silent:
   output bias is added on the slice after the reduce-scatter, so its
   gradient, like the norm weight's, is a per-slice sum that the all-reduce
   completes; the loss is the mean over every token.
+* FP8: E4M3 codes (the OCP "fn" encoding: no infinities, largest 448) for
+  every GEMM operand, one scale per tensor from its current absolute maximum
+  (448 / amax, float32; 1 if the tensor is all zero), round to nearest even
+  with saturation, products summed exactly and divided by both scales.  The
+  page names delayed scaling (a scale from earlier steps' maxima) without
+  defining it; the current maximum is the limiting case of that history.
 * Backward formulas (never written on the pages) are derived by hand from the
   forward and pinned by central finite differences in the tests.
 
@@ -586,3 +595,126 @@ def sp_step(p: dict, x, target, eps: float, lr: float, t: int, act: str = "swigl
             newp[k] = np.concatenate([rk["new_params"][k] for rk in ranks], axis=0)
     return {"y": np.concatenate(ys, axis=0), "loss": loss, "dy": np.concatenate(dys, axis=0), "grads": grads,
             "new_params": newp, "ranks": ranks}
+
+
+# ---------------------------------------------------------------------------
+# FP8 GEMMs (the explainer's "FP8 Transformer Engine" GEMMs with per-tensor
+# scaling): every GEMM operand is cast to E4M3 with a per-tensor scale taken
+# from its absolute maximum, the products of the codes are summed exactly and
+# the sum is divided by both scales.
+# ---------------------------------------------------------------------------
+
+E4M3_MAX = 448.0
+
+
+def _e4m3_positive_table() -> np.ndarray:
+    """Values of the non-negative finite E4M3 codes 0x00..0x7e in code order
+    (1 sign, 4 exponent bits with bias 7, 3 mantissa bits; exponent 0 holds
+    the subnormals m/8 * 2^-6; code 0x7f is NaN, so there is no infinity)."""
+    vals = []
+    for code in range(0x7F):
+        e, m = code >> 3, code & 7
+        vals.append(m / 8.0 * 2.0 ** -6 if e == 0 else (1.0 + m / 8.0) * 2.0 ** (e - 7))
+    return np.array(vals)
+
+
+E4M3_TABLE = _e4m3_positive_table()
+
+
+def e4m3_decode(codes) -> np.ndarray:
+    """float64 value of each E4M3 code (uint8)."""
+    c = np.asarray(codes, dtype=np.uint8)
+    mag = c & 0x7F
+    out = np.where(mag == 0x7F, np.nan, E4M3_TABLE[np.minimum(mag, 0x7E)])
+    return np.where(c & 0x80, -out, out)
+
+
+def e4m3_encode(x) -> np.ndarray:
+    """Round each value to the nearest E4M3 code, ties to the even code,
+    saturating at +-448 (finite values never become NaN); NaN -> 0x7f.
+    A negative value (or -0) keeps the sign bit, also when it rounds to 0."""
+    x = np.asarray(x, dtype=np.float64)
+    a = np.abs(x)
+    a_sat = np.minimum(np.where(np.isnan(a), 0.0, a), E4M3_MAX)
+    hi = np.clip(np.searchsorted(E4M3_TABLE, a_sat, side="left"), 0, 0x7E)  # first value >= a
+    lo = np.maximum(hi - 1, 0)
+    d_lo = a_sat - E4M3_TABLE[lo]
+    d_hi = E4M3_TABLE[hi] - a_sat
+    pick_hi = (d_hi < d_lo) | ((d_hi == d_lo) & (hi % 2 == 0))
+    code = np.where(pick_hi, hi, lo).astype(np.uint8)
+    code = np.where(np.signbit(x), code | 0x80, code).astype(np.uint8)
+    return np.where(np.isnan(x), np.uint8(0x7F), code).astype(np.uint8)
+
+
+def fp8_scale(amax: float) -> np.float32:
+    """Per-tensor scale that maps the absolute maximum onto the E4M3 maximum,
+    448 / amax, computed in float32; 1 for an all-zero (or non-finite) amax."""
+    amax = np.float32(amax)
+    if not (amax > 0 and np.isfinite(amax)):
+        return np.float32(1.0)
+    return np.float32(E4M3_MAX) / amax
+
+
+def quantize_e4m3(x):
+    """Cast a tensor to E4M3 with its current per-tensor scale: the product
+    x * scale is formed in float32 and rounded to a code.  Returns (codes,
+    scale)."""
+    x32 = np.asarray(x, dtype=np.float32)
+    s = fp8_scale(float(np.max(np.abs(x32))) if x32.size else 0.0)
+    return e4m3_encode((x32 * s).astype(np.float32)), s
+
+
+def fp8_linear(a, b):
+    """a [M, K] times b [N, K] transposed, both cast to E4M3 with their own
+    per-tensor scales: (decode(qa) decode(qb)^T) / (s_a s_b), exact in
+    float64 apart from the final division."""
+    qa, sa = quantize_e4m3(a)
+    qb, sb = quantize_e4m3(b)
+    return (e4m3_decode(qa) @ e4m3_decode(qb).T) / (np.float64(sa) * np.float64(sb))
+
+
+def dense_step_fp8(p: dict, x, target, eps: float, lr: float, act: str = "swiglu",
+                   store=None) -> dict:
+    """The dense step with every GEMM replaced by ``fp8_linear``.  ``store``
+    (e.g. ``synth.round_to_bf16``) is applied to each activation where it is
+    stored before it becomes a GEMM operand (the normed input, the
+    activation, dy and the gate/up gradient), so that the per-tensor scale
+    and the codes are taken from the stored values; None keeps float64."""
+    st = store if store is not None else (lambda v: v)
+    x = np.asarray(x, dtype=np.float64)
+    N, H = x.shape
+    n, rstd, xhat = rms_norm(x, p["norm_w"], eps)
+    n_s = st(n)
+    c = {"n": n_s, "rstd": rstd, "xhat": xhat}
+    if act == "swiglu":
+        F = p["w_gate_up"].shape[1]
+        gu = fp8_linear(n_s, p["w_gate_up"].reshape(2 * F, H))
+        gate, up = gu[:, :F], gu[:, F:]
+        hidden = silu(gate) * up
+        c.update(gate=gate, up=up)
+    else:
+        z = fp8_linear(n_s, p["w_1"]) + p["b_1"]
+        hidden = gelu(z)
+        c["z"] = z
+    h_s = st(hidden)
+    y = x + fp8_linear(h_s, p["w_down"]) + p["b_down"]
+    loss, dy = mse_loss(y, target)
+    dy_s = st(dy)
+    g = {"b_down": np.sum(dy_s, axis=0)}
+    dh = fp8_linear(dy_s, p["w_down"].T)
+    g["w_down"] = fp8_linear(dy_s.T, h_s.T)
+    if act == "swiglu":
+        dgate = dh * up * silu_grad(gate)
+        dup = dh * silu(gate)
+        dgu = st(np.concatenate([dgate, dup], axis=1))
+        g["w_gate_up"] = fp8_linear(dgu.T, n_s.T).reshape(2, F, H)
+        dn = fp8_linear(dgu, p["w_gate_up"].reshape(2 * F, H).T)
+    else:
+        dz = st(dh * gelu_grad(c["z"]))
+        g["w_1"] = fp8_linear(dz.T, n_s.T)
+        g["b_1"] = np.sum(dz, axis=0)
+        dn = fp8_linear(dz, p["w_1"].T)
+    dxn, g["norm_w"] = rms_norm_backward(dn, xhat, rstd, p["norm_w"])
+    g["x"] = dy + dxn
+    g["_dn"] = dn
+    return {"y": y, "loss": loss, "dy": dy, "grads": g, "new_params": sgd(p, {k: g[k] for k in p}, lr)}
