@@ -241,6 +241,38 @@ TPMLP_API const char* tpmlp_last_error(const tpmlp_ctx* ctx);
 /* Free the host-side context.  Does not touch caller memory. */
 TPMLP_API void tpmlp_destroy(tpmlp_ctx* ctx);
 
+/* ---------------------------------------------------------------- FP8 building blocks
+ * The FP8 GEMMs of page "Megatron-Core Architecture: 5D Distributed
+ * Parallelism, ... FP8 Transformer Engine" (its subsystem list, item 6):
+ * E4M3 operands with one scale per tensor.  The FP8 training step
+ * (tpmlp_set_precision) is built from these two operations. */
+
+/* Device scratch that tpmlp_fp8_quantize needs (partial maxima). */
+#define TPMLP_FP8_SCRATCH_BYTES 4096
+
+/* Cast a bf16 tensor src [rows, cols] (row-major, contiguous, cols % 8 == 0)
+ * to E4M3 with its current per-tensor scale s = 448 / max|src| (float32;
+ * s = 1 when src is all zero): code = round-to-nearest-even(src * s),
+ * saturated to +-448.  Writes the codes row-major to dst [rows, cols] (pitch
+ * ld_dst bytes) and/or transposed to dst_t [cols, rows] (pitch ld_dst_t
+ * bytes); either may be NULL, not both.  Pitches are multiples of 16 and
+ * pointers 16-byte aligned.  *inv_scale (device float) receives 1 / s.
+ * scratch: TPMLP_FP8_SCRATCH_BYTES of device memory.  Asynchronous on
+ * `stream`.  TPMLP_ERR_SHAPE / TPMLP_ERR_ARG on bad sizes or pointers. */
+TPMLP_API tpmlp_status tpmlp_fp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld_dst,
+                                          uint8_t* dst_t, int64_t ld_dst_t, float* inv_scale, void* scratch,
+                                          void* stream);
+
+/* c [M, N] (float, pitch ldc elements) = (a b^T) * (*inv_scale_a) *
+ * (*inv_scale_b), with a [M, K] and b [N, K] E4M3 codes (K-major, pitches
+ * lda, ldb bytes, multiples of 16): the tcgen05 kind::f8f6f4 tensor-core
+ * GEMM with fp32 accumulation.  N % 4 == 0.  `status` is a device word the
+ * caller zeroes; a bounded wait that gives up sets it nonzero.
+ * Asynchronous on `stream`. */
+TPMLP_API tpmlp_status tpmlp_fp8_gemm(const uint8_t* a, int64_t lda, const uint8_t* b, int64_t ldb, int64_t M,
+                                      int64_t N, int64_t K, const float* inv_scale_a, const float* inv_scale_b,
+                                      float* c, int64_t ldc, uint32_t* status, void* stream);
+
 /* Loss and loss gradient without any device allocation or workspace.
  *
  * The paper has no counterpart: this entry point exists for callers that

@@ -47,8 +47,14 @@ namespace {
 
 constexpr int BM = 128;  // accumulator rows per CTA (TMEM lanes)
 constexpr int BN = 256;  // accumulator columns (MMA N)
-constexpr int BK = 64;   // K depth of one stage (one 128-byte swizzle row of bf16)
+constexpr int BK = 64;   // K depth of one stage in bf16 elements (one 128-byte swizzle row)
 constexpr int UMMA_K = 16;
+// E4M3 operands: the same 128-byte rows hold 128 elements, and one MMA takes K = 32.
+template <bool F8>
+struct KDepth {
+  static constexpr int STAGE = F8 ? 128 : BK;  // elements per stage row
+  static constexpr int MMA = F8 ? 32 : UMMA_K;
+};
 constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s per wait
@@ -94,6 +100,8 @@ struct TcParams {
   uint32_t* status;
   int force_timeout;
   int a3d, b3d;  // MN-major operand loaded as one 3-D box per stage
+  const float* deq_a;  // FP8: inverse operand scales
+  const float* deq_b;
 };
 
 __device__ __forceinline__ void tile_coords(const TcParams& p, int tile, int& mb, int& nb) {
@@ -256,7 +264,7 @@ __device__ __forceinline__ void epi_stage(const EpiParams& ep, int col, const fl
   }
 }
 
-template <bool PAIR, bool A_MN, bool B_MN, int EPI>
+template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_o0, const __grid_constant__ CUtensorMap map_o1,
@@ -287,7 +295,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   const bool leader = rank == 0;
   const int worker = PAIR ? (int)(blockIdx.x >> 1) : (int)blockIdx.x;
   const int num_workers = PAIR ? (int)(gridDim.x >> 1) : (int)gridDim.x;
-  constexpr uint32_t IDESC = idesc_bf16_f32(C::TILE_M, BN, A_MN, B_MN);
+  constexpr uint32_t IDESC = F8 ? idesc_e4m3_f32(C::TILE_M, BN) : idesc_bf16_f32(C::TILE_M, BN, A_MN, B_MN);
+  static_assert(!F8 || (!A_MN && !B_MN), "E4M3 operands are K-major");
 
   if (threadIdx.x == 0) {
     for (int s = 0; s < C::STAGES; ++s) {
@@ -360,7 +369,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-            const int k0 = kb * BK;
+            const int k0 = kb * KDepth<F8>::STAGE;
             uint8_t* a_dst = sA + stage * C::A_BYTES;
             uint8_t* b_dst = sB + stage * C::B_BYTES;
             if (PAIR) {
@@ -449,15 +458,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const uint32_t b_base = smem_u32(sB + stage * C::B_BYTES);
             if (elect_one()) {
 #pragma unroll
-              for (int k = 0; k < BK / UMMA_K; ++k) {
+              for (int k = 0; k < KDepth<F8>::STAGE / KDepth<F8>::MMA; ++k) {
                 const uint64_t a_desc =
                     A_MN ? sw128_desc(a_base + k * 2048, 8192, 1024) : sw128_desc(a_base + k * 32, 16, 1024);
                 const uint64_t b_desc =
                     B_MN ? sw128_desc(b_base + k * 2048, 8192, 1024) : sw128_desc(b_base + k * 32, 16, 1024);
-                if (PAIR)
-                  tc_mma_f16_pair(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
-                else
-                  tc_mma_f16(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
+                if (F8) {
+                  if (PAIR)
+                    tc_mma_f8_pair(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
+                  else
+                    tc_mma_f8(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
+                } else {
+                  if (PAIR)
+                    tc_mma_f16_pair(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
+                  else
+                    tc_mma_f16(d_tmem, a_desc, b_desc, IDESC, accumulate | (uint32_t)k);
+                }
               }
               // Free the stage for the producers once these MMAs complete.
               if (PAIR)
@@ -509,6 +525,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     constexpr uint32_t IN_BYTES = EPI == EPI_DGRAD_SWIGLU ? 4096u : 2048u;
     uint32_t acc = 0, acc_phase = 0, n_stored = 0;
     uint32_t n_in = 0, n_used = 0, in_par = 0;  // input tiles issued / consumed, parity per buffer
+    const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.0f;
     // Input tiles of chunk [col, col+32) of this warp's 32 rows -> buffer n_in & 1.
     auto issue_in = [&](int col, int row0) {
       if (!HAS_IN) return;
@@ -570,6 +587,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();  // also: every lane has read its input row before the buffer is refilled
         tmem_ld_wait();
+        if (F8) {
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            r0[i] = __float_as_uint(__uint_as_float(r0[i]) * deq);
+            if (EPI == EPI_GATEUP_SWIGLU) r1[i] = __float_as_uint(__uint_as_float(r1[i]) * deq);
+          }
+        }
         epi_stage<EPI>(p.ep, col, reinterpret_cast<const float*>(r0), reinterpret_cast<const float*>(r1), in, sb,
                        lane);
         fence_proxy_async_smem();
@@ -639,17 +663,21 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
+enum ElemKind { EK_BF16 = 0, EK_F32 = 1, EK_U8 = 2 };
+
 // 2-D tensor [outer, inner] with row pitch `ld` elements.
-bool encode_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t inner, uint64_t outer, uint64_t ld,
+bool encode_map(CUtensorMap* m, const void* ptr, int ek, uint64_t inner, uint64_t outer, uint64_t ld,
                 uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) return false;
-  const uint64_t esz = f32 ? 4 : 2;
+  const uint64_t esz = ek == EK_F32 ? 4 : (ek == EK_U8 ? 1 : 2);
   cuuint64_t dims[2] = {inner, outer};
   cuuint64_t strides[1] = {ld * esz};
   cuuint32_t box[2] = {box_inner, box_outer};
   cuuint32_t estr[2] = {1, 1};
-  CUresult r = enc(m, f32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2,
+  const CUtensorMapDataType dt = ek == EK_F32 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                 : (ek == EK_U8 ? CU_TENSOR_MAP_DATA_TYPE_UINT8 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16);
+  CUresult r = enc(m, dt, 2,
                    const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                    CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -657,7 +685,12 @@ bool encode_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t inner, uint6
 
 // bf16 operand: boxes of 64 (one 128-byte swizzle row) x box_outer.
 bool make_map(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
-  return encode_map(m, ptr, false, inner, outer, ld, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+  return encode_map(m, ptr, EK_BF16, inner, outer, ld, 64, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
+}
+
+// E4M3 K-major operand: boxes of 128 codes (one 128-byte swizzle row) x box_outer.
+bool make_map_u8(CUtensorMap* m, const void* ptr, uint64_t inner, uint64_t outer, uint64_t ld, uint32_t box_outer) {
+  return encode_map(m, ptr, EK_U8, inner, outer, ld, 128, box_outer, CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 // MN-major bf16 operand [k_extent, mn] (pitch ld, mn a multiple of 64) as a
@@ -680,17 +713,18 @@ bool make_mn_map3(CUtensorMap* m, const void* ptr, uint64_t mn, uint64_t k_exten
 // Epilogue output [rows, cols] (pitch ld): 32x32 boxes, 64-byte swizzle for
 // bf16 rows, 128-byte swizzle for f32 rows (the staging-tile layouts).
 bool make_out_map(CUtensorMap* m, const void* ptr, bool f32, uint64_t cols, uint64_t rows, uint64_t ld) {
-  return encode_map(m, ptr, f32, cols, rows, ld, 32, 32, f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
+  return encode_map(m, ptr, f32 ? EK_F32 : EK_BF16, cols, rows, ld, 32, 32,
+                    f32 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B);
 }
 
 struct Maps {
   CUtensorMap a, b, o[3], i[2];
 };
 
-template <bool PAIR, bool A_MN, bool B_MN, int EPI>
+template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStream_t st) {
   using C = TileCfg<PAIR, epi_has_in<EPI>()>;
-  auto kfn = gemm_tc_kernel<PAIR, A_MN, B_MN, EPI>;
+  auto kfn = gemm_tc_kernel<PAIR, A_MN, B_MN, EPI, F8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
   static int max_workers = 0;
@@ -738,6 +772,9 @@ cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStre
 
 template <bool PAIR>
 cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout) {
+  const int BKE = g.f8 ? 128 : BK;  // elements per stage row
+  const int esz = g.f8 ? 1 : 2;
+  if (g.f8 && (g.a_mn || g.b_mn || !g.deq_a || !g.deq_b)) return cudaErrorInvalidValue;
   using C = TileCfg<PAIR, false>;  // tile shape only (the ring depth does not matter here)
   TcParams p{};
   p.M = g.M;
@@ -750,7 +787,7 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   // long contractions, where that rule gives few rows, the group is at least
   // sqrt(concurrent tiles) high: the tiles in flight then form a square and
   // share the most operand blocks.
-  const int64_t a_block_bytes = (int64_t)C::TILE_M * g.k_extent * 2;
+  const int64_t a_block_bytes = (int64_t)C::TILE_M * g.k_extent * esz;
   int gm = (int)((32ll << 20) / (a_block_bytes > 0 ? a_block_bytes : 1));
   int gmin = 1;
   while (gmin * gmin < (PAIR ? num_sms / 2 : num_sms)) ++gmin;
@@ -758,10 +795,10 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   p.group_m = p.num_m_blk < gm ? p.num_m_blk : gm;
   for (int s = 0; s < 2; ++s) {
     const int64_t k0 = g.kseg[2 * s], k1 = g.kseg[2 * s + 1];
-    if (k1 < k0 || k0 % BK != 0 || (k1 % BK != 0 && k1 != g.k_extent) || k1 > g.k_extent)
+    if (k1 < k0 || k0 % BKE != 0 || (k1 % BKE != 0 && k1 != g.k_extent) || k1 > g.k_extent)
       return cudaErrorInvalidValue;
-    p.kb[2 * s] = (int)(k0 / BK);
-    p.kb[2 * s + 1] = (int)((k1 + BK - 1) / BK);
+    p.kb[2 * s] = (int)(k0 / BKE);
+    p.kb[2 * s + 1] = (int)((k1 + BKE - 1) / BKE);
   }
   if (p.kb[1] - p.kb[0] + p.kb[3] - p.kb[2] <= 0) return cudaErrorInvalidValue;
   p.paired = g.paired ? 1 : 0;
@@ -771,6 +808,8 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   p.ep.N = g.N;
   p.status = status;
   p.force_timeout = force_timeout;
+  p.deq_a = g.deq_a;
+  p.deq_b = g.deq_b;
 
   // Box heights: K-major A = this CTA's 128 rows; K-major B = 128 rows per
   // box; MN-major operands move in 64 (MN) x 64 (K) boxes.
@@ -780,14 +819,18 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   bool ok;
   p.a3d = g.a_mn && g.M % 64 == 0;
   p.b3d = g.b_mn && g.N % 64 == 0;
-  if (!g.a_mn)
+  if (g.f8)
+    ok = make_map_u8(&mp.a, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
+  else if (!g.a_mn)
     ok = make_map(&mp.a, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
   else if (p.a3d)
     ok = make_mn_map3(&mp.a, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, BM / 64);
   else
     ok = make_map(&mp.a, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, 64);
   if (!ok) return cudaErrorInvalidValue;
-  if (!g.b_mn)
+  if (g.f8)
+    ok = make_map_u8(&mp.b, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
+  else if (!g.b_mn)
     ok = make_map(&mp.b, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
   else if (p.b3d)
     ok = make_mn_map3(&mp.b, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, C::B_ROWS / 64);
@@ -834,6 +877,25 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
          make_out_map(&mp.i[1], i0 + e.pair_off, false, N, M, e.ld_in0);
   if (!ok) return cudaErrorInvalidValue;
 
+  if (g.f8) {
+    switch (g.epi) {
+      case EPI_GATEUP_SWIGLU:
+        if (!g.paired) return cudaErrorInvalidValue;
+        return launch_inst<PAIR, false, false, EPI_GATEUP_SWIGLU, true>(mp, p, num_sms, st);
+      case EPI_FC1_GELU:
+        return launch_inst<PAIR, false, false, EPI_FC1_GELU, true>(mp, p, num_sms, st);
+      case EPI_DOWN_RESID:
+        return launch_inst<PAIR, false, false, EPI_DOWN_RESID, true>(mp, p, num_sms, st);
+      case EPI_DGRAD_SWIGLU:
+        return launch_inst<PAIR, false, false, EPI_DGRAD_SWIGLU, true>(mp, p, num_sms, st);
+      case EPI_DGRAD_GELU:
+        return launch_inst<PAIR, false, false, EPI_DGRAD_GELU, true>(mp, p, num_sms, st);
+      case EPI_STORE_F32:
+        return launch_inst<PAIR, false, false, EPI_STORE_F32, true>(mp, p, num_sms, st);
+      default:
+        return cudaErrorNotSupported;
+    }
+  }
   const int key = (g.a_mn ? 100 : 0) + (g.b_mn ? 10 : 0) + g.epi;
   switch (key) {
     case 0 + EPI_GATEUP_SWIGLU:

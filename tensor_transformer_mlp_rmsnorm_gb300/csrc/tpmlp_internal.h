@@ -37,10 +37,17 @@ struct GemmDesc {
   int epi = EPI_STORE_F32;
   EpiParams ep{};
   int tile_mode = 0;  // tensor-core path: 0 automatic, 1 single-CTA tiles, 2 CTA-pair tiles
+  // FP8: A and B are E4M3 codes (K-major only, pitches in bytes, multiples of
+  // 16); the accumulator is multiplied by (*deq_a) * (*deq_b) before the
+  // epilogue (the inverse per-tensor scales, device floats).
+  bool f8 = false;
+  const float* deq_a = nullptr;
+  const float* deq_b = nullptr;
 };
 
-// tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory).
-// Segment boundaries must be multiples of 64, except an end equal to k_extent.
+// tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory), or
+// E4M3 operands with f8 set.  Segment boundaries must be multiples of 64
+// elements (128 for E4M3), except an end equal to k_extent.
 cudaError_t launch_gemm_tc(const GemmDesc& g, cudaStream_t st, int num_sms, uint32_t* status, int force_timeout);
 
 // fp32 SIMT GEMM (exact fp32 path), any segments.
@@ -113,6 +120,15 @@ struct AdamArgs {
 int adam_blocks(const AdamArgs& a, int num_sms);
 cudaError_t launch_grad_sqnorm(const AdamArgs& a, int nblocks, cudaStream_t st);
 cudaError_t launch_adamw(int dtype, const AdamArgs& a, int nblocks, cudaStream_t st);
+
+// FP8 casts: amax partials (at most FP8_MAX_PARTS floats in `part`), then
+// E4M3 codes row-major (dst, pitch ld bytes) and/or transposed (dst_t, pitch
+// ld_t bytes) with the scale 448 / amax; 1 / scale goes to *inv_scale.
+constexpr int FP8_MAX_PARTS = 1024;
+int fp8_blocks(int64_t elems, int num_sms);
+cudaError_t launch_fp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld,
+                                uint8_t* dst_t, int64_t ld_t, float* part, float* inv_scale, int num_sms,
+                                cudaStream_t st);
 
 // Message returned by tpmlp_last_error(NULL) on this host thread.
 void set_thread_error(const std::string& msg);

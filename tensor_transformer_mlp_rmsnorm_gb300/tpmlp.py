@@ -80,7 +80,10 @@ _SIGNATURES = {
     "tpmlp_last_error": (ctypes.c_char_p, [_vp]),
     "tpmlp_destroy": (None, [_vp]),
     "tpmlp_mse_loss_grad_noalloc": (_i32, [_i32, _i64, _vp, _vp, _vp, _fp, _vp]),
+    "tpmlp_fp8_quantize": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _fp, _vp, _vp]),
+    "tpmlp_fp8_gemm": (_i32, [_vp, _i64, _vp, _i64, _i64, _i64, _i64, _fp, _fp, _fp, _i64, _vp, _vp]),
 }
+FP8_SCRATCH_BYTES = 4096
 NOALLOC_LOSS_MAX_BLOCKS = 65536
 
 _LIB = None
@@ -149,6 +152,44 @@ def tpmlp_mse_loss_grad_noalloc(y, target, dy, loss, stream=None):
         _check(lib().tpmlp_mse_loss_grad_noalloc(dt, y.numel(), _ptr(y), _ptr(target), _ptr(dy), _ptr(loss),
                                                  ctypes.c_void_p(s)))
     return loss, dy
+
+
+def _pitch16(n: int) -> int:
+    return (n + 15) // 16 * 16
+
+
+def fp8_quantize(src, rows_major: bool = True, transposed: bool = True, stream=None):
+    """E4M3 codes of a bf16 tensor [rows, cols] with its per-tensor scale
+    (tpmlp_fp8_quantize).  Returns (codes [rows, pitch] or None,
+    codes_t [cols, pitch] or None, inv_scale [1] float): the pitches are
+    rounded up to 16 bytes; columns past cols (rows past rows) are padding."""
+    if src.dtype != torch.bfloat16 or src.dim() != 2 or not src.is_contiguous():
+        raise TPMLPError(ERR_ARG, "src must be a contiguous 2-D bf16 tensor")
+    rows, cols = src.shape
+    dev = src.device
+    dst = torch.empty(rows, _pitch16(cols), dtype=torch.uint8, device=dev) if rows_major else None
+    dst_t = torch.empty(cols, _pitch16(rows), dtype=torch.uint8, device=dev) if transposed else None
+    inv = torch.empty(1, dtype=torch.float32, device=dev)
+    scratch = torch.empty(FP8_SCRATCH_BYTES, dtype=torch.uint8, device=dev)
+    st = (stream or torch.cuda.current_stream(dev)).cuda_stream
+    _check(lib().tpmlp_fp8_quantize(_ptr(src), rows, cols, _ptr(dst) if dst is not None else None,
+                                    dst.shape[1] if dst is not None else 0,
+                                    _ptr(dst_t) if dst_t is not None else None,
+                                    dst_t.shape[1] if dst_t is not None else 0, _ptr(inv), _ptr(scratch), st))
+    return dst, dst_t, inv
+
+
+def fp8_gemm(a, b, k: int, inv_a, inv_b, n: int | None = None, stream=None):
+    """c = (a b^T) * inv_a * inv_b from E4M3 codes a [M, pitch], b [N, pitch]
+    whose first k bytes per row are the operand (tpmlp_fp8_gemm)."""
+    M = a.shape[0]
+    N = b.shape[0] if n is None else n
+    c = torch.empty(M, N, dtype=torch.float32, device=a.device)
+    status = torch.zeros(1, dtype=torch.int32, device=a.device)
+    st = (stream or torch.cuda.current_stream(a.device)).cuda_stream
+    _check(lib().tpmlp_fp8_gemm(_ptr(a), a.shape[1], _ptr(b), b.shape[1], M, N, k, _ptr(inv_a), _ptr(inv_b),
+                                _ptr(c), N, _ptr(status), st))
+    return c, status
 
 
 class TPMLP:
