@@ -200,6 +200,32 @@ TPMLP_API tpmlp_status tpmlp_bind_adam_state(tpmlp_ctx* ctx, const tpmlp_param_s
  * with hyperparameters out of range. */
 TPMLP_API tpmlp_status tpmlp_adamw_step(tpmlp_ctx* ctx, const tpmlp_adamw_params* hp, float* grad_norm);
 
+/* GEMM operand precision of the bf16 dtype. */
+typedef enum { TPMLP_PREC_BF16 = 0, TPMLP_PREC_FP8 = 1 } tpmlp_precision;
+
+/* Bytes of the extra device workspace the FP8 precision needs (E4M3 copies
+ * of every GEMM operand, row-major and transposed, and their scales); 0 for
+ * the f32 dtype or an invalid config. */
+TPMLP_API size_t tpmlp_fp8_workspace_bytes(const tpmlp_config* cfg);
+
+/* Hand the context the FP8 workspace (256-byte aligned, caller-owned, kept
+ * alive until tpmlp_destroy).  TPMLP_ERR_UNSUPPORTED for the f32 dtype. */
+TPMLP_API tpmlp_status tpmlp_bind_fp8_workspace(tpmlp_ctx* ctx, void* dev, size_t bytes);
+
+/* Select the GEMM operand precision (page "Megatron-Core Architecture: 5D
+ * Distributed Parallelism, ... FP8 Transformer Engine", its list of
+ * Megatron-Core subsystems, item 6).  TPMLP_PREC_FP8: before each of the six
+ * GEMMs its two operands are cast to E4M3 with one scale per tensor (448 /
+ * the tensor's current absolute maximum; tpmlp_fp8_quantize), row-major and
+ * transposed so that every GEMM reads K-major codes; the tensor cores
+ * multiply the codes with fp32 accumulation and the epilogue divides by both
+ * scales before its element-wise step.  Activations, gradients and the
+ * optimizer stay as in TPMLP_PREC_BF16.  Needs the bf16 dtype
+ * (TPMLP_ERR_UNSUPPORTED) and a bound FP8 workspace (TPMLP_ERR_ORDER); the
+ * shard restrictions of the SKIP flags must fall on 128-element blocks.
+ * Changing the precision requires a new forward. */
+TPMLP_API tpmlp_status tpmlp_set_precision(tpmlp_ctx* ctx, int32_t precision);
+
 /* Sequence-parallel form ("Megatron-LM walkthrough", "Deep dive: sequence
  * parallelism, memory for free"): shard s of t owns the contiguous tokens
  * [s N/t, (s+1) N/t) outside the tensor-parallel region.  On one GPU the

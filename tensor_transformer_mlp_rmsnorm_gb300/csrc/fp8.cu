@@ -149,26 +149,31 @@ int fp8_blocks(int64_t elems, int num_sms) {
   return (int)(b < 1 ? 1 : b);
 }
 
-cudaError_t launch_fp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld,
-                                uint8_t* dst_t, int64_t ld_t, float* part, float* inv_scale, int num_sms,
-                                cudaStream_t st) {
-  const int64_t n = rows * cols;
-  const int nb = fp8_blocks(n, num_sms);
-  if (n > 0) {
-    amax_partials_kernel<<<nb, THREADS, 0, st>>>(static_cast<const __nv_bfloat16*>(src), n / 8, part);
-  } else {
-    cudaError_t e = cudaMemsetAsync(part, 0, sizeof(float), st);
-    if (e != cudaSuccess) return e;
-  }
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  QuantArgs q{static_cast<const __nv_bfloat16*>(src), rows, cols, dst, ld, dst_t, ld_t, part, n > 0 ? nb : 1,
-              inv_scale};
+cudaError_t launch_fp8_amax(const void* src, int64_t n, float* part, int nparts, cudaStream_t st) {
+  if (n <= 0) return cudaMemsetAsync(part, 0, sizeof(float), st);
+  amax_partials_kernel<<<nparts, THREADS, 0, st>>>(static_cast<const __nv_bfloat16*>(src), n / 8, part);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_cast(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld, uint8_t* dst_t,
+                            int64_t ld_t, const float* part, int nparts, float* inv_scale, int num_sms,
+                            cudaStream_t st) {
+  QuantArgs q{static_cast<const __nv_bfloat16*>(src), rows, cols, dst, ld, dst_t, ld_t, part, nparts, inv_scale};
   const int64_t tiles = ((rows + TILE - 1) / TILE) * ((cols + TILE - 1) / TILE);
   int64_t qb = tiles < 8LL * num_sms ? tiles : 8LL * num_sms;
   if (qb < 1) qb = 1;
   quantize_e4m3_kernel<<<(unsigned)qb, THREADS, 0, st>>>(q);
   return cudaGetLastError();
+}
+
+cudaError_t launch_fp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld,
+                                uint8_t* dst_t, int64_t ld_t, float* part, float* inv_scale, int num_sms,
+                                cudaStream_t st) {
+  const int64_t n = rows * cols;
+  const int nb = n > 0 ? fp8_blocks(n, num_sms) : 1;
+  const cudaError_t e = launch_fp8_amax(src, n, part, nb, st);
+  if (e != cudaSuccess) return e;
+  return launch_fp8_cast(src, rows, cols, dst, ld, dst_t, ld_t, part, nb, inv_scale, num_sms, st);
 }
 
 }  // namespace tpmlp

@@ -45,6 +45,8 @@ enum KernelId {
   K_SGD,
   K_GRAD_NORM,
   K_ADAMW,
+  K_FP8_AMAX,
+  K_FP8_CAST,
   K_PROBE,
   K_COUNT
 };
@@ -53,7 +55,8 @@ const char* const kKernelNames[K_COUNT] = {
     "rmsnorm_fwd",        "gemm_gateup_act",     "gemm_down_reduce",     "mse_loss_grad",
     "loss_finalize",      "gemm_dgrad_act",      "gemm_wgrad_down",      "gemm_wgrad_gateup",
     "gemm_dgrad_norm_reduce", "rmsnorm_bwd_residual", "colsum_finalize", "colsum_b1",
-    "sgd_update",         "grad_sqnorm",         "adamw_update",         "timeout_probe"};
+    "sgd_update",         "grad_sqnorm",         "adamw_update",         "fp8_amax",
+    "fp8_cast",           "timeout_probe"};
 
 constexpr int MAX_BWD_PARTS = 1024;
 constexpr int MAX_B1_PARTS = 256;
@@ -119,6 +122,39 @@ Layout make_layout(const tpmlp_config& c) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+int64_t pitch16(int64_t n) { return (n + 15) / 16 * 16; }
+
+// FP8 operand buffers (E4M3 codes, pitches rounded up to 16 bytes): each
+// tensor that feeds a GEMM row-major (q) and transposed (t), with one inverse
+// scale per tensor.  Transposed copies of token-major tensors are sized for
+// max_tokens and used with the pitch of the actual token count.
+enum Fp8Tensor { F8_NRM = 0, F8_WGU, F8_ACT, F8_WD, F8_DY, F8_DGU, F8_COUNT };
+struct Fp8Layout {
+  size_t inv, part, q[F8_COUNT], t[F8_COUNT], total;
+};
+
+Fp8Layout make_fp8_layout(const tpmlp_config& c) {
+  Fp8Layout L{};
+  const size_t N = (size_t)c.max_tokens, H = (size_t)c.hidden, F = (size_t)c.ffn;
+  const size_t guw = c.act == TPMLP_SWIGLU ? 2 * F : F;
+  const size_t rows[F8_COUNT] = {N, guw, N, H, N, N};  // row-major shape [rows, cols]
+  const size_t cols[F8_COUNT] = {H, H, F, F, H, guw};
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = align256(off + bytes);
+    return o;
+  };
+  L.inv = take(F8_COUNT * sizeof(float));
+  L.part = take(FP8_MAX_PARTS * sizeof(float));
+  for (int i = 0; i < F8_COUNT; ++i) {
+    L.q[i] = take(rows[i] * (size_t)pitch16((int64_t)cols[i]));
+    L.t[i] = take(cols[i] * (size_t)pitch16((int64_t)rows[i]));
+  }
+  L.total = off;
+  return L;
+}
+
 }  // namespace
 
 void tpmlp::set_thread_error(const std::string& msg) { g_thread_err = msg; }
@@ -139,6 +175,9 @@ struct tpmlp_ctx {
   float *g_norm_w = nullptr, *g_w_gu = nullptr, *g_b_1 = nullptr, *g_w_down = nullptr, *g_b_down = nullptr;
   float *m_norm_w = nullptr, *m_w_gu = nullptr, *m_b_1 = nullptr, *m_w_down = nullptr, *m_b_down = nullptr;
   bool sp = false;  // sequence-parallel form: token shards of N / t rows
+  bool fp8 = false;  // E4M3 GEMM operands (needs the FP8 workspace)
+  uint8_t* ws8 = nullptr;
+  Fp8Layout L8{};
   tpmlp_param_set adam_m{}, adam_v{};
   bool adam_bound = false;
   uint32_t dbg_flags = 0;
@@ -215,10 +254,43 @@ tpmlp_status run_gemm(tpmlp_ctx* c, int id, const GemmDesc& desc, int force_time
 }
 
 // Contraction segments in elements for a shard restriction; the tensor-core
-// path needs 64-element block boundaries.
+// path needs 64-element block boundaries (128 for E4M3 operands).
 bool seg_ok(const tpmlp_ctx* c, int64_t b, int64_t e, int64_t extent) {
   if (c->cfg.dtype != TPMLP_BF16) return true;
-  return b % 64 == 0 && (e % 64 == 0 || e == extent);
+  const int64_t blk = c->fp8 ? 128 : 64;
+  return b % blk == 0 && (e % blk == 0 || e == extent);
+}
+
+// E4M3 copies (row-major and transposed) of a bf16 tensor [rows, cols] with
+// its per-tensor scale: the amax pass, then the cast.
+tpmlp_status fp8_cast(tpmlp_ctx* c, int tensor, const void* src, int64_t rows, int64_t cols) {
+  float* part = reinterpret_cast<float*>(c->ws8 + c->L8.part);
+  float* inv = reinterpret_cast<float*>(c->ws8 + c->L8.inv) + tensor;
+  uint8_t* q = c->ws8 + c->L8.q[tensor];
+  uint8_t* t = c->ws8 + c->L8.t[tensor];
+  const int64_t n = rows * cols;
+  const int nb = n > 0 ? fp8_blocks(n, c->num_sms) : 1;
+  TPMLP_TRY(c->run(K_FP8_AMAX, [&] { return launch_fp8_amax(src, n, part, nb, c->stream); }));
+  return c->run(K_FP8_CAST, [&] {
+    return launch_fp8_cast(src, rows, cols, q, pitch16(cols), t, pitch16(rows), part, nb, inv, c->num_sms, c->stream);
+  });
+}
+
+// Point a GEMM at E4M3 operands: A = tensor ta (row-major copy, or the
+// transposed one with ta_t), B = tensor tb likewise, both K-major.
+void use_fp8(const tpmlp_ctx* c, GemmDesc& g, int ta, bool ta_t, int64_t lda, int tb, bool tb_t, int64_t ldb,
+             int64_t b_rows) {
+  const float* inv = reinterpret_cast<const float*>(c->ws8 + c->L8.inv);
+  g.f8 = true;
+  g.a = c->ws8 + (ta_t ? c->L8.t[ta] : c->L8.q[ta]);
+  g.lda = lda;
+  g.a_mn = false;
+  g.b = c->ws8 + (tb_t ? c->L8.t[tb] : c->L8.q[tb]);
+  g.ldb = ldb;
+  g.b_mn = false;
+  g.b_rows = b_rows;
+  g.deq_a = inv + ta;
+  g.deq_b = inv + tb;
 }
 
 }  // namespace
@@ -290,6 +362,35 @@ tpmlp_status tpmlp_bind_workspace(tpmlp_ctx* c, void* dev, size_t bytes) {
   c->ws_bytes = bytes;
   const cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
   if (e != cudaSuccess) return c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
+  return TPMLP_OK;
+}
+
+size_t tpmlp_fp8_workspace_bytes(const tpmlp_config* cfg) {
+  if (config_error(cfg, nullptr, nullptr) || cfg->dtype != TPMLP_BF16) return 0;
+  return make_fp8_layout(*cfg).total;
+}
+
+tpmlp_status tpmlp_bind_fp8_workspace(tpmlp_ctx* c, void* dev, size_t bytes) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (c->cfg.dtype != TPMLP_BF16) return c->fail(TPMLP_ERR_UNSUPPORTED, "FP8 operands are for the bf16 dtype");
+  if (!dev || (reinterpret_cast<uintptr_t>(dev) & 255u))
+    return c->fail(TPMLP_ERR_ARG, "FP8 workspace must be 256-byte aligned");
+  c->L8 = make_fp8_layout(c->cfg);
+  if (bytes < c->L8.total) return c->fail(TPMLP_ERR_ARG, "FP8 workspace too small");
+  c->ws8 = static_cast<uint8_t*>(dev);
+  return TPMLP_OK;
+}
+
+tpmlp_status tpmlp_set_precision(tpmlp_ctx* c, int32_t precision) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (precision != TPMLP_PREC_BF16 && precision != TPMLP_PREC_FP8)
+    return c->fail(TPMLP_ERR_ARG, "unknown precision");
+  if (precision == TPMLP_PREC_FP8) {
+    if (c->cfg.dtype != TPMLP_BF16) return c->fail(TPMLP_ERR_UNSUPPORTED, "FP8 GEMMs are for the bf16 dtype");
+    if (!c->ws8) return c->fail(TPMLP_ERR_ORDER, "no FP8 workspace bound");
+  }
+  c->fp8 = precision == TPMLP_PREC_FP8;
+  c->fwd_done = c->bwd_done = false;
   return TPMLP_OK;
 }
 
@@ -393,6 +494,13 @@ tpmlp_status tpmlp_forward(tpmlp_ctx* c, int64_t tokens, const void* x, const vo
     }
     g.ep.out1 = c->wsp<void>(c->L.act);
     g.ep.ld_out1 = F;
+    const int64_t guw = c->swiglu() ? 2 * F : F;
+    if (c->fp8) {
+      TPMLP_TRY(fp8_cast(c, F8_NRM, nrm, tokens, H));
+      TPMLP_TRY(fp8_cast(c, F8_WGU, w_gate_up, guw, H));
+      TPMLP_TRY(fp8_cast(c, F8_WD, w_down, H, F));
+      use_fp8(c, g, F8_NRM, false, pitch16(H), F8_WGU, false, pitch16(H), guw);
+    }
     TPMLP_TRY(run_gemm(c, K_GEMM_GATEUP, g, force_timeout && dt == 1));
 
     GemmDesc d;
@@ -412,6 +520,10 @@ tpmlp_status tpmlp_forward(tpmlp_ctx* c, int64_t tokens, const void* x, const vo
     d.ep.in0 = x;
     d.ep.ld_in0 = H;
     d.ep.vec = b_down;
+    if (c->fp8) {
+      TPMLP_TRY(fp8_cast(c, F8_ACT, c->wsp<void>(c->L.act), tokens, F));
+      use_fp8(c, d, F8_ACT, false, pitch16(F), F8_WD, false, pitch16(F), H);
+    }
     TPMLP_TRY(run_gemm(c, K_GEMM_DOWN, d));
   }
   c->fwd_done = true;
@@ -494,6 +606,10 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   a.ep.out0 = dgu;
   a.ep.ld_out0 = guw;
   a.ep.pair_off = F;
+  if (c->fp8) {
+    TPMLP_TRY(fp8_cast(c, F8_DY, dy, N, H));
+    use_fp8(c, a, F8_DY, false, pitch16(H), F8_WD, true, pitch16(H), F);
+  }
   TPMLP_TRY(run_gemm(c, K_GEMM_DGRAD_ACT, a));
 
   // dW_d = dy^T A (contraction over tokens).
@@ -511,6 +627,7 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   wd.epi = EPI_STORE_F32;
   wd.ep.out0 = dw_down;
   wd.ep.ld_out0 = F;
+  if (c->fp8) use_fp8(c, wd, F8_DY, true, pitch16(N), F8_ACT, true, pitch16(N), F);
   TPMLP_TRY(run_gemm(c, K_GEMM_WGRAD_DOWN, wd));
 
   // dW_gate_up = dGU^T n  ([2F, H]; GeLU: dW_1 [F, H]).
@@ -528,6 +645,10 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   wg.epi = EPI_STORE_F32;
   wg.ep.out0 = dw_gate_up;
   wg.ep.ld_out0 = H;
+  if (c->fp8) {
+    TPMLP_TRY(fp8_cast(c, F8_DGU, dgu, N, guw));
+    use_fp8(c, wg, F8_DGU, true, pitch16(N), F8_NRM, true, pitch16(N), H);
+  }
   TPMLP_TRY(run_gemm(c, K_GEMM_WGRAD_GATEUP, wg));
 
   if (!sw) {
@@ -559,6 +680,7 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   dn.epi = EPI_STORE_F32;
   dn.ep.out0 = dnrm;
   dn.ep.ld_out0 = H;
+  if (c->fp8) use_fp8(c, dn, F8_DGU, false, pitch16(guw), F8_WGU, true, pitch16(guw), H);
   TPMLP_TRY(run_gemm(c, K_GEMM_DGRAD_NORM, dn));
 
   const int shards = c->sp ? c->t : 1;

@@ -129,6 +129,11 @@ int fp8_blocks(int64_t elems, int num_sms);
 cudaError_t launch_fp8_quantize(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld,
                                 uint8_t* dst_t, int64_t ld_t, float* part, float* inv_scale, int num_sms,
                                 cudaStream_t st);
+// The two kernels of launch_fp8_quantize: nparts = fp8_blocks(rows * cols) partial maxima, then the cast.
+cudaError_t launch_fp8_amax(const void* src, int64_t n, float* part, int nparts, cudaStream_t st);
+cudaError_t launch_fp8_cast(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld, uint8_t* dst_t,
+                            int64_t ld_t, const float* part, int nparts, float* inv_scale, int num_sms,
+                            cudaStream_t st);
 
 // Message returned by tpmlp_last_error(NULL) on this host thread.
 void set_thread_error(const std::string& msg);

@@ -23,6 +23,7 @@ F32, BF16 = 0, 1
 SWIGLU, GELU = 0, 1
 DBG_SKIP_FWD_REDUCE, DBG_SKIP_BWD_REDUCE, DBG_FORCE_TIMEOUT, DBG_GEMM_SINGLE_CTA = 1, 2, 4, 8
 DBG_SKIP_SP_GRAD_SYNC = 16
+PREC_BF16, PREC_FP8 = 0, 1
 
 _DTYPES = {"f32": F32, "bf16": BF16}
 _ACTS = {"swiglu": SWIGLU, "gelu": GELU}
@@ -70,6 +71,9 @@ _SIGNATURES = {
     "tpmlp_adamw_step": (_i32, [_vp, ctypes.POINTER(AdamWParams), _fp]),
     "tpmlp_set_debug": (_i32, [_vp, _u32, _i32]),
     "tpmlp_set_sequence_parallel": (_i32, [_vp, _i32]),
+    "tpmlp_fp8_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Config)]),
+    "tpmlp_bind_fp8_workspace": (_i32, [_vp, _vp, ctypes.c_size_t]),
+    "tpmlp_set_precision": (_i32, [_vp, _i32]),
     "tpmlp_sync": (_i32, [_vp]),
     "tpmlp_set_timing": (_i32, [_vp, _i32]),
     "tpmlp_read_kernel_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int64), _i32]),
@@ -345,6 +349,18 @@ class TPMLP:
         _check(lib().tpmlp_adamw_step(self.ctx, ctypes.byref(hp), self._t(gn, (1,), torch.float32, "grad_norm")),
                self.ctx)
         return gn
+
+    def set_precision(self, precision: str):
+        """"bf16" or "fp8" GEMM operands; the first switch to FP8 allocates and binds its workspace."""
+        prec = {"bf16": PREC_BF16, "fp8": PREC_FP8}[precision]
+        if prec == PREC_FP8 and getattr(self, "workspace8", None) is None:
+            nbytes = lib().tpmlp_fp8_workspace_bytes(ctypes.byref(self.cfg))
+            if nbytes == 0:
+                raise TPMLPError(ERR_UNSUPPORTED, "FP8 needs the bf16 dtype")
+            self.workspace8 = torch.empty(nbytes, dtype=torch.uint8, device=self.device)
+            _check(lib().tpmlp_bind_fp8_workspace(self.ctx, _ptr(self.workspace8), nbytes), self.ctx)
+        _check(lib().tpmlp_set_precision(self.ctx, prec), self.ctx)
+        self._fwd = False
 
     def set_sequence_parallel(self, enable: bool):
         _check(lib().tpmlp_set_sequence_parallel(self.ctx, int(bool(enable))), self.ctx)

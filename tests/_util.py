@@ -10,6 +10,17 @@ Tolerances (written here, used by every parity test):
   2e-2 * |oracle| + 1e-2 * max|oracle|, and ||gpu - oracle||_2 <= 2e-2 *
   ||oracle||_2 per tensor.
 
+* FP8 GEMM operands, against the oracle's FP8 step (``tol="fp8"``): per
+  element |gpu - oracle| <= 0.1 * |oracle| + 0.05 * max|oracle|, normwise
+  0.05.  Both sides quantise with the same rule, but from stored operands
+  that differ by bf16 rounding (and whose maxima, hence scales, may differ
+  by one bf16 unit, 2^-8): a fraction of about 2^-8 / 2^-3 = 3% of the codes
+  then round the other way, each by one E4M3 unit (up to 2^-3 relative).
+  Through a sum of K such products with mixed signs that is a normwise
+  error of about sqrt(0.03) * 2^-3 / sqrt(3) ~ 1.2% per GEMM, compounded
+  over the chained GEMMs of the backward; small elements of a cancelling
+  sum see several times that, hence the per-element bound.
+
 The absolute term is the stated absolute tolerance applied to the tensor
 divided by its largest magnitude: gradients of a mean loss are ~1e-8..1e-4,
 where a fixed absolute 1e-2 would accept anything.  Scaling by the rms instead
@@ -27,6 +38,7 @@ import synth
 TOL = {
     "f32": dict(rtol=1e-5, atol_max=1e-5, norm=1e-5),
     "bf16": dict(rtol=2e-2, atol_max=1e-2, norm=2e-2),
+    "fp8": dict(rtol=1e-1, atol_max=5e-2, norm=5e-2),
 }
 
 
@@ -107,8 +119,8 @@ def gpu_step(cfg: synth.Config, inp: dict, t: int, lr: float, flags: int = 0, sh
 
 
 def compare_step(cfg: synth.Config, gpu: dict, ora: dict, inp: dict, lr: float, report: dict | None = None,
-                 grad_keys=None):
-    dt = cfg.dtype
+                 grad_keys=None, tol: str | None = None):
+    dt = tol or cfg.dtype
     compare("y", gpu["y"], ora["y"], dt, report)
     assert abs(gpu["loss"] - ora["loss"]) <= TOL[dt]["rtol"] * abs(ora["loss"]) + 1e-12, (gpu["loss"], ora["loss"])
     compare("dx", gpu["dx"], ora["grads"]["x"], dt, report)

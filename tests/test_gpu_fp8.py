@@ -87,3 +87,47 @@ def test_fp8_gemm_matches_oracle(M, N, K):
     # and the quantisation really happened: FP8 differs from the exact product
     exact = a @ b.T
     assert np.linalg.norm(to_np(c) - exact) / np.linalg.norm(exact) > 1e-3
+
+
+# ------------------------------------------------------------------ the FP8 training step
+
+LR = 0.1
+
+
+def _cfg(act, N, H, F):
+    import dataclasses
+    c = dataclasses.replace(synth.CONFIGS["bf16_h2048"].with_shape(N, H, F), act=act)
+    return dataclasses.replace(c, b_1_std=0.01) if act == "gelu" else c
+
+
+@pytest.mark.parametrize("act,N,H,F,t", [("swiglu", 300, 512, 1536, 4), ("gelu", 333, 384, 1280, 8),
+                                         ("swiglu", 1024, 256, 2048, 1), ("swiglu", 77, 328, 1024, 8),
+                                         ("swiglu", 600, 320, 1000, 1)])
+def test_fp8_step_matches_fp8_oracle(act, N, H, F, t):
+    """The step with every GEMM in FP8 against the oracle's FP8 step, which
+    quantises the same stored (bf16) operands with the same per-tensor rule:
+    the FP8 tolerance of tests/_util.py.  Against the exact step the FP8
+    error must be present and inside the FP8 band."""
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP
+    from tests._util import compare_step, gpu_step
+    cfg = _cfg(act, N, H, F)
+    inp = synth.make_inputs(cfg, seed=31)
+    m = TPMLP(N, H, F, max_t=8, dtype="bf16", act=act)
+    m.set_precision("fp8")
+    gpu = gpu_step(cfg, inp, t, LR, mod=m)
+    p = {k: inp[k] for k in synth.param_names(act)}
+    ora = O.dense_step_fp8(p, inp["x"], inp["target"], cfg.eps, LR, act, store=synth.round_to_bf16)
+    compare_step(cfg, gpu, ora, inp, LR, tol="fp8")
+    exact = O.dense_step(p, inp["x"], inp["target"], cfg.eps, LR, act)
+    rel = lambda a, b: float(np.linalg.norm(a - b) / np.linalg.norm(b))
+    assert 1e-3 < rel(gpu["y"] - inp["x"], exact["y"] - inp["x"]) < 0.1
+    gk = "w_gate_up" if act == "swiglu" else "w_1"
+    assert 1e-3 < rel(gpu["grads"][gk], exact["grads"][gk]) < 0.15
+
+
+def test_fp8_precision_errors():
+    from tensor_transformer_mlp_rmsnorm_gb300 import ERR_UNSUPPORTED, TPMLP, TPMLPError
+    m = TPMLP(16, 64, 256, max_t=8, dtype="f32", act="swiglu")
+    with pytest.raises(TPMLPError) as e:
+        m.set_precision("fp8")
+    assert e.value.status == ERR_UNSUPPORTED
