@@ -37,6 +37,10 @@ struct EpiParams {
   int64_t ld_out0, ld_out1, ld_in0;
   int64_t pair_off;  // F: column offset of U / dU in the paired layouts
   int M, N;          // valid output rows / columns (channels for the paired layouts)
+  // Optional (tensor-core path): the largest magnitude of the activation
+  // output (A, or dG and dU, or dZ) after bf16 rounding, as float bits,
+  // combined with atomicMax (the caller zeroes it first).
+  uint32_t* amax;
 };
 
 __device__ __forceinline__ float to_f(float v) { return v; }

@@ -7,7 +7,7 @@
 //                   on the magnitude bits, so order-independent and exact);
 //   quantize_e4m3 : every block folds the partials into the same amax and
 //                   scale s = 448 / amax (float32; 1 for an all-zero tensor),
-//                   then casts 64x64 tiles: codes = RN_satfinite(x * s),
+//                   then casts 128x128 tiles: codes = RN_satfinite(x * s),
 //                   written row-major (dst) and/or transposed (dst_t) through
 //                   shared memory; block 0 stores 1 / s for the GEMM epilogue.
 //
@@ -25,7 +25,6 @@ namespace tpmlp {
 namespace {
 
 constexpr int THREADS = 256;
-constexpr int TILE = 64;
 
 __global__ void __launch_bounds__(THREADS) amax_partials_kernel(const __nv_bfloat16* __restrict__ x, int64_t n8,
                                                                 float* __restrict__ part) {
@@ -82,8 +81,26 @@ struct QuantArgs {
   float* inv_scale;  // out: 1 / s
 };
 
+// One block casts 128x128 tiles.  Phase 1: each thread converts 16-element
+// row segments (row-major codes go straight to dst) and parks the codes
+// row-major in shared memory.  Phase 2: each thread takes a 16-row x 4-column
+// block of codes (16 word reads; a warp reads 32 consecutive words of one
+// row, so no bank conflicts), transposes it as 4x4 byte blocks with
+// __byte_perm, and writes four 16-byte rows of dst_t.
+constexpr int QT = 128;
+
+__device__ __forceinline__ void transpose4x4(uint32_t& a, uint32_t& b, uint32_t& c, uint32_t& d) {
+  // rows a..d hold bytes [x0 x1 x2 x3] (x0 lowest); afterwards a..d hold the columns
+  const uint32_t t0 = __byte_perm(a, b, 0x5140), t1 = __byte_perm(a, b, 0x7362);
+  const uint32_t t2 = __byte_perm(c, d, 0x5140), t3 = __byte_perm(c, d, 0x7362);
+  a = __byte_perm(t0, t2, 0x5410);
+  b = __byte_perm(t0, t2, 0x7632);
+  c = __byte_perm(t1, t3, 0x5410);
+  d = __byte_perm(t1, t3, 0x7632);
+}
+
 __global__ void __launch_bounds__(THREADS) quantize_e4m3_kernel(const QuantArgs q) {
-  __shared__ __align__(16) uint8_t tile_t[TILE][TILE + 16];  // codes by [column][row]
+  __shared__ __align__(16) uint32_t tile[QT][QT / 4];  // codes, row-major, 4 per word
   __shared__ float red[THREADS / 32];
   __shared__ float s_scale;
   float m = 0.0f;
@@ -101,38 +118,62 @@ __global__ void __launch_bounds__(THREADS) quantize_e4m3_kernel(const QuantArgs 
   }
   __syncthreads();
   const float s = s_scale;
-  const int64_t tiles_c = (q.cols + TILE - 1) / TILE;
-  const int64_t ntiles = ((q.rows + TILE - 1) / TILE) * tiles_c;
-  const int tr = threadIdx.x >> 2;         // tile row (load) / tile column (transposed store)
-  const int tc = (threadIdx.x & 3) * 16;   // 16-element segment
-  for (int64_t tile = blockIdx.x; tile < ntiles; tile += gridDim.x) {
-    const int64_t r0 = (tile / tiles_c) * TILE, c0 = (tile % tiles_c) * TILE;
-    const int64_t r = r0 + tr;
-    if (r < q.rows) {
+  const int64_t tiles_c = (q.cols + QT - 1) / QT;
+  const int64_t ntiles = ((q.rows + QT - 1) / QT) * tiles_c;
+  // phase 1: 8 threads per row, 16 codes each; 32 rows per pass, 4 passes
+  const int seg = threadIdx.x & 7, prow = threadIdx.x >> 3;
+  // phase 2: a warp per 16-row group, a lane per 4-column group
+  const int cg = threadIdx.x & 31, rg = threadIdx.x >> 5;
+  for (int64_t tile_i = blockIdx.x; tile_i < ntiles; tile_i += gridDim.x) {
+    const int64_t r0 = (tile_i / tiles_c) * QT, c0 = (tile_i % tiles_c) * QT;
+    const int64_t c = c0 + seg * 16;
+    // all eight 16-byte loads of this thread first, then the casts and stores
+    uint4 raw[4][2];
 #pragma unroll
-      for (int h = 0; h < 2; ++h) {
-        const int64_t c = c0 + tc + 8 * h;
-        if (c < q.cols) {  // cols is a multiple of 8
-          const uint2 codes = quant8(*reinterpret_cast<const uint4*>(q.src + r * q.cols + c), s);
-          if (q.dst) *reinterpret_cast<uint2*>(q.dst + r * q.ld + c) = codes;
-          if (q.dst_t) {
-            const uint8_t* b = reinterpret_cast<const uint8_t*>(&codes);
+    for (int pass = 0; pass < 4; ++pass) {
+      const int64_t r = r0 + pass * 32 + prow;
+      const __nv_bfloat16* src = q.src + r * q.cols + c;
+      raw[pass][0] = (r < q.rows && c < q.cols) ? __ldg(reinterpret_cast<const uint4*>(src)) : make_uint4(0, 0, 0, 0);
+      raw[pass][1] =
+          (r < q.rows && c + 8 < q.cols) ? __ldg(reinterpret_cast<const uint4*>(src + 8)) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
-            for (int j = 0; j < 8; ++j) tile_t[tc + 8 * h + j][tr] = b[j];
-          }
+    for (int pass = 0; pass < 4; ++pass) {
+      const int tr = pass * 32 + prow;
+      const int64_t r = r0 + tr;
+      const uint2 lo = quant8(raw[pass][0], s), hi = quant8(raw[pass][1], s);
+      if (r < q.rows) {
+        if (q.dst) {
+          uint8_t* d = q.dst + r * q.ld + c;
+          if (c + 8 < q.cols)
+            *reinterpret_cast<uint4*>(d) = make_uint4(lo.x, lo.y, hi.x, hi.y);
+          else if (c < q.cols)
+            *reinterpret_cast<uint2*>(d) = lo;
         }
       }
+      if (q.dst_t) *reinterpret_cast<uint4*>(&tile[tr][seg * 4]) = make_uint4(lo.x, lo.y, hi.x, hi.y);
     }
     if (q.dst_t) {
       __syncthreads();
-      const int64_t c = c0 + tr;             // source column = destination row
-      const int64_t rr = r0 + tc;            // first source row of this segment
-      if (c < q.cols && rr < q.rows) {
-        uint8_t* out = q.dst_t + c * q.ld_t + rr;
-        if (rr + 16 <= q.rows) {
-          *reinterpret_cast<uint4*>(out) = *reinterpret_cast<const uint4*>(&tile_t[tr][tc]);
-        } else {
-          for (int j = 0; j < 16 && rr + j < q.rows; ++j) out[j] = tile_t[tr][tc + j];
+      uint32_t w[16];
+#pragma unroll
+      for (int k = 0; k < 16; ++k) w[k] = tile[rg * 16 + k][cg];
+#pragma unroll
+      for (int k = 0; k < 16; k += 4) transpose4x4(w[k], w[k + 1], w[k + 2], w[k + 3]);
+      // w[4 j + i] now holds rows 4j..4j+3 of source column 4 cg + i
+      const int64_t rr = r0 + rg * 16;
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int64_t col = c0 + cg * 4 + i;  // source column = destination row
+        if (col < q.cols && rr < q.rows) {
+          uint8_t* out = q.dst_t + col * q.ld_t + rr;
+          const uint4 v = make_uint4(w[i], w[4 + i], w[8 + i], w[12 + i]);
+          if (rr + 16 <= q.rows) {
+            *reinterpret_cast<uint4*>(out) = v;
+          } else {
+            const uint8_t* b = reinterpret_cast<const uint8_t*>(&v);
+            for (int j = 0; j < 16 && rr + j < q.rows; ++j) out[j] = b[j];
+          }
         }
       }
       __syncthreads();
@@ -159,8 +200,8 @@ cudaError_t launch_fp8_cast(const void* src, int64_t rows, int64_t cols, uint8_t
                             int64_t ld_t, const float* part, int nparts, float* inv_scale, int num_sms,
                             cudaStream_t st) {
   QuantArgs q{static_cast<const __nv_bfloat16*>(src), rows, cols, dst, ld, dst_t, ld_t, part, nparts, inv_scale};
-  const int64_t tiles = ((rows + TILE - 1) / TILE) * ((cols + TILE - 1) / TILE);
-  int64_t qb = tiles < 8LL * num_sms ? tiles : 8LL * num_sms;
+  const int64_t tiles = ((rows + QT - 1) / QT) * ((cols + QT - 1) / QT);
+  int64_t qb = tiles < 4LL * num_sms ? tiles : 4LL * num_sms;
   if (qb < 1) qb = 1;
   quantize_e4m3_kernel<<<(unsigned)qb, THREADS, 0, st>>>(q);
   return cudaGetLastError();

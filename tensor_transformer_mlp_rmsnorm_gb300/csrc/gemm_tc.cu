@@ -217,18 +217,30 @@ struct EpiOut {
 // on the accumulator values v (and u, the second half, for the paired
 // layouts), results written into the warp's staging tiles (row r).  Inputs
 // outside the matrix read as zero; the TMA store clips the outputs.
+// Largest |o[i]| over the first n (<= 32 or more) columns.
+__device__ __forceinline__ float max_abs32(const float* o, int n) {
+  float m = 0.0f;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) m = i < n ? fmaxf(m, fabsf(o[i])) : m;
+  return m;
+}
+
+// Returns, when `want_max`, the largest magnitude among the activation
+// outputs of this row's valid columns (A; dG and dU; dZ), else 0.
 template <int EPI>
-__device__ __forceinline__ void epi_stage(const EpiParams& ep, int col, const float* v, const float* u,
-                                          const EpiIn& in, uint8_t* st, int r) {
+__device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const float* v, const float* u,
+                                           const EpiIn& in, uint8_t* st, int r, bool want_max) {
   typedef __nv_bfloat16 T;
   const int ncols = ep.N - col;  // valid columns of this chunk (may exceed 32)
   float o[32];
+  float mx = 0.0f;
   if (EPI == EPI_GATEUP_SWIGLU) {
     stage_row_bf16(st, r, v);
     stage_row_bf16(st + 2048, r, u);
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = silu_fast(v[i]) * u[i];
     stage_row_bf16(st + 4096, r, o);
+    if (want_max) mx = max_abs32(o, ncols);
   } else if (EPI == EPI_FC1_GELU) {
     float b[32];
     load32_bf16_guard(static_cast<const T*>(ep.vec) + col, ncols, b);
@@ -238,6 +250,7 @@ __device__ __forceinline__ void epi_stage(const EpiParams& ep, int col, const fl
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = gelu_f(b[i]);
     stage_row_bf16(st + 2048, r, o);
+    if (want_max) mx = max_abs32(o, ncols);
   } else if (EPI == EPI_DOWN_RESID) {
     float x[32], b[32];
     unpack32(in.a, x);
@@ -253,15 +266,18 @@ __device__ __forceinline__ void epi_stage(const EpiParams& ep, int col, const fl
     for (int i = 0; i < 32; ++i) swiglu_bwd_fast(v[i], g[i], uu[i], o[i], uu[i]);
     stage_row_bf16(st, r, o);
     stage_row_bf16(st + 2048, r, uu);
+    if (want_max) mx = fmaxf(max_abs32(o, ncols), max_abs32(uu, ncols));
   } else if (EPI == EPI_DGRAD_GELU) {
     float z[32];
     unpack32(in.a, z);
 #pragma unroll
     for (int i = 0; i < 32; ++i) o[i] = v[i] * gelu_grad_f(z[i]);
     stage_row_bf16(st, r, o);
+    if (want_max) mx = max_abs32(o, ncols);
   } else {
     stage_row_f32(st, r, v);
   }
+  return mx;
 }
 
 template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8>
@@ -526,6 +542,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint32_t acc = 0, acc_phase = 0, n_stored = 0;
     uint32_t n_in = 0, n_used = 0, in_par = 0;  // input tiles issued / consumed, parity per buffer
     const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.0f;
+    const bool want_max = p.ep.amax != nullptr;
+    float amax_acc = 0.0f;
     // Input tiles of chunk [col, col+32) of this warp's 32 rows -> buffer n_in & 1.
     auto issue_in = [&](int col, int row0) {
       if (!HAS_IN) return;
@@ -594,8 +612,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (EPI == EPI_GATEUP_SWIGLU) r1[i] = __float_as_uint(__uint_as_float(r1[i]) * deq);
           }
         }
-        epi_stage<EPI>(p.ep, col, reinterpret_cast<const float*>(r0), reinterpret_cast<const float*>(r1), in, sb,
-                       lane);
+        const float cm = epi_stage<EPI>(p.ep, col, reinterpret_cast<const float*>(r0),
+                                        reinterpret_cast<const float*>(r1), in, sb, lane, want_max);
+        if (row0 + lane < p.M) amax_acc = fmaxf(amax_acc, cm);
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -625,6 +644,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       mbar_wait(&in_bar[ew][b], (in_par >> b) & 1u, &no_abort, p.status, 0u, DRAIN_LIMIT_NS);
       in_par ^= 1u << b;
       ++n_used;
+    }
+    if (want_max) {
+      // The stored values are the bf16 roundings; rounding is monotone, so the
+      // largest stored magnitude is the rounding of the largest value.
+      float m = amax_acc;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) atomicMax(p.ep.amax, __float_as_uint(__bfloat162float(__float2bfloat16_rn(m))));
     }
     if (lane == 0) bulk_wait_all();  // the stores complete before the CTA may exit
     __syncwarp();

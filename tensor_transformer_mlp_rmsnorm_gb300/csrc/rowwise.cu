@@ -17,10 +17,13 @@ namespace {
 // ------------------------------------------------------------- RMSNorm fwd
 // TPR threads per row, each holding up to MAXV 16-byte vectors of the row in
 // registers: one read of x, one write of the normed row, one float rstd.
+// With `amax`, the largest stored |normed value| of the block is combined into
+// *amax (float bits, atomicMax; rounding to T is monotone, so the rounding of
+// the largest value is the largest stored value).
 template <typename T, int TPR, int MAXV>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const T* __restrict__ x, const T* __restrict__ w, float eps,
                                                           T* __restrict__ nrm, float* __restrict__ rstd, int64_t N,
-                                                          int H) {
+                                                          int H, uint32_t* __restrict__ amax) {
   constexpr int V = Vec<T>::N;
   constexpr int RPB = 256 / TPR;
   __shared__ float red[8];
@@ -51,39 +54,55 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const T* __restrict__ 
 #pragma unroll
     for (int k = 0; k < TPR / 32; ++k) ss += red[w0 + k];
   }
-  if (!active) return;
-  const float r = 1.0f / sqrtf(ss / (float)H + eps);
-  T* nr = nrm + row * H;
+  float m = 0.0f;
+  if (active) {
+    const float r = 1.0f / sqrtf(ss / (float)H + eps);
+    T* nr = nrm + row * H;
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int v = t + i * TPR;
-    if (v < nvec) {
-      float wv[V], o[V];
-      Vec<T>::load(w + v * V, wv);
+    for (int i = 0; i < MAXV; ++i) {
+      const int v = t + i * TPR;
+      if (v < nvec) {
+        float wv[V], o[V];
+        Vec<T>::load(w + v * V, wv);
 #pragma unroll
-      for (int j = 0; j < V; ++j) o[j] = xs[i][j] * r * wv[j];
-      Vec<T>::store(nr + v * V, o);
+        for (int j = 0; j < V; ++j) {
+          o[j] = xs[i][j] * r * wv[j];
+          m = fmaxf(m, fabsf(o[j]));
+        }
+        Vec<T>::store(nr + v * V, o);
+      }
+    }
+    if (t == 0) rstd[row] = r;
+  }
+  if (amax) {
+    __shared__ float redm[8];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if ((threadIdx.x & 31) == 0) redm[threadIdx.x >> 5] = m;
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      for (int k = 1; k < 8; ++k) m = fmaxf(m, redm[k]);
+      atomicMax(amax, __float_as_uint(to_f(from_f<T>(m))));
     }
   }
-  if (t == 0) rstd[row] = r;
 }
 
 template <typename T, int TPR>
 cudaError_t rmsnorm_fwd_tpr(const T* x, const T* w, float eps, T* nrm, float* rstd, int64_t N, int H,
-                            cudaStream_t st) {
+                            uint32_t* amax, cudaStream_t st) {
   const int64_t blocks = (N + (256 / TPR) - 1) / (256 / TPR);
-  rmsnorm_fwd_kernel<T, TPR, 8><<<(unsigned)blocks, 256, 0, st>>>(x, w, eps, nrm, rstd, N, H);
+  rmsnorm_fwd_kernel<T, TPR, 8><<<(unsigned)blocks, 256, 0, st>>>(x, w, eps, nrm, rstd, N, H, amax);
   return cudaGetLastError();
 }
 
 template <typename T>
 cudaError_t rmsnorm_fwd_t(const T* x, const T* w, float eps, T* nrm, float* rstd, int64_t N, int64_t H,
-                          cudaStream_t st) {
+                          uint32_t* amax, cudaStream_t st) {
   const int64_t nvec = H / Vec<T>::N;
-  if (nvec <= 32 * 8) return rmsnorm_fwd_tpr<T, 32>(x, w, eps, nrm, rstd, N, (int)H, st);
-  if (nvec <= 64 * 8) return rmsnorm_fwd_tpr<T, 64>(x, w, eps, nrm, rstd, N, (int)H, st);
-  if (nvec <= 128 * 8) return rmsnorm_fwd_tpr<T, 128>(x, w, eps, nrm, rstd, N, (int)H, st);
-  if (nvec <= 256 * 8) return rmsnorm_fwd_tpr<T, 256>(x, w, eps, nrm, rstd, N, (int)H, st);
+  if (nvec <= 32 * 8) return rmsnorm_fwd_tpr<T, 32>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
+  if (nvec <= 64 * 8) return rmsnorm_fwd_tpr<T, 64>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
+  if (nvec <= 128 * 8) return rmsnorm_fwd_tpr<T, 128>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
+  if (nvec <= 256 * 8) return rmsnorm_fwd_tpr<T, 256>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
   return cudaErrorInvalidValue;
 }
 
@@ -310,12 +329,12 @@ __global__ void __launch_bounds__(256) sgd_kernel(const SgdArgs a) {
 }  // namespace
 
 cudaError_t launch_rmsnorm_fwd(int dtype, const void* x, const void* w, float eps, void* nrm, float* rstd, int64_t N,
-                               int64_t H, cudaStream_t st) {
+                               int64_t H, cudaStream_t st, uint32_t* amax) {
   if (N <= 0) return cudaSuccess;
   if (dtype == 0)
-    return rmsnorm_fwd_t<float>((const float*)x, (const float*)w, eps, (float*)nrm, rstd, N, H, st);
+    return rmsnorm_fwd_t<float>((const float*)x, (const float*)w, eps, (float*)nrm, rstd, N, H, amax, st);
   return rmsnorm_fwd_t<__nv_bfloat16>((const __nv_bfloat16*)x, (const __nv_bfloat16*)w, eps, (__nv_bfloat16*)nrm,
-                                      rstd, N, H, st);
+                                      rstd, N, H, amax, st);
 }
 
 int rmsnorm_bwd_blocks(int64_t N, int num_sms, int shards) {

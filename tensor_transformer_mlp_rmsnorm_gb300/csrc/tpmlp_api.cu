@@ -130,7 +130,7 @@ int64_t pitch16(int64_t n) { return (n + 15) / 16 * 16; }
 // max_tokens and used with the pitch of the actual token count.
 enum Fp8Tensor { F8_NRM = 0, F8_WGU, F8_ACT, F8_WD, F8_DY, F8_DGU, F8_COUNT };
 struct Fp8Layout {
-  size_t inv, part, q[F8_COUNT], t[F8_COUNT], total;
+  size_t inv, amax, part, q[F8_COUNT], t[F8_COUNT], total;
 };
 
 Fp8Layout make_fp8_layout(const tpmlp_config& c) {
@@ -146,6 +146,7 @@ Fp8Layout make_fp8_layout(const tpmlp_config& c) {
     return o;
   };
   L.inv = take(F8_COUNT * sizeof(float));
+  L.amax = take(F8_COUNT * sizeof(float));  // maxima that producers fold in with atomicMax
   L.part = take(FP8_MAX_PARTS * sizeof(float));
   for (int i = 0; i < F8_COUNT; ++i) {
     L.q[i] = take(rows[i] * (size_t)pitch16((int64_t)cols[i]));
@@ -261,16 +262,33 @@ bool seg_ok(const tpmlp_ctx* c, int64_t b, int64_t e, int64_t extent) {
   return b % blk == 0 && (e % blk == 0 || e == extent);
 }
 
+uint32_t* fp8_amax_slot(const tpmlp_ctx* c, int tensor) {
+  return reinterpret_cast<uint32_t*>(c->ws8 + c->L8.amax) + tensor;
+}
+
+// Zero the fused maxima of the listed tensors before their producers run.
+tpmlp_status fp8_clear_amax(tpmlp_ctx* c, int first, int count) {
+  const cudaError_t e = cudaMemsetAsync(fp8_amax_slot(c, first), 0, count * sizeof(uint32_t), c->stream);
+  return e == cudaSuccess ? TPMLP_OK : c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
+}
+
 // E4M3 copies (row-major and transposed) of a bf16 tensor [rows, cols] with
-// its per-tensor scale: the amax pass, then the cast.
-tpmlp_status fp8_cast(tpmlp_ctx* c, int tensor, const void* src, int64_t rows, int64_t cols) {
+// its per-tensor scale.  With fused_amax the producer already folded the
+// tensor's maximum into its slot; otherwise an amax pass runs first.
+tpmlp_status fp8_cast(tpmlp_ctx* c, int tensor, const void* src, int64_t rows, int64_t cols,
+                      bool fused_amax = false) {
   float* part = reinterpret_cast<float*>(c->ws8 + c->L8.part);
   float* inv = reinterpret_cast<float*>(c->ws8 + c->L8.inv) + tensor;
   uint8_t* q = c->ws8 + c->L8.q[tensor];
   uint8_t* t = c->ws8 + c->L8.t[tensor];
   const int64_t n = rows * cols;
-  const int nb = n > 0 ? fp8_blocks(n, c->num_sms) : 1;
-  TPMLP_TRY(c->run(K_FP8_AMAX, [&] { return launch_fp8_amax(src, n, part, nb, c->stream); }));
+  int nb = 1;
+  if (fused_amax) {
+    part = reinterpret_cast<float*>(fp8_amax_slot(c, tensor));
+  } else {
+    nb = n > 0 ? fp8_blocks(n, c->num_sms) : 1;
+    TPMLP_TRY(c->run(K_FP8_AMAX, [&] { return launch_fp8_amax(src, n, part, nb, c->stream); }));
+  }
   return c->run(K_FP8_CAST, [&] {
     return launch_fp8_cast(src, rows, cols, q, pitch16(cols), t, pitch16(rows), part, nb, inv, c->num_sms, c->stream);
   });
@@ -465,7 +483,11 @@ tpmlp_status tpmlp_forward(tpmlp_ctx* c, int64_t tokens, const void* x, const vo
   if (tokens > 0) {
     void* nrm = c->wsp<void>(c->L.nrm);
     float* rstd = c->wsp<float>(c->L.rstd);
-    TPMLP_TRY(c->run(K_RMSNORM_FWD, [&] { return launch_rmsnorm_fwd(dt, x, norm_w, eps, nrm, rstd, tokens, H, c->stream); }));
+    if (c->fp8) TPMLP_TRY(fp8_clear_amax(c, 0, F8_COUNT));
+    uint32_t* nrm_amax = c->fp8 ? fp8_amax_slot(c, F8_NRM) : nullptr;
+    TPMLP_TRY(c->run(K_RMSNORM_FWD, [&] {
+      return launch_rmsnorm_fwd(dt, x, norm_w, eps, nrm, rstd, tokens, H, c->stream, nrm_amax);
+    }));
     if (force_timeout && dt == 0) TPMLP_TRY(c->run(K_PROBE, [&] { return launch_timeout_probe(c->status(), c->stream); }));
     GemmDesc g;
     g.M = (int)tokens;
@@ -496,10 +518,11 @@ tpmlp_status tpmlp_forward(tpmlp_ctx* c, int64_t tokens, const void* x, const vo
     g.ep.ld_out1 = F;
     const int64_t guw = c->swiglu() ? 2 * F : F;
     if (c->fp8) {
-      TPMLP_TRY(fp8_cast(c, F8_NRM, nrm, tokens, H));
+      TPMLP_TRY(fp8_cast(c, F8_NRM, nrm, tokens, H, true));
       TPMLP_TRY(fp8_cast(c, F8_WGU, w_gate_up, guw, H));
       TPMLP_TRY(fp8_cast(c, F8_WD, w_down, H, F));
       use_fp8(c, g, F8_NRM, false, pitch16(H), F8_WGU, false, pitch16(H), guw);
+      g.ep.amax = fp8_amax_slot(c, F8_ACT);
     }
     TPMLP_TRY(run_gemm(c, K_GEMM_GATEUP, g, force_timeout && dt == 1));
 
@@ -521,7 +544,7 @@ tpmlp_status tpmlp_forward(tpmlp_ctx* c, int64_t tokens, const void* x, const vo
     d.ep.ld_in0 = H;
     d.ep.vec = b_down;
     if (c->fp8) {
-      TPMLP_TRY(fp8_cast(c, F8_ACT, c->wsp<void>(c->L.act), tokens, F));
+      TPMLP_TRY(fp8_cast(c, F8_ACT, c->wsp<void>(c->L.act), tokens, F, true));
       use_fp8(c, d, F8_ACT, false, pitch16(F), F8_WD, false, pitch16(F), H);
     }
     TPMLP_TRY(run_gemm(c, K_GEMM_DOWN, d));
@@ -609,6 +632,8 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   if (c->fp8) {
     TPMLP_TRY(fp8_cast(c, F8_DY, dy, N, H));
     use_fp8(c, a, F8_DY, false, pitch16(H), F8_WD, true, pitch16(H), F);
+    TPMLP_TRY(fp8_clear_amax(c, F8_DGU, 1));
+    a.ep.amax = fp8_amax_slot(c, F8_DGU);
   }
   TPMLP_TRY(run_gemm(c, K_GEMM_DGRAD_ACT, a));
 
@@ -646,7 +671,7 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   wg.ep.out0 = dw_gate_up;
   wg.ep.ld_out0 = H;
   if (c->fp8) {
-    TPMLP_TRY(fp8_cast(c, F8_DGU, dgu, N, guw));
+    TPMLP_TRY(fp8_cast(c, F8_DGU, dgu, N, guw, true));
     use_fp8(c, wg, F8_DGU, true, pitch16(N), F8_NRM, true, pitch16(N), H);
   }
   TPMLP_TRY(run_gemm(c, K_GEMM_WGRAD_GATEUP, wg));

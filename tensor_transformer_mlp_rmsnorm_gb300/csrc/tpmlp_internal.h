@@ -57,8 +57,9 @@ cudaError_t launch_gemm_simt_f32(const GemmDesc& g, cudaStream_t st);
 cudaError_t launch_timeout_probe(uint32_t* status, cudaStream_t st);
 
 // Row-wise and reduction kernels (dtype: 0 = f32, 1 = bf16).
+// amax (optional): largest stored |normed value|, float bits, atomicMax (zeroed by the caller).
 cudaError_t launch_rmsnorm_fwd(int dtype, const void* x, const void* w, float eps, void* nrm, float* rstd,
-                               int64_t N, int64_t H, cudaStream_t st);
+                               int64_t N, int64_t H, cudaStream_t st, uint32_t* amax = nullptr);
 // RMSNorm backward blocks: a multiple of `shards` (N % shards == 0); each block
 // covers rows of one token shard only, so the per-block partials of dnorm_w
 // and db_down sum per shard.
