@@ -82,7 +82,7 @@ def source_digests() -> str:
     return ",".join(f"{fam}:{kernel_source_digest(fam)}" for fam in sorted(KERNEL_FAMILIES))
 
 
-def recorded_traffic(workload: str, t: int, tokens: int, kernel: str):
+def recorded_traffic(workload: str, t: int, tokens: int, kernel: str, precision: str = "bf16"):
     """DRAM bytes (read + write) per launch of `kernel`, from a `traffic-record:` line of an ncu
     summary under profiles/ taken on the same workload and on the current sources of the kernel's
     family; None if there is none (never measured, or the kernel changed since)."""
@@ -96,7 +96,7 @@ def recorded_traffic(workload: str, t: int, tokens: int, kernel: str):
             kv = dict(tok.split("=", 1) for tok in line.split()[1:] if "=" in tok)
             digests = dict(d.split(":", 1) for d in kv.get("digest", "").split(",") if ":" in d)
             if (kv.get("workload") == workload and kv.get("t") == str(t) and kv.get("tokens") == str(tokens)
-                    and digests.get(fam) == want and kernel in kv):
+                    and kv.get("precision", "bf16") == precision and digests.get(fam) == want and kernel in kv):
                 return float(kv[kernel]), os.path.relpath(path, ROOT)
     return None, None
 
@@ -408,7 +408,7 @@ def ours(args):
     per_launch_ms = top_ms / max(1, top_n)
     units = GEMM_UNITS if cfg.act == "swiglu" else GELU_UNITS
     gemm_ms = sum(ktimes[k][0] for k in ktimes if k in units)
-    traffic, traffic_src = recorded_traffic(cfg.name, t, N, top)
+    traffic, traffic_src = recorded_traffic(cfg.name, t, N, top, args.precision)
     # E4M3 operands: the measured bf16 peaks times the nominal dense ratio 4.5 / 2.25
     ratio, pname = (2.0, "e4m3 = 2 x measured bf16") if args.precision == "fp8" else (1.0, "bf16")
     if top in units:
