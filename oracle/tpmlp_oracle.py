@@ -25,7 +25,11 @@ Sources (web pages, cited by title and section):
   columns, B by rows ("The MLP block: column-parallel, then row-parallel").
 * "Megatron-Core Architecture: 5D Distributed Parallelism, ... FP8
   Transformer Engine" -- FP8 GEMMs with per-tensor scaling (its list of
-  Megatron-Core subsystems, item 6).
+  Megatron-Core subsystems, item 6); W_QKV split column-wise and W_out
+  row-wise with one all-reduce for the attention block.
+* "Megatron-LM Explained" -- "Self-attention: split across heads"; and the
+  TP-MLP page's closing note on grouped-query attention with complete
+  query/KV head groups per rank.
 
 Readings where the pages are silent:
 
@@ -52,6 +56,12 @@ Readings where the pages are silent:
   with saturation, products summed exactly and divided by both scales.  The
   page names delayed scaling (a scale from earlier steps' maxima) without
   defining it; the current maximum is the limiting case of that history.
+* Attention: W_qkv stacks the query, key and value rows [(n_q + 2 n_kv) d, H]
+  (no bias); scores are scaled by 1/sqrt(d); the mask is causal (GPT-style
+  decoder); no positional rotation is applied inside the sublayer; query head
+  h reads group h // (n_q / n_kv); rank r holds KV groups
+  [r n_kv / t, (r+1) n_kv / t) and their query heads; only the output
+  projection has a bias, added once after the reduction.
 * Backward formulas (never written on the pages) are derived by hand from the
   forward and pinned by central finite differences in the tests.
 
@@ -718,3 +728,167 @@ def dense_step_fp8(p: dict, x, target, eps: float, lr: float, act: str = "swiglu
     g["x"] = dy + dxn
     g["_dn"] = dn
     return {"y": y, "loss": loss, "dy": dy, "grads": g, "new_params": sgd(p, {k: g[k] for k in p}, lr)}
+
+
+# ---------------------------------------------------------------------------
+# Tensor-parallel attention sublayer (the explainer, "Self-attention: split
+# across heads"; the architecture page's W_QKV split column-wise and W_out
+# row-wise with one all-reduce; the TP-MLP page's closing note: grouped-query
+# attention with complete query/KV head groups kept together per rank).
+# Pre-RMSNorm, QKV projection, causal softmax attention per query head (each
+# query head reads the K/V of its group), output projection, bias, residual.
+# ---------------------------------------------------------------------------
+
+
+def attn_split_heads(p: dict, n_q: int, n_kv: int):
+    """W_qkv [(n_q + 2 n_kv) d, H] -> (W_q [n_q d, H], W_k [n_kv d, H], W_v [n_kv d, H]), d."""
+    rows = p["w_qkv"].shape[0]
+    d = rows // (n_q + 2 * n_kv)
+    if d * (n_q + 2 * n_kv) != rows or n_q % n_kv != 0:
+        raise ShapeError("w_qkv rows must be (n_q + 2 n_kv) d with n_q a multiple of n_kv")
+    wq = p["w_qkv"][: n_q * d]
+    wk = p["w_qkv"][n_q * d: (n_q + n_kv) * d]
+    wv = p["w_qkv"][(n_q + n_kv) * d:]
+    return wq, wk, wv, d
+
+
+def causal_softmax(s):
+    """Row softmax of s [..., S, S] over keys j <= i (the causal mask)."""
+    S = s.shape[-1]
+    mask = np.triu(np.ones((S, S), dtype=bool), k=1)
+    s = np.where(mask, -np.inf, s)
+    m = np.max(s, axis=-1, keepdims=True)
+    e = np.exp(s - m)
+    return e / np.sum(e, axis=-1, keepdims=True)
+
+
+def attention_heads(q, k, v, batch: int, n_q: int, n_kv: int, d: int):
+    """Causal attention of every (sequence, query head): q [N, n_q d], k, v
+    [N, n_kv d], tokens grouped as batch sequences of N / batch.  Returns
+    z [N, n_q d] and the probabilities P [batch, n_q, S, S]."""
+    N = q.shape[0]
+    S = N // batch
+    hpg = n_q // n_kv
+    qh = q.reshape(batch, S, n_q, d).transpose(0, 2, 1, 3)
+    kh = k.reshape(batch, S, n_kv, d).transpose(0, 2, 1, 3)
+    vh = v.reshape(batch, S, n_kv, d).transpose(0, 2, 1, 3)
+    kq = np.repeat(kh, hpg, axis=1)  # query head h reads group h // hpg
+    vq = np.repeat(vh, hpg, axis=1)
+    P = causal_softmax(qh @ kq.transpose(0, 1, 3, 2) / math.sqrt(d))
+    z = (P @ vq).transpose(0, 2, 1, 3).reshape(N, n_q * d)
+    return z, P
+
+
+def attn_dense_forward(p: dict, x, eps: float, batch: int, n_q: int, n_kv: int):
+    """y = x + Attention(RMSNorm(x) W_qkv^T) W_o^T + b_o; p holds norm_w,
+    w_qkv, w_o [H, n_q d], b_o."""
+    x = np.asarray(x, dtype=np.float64)
+    wq, wk, wv, d = attn_split_heads(p, n_q, n_kv)
+    n, rstd, xhat = rms_norm(x, p["norm_w"], eps)
+    q, k, v = linear(n, wq), linear(n, wk), linear(n, wv)
+    z, P = attention_heads(q, k, v, batch, n_q, n_kv, d)
+    y = x + linear(z, p["w_o"]) + p["b_o"]
+    return y, {"n": n, "rstd": rstd, "xhat": xhat, "q": q, "k": k, "v": v, "z": z, "P": P, "d": d,
+               "batch": batch, "n_q": n_q, "n_kv": n_kv}
+
+
+def attention_heads_backward(c: dict, dz):
+    """Gradients of the attention outputs with respect to q, k and v:
+    dP = dZ V^T, dS = P (dP - rowsum(dP P)) / sqrt(d), dQ = dS K, dK = dS^T Q,
+    dV = P^T dZ, with the K/V gradients of a group summed over its heads."""
+    batch, n_q, n_kv, d = c["batch"], c["n_q"], c["n_kv"], c["d"]
+    N = dz.shape[0]
+    S = N // batch
+    hpg = n_q // n_kv
+    P = c["P"]
+    sh = lambda t, h: t.reshape(batch, S, h, d).transpose(0, 2, 1, 3)
+    qh, kq, vq = sh(c["q"], n_q), np.repeat(sh(c["k"], n_kv), hpg, axis=1), np.repeat(sh(c["v"], n_kv), hpg, axis=1)
+    dzh = sh(dz, n_q)
+    dP = dzh @ vq.transpose(0, 1, 3, 2)
+    dS = P * (dP - np.sum(dP * P, axis=-1, keepdims=True)) / math.sqrt(d)
+    dq = dS @ kq
+    dk = (dS.transpose(0, 1, 3, 2) @ qh).reshape(batch, n_kv, hpg, S, d).sum(axis=2)
+    dv = (P.transpose(0, 1, 3, 2) @ dzh).reshape(batch, n_kv, hpg, S, d).sum(axis=2)
+    un = lambda t, h: t.transpose(0, 2, 1, 3).reshape(N, h * d)
+    return un(dq, n_q), un(dk, n_kv), un(dv, n_kv)
+
+
+def attn_dense_backward(p: dict, c: dict, dy) -> dict:
+    """Parameter and input gradients of the attention sublayer."""
+    wq, wk, wv, d = attn_split_heads(p, c["n_q"], c["n_kv"])
+    g = {"b_o": np.sum(dy, axis=0), "w_o": dy.T @ c["z"]}
+    dz = dy @ p["w_o"]
+    dq, dk, dv = attention_heads_backward(c, dz)
+    dqkv = np.concatenate([dq, dk, dv], axis=1)
+    g["w_qkv"] = dqkv.T @ c["n"]
+    dn = dqkv @ p["w_qkv"]
+    dxn, g["norm_w"] = rms_norm_backward(dn, c["xhat"], c["rstd"], p["norm_w"])
+    g["x"] = dy + dxn
+    g["_dn"] = dn
+    return g
+
+
+def attn_dense_step(p: dict, x, target, eps: float, lr: float, batch: int, n_q: int, n_kv: int) -> dict:
+    """Forward, MSE loss, backward and SGD of the attention sublayer."""
+    y, c = attn_dense_forward(p, x, eps, batch, n_q, n_kv)
+    loss, dy = mse_loss(y, target)
+    g = attn_dense_backward(p, c, dy)
+    return {"y": y, "loss": loss, "dy": dy, "grads": g, "new_params": sgd(p, {k: g[k] for k in p}, lr),
+            "cache": c}
+
+
+def attn_local_params(p: dict, t: int, rank: int, n_q: int, n_kv: int) -> dict:
+    """Rank r's slices: KV groups [r n_kv/t, (r+1) n_kv/t) with their query
+    heads (complete groups per rank), the matching rows of W_q, W_k, W_v and
+    columns of W_o; norm_w and b_o replicated."""
+    if n_kv % t != 0:
+        raise ShapeError(f"n_kv={n_kv} is not divisible by t={t}")
+    wq, wk, wv, d = attn_split_heads(p, n_q, n_kv)
+    gq, gk = n_q // t, n_kv // t
+    sq = slice(rank * gq * d, (rank + 1) * gq * d)
+    sk = slice(rank * gk * d, (rank + 1) * gk * d)
+    return {"norm_w": p["norm_w"], "w_qkv": np.concatenate([wq[sq], wk[sk], wv[sk]], axis=0),
+            "w_o": p["w_o"][:, sq], "b_o": p["b_o"]}
+
+
+def attn_sharded_step(p: dict, x, target, eps: float, lr: float, t: int, batch: int, n_q: int, n_kv: int) -> dict:
+    """One step of the t-rank decomposition: each rank runs its head groups'
+    attention on the replicated normed input and produces a partial output
+    z_r W_o,r^T; the partials are summed (the all-reduce closing attention),
+    then bias and residual.  In the backward each rank's normed-input
+    gradient is partial and is summed the same way (the f all-reduce)."""
+    x = np.asarray(x, dtype=np.float64)
+    qs = [attn_local_params(p, t, r, n_q, n_kv) for r in range(t)]
+    parts, caches = [], []
+    for r in range(t):
+        n, rstd, xhat = rms_norm(x, p["norm_w"], eps)
+        wq, wk, wv, d = attn_split_heads(qs[r], n_q // t, n_kv // t)
+        q, k, v = linear(n, wq), linear(n, wk), linear(n, wv)
+        z, P = attention_heads(q, k, v, batch, n_q // t, n_kv // t, d)
+        parts.append(linear(z, qs[r]["w_o"]))
+        caches.append({"n": n, "rstd": rstd, "xhat": xhat, "q": q, "k": k, "v": v, "z": z, "P": P, "d": d,
+                       "batch": batch, "n_q": n_q // t, "n_kv": n_kv // t})
+    y = x + reduce_from_tp_region_forward(parts) + p["b_o"]
+    loss, dy = mse_loss(y, target)
+    gl, dnl = [], []
+    for r in range(t):
+        c = caches[r]
+        g = {"w_o": dy.T @ c["z"], "b_o": np.sum(dy, axis=0)}
+        dq, dk, dv = attention_heads_backward(c, dy @ qs[r]["w_o"])
+        dqkv = np.concatenate([dq, dk, dv], axis=1)
+        g["w_qkv"] = dqkv.T @ c["n"]
+        gl.append(g)
+        dnl.append(dqkv @ qs[r]["w_qkv"])
+    dn = copy_to_tp_region_backward(dnl)
+    c0 = caches[0]
+    dxn, dnw = rms_norm_backward(dn, c0["xhat"], c0["rstd"], p["norm_w"])
+    # reassemble the sharded gradients in the dense layout
+    d = c0["d"]
+    gq = [g["w_qkv"][: (n_q // t) * d] for g in gl]
+    gk = [g["w_qkv"][(n_q // t) * d: (n_q // t + n_kv // t) * d] for g in gl]
+    gv = [g["w_qkv"][(n_q // t + n_kv // t) * d:] for g in gl]
+    grads = {"x": dy + dxn, "norm_w": dnw, "b_o": gl[0]["b_o"], "_dn": dn,
+             "w_qkv": np.concatenate(gq + gk + gv, axis=0),
+             "w_o": np.concatenate([g["w_o"] for g in gl], axis=1)}
+    return {"y": y, "loss": loss, "dy": dy, "grads": grads,
+            "new_params": sgd(p, {k: grads[k] for k in p}, lr)}
