@@ -299,6 +299,61 @@ TPMLP_API tpmlp_status tpmlp_fp8_gemm(const uint8_t* a, int64_t lda, const uint8
                                       int64_t N, int64_t K, const float* inv_scale_a, const float* inv_scale_b,
                                       float* c, int64_t ldc, uint32_t* status, void* stream);
 
+/* ---------------------------------------------------------------- attention sublayer
+ * The tensor-parallel attention sublayer ("Megatron-LM Explained",
+ * "Self-attention: split across heads"; page "Megatron-Core Architecture: 5D
+ * Distributed Parallelism, ...": W_QKV split column-wise, W_out row-wise, one
+ * all-reduce; page "Megatron tensor-parallel MLP", closing note: grouped-query
+ * attention keeping complete query/KV head groups per rank):
+ *
+ *     n = RMSNorm(x) * norm_w
+ *     [Q | K | V] = n W_qkv^T,  W_qkv [(n_q + 2 n_kv) d, H] (query, key, value rows)
+ *     Z_h = softmax_causal(Q_h K_g^T / sqrt(d)) V_g  for query head h, group g = h / (n_q / n_kv)
+ *     y = x + sum over ranks of Z_r W_o,r^T + b_o,  W_o [H, n_q d]
+ *
+ * Tokens are `batch` sequences of `seq` rows each (token-major, [batch*seq, H]);
+ * the mask is causal within each sequence.  Rank r of t owns KV groups
+ * [r n_kv/t, (r+1) n_kv/t) and their query heads; on one GPU the ranks'
+ * partial outputs and normed-input gradients are summed on chip in head
+ * order.  bf16 storage, fp32 accumulation; the scores and their gradient are
+ * materialised per (sequence, head) in the workspace (fp32 scores, bf16
+ * probabilities).  Loss: tpmlp_mse_loss_grad_noalloc.  Same conventions as
+ * the MLP calls above (caller-owned memory, asynchronous, status codes). */
+typedef struct tpattn_ctx tpattn_ctx;
+typedef struct {
+  int64_t max_tokens; /* batch * seq upper bound */
+  int64_t hidden;     /* H, a multiple of 8, at most 8192 */
+  int32_t n_heads;    /* query heads n_q, a multiple of n_kv_heads */
+  int32_t n_kv_heads; /* key/value heads n_kv (groups) */
+  int32_t head_dim;   /* d: 64, 128, 192 or 256 */
+  int32_t max_seq;    /* largest seq, a multiple of 64, at most 4096 */
+  int32_t max_t;      /* largest logical TP degree; must divide n_kv_heads */
+  int32_t dtype;      /* TPMLP_BF16 */
+  int32_t reserved;   /* must be 0 */
+} tpattn_config;
+
+TPMLP_API size_t tpattn_workspace_bytes(const tpattn_config* cfg);
+TPMLP_API tpmlp_status tpattn_create(const tpattn_config* cfg, void* cuda_stream, tpattn_ctx** out);
+TPMLP_API tpmlp_status tpattn_bind_workspace(tpattn_ctx* ctx, void* dev, size_t bytes);
+/* batch sequences of seq tokens (seq % 64 == 0, seq <= max_seq); t divides n_kv_heads.
+ * x [batch*seq, H], norm_w [H], w_qkv [(n_q+2n_kv) d, H], w_o [H, n_q d], b_o [H] -> y. */
+TPMLP_API tpmlp_status tpattn_forward(tpattn_ctx* ctx, int64_t batch, int64_t seq, const void* x, const void* norm_w,
+                                      const void* w_qkv, const void* w_o, const void* b_o, float eps, int32_t t,
+                                      void* y);
+/* dx (bf16) and float gradients dnorm_w [H], dw_qkv, dw_o, db_o. */
+TPMLP_API tpmlp_status tpattn_backward(tpattn_ctx* ctx, const void* dy, void* dx, float* dnorm_w, float* dw_qkv,
+                                       float* dw_o, float* db_o);
+TPMLP_API tpmlp_status tpattn_bind_master(tpattn_ctx* ctx, float* norm_w, float* w_qkv, float* w_o, float* b_o);
+TPMLP_API tpmlp_status tpattn_sgd_step(tpattn_ctx* ctx, float lr);
+TPMLP_API tpmlp_status tpattn_sync(tpattn_ctx* ctx);
+TPMLP_API tpmlp_status tpattn_set_timing(tpattn_ctx* ctx, int32_t enable);
+TPMLP_API int32_t tpattn_read_kernel_times(tpattn_ctx* ctx, float* ms, int64_t* launches, int32_t n);
+TPMLP_API const char* tpattn_kernel_name(int32_t id);
+TPMLP_API int32_t tpattn_num_kernel_ids(void);
+TPMLP_API uint64_t tpattn_launch_count(const tpattn_ctx* ctx);
+TPMLP_API const char* tpattn_last_error(const tpattn_ctx* ctx);
+TPMLP_API void tpattn_destroy(tpattn_ctx* ctx);
+
 /* Loss and loss gradient without any device allocation or workspace.
  *
  * The paper has no counterpart: this entry point exists for callers that

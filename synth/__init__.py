@@ -213,3 +213,55 @@ def make_optimizer_state(cfg: Config, seed: int = 1234, grad_std: float = 1e-4, 
 def param_names(act: str) -> tuple:
     return ("norm_w", "w_gate_up", "w_down", "b_down") if act == "swiglu" else \
            ("norm_w", "w_1", "b_1", "w_down", "b_down")
+
+
+@dataclasses.dataclass(frozen=True)
+class AttnConfig:
+    """One workload of the attention sublayer: batch sequences of seq tokens,
+    hidden H, n_q query heads in n_kv groups of head dimension d."""
+    name: str
+    batch: int
+    seq: int
+    hidden: int
+    n_q: int
+    n_kv: int
+    d: int
+    t_list: tuple
+    w_std: float = 0.02
+    lr: float = 1e-3
+    eps: float = 1e-6
+
+    @property
+    def tokens(self) -> int:
+        return self.batch * self.seq
+
+    @property
+    def gemm_flops(self) -> float:
+        """Algorithmic flops of one fwd+bwd step: the projections (2 N H (W + n_q d) forward, twice that
+        backward) and the attention contractions (4 per (sequence, head): S^2 d each, the causal mask
+        ignored: 2 forward, 4 backward)."""
+        N, H, d = self.tokens, self.hidden, self.d
+        W = (self.n_q + 2 * self.n_kv) * d
+        proj = 2.0 * N * H * (W + self.n_q * d)
+        att = 2.0 * self.batch * self.n_q * self.seq * self.seq * d * 2
+        return 3.0 * (proj + att)
+
+
+ATTN_CONFIGS = {
+    "attn_small": AttnConfig("attn_small", 2, 128, 256, 4, 2, 64, (1, 2)),
+    "attn_gpt_h4096": AttnConfig("attn_gpt_h4096", 4, 2048, 4096, 32, 8, 128, (8, 4)),
+}
+
+
+def make_attn_inputs(cfg: AttnConfig, seed: int = 1234) -> dict:
+    """All inputs of one attention step as float64 arrays of bf16-representable
+    values: x, target [N, H] ~ N(0, 1); norm_w ~ 1 + N(0, 0.1); w_qkv
+    [(n_q + 2 n_kv) d, H] and w_o [H, n_q d] ~ N(0, w_std); b_o ~ N(0, 0.01).
+    Streams 40..45."""
+    N, H, d = cfg.tokens, cfg.hidden, cfg.d
+    W = (cfg.n_q + 2 * cfg.n_kv) * d
+    r = round_to_bf16
+    return {"x": r(normal(seed, 40, (N, H))), "target": r(normal(seed, 41, (N, H))),
+            "norm_w": r(normal(seed, 42, (H,), 1.0, 0.1)), "w_qkv": r(normal(seed, 43, (W, H), 0.0, cfg.w_std)),
+            "w_o": r(normal(seed, 44, (H, cfg.n_q * d), 0.0, cfg.w_std)),
+            "b_o": r(normal(seed, 45, (H,), 0.0, 0.01))}

@@ -15,7 +15,7 @@ raises ``TPMLPError``.
 from .tpmlp import (  # noqa: F401
     BF16, DBG_FORCE_TIMEOUT, DBG_GEMM_SINGLE_CTA, DBG_SKIP_BWD_REDUCE, DBG_SKIP_FWD_REDUCE, DBG_SKIP_SP_GRAD_SYNC,
     ERR_ARG, ERR_ORDER, ERR_SHAPE, PREC_BF16, PREC_FP8,
-    ERR_TIMEOUT, ERR_UNSUPPORTED, F32, GELU, LIB_PATH, SWIGLU, TPMLP, AdamWParams, Config, ParamSet, TPMLPError,
+    ERR_TIMEOUT, ERR_UNSUPPORTED, F32, GELU, LIB_PATH, SWIGLU, TPMLP, TPAttn, AdamWParams, Config, ParamSet, TPMLPError,
     fp8_gemm, fp8_quantize, kernel_names, lib,
     make_config, tpmlp_create, tpmlp_workspace_bytes,
 )

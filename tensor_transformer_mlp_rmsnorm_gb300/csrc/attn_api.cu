@@ -1,0 +1,674 @@
+// C ABI of the tensor-parallel attention sublayer ("Megatron-LM Explained",
+// "Self-attention: split across heads"; the W_QKV column split and W_out row
+// split with one all-reduce on the architecture page; grouped-query attention
+// with complete head groups per rank, the TP-MLP page's closing note).
+//
+//   forward : rmsnorm_fwd -> gemm_qkv -> gemm_scores (batched Q K^T)
+//             -> softmax_fwd (causal) -> gemm_pv (batched P V) -> gemm_out_proj
+//             (the head-ordered K sum is the all-reduce, + bias + residual)
+//   backward: gemm_dz (dy W_o) -> gemm_wgrad_out -> gemm_dp (batched dZ V^T)
+//             -> gemm_dv (batched P^T dZ per query head) -> group_sum ->
+//             softmax_bwd -> gemm_dq (batched dS K) -> gemm_dk (batched
+//             dS^T Q per query head) -> group_sum -> gemm_wgrad_qkv ->
+//             gemm_dgrad_norm (every head's contribution summed on chip: the
+//             f all-reduce) -> rmsnorm_bwd_residual -> colsum_finalize
+//   sgd     : sgd_update
+// The logical degree t fixes which heads a rank owns (complete KV groups);
+// on one GPU the ranks' work is the same set of GEMMs in head order.
+#include <cuda_runtime.h>
+
+#include <cmath>
+#include <string>
+#include <vector>
+
+#include "../../include/tpmlp.h"
+#include "tpmlp_internal.h"
+
+using namespace tpmlp;
+
+namespace {
+
+enum AttnKernel {
+  A_RMSNORM_FWD = 0,
+  A_GEMM_QKV,
+  A_GEMM_SCORES,
+  A_SOFTMAX_FWD,
+  A_GEMM_PV,
+  A_GEMM_OUT,
+  A_GEMM_DZ,
+  A_GEMM_WGRAD_OUT,
+  A_GEMM_DP,
+  A_GEMM_DV,
+  A_GROUP_SUM,
+  A_SOFTMAX_BWD,
+  A_GEMM_DQ,
+  A_GEMM_DK,
+  A_GEMM_WGRAD_QKV,
+  A_GEMM_DGRAD_NORM,
+  A_RMSNORM_BWD,
+  A_COLSUM,
+  A_SGD,
+  A_COUNT
+};
+const char* const kAttnNames[A_COUNT] = {
+    "rmsnorm_fwd",     "gemm_qkv",        "gemm_scores",     "softmax_fwd",      "gemm_pv",
+    "gemm_out_proj",   "gemm_dz",         "gemm_wgrad_out",  "gemm_dp",          "gemm_dv",
+    "group_sum",       "softmax_bwd",     "gemm_dq",         "gemm_dk",          "gemm_wgrad_qkv",
+    "gemm_dgrad_norm", "rmsnorm_bwd_residual", "colsum_finalize", "sgd_update"};
+
+constexpr int MAX_PARTS = 1024;
+thread_local std::string g_attn_err;
+
+size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
+bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+struct AttnLayout {
+  size_t status, nrm, rstd, qkv, z, dz, dqkv, dnrm, scores, probs, dkv_head, part_dw, part_db, total;
+};
+
+bool attn_config_error(const tpattn_config* c, std::string* why) {
+  auto fail = [&](const char* m) {
+    if (why) *why = m;
+    return true;
+  };
+  if (!c) return fail("config is NULL");
+  if (c->dtype != TPMLP_BF16) return fail("the attention sublayer runs in bf16");
+  if (c->reserved != 0) return fail("reserved field must be 0");
+  if (c->max_tokens < 0 || c->hidden <= 0 || c->hidden % 8 != 0 || c->hidden > 8192)
+    return fail("hidden must be a positive multiple of 8, at most 8192");
+  if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads != 0)
+    return fail("n_heads must be a positive multiple of n_kv_heads");
+  if (c->head_dim < 64 || c->head_dim % 64 != 0 || c->head_dim > 256) return fail("head_dim must be 64, 128, 192 or 256");
+  if (c->max_seq < 64 || c->max_seq % 64 != 0 || c->max_seq > 4096) return fail("max_seq must be a multiple of 64, at most 4096");
+  if (c->max_t < 1 || c->n_kv_heads % c->max_t != 0) return fail("max_t must divide n_kv_heads");
+  if (c->max_tokens > (int64_t)1 << 24) return fail("max_tokens too large");
+  return false;
+}
+
+AttnLayout attn_layout(const tpattn_config& c) {
+  AttnLayout L{};
+  const size_t N = (size_t)c.max_tokens, H = (size_t)c.hidden, d = (size_t)c.head_dim;
+  const size_t W = (size_t)(c.n_heads + 2 * c.n_kv_heads) * d, Z = (size_t)c.n_heads * d;
+  const size_t SS = N * (size_t)c.max_seq * (size_t)c.n_heads;  // score elements: batch * n_q * S * S
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    const size_t o = off;
+    off = al256(off + bytes);
+    return o;
+  };
+  L.status = take(256);
+  L.nrm = take(N * H * 2);
+  L.rstd = take(N * 4);
+  L.qkv = take(N * W * 2);
+  L.z = take(N * Z * 2);
+  L.dz = take(N * Z * 2);
+  L.dqkv = take(N * W * 2);
+  L.dnrm = take(N * H * 4);
+  L.scores = take(SS * 4);   // S, then dP
+  L.probs = take(SS * 2);    // P, then dS
+  L.dkv_head = take(N * Z * 4);  // per-query-head dK or dV
+  L.part_dw = take((size_t)MAX_PARTS * H * 4);
+  L.part_db = take((size_t)MAX_PARTS * H * 4);
+  L.total = off;
+  return L;
+}
+
+}  // namespace
+
+struct tpattn_ctx {
+  tpattn_config cfg{};
+  cudaStream_t stream = nullptr;
+  int num_sms = 0;
+  uint8_t* ws = nullptr;
+  AttnLayout L{};
+  bool fwd_done = false, bwd_done = false;
+  int64_t batch = 0, seq = 0;
+  const void *x = nullptr, *norm_w = nullptr, *w_qkv = nullptr, *w_o = nullptr, *b_o = nullptr;
+  float *g_norm_w = nullptr, *g_w_qkv = nullptr, *g_w_o = nullptr, *g_b_o = nullptr;
+  float *m_norm_w = nullptr, *m_w_qkv = nullptr, *m_w_o = nullptr, *m_b_o = nullptr;
+  bool timing = false;
+  struct Rec {
+    int id;
+    cudaEvent_t a, b;
+  };
+  std::vector<Rec> recs;
+  std::vector<cudaEvent_t> spare;
+  uint64_t launches = 0;
+  std::string err;
+
+  template <typename P>
+  P* wsp(size_t off) const {
+    return reinterpret_cast<P*>(ws + off);
+  }
+  tpmlp_status fail(tpmlp_status s, const std::string& m) {
+    err = m;
+    return s;
+  }
+  cudaEvent_t event() {
+    if (!spare.empty()) {
+      cudaEvent_t e = spare.back();
+      spare.pop_back();
+      return e;
+    }
+    cudaEvent_t e = nullptr;
+    cudaEventCreate(&e);
+    return e;
+  }
+  template <typename Fn>
+  tpmlp_status run(int id, Fn&& fn) {
+    cudaEvent_t a = nullptr, b = nullptr;
+    if (timing) {
+      a = event();
+      b = event();
+      cudaEventRecord(a, stream);
+    }
+    const cudaError_t e = fn();
+    if (timing) {
+      cudaEventRecord(b, stream);
+      recs.push_back({id, a, b});
+    }
+    ++launches;
+    if (e != cudaSuccess) return fail(TPMLP_ERR_CUDA, std::string(kAttnNames[id]) + ": " + cudaGetErrorString(e));
+    return TPMLP_OK;
+  }
+  tpmlp_status gemm(int id, const GemmDesc& g) {
+    return run(id, [&] { return launch_gemm_tc(g, stream, num_sms, wsp<uint32_t>(L.status), 0); });
+  }
+};
+
+#define ATTN_TRY(expr)                 \
+  do {                                 \
+    const tpmlp_status s_ = (expr);    \
+    if (s_ != TPMLP_OK) return s_;     \
+  } while (0)
+
+namespace {
+
+// Batch index (b, g, hq) over sequences, KV groups and the query heads of a group.
+BatchDesc head_batch(int B, int n_kv, int hpg) {
+  BatchDesc bd;
+  bd.dims[0] = B;
+  bd.dims[1] = n_kv;
+  bd.dims[2] = hpg;
+  return bd;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tpattn_workspace_bytes(const tpattn_config* cfg) {
+  if (attn_config_error(cfg, nullptr)) return 0;
+  return attn_layout(*cfg).total;
+}
+
+tpmlp_status tpattn_create(const tpattn_config* cfg, void* stream, tpattn_ctx** out) {
+  if (!out) return TPMLP_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  if (attn_config_error(cfg, &why)) {
+    g_attn_err = why;
+    return TPMLP_ERR_SHAPE;
+  }
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) {
+    g_attn_err = "no CUDA device";
+    return TPMLP_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) {
+    g_attn_err = "needs an sm_103 device";
+    return TPMLP_ERR_UNSUPPORTED;
+  }
+  tpattn_ctx* c = new tpattn_ctx();
+  c->cfg = *cfg;
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->num_sms = sms;
+  c->L = attn_layout(*cfg);
+  *out = c;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpattn_bind_workspace(tpattn_ctx* c, void* dev, size_t bytes) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!dev || (reinterpret_cast<uintptr_t>(dev) & 255u)) return c->fail(TPMLP_ERR_ARG, "workspace must be 256-byte aligned");
+  if (bytes < c->L.total) return c->fail(TPMLP_ERR_ARG, "workspace too small");
+  c->ws = static_cast<uint8_t*>(dev);
+  const cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
+  return e == cudaSuccess ? TPMLP_OK : c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
+}
+
+tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const void* x, const void* norm_w,
+                            const void* w_qkv, const void* w_o, const void* b_o, float eps, int32_t t, void* y) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!c->ws) return c->fail(TPMLP_ERR_ORDER, "no workspace bound");
+  const tpattn_config& cf = c->cfg;
+  if (batch < 1 || seq < 64 || seq % 64 != 0 || seq > cf.max_seq || batch * seq > cf.max_tokens)
+    return c->fail(TPMLP_ERR_SHAPE, "seq must be a multiple of 64 within max_seq, batch * seq within max_tokens");
+  if (t < 1 || t > cf.max_t || cf.n_kv_heads % t != 0) return c->fail(TPMLP_ERR_SHAPE, "t must divide n_kv_heads");
+  if (!x || !norm_w || !w_qkv || !w_o || !b_o || !y) return c->fail(TPMLP_ERR_ARG, "NULL tensor");
+  for (const void* p : {x, norm_w, w_qkv, w_o, b_o, (const void*)y})
+    if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return c->fail(TPMLP_ERR_ARG, "eps must be finite and >= 0");
+  const int B = (int)batch, S = (int)seq, N = B * S, H = (int)cf.hidden, d = cf.head_dim;
+  const int nq = cf.n_heads, nkv = cf.n_kv_heads, hpg = nq / nkv, W = (nq + 2 * nkv) * d, Zc = nq * d;
+  c->fwd_done = c->bwd_done = false;
+  c->batch = batch;
+  c->seq = seq;
+  c->x = x;
+  c->norm_w = norm_w;
+  c->w_qkv = w_qkv;
+  c->w_o = w_o;
+  c->b_o = b_o;
+  void* nrm = c->wsp<void>(c->L.nrm);
+  void* qkv = c->wsp<void>(c->L.qkv);
+  void* z = c->wsp<void>(c->L.z);
+  float* sc = c->wsp<float>(c->L.scores);
+  void* pr = c->wsp<void>(c->L.probs);
+  ATTN_TRY(c->run(A_RMSNORM_FWD, [&] {
+    return launch_rmsnorm_fwd(1, x, norm_w, eps, nrm, c->wsp<float>(c->L.rstd), N, H, c->stream);
+  }));
+  // qkv = n W_qkv^T
+  GemmDesc g;
+  g.M = N;
+  g.N = W;
+  g.k_extent = H;
+  g.a = nrm;
+  g.lda = H;
+  g.b = w_qkv;
+  g.ldb = H;
+  g.b_rows = W;
+  g.kseg[1] = H;
+  g.epi = EPI_STORE_BF16;
+  g.ep.out0 = qkv;
+  g.ep.ld_out0 = W;
+  ATTN_TRY(c->gemm(A_GEMM_QKV, g));
+  // S[b, h] = Q_h K_g^T  (batched over sequence b, group g, head hq of the group)
+  GemmDesc s;
+  s.M = S;
+  s.N = S;
+  s.k_extent = d;
+  s.a = qkv;
+  s.lda = W;
+  s.a_ext_col = W;
+  s.a_ext_row = N;
+  s.b = qkv;
+  s.ldb = W;
+  s.b_rows = S;
+  s.b_ext_col = W;
+  s.b_ext_row = N;
+  s.kseg[1] = d;
+  s.batch = head_batch(B, nkv, hpg);
+  s.batch.a.col[2] = (int64_t)hpg * d;  // Q head g hpg + hq
+  s.batch.a.col[3] = d;
+  s.batch.a.row[1] = S;                 // sequence b
+  s.batch.b.col[0] = (int64_t)nq * d;   // K group g
+  s.batch.b.col[2] = d;
+  s.batch.b.row[1] = S;
+  s.batch.o.row[1] = (int64_t)nq * S;   // score block (b nq + g hpg + hq) S
+  s.batch.o.row[2] = (int64_t)hpg * S;
+  s.batch.o.row[3] = S;
+  s.epi = EPI_STORE_F32;
+  s.ep.out0 = sc;
+  s.ep.ld_out0 = S;
+  s.ep.out_rows = (int64_t)B * nq * S;
+  s.ep.out_cols = S;
+  ATTN_TRY(c->gemm(A_GEMM_SCORES, s));
+  const int64_t rows = (int64_t)B * nq * S;
+  const float scale = 1.0f / std::sqrt((float)d);
+  ATTN_TRY(c->run(A_SOFTMAX_FWD, [&] { return launch_attn_softmax_fwd(sc, pr, rows, S, scale, c->stream); }));
+  // Z[:, head h] = P[b, h] V_g
+  GemmDesc pv;
+  pv.M = S;
+  pv.N = d;
+  pv.k_extent = S;
+  pv.a = pr;
+  pv.lda = S;
+  pv.a_ext_col = S;
+  pv.a_ext_row = rows;
+  pv.b = qkv;
+  pv.ldb = W;
+  pv.b_mn = true;
+  pv.b_ext_col = W;
+  pv.b_ext_row = N;
+  pv.kseg[1] = S;
+  pv.batch = head_batch(B, nkv, hpg);
+  pv.batch.a.row[1] = (int64_t)nq * S;
+  pv.batch.a.row[2] = (int64_t)hpg * S;
+  pv.batch.a.row[3] = S;
+  pv.batch.b.col[0] = (int64_t)(nq + nkv) * d;  // V group g
+  pv.batch.b.col[2] = d;
+  pv.batch.b.row[1] = S;
+  pv.batch.o.col[2] = (int64_t)hpg * d;
+  pv.batch.o.col[3] = d;
+  pv.batch.o.row[1] = S;
+  pv.epi = EPI_STORE_BF16;
+  pv.ep.out0 = z;
+  pv.ep.ld_out0 = Zc;
+  pv.ep.out_rows = N;
+  pv.ep.out_cols = Zc;
+  ATTN_TRY(c->gemm(A_GEMM_PV, pv));
+  // y = x + Z W_o^T + b_o; the K loop runs over the heads in order: the
+  // ranks' partial outputs summed on chip.
+  GemmDesc o;
+  o.M = N;
+  o.N = H;
+  o.k_extent = Zc;
+  o.a = z;
+  o.lda = Zc;
+  o.b = w_o;
+  o.ldb = Zc;
+  o.b_rows = H;
+  o.kseg[1] = Zc;
+  o.epi = EPI_DOWN_RESID;
+  o.ep.out0 = y;
+  o.ep.ld_out0 = H;
+  o.ep.in0 = x;
+  o.ep.ld_in0 = H;
+  o.ep.vec = b_o;
+  ATTN_TRY(c->gemm(A_GEMM_OUT, o));
+  c->fwd_done = true;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dnorm_w, float* dw_qkv, float* dw_o,
+                             float* db_o) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!c->fwd_done) return c->fail(TPMLP_ERR_ORDER, "backward before forward");
+  if (!dy || !dx || !dnorm_w || !dw_qkv || !dw_o || !db_o) return c->fail(TPMLP_ERR_ARG, "NULL tensor");
+  for (const void* p : {dy, (const void*)dx, (const void*)dnorm_w, (const void*)dw_qkv, (const void*)dw_o,
+                        (const void*)db_o})
+    if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
+  const tpattn_config& cf = c->cfg;
+  const int B = (int)c->batch, S = (int)c->seq, N = B * S, H = (int)cf.hidden, d = cf.head_dim;
+  const int nq = cf.n_heads, nkv = cf.n_kv_heads, hpg = nq / nkv, W = (nq + 2 * nkv) * d, Zc = nq * d;
+  const int64_t rows = (int64_t)B * nq * S;
+  c->bwd_done = false;
+  c->g_norm_w = dnorm_w;
+  c->g_w_qkv = dw_qkv;
+  c->g_w_o = dw_o;
+  c->g_b_o = db_o;
+  void* nrm = c->wsp<void>(c->L.nrm);
+  void* qkv = c->wsp<void>(c->L.qkv);
+  void* z = c->wsp<void>(c->L.z);
+  void* dz = c->wsp<void>(c->L.dz);
+  void* dqkv = c->wsp<void>(c->L.dqkv);
+  float* dnrm = c->wsp<float>(c->L.dnrm);
+  float* dp = c->wsp<float>(c->L.scores);
+  void* pr = c->wsp<void>(c->L.probs);
+  float* dkv = c->wsp<float>(c->L.dkv_head);
+  // dZ = dy W_o
+  GemmDesc a;
+  a.M = N;
+  a.N = Zc;
+  a.k_extent = H;
+  a.a = dy;
+  a.lda = H;
+  a.b = c->w_o;
+  a.ldb = Zc;
+  a.b_mn = true;
+  a.kseg[1] = H;
+  a.epi = EPI_STORE_BF16;
+  a.ep.out0 = dz;
+  a.ep.ld_out0 = Zc;
+  ATTN_TRY(c->gemm(A_GEMM_DZ, a));
+  // dW_o = dy^T Z
+  GemmDesc wo;
+  wo.M = H;
+  wo.N = Zc;
+  wo.k_extent = N;
+  wo.a = dy;
+  wo.lda = H;
+  wo.a_mn = true;
+  wo.b = z;
+  wo.ldb = Zc;
+  wo.b_mn = true;
+  wo.kseg[1] = N;
+  wo.epi = EPI_STORE_F32;
+  wo.ep.out0 = dw_o;
+  wo.ep.ld_out0 = Zc;
+  ATTN_TRY(c->gemm(A_GEMM_WGRAD_OUT, wo));
+  // dP[b, h] = dZ_h V_g^T  (into the score buffer)
+  GemmDesc g;
+  g.M = S;
+  g.N = S;
+  g.k_extent = d;
+  g.a = dz;
+  g.lda = Zc;
+  g.a_ext_col = Zc;
+  g.a_ext_row = N;
+  g.b = qkv;
+  g.ldb = W;
+  g.b_rows = S;
+  g.b_ext_col = W;
+  g.b_ext_row = N;
+  g.kseg[1] = d;
+  g.batch = head_batch(B, nkv, hpg);
+  g.batch.a.col[2] = (int64_t)hpg * d;
+  g.batch.a.col[3] = d;
+  g.batch.a.row[1] = S;
+  g.batch.b.col[0] = (int64_t)(nq + nkv) * d;
+  g.batch.b.col[2] = d;
+  g.batch.b.row[1] = S;
+  g.batch.o.row[1] = (int64_t)nq * S;
+  g.batch.o.row[2] = (int64_t)hpg * S;
+  g.batch.o.row[3] = S;
+  g.epi = EPI_STORE_F32;
+  g.ep.out0 = dp;
+  g.ep.ld_out0 = S;
+  g.ep.out_rows = rows;
+  g.ep.out_cols = S;
+  ATTN_TRY(c->gemm(A_GEMM_DP, g));
+  // Per query head: dV_h = P^T dZ_h (f32), then the sum over each group's heads.
+  GemmDesc v;
+  v.M = S;
+  v.N = d;
+  v.k_extent = S;
+  v.a = pr;
+  v.lda = S;
+  v.a_mn = true;
+  v.a_ext_col = S;
+  v.a_ext_row = rows;
+  v.b = dz;
+  v.ldb = Zc;
+  v.b_mn = true;
+  v.b_ext_col = Zc;
+  v.b_ext_row = N;
+  v.kseg[1] = S;
+  v.batch = head_batch(B, nkv, hpg);
+  v.batch.a.row[1] = (int64_t)nq * S;
+  v.batch.a.row[2] = (int64_t)hpg * S;
+  v.batch.a.row[3] = S;
+  v.batch.b.col[2] = (int64_t)hpg * d;
+  v.batch.b.col[3] = d;
+  v.batch.b.row[1] = S;
+  v.batch.o.row[1] = (int64_t)nq * S;
+  v.batch.o.row[2] = (int64_t)hpg * S;
+  v.batch.o.row[3] = S;
+  v.epi = EPI_STORE_F32;
+  v.ep.out0 = dkv;
+  v.ep.ld_out0 = d;
+  v.ep.out_rows = rows;
+  v.ep.out_cols = d;
+  ATTN_TRY(c->gemm(A_GEMM_DV, v));
+  ATTN_TRY(c->run(A_GROUP_SUM, [&] {
+    return launch_attn_group_sum(dkv, dqkv, B, S, nq, nkv, d, W, (int64_t)(nq + nkv) * d, c->num_sms, c->stream);
+  }));
+  // dS = P (dP - rowsum(P dP)) / sqrt(d), over P
+  const float scale = 1.0f / std::sqrt((float)d);
+  ATTN_TRY(c->run(A_SOFTMAX_BWD, [&] { return launch_attn_softmax_bwd(pr, dp, rows, S, scale, c->stream); }));
+  // dQ_h = dS K_g  (into dqkv's query columns)
+  GemmDesc q;
+  q.M = S;
+  q.N = d;
+  q.k_extent = S;
+  q.a = pr;
+  q.lda = S;
+  q.a_ext_col = S;
+  q.a_ext_row = rows;
+  q.b = qkv;
+  q.ldb = W;
+  q.b_mn = true;
+  q.b_ext_col = W;
+  q.b_ext_row = N;
+  q.kseg[1] = S;
+  q.batch = head_batch(B, nkv, hpg);
+  q.batch.a.row[1] = (int64_t)nq * S;
+  q.batch.a.row[2] = (int64_t)hpg * S;
+  q.batch.a.row[3] = S;
+  q.batch.b.col[0] = (int64_t)nq * d;  // K group g
+  q.batch.b.col[2] = d;
+  q.batch.b.row[1] = S;
+  q.batch.o.col[2] = (int64_t)hpg * d;
+  q.batch.o.col[3] = d;
+  q.batch.o.row[1] = S;
+  q.epi = EPI_STORE_BF16;
+  q.ep.out0 = dqkv;
+  q.ep.ld_out0 = W;
+  q.ep.out_rows = N;
+  q.ep.out_cols = W;
+  ATTN_TRY(c->gemm(A_GEMM_DQ, q));
+  // Per query head: dK_h = dS^T Q_h (f32), then the sum over each group's heads.
+  GemmDesc k = v;
+  k.a = pr;
+  k.b = qkv;
+  k.ldb = W;
+  k.b_ext_col = W;
+  k.b_ext_row = N;
+  k.batch.b.col[0] = 0;  // Q head g hpg + hq
+  k.batch.b.col[2] = (int64_t)hpg * d;
+  k.batch.b.col[3] = d;
+  ATTN_TRY(c->gemm(A_GEMM_DK, k));
+  ATTN_TRY(c->run(A_GROUP_SUM, [&] {
+    return launch_attn_group_sum(dkv, dqkv, B, S, nq, nkv, d, W, (int64_t)nq * d, c->num_sms, c->stream);
+  }));
+  // dW_qkv = dqkv^T n
+  GemmDesc wq;
+  wq.M = W;
+  wq.N = H;
+  wq.k_extent = N;
+  wq.a = dqkv;
+  wq.lda = W;
+  wq.a_mn = true;
+  wq.b = nrm;
+  wq.ldb = H;
+  wq.b_mn = true;
+  wq.kseg[1] = N;
+  wq.epi = EPI_STORE_F32;
+  wq.ep.out0 = dw_qkv;
+  wq.ep.ld_out0 = H;
+  ATTN_TRY(c->gemm(A_GEMM_WGRAD_QKV, wq));
+  // dN = dqkv W_qkv: every head's contribution summed on chip (the f all-reduce)
+  GemmDesc dn;
+  dn.M = N;
+  dn.N = H;
+  dn.k_extent = W;
+  dn.a = dqkv;
+  dn.lda = W;
+  dn.b = c->w_qkv;
+  dn.ldb = H;
+  dn.b_mn = true;
+  dn.kseg[1] = W;
+  dn.epi = EPI_STORE_F32;
+  dn.ep.out0 = dnrm;
+  dn.ep.ld_out0 = H;
+  ATTN_TRY(c->gemm(A_GEMM_DGRAD_NORM, dn));
+  const int nb = rmsnorm_bwd_blocks(N, c->num_sms, 1);
+  float* pdw = c->wsp<float>(c->L.part_dw);
+  float* pdb = c->wsp<float>(c->L.part_db);
+  ATTN_TRY(c->run(A_RMSNORM_BWD, [&] {
+    return launch_rmsnorm_bwd(1, dnrm, c->x, c->wsp<float>(c->L.rstd), c->norm_w, dy, dx, pdw, pdb, N, H, 1, nb,
+                              c->stream);
+  }));
+  ATTN_TRY(c->run(A_COLSUM, [&] { return launch_colsum_finalize(pdw, dnorm_w, pdb, db_o, nb, H, c->stream); }));
+  c->bwd_done = true;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpattn_bind_master(tpattn_ctx* c, float* norm_w, float* w_qkv, float* w_o, float* b_o) {
+  if (!c) return TPMLP_ERR_ARG;
+  const bool none = !norm_w && !w_qkv && !w_o && !b_o;
+  if (!none && (!norm_w || !w_qkv || !w_o || !b_o)) return c->fail(TPMLP_ERR_ARG, "bind all master tensors or none");
+  for (const void* p : {(const void*)norm_w, (const void*)w_qkv, (const void*)w_o, (const void*)b_o})
+    if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
+  c->m_norm_w = norm_w;
+  c->m_w_qkv = w_qkv;
+  c->m_w_o = w_o;
+  c->m_b_o = b_o;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpattn_sgd_step(tpattn_ctx* c, float lr) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!c->bwd_done) return c->fail(TPMLP_ERR_ORDER, "sgd_step before backward");
+  if (!std::isfinite(lr)) return c->fail(TPMLP_ERR_ARG, "lr must be finite");
+  const tpattn_config& cf = c->cfg;
+  const int64_t H = cf.hidden, d = cf.head_dim, W = (int64_t)(cf.n_heads + 2 * cf.n_kv_heads) * d,
+                Zc = (int64_t)cf.n_heads * d;
+  SgdArgs a{};
+  a.lr = lr;
+  a.seg[a.nseg++] = SgdSeg{c->m_norm_w, c->g_norm_w, const_cast<void*>(c->norm_w), H};
+  a.seg[a.nseg++] = SgdSeg{c->m_w_qkv, c->g_w_qkv, const_cast<void*>(c->w_qkv), W * H};
+  a.seg[a.nseg++] = SgdSeg{c->m_w_o, c->g_w_o, const_cast<void*>(c->w_o), H * Zc};
+  a.seg[a.nseg++] = SgdSeg{c->m_b_o, c->g_b_o, const_cast<void*>(c->b_o), H};
+  return c->run(A_SGD, [&] { return launch_sgd(1, a, c->num_sms, c->stream); });
+}
+
+tpmlp_status tpattn_sync(tpattn_ctx* c) {
+  if (!c) return TPMLP_ERR_ARG;
+  cudaError_t e = cudaStreamSynchronize(c->stream);
+  if (e == cudaSuccess) e = cudaGetLastError();
+  if (e != cudaSuccess) return c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
+  if (!c->ws) return TPMLP_OK;
+  uint32_t st = 0;
+  e = cudaMemcpy(&st, c->wsp<uint32_t>(c->L.status), sizeof st, cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
+  if (st) {
+    cudaMemsetAsync(c->wsp<uint32_t>(c->L.status), 0, sizeof st, c->stream);
+    return c->fail(TPMLP_ERR_TIMEOUT, "a bounded device wait gave up");
+  }
+  return TPMLP_OK;
+}
+
+tpmlp_status tpattn_set_timing(tpattn_ctx* c, int32_t enable) {
+  if (!c) return TPMLP_ERR_ARG;
+  c->timing = enable != 0;
+  return TPMLP_OK;
+}
+
+int32_t tpattn_read_kernel_times(tpattn_ctx* c, float* ms, int64_t* launches, int32_t n) {
+  if (!c || !ms || !launches || n < A_COUNT) return -1;
+  cudaStreamSynchronize(c->stream);
+  for (int i = 0; i < A_COUNT; ++i) {
+    ms[i] = 0.0f;
+    launches[i] = 0;
+  }
+  for (const auto& r : c->recs) {
+    float t = 0.0f;
+    cudaEventElapsedTime(&t, r.a, r.b);
+    ms[r.id] += t;
+    launches[r.id] += 1;
+    c->spare.push_back(r.a);
+    c->spare.push_back(r.b);
+  }
+  c->recs.clear();
+  return A_COUNT;
+}
+
+const char* tpattn_kernel_name(int32_t id) { return id >= 0 && id < A_COUNT ? kAttnNames[id] : nullptr; }
+int32_t tpattn_num_kernel_ids(void) { return A_COUNT; }
+uint64_t tpattn_launch_count(const tpattn_ctx* c) { return c ? c->launches : 0; }
+const char* tpattn_last_error(const tpattn_ctx* c) { return c ? c->err.c_str() : g_attn_err.c_str(); }
+
+void tpattn_destroy(tpattn_ctx* c) {
+  if (!c) return;
+  for (auto& r : c->recs) {
+    cudaEventDestroy(r.a);
+    cudaEventDestroy(r.b);
+  }
+  for (auto e : c->spare) cudaEventDestroy(e);
+  delete c;
+}
+
+}  // extern "C"

@@ -19,7 +19,8 @@ enum EpiKind : int {
   EPI_DOWN_RESID = 2,     // y = x + acc + b_down
   EPI_DGRAD_SWIGLU = 3,   // dA = acc: store dG = dA U SiLU'(G), dU = dA SiLU(G)
   EPI_DGRAD_GELU = 4,     // dZ = acc * GeLU'(Z)
-  EPI_STORE_F32 = 5       // out = acc (float)
+  EPI_STORE_F32 = 5,      // out = acc (float)
+  EPI_STORE_BF16 = 6      // out = acc (bf16)
 };
 
 // Pointers and leading dimensions (in elements) of the epilogue's operands.
@@ -29,6 +30,7 @@ enum EpiKind : int {
 //  DGRAD_SWIGLU : in0 = GU [M, 2F], out0 = dGU [M, 2F]
 //  DGRAD_GELU   : in0 = Z [M, F], out0 = dZ [M, F]
 //  STORE_F32    : out0 = float [M, N]
+//  STORE_BF16   : out0 = bf16 [M, N] (tensor-core path only)
 struct EpiParams {
   void* out0;
   void* out1;
@@ -37,6 +39,9 @@ struct EpiParams {
   int64_t ld_out0, ld_out1, ld_in0;
   int64_t pair_off;  // F: column offset of U / dU in the paired layouts
   int M, N;          // valid output rows / columns (channels for the paired layouts)
+  // STORE_F32 / STORE_BF16: extent of the whole output tensor (rows x cols),
+  // which a batched problem fills block by block; 0 = M x N.
+  int64_t out_rows, out_cols;
   // Optional (tensor-core path): the largest magnitude of the activation
   // output (A, or dG and dU, or dZ) after bf16 rounding, as float bits,
   // combined with atomicMax (the caller zeroes it first).

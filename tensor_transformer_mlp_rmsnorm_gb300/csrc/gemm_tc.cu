@@ -102,9 +102,26 @@ struct TcParams {
   int a3d, b3d;  // MN-major operand loaded as one 3-D box per stage
   const float* deq_a;  // FP8: inverse operand scales
   const float* deq_b;
+  int tiles_per_batch;  // num_m_blk * num_n_blk
+  BatchDesc batch;
 };
 
-__device__ __forceinline__ void tile_coords(const TcParams& p, int tile, int& mb, int& nb) {
+// Coordinate shift of one operand for batch index z.
+struct Shift {
+  int col, row;
+};
+__device__ __forceinline__ Shift batch_shift(const BatchDesc& b, const BatchOffsets& o, int z) {
+  const int z2 = z % b.dims[2];
+  const int z1 = (z / b.dims[2]) % b.dims[1];
+  const int z0 = z / (b.dims[2] * b.dims[1]);
+  return Shift{(int)(o.col[0] + z0 * o.col[1] + z1 * o.col[2] + z2 * o.col[3]),
+               (int)(o.row[0] + z0 * o.row[1] + z1 * o.row[2] + z2 * o.row[3])};
+}
+
+// Tile -> (batch index, row block, column block); the raster runs inside a batch.
+__device__ __forceinline__ void tile_coords(const TcParams& p, int tile, int& mb, int& nb, int& z) {
+  z = tile / p.tiles_per_batch;
+  tile -= z * p.tiles_per_batch;
   const int per_group = p.group_m * p.num_n_blk;
   const int g = tile / per_group;
   const int first_m = g * p.group_m;
@@ -274,6 +291,8 @@ __device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const f
     for (int i = 0; i < 32; ++i) o[i] = v[i] * gelu_grad_f(z[i]);
     stage_row_bf16(st, r, o);
     if (want_max) mx = max_abs32(o, ncols);
+  } else if (EPI == EPI_STORE_BF16) {
+    stage_row_bf16(st, r, v);
   } else {
     stage_row_f32(st, r, v);
   }
@@ -364,9 +383,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t armed = 0, armed_par = 0;
       bool ok = true;
       for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
-        int mb, nb;
-        tile_coords(p, tile, mb, nb);
-        const int m0 = mb * C::TILE_M + (int)rank * BM;
+        int mb, nb, z;
+        tile_coords(p, tile, mb, nb, z);
+        const Shift sa = batch_shift(p.batch, p.batch.a, z), sbt = batch_shift(p.batch, p.batch.b, z);
+        const int m0 = mb * C::TILE_M + (int)rank * BM + (A_MN ? sa.col : sa.row);
         int brow0, brow1;  // first B row (K-major) / column (MN-major) of each 128-wide half
         if (p.paired) {
           brow0 = nb * (BN / 2);
@@ -376,6 +396,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           brow1 = nb * BN + BN / 2;
         }
         if (PAIR) brow0 = rank ? brow1 : brow0;  // each CTA of the pair holds one half
+        brow0 += B_MN ? sbt.col : sbt.row;
+        brow1 += B_MN ? sbt.col : sbt.row;
         for (int seg = 0; ok && seg < 2; ++seg) {
           for (int kb = p.kb[2 * seg]; kb < p.kb[2 * seg + 1]; ++kb) {
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
@@ -385,18 +407,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (leader) mbar_arrive_expect_tx(&full_bar[stage], C::TX_BYTES);
             armed |= 1u << stage;
             armed_par = (armed_par & ~(1u << stage)) | (phase << stage);
-            const int k0 = kb * KDepth<F8>::STAGE;
+            const int ka = kb * KDepth<F8>::STAGE + (A_MN ? sa.row : sa.col);  // A's K coordinate
+            const int k0 = kb * KDepth<F8>::STAGE + (B_MN ? sbt.row : sbt.col);  // B's K coordinate
             uint8_t* a_dst = sA + stage * C::A_BYTES;
             uint8_t* b_dst = sB + stage * C::B_BYTES;
             if (PAIR) {
               const uint32_t fb = mapa_shared(smem_u32(&full_bar[stage]), 0);  // the leader's barrier
               if (!A_MN) {
-                tma_load_2d_pair(a_dst, &map_a, fb, k0, m0);
+                tma_load_2d_pair(a_dst, &map_a, fb, ka, m0);
               } else if (p.a3d) {
-                tma_load_3d_pair(a_dst, &map_a, fb, 0, k0, m0 >> 6);
+                tma_load_3d_pair(a_dst, &map_a, fb, 0, ka, m0 >> 6);
               } else {
-                tma_load_2d_pair(a_dst, &map_a, fb, m0, k0);
-                tma_load_2d_pair(a_dst + 8192, &map_a, fb, m0 + 64, k0);
+                tma_load_2d_pair(a_dst, &map_a, fb, m0, ka);
+                tma_load_2d_pair(a_dst + 8192, &map_a, fb, m0 + 64, ka);
               }
               if (!B_MN) {
                 tma_load_2d_pair(b_dst, &map_b, fb, k0, brow0);
@@ -408,12 +431,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
               }
             } else {
               if (!A_MN) {
-                tma_load_2d(a_dst, &map_a, &full_bar[stage], k0, m0);
+                tma_load_2d(a_dst, &map_a, &full_bar[stage], ka, m0);
               } else if (p.a3d) {
-                tma_load_3d(a_dst, &map_a, &full_bar[stage], 0, k0, m0 >> 6);
+                tma_load_3d(a_dst, &map_a, &full_bar[stage], 0, ka, m0 >> 6);
               } else {
-                tma_load_2d(a_dst, &map_a, &full_bar[stage], m0, k0);
-                tma_load_2d(a_dst + 8192, &map_a, &full_bar[stage], m0 + 64, k0);
+                tma_load_2d(a_dst, &map_a, &full_bar[stage], m0, ka);
+                tma_load_2d(a_dst + 8192, &map_a, &full_bar[stage], m0 + 64, ka);
               }
               if (!B_MN) {
                 tma_load_2d(b_dst, &map_b, &full_bar[stage], k0, brow0);
@@ -556,14 +579,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ++n_in;
     };
     for (int tile = worker; tile < p.num_tiles; tile += num_workers) {
-      int mb, nb;
-      tile_coords(p, tile, mb, nb);
+      int mb, nb, z;
+      tile_coords(p, tile, mb, nb, z);
+      const Shift so = batch_shift(p.batch, p.batch.o, z);  // output / input coordinate shift
       const int row0 = mb * C::TILE_M + (int)rank * BM + q * 32;  // first row of this warp
       constexpr int CHUNKS = EPI == EPI_GATEUP_SWIGLU ? BN / 2 / 32 : BN / 32;
       const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
       // The first chunk's inputs are fetched while the tile's main loop runs,
       // each later chunk's while the previous one is computed.
-      if (col_base < p.N && row0 < p.M) issue_in(col_base, row0);
+      if (col_base < p.N && row0 < p.M) issue_in(col_base + so.col, row0 + so.row);
       int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -575,7 +599,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int col = col_base + c * 32;
         // Chunks wholly outside the output are skipped by the whole warp.
         if (col >= p.N || row0 >= p.M) break;
-        if (c + 1 < CHUNKS && col + 32 < p.N) issue_in(col + 32, row0);
+        if (c + 1 < CHUNKS && col + 32 < p.N) issue_in(col + 32 + so.col, row0 + so.row);
         tmem_ld_32x32b_x32(tbase + c * 32, r0);
         if (EPI == EPI_GATEUP_SWIGLU) tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, r1);
         EpiIn in;
@@ -618,9 +642,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_2d(&map_o0, sb, col, row0);
-          if (EpiOut<EPI>::N > 1) tma_store_2d(&map_o1, sb + 2048, col, row0);
-          if (EpiOut<EPI>::N > 2) tma_store_2d(&map_o2, sb + 4096, col, row0);
+          tma_store_2d(&map_o0, sb, col + so.col, row0 + so.row);
+          if (EpiOut<EPI>::N > 1) tma_store_2d(&map_o1, sb + 2048, col + so.col, row0 + so.row);
+          if (EpiOut<EPI>::N > 2) tma_store_2d(&map_o2, sb + 4096, col + so.col, row0 + so.row);
           bulk_commit_group();
         }
         ++n_stored;
@@ -808,7 +832,12 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   p.N = g.N;
   p.num_m_blk = (g.M + C::TILE_M - 1) / C::TILE_M;
   p.num_n_blk = g.paired ? (g.N + BN / 2 - 1) / (BN / 2) : (g.N + BN - 1) / BN;
-  p.num_tiles = p.num_m_blk * p.num_n_blk;
+  p.tiles_per_batch = p.num_m_blk * p.num_n_blk;
+  const int64_t nbatch = (int64_t)g.batch.dims[0] * g.batch.dims[1] * g.batch.dims[2];
+  if (nbatch < 1 || (int64_t)p.tiles_per_batch * nbatch > (1ll << 30)) return cudaErrorInvalidValue;
+  if (nbatch > 1 && (g.M % 32 != 0 || g.N % 32 != 0 || g.k_extent % BKE != 0)) return cudaErrorInvalidValue;
+  p.num_tiles = (int)(p.tiles_per_batch * nbatch);
+  p.batch = g.batch;
   // Tiles run in groups of group_m row blocks sweeping every column block, so
   // a group's A rows (about 32 MB) stay in L2 while B streams past them.  For
   // long contractions, where that rule gives few rows, the group is at least
@@ -844,25 +873,31 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   // per stage (fewer TMA instructions); otherwise as 64x64 2-D boxes.
   Maps mp;
   bool ok;
-  p.a3d = g.a_mn && g.M % 64 == 0;
-  p.b3d = g.b_mn && g.N % 64 == 0;
+  // Extents of the operand tensors (contiguous x strided); a batched problem
+  // reads blocks of larger tensors.
+  const uint64_t a_col = g.a_ext_col ? g.a_ext_col : (uint64_t)(g.a_mn ? g.M : g.k_extent);
+  const uint64_t a_row = g.a_ext_row ? g.a_ext_row : (uint64_t)(g.a_mn ? g.k_extent : g.M);
+  const uint64_t b_col = g.b_ext_col ? g.b_ext_col : (uint64_t)(g.b_mn ? g.N : g.k_extent);
+  const uint64_t b_row = g.b_ext_row ? g.b_ext_row : (uint64_t)(g.b_mn ? g.k_extent : g.b_rows);
+  p.a3d = g.a_mn && a_col % 64 == 0 && g.M % 64 == 0;
+  p.b3d = g.b_mn && b_col % 64 == 0 && g.N % 64 == 0;
   if (g.f8)
-    ok = make_map_u8(&mp.a, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
+    ok = make_map_u8(&mp.a, g.a, a_col, a_row, (uint64_t)g.lda, BM);
   else if (!g.a_mn)
-    ok = make_map(&mp.a, g.a, (uint64_t)g.k_extent, (uint64_t)g.M, (uint64_t)g.lda, BM);
+    ok = make_map(&mp.a, g.a, a_col, a_row, (uint64_t)g.lda, BM);
   else if (p.a3d)
-    ok = make_mn_map3(&mp.a, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, BM / 64);
+    ok = make_mn_map3(&mp.a, g.a, a_col, a_row, (uint64_t)g.lda, BM / 64);
   else
-    ok = make_map(&mp.a, g.a, (uint64_t)g.M, (uint64_t)g.k_extent, (uint64_t)g.lda, 64);
+    ok = make_map(&mp.a, g.a, a_col, a_row, (uint64_t)g.lda, 64);
   if (!ok) return cudaErrorInvalidValue;
   if (g.f8)
-    ok = make_map_u8(&mp.b, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
+    ok = make_map_u8(&mp.b, g.b, b_col, b_row, (uint64_t)g.ldb, BN / 2);
   else if (!g.b_mn)
-    ok = make_map(&mp.b, g.b, (uint64_t)g.k_extent, (uint64_t)g.b_rows, (uint64_t)g.ldb, BN / 2);
+    ok = make_map(&mp.b, g.b, b_col, b_row, (uint64_t)g.ldb, BN / 2);
   else if (p.b3d)
-    ok = make_mn_map3(&mp.b, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, C::B_ROWS / 64);
+    ok = make_mn_map3(&mp.b, g.b, b_col, b_row, (uint64_t)g.ldb, C::B_ROWS / 64);
   else
-    ok = make_map(&mp.b, g.b, (uint64_t)g.N, (uint64_t)g.k_extent, (uint64_t)g.ldb, 64);
+    ok = make_map(&mp.b, g.b, b_col, b_row, (uint64_t)g.ldb, 64);
   if (!ok) return cudaErrorInvalidValue;
   // Output maps; the paired layouts get one map per half so that stores clip
   // at the half's last channel (F) rather than at 2F.
@@ -885,7 +920,10 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
       mp.o[2] = mp.o[1];
       break;
     case EPI_STORE_F32:
-      ok = make_out_map(&mp.o[0], e.out0, true, N, M, e.ld_out0);
+    case EPI_STORE_BF16:
+      // batched problems store into one tensor holding every batch's block
+      ok = make_out_map(&mp.o[0], e.out0, g.epi == EPI_STORE_F32, e.out_cols ? (uint64_t)e.out_cols : N,
+                        e.out_rows ? (uint64_t)e.out_rows : M, e.ld_out0);
       mp.o[1] = mp.o[2] = mp.o[0];
       break;
     default:  // DOWN_RESID, DGRAD_GELU
@@ -940,6 +978,12 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
       return launch_inst<PAIR, true, true, EPI_STORE_F32>(mp, p, num_sms, st);
     case 10 + EPI_STORE_F32:
       return launch_inst<PAIR, false, true, EPI_STORE_F32>(mp, p, num_sms, st);
+    case 0 + EPI_STORE_F32:
+      return launch_inst<PAIR, false, false, EPI_STORE_F32>(mp, p, num_sms, st);
+    case 0 + EPI_STORE_BF16:
+      return launch_inst<PAIR, false, false, EPI_STORE_BF16>(mp, p, num_sms, st);
+    case 10 + EPI_STORE_BF16:
+      return launch_inst<PAIR, false, true, EPI_STORE_BF16>(mp, p, num_sms, st);
     default:
       return cudaErrorNotSupported;
   }

@@ -21,6 +21,23 @@ constexpr uint32_t STATUS_TIMEOUT = 1u;
 // paired (K-major B only): output channel n takes B rows n (gate) and
 // pair_off + n (up); the epilogue receives both sums.
 // Contraction segments [k0, k1) and [k2, k3) (k2 == k3 for one segment).
+// Batched GEMMs (tensor-core path): one problem of M x N x K per batch index
+// z = (z0, z1, z2) < dims, all with the same tensor maps.  Each operand's
+// coordinates are shifted by base + z0 s0 + z1 s1 + z2 s2, separately for its
+// contiguous ("col") and strided ("row") coordinate: for a K-major operand
+// col = k and row = m or n; for an MN-major operand col = m or n and row = k.
+// The output (and epilogue-input) coordinates shift by o.  Offsets of
+// MN-major operands' columns are multiples of 64; M and N of a batched
+// problem are multiples of 32, K of 64.
+struct BatchOffsets {
+  int64_t col[4] = {0, 0, 0, 0};  // base, s0, s1, s2
+  int64_t row[4] = {0, 0, 0, 0};
+};
+struct BatchDesc {
+  int dims[3] = {1, 1, 1};
+  BatchOffsets a, b, o;
+};
+
 struct GemmDesc {
   int M = 0, N = 0;
   int64_t k_extent = 0;  // K extent of the A/B tensors
@@ -31,6 +48,9 @@ struct GemmDesc {
   int64_t ldb = 0;
   bool b_mn = false;
   int64_t b_rows = 0;  // rows of a K-major B tensor
+  // Operand tensor extents (contiguous, strided) when they exceed the
+  // problem's own (batched problems); 0 = the problem's extents.
+  int64_t a_ext_col = 0, a_ext_row = 0, b_ext_col = 0, b_ext_row = 0;
   bool paired = false;
   int64_t pair_off = 0;
   int64_t kseg[4] = {0, 0, 0, 0};
@@ -43,6 +63,7 @@ struct GemmDesc {
   bool f8 = false;
   const float* deq_a = nullptr;
   const float* deq_b = nullptr;
+  BatchDesc batch;
 };
 
 // tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory), or
@@ -135,6 +156,15 @@ cudaError_t launch_fp8_amax(const void* src, int64_t n, float* part, int nparts,
 cudaError_t launch_fp8_cast(const void* src, int64_t rows, int64_t cols, uint8_t* dst, int64_t ld, uint8_t* dst_t,
                             int64_t ld_t, const float* part, int nparts, float* inv_scale, int num_sms,
                             cudaStream_t st);
+
+// Attention rows: P = causal softmax(scale * S) (bf16, zeros above the
+// diagonal), dS = scale * P (dP - rowsum(P dP)) written over P, and the sum
+// of per-query-head K/V gradients over each group into the QKV gradient.
+// Rows of S floats (S % 4 == 0, S <= 4096), row r at query r % S.
+cudaError_t launch_attn_softmax_fwd(const float* s, void* p, int64_t rows, int S, float scale, cudaStream_t st);
+cudaError_t launch_attn_softmax_bwd(void* p, const float* dp, int64_t rows, int S, float scale, cudaStream_t st);
+cudaError_t launch_attn_group_sum(const float* in, void* out, int batch, int S, int n_q, int n_kv, int d,
+                                  int64_t ld_out, int64_t col0, int num_sms, cudaStream_t st);
 
 // Message returned by tpmlp_last_error(NULL) on this host thread.
 void set_thread_error(const std::string& msg);

@@ -36,6 +36,13 @@ class TPMLPError(RuntimeError):
         self.status = status
 
 
+class AttnConfig(ctypes.Structure):
+    """tpattn_config."""
+    _fields_ = [("max_tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("n_heads", ctypes.c_int32),
+                ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("max_seq", ctypes.c_int32),
+                ("max_t", ctypes.c_int32), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+
+
 class ParamSet(ctypes.Structure):
     """tpmlp_param_set: one device float* per parameter (b_1 for GeLU only)."""
     _fields_ = [("norm_w", ctypes.c_void_p), ("w_gate_up", ctypes.c_void_p), ("b_1", ctypes.c_void_p),
@@ -84,6 +91,21 @@ _SIGNATURES = {
     "tpmlp_last_error": (ctypes.c_char_p, [_vp]),
     "tpmlp_destroy": (None, [_vp]),
     "tpmlp_mse_loss_grad_noalloc": (_i32, [_i32, _i64, _vp, _vp, _vp, _fp, _vp]),
+    "tpattn_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(AttnConfig)]),
+    "tpattn_create": (_i32, [ctypes.POINTER(AttnConfig), _vp, ctypes.POINTER(_vp)]),
+    "tpattn_bind_workspace": (_i32, [_vp, _vp, ctypes.c_size_t]),
+    "tpattn_forward": (_i32, [_vp, _i64, _i64, _vp, _vp, _vp, _vp, _vp, _f32, _i32, _vp]),
+    "tpattn_backward": (_i32, [_vp, _vp, _vp, _fp, _fp, _fp, _fp]),
+    "tpattn_bind_master": (_i32, [_vp, _fp, _fp, _fp, _fp]),
+    "tpattn_sgd_step": (_i32, [_vp, _f32]),
+    "tpattn_sync": (_i32, [_vp]),
+    "tpattn_set_timing": (_i32, [_vp, _i32]),
+    "tpattn_read_kernel_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int64), _i32]),
+    "tpattn_kernel_name": (ctypes.c_char_p, [_i32]),
+    "tpattn_num_kernel_ids": (_i32, []),
+    "tpattn_launch_count": (ctypes.c_uint64, [_vp]),
+    "tpattn_last_error": (ctypes.c_char_p, [_vp]),
+    "tpattn_destroy": (None, [_vp]),
     "tpmlp_fp8_quantize": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _fp, _vp, _vp]),
     "tpmlp_fp8_gemm": (_i32, [_vp, _i64, _vp, _i64, _i64, _i64, _i64, _fp, _fp, _fp, _i64, _vp, _vp]),
 }
@@ -387,3 +409,112 @@ class TPMLP:
 
     def launch_count(self) -> int:
         return int(lib().tpmlp_launch_count(self.ctx))
+
+
+def _acheck(status: int, ctx=None):
+    if status != OK:
+        msg = lib().tpattn_last_error(ctx).decode(errors="replace")
+        raise TPMLPError(status, msg or lib().tpmlp_status_string(status).decode())
+
+
+class TPAttn:
+    """The tensor-parallel attention sublayer through the C ABI (tpattn_*):
+    bf16 tensors on one CUDA device; the workspace is a torch uint8 tensor."""
+
+    def __init__(self, max_tokens: int, hidden: int, n_heads: int, n_kv_heads: int, head_dim: int,
+                 max_seq: int, max_t: int = 8, device=None, stream=None):
+        dev = torch.device(device) if device is not None else torch.device("cuda")
+        if dev.index is None:
+            dev = torch.device("cuda", torch.cuda.current_device())
+        self.device = dev
+        self.cfg = AttnConfig(max_tokens, hidden, n_heads, n_kv_heads, head_dim, max_seq, max_t, BF16, 0)
+        self.H, self.nq, self.nkv, self.d = hidden, n_heads, n_kv_heads, head_dim
+        self.W = (n_heads + 2 * n_kv_heads) * head_dim
+        self.stream = stream if stream is not None else torch.cuda.current_stream(dev)
+        ctx = ctypes.c_void_p()
+        with torch.cuda.device(dev):
+            _acheck(lib().tpattn_create(ctypes.byref(self.cfg), self.stream.cuda_stream, ctypes.byref(ctx)))
+            self.ctx = ctx
+            nbytes = int(lib().tpattn_workspace_bytes(ctypes.byref(self.cfg)))
+            self.workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+        _acheck(lib().tpattn_bind_workspace(self.ctx, _ptr(self.workspace), nbytes), self.ctx)
+        self._masters = None
+        self.tokens = None  # set by forward; the C ABI reports a backward before it
+
+    def close(self):
+        if getattr(self, "ctx", None):
+            lib().tpattn_destroy(self.ctx)
+            self.ctx = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _t(self, t, shape, dtype=torch.bfloat16, name="tensor"):
+        if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous() or t.device != self.device:
+            raise TPMLPError(ERR_ARG, f"{name}: expected contiguous {dtype} {tuple(shape)} on {self.device}")
+        return _ptr(t)
+
+    def forward(self, x, norm_w, w_qkv, w_o, b_o, eps: float, t: int, batch: int, seq: int, y=None):
+        y = torch.empty_like(x) if y is None else y
+        n = batch * seq
+        _acheck(lib().tpattn_forward(self.ctx, batch, seq, self._t(x, (n, self.H), name="x"),
+                                     self._t(norm_w, (self.H,), name="norm_w"),
+                                     self._t(w_qkv, (self.W, self.H), name="w_qkv"),
+                                     self._t(w_o, (self.H, self.nq * self.d), name="w_o"),
+                                     self._t(b_o, (self.H,), name="b_o"), float(eps), int(t),
+                                     self._t(y, (n, self.H), name="y")), self.ctx)
+        self.params = (norm_w, w_qkv, w_o, b_o)
+        self.tokens = n
+        return y
+
+    def new_grads(self):
+        f = dict(dtype=torch.float32, device=self.device)
+        return {"norm_w": torch.empty(self.H, **f), "w_qkv": torch.empty(self.W, self.H, **f),
+                "w_o": torch.empty(self.H, self.nq * self.d, **f), "b_o": torch.empty(self.H, **f)}
+
+    def backward(self, dy, dx=None, grads=None):
+        dx = torch.empty_like(dy) if dx is None else dx
+        g = self.new_grads() if grads is None else grads
+        f32 = torch.float32
+        n = dy.shape[0] if self.tokens is None else self.tokens
+        _acheck(lib().tpattn_backward(self.ctx, self._t(dy, (n, self.H), name="dy"),
+                                      self._t(dx, (n, self.H), name="dx"),
+                                      self._t(g["norm_w"], (self.H,), f32, "dnorm_w"),
+                                      self._t(g["w_qkv"], (self.W, self.H), f32, "dw_qkv"),
+                                      self._t(g["w_o"], (self.H, self.nq * self.d), f32, "dw_o"),
+                                      self._t(g["b_o"], (self.H,), f32, "db_o")), self.ctx)
+        return dx, g
+
+    def bind_master(self, m: dict | None):
+        if m is None:
+            _acheck(lib().tpattn_bind_master(self.ctx, None, None, None, None), self.ctx)
+            self._masters = None
+            return
+        f32 = torch.float32
+        _acheck(lib().tpattn_bind_master(self.ctx, self._t(m["norm_w"], (self.H,), f32, "norm_w"),
+                                         self._t(m["w_qkv"], (self.W, self.H), f32, "w_qkv"),
+                                         self._t(m["w_o"], (self.H, self.nq * self.d), f32, "w_o"),
+                                         self._t(m["b_o"], (self.H,), f32, "b_o")), self.ctx)
+        self._masters = m
+
+    def sgd_step(self, lr: float):
+        _acheck(lib().tpattn_sgd_step(self.ctx, float(lr)), self.ctx)
+
+    def sync(self):
+        _acheck(lib().tpattn_sync(self.ctx), self.ctx)
+
+    def set_timing(self, enable: bool):
+        _acheck(lib().tpattn_set_timing(self.ctx, int(bool(enable))), self.ctx)
+
+    def read_kernel_times(self) -> dict:
+        n = lib().tpattn_num_kernel_ids()
+        ms = (ctypes.c_float * n)()
+        cnt = (ctypes.c_int64 * n)()
+        lib().tpattn_read_kernel_times(self.ctx, ms, cnt, n)
+        return {lib().tpattn_kernel_name(i).decode(): (float(ms[i]), int(cnt[i])) for i in range(n) if cnt[i]}
+
+    def launch_count(self) -> int:
+        return int(lib().tpattn_launch_count(self.ctx))
