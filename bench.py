@@ -268,6 +268,144 @@ def reference_arm(args):
     return 0
 
 
+def ours_attn(args):
+    """The attention sublayer's training step (tpattn_* + the allocation-free loss) on one GPU."""
+    import torch
+    world, rank, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    else:
+        torch.cuda.set_device(0)
+    dev = torch.device("cuda", torch.cuda.current_device())
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPAttn, build
+    from tensor_transformer_mlp_rmsnorm_gb300.tpmlp import tpmlp_mse_loss_grad_noalloc
+    build.build()
+    cfg = synth.ATTN_CONFIGS[args.workload]
+    t = args.t if cfg.n_kv % args.t == 0 else cfg.t_list[0]
+    inp = synth.make_attn_inputs(cfg, seed=1234 + rank)
+    names = ("norm_w", "w_qkv", "w_o", "b_o")
+    bf = torch.bfloat16
+    p = {k: torch.from_numpy(np.ascontiguousarray(inp[k], dtype=np.float32)).to(dev).to(bf) for k in names}
+    masters = {k: torch.from_numpy(np.ascontiguousarray(inp[k], dtype=np.float32)).to(dev) for k in names}
+    x_host = torch.from_numpy(np.ascontiguousarray(inp["x"], dtype=np.float32)).to(bf).pin_memory()
+    tg_host = torch.from_numpy(np.ascontiguousarray(inp["target"], dtype=np.float32)).to(bf).pin_memory()
+    del inp
+    x, target = x_host.to(dev), tg_host.to(dev)
+    m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=t, device=dev)
+    m.bind_master(masters)
+    y, dy, dx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+    grads = m.new_grads()
+    loss = torch.zeros(1, dtype=torch.float32, device=dev)
+    loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
+    stream = m.stream
+
+    def step():
+        m.forward(x, p["norm_w"], p["w_qkv"], p["w_o"], p["b_o"], cfg.eps, t, cfg.batch, cfg.seq, y=y)
+        tpmlp_mse_loss_grad_noalloc(y, target, dy, loss, stream=stream.cuda_stream)
+        m.backward(dy, dx=dx, grads=grads)
+        m.sgd_step(cfg.lr)
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    m.sync()
+    clocks = ClockSampler(local)
+    barrier()
+    torch.cuda.synchronize()
+    clocks.start()
+    time.sleep(0.3)
+    m.set_timing(True)
+    l0 = m.launch_count()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    # the loss kernels run outside the context: 2 launches per step
+    launches = m.launch_count() - l0 + 2 * args.steps
+    ktimes = m.read_kernel_times()
+    m.set_timing(False)
+    clk = clocks.stop()
+    barrier()
+    ms = e0.elapsed_time(e1)
+    m.sync()
+    if world > 1:
+        tt = torch.tensor([ms], device=dev)
+        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+        ms = float(tt.item())
+    flops = cfg.gemm_flops
+    value = flops * args.steps * world / (ms / 1e3) / 1e12
+    barrier()
+    torch.cuda.synchronize()
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e2e_steps = max(3, args.steps // 2)
+    f0.record(stream)
+    with torch.cuda.stream(stream):
+        for _ in range(e2e_steps):
+            x.copy_(x_host, non_blocking=True)
+            target.copy_(tg_host, non_blocking=True)
+            step()
+            loss_host.copy_(loss, non_blocking=True)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    ems = f0.elapsed_time(f1)
+    m.sync()
+    if rank != 0:
+        if world > 1:
+            torch.distributed.destroy_process_group()
+        return 0
+    pk, pk_src = peaks()
+    N, H, d, S, B, nq, nkv = cfg.tokens, cfg.hidden, cfg.d, cfg.seq, cfg.batch, cfg.n_q, cfg.n_kv
+    W = (nq + 2 * nkv) * d
+    causal = 2.0 * B * nq * (S * (S + 1) / 2.0) * d  # one attention product over the causal half
+    kflops = {"gemm_qkv": 2.0 * N * H * W, "gemm_out_proj": 2.0 * N * nq * d * H, "gemm_dz": 2.0 * N * nq * d * H,
+              "gemm_wgrad_out": 2.0 * N * nq * d * H, "gemm_wgrad_qkv": 2.0 * N * H * W,
+              "gemm_dgrad_norm": 2.0 * N * H * W, "gemm_scores": causal, "gemm_pv": causal, "gemm_dp": causal,
+              "gemm_dv": causal, "gemm_dq": causal, "gemm_dk": causal}
+    top = max(ktimes, key=lambda k: ktimes[k][0])
+    per_launch = ktimes[top][0] / max(1, ktimes[top][1])
+    if top in kflops:
+        ach = kflops[top] / (per_launch / 1e3) / 1e12
+        roof = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
+                "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": None,
+                "peak_kind": f"bf16_tflops_sustained ({pk_src})", "avg_launch_ms": per_launch,
+                "note": "attention products counted over the causal half of the score square"}
+    else:
+        nbytes = {"softmax_fwd": 6.0 * B * nq * S * S, "softmax_bwd": 8.0 * B * nq * S * S}.get(top)
+        ach = nbytes / (per_launch / 1e3) / 1e9 if nbytes else None
+        roof = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
+                "frac": ach / pk["hbm_gbs"] if ach else None, "traffic": None, "avg_launch_ms": per_launch}
+    gemm_ms = sum(v[0] for k, v in ktimes.items() if k in kflops)
+    line = {
+        "metric": "TP-attention fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak",
+        "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
+        "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": f"{cfg.name}: attention sublayer, {B}x{S} tokens, hidden={H}, {nq} query heads in "
+                               f"{nkv} KV groups, head dim {d}, causal, t={t} logical shards, lr={cfg.lr}",
+                   "global_batch": B * world, "seq_len": S, "tokens_per_gpu": N, "t": t,
+                   "parallelism": f"replicas x{world}", "l2": "no flush: per-step working set >> 129 MB L2"},
+        "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
+                             "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"], "source": pk_src},
+        "gemm_only_tflops": flops * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None,
+        "kernels_ms_per_step": {k: v[0] / args.steps for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][0])},
+        "roofline": roof, "cpu_baseline": None,
+        "e2e": {"value": flops * e2e_steps * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 4, "steps": e2e_steps},
+        "clocks": clk, "gpu_launches": launches, "loss": float(loss_host.item()),
+    }
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
 def ours(args):
     import torch
     world, rank, local = dist_env()
@@ -467,7 +605,7 @@ def main():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.CONFIGS))
+    ap.add_argument("--workload", default=WORKLOAD, choices=sorted(synth.CONFIGS) + sorted(synth.ATTN_CONFIGS))
     ap.add_argument("--t", type=int, default=T_SHARDS)
     ap.add_argument("--tokens", type=int, default=0, help="override the workload's token count")
     ap.add_argument("--optimizer", choices=["sgd", "adamw"], default="sgd")
@@ -480,7 +618,13 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
+        if args.workload in synth.ATTN_CONFIGS:
+            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the MLP oracle; "
+                                                                  "run the attention oracle through the tests"}))
+            return 0
         return reference_arm(args)
+    if args.workload in synth.ATTN_CONFIGS:
+        return ours_attn(args)
     return ours(args)
 
 

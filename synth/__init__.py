@@ -237,13 +237,14 @@ class AttnConfig:
 
     @property
     def gemm_flops(self) -> float:
-        """Algorithmic flops of one fwd+bwd step: the projections (2 N H (W + n_q d) forward, twice that
-        backward) and the attention contractions (4 per (sequence, head): S^2 d each, the causal mask
-        ignored: 2 forward, 4 backward)."""
+        """Algorithmic flops of one fwd+bwd step: the projections, 2 N H (W + n_q d) forward and twice
+        that backward, and the attention contractions Q K^T and P V forward (2 S^2 d each per sequence
+        and query head) and their four backward products, each counted for the causal half of the
+        score square (S (S + 1) / 2 entries)."""
         N, H, d = self.tokens, self.hidden, self.d
         W = (self.n_q + 2 * self.n_kv) * d
         proj = 2.0 * N * H * (W + self.n_q * d)
-        att = 2.0 * self.batch * self.n_q * self.seq * self.seq * d * 2
+        att = 2.0 * 2.0 * self.batch * self.n_q * (self.seq * (self.seq + 1) / 2.0) * d
         return 3.0 * (proj + att)
 
 
