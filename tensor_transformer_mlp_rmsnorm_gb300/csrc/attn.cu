@@ -5,8 +5,8 @@
 // around them run on the tensor-core GEMM as batched problems.
 //
 // Scores are rows of S floats, one row per (sequence, query head, query i);
-// keys j > i are masked.  One warp owns a row: S / 32 values per lane in
-// registers, 16-byte accesses, warp-shuffle max and sums.
+// keys j > i are masked.  128 threads own a row, with its values in
+// registers, 16-byte accesses and warp-shuffle plus shared-memory reductions.
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -16,9 +16,8 @@
 namespace tpmlp {
 namespace {
 
-constexpr int WARPS = 8;
-constexpr int MAX_SEQ = 4096;              // 128 floats per lane
-constexpr int MAX_V4 = MAX_SEQ / 32 / 4;  // float4 per lane
+constexpr int MAX_SEQ = 4096;
+constexpr int MAX_V4 = MAX_SEQ / 4 / 128;  // float4 per thread at 128 threads per row
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll
@@ -31,23 +30,51 @@ __device__ __forceinline__ float warp_sum(float v) {
   return v;
 }
 
-// P[r, j] = exp(scale (s[r, j] - max)) / sum over j <= i, zero for j > i,
-// where i = r % S.  Lane l holds columns 4 (l + 32 v) .. +3.
+// Causal rows are only read up to the diagonal and written up to the end of
+// the diagonal's 256-column block: the GEMMs that consume P and dS contract
+// over the causal part at 256-row tile granularity, so the zeros inside the
+// diagonal block are read and the columns beyond it never are.
+constexpr int CAUSAL_BLOCK = 256;
+
+// 128 threads own a row (two rows per 256-thread block); thread t holds the
+// float4 vectors at columns 4 (t + 128 k), so a row of S <= 4096 floats sits
+// in at most 8 registers x 4 per thread.  Row maxima and sums combine the four
+// warps through shared memory.
+constexpr int ROW_THREADS = 128;
+constexpr int ROWS_PER_BLOCK = 2;
+
+__device__ __forceinline__ float row_reduce(float v, bool is_max, float (*red)[ROW_THREADS / 32]) {
+  v = is_max ? warp_max(v) : warp_sum(v);
+  const int slot = threadIdx.x / ROW_THREADS, w = (threadIdx.x % ROW_THREADS) >> 5;
+  if ((threadIdx.x & 31) == 0) red[slot][w] = v;
+  __syncthreads();
+  float r = red[slot][0];
+#pragma unroll
+  for (int k = 1; k < ROW_THREADS / 32; ++k) r = is_max ? fmaxf(r, red[slot][k]) : r + red[slot][k];
+  __syncthreads();  // red is reused by the next reduction
+  return r;
+}
+
+// P[r, j] = exp(scale (s[r, j] - max)) / sum over j <= i, zero for i < j < the
+// end of i's 256-column block, where i = r % S.
 template <int NV>
-__global__ void __launch_bounds__(WARPS * 32) softmax_fwd_kernel(const float* __restrict__ s,
-                                                                 __nv_bfloat16* __restrict__ p, int64_t rows,
-                                                                 int S, float scale_log2) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
-  if (r >= rows) return;
-  const int i = (int)(r % S);
+__global__ void __launch_bounds__(ROW_THREADS * ROWS_PER_BLOCK) softmax_fwd_kernel(const float* __restrict__ s,
+                                                                                   __nv_bfloat16* __restrict__ p,
+                                                                                   int64_t rows, int S,
+                                                                                   float scale_log2) {
+  __shared__ float red[ROWS_PER_BLOCK][ROW_THREADS / 32];
+  const int t = threadIdx.x % ROW_THREADS;
+  const int64_t r = (int64_t)blockIdx.x * ROWS_PER_BLOCK + threadIdx.x / ROW_THREADS;
+  const bool valid = r < rows;
+  const int i = valid ? (int)(r % S) : -1;
+  const int lim = valid ? min(S, (i / CAUSAL_BLOCK + 1) * CAUSAL_BLOCK) : 0;
   const float* sr = s + r * S;
   float v[NV][4];
   float m = -INFINITY;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    const int c = 4 * (lane + 32 * k);
-    if (c < S) {
+    const int c = 4 * (t + ROW_THREADS * k);
+    if (c <= i) {
       load4(sr + c, v[k]);
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -59,21 +86,23 @@ __global__ void __launch_bounds__(WARPS * 32) softmax_fwd_kernel(const float* __
       for (int e = 0; e < 4; ++e) v[k][e] = -INFINITY;
     }
   }
-  m = warp_max(m);  // finite: column 0 is always kept
+  m = row_reduce(m, true, red);  // finite for a valid row: column 0 is always kept
   float sum = 0.0f;
 #pragma unroll
   for (int k = 0; k < NV; ++k)
 #pragma unroll
     for (int e = 0; e < 4; ++e) {
-      v[k][e] = exp2f((v[k][e] - m) * scale_log2);  // masked -> 0
+      v[k][e] = valid ? exp2f((v[k][e] - m) * scale_log2) : 0.0f;  // masked -> 0
       sum += v[k][e];
     }
-  const float inv = 1.0f / warp_sum(sum);
+  sum = row_reduce(sum, false, red);
+  if (!valid) return;
+  const float inv = 1.0f / sum;
   __nv_bfloat16* pr = p + r * S;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    const int c = 4 * (lane + 32 * k);
-    if (c < S) {
+    const int c = 4 * (t + ROW_THREADS * k);
+    if (c < lim) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) v[k][e] *= inv;
       store4(pr + c, v[k]);
@@ -81,33 +110,44 @@ __global__ void __launch_bounds__(WARPS * 32) softmax_fwd_kernel(const float* __
   }
 }
 
-// dS[r, j] = scale * P[r, j] (dP[r, j] - sum_j P dP), written over P.
+// dS[r, j] = scale * P[r, j] (dP[r, j] - sum_j P dP), written over P (zeros
+// past the diagonal up to the end of its 256-column block).
 template <int NV>
-__global__ void __launch_bounds__(WARPS * 32) softmax_bwd_kernel(__nv_bfloat16* __restrict__ p,
-                                                                 const float* __restrict__ dp, int64_t rows, int S,
-                                                                 float scale) {
-  const int lane = threadIdx.x & 31;
-  const int64_t r = (int64_t)blockIdx.x * WARPS + (threadIdx.x >> 5);
-  if (r >= rows) return;
+__global__ void __launch_bounds__(ROW_THREADS * ROWS_PER_BLOCK) softmax_bwd_kernel(__nv_bfloat16* __restrict__ p,
+                                                                                   const float* __restrict__ dp,
+                                                                                   int64_t rows, int S, float scale) {
+  __shared__ float red[ROWS_PER_BLOCK][ROW_THREADS / 32];
+  const int t = threadIdx.x % ROW_THREADS;
+  const int64_t r = (int64_t)blockIdx.x * ROWS_PER_BLOCK + threadIdx.x / ROW_THREADS;
+  const bool valid = r < rows;
+  const int i = valid ? (int)(r % S) : -1;
+  const int lim = valid ? min(S, (i / CAUSAL_BLOCK + 1) * CAUSAL_BLOCK) : 0;
   __nv_bfloat16* pr = p + r * S;
   const float* dr = dp + r * S;
   float pv[NV][4], dv[NV][4];
   float dot = 0.0f;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    const int c = 4 * (lane + 32 * k);
-    if (c < S) {
+    const int c = 4 * (t + ROW_THREADS * k);
+    if (c <= i) {  // P is zero past the diagonal; dP is only computed up to the diagonal's tile
       load4(pr + c, pv[k]);
       load4(dr + c, dv[k]);
 #pragma unroll
-      for (int e = 0; e < 4; ++e) dot = fmaf(pv[k][e], dv[k][e], dot);
+      for (int e = 0; e < 4; ++e) {
+        if (c + e > i) pv[k][e] = dv[k][e] = 0.0f;
+        dot = fmaf(pv[k][e], dv[k][e], dot);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < 4; ++e) pv[k][e] = dv[k][e] = 0.0f;
     }
   }
-  dot = warp_sum(dot);
+  dot = row_reduce(dot, false, red);
+  if (!valid) return;
 #pragma unroll
   for (int k = 0; k < NV; ++k) {
-    const int c = 4 * (lane + 32 * k);
-    if (c < S) {
+    const int c = 4 * (t + ROW_THREADS * k);
+    if (c < lim) {
       float o[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[e] = scale * pv[k][e] * (dv[k][e] - dot);
@@ -144,12 +184,14 @@ __global__ void __launch_bounds__(256) group_sum_kernel(const float* __restrict_
 
 template <template <int> class K, typename... A>
 cudaError_t launch_rows(int S, int64_t rows, cudaStream_t st, A... args) {
-  const unsigned blocks = (unsigned)((rows + WARPS - 1) / WARPS);
-  const int nv = (S / 4 + 31) / 32;
-  if (nv <= 4)
+  const unsigned blocks = (unsigned)((rows + ROWS_PER_BLOCK - 1) / ROWS_PER_BLOCK);
+  const int nv = (S / 4 + ROW_THREADS - 1) / ROW_THREADS;  // float4 per thread
+  if (nv <= 1)
+    K<1>::launch(blocks, st, args...);
+  else if (nv <= 2)
+    K<2>::launch(blocks, st, args...);
+  else if (nv <= 4)
     K<4>::launch(blocks, st, args...);
-  else if (nv <= 16)
-    K<16>::launch(blocks, st, args...);
   else if (nv <= MAX_V4)
     K<MAX_V4>::launch(blocks, st, args...);
   else
@@ -161,14 +203,14 @@ template <int NV>
 struct FwdL {
   static void launch(unsigned blocks, cudaStream_t st, const float* s, __nv_bfloat16* p, int64_t rows, int S,
                      float sl2) {
-    softmax_fwd_kernel<NV><<<blocks, WARPS * 32, 0, st>>>(s, p, rows, S, sl2);
+    softmax_fwd_kernel<NV><<<blocks, ROW_THREADS * ROWS_PER_BLOCK, 0, st>>>(s, p, rows, S, sl2);
   }
 };
 template <int NV>
 struct BwdL {
   static void launch(unsigned blocks, cudaStream_t st, __nv_bfloat16* p, const float* dp, int64_t rows, int S,
                      float scale) {
-    softmax_bwd_kernel<NV><<<blocks, WARPS * 32, 0, st>>>(p, dp, rows, S, scale);
+    softmax_bwd_kernel<NV><<<blocks, ROW_THREADS * ROWS_PER_BLOCK, 0, st>>>(p, dp, rows, S, scale);
   }
 };
 

@@ -14,7 +14,10 @@
 //             f all-reduce) -> rmsnorm_bwd_residual -> colsum_finalize
 //   sgd     : sgd_update
 // The logical degree t fixes which heads a rank owns (complete KV groups);
-// on one GPU the ranks' work is the same set of GEMMs in head order.
+// on one GPU the ranks' work is the same set of GEMMs in head order.  The
+// causal mask is used at tile granularity: score tiles above the diagonal are
+// never computed, and the products with P or dS contract only over the causal
+// part of each tile row or column.
 #include <cuda_runtime.h>
 
 #include <cmath>
@@ -309,6 +312,7 @@ tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const voi
   s.batch.o.row[1] = (int64_t)nq * S;   // score block (b nq + g hpg + hq) S
   s.batch.o.row[2] = (int64_t)hpg * S;
   s.batch.o.row[3] = S;
+  s.causal = CAUSAL_SKIP_UPPER;
   s.epi = EPI_STORE_F32;
   s.ep.out0 = sc;
   s.ep.ld_out0 = S;
@@ -343,6 +347,7 @@ tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const voi
   pv.batch.o.col[2] = (int64_t)hpg * d;
   pv.batch.o.col[3] = d;
   pv.batch.o.row[1] = S;
+  pv.causal = CAUSAL_K_UPTO;
   pv.epi = EPI_STORE_BF16;
   pv.ep.out0 = z;
   pv.ep.ld_out0 = Zc;
@@ -454,6 +459,7 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   g.batch.o.row[1] = (int64_t)nq * S;
   g.batch.o.row[2] = (int64_t)hpg * S;
   g.batch.o.row[3] = S;
+  g.causal = CAUSAL_SKIP_UPPER;
   g.epi = EPI_STORE_F32;
   g.ep.out0 = dp;
   g.ep.ld_out0 = S;
@@ -486,6 +492,7 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   v.batch.o.row[1] = (int64_t)nq * S;
   v.batch.o.row[2] = (int64_t)hpg * S;
   v.batch.o.row[3] = S;
+  v.causal = CAUSAL_K_FROM;
   v.epi = EPI_STORE_F32;
   v.ep.out0 = dkv;
   v.ep.ld_out0 = d;
@@ -523,6 +530,7 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   q.batch.o.col[2] = (int64_t)hpg * d;
   q.batch.o.col[3] = d;
   q.batch.o.row[1] = S;
+  q.causal = CAUSAL_K_UPTO;
   q.epi = EPI_STORE_BF16;
   q.ep.out0 = dqkv;
   q.ep.ld_out0 = W;

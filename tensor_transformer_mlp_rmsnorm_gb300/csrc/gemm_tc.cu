@@ -104,7 +104,22 @@ struct TcParams {
   const float* deq_b;
   int tiles_per_batch;  // num_m_blk * num_n_blk
   BatchDesc batch;
+  int causal;  // CAUSAL_* restriction for attention problems
 };
+
+// Causal restrictions of attention problems (M = queries or keys of one
+// sequence): tiles wholly above the diagonal skipped (score GEMMs), or the
+// contraction over keys cut at the tile's last query (P V, dS K), or over
+// queries started at the tile's first key (P^T dZ, dS^T Q).
+__device__ __forceinline__ bool tile_active(const TcParams& p, int mb, int nb, int tile_m) {
+  return p.causal != CAUSAL_SKIP_UPPER || nb * BN <= (mb + 1) * tile_m - 1;
+}
+__device__ __forceinline__ void seg_range(const TcParams& p, int mb, int seg, int tile_m, int bke, int& lo, int& hi) {
+  lo = p.kb[2 * seg];
+  hi = p.kb[2 * seg + 1];
+  if (p.causal == CAUSAL_K_UPTO) hi = min(hi, ((mb + 1) * tile_m + bke - 1) / bke);
+  if (p.causal == CAUSAL_K_FROM) lo = max(lo, (mb * tile_m) / bke);
+}
 
 // Coordinate shift of one operand for batch index z.
 struct Shift {
@@ -385,6 +400,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
         int mb, nb, z;
         tile_coords(p, tile, mb, nb, z);
+        if (!tile_active(p, mb, nb, C::TILE_M)) continue;
         const Shift sa = batch_shift(p.batch, p.batch.a, z), sbt = batch_shift(p.batch, p.batch.b, z);
         const int m0 = mb * C::TILE_M + (int)rank * BM + (A_MN ? sa.col : sa.row);
         int brow0, brow1;  // first B row (K-major) / column (MN-major) of each 128-wide half
@@ -399,7 +415,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         brow0 += B_MN ? sbt.col : sbt.row;
         brow1 += B_MN ? sbt.col : sbt.row;
         for (int seg = 0; ok && seg < 2; ++seg) {
-          for (int kb = p.kb[2 * seg]; kb < p.kb[2 * seg + 1]; ++kb) {
+          int kb_lo, kb_hi;
+          seg_range(p, mb, seg, C::TILE_M, KDepth<F8>::STAGE, kb_lo, kb_hi);
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
               ok = false;
               break;
@@ -481,6 +499,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       int ok = !*abort_flag;
       for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
+        int mb, nb, z;
+        tile_coords(p, tile, mb, nb, z);
+        if (!tile_active(p, mb, nb, C::TILE_M)) continue;
         ok = __all_sync(0xffffffffu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status,
                                                STATUS_TIMEOUT, WAIT_LIMIT_NS));
         if (!ok) break;
@@ -488,7 +509,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t d_tmem = tmem_base + acc * BN;
         uint32_t accumulate = 0;
         for (int seg = 0; ok && seg < 2; ++seg) {
-          for (int kb = p.kb[2 * seg]; kb < p.kb[2 * seg + 1]; ++kb) {
+          int kb_lo, kb_hi;
+          seg_range(p, mb, seg, C::TILE_M, KDepth<F8>::STAGE, kb_lo, kb_hi);
+          for (int kb = kb_lo; kb < kb_hi; ++kb) {
             ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, abort_flag, p.status, STATUS_TIMEOUT,
                                                    WAIT_LIMIT_NS));
             if (!ok) break;
@@ -581,6 +604,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     for (int tile = worker; tile < p.num_tiles; tile += num_workers) {
       int mb, nb, z;
       tile_coords(p, tile, mb, nb, z);
+      if (!tile_active(p, mb, nb, C::TILE_M)) continue;
       const Shift so = batch_shift(p.batch, p.batch.o, z);  // output / input coordinate shift
       const int row0 = mb * C::TILE_M + (int)rank * BM + q * 32;  // first row of this warp
       constexpr int CHUNKS = EPI == EPI_GATEUP_SWIGLU ? BN / 2 / 32 : BN / 32;
@@ -838,6 +862,8 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
   if (nbatch > 1 && (g.M % 32 != 0 || g.N % 32 != 0 || g.k_extent % BKE != 0)) return cudaErrorInvalidValue;
   p.num_tiles = (int)(p.tiles_per_batch * nbatch);
   p.batch = g.batch;
+  p.causal = g.causal;
+  if (g.causal != CAUSAL_NONE && (g.paired || g.kseg[0] != 0 || g.kseg[3] > g.kseg[2])) return cudaErrorInvalidValue;
   // Tiles run in groups of group_m row blocks sweeping every column block, so
   // a group's A rows (about 32 MB) stay in L2 while B streams past them.  For
   // long contractions, where that rule gives few rows, the group is at least

@@ -38,6 +38,8 @@ struct BatchDesc {
   BatchOffsets a, b, o;
 };
 
+enum CausalMode { CAUSAL_NONE = 0, CAUSAL_SKIP_UPPER = 1, CAUSAL_K_UPTO = 2, CAUSAL_K_FROM = 3 };
+
 struct GemmDesc {
   int M = 0, N = 0;
   int64_t k_extent = 0;  // K extent of the A/B tensors
@@ -64,6 +66,12 @@ struct GemmDesc {
   const float* deq_a = nullptr;
   const float* deq_b = nullptr;
   BatchDesc batch;
+  // Attention problems (one segment, M = one sequence's queries or keys):
+  // SKIP_UPPER leaves out output tiles wholly above the diagonal; K_UPTO
+  // contracts only over K < the tile's last row + 1; K_FROM only over
+  // K >= the tile's first row (all at tile granularity; the entries beyond
+  // the causal boundary inside a tile must be zero in A).
+  int causal = CAUSAL_NONE;
 };
 
 // tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory), or
