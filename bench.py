@@ -377,7 +377,10 @@ def ours_attn(args):
                 "peak_kind": f"bf16_tflops_sustained ({pk_src})", "avg_launch_ms": per_launch,
                 "note": "attention products counted over the causal half of the score square"}
     else:
-        nbytes = {"softmax_fwd": 6.0 * B * nq * S * S, "softmax_bwd": 8.0 * B * nq * S * S}.get(top)
+        # causal rows: read up to the diagonal, written up to the end of the diagonal's 256-column block
+        tri = B * nq * (S * (S + 1) / 2.0)
+        pad = B * nq * S * 128.0  # mean zero tail written past the diagonal
+        nbytes = {"softmax_fwd": 4.0 * tri + 2.0 * (tri + pad), "softmax_bwd": 6.0 * tri + 2.0 * (tri + pad)}.get(top)
         ach = nbytes / (per_launch / 1e3) / 1e9 if nbytes else None
         roof = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / pk["hbm_gbs"] if ach else None, "traffic": None, "avg_launch_ms": per_launch}
