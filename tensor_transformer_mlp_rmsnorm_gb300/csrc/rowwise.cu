@@ -111,6 +111,28 @@ cudaError_t rmsnorm_fwd_t(const T* x, const T* w, float eps, T* nrm, float* rstd
 // c = mean_h(g * xhat), dx = dy + rstd * (g - xhat * c).  Each thread also
 // keeps running column sums of dN * xhat (norm weight gradient) and dy (down
 // bias gradient) for its columns; they are written as the block's partials.
+// The next row's dN, x, dy and rstd are loaded (as raw 16/8-byte vectors)
+// before the current row's reduction, so a block keeps two rows of loads in
+// flight; w is re-read from L1 each row to leave room in the register file.
+template <typename T>
+struct Raw4;  // 4 consecutive elements as loaded
+template <>
+struct Raw4<float> {
+  float4 v;
+  __device__ void load(const float* p) { v = __ldg(reinterpret_cast<const float4*>(p)); }
+  __device__ void get(float* f) const { f[0] = v.x; f[1] = v.y; f[2] = v.z; f[3] = v.w; }
+};
+template <>
+struct Raw4<__nv_bfloat16> {
+  uint2 v;
+  __device__ void load(const __nv_bfloat16* p) { v = __ldg(reinterpret_cast<const uint2*>(p)); }
+  __device__ void get(float* f) const {
+    const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+    const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+    f[0] = a.x; f[1] = a.y; f[2] = b.x; f[3] = b.y;
+  }
+};
+
 template <typename T, int MAXV>
 __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restrict__ dnrm, const T* __restrict__ x,
                                                           const float* __restrict__ rstd, const T* __restrict__ w,
@@ -120,41 +142,58 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
                                                           int rows_per_block) {
   __shared__ float red[2][8];
   const int nv = H / 4;
-  float wv[MAXV][4], adw[MAXV][4], adb[MAXV][4];
+  float adw[MAXV][4], adb[MAXV][4];
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int v = threadIdx.x + 256 * i;
+  for (int i = 0; i < MAXV; ++i)
 #pragma unroll
-    for (int j = 0; j < 4; ++j) adw[i][j] = adb[i][j] = wv[i][j] = 0.0f;
-    if (v < nv) load4(w + 4 * v, wv[i]);
-  }
+    for (int j = 0; j < 4; ++j) adw[i][j] = adb[i][j] = 0.0f;
   // Blocks tile each token shard separately, so no block's partial mixes two
   // shards (one shard spanning all N rows when the tokens are not split).
   const int64_t shard = blockIdx.x / blocks_per_shard;
   const int64_t s0 = shard * shard_rows;
   const int64_t r0 = s0 + (int64_t)(blockIdx.x % blocks_per_shard) * rows_per_block;
   const int64_t r1 = min(min(N, s0 + shard_rows), r0 + rows_per_block);
+  float4 dn_n[MAXV];
+  Raw4<T> x_n[MAXV], dy_n[MAXV];
+  float rs_n = 0.0f;
+  auto prefetch = [&](int64_t row) {
+    rs_n = __ldg(rstd + row);
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      if (v < nv) {
+        dn_n[i] = __ldg(reinterpret_cast<const float4*>(dnrm + row * H) + v);
+        x_n[i].load(x + row * H + 4 * v);
+        dy_n[i].load(dy + row * H + 4 * v);
+      }
+    }
+  };
+  if (r0 < r1) prefetch(r0);
   int par = 0;
   for (int64_t row = r0; row < r1; ++row, par ^= 1) {
-    const float rs = rstd[row];
-    float g[MAXV][4], xh[MAXV][4], d[MAXV][4];
+    float4 dn_c[MAXV];
+    Raw4<T> x_c[MAXV], dy_c[MAXV];
+#pragma unroll
+    for (int i = 0; i < MAXV; ++i) {
+      dn_c[i] = dn_n[i];
+      x_c[i] = x_n[i];
+      dy_c[i] = dy_n[i];
+    }
+    const float rs = rs_n;
+    if (row + 1 < r1) prefetch(row + 1);
     float dot = 0.0f;
 #pragma unroll
     for (int i = 0; i < MAXV; ++i) {
       const int v = threadIdx.x + 256 * i;
       if (v < nv) {
-        float dn[4], xv[4];
-        load4(dnrm + row * H + 4 * v, dn);
-        load4(x + row * H + 4 * v, xv);
-        load4(dy + row * H + 4 * v, d[i]);
+        float xv[4], wv[4];
+        x_c[i].get(xv);
+        Raw4<T> wr;
+        wr.load(w + 4 * v);
+        wr.get(wv);
+        const float dn[4] = {dn_c[i].x, dn_c[i].y, dn_c[i].z, dn_c[i].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          xh[i][j] = xv[j] * rs;
-          g[i][j] = dn[j] * wv[i][j];
-          dot = fmaf(g[i][j], xh[i][j], dot);
-          adw[i][j] = fmaf(dn[j], xh[i][j], adw[i][j]);
-          adb[i][j] += d[i][j];
-        }
+        for (int j = 0; j < 4; ++j) dot = fmaf(dn[j] * wv[j], xv[j] * rs, dot);
       }
     }
 #pragma unroll
@@ -169,9 +208,21 @@ __global__ void __launch_bounds__(256) rmsnorm_bwd_kernel(const float* __restric
     for (int i = 0; i < MAXV; ++i) {
       const int v = threadIdx.x + 256 * i;
       if (v < nv) {
-        float o[4];
+        float xv[4], wv[4], d[4], o[4];
+        x_c[i].get(xv);
+        dy_c[i].get(d);
+        Raw4<T> wr;
+        wr.load(w + 4 * v);
+        wr.get(wv);
+        const float dn[4] = {dn_c[i].x, dn_c[i].y, dn_c[i].z, dn_c[i].w};
 #pragma unroll
-        for (int j = 0; j < 4; ++j) o[j] = d[i][j] + rs * (g[i][j] - xh[i][j] * c);
+        for (int j = 0; j < 4; ++j) {
+          const float xh = xv[j] * rs;
+          const float g = dn[j] * wv[j];
+          o[j] = d[j] + rs * (g - xh * c);
+          adw[i][j] = fmaf(dn[j], xh, adw[i][j]);
+          adb[i][j] += d[j];
+        }
         store4(dx + row * H + 4 * v, o);
       }
     }
@@ -338,7 +389,7 @@ cudaError_t launch_rmsnorm_fwd(int dtype, const void* x, const void* w, float ep
 }
 
 int rmsnorm_bwd_blocks(int64_t N, int num_sms, int shards) {
-  int64_t b = 4LL * num_sms;
+  int64_t b = 2LL * num_sms;  // one wave at two resident blocks per SM
   if (b > 1024) b = 1024;
   int64_t bps = b / shards;
   if (bps > N / shards) bps = N / shards;
