@@ -15,64 +15,77 @@ namespace tpmlp {
 namespace {
 
 // ------------------------------------------------------------- RMSNorm fwd
-// TPR threads per row, each holding up to MAXV 16-byte vectors of the row in
-// registers: one read of x, one write of the normed row, one float rstd.
-// With `amax`, the largest stored |normed value| of the block is combined into
-// *amax (float bits, atomicMax; rounding to T is monotone, so the rounding of
-// the largest value is the largest stored value).
-template <typename T, int TPR, int MAXV>
+// A block of 256 threads walks rows r = blockIdx.x, + gridDim.x, ...; each
+// thread holds NVT 16-byte vectors of the row (and of w, loaded once).  The
+// next row's vectors are loaded before the current row's block-wide sum of
+// squares, so two rows of loads are in flight per block.  With `amax`, the
+// largest stored |normed value| of the block is combined into *amax (float
+// bits, atomicMax; rounding to T is monotone, so the rounding of the largest
+// value is the largest stored value).
+template <typename T, int NVT>
 __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const T* __restrict__ x, const T* __restrict__ w, float eps,
                                                           T* __restrict__ nrm, float* __restrict__ rstd, int64_t N,
                                                           int H, uint32_t* __restrict__ amax) {
   constexpr int V = Vec<T>::N;
-  constexpr int RPB = 256 / TPR;
-  __shared__ float red[8];
-  const int rib = threadIdx.x / TPR;
-  const int t = threadIdx.x % TPR;
-  const int64_t row = (int64_t)blockIdx.x * RPB + rib;
-  const bool active = row < N;
+  __shared__ float red[2][8];
   const int nvec = H / V;
-  const T* xr = x + row * H;
-  float xs[MAXV][V];
-  float ss = 0.0f;
+  float wv[NVT][V];
+  uint4 nx[NVT];  // next row, raw
 #pragma unroll
-  for (int i = 0; i < MAXV; ++i) {
-    const int v = t + i * TPR;
-    if (active && v < nvec) {
-      Vec<T>::load(xr + v * V, xs[i]);
+  for (int i = 0; i < NVT; ++i) {
+    const int v = threadIdx.x + 256 * i;
+    if (v < nvec) Vec<T>::load(w + v * V, wv[i]);
+  }
+  auto prefetch = [&](int64_t row) {
+#pragma unroll
+    for (int i = 0; i < NVT; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      if (v < nvec) nx[i] = __ldg(reinterpret_cast<const uint4*>(x + row * H + v * V));
+    }
+  };
+  float m = 0.0f;
+  int par = 0;
+  if ((int64_t)blockIdx.x < N) prefetch(blockIdx.x);
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x, par ^= 1) {
+    float xs[NVT][V];
+#pragma unroll
+    for (int i = 0; i < NVT; ++i) {
+      const int v = threadIdx.x + 256 * i;
+      if (v < nvec)
+        Vec<T>::load(reinterpret_cast<const T*>(&nx[i]), xs[i]);
+      else
+#pragma unroll
+        for (int j = 0; j < V; ++j) xs[i][j] = 0.0f;
+    }
+    if (row + gridDim.x < N) prefetch(row + gridDim.x);
+    float ss = 0.0f;
+#pragma unroll
+    for (int i = 0; i < NVT; ++i)
 #pragma unroll
       for (int j = 0; j < V; ++j) ss = fmaf(xs[i][j], xs[i][j], ss);
-    }
-  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
-  if (TPR > 32) {
-    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = ss;
+    for (int o = 16; o > 0; o >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, o);
+    if ((threadIdx.x & 31) == 0) red[par][threadIdx.x >> 5] = ss;
     __syncthreads();
     ss = 0.0f;
-    const int w0 = rib * (TPR / 32);
 #pragma unroll
-    for (int k = 0; k < TPR / 32; ++k) ss += red[w0 + k];
-  }
-  float m = 0.0f;
-  if (active) {
+    for (int k = 0; k < 8; ++k) ss += red[par][k];
     const float r = 1.0f / sqrtf(ss / (float)H + eps);
     T* nr = nrm + row * H;
 #pragma unroll
-    for (int i = 0; i < MAXV; ++i) {
-      const int v = t + i * TPR;
+    for (int i = 0; i < NVT; ++i) {
+      const int v = threadIdx.x + 256 * i;
       if (v < nvec) {
-        float wv[V], o[V];
-        Vec<T>::load(w + v * V, wv);
+        float o[V];
 #pragma unroll
         for (int j = 0; j < V; ++j) {
-          o[j] = xs[i][j] * r * wv[j];
+          o[j] = xs[i][j] * r * wv[i][j];
           m = fmaxf(m, fabsf(o[j]));
         }
         Vec<T>::store(nr + v * V, o);
       }
     }
-    if (t == 0) rstd[row] = r;
+    if (threadIdx.x == 0) rstd[row] = r;
   }
   if (amax) {
     __shared__ float redm[8];
@@ -87,11 +100,15 @@ __global__ void __launch_bounds__(256) rmsnorm_fwd_kernel(const T* __restrict__ 
   }
 }
 
-template <typename T, int TPR>
-cudaError_t rmsnorm_fwd_tpr(const T* x, const T* w, float eps, T* nrm, float* rstd, int64_t N, int H,
+template <typename T, int NVT>
+cudaError_t rmsnorm_fwd_nvt(const T* x, const T* w, float eps, T* nrm, float* rstd, int64_t N, int H,
                             uint32_t* amax, cudaStream_t st) {
-  const int64_t blocks = (N + (256 / TPR) - 1) / (256 / TPR);
-  rmsnorm_fwd_kernel<T, TPR, 8><<<(unsigned)blocks, 256, 0, st>>>(x, w, eps, nrm, rstd, N, H, amax);
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = 4LL * (sms > 0 ? sms : 1);  // one wave
+  if (blocks > N) blocks = N;
+  rmsnorm_fwd_kernel<T, NVT><<<(unsigned)blocks, 256, 0, st>>>(x, w, eps, nrm, rstd, N, H, amax);
   return cudaGetLastError();
 }
 
@@ -99,10 +116,10 @@ template <typename T>
 cudaError_t rmsnorm_fwd_t(const T* x, const T* w, float eps, T* nrm, float* rstd, int64_t N, int64_t H,
                           uint32_t* amax, cudaStream_t st) {
   const int64_t nvec = H / Vec<T>::N;
-  if (nvec <= 32 * 8) return rmsnorm_fwd_tpr<T, 32>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
-  if (nvec <= 64 * 8) return rmsnorm_fwd_tpr<T, 64>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
-  if (nvec <= 128 * 8) return rmsnorm_fwd_tpr<T, 128>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
-  if (nvec <= 256 * 8) return rmsnorm_fwd_tpr<T, 256>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
+  if (nvec <= 256) return rmsnorm_fwd_nvt<T, 1>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
+  if (nvec <= 512) return rmsnorm_fwd_nvt<T, 2>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
+  if (nvec <= 1024) return rmsnorm_fwd_nvt<T, 4>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
+  if (nvec <= 2048) return rmsnorm_fwd_nvt<T, 8>(x, w, eps, nrm, rstd, N, (int)H, amax, st);
   return cudaErrorInvalidValue;
 }
 
