@@ -20,13 +20,15 @@ def T():
 
 def declared_functions():
     text = open(HEADER).read()
-    return sorted(set(re.findall(r"^TPMLP_API\s+[\w\s\*]+?\b(tpmlp_\w+)\(", text, flags=re.M)))
+    return sorted(set(re.findall(r"^TPMLP_API\s+[\w\s\*]+?\b(tp(?:mlp|attn)_\w+)\(", text, flags=re.M)))
 
 
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for must in ("tpmlp_forward", "tpmlp_backward", "tpmlp_sgd_step", "tpmlp_mse_loss_grad", "tpmlp_create",
-                 "tpmlp_workspace_bytes", "tpmlp_bind_workspace", "tpmlp_sync", "tpmlp_destroy"):
+                 "tpmlp_workspace_bytes", "tpmlp_bind_workspace", "tpmlp_sync", "tpmlp_destroy",
+                 "tpmlp_adamw_step", "tpmlp_set_sequence_parallel", "tpmlp_set_precision", "tpmlp_fp8_quantize",
+                 "tpmlp_fp8_gemm", "tpattn_forward", "tpattn_backward", "tpattn_sgd_step"):
         assert must in names
 
 
@@ -95,3 +97,55 @@ def test_missing_library_fails_loudly(tmp_path, monkeypatch):
     monkeypatch.setattr(tpmlp, "_LIB", None)
     with pytest.raises(tpmlp.TPMLPError):
         tpmlp.lib()
+
+
+def test_fp8_and_attention_validation_without_gpu(T):
+    from tensor_transformer_mlp_rmsnorm_gb300 import tpmlp
+    L = T.lib()
+    bf = T.make_config(64, 128, 512, 8, "bf16", "swiglu")
+    f32 = T.make_config(64, 128, 512, 8, "f32", "swiglu")
+    assert L.tpmlp_fp8_workspace_bytes(ctypes.byref(bf)) > 0
+    assert L.tpmlp_fp8_workspace_bytes(ctypes.byref(f32)) == 0
+    buf = ctypes.create_string_buffer(64)  # host memory: every call below is rejected before touching it
+    p = ctypes.cast(buf, ctypes.c_void_p)
+    # cols not a multiple of 8; no output at all; negative rows
+    assert L.tpmlp_fp8_quantize(p, 4, 12, p, 16, None, 0, p, p, None) == T.ERR_SHAPE
+    assert L.tpmlp_fp8_quantize(p, 4, 16, None, 0, None, 0, p, p, None) == T.ERR_ARG
+    assert L.tpmlp_fp8_quantize(p, -1, 16, p, 16, None, 0, p, p, None) == T.ERR_SHAPE
+    # N not a multiple of 4; pitch below K
+    assert L.tpmlp_fp8_gemm(p, 16, p, 16, 4, 6, 16, p, p, p, 8, p, None) == T.ERR_SHAPE
+    assert L.tpmlp_fp8_gemm(p, 16, p, 16, 4, 8, 32, p, p, p, 8, p, None) == T.ERR_ARG
+    # attention configs
+    good = tpmlp.AttnConfig(512, 256, 4, 2, 64, 128, 2, T.BF16, 0)
+    assert L.tpattn_workspace_bytes(ctypes.byref(good)) > 0
+    bad = [dict(n_heads=3), dict(head_dim=96), dict(max_seq=100), dict(max_t=4), dict(dtype=T.F32),
+           dict(hidden=12), dict(reserved=1)]
+    for kw in bad:
+        c = tpmlp.AttnConfig(512, 256, 4, 2, 64, 128, 2, T.BF16, 0)
+        for k, v in kw.items():
+            setattr(c, k, v)
+        assert L.tpattn_workspace_bytes(ctypes.byref(c)) == 0, kw
+        ctx = ctypes.c_void_p()
+        assert L.tpattn_create(ctypes.byref(c), None, ctypes.byref(ctx)) == T.ERR_SHAPE, kw
+        assert L.tpattn_last_error(None)
+
+
+def test_traffic_record_lookup(tmp_path, monkeypatch):
+    import bench
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    (tmp_path / "profiles").mkdir()
+    csrc = tmp_path / "tensor_transformer_mlp_rmsnorm_gb300" / "csrc"
+    csrc.mkdir(parents=True)
+    for fam in bench.KERNEL_FAMILIES.values():
+        for f in fam:
+            (csrc / f).write_text("// " + f)
+    dg = dict(x.split(":") for x in bench.source_digests().split(","))
+    (tmp_path / "profiles" / "x.md").write_text(
+        "text\ntraffic-record: workload=w t=8 tokens=16 digest=gemm:%s,rowwise:deadbeef gemm_a=123 sgd_update=7\n"
+        "traffic-record: workload=w t=8 tokens=16 precision=fp8 digest=gemm:%s gemm_a=55\n" % (dg["gemm"], dg["gemm"]))
+    assert bench.recorded_traffic("w", 8, 16, "gemm_a") == (123.0, "profiles/x.md")
+    assert bench.recorded_traffic("w", 8, 16, "gemm_a", "fp8") == (55.0, "profiles/x.md")
+    assert bench.recorded_traffic("w", 8, 16, "sgd_update") == (None, None)  # rowwise digest does not match
+    assert bench.recorded_traffic("w", 4, 16, "gemm_a") == (None, None)
+    (csrc / "gemm_tc.cu").write_text("// changed")
+    assert bench.recorded_traffic("w", 8, 16, "gemm_a") == (None, None)
