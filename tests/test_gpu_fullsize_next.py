@@ -1,0 +1,114 @@
+"""Full-size checks of the E4M3 step and the attention sublayer, in the
+configurations `bench.py --precision fp8` and `bench.py --workload
+attn_gpt_h4096` time.  As in tests/test_gpu_fullsize.py, the oracle computes
+sampled token rows exactly and the reductions over tokens are checked by
+identities that hold at any size:
+
+* E4M3 step (16384 x 4096 x 14336, t = 8): y and dx of sampled rows against
+  the exact step inside the FP8 band (normwise per row, relative to the MLP
+  output for y); the MLP identities with the tolerance widened to the FP8
+  band, because the two sides of each identity quantise different tensors
+  (dy against Q(dy), W against Q(W));
+* attention (4 x 2048 tokens, hidden 4096, 32/8 heads of 128, t = 8): y of
+  sampled rows of two sequences at the bf16 tolerance (a row needs the keys
+  and values of its sequence's prefix, computed here in full for those two
+  sequences), and
+    sum(db_o)             = sum over tokens of dy
+    sum(dW_o * W_o)       = sum(dy * (y - x - b_o))
+    sum(dW_qkv * W_qkv)   = sum(dnorm_w * norm_w)   (qkv is linear in W_qkv, n = xhat * norm_w)
+    (dx - dy) . x = 0 per row.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import synth
+from oracle import tpmlp_oracle as O
+from tests._util import compare, gpu_step, to_np
+
+pytestmark = pytest.mark.gpu
+
+
+def _rows(N, seed, k=6):
+    rng = np.random.default_rng(seed)
+    return np.array(sorted({0, N - 1, N // 2} | set(int(r) for r in rng.integers(0, N, size=k))))
+
+
+def _close(a, b, rel, what):
+    assert abs(a - b) <= rel * max(abs(a), abs(b)), (what, a, b)
+
+
+def test_fp8_step_llama8b_shape():
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP
+    cfg = synth.CONFIGS["bf16_llama8b"]
+    inp = synth.make_inputs(cfg)
+    m = TPMLP(cfg.tokens, cfg.hidden, cfg.ffn, max_t=8, dtype="bf16", act="swiglu")
+    m.set_precision("fp8")
+    gpu = gpu_step(cfg, inp, 8, cfg.lr, mod=m, with_params=False)
+    rows = _rows(cfg.tokens, 3)
+    p = {k: inp[k] for k in synth.param_names(cfg.act)}
+    x = inp["x"][rows]
+    y, c = O.dense_forward(p, x, cfg.eps, cfg.act)
+    dy = (y - inp["target"][rows]) / (cfg.tokens * cfg.hidden)
+    dx = O.dense_backward(p, c, dy)["x"]
+    for r, row in enumerate(rows):
+        out_g = gpu["y"][row] - x[r]
+        out_o = y[r] - x[r]
+        assert np.linalg.norm(out_g - out_o) <= 0.1 * np.linalg.norm(out_o), row
+        assert np.linalg.norm(gpu["dx"][row] - dx[r]) <= 0.15 * np.linalg.norm(dx[r]), row
+    g = gpu["grads"]
+    gdy = gpu["dy"]
+    _close(float(np.sum(g["b_down"])), float(np.sum(gdy)), 2e-2, "sum db_down")
+    _close(float(np.sum(g["w_down"] * inp["w_down"])), float(np.sum(gdy * (gpu["y"] - inp["x"] - inp["b_down"]))),
+           0.1, "dW_down . W_down")
+    _close(float(np.sum(g["w_gate_up"] * inp["w_gate_up"])), float(np.sum(g["norm_w"] * inp["norm_w"])), 0.1,
+           "dW_gate_up . W_gate_up")
+
+
+def test_attention_gpt_h4096():
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPAttn
+    from tensor_transformer_mlp_rmsnorm_gb300.tpmlp import tpmlp_mse_loss_grad_noalloc
+    cfg = synth.ATTN_CONFIGS["attn_gpt_h4096"]
+    inp = synth.make_attn_inputs(cfg)
+    names = ("norm_w", "w_qkv", "w_o", "b_o")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
+    p = {k: dev(inp[k]) for k in names}
+    m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=8)
+    x, tgt = dev(inp["x"]), dev(inp["target"])
+    y = m.forward(x, p["norm_w"], p["w_qkv"], p["w_o"], p["b_o"], cfg.eps, 8, cfg.batch, cfg.seq)
+    dy = torch.empty_like(y)
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    tpmlp_mse_loss_grad_noalloc(y, tgt, dy, loss)
+    dx, g = m.backward(dy)
+    m.sync()
+    yg, dyg, dxg = to_np(y), to_np(dy), to_np(dx)
+    g = {k: to_np(v) for k, v in g.items()}
+    # sampled rows of two sequences, from the oracle's attention over each prefix
+    S, H, d, nq, nkv = cfg.seq, cfg.hidden, cfg.d, cfg.n_q, cfg.n_kv
+    hpg = nq // nkv
+    wq, wk, wv, _ = O.attn_split_heads({"w_qkv": inp["w_qkv"]}, nq, nkv)
+    for b, qrows in ((0, [0, 1, 255, 256, 1000, S - 1]), (3, [0, 777, S - 2, S - 1])):
+        xs = inp["x"][b * S:(b + 1) * S]
+        n, _, _ = O.rms_norm(xs, inp["norm_w"], cfg.eps)
+        k, v = O.linear(n, wk), O.linear(n, wv)
+        q = O.linear(n[qrows], wq)
+        z = np.zeros((len(qrows), nq * d))
+        for r, i in enumerate(qrows):
+            for h in range(nq):
+                gg = h // hpg
+                s = k[: i + 1, gg * d:(gg + 1) * d] @ q[r, h * d:(h + 1) * d] / math.sqrt(d)
+                e = np.exp(s - np.max(s))
+                z[r, h * d:(h + 1) * d] = (e / np.sum(e)) @ v[: i + 1, gg * d:(gg + 1) * d]
+        yo = xs[qrows] + O.linear(z, inp["w_o"]) + inp["b_o"]
+        compare("y_rows_seq%d" % b, yg[[b * S + i for i in qrows]], yo, "bf16")
+    _close(float(np.sum(g["b_o"])), float(np.sum(dyg)), 2e-2, "sum db_o")
+    _close(float(np.sum(g["w_o"] * inp["w_o"])), float(np.sum(dyg * (yg - inp["x"] - inp["b_o"]))), 2e-2,
+           "dW_o . W_o")
+    _close(float(np.sum(g["w_qkv"] * inp["w_qkv"])), float(np.sum(g["norm_w"] * inp["norm_w"])), 2e-2,
+           "dW_qkv . W_qkv")
+    dxn = dxg - dyg
+    num = np.abs(np.sum(dxn * inp["x"], axis=1))
+    den = np.sum(np.abs(dxn) * np.abs(inp["x"]), axis=1) + 1e-300
+    assert np.max(num / den) < 1e-2, float(np.max(num / den))
