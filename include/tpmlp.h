@@ -315,8 +315,12 @@ TPMLP_API tpmlp_status tpmlp_fp8_gemm(const uint8_t* a, int64_t lda, const uint8
  * the mask is causal within each sequence.  Rank r of t owns KV groups
  * [r n_kv/t, (r+1) n_kv/t) and their query heads; on one GPU the ranks'
  * partial outputs and normed-input gradients are summed on chip in head
- * order.  bf16 storage, fp32 accumulation; the scores and their gradient are
- * materialised per (sequence, head) in the workspace (fp32 scores, bf16
+ * order.  bf16 storage, fp32 accumulation.  Two kernel paths compute the
+ * same function: the fused one (default where head_dim == 128 and seq % 128
+ * == 0) streams key/value blocks through tensor memory with an online
+ * softmax and never stores scores (the backward recomputes them from each
+ * query row's log-sum-exp); the unfused one materialises the scores and their
+ * gradient per (sequence, head) in the workspace (fp32 scores, bf16
  * probabilities).  Loss: tpmlp_mse_loss_grad_noalloc.  Same conventions as
  * the MLP calls above (caller-owned memory, asynchronous, status codes). */
 typedef struct tpattn_ctx tpattn_ctx;
@@ -344,6 +348,13 @@ TPMLP_API tpmlp_status tpattn_forward(tpattn_ctx* ctx, int64_t batch, int64_t se
 TPMLP_API tpmlp_status tpattn_backward(tpattn_ctx* ctx, const void* dy, void* dx, float* dnorm_w, float* dw_qkv,
                                        float* dw_o, float* db_o);
 TPMLP_API tpmlp_status tpattn_bind_master(tpattn_ctx* ctx, float* norm_w, float* w_qkv, float* w_o, float* b_o);
+/* enable != 0 (the default): forwards whose shape allows it (head_dim 128,
+ * seq % 128 == 0) run the fused attention kernels; 0: always the unfused
+ * path.  Takes effect at the next tpattn_forward; a backward follows the path
+ * of its forward. */
+TPMLP_API tpmlp_status tpattn_set_fused(tpattn_ctx* ctx, int32_t enable);
+/* 1 if the last tpattn_forward ran the fused kernels, 0 if not (or no forward yet). */
+TPMLP_API int32_t tpattn_fused_active(const tpattn_ctx* ctx);
 TPMLP_API tpmlp_status tpattn_sgd_step(tpattn_ctx* ctx, float lr);
 TPMLP_API tpmlp_status tpattn_sync(tpattn_ctx* ctx);
 TPMLP_API tpmlp_status tpattn_set_timing(tpattn_ctx* ctx, int32_t enable);

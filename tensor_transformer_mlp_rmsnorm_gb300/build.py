@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libtpmlp.so")
-SOURCES = ["gemm_tc.cu", "gemm_simt.cu", "rowwise.cu", "optim.cu", "fp8.cu", "attn.cu", "attn_api.cu", "tpmlp_api.cu", "noalloc.cu"]
+SOURCES = ["gemm_tc.cu", "gemm_simt.cu", "rowwise.cu", "optim.cu", "fp8.cu", "attn.cu", "flash_attn.cu", "attn_api.cu", "tpmlp_api.cu", "noalloc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
 

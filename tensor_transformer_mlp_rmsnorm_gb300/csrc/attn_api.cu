@@ -13,6 +13,11 @@
 //             gemm_dgrad_norm (every head's contribution summed on chip: the
 //             f all-reduce) -> rmsnorm_bwd_residual -> colsum_finalize
 //   sgd     : sgd_update
+// Fused path (head_dim 128, seq % 128 == 0; the default): gemm_scores ->
+// softmax_fwd -> gemm_pv become flash_attn_fwd (Z and each row's log-sum-exp),
+// and gemm_dp .. group_sum become flash_bwd_prep (D = rowsum(dZ o Z), dQ
+// accumulator cleared) -> flash_attn_bwd (dK, dV per group into dqkv, dQ added
+// into the accumulator) -> flash_dq_cast.
 // The logical degree t fixes which heads a rank owns (complete KV groups);
 // on one GPU the ranks' work is the same set of GEMMs in head order.  The
 // causal mask is used at tile granularity: score tiles above the diagonal are
@@ -51,13 +56,18 @@ enum AttnKernel {
   A_RMSNORM_BWD,
   A_COLSUM,
   A_SGD,
+  A_FLASH_FWD,
+  A_FLASH_BWD_PREP,
+  A_FLASH_BWD,
+  A_FLASH_DQ_CAST,
   A_COUNT
 };
 const char* const kAttnNames[A_COUNT] = {
     "rmsnorm_fwd",     "gemm_qkv",        "gemm_scores",     "softmax_fwd",      "gemm_pv",
     "gemm_out_proj",   "gemm_dz",         "gemm_wgrad_out",  "gemm_dp",          "gemm_dv",
     "group_sum",       "softmax_bwd",     "gemm_dq",         "gemm_dk",          "gemm_wgrad_qkv",
-    "gemm_dgrad_norm", "rmsnorm_bwd_residual", "colsum_finalize", "sgd_update"};
+    "gemm_dgrad_norm", "rmsnorm_bwd_residual", "colsum_finalize", "sgd_update",
+    "flash_attn_fwd",  "flash_bwd_prep",  "flash_attn_bwd",  "flash_dq_cast"};
 
 constexpr int MAX_PARTS = 1024;
 thread_local std::string g_attn_err;
@@ -66,7 +76,7 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnLayout {
-  size_t status, nrm, rstd, qkv, z, dz, dqkv, dnrm, scores, probs, dkv_head, part_dw, part_db, total;
+  size_t status, nrm, rstd, qkv, z, dz, dqkv, dnrm, scores, probs, dkv_head, lse2, dsum, part_dw, part_db, total;
 };
 
 bool attn_config_error(const tpattn_config* c, std::string* why) {
@@ -109,7 +119,9 @@ AttnLayout attn_layout(const tpattn_config& c) {
   L.dnrm = take(N * H * 4);
   L.scores = take(SS * 4);   // S, then dP
   L.probs = take(SS * 2);    // P, then dS
-  L.dkv_head = take(N * Z * 4);  // per-query-head dK or dV
+  L.dkv_head = take(N * Z * 4);  // per-query-head dK or dV; the fused path's f32 dQ accumulator
+  L.lse2 = take(N * (size_t)c.n_heads * 4);  // fused path: base-2 log-sum-exp per (sequence, head, query)
+  L.dsum = take(N * (size_t)c.n_heads * 4);  // fused path: rowsum(dZ o Z), same layout
   L.part_dw = take((size_t)MAX_PARTS * H * 4);
   L.part_db = take((size_t)MAX_PARTS * H * 4);
   L.total = off;
@@ -125,6 +137,7 @@ struct tpattn_ctx {
   uint8_t* ws = nullptr;
   AttnLayout L{};
   bool fwd_done = false, bwd_done = false;
+  bool fused = true, fwd_fused = false;
   int64_t batch = 0, seq = 0;
   const void *x = nullptr, *norm_w = nullptr, *w_qkv = nullptr, *w_o = nullptr, *b_o = nullptr;
   float *g_norm_w = nullptr, *g_w_qkv = nullptr, *g_w_o = nullptr, *g_b_o = nullptr;
@@ -196,97 +209,12 @@ BatchDesc head_batch(int B, int n_kv, int hpg) {
   return bd;
 }
 
-}  // namespace
-
-extern "C" {
-
-size_t tpattn_workspace_bytes(const tpattn_config* cfg) {
-  if (attn_config_error(cfg, nullptr)) return 0;
-  return attn_layout(*cfg).total;
-}
-
-tpmlp_status tpattn_create(const tpattn_config* cfg, void* stream, tpattn_ctx** out) {
-  if (!out) return TPMLP_ERR_ARG;
-  *out = nullptr;
-  std::string why;
-  if (attn_config_error(cfg, &why)) {
-    g_attn_err = why;
-    return TPMLP_ERR_SHAPE;
-  }
-  int dev = 0, major = 0, minor = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
-      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) {
-    g_attn_err = "no CUDA device";
-    return TPMLP_ERR_CUDA;
-  }
-  if (major != 10 || minor != 3) {
-    g_attn_err = "needs an sm_103 device";
-    return TPMLP_ERR_UNSUPPORTED;
-  }
-  tpattn_ctx* c = new tpattn_ctx();
-  c->cfg = *cfg;
-  c->stream = static_cast<cudaStream_t>(stream);
-  c->num_sms = sms;
-  c->L = attn_layout(*cfg);
-  *out = c;
-  return TPMLP_OK;
-}
-
-tpmlp_status tpattn_bind_workspace(tpattn_ctx* c, void* dev, size_t bytes) {
-  if (!c) return TPMLP_ERR_ARG;
-  if (!dev || (reinterpret_cast<uintptr_t>(dev) & 255u)) return c->fail(TPMLP_ERR_ARG, "workspace must be 256-byte aligned");
-  if (bytes < c->L.total) return c->fail(TPMLP_ERR_ARG, "workspace too small");
-  c->ws = static_cast<uint8_t*>(dev);
-  const cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
-  return e == cudaSuccess ? TPMLP_OK : c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
-}
-
-tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const void* x, const void* norm_w,
-                            const void* w_qkv, const void* w_o, const void* b_o, float eps, int32_t t, void* y) {
-  if (!c) return TPMLP_ERR_ARG;
-  if (!c->ws) return c->fail(TPMLP_ERR_ORDER, "no workspace bound");
+// Unfused attention core: scores, causal softmax and P V as batched GEMMs
+// and a row kernel, with the scores materialised.
+tpmlp_status attn_core_unfused(tpattn_ctx* c, int B, int S, void* qkv, float* sc, void* pr, void* z) {
   const tpattn_config& cf = c->cfg;
-  if (batch < 1 || seq < 64 || seq % 64 != 0 || seq > cf.max_seq || batch * seq > cf.max_tokens)
-    return c->fail(TPMLP_ERR_SHAPE, "seq must be a multiple of 64 within max_seq, batch * seq within max_tokens");
-  if (t < 1 || t > cf.max_t || cf.n_kv_heads % t != 0) return c->fail(TPMLP_ERR_SHAPE, "t must divide n_kv_heads");
-  if (!x || !norm_w || !w_qkv || !w_o || !b_o || !y) return c->fail(TPMLP_ERR_ARG, "NULL tensor");
-  for (const void* p : {x, norm_w, w_qkv, w_o, b_o, (const void*)y})
-    if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
-  if (!(eps >= 0.0f) || !std::isfinite(eps)) return c->fail(TPMLP_ERR_ARG, "eps must be finite and >= 0");
-  const int B = (int)batch, S = (int)seq, N = B * S, H = (int)cf.hidden, d = cf.head_dim;
+  const int N = B * S, d = cf.head_dim;
   const int nq = cf.n_heads, nkv = cf.n_kv_heads, hpg = nq / nkv, W = (nq + 2 * nkv) * d, Zc = nq * d;
-  c->fwd_done = c->bwd_done = false;
-  c->batch = batch;
-  c->seq = seq;
-  c->x = x;
-  c->norm_w = norm_w;
-  c->w_qkv = w_qkv;
-  c->w_o = w_o;
-  c->b_o = b_o;
-  void* nrm = c->wsp<void>(c->L.nrm);
-  void* qkv = c->wsp<void>(c->L.qkv);
-  void* z = c->wsp<void>(c->L.z);
-  float* sc = c->wsp<float>(c->L.scores);
-  void* pr = c->wsp<void>(c->L.probs);
-  ATTN_TRY(c->run(A_RMSNORM_FWD, [&] {
-    return launch_rmsnorm_fwd(1, x, norm_w, eps, nrm, c->wsp<float>(c->L.rstd), N, H, c->stream);
-  }));
-  // qkv = n W_qkv^T
-  GemmDesc g;
-  g.M = N;
-  g.N = W;
-  g.k_extent = H;
-  g.a = nrm;
-  g.lda = H;
-  g.b = w_qkv;
-  g.ldb = H;
-  g.b_rows = W;
-  g.kseg[1] = H;
-  g.epi = EPI_STORE_BF16;
-  g.ep.out0 = qkv;
-  g.ep.ld_out0 = W;
-  ATTN_TRY(c->gemm(A_GEMM_QKV, g));
   // S[b, h] = Q_h K_g^T  (batched over sequence b, group g, head hq of the group)
   GemmDesc s;
   s.M = S;
@@ -353,87 +281,17 @@ tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const voi
   pv.ep.ld_out0 = Zc;
   pv.ep.out_rows = N;
   pv.ep.out_cols = Zc;
-  ATTN_TRY(c->gemm(A_GEMM_PV, pv));
-  // y = x + Z W_o^T + b_o; the K loop runs over the heads in order: the
-  // ranks' partial outputs summed on chip.
-  GemmDesc o;
-  o.M = N;
-  o.N = H;
-  o.k_extent = Zc;
-  o.a = z;
-  o.lda = Zc;
-  o.b = w_o;
-  o.ldb = Zc;
-  o.b_rows = H;
-  o.kseg[1] = Zc;
-  o.epi = EPI_DOWN_RESID;
-  o.ep.out0 = y;
-  o.ep.ld_out0 = H;
-  o.ep.in0 = x;
-  o.ep.ld_in0 = H;
-  o.ep.vec = b_o;
-  ATTN_TRY(c->gemm(A_GEMM_OUT, o));
-  c->fwd_done = true;
-  return TPMLP_OK;
+  return c->gemm(A_GEMM_PV, pv);
 }
 
-tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dnorm_w, float* dw_qkv, float* dw_o,
-                             float* db_o) {
-  if (!c) return TPMLP_ERR_ARG;
-  if (!c->fwd_done) return c->fail(TPMLP_ERR_ORDER, "backward before forward");
-  if (!dy || !dx || !dnorm_w || !dw_qkv || !dw_o || !db_o) return c->fail(TPMLP_ERR_ARG, "NULL tensor");
-  for (const void* p : {dy, (const void*)dx, (const void*)dnorm_w, (const void*)dw_qkv, (const void*)dw_o,
-                        (const void*)db_o})
-    if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
+// Unfused attention core backward: dP, dV, the softmax backward, dQ and dK
+// as batched GEMMs and row kernels over the materialised P.
+tpmlp_status attn_core_bwd_unfused(tpattn_ctx* c, int B, int S, void* qkv, void* dz, void* dqkv, float* dp, void* pr,
+                                   float* dkv) {
   const tpattn_config& cf = c->cfg;
-  const int B = (int)c->batch, S = (int)c->seq, N = B * S, H = (int)cf.hidden, d = cf.head_dim;
+  const int N = B * S, d = cf.head_dim;
   const int nq = cf.n_heads, nkv = cf.n_kv_heads, hpg = nq / nkv, W = (nq + 2 * nkv) * d, Zc = nq * d;
   const int64_t rows = (int64_t)B * nq * S;
-  c->bwd_done = false;
-  c->g_norm_w = dnorm_w;
-  c->g_w_qkv = dw_qkv;
-  c->g_w_o = dw_o;
-  c->g_b_o = db_o;
-  void* nrm = c->wsp<void>(c->L.nrm);
-  void* qkv = c->wsp<void>(c->L.qkv);
-  void* z = c->wsp<void>(c->L.z);
-  void* dz = c->wsp<void>(c->L.dz);
-  void* dqkv = c->wsp<void>(c->L.dqkv);
-  float* dnrm = c->wsp<float>(c->L.dnrm);
-  float* dp = c->wsp<float>(c->L.scores);
-  void* pr = c->wsp<void>(c->L.probs);
-  float* dkv = c->wsp<float>(c->L.dkv_head);
-  // dZ = dy W_o
-  GemmDesc a;
-  a.M = N;
-  a.N = Zc;
-  a.k_extent = H;
-  a.a = dy;
-  a.lda = H;
-  a.b = c->w_o;
-  a.ldb = Zc;
-  a.b_mn = true;
-  a.kseg[1] = H;
-  a.epi = EPI_STORE_BF16;
-  a.ep.out0 = dz;
-  a.ep.ld_out0 = Zc;
-  ATTN_TRY(c->gemm(A_GEMM_DZ, a));
-  // dW_o = dy^T Z
-  GemmDesc wo;
-  wo.M = H;
-  wo.N = Zc;
-  wo.k_extent = N;
-  wo.a = dy;
-  wo.lda = H;
-  wo.a_mn = true;
-  wo.b = z;
-  wo.ldb = Zc;
-  wo.b_mn = true;
-  wo.kseg[1] = N;
-  wo.epi = EPI_STORE_F32;
-  wo.ep.out0 = dw_o;
-  wo.ep.ld_out0 = Zc;
-  ATTN_TRY(c->gemm(A_GEMM_WGRAD_OUT, wo));
   // dP[b, h] = dZ_h V_g^T  (into the score buffer)
   GemmDesc g;
   g.M = S;
@@ -548,9 +406,205 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   k.batch.b.col[2] = (int64_t)hpg * d;
   k.batch.b.col[3] = d;
   ATTN_TRY(c->gemm(A_GEMM_DK, k));
-  ATTN_TRY(c->run(A_GROUP_SUM, [&] {
+  return c->run(A_GROUP_SUM, [&] {
     return launch_attn_group_sum(dkv, dqkv, B, S, nq, nkv, d, W, (int64_t)nq * d, c->num_sms, c->stream);
+  });
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t tpattn_workspace_bytes(const tpattn_config* cfg) {
+  if (attn_config_error(cfg, nullptr)) return 0;
+  return attn_layout(*cfg).total;
+}
+
+tpmlp_status tpattn_create(const tpattn_config* cfg, void* stream, tpattn_ctx** out) {
+  if (!out) return TPMLP_ERR_ARG;
+  *out = nullptr;
+  std::string why;
+  if (attn_config_error(cfg, &why)) {
+    g_attn_err = why;
+    return TPMLP_ERR_SHAPE;
+  }
+  int dev = 0, major = 0, minor = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) ||
+      cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) {
+    g_attn_err = "no CUDA device";
+    return TPMLP_ERR_CUDA;
+  }
+  if (major != 10 || minor != 3) {
+    g_attn_err = "needs an sm_103 device";
+    return TPMLP_ERR_UNSUPPORTED;
+  }
+  tpattn_ctx* c = new tpattn_ctx();
+  c->cfg = *cfg;
+  c->stream = static_cast<cudaStream_t>(stream);
+  c->num_sms = sms;
+  c->L = attn_layout(*cfg);
+  *out = c;
+  return TPMLP_OK;
+}
+
+tpmlp_status tpattn_bind_workspace(tpattn_ctx* c, void* dev, size_t bytes) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!dev || (reinterpret_cast<uintptr_t>(dev) & 255u)) return c->fail(TPMLP_ERR_ARG, "workspace must be 256-byte aligned");
+  if (bytes < c->L.total) return c->fail(TPMLP_ERR_ARG, "workspace too small");
+  c->ws = static_cast<uint8_t*>(dev);
+  const cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
+  return e == cudaSuccess ? TPMLP_OK : c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
+}
+
+tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const void* x, const void* norm_w,
+                            const void* w_qkv, const void* w_o, const void* b_o, float eps, int32_t t, void* y) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!c->ws) return c->fail(TPMLP_ERR_ORDER, "no workspace bound");
+  const tpattn_config& cf = c->cfg;
+  if (batch < 1 || seq < 64 || seq % 64 != 0 || seq > cf.max_seq || batch * seq > cf.max_tokens)
+    return c->fail(TPMLP_ERR_SHAPE, "seq must be a multiple of 64 within max_seq, batch * seq within max_tokens");
+  if (t < 1 || t > cf.max_t || cf.n_kv_heads % t != 0) return c->fail(TPMLP_ERR_SHAPE, "t must divide n_kv_heads");
+  if (!x || !norm_w || !w_qkv || !w_o || !b_o || !y) return c->fail(TPMLP_ERR_ARG, "NULL tensor");
+  for (const void* p : {x, norm_w, w_qkv, w_o, b_o, (const void*)y})
+    if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
+  if (!(eps >= 0.0f) || !std::isfinite(eps)) return c->fail(TPMLP_ERR_ARG, "eps must be finite and >= 0");
+  const int B = (int)batch, S = (int)seq, N = B * S, H = (int)cf.hidden, d = cf.head_dim;
+  const int nq = cf.n_heads, nkv = cf.n_kv_heads, W = (nq + 2 * nkv) * d, Zc = nq * d;
+  c->fwd_done = c->bwd_done = false;
+  c->batch = batch;
+  c->seq = seq;
+  c->x = x;
+  c->norm_w = norm_w;
+  c->w_qkv = w_qkv;
+  c->w_o = w_o;
+  c->b_o = b_o;
+  void* nrm = c->wsp<void>(c->L.nrm);
+  void* qkv = c->wsp<void>(c->L.qkv);
+  void* z = c->wsp<void>(c->L.z);
+  float* sc = c->wsp<float>(c->L.scores);
+  void* pr = c->wsp<void>(c->L.probs);
+  c->fwd_fused = c->fused && d == 128 && S % 128 == 0;
+  ATTN_TRY(c->run(A_RMSNORM_FWD, [&] {
+    return launch_rmsnorm_fwd(1, x, norm_w, eps, nrm, c->wsp<float>(c->L.rstd), N, H, c->stream);
   }));
+  // qkv = n W_qkv^T
+  GemmDesc g;
+  g.M = N;
+  g.N = W;
+  g.k_extent = H;
+  g.a = nrm;
+  g.lda = H;
+  g.b = w_qkv;
+  g.ldb = H;
+  g.b_rows = W;
+  g.kseg[1] = H;
+  g.epi = EPI_STORE_BF16;
+  g.ep.out0 = qkv;
+  g.ep.ld_out0 = W;
+  ATTN_TRY(c->gemm(A_GEMM_QKV, g));
+  if (c->fwd_fused) {
+    ATTN_TRY(c->run(A_FLASH_FWD, [&] {
+      return launch_flash_attn_fwd(qkv, B, S, nq, nkv, d, z, c->wsp<float>(c->L.lse2), c->wsp<uint32_t>(c->L.status),
+                                   c->stream);
+    }));
+  } else {
+    ATTN_TRY(attn_core_unfused(c, B, S, qkv, sc, pr, z));
+  }
+  // y = x + Z W_o^T + b_o; the K loop runs over the heads in order: the
+  // ranks' partial outputs summed on chip.
+  GemmDesc o;
+  o.M = N;
+  o.N = H;
+  o.k_extent = Zc;
+  o.a = z;
+  o.lda = Zc;
+  o.b = w_o;
+  o.ldb = Zc;
+  o.b_rows = H;
+  o.kseg[1] = Zc;
+  o.epi = EPI_DOWN_RESID;
+  o.ep.out0 = y;
+  o.ep.ld_out0 = H;
+  o.ep.in0 = x;
+  o.ep.ld_in0 = H;
+  o.ep.vec = b_o;
+  ATTN_TRY(c->gemm(A_GEMM_OUT, o));
+  c->fwd_done = true;
+  return TPMLP_OK;
+}
+
+
+tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dnorm_w, float* dw_qkv, float* dw_o,
+                             float* db_o) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!c->fwd_done) return c->fail(TPMLP_ERR_ORDER, "backward before forward");
+  if (!dy || !dx || !dnorm_w || !dw_qkv || !dw_o || !db_o) return c->fail(TPMLP_ERR_ARG, "NULL tensor");
+  for (const void* p : {dy, (const void*)dx, (const void*)dnorm_w, (const void*)dw_qkv, (const void*)dw_o,
+                        (const void*)db_o})
+    if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
+  const tpattn_config& cf = c->cfg;
+  const int B = (int)c->batch, S = (int)c->seq, N = B * S, H = (int)cf.hidden, d = cf.head_dim;
+  const int nq = cf.n_heads, nkv = cf.n_kv_heads, W = (nq + 2 * nkv) * d, Zc = nq * d;
+  c->bwd_done = false;
+  c->g_norm_w = dnorm_w;
+  c->g_w_qkv = dw_qkv;
+  c->g_w_o = dw_o;
+  c->g_b_o = db_o;
+  void* nrm = c->wsp<void>(c->L.nrm);
+  void* qkv = c->wsp<void>(c->L.qkv);
+  void* z = c->wsp<void>(c->L.z);
+  void* dz = c->wsp<void>(c->L.dz);
+  void* dqkv = c->wsp<void>(c->L.dqkv);
+  float* dnrm = c->wsp<float>(c->L.dnrm);
+  float* dp = c->wsp<float>(c->L.scores);
+  void* pr = c->wsp<void>(c->L.probs);
+  float* dkv = c->wsp<float>(c->L.dkv_head);
+  // dZ = dy W_o
+  GemmDesc a;
+  a.M = N;
+  a.N = Zc;
+  a.k_extent = H;
+  a.a = dy;
+  a.lda = H;
+  a.b = c->w_o;
+  a.ldb = Zc;
+  a.b_mn = true;
+  a.kseg[1] = H;
+  a.epi = EPI_STORE_BF16;
+  a.ep.out0 = dz;
+  a.ep.ld_out0 = Zc;
+  ATTN_TRY(c->gemm(A_GEMM_DZ, a));
+  // dW_o = dy^T Z
+  GemmDesc wo;
+  wo.M = H;
+  wo.N = Zc;
+  wo.k_extent = N;
+  wo.a = dy;
+  wo.lda = H;
+  wo.a_mn = true;
+  wo.b = z;
+  wo.ldb = Zc;
+  wo.b_mn = true;
+  wo.kseg[1] = N;
+  wo.epi = EPI_STORE_F32;
+  wo.ep.out0 = dw_o;
+  wo.ep.ld_out0 = Zc;
+  ATTN_TRY(c->gemm(A_GEMM_WGRAD_OUT, wo));
+  if (c->fwd_fused) {
+    float* dq_acc = c->wsp<float>(c->L.dkv_head);
+    float* dsum = c->wsp<float>(c->L.dsum);
+    ATTN_TRY(c->run(A_FLASH_BWD_PREP,
+                    [&] { return launch_flash_bwd_prep(dz, z, dsum, dq_acc, B, S, nq, d, c->num_sms, c->stream); }));
+    ATTN_TRY(c->run(A_FLASH_BWD, [&] {
+      return launch_flash_attn_bwd(qkv, dz, c->wsp<float>(c->L.lse2), dsum, dq_acc, dqkv, B, S, nq, nkv, d,
+                                   c->wsp<uint32_t>(c->L.status), c->stream);
+    }));
+    ATTN_TRY(c->run(A_FLASH_DQ_CAST,
+                    [&] { return launch_flash_dq_cast(dq_acc, dqkv, N, Zc, W, c->num_sms, c->stream); }));
+  } else {
+    ATTN_TRY(attn_core_bwd_unfused(c, B, S, qkv, dz, dqkv, dp, pr, dkv));
+  }
   // dW_qkv = dqkv^T n
   GemmDesc wq;
   wq.M = W;
@@ -606,6 +660,14 @@ tpmlp_status tpattn_bind_master(tpattn_ctx* c, float* norm_w, float* w_qkv, floa
   c->m_b_o = b_o;
   return TPMLP_OK;
 }
+
+tpmlp_status tpattn_set_fused(tpattn_ctx* c, int32_t enable) {
+  if (!c) return TPMLP_ERR_ARG;
+  c->fused = enable != 0;
+  return TPMLP_OK;
+}
+
+int32_t tpattn_fused_active(const tpattn_ctx* c) { return c && c->fwd_done && c->fwd_fused ? 1 : 0; }
 
 tpmlp_status tpattn_sgd_step(tpattn_ctx* c, float lr) {
   if (!c) return TPMLP_ERR_ARG;

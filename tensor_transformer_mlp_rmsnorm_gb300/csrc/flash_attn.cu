@@ -1,0 +1,886 @@
+// Fused causal attention forward on the sm_103a tensor cores, for the
+// tensor-parallel attention sublayer ("Megatron-LM Explained",
+// "Self-attention: split across heads").  One CTA computes the output rows of
+// a 128-query block of one (sequence, query head), streaming the key/value
+// blocks of its KV group up to the diagonal, without materialising scores:
+//
+//   warp 0     : TMA producer -- Q once; K_j and V_j into a two-stage ring.
+//   warp 1     : owns tensor memory (two 128-column score buffers, two
+//                128-column P V buffers) and issues tcgen05.mma: S_j = Q K_j^T,
+//                then P_{j-1} V_{j-1} once the softmax warps have written P.
+//   warps 2..5 : online softmax, one query row per thread: the row maximum
+//                and sum over two passes of S_j from tensor memory, P_j
+//                (bf16) into shared memory in the MMA's K-major layout, and
+//                the running output O = alpha O + P V in registers; finally
+//                O / l as bf16 (TMA store) and the row's log-sum-exp
+//                (base 2, of the log2(e)-scaled scores) for the backward.
+//
+// Scores are scaled by 1/sqrt(d); exponentials run in base 2 with log2(e)
+// folded into the scale.  The diagonal block masks keys above the query.
+// Every wait is bounded (1 s); a wait that gives up sets the status word,
+// and the CTA drains and exits.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "ptx_sm103.cuh"
+#include "tma_maps.cuh"
+#include "tpmlp_internal.h"
+#include "vec.cuh"
+
+namespace tpmlp {
+namespace {
+
+constexpr int FB = 128;        // queries per CTA = keys per block
+constexpr int FD = 128;        // head dimension
+constexpr int FTHREADS = 192;
+constexpr uint32_t FCOLS = 512;
+constexpr uint64_t FWAIT_NS = 1000000000ull;
+constexpr uint64_t FDRAIN_NS = 200000000ull;
+constexpr uint32_t TILE_BYTES = FB * 64 * 2;     // one [128 x 64] bf16 SW128 tile, 16 KB
+constexpr uint32_t OPND_BYTES = 2 * TILE_BYTES;  // a [128 x 128] operand: two tiles
+// shared memory: Q, K[2], V[2], P, output staging
+constexpr uint32_t SQ = 0;
+constexpr uint32_t SK = SQ + OPND_BYTES;
+constexpr uint32_t SV = SK + 2 * OPND_BYTES;
+constexpr uint32_t SP = SV + 2 * OPND_BYTES;
+constexpr uint32_t SO = SP + OPND_BYTES;
+constexpr uint32_t FSMEM = SO + 4 * 4096 + 1024;
+
+struct FaParams {
+  int S, nq, nkv, hpg, nqblk;
+  int k_col0, v_col0;  // first key / value column of the QKV tensor
+  float scale_log2;    // log2(e) / sqrt(d)
+  float* lse2;         // [batch * nq * S] base-2 log-sum-exp of the scaled scores
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void stage_row_bf16_fa(uint8_t* tile, int r, const float* v) {
+  uint8_t* rowp = tile + r * 64;
+#pragma unroll
+  for (int c = 0; c < 4; ++c) {
+    uint4 w;
+    __nv_bfloat162 h;
+    h = __floats2bfloat162_rn(v[8 * c], v[8 * c + 1]);
+    w.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * c + 2], v[8 * c + 3]);
+    w.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * c + 4], v[8 * c + 5]);
+    w.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * c + 6], v[8 * c + 7]);
+    w.w = *reinterpret_cast<uint32_t*>(&h);
+    *reinterpret_cast<uint4*>(rowp + ((c ^ ((r >> 1) & 3)) << 4)) = w;
+  }
+}
+
+__global__ void __launch_bounds__(FTHREADS, 1)
+    flash_fwd_kernel(const __grid_constant__ CUtensorMap map_qk, const __grid_constant__ CUtensorMap map_v,
+                     const __grid_constant__ CUtensorMap map_z, const FaParams p) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, p_empty,
+      pv_full[2], pv_empty[2], drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  volatile int* abort_flag = &abort_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // block -> (query block, head, sequence); the longest (diagonal-most) query blocks first
+  const int qb = p.nqblk - 1 - (int)(blockIdx.x % p.nqblk);
+  const int bh = (int)(blockIdx.x / p.nqblk);
+  const int h = bh % p.nq, b = bh / p.nq;
+  const int g = h / p.hpg;
+  const int nk = qb + 1;  // key blocks up to the diagonal
+  const int row_q = b * p.S + qb * FB;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&q_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&kv_full[i], 1);
+      mbar_init(&kv_empty[i], 1);
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+      mbar_init(&pv_full[i], 1);
+      mbar_init(&pv_empty[i], 4);
+    }
+    mbar_init(&p_full, 4);
+    mbar_init(&p_empty, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_qk);
+    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_z);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, FCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(&q_full, OPND_BYTES);
+      for (int t = 0; t < 2; ++t) tma_load_2d(smem + SQ + t * TILE_BYTES, &map_qk, &q_full, h * FD + 64 * t, row_q);
+      for (int j = 0; ok && j < nk; ++j) {
+        const int s = j & 1;
+        if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(&kv_full[s], 2 * OPND_BYTES);
+        armed |= 1u << s;
+        armed_par = (armed_par & ~(1u << s)) | ((uint32_t)((j >> 1) & 1) << s);
+        const int row_k = b * p.S + j * FB;
+        for (int t = 0; t < 2; ++t) {
+          tma_load_2d(smem + SK + s * OPND_BYTES + t * TILE_BYTES, &map_qk, &kv_full[s], p.k_col0 + g * FD + 64 * t,
+                      row_k);
+          tma_load_3d(smem + SV + s * OPND_BYTES + t * TILE_BYTES, &map_v, &kv_full[s], 0, row_k + 64 * t,
+                      (p.v_col0 + g * FD) >> 6);
+        }
+      }
+      if (!ok || *abort_flag) {
+        int no_abort = 0;
+        mbar_wait(&q_full, 0, &no_abort, p.status, 0u, FDRAIN_NS);
+        // copies still in flight land on the full barriers of the phases armed last
+        for (int s = 0; s < 2; ++s)
+          if (armed & (1u << s)) mbar_wait(&kv_full[s], (armed_par >> s) & 1u, &no_abort, p.status, 0u, FDRAIN_NS / 4);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    constexpr uint32_t IDESC_S = idesc_bf16_f32(FB, FB, false, false);
+    constexpr uint32_t IDESC_PV = idesc_bf16_f32(FB, FD, false, true);
+    int ok = __all_sync(0xffffffffu, mbar_wait(&q_full, 0, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
+    auto issue_pv = [&](int jj) -> int {
+      const int s = jj & 1;
+      int w = mbar_wait(&p_full, jj & 1, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
+      w = w && mbar_wait(&pv_empty[s], ((jj >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
+      if (!__all_sync(0xffffffffu, w)) return 0;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t d_tmem = tmem_base + 256 + s * FB;
+        const uint32_t pa = smem_u32(smem + SP), vb = smem_u32(smem + SV + s * OPND_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a_desc = sw128_desc(pa + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024);
+          const uint64_t b_desc = sw128_desc(vb + (kk >> 2) * TILE_BYTES + (kk & 3) * 2048, 8192, 1024);
+          tc_mma_f16(d_tmem, a_desc, b_desc, IDESC_PV, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&pv_full[s]);
+        tc_commit(&p_empty);
+        tc_commit(&kv_empty[s]);
+      }
+      __syncwarp();
+      return 1;
+    };
+    for (int j = 0; ok && j < nk; ++j) {
+      const int s = j & 1;
+      int w = mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
+      w = w && mbar_wait(&s_empty[s], ((j >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
+      ok = __all_sync(0xffffffffu, w);
+      if (!ok) break;
+      tc_fence_after();
+      if (elect_one()) {
+        const uint32_t d_tmem = tmem_base + s * FB;
+        const uint32_t qa = smem_u32(smem + SQ), kb = smem_u32(smem + SK + s * OPND_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a_desc = sw128_desc(qa + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024);
+          const uint64_t b_desc = sw128_desc(kb + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024);
+          tc_mma_f16(d_tmem, a_desc, b_desc, IDESC_S, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(&s_full[s]);
+      }
+      __syncwarp();
+      if (j >= 1) ok = issue_pv(j - 1);
+    }
+    if (ok) issue_pv(nk - 1);
+    if (elect_one()) tc_commit(&drain_bar);
+    __syncwarp();
+    int no_abort = 0;
+    mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
+  } else {
+    // --------------------------------------------------------- softmax warps
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // query row within the block
+    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint8_t* stg = smem + SO + (warp - 2) * 4096;
+    float o[FD];
+#pragma unroll
+    for (int c = 0; c < FD; ++c) o[c] = 0.0f;
+    float m2 = -INFINITY, l = 0.0f;  // running max (log2 units) and sum
+    int ok = 1;
+    for (int j = 0; j < nk; ++j) {
+      const int s = j & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag, p.status, STATUS_TIMEOUT,
+                                             FWAIT_NS));
+      if (!ok) break;
+      tc_fence_after();
+      const bool diag = j == qb;
+      // pass 1: the row maximum of this block
+      float bm = -INFINITY;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(trow + s * FB + c * 32, v);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const bool masked = diag && (c * 32 + e > r);
+          bm = masked ? bm : fmaxf(bm, __uint_as_float(v[e]));
+        }
+      }
+      const float m2n = fmaxf(m2, bm * p.scale_log2);
+      const float alpha = exp2f(m2 - m2n);  // 0 on the first block
+      // P must not overwrite the tile the previous P V is still reading
+      ok = __all_sync(0xffffffffu, mbar_wait(&p_empty, (j & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
+      if (!ok) break;
+      // pass 2: P = exp2(s * scale_log2 - m2n) into shared memory, and its sum
+      float ps = 0.0f;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(trow + s * FB + c * 32, v);
+        tmem_ld_wait();
+        float pv[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const bool masked = diag && (c * 32 + e > r);
+          pv[e] = masked ? 0.0f : exp2f(__uint_as_float(v[e]) * p.scale_log2 - m2n);
+          ps += pv[e];
+        }
+        // keys [32c, 32c+32) sit in tile c / 2, 16-byte chunks 4 (c % 2) .. +3
+        uint8_t* tile = smem + SP + (c >> 1) * TILE_BYTES + r * 128;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int chunk = (c & 1) * 4 + k;
+          uint4 w;
+          __nv_bfloat162 hh;
+          hh = __floats2bfloat162_rn(pv[8 * k], pv[8 * k + 1]);
+          w.x = *reinterpret_cast<uint32_t*>(&hh);
+          hh = __floats2bfloat162_rn(pv[8 * k + 2], pv[8 * k + 3]);
+          w.y = *reinterpret_cast<uint32_t*>(&hh);
+          hh = __floats2bfloat162_rn(pv[8 * k + 4], pv[8 * k + 5]);
+          w.z = *reinterpret_cast<uint32_t*>(&hh);
+          hh = __floats2bfloat162_rn(pv[8 * k + 6], pv[8 * k + 7]);
+          w.w = *reinterpret_cast<uint32_t*>(&hh);
+          *reinterpret_cast<uint4*>(tile + ((chunk ^ (r & 7)) << 4)) = w;
+        }
+      }
+      tc_fence_before();
+      fence_proxy_async_smem();  // P is read by the tensor cores (async proxy)
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(&s_empty[s]);
+        mbar_arrive(&p_full);
+      }
+      // O = alpha (O + P_{j-1} V_{j-1}); the sum follows the same frame
+      if (j >= 1) {
+        const int sp = (j - 1) & 1;
+        ok = __all_sync(0xffffffffu, mbar_wait(&pv_full[sp], ((j - 1) >> 1) & 1, abort_flag, p.status,
+                                               STATUS_TIMEOUT, FWAIT_NS));
+        if (!ok) break;
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(trow + 256 + sp * FB + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c * 32 + e] += __uint_as_float(v[e]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(&pv_empty[sp]);
+      }
+#pragma unroll
+      for (int c = 0; c < FD; ++c) o[c] *= alpha;
+      l = l * alpha + ps;
+      m2 = m2n;
+    }
+    if (ok) {
+      const int sp = (nk - 1) & 1;
+      ok = __all_sync(0xffffffffu, mbar_wait(&pv_full[sp], ((nk - 1) >> 1) & 1, abort_flag, p.status,
+                                             STATUS_TIMEOUT, FWAIT_NS));
+      if (ok) {
+        tc_fence_after();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(trow + 256 + sp * FB + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[c * 32 + e] += __uint_as_float(v[e]);
+        }
+        const float inv = 1.0f / l;
+#pragma unroll
+        for (int c = 0; c < FD; ++c) o[c] *= inv;
+        p.lse2[(size_t)bh * p.S + qb * FB + r] = m2 + log2f(l);
+        // output rows [row_q + 32 q, +32), 32 columns at a time through two staging tiles
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+          uint8_t* sb = stg + (c & 1) * 2048;
+          if (lane == 0) bulk_wait_read_but_last();
+          __syncwarp();
+          stage_row_bf16_fa(sb, lane, o + c * 32);
+          fence_proxy_async_smem();
+          __syncwarp();
+          if (lane == 0) {
+            tma_store_2d(&map_z, sb, h * FD + c * 32, row_q + q * 32);
+            bulk_commit_group();
+          }
+        }
+        if (lane == 0) bulk_wait_all();
+        __syncwarp();
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, FCOLS);
+  }
+}
+
+
+// ---------------------------------------------------------------- backward
+// One CTA per (sequence b, KV group g, 128-key block j) accumulates dK_j and
+// dV_j of the group in tensor memory over every query head of the group and
+// every 64-query block i that sees the keys (i >= 2 j), and adds each
+// dQ_i contribution into an f32 accumulator with a TMA reduce-add.  With P
+// recomputed from the forward's log-sum-exp and D_i = rowsum(dO_i o O_i):
+//
+//   S^T  = K_j Q_i^T               dP^T = V_j dO_i^T
+//   P^T  = exp2(S^T log2(e)/sqrt(d) - lse2_i)    (keys above a query masked)
+//   dS^T = P^T o (dP^T - D_i) / sqrt(d)
+//   dV_j += P^T dO_i               dK_j += dS^T Q_i      dQ_i^T += K_j^T dS^T
+//
+//   warp 0     : TMA producer -- K_j, V_j once; Q_i, dO_i, lse2_i, D_i per
+//                step into a two-stage ring.
+//   warp 1     : tensor memory owner and MMA issuer.
+//   warps 2..5 : one key row per thread for P^T and dS^T (bf16, into shared
+//                memory in the K-major layout the MMAs read), one head-dim row
+//                per thread for the dQ^T epilogue, and the final dK / dV rows.
+// The same shared-memory tile of Q, dO, K or dS^T serves as a K-major operand
+// of one product and an MN-major operand of another: a 128-byte swizzled tile
+// of 64-element rows is both.
+constexpr int BKB = 128;  // keys per CTA
+constexpr int BQB = 64;   // queries per step
+constexpr int BTHREADS = 192;
+constexpr uint32_t KT_BYTES = BKB * 64 * 2;   // [128 keys x 64 d] tile, 16 KB
+constexpr uint32_t QT_BYTES = BQB * 64 * 2;   // [64 queries x 64 d] tile, 8 KB
+// shared memory
+constexpr uint32_t B_SK = 0;                          // K_j: two 16 KB tiles
+constexpr uint32_t B_SV = B_SK + 2 * KT_BYTES;        // V_j
+constexpr uint32_t B_SQ = B_SV + 2 * KT_BYTES;        // Q_i ring: 2 stages x two 8 KB tiles
+constexpr uint32_t B_SDO = B_SQ + 4 * QT_BYTES;       // dO_i ring
+constexpr uint32_t B_SP = B_SDO + 4 * QT_BYTES;       // P^T [128 keys x 64 queries], 16 KB
+constexpr uint32_t B_SDS = B_SP + KT_BYTES;           // dS^T
+constexpr uint32_t B_SDQ = B_SDS + KT_BYTES;          // dQ^T staging: 4 warps x [64 q x 32 d] f32
+constexpr uint32_t B_SLD = B_SDQ + 4 * BQB * 32 * 4;  // lse2 / D ring: 2 stages x 2 x 64 floats
+constexpr uint32_t BSMEM = B_SLD + 2 * 2 * BQB * 4 + 1024;
+constexpr uint32_t IN_TX = 4 * QT_BYTES + 2 * BQB * 4;
+// tensor memory columns
+constexpr uint32_t T_S = 0;     // S^T ring: 2 x 64
+constexpr uint32_t T_DP = 128;  // dP^T: 64
+constexpr uint32_t T_DQ = 192;  // dQ^T: 64
+constexpr uint32_t T_DV = 256;  // dV_j: 128
+constexpr uint32_t T_DK = 384;  // dK_j: 128
+
+struct FbParams {
+  int S, nq, nkv, hpg;
+  int q64;  // S / 64
+  int k_col0, v_col0;
+  float scale_log2, scale;
+  const float* lse2;  // [batch * nq * S]
+  const float* dsum;  // D, same layout
+  __nv_bfloat16* dqkv;
+  int64_t ld_dqkv;
+  uint32_t* status;
+};
+
+__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v) {
+#pragma unroll
+  for (int c = 0; c < 8; ++c) {
+    uint4 w;
+    __nv_bfloat162 h;
+    h = __floats2bfloat162_rn(v[8 * c], v[8 * c + 1]);
+    w.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * c + 2], v[8 * c + 3]);
+    w.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * c + 4], v[8 * c + 5]);
+    w.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * c + 6], v[8 * c + 7]);
+    w.w = *reinterpret_cast<uint32_t*>(&h);
+    reinterpret_cast<uint4*>(dst)[c] = w;
+  }
+}
+
+// A 128-byte swizzled K-major row of 64 bf16 values (row r of a 1024-byte
+// aligned tile).
+__device__ __forceinline__ void write_sw128_row(uint8_t* tile, int r, const float* v) {
+  uint8_t* rowp = tile + r * 128;
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    uint4 w;
+    __nv_bfloat162 h;
+    h = __floats2bfloat162_rn(v[8 * k], v[8 * k + 1]);
+    w.x = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * k + 2], v[8 * k + 3]);
+    w.y = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * k + 4], v[8 * k + 5]);
+    w.z = *reinterpret_cast<uint32_t*>(&h);
+    h = __floats2bfloat162_rn(v[8 * k + 6], v[8 * k + 7]);
+    w.w = *reinterpret_cast<uint32_t*>(&h);
+    *reinterpret_cast<uint4*>(rowp + ((k ^ (r & 7)) << 4)) = w;
+  }
+}
+
+__global__ void __launch_bounds__(BTHREADS, 1)
+    flash_bwd_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_q,
+                     const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dq,
+                     const FbParams p, int batch) {
+  extern __shared__ uint8_t smem_raw[];
+  __shared__ __align__(8) uint64_t kv_full, in_full[2], in_empty[2], s_full[2], s_empty[2], dp_full, dp_empty,
+      p_full, ds_full, pds_empty, dq_full, dq_empty, acc_full, drain_bar;
+  __shared__ uint32_t tmem_base_sh;
+  __shared__ int abort_sh;
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  volatile int* abort_flag = &abort_sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  // block -> (key block j, sequence b, group g); the key blocks with the most query blocks first
+  const int nbg = batch * p.nkv;
+  const int j = (int)(blockIdx.x / nbg);
+  const int bg = (int)(blockIdx.x % nbg);
+  const int b = bg / p.nkv, g = bg % p.nkv;
+  const int i0 = 2 * j;                 // first 64-query block that sees key block j
+  const int per_head = p.q64 - i0;
+  const int nsteps = p.hpg * per_head;  // >= hpg * 2
+  const int row_k = b * p.S + j * BKB;
+
+  if (threadIdx.x == 0) {
+    mbar_init(&kv_full, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(&in_full[i], 1);
+      mbar_init(&in_empty[i], 1 + 4);  // the MMA commit and the four row warps (lse2 / D reads)
+      mbar_init(&s_full[i], 1);
+      mbar_init(&s_empty[i], 4);
+    }
+    mbar_init(&dp_full, 1);
+    mbar_init(&dp_empty, 4);
+    mbar_init(&p_full, 4);
+    mbar_init(&ds_full, 4);
+    mbar_init(&pds_empty, 1);
+    mbar_init(&dq_full, 1);
+    mbar_init(&dq_empty, 4);
+    mbar_init(&acc_full, 1);
+    mbar_init(&drain_bar, 1);
+    abort_sh = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0 && lane == 0) {
+    tma_prefetch_desc(&map_kv);
+    tma_prefetch_desc(&map_q);
+    tma_prefetch_desc(&map_do);
+    tma_prefetch_desc(&map_dq);
+  }
+  if (warp == 1) {
+    tmem_alloc(&tmem_base_sh, FCOLS);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem_base = tmem_base_sh;
+
+  if (warp == 0) {
+    if (lane == 0) {
+      // ------------------------------------------------------------ producer
+      uint32_t armed = 0, armed_par = 0;
+      bool ok = true;
+      mbar_arrive_expect_tx(&kv_full, 4 * KT_BYTES);
+      for (int t = 0; t < 2; ++t) {
+        tma_load_2d(smem + B_SK + t * KT_BYTES, &map_kv, &kv_full, p.k_col0 + g * FD + 64 * t, row_k);
+        tma_load_2d(smem + B_SV + t * KT_BYTES, &map_kv, &kv_full, p.v_col0 + g * FD + 64 * t, row_k);
+      }
+      for (int n = 0; ok && n < nsteps; ++n) {
+        const int s = n & 1;
+        if (!mbar_wait(&in_empty[s], ((n >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS)) {
+          ok = false;
+          break;
+        }
+        const int h = g * p.hpg + n / per_head, i = i0 + n % per_head;
+        const int row_q = b * p.S + i * BQB;
+        mbar_arrive_expect_tx(&in_full[s], IN_TX);
+        armed |= 1u << s;
+        armed_par = (armed_par & ~(1u << s)) | ((uint32_t)((n >> 1) & 1) << s);
+        for (int t = 0; t < 2; ++t) {
+          tma_load_2d(smem + B_SQ + (2 * s + t) * QT_BYTES, &map_q, &in_full[s], h * FD + 64 * t, row_q);
+          tma_load_2d(smem + B_SDO + (2 * s + t) * QT_BYTES, &map_do, &in_full[s], h * FD + 64 * t, row_q);
+        }
+        const size_t li = ((size_t)(b * p.nq + h)) * p.S + (size_t)i * BQB;
+        bulk_load_1d(smem + B_SLD + s * 512, p.lse2 + li, BQB * 4, &in_full[s]);
+        bulk_load_1d(smem + B_SLD + s * 512 + 256, p.dsum + li, BQB * 4, &in_full[s]);
+      }
+      if (!ok || *abort_flag) {
+        int no_abort = 0;
+        mbar_wait(&kv_full, 0, &no_abort, p.status, 0u, FDRAIN_NS);
+        for (int s = 0; s < 2; ++s)
+          if (armed & (1u << s)) mbar_wait(&in_full[s], (armed_par >> s) & 1u, &no_abort, p.status, 0u, FDRAIN_NS / 4);
+      }
+    }
+  } else if (warp == 1) {
+    // -------------------------------------------------------------- MMA issuer
+    constexpr uint32_t IDESC_SP = idesc_bf16_f32(BKB, BQB, false, false);   // S^T, dP^T
+    constexpr uint32_t IDESC_KV = idesc_bf16_f32(BKB, FD, false, true);     // dV, dK
+    constexpr uint32_t IDESC_DQ = idesc_bf16_f32(FD, BQB, true, true);      // dQ^T
+    const uint32_t sk = smem_u32(smem + B_SK), sv = smem_u32(smem + B_SV);
+    const uint32_t sp = smem_u32(smem + B_SP), sds = smem_u32(smem + B_SDS);
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
+    };
+    // S^T_n = K Q_n^T (ring slot n & 1) or dP^T_n = V dO_n^T, then a commit to `done`
+    auto issue_nt = [&](uint32_t d_tmem, uint32_t a, uint32_t bq, uint64_t* done) {
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+          const uint64_t a_desc = sw128_desc(a + (kk >> 2) * KT_BYTES + (kk & 3) * 32, 16, 1024);
+          const uint64_t b_desc = sw128_desc(bq + (kk >> 2) * QT_BYTES + (kk & 3) * 32, 16, 1024);
+          tc_mma_f16(d_tmem, a_desc, b_desc, IDESC_SP, kk > 0 ? 1u : 0u);
+        }
+        tc_commit(done);
+      }
+      __syncwarp();
+    };
+    int ok = wait_all(&kv_full, 0);
+    auto issue_s = [&](int n) -> int {
+      const int s = n & 1;
+      if (!wait_all(&in_full[s], (n >> 1) & 1)) return 0;
+      if (!wait_all(&s_empty[s], ((n >> 1) & 1) ^ 1u)) return 0;
+      tc_fence_after();
+      issue_nt(tmem_base + T_S + s * BQB, sk, smem_u32(smem + B_SQ + 2 * s * QT_BYTES), &s_full[s]);
+      return 1;
+    };
+    auto issue_dp = [&](int n) -> int {
+      if (!wait_all(&dp_empty, (n & 1) ^ 1u)) return 0;
+      tc_fence_after();
+      issue_nt(tmem_base + T_DP, sv, smem_u32(smem + B_SDO + 2 * (n & 1) * QT_BYTES), &dp_full);
+      return 1;
+    };
+    if (ok) ok = issue_s(0);
+    if (ok) ok = issue_dp(0);
+    for (int n = 0; ok && n < nsteps; ++n) {
+      const int s = n & 1;
+      if (n + 1 < nsteps && !(ok = issue_s(n + 1))) break;
+      const uint32_t sq = smem_u32(smem + B_SQ + 2 * s * QT_BYTES), sdo = smem_u32(smem + B_SDO + 2 * s * QT_BYTES);
+      // dV += P^T dO_n
+      if (!(ok = wait_all(&p_full, n & 1))) break;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16(tmem_base + T_DV, sw128_desc(sp + kk * 32, 16, 1024), sw128_desc(sdo + kk * 2048, QT_BYTES, 1024),
+                     IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+      }
+      __syncwarp();
+      // dK += dS^T Q_n ; dQ^T_n = K^T dS^T
+      if (!(ok = wait_all(&ds_full, n & 1))) break;
+      if (!(ok = wait_all(&dq_empty, (n & 1) ^ 1u))) break;
+      tc_fence_after();
+      if (elect_one()) {
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16(tmem_base + T_DK, sw128_desc(sds + kk * 32, 16, 1024), sw128_desc(sq + kk * 2048, QT_BYTES, 1024),
+                     IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem_base + T_DQ, sw128_desc(sk + kk * 2048, KT_BYTES, 1024),
+                     sw128_desc(sds + kk * 2048, KT_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
+        tc_commit(&dq_full);
+        tc_commit(&pds_empty);
+        tc_commit(&in_empty[s]);
+        if (n + 1 == nsteps) tc_commit(&acc_full);
+      }
+      __syncwarp();
+      if (n + 1 < nsteps && !(ok = issue_dp(n + 1))) break;
+    }
+    if (elect_one()) tc_commit(&drain_bar);
+    __syncwarp();
+    int no_abort = 0;
+    mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
+  } else {
+    // ------------------------------------------------------------ row warps
+    const int q = warp & 3;
+    const int r = q * 32 + lane;  // key row (P^T, dS^T, dK, dV) or head-dim row (dQ^T)
+    const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint8_t* stg = smem + B_SDQ + q * (BQB * 32 * 4);
+    const int key = j * BKB + r;
+    int ok = 1;
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
+    };
+    auto arrive = [&](uint64_t* bar) {
+      __syncwarp();
+      if (lane == 0) mbar_arrive(bar);
+    };
+    // dQ^T of step m: this thread's head-dim row, 64 queries, into the warp's
+    // [64 x 32] staging tile, then one reduce-add into the f32 accumulator.
+    auto dq_epilogue = [&](int m) -> int {
+      if (!wait_all(&dq_full, m & 1)) return 0;
+      tc_fence_after();
+      uint32_t v[2][32];
+      tmem_ld_32x32b_x32(tl + T_DQ, v[0]);
+      tmem_ld_32x32b_x32(tl + T_DQ + 32, v[1]);
+      tmem_ld_wait();
+      tc_fence_before();
+      arrive(&dq_empty);
+      if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging tile
+      __syncwarp();
+      float* st = reinterpret_cast<float*>(stg);
+#pragma unroll
+      for (int c = 0; c < 64; ++c) st[c * 32 + lane] = __uint_as_float(v[c >> 5][c & 31]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        const int h = g * p.hpg + m / per_head, i = i0 + m % per_head;
+        tma_reduce_add_2d(&map_dq, stg, h * FD + q * 32, b * p.S + i * BQB);
+        bulk_commit_group();
+      }
+      return 1;
+    };
+    for (int n = 0; n < nsteps; ++n) {
+      const int s = n & 1;
+      const int i = i0 + n % per_head;
+      if (!(ok = wait_all(&in_full[s], (n >> 1) & 1))) break;
+      if (!(ok = wait_all(&s_full[s], (n >> 1) & 1))) break;
+      tc_fence_after();
+      const float* lse2 = reinterpret_cast<const float*>(smem + B_SLD + s * 512);
+      const float* dsum = lse2 + 64;
+      float pr[64];
+      {
+        uint32_t v[2][32];
+        tmem_ld_32x32b_x32(tl + T_S + s * BQB, v[0]);
+        tmem_ld_32x32b_x32(tl + T_S + s * BQB + 32, v[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        arrive(&s_empty[s]);
+        const bool diag = i < i0 + 2;
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float e = exp2f(fmaf(__uint_as_float(v[c >> 5][c & 31]), p.scale_log2, -lse2[c]));
+          pr[c] = (diag && i * BQB + c < key) ? 0.0f : e;
+        }
+      }
+      // P^T row, once the previous step's products have read P^T and dS^T
+      if (!(ok = wait_all(&pds_empty, (n & 1) ^ 1u))) break;
+      write_sw128_row(smem + B_SP, r, pr);
+      fence_proxy_async_smem();
+      arrive(&p_full);
+      if (n >= 1 && !(ok = dq_epilogue(n - 1))) break;
+      if (!(ok = wait_all(&dp_full, n & 1))) break;
+      tc_fence_after();
+      {
+        uint32_t v[2][32];
+        tmem_ld_32x32b_x32(tl + T_DP, v[0]);
+        tmem_ld_32x32b_x32(tl + T_DP + 32, v[1]);
+        tmem_ld_wait();
+        tc_fence_before();
+        arrive(&dp_empty);
+#pragma unroll
+        for (int c = 0; c < 64; ++c) pr[c] = pr[c] * (__uint_as_float(v[c >> 5][c & 31]) - dsum[c]) * p.scale;
+      }
+      write_sw128_row(smem + B_SDS, r, pr);
+      fence_proxy_async_smem();
+      arrive(&ds_full);
+      arrive(&in_empty[s]);
+    }
+    if (ok) ok = dq_epilogue(nsteps - 1);
+    if (ok && (ok = wait_all(&acc_full, 0))) {
+      tc_fence_after();
+      // dK_j and dV_j rows (bf16) into the group's K and V columns of dqkv
+      __nv_bfloat16* dk = p.dqkv + (size_t)(b * p.S + key) * p.ld_dqkv + p.k_col0 + g * FD;
+      __nv_bfloat16* dv = p.dqkv + (size_t)(b * p.S + key) * p.ld_dqkv + p.v_col0 + g * FD;
+#pragma unroll 1
+      for (int half = 0; half < 2; ++half) {
+        const uint32_t col = half ? T_DK : T_DV;
+        __nv_bfloat16* dst = half ? dk : dv;
+#pragma unroll 1
+        for (int c = 0; c < 2; ++c) {
+          uint32_t v[2][32];
+          tmem_ld_32x32b_x32(tl + col + 64 * c, v[0]);
+          tmem_ld_32x32b_x32(tl + col + 64 * c + 32, v[1]);
+          tmem_ld_wait();
+          float f[64];
+#pragma unroll
+          for (int e = 0; e < 64; ++e) f[e] = __uint_as_float(v[e >> 5][e & 31]);
+          store_row_bf16(dst + 64 * c, f);
+        }
+      }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    __syncwarp();
+    tc_fence_after();
+    tmem_dealloc(tmem_base, FCOLS);
+  }
+}
+
+// D[(b nq + h) S + q] = sum_c dO[b S + q, h d + c] O[b S + q, h d + c] (one
+// warp per (token, head)); the f32 dQ accumulator is cleared alongside.
+__global__ void __launch_bounds__(256) flash_bwd_prep_kernel(const __nv_bfloat16* __restrict__ dz,
+                                                             const __nv_bfloat16* __restrict__ z,
+                                                             float* __restrict__ dsum, float* __restrict__ dq_acc,
+                                                             int64_t N, int S, int nq, int d) {
+  const int lane = threadIdx.x & 31;
+  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
+  const int64_t Zc = (int64_t)nq * d;
+  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < N * nq; w += nw) {
+    const int64_t tok = w / nq;
+    const int h = (int)(w % nq);
+    const int64_t base = tok * Zc + (int64_t)h * d;
+    float acc = 0.0f;
+    for (int c = 4 * lane; c < d; c += 128) {
+      float a[4], o[4];
+      load4(dz + base + c, a);
+      load4(z + base + c, o);
+      acc += a[0] * o[0] + a[1] * o[1] + a[2] * o[2] + a[3] * o[3];
+      const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+      store4(dq_acc + base + c, zero);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (lane == 0) {
+      const int64_t b = tok / S, qi = tok % S;
+      dsum[(b * nq + h) * S + qi] = acc;
+    }
+  }
+}
+
+// dqkv[:, 0 : nq d] = bf16(dQ accumulator).
+__global__ void __launch_bounds__(256) flash_dq_cast_kernel(const float* __restrict__ dq_acc,
+                                                            __nv_bfloat16* __restrict__ dqkv, int64_t N, int64_t Zc,
+                                                            int64_t ld) {
+  const int64_t n4 = N * Zc / 4;
+  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4; t += (int64_t)gridDim.x * blockDim.x) {
+    const int64_t e = 4 * t;
+    const int64_t row = e / Zc, col = e % Zc;
+    float v[4];
+    load4(dq_acc + e, v);
+    store4(dqkv + row * ld + col, v);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_flash_attn_fwd(const void* qkv, int batch, int S, int nq, int nkv, int d, void* z, float* lse2,
+                                  uint32_t* status, cudaStream_t st) {
+  if (d != FD || S % FB != 0 || nq % nkv != 0) return cudaErrorInvalidValue;
+  const int64_t N = (int64_t)batch * S;
+  const int64_t W = (int64_t)(nq + 2 * nkv) * d;
+  CUtensorMap map_qk, map_v, map_z;
+  if (!make_map(&map_qk, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, FB) ||
+      !make_mn_map3(&map_v, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, 2) ||
+      !make_out_map(&map_z, z, false, (uint64_t)nq * d, (uint64_t)N, (uint64_t)nq * d))
+    return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(flash_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, FSMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  FaParams p{};
+  p.S = S;
+  p.nq = nq;
+  p.nkv = nkv;
+  p.hpg = nq / nkv;
+  p.nqblk = S / FB;
+  p.k_col0 = nq * d;
+  p.v_col0 = (nq + nkv) * d;
+  p.scale_log2 = 1.4426950408889634f / sqrtf((float)d);
+  p.lse2 = lse2;
+  p.status = status;
+  const unsigned blocks = (unsigned)((int64_t)batch * nq * p.nqblk);
+  flash_fwd_kernel<<<blocks, FTHREADS, FSMEM, st>>>(map_qk, map_v, map_z, p);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flash_bwd_prep(const void* dz, const void* z, float* dsum, float* dq_acc, int batch, int S, int nq,
+                                  int d, int num_sms, cudaStream_t st) {
+  if (d % 4 != 0 || d > 128) return cudaErrorInvalidValue;
+  const int64_t N = (int64_t)batch * S, warps = N * nq;
+  if (warps <= 0) return cudaSuccess;
+  int64_t blocks = (warps + 7) / 8;
+  if (blocks > 16LL * num_sms) blocks = 16LL * num_sms;
+  flash_bwd_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dz),
+                                                          static_cast<const __nv_bfloat16*>(z), dsum, dq_acc, N, S,
+                                                          nq, d);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flash_attn_bwd(const void* qkv, const void* dz, const float* lse2, const float* dsum, float* dq_acc,
+                                  void* dqkv, int batch, int S, int nq, int nkv, int d, uint32_t* status,
+                                  cudaStream_t st) {
+  if (d != FD || S % BKB != 0 || nq % nkv != 0) return cudaErrorInvalidValue;
+  const int64_t N = (int64_t)batch * S;
+  const int64_t W = (int64_t)(nq + 2 * nkv) * d, Zc = (int64_t)nq * d;
+  CUtensorMap map_kv, map_q, map_do, map_dq;
+  if (!make_map(&map_kv, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, BKB) ||
+      !make_map(&map_q, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, BQB) ||
+      !make_map(&map_do, dz, (uint64_t)Zc, (uint64_t)N, (uint64_t)Zc, BQB) ||
+      !encode_map(&map_dq, dq_acc, EK_F32, (uint64_t)Zc, (uint64_t)N, (uint64_t)Zc, 32, BQB,
+                  CU_TENSOR_MAP_SWIZZLE_NONE))
+    return cudaErrorInvalidValue;
+  static bool attr_done = false;
+  if (!attr_done) {
+    const cudaError_t e = cudaFuncSetAttribute(flash_bwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, BSMEM);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  FbParams p{};
+  p.S = S;
+  p.nq = nq;
+  p.nkv = nkv;
+  p.hpg = nq / nkv;
+  p.q64 = S / BQB;
+  p.k_col0 = nq * d;
+  p.v_col0 = (nq + nkv) * d;
+  p.scale = 1.0f / sqrtf((float)d);
+  p.scale_log2 = 1.4426950408889634f * p.scale;
+  p.lse2 = lse2;
+  p.dsum = dsum;
+  p.dqkv = static_cast<__nv_bfloat16*>(dqkv);
+  p.ld_dqkv = W;
+  p.status = status;
+  const unsigned blocks = (unsigned)((int64_t)(S / BKB) * batch * nkv);
+  flash_bwd_kernel<<<blocks, BTHREADS, BSMEM, st>>>(map_kv, map_q, map_do, map_dq, p, batch);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_flash_dq_cast(const float* dq_acc, void* dqkv, int64_t N, int64_t Zc, int64_t ld, int num_sms,
+                                 cudaStream_t st) {
+  if (Zc % 4 != 0) return cudaErrorInvalidValue;
+  const int64_t n4 = N * Zc / 4;
+  if (n4 <= 0) return cudaSuccess;
+  int64_t blocks = (n4 + 255) / 256;
+  if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+  flash_dq_cast_kernel<<<(unsigned)blocks, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dqkv), N, Zc, ld);
+  return cudaGetLastError();
+}
+
+}  // namespace tpmlp

@@ -174,6 +174,22 @@ cudaError_t launch_attn_softmax_bwd(void* p, const float* dp, int64_t rows, int 
 cudaError_t launch_attn_group_sum(const float* in, void* out, int batch, int S, int n_q, int n_kv, int d,
                                   int64_t ld_out, int64_t col0, int num_sms, cudaStream_t st);
 
+// Fused causal attention (head_dim 128, sequence a multiple of 128): the
+// forward writes Z and the base-2 log-sum-exp of every query row
+// ([batch * n_q * S], row (b n_q + h) S + i); the backward takes D =
+// rowsum(dZ o Z) and a cleared f32 dQ accumulator from flash_bwd_prep, writes
+// the K and V columns of dqkv and adds dQ into the accumulator, which
+// flash_dq_cast converts into dqkv's query columns.
+cudaError_t launch_flash_attn_fwd(const void* qkv, int batch, int S, int nq, int nkv, int d, void* z, float* lse2,
+                                  uint32_t* status, cudaStream_t st);
+cudaError_t launch_flash_bwd_prep(const void* dz, const void* z, float* dsum, float* dq_acc, int batch, int S, int nq,
+                                  int d, int num_sms, cudaStream_t st);
+cudaError_t launch_flash_attn_bwd(const void* qkv, const void* dz, const float* lse2, const float* dsum, float* dq_acc,
+                                  void* dqkv, int batch, int S, int nq, int nkv, int d, uint32_t* status,
+                                  cudaStream_t st);
+cudaError_t launch_flash_dq_cast(const float* dq_acc, void* dqkv, int64_t N, int64_t Zc, int64_t ld, int num_sms,
+                                 cudaStream_t st);
+
 // Message returned by tpmlp_last_error(NULL) on this host thread.
 void set_thread_error(const std::string& msg);
 

@@ -98,6 +98,8 @@ _SIGNATURES = {
     "tpattn_backward": (_i32, [_vp, _vp, _vp, _fp, _fp, _fp, _fp]),
     "tpattn_bind_master": (_i32, [_vp, _fp, _fp, _fp, _fp]),
     "tpattn_sgd_step": (_i32, [_vp, _f32]),
+    "tpattn_set_fused": (_i32, [_vp, _i32]),
+    "tpattn_fused_active": (_i32, [_vp]),
     "tpattn_sync": (_i32, [_vp]),
     "tpattn_set_timing": (_i32, [_vp, _i32]),
     "tpattn_read_kernel_times": (_i32, [_vp, ctypes.POINTER(ctypes.c_float), ctypes.POINTER(ctypes.c_int64), _i32]),
@@ -505,6 +507,14 @@ class TPAttn:
 
     def sync(self):
         _acheck(lib().tpattn_sync(self.ctx), self.ctx)
+
+    def set_fused(self, enable: bool):
+        """Fused attention kernels where the shape allows (the default), or always the unfused path."""
+        _acheck(lib().tpattn_set_fused(self.ctx, int(bool(enable))), self.ctx)
+
+    def fused_active(self) -> bool:
+        """Whether the last forward ran the fused kernels."""
+        return bool(lib().tpattn_fused_active(self.ctx))
 
     def set_timing(self, enable: bool):
         _acheck(lib().tpattn_set_timing(self.ctx, int(bool(enable))), self.ctx)

@@ -27,10 +27,11 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
 
 
-def _run(cfg, t, inp):
+def _run(cfg, t, inp, fused=True):
     from tensor_transformer_mlp_rmsnorm_gb300 import TPAttn, tpmlp_create  # noqa: F401
     from tensor_transformer_mlp_rmsnorm_gb300.tpmlp import tpmlp_mse_loss_grad_noalloc
     m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=max(t, 1))
+    m.set_fused(fused)
     p = {k: _dev(inp[k]) for k in NAMES}
     masters = {k: torch.from_numpy(np.asarray(inp[k], dtype=np.float32)).cuda() for k in NAMES}
     m.bind_master(masters)
@@ -42,6 +43,7 @@ def _run(cfg, t, inp):
     dx, g = m.backward(dy)
     m.sgd_step(LR)
     m.sync()
+    assert m.fused_active() == (fused and cfg.d == 128 and cfg.seq % 128 == 0)
     return {"y": to_np(y), "loss": float(loss.item()), "dx": to_np(dx), "grads": {k: to_np(v) for k, v in g.items()},
             "master": {k: to_np(v) for k, v in masters.items()}}
 
@@ -52,15 +54,35 @@ CASES = [  # batch, seq, hidden, n_q, n_kv, d, t
     (3, 192, 384, 6, 1, 128, 1),
     (2, 512, 1024, 8, 2, 128, 2),
     (1, 64, 128, 2, 2, 64, 2),
+    # shapes the fused kernels take (head_dim 128, seq % 128 == 0): one key
+    # block, an odd number of key blocks, multi-query, multi-head
+    (3, 128, 256, 2, 2, 128, 2),
+    (1, 384, 1024, 8, 4, 128, 4),
+    (2, 256, 512, 4, 1, 128, 1),
 ]
+FUSABLE = [c for c in CASES if c[5] == 128 and c[1] % 128 == 0]
+
+
+def _case(B, S, H, nq, nkv, d, t, fused):
+    cfg = dataclasses.replace(synth.ATTN_CONFIGS["attn_small"], name="case", batch=B, seq=S, hidden=H, n_q=nq,
+                              n_kv=nkv, d=d, w_std=0.05)
+    inp = synth.make_attn_inputs(cfg, seed=B * 1000 + S)
+    return cfg, inp, _run(cfg, t, inp, fused)
 
 
 @pytest.mark.parametrize("B,S,H,nq,nkv,d,t", CASES)
 def test_attention_step_matches_oracle(B, S, H, nq, nkv, d, t):
-    cfg = dataclasses.replace(synth.ATTN_CONFIGS["attn_small"], name="case", batch=B, seq=S, hidden=H, n_q=nq,
-                              n_kv=nkv, d=d, w_std=0.05)
-    inp = synth.make_attn_inputs(cfg, seed=B * 1000 + S)
-    gpu = _run(cfg, t, inp)
+    _check(B, S, H, nq, nkv, d, t, True)
+
+
+@pytest.mark.parametrize("B,S,H,nq,nkv,d,t", FUSABLE)
+def test_attention_step_unfused_matches_oracle(B, S, H, nq, nkv, d, t):
+    """The materialised-score path on the shapes the fused kernels otherwise take."""
+    _check(B, S, H, nq, nkv, d, t, False)
+
+
+def _check(B, S, H, nq, nkv, d, t, fused):
+    cfg, inp, gpu = _case(B, S, H, nq, nkv, d, t, fused)
     p = {k: inp[k] for k in NAMES}
     ora = O.attn_sharded_step(p, inp["x"], inp["target"], cfg.eps, LR, t, B, nq, nkv)
     compare("y", gpu["y"], ora["y"], "bf16")
