@@ -18,6 +18,7 @@ a bounded token sample of the same workload; it is the reference arm here.
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import json
 import os
 import signal
@@ -52,7 +53,7 @@ GELU_UNITS = dict(GEMM_UNITS, gemm_gateup_act=2, gemm_wgrad_gateup=2, gemm_dgrad
 # kernel sources per family: a change to any of them invalidates the recorded DRAM traffic of that
 # family's kernels
 KERNEL_FAMILIES = {
-    "gemm": ("gemm_tc.cu", "gemm_simt.cu", "ptx_sm103.cuh", "epilogue.cuh"),
+    "gemm": ("gemm_tc.cu", "gemm_simt.cu", "ptx_sm103.cuh", "epilogue.cuh", "tma_maps.cuh"),
     "rowwise": ("rowwise.cu", "vec.cuh", "epilogue.cuh"),
     "optim": ("optim.cu", "vec.cuh"),
     "fp8": ("fp8.cu",),
@@ -283,6 +284,8 @@ def ours_attn(args):
     from tensor_transformer_mlp_rmsnorm_gb300.tpmlp import tpmlp_mse_loss_grad_noalloc
     build.build()
     cfg = synth.ATTN_CONFIGS[args.workload]
+    if args.tokens:
+        cfg = dataclasses.replace(cfg, batch=max(1, args.tokens // cfg.seq))
     t = args.t if cfg.n_kv % args.t == 0 else cfg.t_list[0]
     inp = synth.make_attn_inputs(cfg, seed=1234 + rank)
     names = ("norm_w", "w_qkv", "w_o", "b_o")
@@ -295,6 +298,7 @@ def ours_attn(args):
     x, target = x_host.to(dev), tg_host.to(dev)
     m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=t, device=dev)
     m.bind_master(masters)
+    m.set_fused(args.attn_path == "fused")
     y, dy, dx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
     grads = m.new_grads()
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
@@ -314,6 +318,7 @@ def ours_attn(args):
     for _ in range(max(3, args.warmup)):
         step()
     m.sync()
+    fused = m.fused_active()
     clocks = ClockSampler(local)
     barrier()
     torch.cuda.synchronize()
@@ -367,7 +372,9 @@ def ours_attn(args):
     kflops = {"gemm_qkv": 2.0 * N * H * W, "gemm_out_proj": 2.0 * N * nq * d * H, "gemm_dz": 2.0 * N * nq * d * H,
               "gemm_wgrad_out": 2.0 * N * nq * d * H, "gemm_wgrad_qkv": 2.0 * N * H * W,
               "gemm_dgrad_norm": 2.0 * N * H * W, "gemm_scores": causal, "gemm_pv": causal, "gemm_dp": causal,
-              "gemm_dv": causal, "gemm_dq": causal, "gemm_dk": causal}
+              "gemm_dv": causal, "gemm_dq": causal, "gemm_dk": causal,
+              # fused kernels: the products of the algorithm, not the backward's recomputed scores
+              "flash_attn_fwd": 2 * causal, "flash_attn_bwd": 4 * causal}
     top = max(ktimes, key=lambda k: ktimes[k][0])
     per_launch = ktimes[top][0] / max(1, ktimes[top][1])
     if top in kflops:
@@ -375,12 +382,16 @@ def ours_attn(args):
         roof = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": pk["bf16_tflops_sustained"],
                 "unit": "TFLOP/s", "frac": ach / pk["bf16_tflops_sustained"], "traffic": None,
                 "peak_kind": f"bf16_tflops_sustained ({pk_src})", "avg_launch_ms": per_launch,
-                "note": "attention products counted over the causal half of the score square"}
+                "note": "attention products counted over the causal half of the score square"
+                        + ("; the fused backward's score recomputation is not counted" if top == "flash_attn_bwd"
+                           else "")}
     else:
         # causal rows: read up to the diagonal, written up to the end of the diagonal's 256-column block
         tri = B * nq * (S * (S + 1) / 2.0)
         pad = B * nq * S * 128.0  # mean zero tail written past the diagonal
-        nbytes = {"softmax_fwd": 4.0 * tri + 2.0 * (tri + pad), "softmax_bwd": 6.0 * tri + 2.0 * (tri + pad)}.get(top)
+        nbytes = {"softmax_fwd": 4.0 * tri + 2.0 * (tri + pad), "softmax_bwd": 6.0 * tri + 2.0 * (tri + pad),
+                  "flash_bwd_prep": N * nq * d * (2.0 + 2.0 + 4.0) + 4.0 * N * nq,
+                  "flash_dq_cast": N * nq * d * (4.0 + 2.0)}.get(top)
         ach = nbytes / (per_launch / 1e3) / 1e9 if nbytes else None
         roof = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / pk["hbm_gbs"] if ach else None, "traffic": None, "avg_launch_ms": per_launch}
@@ -392,6 +403,7 @@ def ours_attn(args):
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: attention sublayer, {B}x{S} tokens, hidden={H}, {nq} query heads in "
                                f"{nkv} KV groups, head dim {d}, causal, t={t} logical shards, lr={cfg.lr}",
+                   "attention_kernels": "fused (scores never stored)" if fused else "unfused (scores materialised)",
                    "global_batch": B * world, "seq_len": S, "tokens_per_gpu": N, "t": t,
                    "parallelism": f"replicas x{world}", "l2": "no flush: per-step working set >> 129 MB L2"},
         "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
@@ -616,6 +628,8 @@ def main():
                     help="GEMM operands: bf16, or E4M3 with per-tensor scales (fp32 accumulation either way)")
     ap.add_argument("--sequence-parallel", action="store_true",
                     help="sequence-parallel form: per-shard norm-weight / bias gradients, then their sum")
+    ap.add_argument("--attn-path", choices=["fused", "unfused"], default="fused",
+                    help="attention workloads: fused kernels (scores never stored) or materialised scores")
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")

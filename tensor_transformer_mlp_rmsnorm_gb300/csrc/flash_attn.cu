@@ -1,19 +1,27 @@
-// Fused causal attention forward on the sm_103a tensor cores, for the
-// tensor-parallel attention sublayer ("Megatron-LM Explained",
-// "Self-attention: split across heads").  One CTA computes the output rows of
-// a 128-query block of one (sequence, query head), streaming the key/value
-// blocks of its KV group up to the diagonal, without materialising scores:
+// Fused causal attention on the sm_103a tensor cores, for the tensor-parallel
+// attention sublayer ("Megatron-LM Explained", "Self-attention: split across
+// heads"): softmax(Q K^T / sqrt(d)) V per (sequence, query head) with the
+// scores kept on chip, and its backward from each query row's log-sum-exp.
 //
-//   warp 0     : TMA producer -- Q once; K_j and V_j into a two-stage ring.
-//   warp 1     : owns tensor memory (two 128-column score buffers, two
-//                128-column P V buffers) and issues tcgen05.mma: S_j = Q K_j^T,
-//                then P_{j-1} V_{j-1} once the softmax warps have written P.
-//   warps 2..5 : online softmax, one query row per thread: the row maximum
-//                and sum over two passes of S_j from tensor memory, P_j
-//                (bf16) into shared memory in the MMA's K-major layout, and
-//                the running output O = alpha O + P V in registers; finally
-//                O / l as bf16 (TMA store) and the row's log-sum-exp
-//                (base 2, of the log2(e)-scaled scores) for the backward.
+// Forward.  One CTA owns two 128-query tiles (A, B) of one (sequence, query
+// head) and streams the key/value blocks of its KV group up to the diagonal;
+// both tiles share every K_j / V_j load:
+//
+//   warp 0     : TMA producer -- Q_A, Q_B once; K_j and V_j into two-stage rings.
+//   warp 1     : owns tensor memory -- per tile a 128-column score buffer
+//                S (later overwritten by P as packed bf16) and a 128-column
+//                output accumulator O -- and issues tcgen05.mma:
+//                S_X = Q_X K_j^T, then O_X += P_X V_j with P_X read straight
+//                from tensor memory, alternating the tiles so one tile's
+//                softmax runs under the other tile's products.
+//   warps 2..5 : online softmax of tile A, one query row per thread;
+//   warps 6..9 : the same for tile B.  Per key block: one read of the score
+//                row, the row maximum, P = exp2(s - m) written back as bf16,
+//                the running sum l.  The running maximum m is only moved
+//                (and O rescaled in tensor memory) when a block's maximum
+//                exceeds it by more than 2^8, so most blocks touch O not at
+//                all; P stays below 2^8 in the stale frame.  Finally O / l as
+//                bf16 (TMA store) and the base-2 log-sum-exp m + log2(l).
 //
 // Scores are scaled by 1/sqrt(d); exponentials run in base 2 with log2(e)
 // folded into the scale.  The diagonal block masks keys above the query.
@@ -31,30 +39,30 @@
 namespace tpmlp {
 namespace {
 
-constexpr int FB = 128;        // queries per CTA = keys per block
-constexpr int FD = 128;        // head dimension
-constexpr int FTHREADS = 192;
+constexpr int FB = 128;  // queries per tile = keys per block
+constexpr int FD = 128;  // head dimension
+constexpr int FTHREADS = 320;
 constexpr uint32_t FCOLS = 512;
 constexpr uint64_t FWAIT_NS = 1000000000ull;
 constexpr uint64_t FDRAIN_NS = 200000000ull;
 constexpr uint32_t TILE_BYTES = FB * 64 * 2;     // one [128 x 64] bf16 SW128 tile, 16 KB
 constexpr uint32_t OPND_BYTES = 2 * TILE_BYTES;  // a [128 x 128] operand: two tiles
-// shared memory: Q, K[2], V[2], P, output staging
+constexpr float RESCALE_LOG2 = 8.0f;             // move the running maximum only past 2^8
+// shared memory: Q_A, Q_B (each reused as its tile's output staging), K ring, V ring
 constexpr uint32_t SQ = 0;
-constexpr uint32_t SK = SQ + OPND_BYTES;
+constexpr uint32_t SK = SQ + 2 * OPND_BYTES;
 constexpr uint32_t SV = SK + 2 * OPND_BYTES;
-constexpr uint32_t SP = SV + 2 * OPND_BYTES;
-constexpr uint32_t SO = SP + OPND_BYTES;
-constexpr uint32_t FSMEM = SO + 4 * 4096 + 1024;
+constexpr uint32_t FSMEM = SV + 2 * OPND_BYTES + 1024;
 
 struct FaParams {
-  int S, nq, nkv, hpg, nqblk;
-  int k_col0, v_col0;  // first key / value column of the QKV tensor
-  float scale_log2;    // log2(e) / sqrt(d)
-  float* lse2;         // [batch * nq * S] base-2 log-sum-exp of the scaled scores
+  int S, nq, nkv, hpg, nqblk;  // nqblk: 256-query blocks per sequence
+  int k_col0, v_col0;          // first key / value column of the QKV tensor
+  float scale_log2;            // log2(e) / sqrt(d)
+  float* lse2;                 // [batch * nq * S] base-2 log-sum-exp of the scaled scores
   uint32_t* status;
 };
 
+// Row r of a [32 x 32] bf16 box with the 64-byte swizzle (TMA store staging).
 __device__ __forceinline__ void stage_row_bf16_fa(uint8_t* tile, int r, const float* v) {
   uint8_t* rowp = tile + r * 64;
 #pragma unroll
@@ -73,44 +81,51 @@ __device__ __forceinline__ void stage_row_bf16_fa(uint8_t* tile, int r, const fl
   }
 }
 
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 h = __floats2bfloat162_rn(lo, hi);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
 __global__ void __launch_bounds__(FTHREADS, 1)
-    flash_fwd_kernel(const __grid_constant__ CUtensorMap map_qk, const __grid_constant__ CUtensorMap map_v,
-                     const __grid_constant__ CUtensorMap map_z, const FaParams p) {
+    flash_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_z,
+                     const FaParams p) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t q_full, kv_full[2], kv_empty[2], s_full[2], s_empty[2], p_full, p_empty,
-      pv_full[2], pv_empty[2], drain_bar;
+  __shared__ __align__(8) uint64_t q_full, k_full[2], k_empty[2], v_full[2], v_empty[2], s_full[2], p_full[2],
+      o_full[2], drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   volatile int* abort_flag = &abort_sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  // block -> (query block, head, sequence); the longest (diagonal-most) query blocks first
+  // block -> (256-query block, head, sequence); the longest (diagonal-most) query blocks first
   const int qb = p.nqblk - 1 - (int)(blockIdx.x % p.nqblk);
   const int bh = (int)(blockIdx.x / p.nqblk);
   const int h = bh % p.nq, b = bh / p.nq;
   const int g = h / p.hpg;
-  const int nk = qb + 1;  // key blocks up to the diagonal
-  const int row_q = b * p.S + qb * FB;
+  const int q0 = qb * 2 * FB;           // first query of tile A
+  const bool has_b = q0 + FB < p.S;     // tile B exists (S % 256 == 128 leaves the last CTA one tile)
+  const int nk_a = 2 * qb + 1;          // key blocks seen by tile A (its diagonal is the last)
+  const int nk_b = has_b ? 2 * qb + 2 : 0;
+  const int nk = has_b ? nk_b : nk_a;
+  const int row_seq = b * p.S;
 
   if (threadIdx.x == 0) {
     mbar_init(&q_full, 1);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(&kv_full[i], 1);
-      mbar_init(&kv_empty[i], 1);
+      mbar_init(&k_full[i], 1);
+      mbar_init(&k_empty[i], 1);
+      mbar_init(&v_full[i], 1);
+      mbar_init(&v_empty[i], 1);
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
-      mbar_init(&pv_full[i], 1);
-      mbar_init(&pv_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&o_full[i], 1);
     }
-    mbar_init(&p_full, 4);
-    mbar_init(&p_empty, 1);
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
   if (warp == 0 && lane == 0) {
-    tma_prefetch_desc(&map_qk);
-    tma_prefetch_desc(&map_v);
+    tma_prefetch_desc(&map_qkv);
     tma_prefetch_desc(&map_z);
   }
   if (warp == 1) {
@@ -125,220 +140,212 @@ __global__ void __launch_bounds__(FTHREADS, 1)
   if (warp == 0) {
     if (lane == 0) {
       // ------------------------------------------------------------ producer
-      uint32_t armed = 0, armed_par = 0;
+      uint32_t armed_k = 0, par_k = 0, armed_v = 0, par_v = 0;
       bool ok = true;
-      mbar_arrive_expect_tx(&q_full, OPND_BYTES);
-      for (int t = 0; t < 2; ++t) tma_load_2d(smem + SQ + t * TILE_BYTES, &map_qk, &q_full, h * FD + 64 * t, row_q);
+      mbar_arrive_expect_tx(&q_full, (has_b ? 2 : 1) * OPND_BYTES);
+      for (int x = 0; x < (has_b ? 2 : 1); ++x)
+        for (int t = 0; t < 2; ++t)
+          tma_load_2d(smem + SQ + x * OPND_BYTES + t * TILE_BYTES, &map_qkv, &q_full, h * FD + 64 * t,
+                      row_seq + q0 + x * FB);
       for (int j = 0; ok && j < nk; ++j) {
         const int s = j & 1;
-        if (!mbar_wait(&kv_empty[s], ((j >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS)) {
+        const uint32_t par = (uint32_t)((j >> 1) & 1);
+        const int row_k = row_seq + j * FB;
+        if (!mbar_wait(&k_empty[s], par ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(&kv_full[s], 2 * OPND_BYTES);
-        armed |= 1u << s;
-        armed_par = (armed_par & ~(1u << s)) | ((uint32_t)((j >> 1) & 1) << s);
-        const int row_k = b * p.S + j * FB;
-        for (int t = 0; t < 2; ++t) {
-          tma_load_2d(smem + SK + s * OPND_BYTES + t * TILE_BYTES, &map_qk, &kv_full[s], p.k_col0 + g * FD + 64 * t,
+        mbar_arrive_expect_tx(&k_full[s], OPND_BYTES);
+        armed_k |= 1u << s;
+        par_k = (par_k & ~(1u << s)) | (par << s);
+        for (int t = 0; t < 2; ++t)
+          tma_load_2d(smem + SK + s * OPND_BYTES + t * TILE_BYTES, &map_qkv, &k_full[s], p.k_col0 + g * FD + 64 * t,
                       row_k);
-          tma_load_3d(smem + SV + s * OPND_BYTES + t * TILE_BYTES, &map_v, &kv_full[s], 0, row_k + 64 * t,
-                      (p.v_col0 + g * FD) >> 6);
+        if (!mbar_wait(&v_empty[s], par ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS)) {
+          ok = false;
+          break;
         }
+        mbar_arrive_expect_tx(&v_full[s], OPND_BYTES);
+        armed_v |= 1u << s;
+        par_v = (par_v & ~(1u << s)) | (par << s);
+        for (int t = 0; t < 2; ++t)
+          tma_load_2d(smem + SV + s * OPND_BYTES + t * TILE_BYTES, &map_qkv, &v_full[s], p.v_col0 + g * FD + 64 * t,
+                      row_k);
       }
       if (!ok || *abort_flag) {
+        // copies still in flight land on the full barriers of the phases armed last
         int no_abort = 0;
         mbar_wait(&q_full, 0, &no_abort, p.status, 0u, FDRAIN_NS);
-        // copies still in flight land on the full barriers of the phases armed last
-        for (int s = 0; s < 2; ++s)
-          if (armed & (1u << s)) mbar_wait(&kv_full[s], (armed_par >> s) & 1u, &no_abort, p.status, 0u, FDRAIN_NS / 4);
+        for (int s = 0; s < 2; ++s) {
+          if (armed_k & (1u << s)) mbar_wait(&k_full[s], (par_k >> s) & 1u, &no_abort, p.status, 0u, FDRAIN_NS / 4);
+          if (armed_v & (1u << s)) mbar_wait(&v_full[s], (par_v >> s) & 1u, &no_abort, p.status, 0u, FDRAIN_NS / 4);
+        }
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
     constexpr uint32_t IDESC_S = idesc_bf16_f32(FB, FB, false, false);
     constexpr uint32_t IDESC_PV = idesc_bf16_f32(FB, FD, false, true);
-    int ok = __all_sync(0xffffffffu, mbar_wait(&q_full, 0, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
-    auto issue_pv = [&](int jj) -> int {
-      const int s = jj & 1;
-      int w = mbar_wait(&p_full, jj & 1, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
-      w = w && mbar_wait(&pv_empty[s], ((jj >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
-      if (!__all_sync(0xffffffffu, w)) return 0;
-      tc_fence_after();
-      if (elect_one()) {
-        const uint32_t d_tmem = tmem_base + 256 + s * FB;
-        const uint32_t pa = smem_u32(smem + SP), vb = smem_u32(smem + SV + s * OPND_BYTES);
+    const bool leader = elect_one();  // the lane that issues every MMA and commit
+    auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
+      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
+    };
+    // S_x = Q_x K_j^T into tile x's score columns
+    auto issue_s = [&](int x, int j) {
+      if (leader) {
+        const uint32_t qa = smem_u32(smem + SQ + x * OPND_BYTES), kb = smem_u32(smem + SK + (j & 1) * OPND_BYTES);
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a_desc = sw128_desc(pa + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024);
-          const uint64_t b_desc = sw128_desc(vb + (kk >> 2) * TILE_BYTES + (kk & 3) * 2048, 8192, 1024);
-          tc_mma_f16(d_tmem, a_desc, b_desc, IDESC_PV, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&pv_full[s]);
-        tc_commit(&p_empty);
-        tc_commit(&kv_empty[s]);
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(tmem_base + x * FB, sw128_desc(qa + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024),
+                     sw128_desc(kb + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+        tc_commit(&s_full[x]);
       }
       __syncwarp();
-      return 1;
     };
+    // O_x += P_x V_j, P_x from tile x's score columns (bf16 pairs, 8 columns per K = 16)
+    auto issue_pv = [&](int x, int j, bool last) {
+      if (leader) {
+        const uint32_t vb = smem_u32(smem + SV + (j & 1) * OPND_BYTES);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16_ts(tmem_base + 256 + x * FD, tmem_base + x * FB + kk * 8,
+                        sw128_desc(vb + kk * 2048, TILE_BYTES, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+        if (last) tc_commit(&o_full[x]);
+      }
+      __syncwarp();
+    };
+    int ok = wait_all(&q_full, 0) && wait_all(&k_full[0], 0);
+    if (ok) {
+      tc_fence_after();
+      issue_s(0, 0);
+      if (has_b) issue_s(1, 0);
+      if (leader) tc_commit(&k_empty[0]);
+      __syncwarp();
+    }
     for (int j = 0; ok && j < nk; ++j) {
       const int s = j & 1;
-      int w = mbar_wait(&kv_full[s], (j >> 1) & 1, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
-      w = w && mbar_wait(&s_empty[s], ((j >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS);
-      ok = __all_sync(0xffffffffu, w);
-      if (!ok) break;
+      if (!(ok = wait_all(&v_full[s], (j >> 1) & 1))) break;
+      const bool next = j + 1 < nk;
+      if (j < nk_a) {
+        if (!(ok = wait_all(&p_full[0], j & 1))) break;
+        tc_fence_after();
+        issue_pv(0, j, j + 1 == nk_a);
+      }
+      if (next && !(ok = wait_all(&k_full[(j + 1) & 1], ((j + 1) >> 1) & 1))) break;
       tc_fence_after();
-      if (elect_one()) {
-        const uint32_t d_tmem = tmem_base + s * FB;
-        const uint32_t qa = smem_u32(smem + SQ), kb = smem_u32(smem + SK + s * OPND_BYTES);
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a_desc = sw128_desc(qa + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024);
-          const uint64_t b_desc = sw128_desc(kb + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024);
-          tc_mma_f16(d_tmem, a_desc, b_desc, IDESC_S, kk > 0 ? 1u : 0u);
-        }
-        tc_commit(&s_full[s]);
+      if (j + 1 < nk_a) issue_s(0, j + 1);
+      if (has_b) {
+        if (!(ok = wait_all(&p_full[1], j & 1))) break;
+        tc_fence_after();
+        issue_pv(1, j, j + 1 == nk_b);
+        if (j + 1 < nk_b) issue_s(1, j + 1);
+      }
+      if (leader) {
+        tc_commit(&v_empty[s]);
+        if (next) tc_commit(&k_empty[(j + 1) & 1]);
       }
       __syncwarp();
-      if (j >= 1) ok = issue_pv(j - 1);
     }
-    if (ok) issue_pv(nk - 1);
-    if (elect_one()) tc_commit(&drain_bar);
+    if (leader) tc_commit(&drain_bar);
     __syncwarp();
     int no_abort = 0;
     mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
   } else {
     // --------------------------------------------------------- softmax warps
-    const int q = warp & 3;
-    const int r = q * 32 + lane;  // query row within the block
-    const uint32_t trow = tmem_base + ((uint32_t)(q * 32) << 16);
-    uint8_t* stg = smem + SO + (warp - 2) * 4096;
-    float o[FD];
-#pragma unroll
-    for (int c = 0; c < FD; ++c) o[c] = 0.0f;
-    float m2 = -INFINITY, l = 0.0f;  // running max (log2 units) and sum
-    int ok = 1;
-    for (int j = 0; j < nk; ++j) {
-      const int s = j & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[s], (j >> 1) & 1, abort_flag, p.status, STATUS_TIMEOUT,
-                                             FWAIT_NS));
+    const int x = (warp - 2) >> 2;  // tile
+    const int q4 = warp & 3;        // TMEM lane quarter of this warp
+    const int r = q4 * 32 + lane;   // query row within the tile
+    const int nkx = x ? nk_b : nk_a;
+    const uint32_t lane_off = (uint32_t)(q4 * 32) << 16;
+    const uint32_t t_s = tmem_base + lane_off + x * FB;
+    const uint32_t t_o = tmem_base + lane_off + 256 + x * FD;
+    float m_run = -INFINITY, l = 0.0f;  // running maximum (log2 units, possibly stale) and sum
+    int ok = nkx > 0;                   // tile B may be absent
+    for (int j = 0; ok && j < nkx; ++j) {
+      ok = __all_sync(0xffffffffu, mbar_wait(&s_full[x], j & 1, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
       if (!ok) break;
       tc_fence_after();
-      const bool diag = j == qb;
-      // pass 1: the row maximum of this block
-      float bm = -INFINITY;
-#pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(trow + s * FB + c * 32, v);
-        tmem_ld_wait();
+      uint32_t v[128];
+      tmem_ld_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_32x32b_x32(t_s + 64, *reinterpret_cast<uint32_t(*)[32]>(v + 64));
+      tmem_ld_32x32b_x32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(v + 96));
+      tmem_ld_wait();
+      const bool diag = j == nkx - 1;  // keys above the query are masked (-> P = 0)
+      if (diag) {
 #pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const bool masked = diag && (c * 32 + e > r);
-          bm = masked ? bm : fmaxf(bm, __uint_as_float(v[e]));
-        }
+        for (int c = 0; c < 128; ++c)
+          if (c > r) v[c] = __float_as_uint(-INFINITY);
       }
-      const float m2n = fmaxf(m2, bm * p.scale_log2);
-      const float alpha = exp2f(m2 - m2n);  // 0 on the first block
-      // P must not overwrite the tile the previous P V is still reading
-      ok = __all_sync(0xffffffffu, mbar_wait(&p_empty, (j & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
-      if (!ok) break;
-      // pass 2: P = exp2(s * scale_log2 - m2n) into shared memory, and its sum
+      float mb = __uint_as_float(v[0]);
+#pragma unroll
+      for (int c = 1; c < 128; ++c) mb = fmaxf(mb, __uint_as_float(v[c]));
+      mb *= p.scale_log2;
+      const bool move = __any_sync(0xffffffffu, mb > m_run + RESCALE_LOG2);
+      float alpha = 1.0f;
+      if (move) {
+        const float m_new = fmaxf(m_run, mb);
+        alpha = exp2f(m_run - m_new);  // 0 on the first block
+        l *= alpha;
+        m_run = m_new;
+      }
       float ps = 0.0f;
+#pragma unroll
+      for (int c = 0; c < 128; c += 2) {
+        const float p0 = exp2f(fmaf(__uint_as_float(v[c]), p.scale_log2, -m_run));
+        const float p1 = exp2f(fmaf(__uint_as_float(v[c + 1]), p.scale_log2, -m_run));
+        ps += p0 + p1;
+        v[c >> 1] = pack_bf16x2(p0, p1);
+      }
+      l += ps;
+      tmem_st_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_st_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      if (move && j > 0) {
+        // O holds blocks < j (the score MMA of block j was issued after the
+        // output MMA of block j - 1, so that one has completed too); the
+        // output MMA of block j waits for p_full below
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t v[32];
-        tmem_ld_32x32b_x32(trow + s * FB + c * 32, v);
-        tmem_ld_wait();
-        float pv[32];
-#pragma unroll
-        for (int e = 0; e < 32; ++e) {
-          const bool masked = diag && (c * 32 + e > r);
-          pv[e] = masked ? 0.0f : exp2f(__uint_as_float(v[e]) * p.scale_log2 - m2n);
-          ps += pv[e];
-        }
-        // keys [32c, 32c+32) sit in tile c / 2, 16-byte chunks 4 (c % 2) .. +3
-        uint8_t* tile = smem + SP + (c >> 1) * TILE_BYTES + r * 128;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int chunk = (c & 1) * 4 + k;
-          uint4 w;
-          __nv_bfloat162 hh;
-          hh = __floats2bfloat162_rn(pv[8 * k], pv[8 * k + 1]);
-          w.x = *reinterpret_cast<uint32_t*>(&hh);
-          hh = __floats2bfloat162_rn(pv[8 * k + 2], pv[8 * k + 3]);
-          w.y = *reinterpret_cast<uint32_t*>(&hh);
-          hh = __floats2bfloat162_rn(pv[8 * k + 4], pv[8 * k + 5]);
-          w.z = *reinterpret_cast<uint32_t*>(&hh);
-          hh = __floats2bfloat162_rn(pv[8 * k + 6], pv[8 * k + 7]);
-          w.w = *reinterpret_cast<uint32_t*>(&hh);
-          *reinterpret_cast<uint4*>(tile + ((chunk ^ (r & 7)) << 4)) = w;
-        }
-      }
-      tc_fence_before();
-      fence_proxy_async_smem();  // P is read by the tensor cores (async proxy)
-      __syncwarp();
-      if (lane == 0) {
-        mbar_arrive(&s_empty[s]);
-        mbar_arrive(&p_full);
-      }
-      // O = alpha (O + P_{j-1} V_{j-1}); the sum follows the same frame
-      if (j >= 1) {
-        const int sp = (j - 1) & 1;
-        ok = __all_sync(0xffffffffu, mbar_wait(&pv_full[sp], ((j - 1) >> 1) & 1, abort_flag, p.status,
-                                               STATUS_TIMEOUT, FWAIT_NS));
-        if (!ok) break;
-        tc_fence_after();
-#pragma unroll
         for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(trow + 256 + sp * FB + c * 32, v);
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(t_o + 32 * c, o);
           tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[c * 32 + e] += __uint_as_float(v[e]);
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st_32x32b_x32(t_o + 32 * c, o);
         }
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&pv_empty[sp]);
       }
-#pragma unroll
-      for (int c = 0; c < FD; ++c) o[c] *= alpha;
-      l = l * alpha + ps;
-      m2 = m2n;
+      tmem_st_wait();
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(&p_full[x]);
     }
     if (ok) {
-      const int sp = (nk - 1) & 1;
-      ok = __all_sync(0xffffffffu, mbar_wait(&pv_full[sp], ((nk - 1) >> 1) & 1, abort_flag, p.status,
-                                             STATUS_TIMEOUT, FWAIT_NS));
+      ok = __all_sync(0xffffffffu, mbar_wait(&o_full[x], 0, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
       if (ok) {
         tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-          uint32_t v[32];
-          tmem_ld_32x32b_x32(trow + 256 + sp * FB + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[c * 32 + e] += __uint_as_float(v[e]);
-        }
         const float inv = 1.0f / l;
-#pragma unroll
-        for (int c = 0; c < FD; ++c) o[c] *= inv;
-        p.lse2[(size_t)bh * p.S + qb * FB + r] = m2 + log2f(l);
-        // output rows [row_q + 32 q, +32), 32 columns at a time through two staging tiles
-#pragma unroll
+        const int row = q0 + x * FB + r;
+        p.lse2[(size_t)bh * p.S + row] = m_run + log2f(l);
+        // output rows [q0 + x FB + 32 q4, +32): this warp's 8 KB of the tile's
+        // (now idle) Q buffer, four [32 x 32] boxes
+        uint8_t* stg = smem + SQ + x * OPND_BYTES + q4 * 8192;
+#pragma unroll 1
         for (int c = 0; c < 4; ++c) {
-          uint8_t* sb = stg + (c & 1) * 2048;
-          if (lane == 0) bulk_wait_read_but_last();
-          __syncwarp();
-          stage_row_bf16_fa(sb, lane, o + c * 32);
-          fence_proxy_async_smem();
-          __syncwarp();
-          if (lane == 0) {
-            tma_store_2d(&map_z, sb, h * FD + c * 32, row_q + q * 32);
-            bulk_commit_group();
-          }
+          uint32_t o[32];
+          tmem_ld_32x32b_x32(t_o + 32 * c, o);
+          tmem_ld_wait();
+          float f[32];
+#pragma unroll
+          for (int e = 0; e < 32; ++e) f[e] = __uint_as_float(o[e]) * inv;
+          stage_row_bf16_fa(stg + c * 2048, lane, f);
         }
-        if (lane == 0) bulk_wait_all();
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+          for (int c = 0; c < 4; ++c) tma_store_2d(&map_z, stg + c * 2048, h * FD + c * 32, row_seq + q0 + x * FB + q4 * 32);
+          bulk_commit_group();
+          bulk_wait_all();
+        }
         __syncwarp();
       }
     }
@@ -352,7 +359,6 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     tmem_dealloc(tmem_base, FCOLS);
   }
 }
-
 
 // ---------------------------------------------------------------- backward
 // One CTA per (sequence b, KV group g, 128-key block j) accumulates dK_j and
@@ -793,9 +799,8 @@ cudaError_t launch_flash_attn_fwd(const void* qkv, int batch, int S, int nq, int
   if (d != FD || S % FB != 0 || nq % nkv != 0) return cudaErrorInvalidValue;
   const int64_t N = (int64_t)batch * S;
   const int64_t W = (int64_t)(nq + 2 * nkv) * d;
-  CUtensorMap map_qk, map_v, map_z;
-  if (!make_map(&map_qk, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, FB) ||
-      !make_mn_map3(&map_v, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, 2) ||
+  CUtensorMap map_qkv, map_z;
+  if (!make_map(&map_qkv, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, FB) ||
       !make_out_map(&map_z, z, false, (uint64_t)nq * d, (uint64_t)N, (uint64_t)nq * d))
     return cudaErrorInvalidValue;
   static bool attr_done = false;
@@ -809,14 +814,14 @@ cudaError_t launch_flash_attn_fwd(const void* qkv, int batch, int S, int nq, int
   p.nq = nq;
   p.nkv = nkv;
   p.hpg = nq / nkv;
-  p.nqblk = S / FB;
+  p.nqblk = (S + 2 * FB - 1) / (2 * FB);
   p.k_col0 = nq * d;
   p.v_col0 = (nq + nkv) * d;
   p.scale_log2 = 1.4426950408889634f / sqrtf((float)d);
   p.lse2 = lse2;
   p.status = status;
   const unsigned blocks = (unsigned)((int64_t)batch * nq * p.nqblk);
-  flash_fwd_kernel<<<blocks, FTHREADS, FSMEM, st>>>(map_qk, map_v, map_z, p);
+  flash_fwd_kernel<<<blocks, FTHREADS, FSMEM, st>>>(map_qkv, map_z, p);
   return cudaGetLastError();
 }
 
