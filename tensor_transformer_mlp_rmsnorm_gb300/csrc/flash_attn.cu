@@ -370,35 +370,46 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 //   S^T  = K_j Q_i^T               dP^T = V_j dO_i^T
 //   P^T  = exp2(S^T log2(e)/sqrt(d) - lse2_i)    (keys above a query masked)
 //   dS^T = P^T o (dP^T - D_i) / sqrt(d)
-//   dV_j += P^T dO_i               dK_j += dS^T Q_i      dQ_i^T += K_j^T dS^T
+//   dV_j += P^T dO_i               dK_j += dS^T Q_i      dQ_i^T = K_j^T dS^T
 //
 //   warp 0     : TMA producer -- K_j, V_j once; Q_i, dO_i, lse2_i, D_i per
-//                step into a two-stage ring.
-//   warp 1     : tensor memory owner and MMA issuer.
-//   warps 2..5 : one key row per thread for P^T and dS^T (bf16, into shared
-//                memory in the K-major layout the MMAs read), one head-dim row
-//                per thread for the dQ^T epilogue, and the final dK / dV rows.
+//                step into a three-stage ring.  Steps run over the query
+//                blocks from the last one down, the heads of the group inner,
+//                so the CTAs of one (sequence, group) read the same Q / dO
+//                blocks at about the same time.
+//   warp 1     : tensor memory owner and MMA issuer; per step n it issues
+//                S^T_{n+1}, dV_n, dP^T_{n+1}, dK_n, dQ^T_n, so the next
+//                step's scores and their gradient are ready before the row
+//                warps reach them.
+//   warps 2..5 : one key row per thread: P^T (bf16, written over its scores
+//                in tensor memory, where the dV product reads it) and dS^T
+//                (bf16, into a double-buffered shared-memory tile in the
+//                K-major layout the MMAs read), and at the end the dK / dV
+//                rows.
+//   warps 6..9 : dQ^T epilogue, one head-dim row per thread: tensor memory to
+//                a shared staging tile, then one reduce-add per warp.
 // The same shared-memory tile of Q, dO, K or dS^T serves as a K-major operand
 // of one product and an MN-major operand of another: a 128-byte swizzled tile
 // of 64-element rows is both.
 constexpr int BKB = 128;  // keys per CTA
 constexpr int BQB = 64;   // queries per step
-constexpr int BTHREADS = 192;
+constexpr int BTHREADS = 320;
 constexpr uint32_t KT_BYTES = BKB * 64 * 2;   // [128 keys x 64 d] tile, 16 KB
 constexpr uint32_t QT_BYTES = BQB * 64 * 2;   // [64 queries x 64 d] tile, 8 KB
 // shared memory
 constexpr uint32_t B_SK = 0;                          // K_j: two 16 KB tiles
 constexpr uint32_t B_SV = B_SK + 2 * KT_BYTES;        // V_j
-constexpr uint32_t B_SQ = B_SV + 2 * KT_BYTES;        // Q_i ring: 2 stages x two 8 KB tiles
-constexpr uint32_t B_SDO = B_SQ + 4 * QT_BYTES;       // dO_i ring
-constexpr uint32_t B_SP = B_SDO + 4 * QT_BYTES;       // P^T [128 keys x 64 queries], 16 KB
-constexpr uint32_t B_SDS = B_SP + KT_BYTES;           // dS^T
-constexpr uint32_t B_SDQ = B_SDS + KT_BYTES;          // dQ^T staging: 4 warps x [64 q x 32 d] f32
-constexpr uint32_t B_SLD = B_SDQ + 4 * BQB * 32 * 4;  // lse2 / D ring: 2 stages x 2 x 64 floats
-constexpr uint32_t BSMEM = B_SLD + 2 * 2 * BQB * 4 + 1024;
+constexpr int QST = 3;                                // Q / dO / lse2 / D ring stages
+constexpr uint32_t B_SQ = B_SV + 2 * KT_BYTES;        // Q_i ring: QST stages x two 8 KB tiles
+constexpr uint32_t B_SDO = B_SQ + 2 * QST * QT_BYTES; // dO_i ring
+constexpr uint32_t B_SDS = B_SDO + 2 * QST * QT_BYTES; // dS^T ring: 2 x [128 keys x 64 queries], 16 KB each
+constexpr uint32_t B_SDQ = B_SDS + 2 * KT_BYTES;      // dQ^T staging: 4 warps x [64 q x 32 d] f32
+constexpr uint32_t B_SLD = B_SDQ + 4 * BQB * 32 * 4;  // lse2 / D ring: QST stages x 2 x 64 floats
+constexpr uint32_t BSMEM = B_SLD + QST * 2 * BQB * 4 + 1024;
+static_assert(BSMEM <= 232448 - 256, "shared memory budget");
 constexpr uint32_t IN_TX = 4 * QT_BYTES + 2 * BQB * 4;
 // tensor memory columns
-constexpr uint32_t T_S = 0;     // S^T ring: 2 x 64
+constexpr uint32_t T_S = 0;     // S^T ring: 2 x 64 (P^T over the first 32 columns of its slot)
 constexpr uint32_t T_DP = 128;  // dP^T: 64
 constexpr uint32_t T_DQ = 192;  // dQ^T: 64
 constexpr uint32_t T_DV = 256;  // dV_j: 128
@@ -420,15 +431,10 @@ __device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* 
 #pragma unroll
   for (int c = 0; c < 8; ++c) {
     uint4 w;
-    __nv_bfloat162 h;
-    h = __floats2bfloat162_rn(v[8 * c], v[8 * c + 1]);
-    w.x = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(v[8 * c + 2], v[8 * c + 3]);
-    w.y = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(v[8 * c + 4], v[8 * c + 5]);
-    w.z = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(v[8 * c + 6], v[8 * c + 7]);
-    w.w = *reinterpret_cast<uint32_t*>(&h);
+    w.x = pack_bf16x2(v[8 * c], v[8 * c + 1]);
+    w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
+    w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
+    w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
     reinterpret_cast<uint4*>(dst)[c] = w;
   }
 }
@@ -440,15 +446,10 @@ __device__ __forceinline__ void write_sw128_row(uint8_t* tile, int r, const floa
 #pragma unroll
   for (int k = 0; k < 8; ++k) {
     uint4 w;
-    __nv_bfloat162 h;
-    h = __floats2bfloat162_rn(v[8 * k], v[8 * k + 1]);
-    w.x = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(v[8 * k + 2], v[8 * k + 3]);
-    w.y = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(v[8 * k + 4], v[8 * k + 5]);
-    w.z = *reinterpret_cast<uint32_t*>(&h);
-    h = __floats2bfloat162_rn(v[8 * k + 6], v[8 * k + 7]);
-    w.w = *reinterpret_cast<uint32_t*>(&h);
+    w.x = pack_bf16x2(v[8 * k], v[8 * k + 1]);
+    w.y = pack_bf16x2(v[8 * k + 2], v[8 * k + 3]);
+    w.z = pack_bf16x2(v[8 * k + 4], v[8 * k + 5]);
+    w.w = pack_bf16x2(v[8 * k + 6], v[8 * k + 7]);
     *reinterpret_cast<uint4*>(rowp + ((k ^ (r & 7)) << 4)) = w;
   }
 }
@@ -458,8 +459,8 @@ __global__ void __launch_bounds__(BTHREADS, 1)
                      const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dq,
                      const FbParams p, int batch) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t kv_full, in_full[2], in_empty[2], s_full[2], s_empty[2], dp_full, dp_empty,
-      p_full, ds_full, pds_empty, dq_full, dq_empty, acc_full, drain_bar;
+  __shared__ __align__(8) uint64_t kv_full, in_full[QST], in_empty[QST], s_full[2], dp_full, dp_empty, p_full[2],
+      ds_full[2], ds_empty[2], dq_full, dq_empty, acc_full, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -472,22 +473,26 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   const int b = bg / p.nkv, g = bg % p.nkv;
   const int i0 = 2 * j;                 // first 64-query block that sees key block j
   const int per_head = p.q64 - i0;
-  const int nsteps = p.hpg * per_head;  // >= hpg * 2
+  const int nsteps = p.hpg * per_head;  // >= 2
   const int row_k = b * p.S + j * BKB;
+  // step n -> 64-query block i (from the last down) and query head h of the group
+  auto step_i = [&](int n) { return p.q64 - 1 - n / p.hpg; };
+  auto step_h = [&](int n) { return g * p.hpg + n % p.hpg; };
 
   if (threadIdx.x == 0) {
     mbar_init(&kv_full, 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < QST; ++i) {
       mbar_init(&in_full[i], 1);
       mbar_init(&in_empty[i], 1 + 4);  // the MMA commit and the four row warps (lse2 / D reads)
+    }
+    for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&s_empty[i], 4);
+      mbar_init(&p_full[i], 4);
+      mbar_init(&ds_full[i], 4);
+      mbar_init(&ds_empty[i], 1);
     }
     mbar_init(&dp_full, 1);
     mbar_init(&dp_empty, 4);
-    mbar_init(&p_full, 4);
-    mbar_init(&ds_full, 4);
-    mbar_init(&pds_empty, 1);
     mbar_init(&dq_full, 1);
     mbar_init(&dq_empty, 4);
     mbar_init(&acc_full, 1);
@@ -509,6 +514,13 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem_base = tmem_base_sh;
+  auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
+    return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
+  };
+  auto arrive = [&](uint64_t* bar) {
+    __syncwarp();
+    if (lane == 0) mbar_arrive(bar);
+  };
 
   if (warp == 0) {
     if (lane == 0) {
@@ -521,16 +533,17 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         tma_load_2d(smem + B_SV + t * KT_BYTES, &map_kv, &kv_full, p.v_col0 + g * FD + 64 * t, row_k);
       }
       for (int n = 0; ok && n < nsteps; ++n) {
-        const int s = n & 1;
-        if (!mbar_wait(&in_empty[s], ((n >> 1) & 1) ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS)) {
+        const int s = n % QST;
+        const uint32_t par = (uint32_t)((n / QST) & 1);
+        if (!mbar_wait(&in_empty[s], par ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS)) {
           ok = false;
           break;
         }
-        const int h = g * p.hpg + n / per_head, i = i0 + n % per_head;
+        const int h = step_h(n), i = step_i(n);
         const int row_q = b * p.S + i * BQB;
         mbar_arrive_expect_tx(&in_full[s], IN_TX);
         armed |= 1u << s;
-        armed_par = (armed_par & ~(1u << s)) | ((uint32_t)((n >> 1) & 1) << s);
+        armed_par = (armed_par & ~(1u << s)) | (par << s);
         for (int t = 0; t < 2; ++t) {
           tma_load_2d(smem + B_SQ + (2 * s + t) * QT_BYTES, &map_q, &in_full[s], h * FD + 64 * t, row_q);
           tma_load_2d(smem + B_SDO + (2 * s + t) * QT_BYTES, &map_do, &in_full[s], h * FD + 64 * t, row_q);
@@ -542,23 +555,20 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       if (!ok || *abort_flag) {
         int no_abort = 0;
         mbar_wait(&kv_full, 0, &no_abort, p.status, 0u, FDRAIN_NS);
-        for (int s = 0; s < 2; ++s)
+        for (int s = 0; s < QST; ++s)
           if (armed & (1u << s)) mbar_wait(&in_full[s], (armed_par >> s) & 1u, &no_abort, p.status, 0u, FDRAIN_NS / 4);
       }
     }
   } else if (warp == 1) {
     // -------------------------------------------------------------- MMA issuer
-    constexpr uint32_t IDESC_SP = idesc_bf16_f32(BKB, BQB, false, false);   // S^T, dP^T
-    constexpr uint32_t IDESC_KV = idesc_bf16_f32(BKB, FD, false, true);     // dV, dK
-    constexpr uint32_t IDESC_DQ = idesc_bf16_f32(FD, BQB, true, true);      // dQ^T
+    constexpr uint32_t IDESC_SP = idesc_bf16_f32(BKB, BQB, false, false);  // S^T, dP^T
+    constexpr uint32_t IDESC_KV = idesc_bf16_f32(BKB, FD, false, true);    // dV, dK
+    constexpr uint32_t IDESC_DQ = idesc_bf16_f32(FD, BQB, true, true);     // dQ^T
+    const bool leader = elect_one();  // the lane that issues every MMA and commit
     const uint32_t sk = smem_u32(smem + B_SK), sv = smem_u32(smem + B_SV);
-    const uint32_t sp = smem_u32(smem + B_SP), sds = smem_u32(smem + B_SDS);
-    auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
-      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
-    };
     // S^T_n = K Q_n^T (ring slot n & 1) or dP^T_n = V dO_n^T, then a commit to `done`
     auto issue_nt = [&](uint32_t d_tmem, uint32_t a, uint32_t bq, uint64_t* done) {
-      if (elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
           const uint64_t a_desc = sw128_desc(a + (kk >> 2) * KT_BYTES + (kk & 3) * 32, 16, 1024);
@@ -569,42 +579,46 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       }
       __syncwarp();
     };
-    int ok = wait_all(&kv_full, 0);
+    // S^T_n goes into slot n & 1, where P^T_{n-2} was read by dV_{n-2}:
+    // issued before it, in order
     auto issue_s = [&](int n) -> int {
-      const int s = n & 1;
-      if (!wait_all(&in_full[s], (n >> 1) & 1)) return 0;
-      if (!wait_all(&s_empty[s], ((n >> 1) & 1) ^ 1u)) return 0;
+      const int q = n % QST;
+      if (!wait_all(&in_full[q], (n / QST) & 1)) return 0;
       tc_fence_after();
-      issue_nt(tmem_base + T_S + s * BQB, sk, smem_u32(smem + B_SQ + 2 * s * QT_BYTES), &s_full[s]);
+      issue_nt(tmem_base + T_S + (n & 1) * BQB, sk, smem_u32(smem + B_SQ + 2 * q * QT_BYTES), &s_full[n & 1]);
       return 1;
     };
-    auto issue_dp = [&](int n) -> int {
+    auto issue_dp = [&](int n) -> int {  // dO_n is in place once S^T_n was issued
       if (!wait_all(&dp_empty, (n & 1) ^ 1u)) return 0;
       tc_fence_after();
-      issue_nt(tmem_base + T_DP, sv, smem_u32(smem + B_SDO + 2 * (n & 1) * QT_BYTES), &dp_full);
+      issue_nt(tmem_base + T_DP, sv, smem_u32(smem + B_SDO + 2 * (n % QST) * QT_BYTES), &dp_full);
       return 1;
     };
+    int ok = wait_all(&kv_full, 0);
     if (ok) ok = issue_s(0);
     if (ok) ok = issue_dp(0);
     for (int n = 0; ok && n < nsteps; ++n) {
-      const int s = n & 1;
-      if (n + 1 < nsteps && !(ok = issue_s(n + 1))) break;
-      const uint32_t sq = smem_u32(smem + B_SQ + 2 * s * QT_BYTES), sdo = smem_u32(smem + B_SDO + 2 * s * QT_BYTES);
-      // dV += P^T dO_n
-      if (!(ok = wait_all(&p_full, n & 1))) break;
+      const int s = n & 1, q = n % QST;
+      const bool next = n + 1 < nsteps;
+      if (next && !(ok = issue_s(n + 1))) break;
+      const uint32_t sq = smem_u32(smem + B_SQ + 2 * q * QT_BYTES), sdo = smem_u32(smem + B_SDO + 2 * q * QT_BYTES);
+      const uint32_t sds = smem_u32(smem + B_SDS + s * KT_BYTES);
+      // dV += P^T dO_n, P^T from tensor memory (bf16 pairs, 8 columns per K = 16)
+      if (!(ok = wait_all(&p_full[s], (n >> 1) & 1))) break;
       tc_fence_after();
-      if (elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_f16(tmem_base + T_DV, sw128_desc(sp + kk * 32, 16, 1024), sw128_desc(sdo + kk * 2048, QT_BYTES, 1024),
-                     IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tmem_base + T_DV, tmem_base + T_S + s * BQB + kk * 8,
+                        sw128_desc(sdo + kk * 2048, QT_BYTES, 1024), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
       }
       __syncwarp();
+      if (next && !(ok = issue_dp(n + 1))) break;
       // dK += dS^T Q_n ; dQ^T_n = K^T dS^T
-      if (!(ok = wait_all(&ds_full, n & 1))) break;
+      if (!(ok = wait_all(&ds_full[s], (n >> 1) & 1))) break;
       if (!(ok = wait_all(&dq_empty, (n & 1) ^ 1u))) break;
       tc_fence_after();
-      if (elect_one()) {
+      if (leader) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_f16(tmem_base + T_DK, sw128_desc(sds + kk * 32, 16, 1024), sw128_desc(sq + kk * 2048, QT_BYTES, 1024),
@@ -614,104 +628,72 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           tc_mma_f16(tmem_base + T_DQ, sw128_desc(sk + kk * 2048, KT_BYTES, 1024),
                      sw128_desc(sds + kk * 2048, KT_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
         tc_commit(&dq_full);
-        tc_commit(&pds_empty);
-        tc_commit(&in_empty[s]);
-        if (n + 1 == nsteps) tc_commit(&acc_full);
+        tc_commit(&ds_empty[s]);
+        tc_commit(&in_empty[q]);
+        if (!next) tc_commit(&acc_full);
       }
       __syncwarp();
-      if (n + 1 < nsteps && !(ok = issue_dp(n + 1))) break;
     }
-    if (elect_one()) tc_commit(&drain_bar);
+    if (leader) tc_commit(&drain_bar);
     __syncwarp();
     int no_abort = 0;
     mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
-  } else {
+  } else if (warp < 6) {
     // ------------------------------------------------------------ row warps
     const int q = warp & 3;
-    const int r = q * 32 + lane;  // key row (P^T, dS^T, dK, dV) or head-dim row (dQ^T)
+    const int r = q * 32 + lane;  // key row of P^T, dS^T, dK, dV
     const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
-    uint8_t* stg = smem + B_SDQ + q * (BQB * 32 * 4);
     const int key = j * BKB + r;
     int ok = 1;
-    auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
-      return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
-    };
-    auto arrive = [&](uint64_t* bar) {
-      __syncwarp();
-      if (lane == 0) mbar_arrive(bar);
-    };
-    // dQ^T of step m: this thread's head-dim row, 64 queries, into the warp's
-    // [64 x 32] staging tile, then one reduce-add into the f32 accumulator.
-    auto dq_epilogue = [&](int m) -> int {
-      if (!wait_all(&dq_full, m & 1)) return 0;
-      tc_fence_after();
-      uint32_t v[2][32];
-      tmem_ld_32x32b_x32(tl + T_DQ, v[0]);
-      tmem_ld_32x32b_x32(tl + T_DQ + 32, v[1]);
-      tmem_ld_wait();
-      tc_fence_before();
-      arrive(&dq_empty);
-      if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging tile
-      __syncwarp();
-      float* st = reinterpret_cast<float*>(stg);
-#pragma unroll
-      for (int c = 0; c < 64; ++c) st[c * 32 + lane] = __uint_as_float(v[c >> 5][c & 31]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        const int h = g * p.hpg + m / per_head, i = i0 + m % per_head;
-        tma_reduce_add_2d(&map_dq, stg, h * FD + q * 32, b * p.S + i * BQB);
-        bulk_commit_group();
-      }
-      return 1;
-    };
     for (int n = 0; n < nsteps; ++n) {
-      const int s = n & 1;
-      const int i = i0 + n % per_head;
-      if (!(ok = wait_all(&in_full[s], (n >> 1) & 1))) break;
-      if (!(ok = wait_all(&s_full[s], (n >> 1) & 1))) break;
+      const int s = n & 1, q3 = n % QST;
+      const uint32_t par = (uint32_t)((n >> 1) & 1);
+      const int i = step_i(n);
+      if (!(ok = wait_all(&in_full[q3], (n / QST) & 1))) break;
+      if (!(ok = wait_all(&s_full[s], par))) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(smem + B_SLD + s * 512);
+      const float* lse2 = reinterpret_cast<const float*>(smem + B_SLD + q3 * 512);
       const float* dsum = lse2 + 64;
       float pr[64];
       {
-        uint32_t v[2][32];
-        tmem_ld_32x32b_x32(tl + T_S + s * BQB, v[0]);
-        tmem_ld_32x32b_x32(tl + T_S + s * BQB + 32, v[1]);
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(tl + T_S + s * BQB, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld_32x32b_x32(tl + T_S + s * BQB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         tmem_ld_wait();
-        tc_fence_before();
-        arrive(&s_empty[s]);
-        const bool diag = i < i0 + 2;
 #pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float e = exp2f(fmaf(__uint_as_float(v[c >> 5][c & 31]), p.scale_log2, -lse2[c]));
-          pr[c] = (diag && i * BQB + c < key) ? 0.0f : e;
+        for (int c = 0; c < 64; ++c) pr[c] = exp2f(fmaf(__uint_as_float(v[c]), p.scale_log2, -lse2[c]));
+        if (i < i0 + 2) {  // the two query blocks that cross the diagonal
+#pragma unroll
+          for (int c = 0; c < 64; ++c)
+            if (i * BQB + c < key) pr[c] = 0.0f;
         }
+        // P^T row (bf16 pairs) over the first 32 columns of the scores
+#pragma unroll
+        for (int c = 0; c < 64; c += 2) v[c >> 1] = pack_bf16x2(pr[c], pr[c + 1]);
+        tmem_st_32x32b_x32(tl + T_S + s * BQB, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_st_wait();
       }
-      // P^T row, once the previous step's products have read P^T and dS^T
-      if (!(ok = wait_all(&pds_empty, (n & 1) ^ 1u))) break;
-      write_sw128_row(smem + B_SP, r, pr);
-      fence_proxy_async_smem();
-      arrive(&p_full);
-      if (n >= 1 && !(ok = dq_epilogue(n - 1))) break;
+      tc_fence_before();
+      arrive(&p_full[s]);
       if (!(ok = wait_all(&dp_full, n & 1))) break;
       tc_fence_after();
       {
-        uint32_t v[2][32];
-        tmem_ld_32x32b_x32(tl + T_DP, v[0]);
-        tmem_ld_32x32b_x32(tl + T_DP + 32, v[1]);
+        uint32_t v[64];
+        tmem_ld_32x32b_x32(tl + T_DP, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tmem_ld_32x32b_x32(tl + T_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         tmem_ld_wait();
         tc_fence_before();
         arrive(&dp_empty);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pr[c] = pr[c] * (__uint_as_float(v[c >> 5][c & 31]) - dsum[c]) * p.scale;
+        for (int c = 0; c < 64; ++c) pr[c] = pr[c] * (__uint_as_float(v[c]) - dsum[c]) * p.scale;
       }
-      write_sw128_row(smem + B_SDS, r, pr);
+      // dS^T row into this step's slot, once step n - 2's products have read it
+      if (!(ok = wait_all(&ds_empty[s], par ^ 1u))) break;
+      write_sw128_row(smem + B_SDS + s * KT_BYTES, r, pr);
       fence_proxy_async_smem();
-      arrive(&ds_full);
-      arrive(&in_empty[s]);
+      arrive(&ds_full[s]);
+      arrive(&in_empty[q3]);
     }
-    if (ok) ok = dq_epilogue(nsteps - 1);
     if (ok && (ok = wait_all(&acc_full, 0))) {
       tc_fence_after();
       // dK_j and dV_j rows (bf16) into the group's K and V columns of dqkv
@@ -723,15 +705,41 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         __nv_bfloat16* dst = half ? dk : dv;
 #pragma unroll 1
         for (int c = 0; c < 2; ++c) {
-          uint32_t v[2][32];
-          tmem_ld_32x32b_x32(tl + col + 64 * c, v[0]);
-          tmem_ld_32x32b_x32(tl + col + 64 * c + 32, v[1]);
+          uint32_t v[64];
+          tmem_ld_32x32b_x32(tl + col + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tmem_ld_32x32b_x32(tl + col + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
           tmem_ld_wait();
           float f[64];
 #pragma unroll
-          for (int e = 0; e < 64; ++e) f[e] = __uint_as_float(v[e >> 5][e & 31]);
+          for (int e = 0; e < 64; ++e) f[e] = __uint_as_float(v[e]);
           store_row_bf16(dst + 64 * c, f);
         }
+      }
+    }
+  } else {
+    // --------------------------------------------------------- dQ epilogue
+    const int q = warp & 3;  // this warp's head-dim rows [32 q, 32 q + 32) of dQ^T
+    const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
+    uint8_t* stg = smem + B_SDQ + q * (BQB * 32 * 4);
+    float* st = reinterpret_cast<float*>(stg);
+    for (int m = 0; m < nsteps; ++m) {
+      if (!wait_all(&dq_full, m & 1)) break;
+      tc_fence_after();
+      uint32_t v[64];
+      tmem_ld_32x32b_x32(tl + T_DQ, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(tl + T_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_wait();
+      tc_fence_before();
+      arrive(&dq_empty);
+      if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging tile
+      __syncwarp();
+#pragma unroll
+      for (int c = 0; c < 64; ++c) st[c * 32 + lane] = __uint_as_float(v[c]);
+      fence_proxy_async_smem();
+      __syncwarp();
+      if (lane == 0) {
+        tma_reduce_add_2d(&map_dq, stg, step_h(m) * FD + q * 32, b * p.S + step_i(m) * BQB);
+        bulk_commit_group();
       }
     }
     if (lane == 0) bulk_wait_all();
