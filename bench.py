@@ -8,7 +8,8 @@ shards), through the library's public API.
 Prints one JSON line (rank 0).  ``value`` is whole-job GEMM TFLOP/s
 (18 N H F algorithmic flops per step) with every input resident in HBM; the
 ``e2e`` figure adds the per-step host->device copy of x and the target from
-pinned memory and the device->host read of the loss.  With N > 1 (torchrun)
+pinned memory (on a copy stream, double-buffered so that the next step's copy
+overlaps the current step) and the device->host read of the loss.  With N > 1 (torchrun)
 every rank runs an independent replica of the step on its own GPU (the path
 has no data exchange between replicas), so scaling is weak.
 
@@ -186,6 +187,46 @@ class ClockSampler:
                 "reasons": sorted(reasons), "samples": len(rows)}
 
 
+def timed_e2e(torch, run_step, stream, x_host, tg_host, xbufs, tbufs, loss, loss_host, steps: int) -> float:
+    """Milliseconds for `steps` training steps fed from pinned host memory.
+
+    Every step copies its x and target host->device and reads its loss back device->host. The
+    copies run on a second stream into two device buffers, so the copy for step i+1 overlaps the
+    compute of step i (as a training loop with a prefetching loader does). A buffer is refilled only
+    after the step that used it has finished, since the backward reads x again. The timer starts
+    before the first copy and stops after the last step's loss has been read.
+    """
+    copy = torch.cuda.Stream(device=stream.device)
+    ready = [torch.cuda.Event() for _ in range(2)]
+    free = [torch.cuda.Event() for _ in range(2)]
+    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    f0.record(stream)
+    copy.wait_event(f0)
+
+    def fill(i):
+        b = i % 2
+        if i >= 2:
+            copy.wait_event(free[b])
+        with torch.cuda.stream(copy):
+            xbufs[b].copy_(x_host, non_blocking=True)
+            tbufs[b].copy_(tg_host, non_blocking=True)
+        ready[b].record(copy)
+
+    fill(0)
+    for i in range(steps):
+        if i + 1 < steps:
+            fill(i + 1)
+        b = i % 2
+        stream.wait_event(ready[b])
+        with torch.cuda.stream(stream):
+            run_step(xbufs[b], tbufs[b])
+            loss_host.copy_(loss, non_blocking=True)
+        free[b].record(stream)
+    f1.record(stream)
+    torch.cuda.synchronize()
+    return f0.elapsed_time(f1)
+
+
 def cpu_oracle_tflops(cfg, inp, budget_s: float, min_tokens: int = 16, max_tokens: int = 4096):
     """Time the oracle's dense step on a token sample sized to about budget_s."""
     from oracle import tpmlp_oracle as O
@@ -305,9 +346,9 @@ def ours_attn(args):
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
     stream = m.stream
 
-    def step():
-        m.forward(x, p["norm_w"], p["w_qkv"], p["w_o"], p["b_o"], cfg.eps, t, cfg.batch, cfg.seq, y=y)
-        tpmlp_mse_loss_grad_noalloc(y, target, dy, loss, stream=stream.cuda_stream)
+    def step(xb=x, tb=target):
+        m.forward(xb, p["norm_w"], p["w_qkv"], p["w_o"], p["b_o"], cfg.eps, t, cfg.batch, cfg.seq, y=y)
+        tpmlp_mse_loss_grad_noalloc(y, tb, dy, loss, stream=stream.cuda_stream)
         m.backward(dy, dx=dx, grads=grads)
         m.sgd_step(cfg.lr)
 
@@ -348,18 +389,9 @@ def ours_attn(args):
     value = flops * args.steps * world / (ms / 1e3) / 1e12
     barrier()
     torch.cuda.synchronize()
-    f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, args.steps // 2)
-    f0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            x.copy_(x_host, non_blocking=True)
-            target.copy_(tg_host, non_blocking=True)
-            step()
-            loss_host.copy_(loss, non_blocking=True)
-    f1.record(stream)
-    torch.cuda.synchronize()
-    ems = f0.elapsed_time(f1)
+    ems = timed_e2e(torch, step, stream, x_host, tg_host, (x, torch.empty_like(x)),
+                    (target, torch.empty_like(target)), loss, loss_host, e2e_steps)
     m.sync()
     if rank != 0:
         if world > 1:
@@ -412,7 +444,8 @@ def ours_attn(args):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][0])},
         "roofline": roof, "cpu_baseline": None,
         "e2e": {"value": flops * e2e_steps * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
-                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 4, "steps": e2e_steps},
+                "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 4, "steps": e2e_steps,
+                "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)"},
         "clocks": clk, "gpu_launches": launches, "loss": float(loss_host.item()),
     }
     print(json.dumps(line), flush=True)
@@ -473,10 +506,10 @@ def ours(args):
         m.new_adam_state()
     nstep = [0]
 
-    def step():
-        m.forward(x, params["norm_w"], params["w_gate_up"], params["w_down"], params["b_down"], cfg.eps, t, y=y,
+    def step(xb=x, tb=target):
+        m.forward(xb, params["norm_w"], params["w_gate_up"], params["w_down"], params["b_down"], cfg.eps, t, y=y,
                   b_1=params.get("b_1"))
-        m.mse_loss_grad(y, target, dy=dy, loss=loss)
+        m.mse_loss_grad(y, tb, dy=dy, loss=loss)
         m.backward(dy, dx=dx, grads=grads)
         if adamw:
             nstep[0] += 1
@@ -528,20 +561,10 @@ def ours(args):
     # ---------------------------------------------------------- end-to-end through the public API
     barrier()
     torch.cuda.synchronize()
-    f0 = torch.cuda.Event(enable_timing=True)
-    f1 = torch.cuda.Event(enable_timing=True)
     e2e_steps = max(3, args.steps // 2)
-    f0.record(stream)
-    with torch.cuda.stream(stream):
-        for _ in range(e2e_steps):
-            x.copy_(x_host, non_blocking=True)
-            target.copy_(tg_host, non_blocking=True)
-            step()
-            loss_host.copy_(loss, non_blocking=True)
-    f1.record(stream)
-    torch.cuda.synchronize()
+    ems = timed_e2e(torch, step, stream, x_host, tg_host, (x, torch.empty_like(x)),
+                    (target, torch.empty_like(target)), loss, loss_host, e2e_steps)
     barrier()
-    ems = f0.elapsed_time(f1)
     if world > 1:
         tt = torch.tensor([ems], device=dev)
         torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
@@ -603,7 +626,8 @@ def ours(args):
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * N * H * e,
-                "d2h_bytes_per_step": 4, "steps": e2e_steps},
+                "d2h_bytes_per_step": 4, "steps": e2e_steps,
+                "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)"},
         "clocks": clk,
         "gpu_launches": launches,
         "loss": float(loss_host.item()),

@@ -86,6 +86,48 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
   return *reinterpret_cast<uint32_t*>(&h);
 }
 
+// 2^x as one multi-function-unit instruction (relative error about 2^-22,
+// far below the bf16 rounding that P and dS get); -inf gives 0 and results
+// below the normal range flush to 0, which is what a masked or negligible
+// probability needs.
+__device__ __forceinline__ float ex2_fast(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// max(a, b, c) in one instruction
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
+// Two-lane f32 arithmetic: one instruction for a pair of values.
+__device__ __forceinline__ uint64_t f2_pack(float lo, float hi) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ void f2_unpack(uint64_t r, float& lo, float& hi) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(r));
+}
+__device__ __forceinline__ uint64_t f2_fma(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_add(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t f2_mul(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
 __global__ void __launch_bounds__(FTHREADS, 1)
     flash_fwd_kernel(const __grid_constant__ CUtensorMap map_qkv, const __grid_constant__ CUtensorMap map_z,
                      const FaParams p) {
@@ -277,27 +319,47 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         for (int c = 0; c < 128; ++c)
           if (c > r) v[c] = __float_as_uint(-INFINITY);
       }
-      float mb = __uint_as_float(v[0]);
+      // row maximum over eight independent chains (column c in chain c % 8)
+      float mx[8];
 #pragma unroll
-      for (int c = 1; c < 128; ++c) mb = fmaxf(mb, __uint_as_float(v[c]));
+      for (int k = 0; k < 8; ++k) {
+        float m = __uint_as_float(v[k]);
+#pragma unroll
+        for (int i = 1; i < 15; i += 2) m = fmax3(m, __uint_as_float(v[k + 8 * i]), __uint_as_float(v[k + 8 * i + 8]));
+        mx[k] = fmaxf(m, __uint_as_float(v[k + 120]));
+      }
+      float mb = fmaxf(fmax3(mx[0], mx[1], mx[2]), fmax3(fmax3(mx[3], mx[4], mx[5]), mx[6], mx[7]));
       mb *= p.scale_log2;
       const bool move = __any_sync(0xffffffffu, mb > m_run + RESCALE_LOG2);
       float alpha = 1.0f;
       if (move) {
         const float m_new = fmaxf(m_run, mb);
-        alpha = exp2f(m_run - m_new);  // 0 on the first block
+        alpha = ex2_fast(m_run - m_new);  // 0 on the first block
         l *= alpha;
         m_run = m_new;
       }
-      float ps = 0.0f;
+      // P = 2^(s scale - m) a column pair at a time; the row sum in four
+      // independent pair accumulators
+      const uint64_t sc2 = f2_pack(p.scale_log2, p.scale_log2), nm2 = f2_pack(-m_run, -m_run);
+      uint64_t ps2[4];
+#pragma unroll
+      for (int k = 0; k < 4; ++k) ps2[k] = f2_pack(0.0f, 0.0f);
 #pragma unroll
       for (int c = 0; c < 128; c += 2) {
-        const float p0 = exp2f(fmaf(__uint_as_float(v[c]), p.scale_log2, -m_run));
-        const float p1 = exp2f(fmaf(__uint_as_float(v[c + 1]), p.scale_log2, -m_run));
-        ps += p0 + p1;
+        float a0, a1;
+        f2_unpack(f2_fma(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])), sc2, nm2), a0, a1);
+        const float p0 = ex2_fast(a0), p1 = ex2_fast(a1);
+        ps2[(c >> 1) & 3] = f2_add(ps2[(c >> 1) & 3], f2_pack(p0, p1));
         v[c >> 1] = pack_bf16x2(p0, p1);
       }
-      l += ps;
+      {
+        float s0, s1, s2, s3, s4, s5, s6, s7;
+        f2_unpack(ps2[0], s0, s1);
+        f2_unpack(ps2[1], s2, s3);
+        f2_unpack(ps2[2], s4, s5);
+        f2_unpack(ps2[3], s6, s7);
+        l += ((s0 + s1) + (s2 + s3)) + ((s4 + s5) + (s6 + s7));
+      }
       tmem_st_32x32b_x32(t_s, *reinterpret_cast<uint32_t(*)[32]>(v));
       tmem_st_32x32b_x32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       if (move && j > 0) {
@@ -661,7 +723,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         tmem_ld_32x32b_x32(tl + T_S + s * BQB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         tmem_ld_wait();
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pr[c] = exp2f(fmaf(__uint_as_float(v[c]), p.scale_log2, -lse2[c]));
+        for (int c = 0; c < 64; ++c) pr[c] = ex2_fast(fmaf(__uint_as_float(v[c]), p.scale_log2, -lse2[c]));
         if (i < i0 + 2) {  // the two query blocks that cross the diagonal
 #pragma unroll
           for (int c = 0; c < 64; ++c)
