@@ -192,13 +192,15 @@ def timed_e2e(torch, run_step, stream, x_host, tg_host, xbufs, tbufs, loss, loss
 
     Every step copies its x and target host->device and reads its loss back device->host. The
     copies run on a second stream into two device buffers, so the copy for step i+1 overlaps the
-    compute of step i (as a training loop with a prefetching loader does). A buffer is refilled only
-    after the step that used it has finished, since the backward reads x again. The timer starts
-    before the first copy and stops after the last step's loss has been read.
+    compute of step i (as a training loop with a prefetching loader does); the compute stream
+    itself carries no copy. A buffer is refilled only after the step that used it has finished,
+    since the backward reads x again. The timer starts before the first copy and stops once the
+    last step has finished and its loss has been read.
     """
     copy = torch.cuda.Stream(device=stream.device)
     ready = [torch.cuda.Event() for _ in range(2)]
     free = [torch.cuda.Event() for _ in range(2)]
+    done = torch.cuda.Event()
     f0, f1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     f0.record(stream)
     copy.wait_event(f0)
@@ -213,15 +215,24 @@ def timed_e2e(torch, run_step, stream, x_host, tg_host, xbufs, tbufs, loss, loss
         ready[b].record(copy)
 
     fill(0)
+    if steps > 1:
+        fill(1)
     for i in range(steps):
-        if i + 1 < steps:
-            fill(i + 1)
         b = i % 2
         stream.wait_event(ready[b])
+        if i > 0:
+            stream.wait_event(done)  # the previous step's loss has been read before it is overwritten
         with torch.cuda.stream(stream):
             run_step(xbufs[b], tbufs[b])
-            loss_host.copy_(loss, non_blocking=True)
         free[b].record(stream)
+        # the loss read, then the next-but-one step's inputs, queue on the copy stream behind it
+        copy.wait_event(free[b])
+        with torch.cuda.stream(copy):
+            loss_host.copy_(loss, non_blocking=True)
+        done.record(copy)
+        if i + 2 < steps:
+            fill(i + 2)
+    stream.wait_event(done)
     f1.record(stream)
     torch.cuda.synchronize()
     return f0.elapsed_time(f1)

@@ -434,28 +434,33 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 //   dS^T = P^T o (dP^T - D_i) / sqrt(d)
 //   dV_j += P^T dO_i               dK_j += dS^T Q_i      dQ_i^T = K_j^T dS^T
 //
-//   warp 0     : TMA producer -- K_j, V_j once; Q_i, dO_i, lse2_i, D_i per
-//                step into a three-stage ring.  Steps run over the query
-//                blocks from the last one down, the heads of the group inner,
-//                so the CTAs of one (sequence, group) read the same Q / dO
-//                blocks at about the same time.
-//   warp 1     : tensor memory owner and MMA issuer; per step n it issues
-//                S^T_{n+1}, dV_n, dP^T_{n+1}, dK_n, dQ^T_n, so the next
-//                step's scores and their gradient are ready before the row
-//                warps reach them.
-//   warps 2..5 : one key row per thread: P^T (bf16, written over its scores
-//                in tensor memory, where the dV product reads it) and dS^T
-//                (bf16, into a double-buffered shared-memory tile in the
-//                K-major layout the MMAs read), and at the end the dK / dV
-//                rows.
-//   warps 6..9 : dQ^T epilogue, one head-dim row per thread: tensor memory to
-//                a shared staging tile, then one reduce-add per warp.
+//   warp 0      : TMA producer -- K_j, V_j once; Q_i, dO_i, lse2_i, D_i per
+//                 step into a three-stage ring.  Steps run over the query
+//                 blocks from the last one down, the heads of the group
+//                 inner, so the CTAs of one (sequence, group) read the same
+//                 Q / dO blocks at about the same time.
+//   warp 1      : tensor memory owner and MMA issuer.
+//   warps 2..5  : row group 0, the even steps; warps 6..9: row group 1, the
+//                 odd steps.  One key row per thread: P^T (bf16, written
+//                 over its scores in tensor memory, where the dV product
+//                 reads it) and dS^T (bf16, into the group's shared-memory
+//                 tile in the K-major layout the MMAs read); at the end
+//                 group 0 writes the dV rows and group 1 the dK rows.
+//   warps 10..13: dQ^T epilogue, one head-dim row per thread: tensor memory
+//                 to registers, then reductions into the f32 dQ accumulator.
+// Every step-indexed buffer has two slots, step n using slot n & 1, so the
+// two row groups work on consecutive steps at the same time and one group's
+// element-wise work runs under the products of the other group's step:
+// tensor memory holds S^T / P^T per slot, dP^T per slot (overwritten by the
+// step's dQ^T once the group has read dP^T), dV_j and dK_j.  Per step n the
+// MMA warp issues dV_n, dP^T_{n+1}, dK_n and dQ^T_n, then S^T_{n+2}.
 // The same shared-memory tile of Q, dO, K or dS^T serves as a K-major operand
 // of one product and an MN-major operand of another: a 128-byte swizzled tile
 // of 64-element rows is both.
 constexpr int BKB = 128;  // keys per CTA
 constexpr int BQB = 64;   // queries per step
-constexpr int BTHREADS = 320;
+constexpr int BTHREADS = 448;
+constexpr int GROUP_WARPS = 4;  // warps per row group: one per TMEM lane quarter
 constexpr uint32_t KT_BYTES = BKB * 64 * 2;   // [128 keys x 64 d] tile, 16 KB
 constexpr uint32_t QT_BYTES = BQB * 64 * 2;   // [64 queries x 64 d] tile, 8 KB
 // shared memory
@@ -464,16 +469,14 @@ constexpr uint32_t B_SV = B_SK + 2 * KT_BYTES;        // V_j
 constexpr int QST = 3;                                // Q / dO / lse2 / D ring stages
 constexpr uint32_t B_SQ = B_SV + 2 * KT_BYTES;        // Q_i ring: QST stages x two 8 KB tiles
 constexpr uint32_t B_SDO = B_SQ + 2 * QST * QT_BYTES; // dO_i ring
-constexpr uint32_t B_SDS = B_SDO + 2 * QST * QT_BYTES; // dS^T ring: 2 x [128 keys x 64 queries], 16 KB each
-constexpr uint32_t B_SDQ = B_SDS + 2 * KT_BYTES;      // dQ^T staging: 4 warps x [64 q x 32 d] f32
-constexpr uint32_t B_SLD = B_SDQ + 4 * BQB * 32 * 4;  // lse2 / D ring: QST stages x 2 x 64 floats
+constexpr uint32_t B_SDS = B_SDO + 2 * QST * QT_BYTES; // dS^T: 2 slots x [128 keys x 64 queries], 16 KB each
+constexpr uint32_t B_SLD = B_SDS + 2 * KT_BYTES;      // lse2 / D ring: QST stages x 2 x 64 floats
 constexpr uint32_t BSMEM = B_SLD + QST * 2 * BQB * 4 + 1024;
 static_assert(BSMEM <= 232448 - 256, "shared memory budget");
 constexpr uint32_t IN_TX = 4 * QT_BYTES + 2 * BQB * 4;
 // tensor memory columns
-constexpr uint32_t T_S = 0;     // S^T ring: 2 x 64 (P^T over the first 32 columns of its slot)
-constexpr uint32_t T_DP = 128;  // dP^T: 64
-constexpr uint32_t T_DQ = 192;  // dQ^T: 64
+constexpr uint32_t T_S = 0;     // S^T: 2 slots x 64 (P^T over the first 32 columns of its slot)
+constexpr uint32_t T_PQ = 128;  // dP^T, then dQ^T: 2 slots x 64
 constexpr uint32_t T_DV = 256;  // dV_j: 128
 constexpr uint32_t T_DK = 384;  // dK_j: 128
 
@@ -486,43 +489,22 @@ struct FbParams {
   const float* dsum;  // D, same layout
   __nv_bfloat16* dqkv;
   int64_t ld_dqkv;
+  float* dq_acc;  // [batch S, nq d] f32 dQ accumulator
+  int64_t ld_dq;
   uint32_t* status;
 };
 
-__device__ __forceinline__ void store_row_bf16(__nv_bfloat16* dst, const float* v) {
-#pragma unroll
-  for (int c = 0; c < 8; ++c) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * c], v[8 * c + 1]);
-    w.y = pack_bf16x2(v[8 * c + 2], v[8 * c + 3]);
-    w.z = pack_bf16x2(v[8 * c + 4], v[8 * c + 5]);
-    w.w = pack_bf16x2(v[8 * c + 6], v[8 * c + 7]);
-    reinterpret_cast<uint4*>(dst)[c] = w;
-  }
-}
-
-// A 128-byte swizzled K-major row of 64 bf16 values (row r of a 1024-byte
-// aligned tile).
-__device__ __forceinline__ void write_sw128_row(uint8_t* tile, int r, const float* v) {
-  uint8_t* rowp = tile + r * 128;
-#pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    uint4 w;
-    w.x = pack_bf16x2(v[8 * k], v[8 * k + 1]);
-    w.y = pack_bf16x2(v[8 * k + 2], v[8 * k + 3]);
-    w.z = pack_bf16x2(v[8 * k + 4], v[8 * k + 5]);
-    w.w = pack_bf16x2(v[8 * k + 6], v[8 * k + 7]);
-    *reinterpret_cast<uint4*>(rowp + ((k ^ (r & 7)) << 4)) = w;
-  }
+// *addr += v in global memory, no value returned
+__device__ __forceinline__ void red_add_f32(float* addr, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(addr), "f"(v) : "memory");
 }
 
 __global__ void __launch_bounds__(BTHREADS, 1)
     flash_bwd_kernel(const __grid_constant__ CUtensorMap map_kv, const __grid_constant__ CUtensorMap map_q,
-                     const __grid_constant__ CUtensorMap map_do, const __grid_constant__ CUtensorMap map_dq,
-                     const FbParams p, int batch) {
+                     const __grid_constant__ CUtensorMap map_do, const FbParams p, int batch) {
   extern __shared__ uint8_t smem_raw[];
-  __shared__ __align__(8) uint64_t kv_full, in_full[QST], in_empty[QST], s_full[2], dp_full, dp_empty, p_full[2],
-      ds_full[2], ds_empty[2], dq_full, dq_empty, acc_full, drain_bar;
+  __shared__ __align__(8) uint64_t kv_full, in_full[QST], in_empty[QST], s_full[2], p_full[2], dp_full[2],
+      ds_full[2], ds_empty[2], dq_full[2], dq_empty[2], acc_full, drain_bar;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -545,18 +527,18 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     mbar_init(&kv_full, 1);
     for (int i = 0; i < QST; ++i) {
       mbar_init(&in_full[i], 1);
-      mbar_init(&in_empty[i], 1 + 4);  // the MMA commit and the four row warps (lse2 / D reads)
+      mbar_init(&in_empty[i], 1 + GROUP_WARPS);  // the MMA commit and the step's row group (lse2 / D reads)
     }
+
     for (int i = 0; i < 2; ++i) {
       mbar_init(&s_full[i], 1);
-      mbar_init(&p_full[i], 4);
-      mbar_init(&ds_full[i], 4);
+      mbar_init(&p_full[i], GROUP_WARPS);
+      mbar_init(&dp_full[i], 1);
+      mbar_init(&ds_full[i], GROUP_WARPS);
       mbar_init(&ds_empty[i], 1);
+      mbar_init(&dq_full[i], 1);
+      mbar_init(&dq_empty[i], 4);
     }
-    mbar_init(&dp_full, 1);
-    mbar_init(&dp_empty, 4);
-    mbar_init(&dq_full, 1);
-    mbar_init(&dq_empty, 4);
     mbar_init(&acc_full, 1);
     mbar_init(&drain_bar, 1);
     abort_sh = 0;
@@ -566,7 +548,6 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     tma_prefetch_desc(&map_kv);
     tma_prefetch_desc(&map_q);
     tma_prefetch_desc(&map_do);
-    tma_prefetch_desc(&map_dq);
   }
   if (warp == 1) {
     tmem_alloc(&tmem_base_sh, FCOLS);
@@ -628,7 +609,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     constexpr uint32_t IDESC_DQ = idesc_bf16_f32(FD, BQB, true, true);     // dQ^T
     const bool leader = elect_one();  // the lane that issues every MMA and commit
     const uint32_t sk = smem_u32(smem + B_SK), sv = smem_u32(smem + B_SV);
-    // S^T_n = K Q_n^T (ring slot n & 1) or dP^T_n = V dO_n^T, then a commit to `done`
+    // S^T_n = K Q_n^T or dP^T_n = V dO_n^T, then a commit to `done`
     auto issue_nt = [&](uint32_t d_tmem, uint32_t a, uint32_t bq, uint64_t* done) {
       if (leader) {
 #pragma unroll
@@ -641,8 +622,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       }
       __syncwarp();
     };
-    // S^T_n goes into slot n & 1, where P^T_{n-2} was read by dV_{n-2}:
-    // issued before it, in order
+    // S^T_n into slot n & 1, where P^T_{n-2} was read by dV_{n-2}: issued before it, in order
     auto issue_s = [&](int n) -> int {
       const int q = n % QST;
       if (!wait_all(&in_full[q], (n / QST) & 1)) return 0;
@@ -650,23 +630,26 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       issue_nt(tmem_base + T_S + (n & 1) * BQB, sk, smem_u32(smem + B_SQ + 2 * q * QT_BYTES), &s_full[n & 1]);
       return 1;
     };
-    auto issue_dp = [&](int n) -> int {  // dO_n is in place once S^T_n was issued
-      if (!wait_all(&dp_empty, (n & 1) ^ 1u)) return 0;
+    // dP^T_n into slot n & 1 once dQ^T_{n-2} has been read out of it; dO_n is
+    // in place since S^T_n was issued
+    auto issue_dp = [&](int n) -> int {
+      if (!wait_all(&dq_empty[n & 1], ((n >> 1) & 1) ^ 1u)) return 0;
       tc_fence_after();
-      issue_nt(tmem_base + T_DP, sv, smem_u32(smem + B_SDO + 2 * (n % QST) * QT_BYTES), &dp_full);
+      issue_nt(tmem_base + T_PQ + (n & 1) * BQB, sv, smem_u32(smem + B_SDO + 2 * (n % QST) * QT_BYTES),
+               &dp_full[n & 1]);
       return 1;
     };
     int ok = wait_all(&kv_full, 0);
     if (ok) ok = issue_s(0);
+    if (ok && nsteps > 1) ok = issue_s(1);
     if (ok) ok = issue_dp(0);
     for (int n = 0; ok && n < nsteps; ++n) {
       const int s = n & 1, q = n % QST;
-      const bool next = n + 1 < nsteps;
-      if (next && !(ok = issue_s(n + 1))) break;
+      const uint32_t par = (uint32_t)((n >> 1) & 1);
       const uint32_t sq = smem_u32(smem + B_SQ + 2 * q * QT_BYTES), sdo = smem_u32(smem + B_SDO + 2 * q * QT_BYTES);
       const uint32_t sds = smem_u32(smem + B_SDS + s * KT_BYTES);
       // dV += P^T dO_n, P^T from tensor memory (bf16 pairs, 8 columns per K = 16)
-      if (!(ok = wait_all(&p_full[s], (n >> 1) & 1))) break;
+      if (!(ok = wait_all(&p_full[s], par))) break;
       tc_fence_after();
       if (leader) {
 #pragma unroll
@@ -675,10 +658,9 @@ __global__ void __launch_bounds__(BTHREADS, 1)
                         sw128_desc(sdo + kk * 2048, QT_BYTES, 1024), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
       }
       __syncwarp();
-      if (next && !(ok = issue_dp(n + 1))) break;
-      // dK += dS^T Q_n ; dQ^T_n = K^T dS^T
-      if (!(ok = wait_all(&ds_full[s], (n >> 1) & 1))) break;
-      if (!(ok = wait_all(&dq_empty, (n & 1) ^ 1u))) break;
+      if (n + 1 < nsteps && !(ok = issue_dp(n + 1))) break;
+      // dK += dS^T Q_n ; dQ^T_n = K^T dS^T over the slot's dP^T, which the group has read
+      if (!(ok = wait_all(&ds_full[s], par))) break;
       tc_fence_after();
       if (leader) {
 #pragma unroll
@@ -687,125 +669,144 @@ __global__ void __launch_bounds__(BTHREADS, 1)
                      IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem_base + T_DQ, sw128_desc(sk + kk * 2048, KT_BYTES, 1024),
+          tc_mma_f16(tmem_base + T_PQ + s * BQB, sw128_desc(sk + kk * 2048, KT_BYTES, 1024),
                      sw128_desc(sds + kk * 2048, KT_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
-        tc_commit(&dq_full);
+        tc_commit(&dq_full[s]);
         tc_commit(&ds_empty[s]);
         tc_commit(&in_empty[q]);
-        if (!next) tc_commit(&acc_full);
+        if (n + 1 == nsteps) tc_commit(&acc_full);
       }
       __syncwarp();
+      if (n + 2 < nsteps && !(ok = issue_s(n + 2))) break;
     }
     if (leader) tc_commit(&drain_bar);
     __syncwarp();
     int no_abort = 0;
     mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
-  } else if (warp < 6) {
-    // ------------------------------------------------------------ row warps
+  } else if (warp < 2 + 2 * GROUP_WARPS) {
+    // ------------------------------------------------------------ row groups
+    const int grp = (warp - 2) / GROUP_WARPS;  // steps n with n & 1 == grp, slot grp
     const int q = warp & 3;
     const int r = q * 32 + lane;  // key row of P^T, dS^T, dK, dV
     const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
     const int key = j * BKB + r;
+    const uint32_t t_s = tl + T_S + grp * BQB, t_dp = tl + T_PQ + grp * BQB;
+    uint8_t* rowp = smem + B_SDS + grp * KT_BYTES + r * 128;
     int ok = 1;
-    for (int n = 0; n < nsteps; ++n) {
-      const int s = n & 1, q3 = n % QST;
+    for (int n = grp; n < nsteps; n += 2) {
+      const int q3 = n % QST;
       const uint32_t par = (uint32_t)((n >> 1) & 1);
       const int i = step_i(n);
       if (!(ok = wait_all(&in_full[q3], (n / QST) & 1))) break;
-      if (!(ok = wait_all(&s_full[s], par))) break;
+      if (!(ok = wait_all(&s_full[grp], par))) break;
       tc_fence_after();
       const float* lse2 = reinterpret_cast<const float*>(smem + B_SLD + q3 * 512);
       const float* dsum = lse2 + 64;
-      float pr[64];
       {
-        uint32_t v[64];
-        tmem_ld_32x32b_x32(tl + T_S + s * BQB, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld_32x32b_x32(tl + T_S + s * BQB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld_wait();
+        // P^T row (bf16 pairs) over the first 32 columns of the scores, read
+        // in two 32-column halves; the half written (columns 0..15, then
+        // 16..31) has been read already
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pr[c] = ex2_fast(fmaf(__uint_as_float(v[c]), p.scale_log2, -lse2[c]));
-        if (i < i0 + 2) {  // the two query blocks that cross the diagonal
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t v[32];
+          tmem_ld_32x32b_x32(t_s + 32 * hh, v);
+          tmem_ld_wait();
+          float pr[32];
 #pragma unroll
-          for (int c = 0; c < 64; ++c)
-            if (i * BQB + c < key) pr[c] = 0.0f;
+          for (int c = 0; c < 32; ++c)
+            pr[c] = ex2_fast(fmaf(__uint_as_float(v[c]), p.scale_log2, -lse2[32 * hh + c]));
+          if (i < i0 + 2) {  // the two query blocks that cross the diagonal
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+              if (i * BQB + 32 * hh + c < key) pr[c] = 0.0f;
+          }
+          uint32_t w[16];
+#pragma unroll
+          for (int c = 0; c < 32; c += 2) w[c >> 1] = pack_bf16x2(pr[c], pr[c + 1]);
+          tmem_st_32x32b_x16(t_s + 16 * hh, w);
+          tmem_st_wait();
         }
-        // P^T row (bf16 pairs) over the first 32 columns of the scores
-#pragma unroll
-        for (int c = 0; c < 64; c += 2) v[c >> 1] = pack_bf16x2(pr[c], pr[c + 1]);
-        tmem_st_32x32b_x32(tl + T_S + s * BQB, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_st_wait();
       }
       tc_fence_before();
-      arrive(&p_full[s]);
-      if (!(ok = wait_all(&dp_full, n & 1))) break;
+      arrive(&p_full[grp]);
+      if (!(ok = wait_all(&dp_full[grp], par))) break;
+      // dS^T row into the group's slot, once step n - 2's products have read it
+      if (!(ok = wait_all(&ds_empty[grp], par ^ 1u))) break;
       tc_fence_after();
-      {
-        uint32_t v[64];
-        tmem_ld_32x32b_x32(tl + T_DP, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tmem_ld_32x32b_x32(tl + T_DP + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tmem_ld_wait();
-        tc_fence_before();
-        arrive(&dp_empty);
+      // dS = P (dP - D) / sqrt(d) in four 16-column quarters, with P the
+      // bf16 values the dV product uses, read back from tensor memory; each
+      // quarter is packed straight into its two 16-byte chunks of the
+      // swizzled row
+      const uint64_t sc2 = f2_pack(p.scale, p.scale);
 #pragma unroll
-        for (int c = 0; c < 64; ++c) pr[c] = pr[c] * (__uint_as_float(v[c]) - dsum[c]) * p.scale;
+      for (int hh = 0; hh < 4; ++hh) {
+        uint32_t v[16], pk[8];
+        tmem_ld_32x32b_x16(t_dp + 16 * hh, v);
+        tmem_ld_32x32b_x8(t_s + 8 * hh, pk);
+        tmem_ld_wait();
+#pragma unroll
+        for (int c = 0; c < 16; c += 2) {
+          const int cc = 16 * hh + c;
+          const uint32_t pw = pk[c >> 1];
+          const uint64_t d2 = f2_add(f2_pack(__uint_as_float(v[c]), __uint_as_float(v[c + 1])),
+                                     f2_pack(-dsum[cc], -dsum[cc + 1]));
+          const uint64_t p2 = f2_pack(__uint_as_float(pw << 16), __uint_as_float(pw & 0xffff0000u));
+          float d0, d1;
+          f2_unpack(f2_mul(f2_mul(p2, sc2), d2), d0, d1);
+          v[c >> 1] = pack_bf16x2(d0, d1);
+        }
+#pragma unroll
+        for (int k = 0; k < 2; ++k)
+          *reinterpret_cast<uint4*>(rowp + (((2 * hh + k) ^ (r & 7)) << 4)) =
+              make_uint4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
       }
-      // dS^T row into this step's slot, once step n - 2's products have read it
-      if (!(ok = wait_all(&ds_empty[s], par ^ 1u))) break;
-      write_sw128_row(smem + B_SDS + s * KT_BYTES, r, pr);
+      // the dP^T reads are complete (waited above); dQ^T_n may overwrite them
+      tc_fence_before();
       fence_proxy_async_smem();
-      arrive(&ds_full[s]);
+      arrive(&ds_full[grp]);
       arrive(&in_empty[q3]);
     }
     if (ok && (ok = wait_all(&acc_full, 0))) {
       tc_fence_after();
-      // dK_j and dV_j rows (bf16) into the group's K and V columns of dqkv
-      __nv_bfloat16* dk = p.dqkv + (size_t)(b * p.S + key) * p.ld_dqkv + p.k_col0 + g * FD;
-      __nv_bfloat16* dv = p.dqkv + (size_t)(b * p.S + key) * p.ld_dqkv + p.v_col0 + g * FD;
+      // group 0: the dV_j row, group 1: the dK_j row (bf16) in the group's V / K columns of dqkv
+      __nv_bfloat16* dst = p.dqkv + (size_t)(b * p.S + key) * p.ld_dqkv + (grp ? p.k_col0 : p.v_col0) + g * FD;
+      const uint32_t col = grp ? T_DK : T_DV;
 #pragma unroll 1
-      for (int half = 0; half < 2; ++half) {
-        const uint32_t col = half ? T_DK : T_DV;
-        __nv_bfloat16* dst = half ? dk : dv;
-#pragma unroll 1
-        for (int c = 0; c < 2; ++c) {
-          uint32_t v[64];
-          tmem_ld_32x32b_x32(tl + col + 64 * c, *reinterpret_cast<uint32_t(*)[32]>(v));
-          tmem_ld_32x32b_x32(tl + col + 64 * c + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-          tmem_ld_wait();
-          float f[64];
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld_32x32b_x32(tl + col + 32 * c, v);
+        tmem_ld_wait();
 #pragma unroll
-          for (int e = 0; e < 64; ++e) f[e] = __uint_as_float(v[e]);
-          store_row_bf16(dst + 64 * c, f);
-        }
+        for (int k = 0; k < 4; ++k)
+          reinterpret_cast<uint4*>(dst + 32 * c)[k] =
+              make_uint4(pack_bf16x2(__uint_as_float(v[8 * k]), __uint_as_float(v[8 * k + 1])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 2]), __uint_as_float(v[8 * k + 3])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 4]), __uint_as_float(v[8 * k + 5])),
+                         pack_bf16x2(__uint_as_float(v[8 * k + 6]), __uint_as_float(v[8 * k + 7])));
       }
     }
   } else {
     // --------------------------------------------------------- dQ epilogue
-    const int q = warp & 3;  // this warp's head-dim rows [32 q, 32 q + 32) of dQ^T
+    // Thread (warp quarter q, lane) owns head-dim column d = 32 q + lane of
+    // dQ^T: it reads its 64 query values out of tensor memory, frees the
+    // slot, and adds them into the f32 accumulator with one reduction per
+    // query (each warp instruction covers 32 consecutive floats of a row).
+    const int q = warp & 3;
     const uint32_t tl = tmem_base + ((uint32_t)(q * 32) << 16);
-    uint8_t* stg = smem + B_SDQ + q * (BQB * 32 * 4);
-    float* st = reinterpret_cast<float*>(stg);
     for (int m = 0; m < nsteps; ++m) {
-      if (!wait_all(&dq_full, m & 1)) break;
+      const int s = m & 1;
+      if (!wait_all(&dq_full[s], (m >> 1) & 1)) break;
       tc_fence_after();
       uint32_t v[64];
-      tmem_ld_32x32b_x32(tl + T_DQ, *reinterpret_cast<uint32_t(*)[32]>(v));
-      tmem_ld_32x32b_x32(tl + T_DQ + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+      tmem_ld_32x32b_x32(tl + T_PQ + s * BQB, *reinterpret_cast<uint32_t(*)[32]>(v));
+      tmem_ld_32x32b_x32(tl + T_PQ + s * BQB + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
       tmem_ld_wait();
       tc_fence_before();
-      arrive(&dq_empty);
-      if (lane == 0) bulk_wait_read_all();  // the previous reduce has read the staging tile
-      __syncwarp();
+      arrive(&dq_empty[s]);
+      float* dst = p.dq_acc + (size_t)(b * p.S + step_i(m) * BQB) * p.ld_dq + step_h(m) * FD + q * 32 + lane;
 #pragma unroll
-      for (int c = 0; c < 64; ++c) st[c * 32 + lane] = __uint_as_float(v[c]);
-      fence_proxy_async_smem();
-      __syncwarp();
-      if (lane == 0) {
-        tma_reduce_add_2d(&map_dq, stg, step_h(m) * FD + q * 32, b * p.S + step_i(m) * BQB);
-        bulk_commit_group();
-      }
+      for (int c = 0; c < 64; ++c) red_add_f32(dst + (size_t)c * p.ld_dq, __uint_as_float(v[c]));
     }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
   }
 
   tc_fence_before();
@@ -914,12 +915,10 @@ cudaError_t launch_flash_attn_bwd(const void* qkv, const void* dz, const float* 
   if (d != FD || S % BKB != 0 || nq % nkv != 0) return cudaErrorInvalidValue;
   const int64_t N = (int64_t)batch * S;
   const int64_t W = (int64_t)(nq + 2 * nkv) * d, Zc = (int64_t)nq * d;
-  CUtensorMap map_kv, map_q, map_do, map_dq;
+  CUtensorMap map_kv, map_q, map_do;
   if (!make_map(&map_kv, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, BKB) ||
       !make_map(&map_q, qkv, (uint64_t)W, (uint64_t)N, (uint64_t)W, BQB) ||
-      !make_map(&map_do, dz, (uint64_t)Zc, (uint64_t)N, (uint64_t)Zc, BQB) ||
-      !encode_map(&map_dq, dq_acc, EK_F32, (uint64_t)Zc, (uint64_t)N, (uint64_t)Zc, 32, BQB,
-                  CU_TENSOR_MAP_SWIZZLE_NONE))
+      !make_map(&map_do, dz, (uint64_t)Zc, (uint64_t)N, (uint64_t)Zc, BQB))
     return cudaErrorInvalidValue;
   static bool attr_done = false;
   if (!attr_done) {
@@ -941,9 +940,11 @@ cudaError_t launch_flash_attn_bwd(const void* qkv, const void* dz, const float* 
   p.dsum = dsum;
   p.dqkv = static_cast<__nv_bfloat16*>(dqkv);
   p.ld_dqkv = W;
+  p.dq_acc = dq_acc;
+  p.ld_dq = Zc;
   p.status = status;
   const unsigned blocks = (unsigned)((int64_t)(S / BKB) * batch * nkv);
-  flash_bwd_kernel<<<blocks, BTHREADS, BSMEM, st>>>(map_kv, map_q, map_do, map_dq, p, batch);
+  flash_bwd_kernel<<<blocks, BTHREADS, BSMEM, st>>>(map_kv, map_q, map_do, p, batch);
   return cudaGetLastError();
 }
 
