@@ -228,30 +228,37 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     // -------------------------------------------------------------- MMA issuer
     constexpr uint32_t IDESC_S = idesc_bf16_f32(FB, FB, false, false);
     constexpr uint32_t IDESC_PV = idesc_bf16_f32(FB, FD, false, true);
-    const bool leader = elect_one();  // the lane that issues every MMA and commit
+    // The warp runs this role in warp-uniform control flow; one lane, elected
+    // at each issue point, issues the MMAs and commits.  Descriptors are
+    // built once and advanced by constant offsets, so an MMA costs an add and
+    // the instruction: a 128-wide product keeps the tensor core busy for only
+    // about 64 cycles, less than rebuilding two descriptors per MMA took.
+    const uint64_t q_desc = sw128_desc(smem_u32(smem + SQ), 16, 1024);
+    const uint64_t k_desc = sw128_desc(smem_u32(smem + SK), 16, 1024);
+    const uint64_t v_desc = sw128_desc(smem_u32(smem + SV), TILE_BYTES, 1024);
     auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
       return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
     };
     // S_x = Q_x K_j^T into tile x's score columns
     auto issue_s = [&](int x, int j) {
-      if (leader) {
-        const uint32_t qa = smem_u32(smem + SQ + x * OPND_BYTES), kb = smem_u32(smem + SK + (j & 1) * OPND_BYTES);
+      const uint64_t qa = desc_advance(q_desc, x * OPND_BYTES), kb = desc_advance(k_desc, (j & 1) * OPND_BYTES);
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem_base + x * FB, sw128_desc(qa + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024),
-                     sw128_desc(kb + (kk >> 2) * TILE_BYTES + (kk & 3) * 32, 16, 1024), IDESC_S, kk > 0 ? 1u : 0u);
+          tc_mma_f16(tmem_base + x * FB, desc_advance(qa, (kk >> 2) * TILE_BYTES + (kk & 3) * 32),
+                     desc_advance(kb, (kk >> 2) * TILE_BYTES + (kk & 3) * 32), IDESC_S, kk > 0 ? 1u : 0u);
         tc_commit(&s_full[x]);
       }
       __syncwarp();
     };
     // O_x += P_x V_j, P_x from tile x's score columns (bf16 pairs, 8 columns per K = 16)
     auto issue_pv = [&](int x, int j, bool last) {
-      if (leader) {
-        const uint32_t vb = smem_u32(smem + SV + (j & 1) * OPND_BYTES);
+      const uint64_t vb = desc_advance(v_desc, (j & 1) * OPND_BYTES);
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16_ts(tmem_base + 256 + x * FD, tmem_base + x * FB + kk * 8,
-                        sw128_desc(vb + kk * 2048, TILE_BYTES, 1024), IDESC_PV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tmem_base + 256 + x * FD, tmem_base + x * FB + kk * 8, desc_advance(vb, kk * 2048), IDESC_PV,
+                        (j > 0 || kk > 0) ? 1u : 0u);
         if (last) tc_commit(&o_full[x]);
       }
       __syncwarp();
@@ -261,7 +268,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
       tc_fence_after();
       issue_s(0, 0);
       if (has_b) issue_s(1, 0);
-      if (leader) tc_commit(&k_empty[0]);
+      if (elect_one()) tc_commit(&k_empty[0]);
       __syncwarp();
     }
     for (int j = 0; ok && j < nk; ++j) {
@@ -282,13 +289,13 @@ __global__ void __launch_bounds__(FTHREADS, 1)
         issue_pv(1, j, j + 1 == nk_b);
         if (j + 1 < nk_b) issue_s(1, j + 1);
       }
-      if (leader) {
+      if (elect_one()) {
         tc_commit(&v_empty[s]);
         if (next) tc_commit(&k_empty[(j + 1) & 1]);
       }
       __syncwarp();
     }
-    if (leader) tc_commit(&drain_bar);
+    if (elect_one()) tc_commit(&drain_bar);
     __syncwarp();
     int no_abort = 0;
     mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
@@ -607,17 +614,25 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     constexpr uint32_t IDESC_SP = idesc_bf16_f32(BKB, BQB, false, false);  // S^T, dP^T
     constexpr uint32_t IDESC_KV = idesc_bf16_f32(BKB, FD, false, true);    // dV, dK
     constexpr uint32_t IDESC_DQ = idesc_bf16_f32(FD, BQB, true, true);     // dQ^T
-    const bool leader = elect_one();  // the lane that issues every MMA and commit
-    const uint32_t sk = smem_u32(smem + B_SK), sv = smem_u32(smem + B_SV);
+    // Warp-uniform control flow; one lane, elected at each issue point,
+    // issues the MMAs and commits.  Descriptors are built once and advanced
+    // by constant offsets, so an MMA costs an add and the instruction.
+    const uint64_t k_kdesc = sw128_desc(smem_u32(smem + B_SK), 16, 1024);        // K, K-major
+    const uint64_t v_kdesc = sw128_desc(smem_u32(smem + B_SV), 16, 1024);        // V, K-major
+    const uint64_t k_mdesc = sw128_desc(smem_u32(smem + B_SK), KT_BYTES, 1024);  // K^T, MN-major
+    const uint64_t q_kdesc = sw128_desc(smem_u32(smem + B_SQ), 16, 1024);        // Q ring, K-major
+    const uint64_t q_mdesc = sw128_desc(smem_u32(smem + B_SQ), QT_BYTES, 1024);  // Q ring, MN-major
+    const uint64_t o_kdesc = sw128_desc(smem_u32(smem + B_SDO), 16, 1024);       // dO ring, K-major
+    const uint64_t o_mdesc = sw128_desc(smem_u32(smem + B_SDO), QT_BYTES, 1024); // dO ring, MN-major
+    const uint64_t ds_kdesc = sw128_desc(smem_u32(smem + B_SDS), 16, 1024);      // dS^T slots, K-major
+    const uint64_t ds_mdesc = sw128_desc(smem_u32(smem + B_SDS), KT_BYTES, 1024);// dS^T slots, MN-major
     // S^T_n = K Q_n^T or dP^T_n = V dO_n^T, then a commit to `done`
-    auto issue_nt = [&](uint32_t d_tmem, uint32_t a, uint32_t bq, uint64_t* done) {
-      if (leader) {
+    auto issue_nt = [&](uint32_t d_tmem, uint64_t a, uint64_t bq, uint64_t* done) {
+      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-          const uint64_t a_desc = sw128_desc(a + (kk >> 2) * KT_BYTES + (kk & 3) * 32, 16, 1024);
-          const uint64_t b_desc = sw128_desc(bq + (kk >> 2) * QT_BYTES + (kk & 3) * 32, 16, 1024);
-          tc_mma_f16(d_tmem, a_desc, b_desc, IDESC_SP, kk > 0 ? 1u : 0u);
-        }
+        for (int kk = 0; kk < 8; ++kk)
+          tc_mma_f16(d_tmem, desc_advance(a, (kk >> 2) * KT_BYTES + (kk & 3) * 32),
+                     desc_advance(bq, (kk >> 2) * QT_BYTES + (kk & 3) * 32), IDESC_SP, kk > 0 ? 1u : 0u);
         tc_commit(done);
       }
       __syncwarp();
@@ -627,7 +642,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       const int q = n % QST;
       if (!wait_all(&in_full[q], (n / QST) & 1)) return 0;
       tc_fence_after();
-      issue_nt(tmem_base + T_S + (n & 1) * BQB, sk, smem_u32(smem + B_SQ + 2 * q * QT_BYTES), &s_full[n & 1]);
+      issue_nt(tmem_base + T_S + (n & 1) * BQB, k_kdesc, desc_advance(q_kdesc, 2 * q * QT_BYTES), &s_full[n & 1]);
       return 1;
     };
     // dP^T_n into slot n & 1 once dQ^T_{n-2} has been read out of it; dO_n is
@@ -635,7 +650,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     auto issue_dp = [&](int n) -> int {
       if (!wait_all(&dq_empty[n & 1], ((n >> 1) & 1) ^ 1u)) return 0;
       tc_fence_after();
-      issue_nt(tmem_base + T_PQ + (n & 1) * BQB, sv, smem_u32(smem + B_SDO + 2 * (n % QST) * QT_BYTES),
+      issue_nt(tmem_base + T_PQ + (n & 1) * BQB, v_kdesc, desc_advance(o_kdesc, 2 * (n % QST) * QT_BYTES),
                &dp_full[n & 1]);
       return 1;
     };
@@ -646,31 +661,31 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     for (int n = 0; ok && n < nsteps; ++n) {
       const int s = n & 1, q = n % QST;
       const uint32_t par = (uint32_t)((n >> 1) & 1);
-      const uint32_t sq = smem_u32(smem + B_SQ + 2 * q * QT_BYTES), sdo = smem_u32(smem + B_SDO + 2 * q * QT_BYTES);
-      const uint32_t sds = smem_u32(smem + B_SDS + s * KT_BYTES);
+      const uint64_t sq = desc_advance(q_mdesc, 2 * q * QT_BYTES), sdo = desc_advance(o_mdesc, 2 * q * QT_BYTES);
+      const uint64_t sds_k = desc_advance(ds_kdesc, s * KT_BYTES), sds_m = desc_advance(ds_mdesc, s * KT_BYTES);
       // dV += P^T dO_n, P^T from tensor memory (bf16 pairs, 8 columns per K = 16)
       if (!(ok = wait_all(&p_full[s], par))) break;
       tc_fence_after();
-      if (leader) {
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_f16_ts(tmem_base + T_DV, tmem_base + T_S + s * BQB + kk * 8,
-                        sw128_desc(sdo + kk * 2048, QT_BYTES, 1024), IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16_ts(tmem_base + T_DV, tmem_base + T_S + s * BQB + kk * 8, desc_advance(sdo, kk * 2048), IDESC_KV,
+                        (n > 0 || kk > 0) ? 1u : 0u);
       }
       __syncwarp();
       if (n + 1 < nsteps && !(ok = issue_dp(n + 1))) break;
       // dK += dS^T Q_n ; dQ^T_n = K^T dS^T over the slot's dP^T, which the group has read
       if (!(ok = wait_all(&ds_full[s], par))) break;
       tc_fence_after();
-      if (leader) {
+      if (elect_one()) {
 #pragma unroll
         for (int kk = 0; kk < 4; ++kk)
-          tc_mma_f16(tmem_base + T_DK, sw128_desc(sds + kk * 32, 16, 1024), sw128_desc(sq + kk * 2048, QT_BYTES, 1024),
-                     IDESC_KV, (n > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_f16(tmem_base + T_DK, desc_advance(sds_k, kk * 32), desc_advance(sq, kk * 2048), IDESC_KV,
+                     (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem_base + T_PQ + s * BQB, sw128_desc(sk + kk * 2048, KT_BYTES, 1024),
-                     sw128_desc(sds + kk * 2048, KT_BYTES, 1024), IDESC_DQ, kk > 0 ? 1u : 0u);
+          tc_mma_f16(tmem_base + T_PQ + s * BQB, desc_advance(k_mdesc, kk * 2048), desc_advance(sds_m, kk * 2048),
+                     IDESC_DQ, kk > 0 ? 1u : 0u);
         tc_commit(&dq_full[s]);
         tc_commit(&ds_empty[s]);
         tc_commit(&in_empty[q]);
@@ -679,7 +694,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       __syncwarp();
       if (n + 2 < nsteps && !(ok = issue_s(n + 2))) break;
     }
-    if (leader) tc_commit(&drain_bar);
+    if (elect_one()) tc_commit(&drain_bar);
     __syncwarp();
     int no_abort = 0;
     mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);

@@ -318,6 +318,12 @@ __device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo_byte
   return d;
 }
 
+// The descriptor of the same layout `bytes` further into shared memory.  The
+// start-address field holds address >> 4 in the low 14 bits, so for operands
+// below 256 KB the add never carries out of it; computing a descriptor once
+// and advancing it keeps the per-MMA issue cost to one add.
+__device__ __forceinline__ uint64_t desc_advance(uint64_t desc, uint32_t bytes) { return desc + (uint64_t)(bytes >> 4); }
+
 // Instruction descriptor, kind::f16: D f32, A/B bf16, dense, no negation.
 // a_mn / b_mn select MN-major (transposed) operands. N>>3 at [17,23), M>>4 at [24,29).
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N, bool a_mn, bool b_mn) {
