@@ -23,7 +23,8 @@
 
 namespace {
 
-// One double per 256-thread block; each thread handles one 16-byte vector.
+// One double per 256-thread block of 16-byte vectors; the size limit on n
+// stays that of one block per 256 vectors.
 constexpr int64_t kMaxBlocks = TPMLP_NOALLOC_LOSS_MAX_BLOCKS;
 static __device__ __align__(256) double g_loss_partials[kMaxBlocks];
 
@@ -96,8 +97,12 @@ extern "C" tpmlp_status tpmlp_mse_loss_grad_noalloc(int32_t dtype, int64_t n, co
     const tpmlp_status s = partials_on_current_device(&part);
     if (s != TPMLP_OK) return s;
     const int dt = dtype == TPMLP_BF16 ? 1 : 0;
-    e = tpmlp::launch_mse_loss_grad(dt, y, target, dy, part, (int)blocks, n, (float)(1.0 / (double)n), st);
-    if (e == cudaSuccess) e = tpmlp::launch_loss_finalize(part, (int)blocks, 0.5 / (double)n, loss_dev, st);
+    // The loss kernel strides over the vectors, so a grid of at most 1024
+    // blocks covers any n (one block per vector group would leave most of
+    // each block's time to launch and reduction overhead at large n).
+    const int grid = (int)(blocks < 1024 ? blocks : 1024);
+    e = tpmlp::launch_mse_loss_grad(dt, y, target, dy, part, grid, n, (float)(1.0 / (double)n), st);
+    if (e == cudaSuccess) e = tpmlp::launch_loss_finalize(part, grid, 0.5 / (double)n, loss_dev, st);
   }
   if (e != cudaSuccess) {
     tpmlp::set_thread_error(std::string("tpmlp_mse_loss_grad_noalloc: ") + cudaGetErrorString(e));
