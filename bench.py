@@ -54,7 +54,7 @@ GELU_UNITS = dict(GEMM_UNITS, gemm_gateup_act=2, gemm_wgrad_gateup=2, gemm_dgrad
 # kernel sources per family: a change to any of them invalidates the recorded DRAM traffic of that
 # family's kernels
 KERNEL_FAMILIES = {
-    "gemm": ("gemm_tc.cu", "gemm_simt.cu", "ptx_sm103.cuh", "epilogue.cuh", "tma_maps.cuh"),
+    "gemm": ("gemm_tc.cu", "gemm_simt.cu", "ptx_sm103.cuh", "epilogue.cuh", "tma_maps.cuh", "f32x2.cuh"),
     "rowwise": ("rowwise.cu", "vec.cuh", "epilogue.cuh"),
     "optim": ("optim.cu", "vec.cuh"),
     "fp8": ("fp8.cu",),

@@ -11,6 +11,8 @@
 #include <cuda_bf16.h>
 #include <stdint.h>
 
+#include "f32x2.cuh"
+
 namespace tpmlp {
 
 enum EpiKind : int {
@@ -81,6 +83,35 @@ __device__ __forceinline__ void swiglu_bwd_fast(float da, float g, float u, floa
   const float s = sigmoid_fast(g);
   dg = da * u * s * (1.0f + g * (1.0f - s));
   du = da * g * s;
+}
+
+// The same two formulas for a pair of channels with two-lane arithmetic:
+// sigma(g) = 1 / (1 + 2^(-g log2 e)) from one ex2 and one rcp per channel,
+// then dG = dA sigma U (1 + g (1 - sigma)) and dU = dA sigma g.  For
+// g -> -inf sigma is 0 and for g -> +inf it is 1, as above.
+__device__ __forceinline__ void swiglu_bwd_fast2(float da0, float da1, float g0, float g1, float u0, float u1,
+                                                 float& dg0, float& dg1, float& du0, float& du1) {
+  const uint64_t one = f2_pack(1.0f, 1.0f);
+  const uint64_t g = f2_pack(g0, g1);
+  float t0, t1;
+  f2_unpack(f2_mul(g, f2_pack(-1.4426950408889634f, -1.4426950408889634f)), t0, t1);
+  float d0, d1;
+  f2_unpack(f2_add(f2_pack(ex2_fast(t0), ex2_fast(t1)), one), d0, d1);
+  const uint64_t s = f2_pack(rcp_fast(d0), rcp_fast(d1));
+  const uint64_t das = f2_mul(f2_pack(da0, da1), s);
+  f2_unpack(f2_mul(das, g), du0, du1);
+  const uint64_t w = f2_fma(g, f2_fma(s, f2_pack(-1.0f, -1.0f), one), one);  // 1 + g (1 - sigma)
+  f2_unpack(f2_mul(f2_mul(das, f2_pack(u0, u1)), w), dg0, dg1);
+}
+
+// SiLU(g) u for a pair of channels: g sigma(g) u.
+__device__ __forceinline__ void swiglu_fwd_fast2(float g0, float g1, float u0, float u1, float& a0, float& a1) {
+  const uint64_t g = f2_pack(g0, g1);
+  float t0, t1;
+  f2_unpack(f2_mul(g, f2_pack(-1.4426950408889634f, -1.4426950408889634f)), t0, t1);
+  float d0, d1;
+  f2_unpack(f2_add(f2_pack(ex2_fast(t0), ex2_fast(t1)), f2_pack(1.0f, 1.0f)), d0, d1);
+  f2_unpack(f2_mul(f2_mul(g, f2_pack(u0, u1)), f2_pack(rcp_fast(d0), rcp_fast(d1))), a0, a1);
 }
 
 // One output element (m, n) of the fp32 SIMT path.  For GATEUP_SWIGLU, `acc`

@@ -271,7 +271,7 @@ __device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const f
     stage_row_bf16(st, r, v);
     stage_row_bf16(st + 2048, r, u);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] = silu_fast(v[i]) * u[i];
+    for (int i = 0; i < 32; i += 2) swiglu_fwd_fast2(v[i], v[i + 1], u[i], u[i + 1], o[i], o[i + 1]);
     stage_row_bf16(st + 4096, r, o);
     if (want_max) mx = max_abs32(o, ncols);
   } else if (EPI == EPI_FC1_GELU) {
@@ -296,7 +296,8 @@ __device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const f
     unpack32(in.a, g);
     unpack32(in.b, uu);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) swiglu_bwd_fast(v[i], g[i], uu[i], o[i], uu[i]);
+    for (int i = 0; i < 32; i += 2)
+      swiglu_bwd_fast2(v[i], v[i + 1], g[i], g[i + 1], uu[i], uu[i + 1], o[i], o[i + 1], uu[i], uu[i + 1]);
     stage_row_bf16(st, r, o);
     stage_row_bf16(st + 2048, r, uu);
     if (want_max) mx = fmaxf(max_abs32(o, ncols), max_abs32(uu, ncols));
