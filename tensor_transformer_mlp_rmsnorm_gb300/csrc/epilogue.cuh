@@ -104,6 +104,34 @@ __device__ __forceinline__ void swiglu_bwd_fast2(float da0, float da1, float g0,
   f2_unpack(f2_mul(f2_mul(das, f2_pack(u0, u1)), w), dg0, dg1);
 }
 
+// Phi(z) and exp(-z^2/2) for the bf16 tensor-core epilogues.  erf comes from
+// the rational approximation of Abramowitz & Stegun, Handbook of
+// Mathematical Functions, eq. 7.1.26: for x >= 0, erf(x) = 1 - t P(t)
+// e^(-x^2) with t = 1 / (1 + p x), |error| <= 1.5e-7, extended to x < 0 by
+// oddness; here x = |z| / sqrt(2), so e^(-x^2) = e^(-z^2/2) serves the
+// density too.  Results are stored in bf16 (2^-9 relative), far coarser
+// than the approximation.  The fp32 path keeps erff / expf.
+__device__ __forceinline__ void gauss_fast(float z, float& Phi, float& e) {
+  const float x = fabsf(z) * 0.70710678118654752f;
+  const float t = rcp_fast(fmaf(0.3275911f, x, 1.0f));
+  const float tp =
+      t * fmaf(t, fmaf(t, fmaf(t, fmaf(t, 1.061405429f, -1.453152027f), 1.421413741f), -0.284496736f),
+               0.254829592f);
+  e = ex2_fast(-1.4426950408889634f * x * x);
+  Phi = fmaf(0.5f, copysignf(fmaf(-tp, e, 1.0f), z), 0.5f);
+}
+// GeLU(z) = z Phi(z) and GeLU'(z) = Phi(z) + z phi(z), phi(z) = e^(-z^2/2) / sqrt(2 pi).
+__device__ __forceinline__ float gelu_fast(float z) {
+  float P, e;
+  gauss_fast(z, P, e);
+  return z * P;
+}
+__device__ __forceinline__ float gelu_grad_fast(float z) {
+  float P, e;
+  gauss_fast(z, P, e);
+  return fmaf(z * 0.39894228040143268f, e, P);
+}
+
 // SiLU(g) u for a pair of channels: g sigma(g) u.
 __device__ __forceinline__ void swiglu_fwd_fast2(float g0, float g1, float u0, float u1, float& a0, float& a1) {
   const uint64_t g = f2_pack(g0, g1);

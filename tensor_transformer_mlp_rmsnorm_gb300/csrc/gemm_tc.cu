@@ -281,7 +281,7 @@ __device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const f
     for (int i = 0; i < 32; ++i) b[i] += v[i];
     stage_row_bf16(st, r, b);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] = gelu_f(b[i]);
+    for (int i = 0; i < 32; ++i) o[i] = gelu_fast(b[i]);
     stage_row_bf16(st + 2048, r, o);
     if (want_max) mx = max_abs32(o, ncols);
   } else if (EPI == EPI_DOWN_RESID) {
@@ -305,7 +305,7 @@ __device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const f
     float z[32];
     unpack32(in.a, z);
 #pragma unroll
-    for (int i = 0; i < 32; ++i) o[i] = v[i] * gelu_grad_f(z[i]);
+    for (int i = 0; i < 32; ++i) o[i] = v[i] * gelu_grad_fast(z[i]);
     stage_row_bf16(st, r, o);
     if (want_max) mx = max_abs32(o, ncols);
   } else if (EPI == EPI_STORE_BF16) {
