@@ -56,7 +56,6 @@ struct KDepth {
   static constexpr int STAGE = F8 ? 128 : BK;  // elements per stage row
   static constexpr int MMA = F8 ? 32 : UMMA_K;
 };
-constexpr int NUM_THREADS = 192;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s per wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s for draining after an abort
@@ -70,7 +69,22 @@ __host__ __device__ constexpr bool epi_has_in() {
   return EPI == EPI_DOWN_RESID || EPI == EPI_DGRAD_SWIGLU || EPI == EPI_DGRAD_GELU;
 }
 
-template <bool PAIR, bool HAS_IN>
+// Epilogue warps per CTA.  The SwiGLU backward epilogue (read G and U, write
+// dG and dU, per element two exponentials' worth of math) takes longer than
+// a tile's main loop with four warps, so it gets eight: two per TMEM lane
+// quarter, taking alternate 32-column chunks, each with one input and one
+// output staging buffer (the same shared memory as four double-buffered
+// warps).
+template <int EPI>
+__host__ __device__ constexpr int epi_warps() {
+  return EPI == EPI_DGRAD_SWIGLU ? 8 : 4;
+}
+template <int EPI>
+__host__ __device__ constexpr int gemm_threads() {
+  return 64 + 32 * epi_warps<EPI>();
+}
+
+template <bool PAIR, bool HAS_IN, int EW = 4>
 struct TileCfg {
   // Operand ring depth: the staging of epilogue inputs takes one stage's room.
   static constexpr int STAGES = PAIR ? (HAS_IN ? 5 : 6) : (HAS_IN ? 3 : 4);
@@ -82,13 +96,14 @@ struct TileCfg {
   // alternately (each up to two 32x32 bf16 tiles or one 32x32 f32 tile) or,
   // for the three-output gate/up epilogue, one 6 KB buffer; inputs in two
   // 4 KB buffers (up to two 32x32 bf16 tiles each).
-  static constexpr int EPI_OUT_BYTES = 8192;
-  static constexpr int EPI_IN_BYTES = HAS_IN ? 8192 : 0;
+  // With eight epilogue warps each has one 4 KB buffer of each kind.
+  static constexpr int EPI_OUT_BYTES = EW == 8 ? 4096 : 8192;
+  static constexpr int EPI_IN_BYTES = HAS_IN ? (EW == 8 ? 4096 : 8192) : 0;
   static constexpr int EPI_WARP_BYTES = EPI_OUT_BYTES + EPI_IN_BYTES;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_WARP_BYTES + 1024;  // + alignment
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * EPI_WARP_BYTES + 1024;  // + alignment
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // output rows per tile (per pair)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;
-  static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8 : 4;  // one per epilogue warp, both CTAs
+  static constexpr uint32_t EPI_ARRIVALS = PAIR ? 2 * EW : EW;  // one per epilogue warp, both CTAs
 };
 
 struct TcParams {
@@ -317,13 +332,14 @@ __device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const f
 }
 
 template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8>
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_o0, const __grid_constant__ CUtensorMap map_o1,
                    const __grid_constant__ CUtensorMap map_o2, const __grid_constant__ CUtensorMap map_i0,
                    const __grid_constant__ CUtensorMap map_i1, const TcParams p) {
   constexpr bool HAS_IN = epi_has_in<EPI>();
-  using C = TileCfg<PAIR, HAS_IN>;
+  constexpr int EW = epi_warps<EPI>();
+  using C = TileCfg<PAIR, HAS_IN, EW>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
   __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
@@ -331,7 +347,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t never_bar;
-  __shared__ __align__(8) uint64_t in_bar[4][2];  // epilogue input tiles, per warp and buffer
+  __shared__ __align__(8) uint64_t in_bar[EW][2];  // epilogue input tiles, per warp and buffer
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -361,7 +377,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
     mbar_init(&drain_bar, 1);
     mbar_init(&never_bar, 1);
-    for (int w = 0; w < 4; ++w)
+    for (int w = 0; w < EW; ++w)
       for (int b = 0; b < 2; ++b) mbar_init(&in_bar[w][b], 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -582,8 +598,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
+    // With four warps, warp ew handles every chunk of its TMEM lane quarter,
+    // double-buffering inputs and outputs.  With eight, the two warps of a
+    // quarter take alternate chunks (first chunk ew / 4), each with single
+    // buffers: a warp refills its input buffer once every lane has read the
+    // current chunk's rows, and its output buffer once the previous store has
+    // read it.
+    constexpr int CSTEP = EW / 4;            // chunks between a warp's consecutive chunks
+    constexpr int NIN = EW == 4 ? 2 : 1;     // input buffers per warp
+    constexpr int NOUT = EW == 4 ? EpiOut<EPI>::NBUF : 1;  // output buffers per warp
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - 2;
+    const int c0 = ew / 4;   // this warp's first chunk of a tile
     uint8_t* st = sE + ew * C::EPI_WARP_BYTES;  // output staging
     uint8_t* si = st + C::EPI_OUT_BYTES;        // input staging
     constexpr uint32_t IN_BYTES = EPI == EPI_DGRAD_SWIGLU ? 4096u : 2048u;
@@ -592,10 +618,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const float deq = F8 ? __ldg(p.deq_a) * __ldg(p.deq_b) : 1.0f;
     const bool want_max = p.ep.amax != nullptr;
     float amax_acc = 0.0f;
-    // Input tiles of chunk [col, col+32) of this warp's 32 rows -> buffer n_in & 1.
+    // Input tiles of chunk [col, col+32) of this warp's 32 rows -> buffer n_in % NIN.
     auto issue_in = [&](int col, int row0) {
       if (!HAS_IN) return;
-      const uint32_t b = n_in & 1u;
+      const uint32_t b = NIN == 2 ? (n_in & 1u) : 0u;
       if (lane == 0) {
         mbar_arrive_expect_tx(&in_bar[ew][b], IN_BYTES);
         tma_load_2d(si + b * 4096, &map_i0, &in_bar[ew][b], col, row0);
@@ -613,7 +639,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
       // The first chunk's inputs are fetched while the tile's main loop runs,
       // each later chunk's while the previous one is computed.
-      if (col_base < p.N && row0 < p.M) issue_in(col_base + so.col, row0 + so.row);
+      if (col_base + 32 * c0 < p.N && row0 < p.M) issue_in(col_base + 32 * c0 + so.col, row0 + so.row);
       int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -621,16 +647,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       uint32_t r0[32], r1[32];
 #pragma unroll 1
-      for (int c = 0; c < CHUNKS; ++c) {
+      for (int c = c0; c < CHUNKS; c += CSTEP) {
         const int col = col_base + c * 32;
         // Chunks wholly outside the output are skipped by the whole warp.
         if (col >= p.N || row0 >= p.M) break;
-        if (c + 1 < CHUNKS && col + 32 < p.N) issue_in(col + 32 + so.col, row0 + so.row);
+        const bool more = c + CSTEP < CHUNKS && col + 32 * CSTEP < p.N;
+        if (NIN == 2 && more) issue_in(col + 32 * CSTEP + so.col, row0 + so.row);
         tmem_ld_32x32b_x32(tbase + c * 32, r0);
         if (EPI == EPI_GATEUP_SWIGLU) tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, r1);
         EpiIn in;
         if (HAS_IN) {
-          const uint32_t b = n_used & 1u;
+          const uint32_t b = NIN == 2 ? (n_used & 1u) : 0u;
           int iok = mbar_wait(&in_bar[ew][b], (in_par >> b) & 1u, abort_flag, p.status, STATUS_TIMEOUT,
                               WAIT_LIMIT_NS);
           iok = __all_sync(0xffffffffu, iok);
@@ -642,13 +669,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           ++n_used;
           read_row_bf16(si + b * 4096, lane, in.a);
           if (EPI == EPI_DGRAD_SWIGLU) read_row_bf16(si + b * 4096 + 2048, lane, in.b);
+          if (NIN == 1) {
+            __syncwarp();  // every lane has read its input row before the buffer is refilled
+            if (more) issue_in(col + 32 * CSTEP + so.col, row0 + so.row);
+          }
         }
-        // Stores alternate between the two staging buffers (counting stored
+        // Stores alternate between the output buffers (counting stored
         // chunks, not chunk indices); a buffer is rewritten once the stores
-        // issued from it two chunks ago have read it.
-        uint8_t* sb = st + (EpiOut<EPI>::NBUF == 2 ? (n_stored & 1u) * 4096 : 0);
+        // issued from it NOUT chunks ago have read it.
+        uint8_t* sb = st + (NOUT == 2 ? (n_stored & 1u) * 4096 : 0);
         if (lane == 0) {
-          if (EpiOut<EPI>::NBUF == 2)
+          if (NOUT == 2)
             bulk_wait_read_but_last();
           else
             bulk_wait_read_all();
@@ -690,7 +721,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // Input tiles still in flight (after an abort) land before the CTA may exit.
     int no_abort = 0;
     while (n_used < n_in) {
-      const uint32_t b = n_used & 1u;
+      const uint32_t b = NIN == 2 ? (n_used & 1u) : 0u;
       mbar_wait(&in_bar[ew][b], (in_par >> b) & 1u, &no_abort, p.status, 0u, DRAIN_LIMIT_NS);
       in_par ^= 1u << b;
       ++n_used;
@@ -728,7 +759,8 @@ struct Maps {
 
 template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStream_t st) {
-  using C = TileCfg<PAIR, epi_has_in<EPI>()>;
+  using C = TileCfg<PAIR, epi_has_in<EPI>(), epi_warps<EPI>()>;
+  constexpr int NUM_THREADS = gemm_threads<EPI>();
   auto kfn = gemm_tc_kernel<PAIR, A_MN, B_MN, EPI, F8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
