@@ -69,25 +69,22 @@ __host__ __device__ constexpr bool epi_has_in() {
   return EPI == EPI_DOWN_RESID || EPI == EPI_DGRAD_SWIGLU || EPI == EPI_DGRAD_GELU;
 }
 
-// Epilogue warps per CTA.  The SwiGLU backward epilogue (read G and U, write
-// dG and dU, per element two exponentials' worth of math) takes longer than
-// a tile's main loop with four warps, so it gets eight: two per TMEM lane
-// quarter, taking alternate 32-column chunks, each with one input and one
-// output staging buffer (the same shared memory as four double-buffered
-// warps).
+constexpr int NUM_THREADS = 192;
+
+// Whether the epilogue warps stage with single (rather than double) input
+// and output buffers.  The SwiGLU backward's main loop contracts over only
+// H with an MN-major W_down: it needs the sixth ring stage more than its
+// epilogue needs double buffers (measured: 4% faster).
 template <int EPI>
-__host__ __device__ constexpr int epi_warps() {
-  return EPI == EPI_DGRAD_SWIGLU ? 8 : 4;
-}
-template <int EPI>
-__host__ __device__ constexpr int gemm_threads() {
-  return 64 + 32 * epi_warps<EPI>();
+__host__ __device__ constexpr bool epi_single() {
+  return EPI == EPI_DGRAD_SWIGLU;
 }
 
-template <bool PAIR, bool HAS_IN, int EW = 4>
+template <bool PAIR, bool HAS_IN, bool SB = false>
 struct TileCfg {
-  // Operand ring depth: the staging of epilogue inputs takes one stage's room.
-  static constexpr int STAGES = PAIR ? (HAS_IN ? 5 : 6) : (HAS_IN ? 3 : 4);
+  // Operand ring depth: double-buffered staging of epilogue inputs takes one
+  // stage's room.
+  static constexpr int STAGES = PAIR ? (HAS_IN && !SB ? 5 : 6) : (HAS_IN ? 3 : 4);
   static constexpr int B_ROWS = PAIR ? BN / 2 : BN;  // B columns held by this CTA per stage
   static constexpr int A_BYTES = BM * BK * 2;
   static constexpr int B_BYTES = B_ROWS * BK * 2;
@@ -96,14 +93,14 @@ struct TileCfg {
   // alternately (each up to two 32x32 bf16 tiles or one 32x32 f32 tile) or,
   // for the three-output gate/up epilogue, one 6 KB buffer; inputs in two
   // 4 KB buffers (up to two 32x32 bf16 tiles each).
-  // With eight epilogue warps each has one 4 KB buffer of each kind.
-  static constexpr int EPI_OUT_BYTES = EW == 8 ? 4096 : 8192;
-  static constexpr int EPI_IN_BYTES = HAS_IN ? (EW == 8 ? 4096 : 8192) : 0;
+  // With single buffers each warp has one 4 KB buffer of each kind.
+  static constexpr int EPI_OUT_BYTES = SB ? 4096 : 8192;
+  static constexpr int EPI_IN_BYTES = HAS_IN ? (SB ? 4096 : 8192) : 0;
   static constexpr int EPI_WARP_BYTES = EPI_OUT_BYTES + EPI_IN_BYTES;
-  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + EW * EPI_WARP_BYTES + 1024;  // + alignment
+  static constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 4 * EPI_WARP_BYTES + 1024;  // + alignment
   static constexpr int TILE_M = PAIR ? 2 * BM : BM;  // output rows per tile (per pair)
   static constexpr uint32_t TX_BYTES = PAIR ? 2 * STAGE_BYTES : STAGE_BYTES;
-  static constexpr uint32_t EPI_ARRIVALS = PAIR ? 2 * EW : EW;  // one per epilogue warp, both CTAs
+  static constexpr uint32_t EPI_ARRIVALS = PAIR ? 8 : 4;  // one per epilogue warp, both CTAs
 };
 
 struct TcParams {
@@ -332,14 +329,14 @@ __device__ __forceinline__ float epi_stage(const EpiParams& ep, int col, const f
 }
 
 template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8>
-__global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
+__global__ void __launch_bounds__(NUM_THREADS, 1)
     gemm_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_b,
                    const __grid_constant__ CUtensorMap map_o0, const __grid_constant__ CUtensorMap map_o1,
                    const __grid_constant__ CUtensorMap map_o2, const __grid_constant__ CUtensorMap map_i0,
                    const __grid_constant__ CUtensorMap map_i1, const TcParams p) {
   constexpr bool HAS_IN = epi_has_in<EPI>();
-  constexpr int EW = epi_warps<EPI>();
-  using C = TileCfg<PAIR, HAS_IN, EW>;
+  constexpr bool SB = epi_single<EPI>();
+  using C = TileCfg<PAIR, HAS_IN, SB>;
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t full_bar[C::STAGES];
   __shared__ __align__(8) uint64_t empty_bar[C::STAGES];
@@ -347,7 +344,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
   __shared__ __align__(8) uint64_t tempty_bar[2];
   __shared__ __align__(8) uint64_t drain_bar;
   __shared__ __align__(8) uint64_t never_bar;
-  __shared__ __align__(8) uint64_t in_bar[EW][2];  // epilogue input tiles, per warp and buffer
+  __shared__ __align__(8) uint64_t in_bar[4][2];  // epilogue input tiles, per warp and buffer
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
 
@@ -377,7 +374,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     }
     mbar_init(&drain_bar, 1);
     mbar_init(&never_bar, 1);
-    for (int w = 0; w < EW; ++w)
+    for (int w = 0; w < 4; ++w)
       for (int b = 0; b < 2; ++b) mbar_init(&in_bar[w][b], 1);
     abort_sh = 0;
     fence_mbar_init();
@@ -598,18 +595,15 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
     }
   } else {
     // -------------------------------------------------------------- epilogue
-    // With four warps, warp ew handles every chunk of its TMEM lane quarter,
-    // double-buffering inputs and outputs.  With eight, the two warps of a
-    // quarter take alternate chunks (first chunk ew / 4), each with single
-    // buffers: a warp refills its input buffer once every lane has read the
-    // current chunk's rows, and its output buffer once the previous store has
-    // read it.
-    constexpr int CSTEP = EW / 4;            // chunks between a warp's consecutive chunks
-    constexpr int NIN = EW == 4 ? 2 : 1;     // input buffers per warp
-    constexpr int NOUT = EW == 4 ? EpiOut<EPI>::NBUF : 1;  // output buffers per warp
+    // Warp ew handles every 32-column chunk of its TMEM lane quarter.  With
+    // double buffers the next chunk's inputs are requested before the current
+    // one is read; with single buffers once every lane has read the current
+    // chunk's rows, and the output buffer is rewritten once the previous
+    // store has read it.
+    constexpr int NIN = SB ? 1 : 2;          // input buffers per warp
+    constexpr int NOUT = SB ? 1 : EpiOut<EPI>::NBUF;  // output buffers per warp
     const int q = warp & 3;  // TMEM lane quarter this warp may access
     const int ew = warp - 2;
-    const int c0 = ew / 4;   // this warp's first chunk of a tile
     uint8_t* st = sE + ew * C::EPI_WARP_BYTES;  // output staging
     uint8_t* si = st + C::EPI_OUT_BYTES;        // input staging
     constexpr uint32_t IN_BYTES = EPI == EPI_DGRAD_SWIGLU ? 4096u : 2048u;
@@ -639,7 +633,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
       // The first chunk's inputs are fetched while the tile's main loop runs,
       // each later chunk's while the previous one is computed.
-      if (col_base + 32 * c0 < p.N && row0 < p.M) issue_in(col_base + 32 * c0 + so.col, row0 + so.row);
+      if (col_base < p.N && row0 < p.M) issue_in(col_base + so.col, row0 + so.row);
       int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -647,12 +641,12 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
       uint32_t r0[32], r1[32];
 #pragma unroll 1
-      for (int c = c0; c < CHUNKS; c += CSTEP) {
+      for (int c = 0; c < CHUNKS; ++c) {
         const int col = col_base + c * 32;
         // Chunks wholly outside the output are skipped by the whole warp.
         if (col >= p.N || row0 >= p.M) break;
-        const bool more = c + CSTEP < CHUNKS && col + 32 * CSTEP < p.N;
-        if (NIN == 2 && more) issue_in(col + 32 * CSTEP + so.col, row0 + so.row);
+        const bool more = c + 1 < CHUNKS && col + 32 < p.N;
+        if (NIN == 2 && more) issue_in(col + 32 + so.col, row0 + so.row);
         tmem_ld_32x32b_x32(tbase + c * 32, r0);
         if (EPI == EPI_GATEUP_SWIGLU) tmem_ld_32x32b_x32(tbase + BN / 2 + c * 32, r1);
         EpiIn in;
@@ -671,7 +665,7 @@ __global__ void __launch_bounds__(gemm_threads<EPI>(), 1)
           if (EPI == EPI_DGRAD_SWIGLU) read_row_bf16(si + b * 4096 + 2048, lane, in.b);
           if (NIN == 1) {
             __syncwarp();  // every lane has read its input row before the buffer is refilled
-            if (more) issue_in(col + 32 * CSTEP + so.col, row0 + so.row);
+            if (more) issue_in(col + 32 + so.col, row0 + so.row);
           }
         }
         // Stores alternate between the output buffers (counting stored
@@ -759,8 +753,7 @@ struct Maps {
 
 template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStream_t st) {
-  using C = TileCfg<PAIR, epi_has_in<EPI>(), epi_warps<EPI>()>;
-  constexpr int NUM_THREADS = gemm_threads<EPI>();
+  using C = TileCfg<PAIR, epi_has_in<EPI>(), epi_single<EPI>()>;
   auto kfn = gemm_tc_kernel<PAIR, A_MN, B_MN, EPI, F8>;
   static std::once_flag once;
   static cudaError_t attr_err = cudaSuccess;
