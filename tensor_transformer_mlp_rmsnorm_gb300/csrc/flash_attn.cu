@@ -392,7 +392,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 // One CTA per (sequence b, KV group g, 128-key block j) accumulates dK_j and
 // dV_j of the group in tensor memory over every query head of the group and
 // every 64-query block i that sees the keys (i >= 2 j), and adds each
-// dQ_i contribution into an f32 accumulator with a TMA reduce-add.  With P
+// dQ_i contribution into an f32 accumulator with reductions.  With P
 // recomputed from the forward's log-sum-exp and D_i = rowsum(dO_i o O_i):
 //
 //   S^T  = K_j Q_i^T               dP^T = V_j dO_i^T
