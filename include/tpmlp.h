@@ -330,11 +330,18 @@ typedef struct {
   int32_t n_heads;    /* query heads n_q, a multiple of n_kv_heads */
   int32_t n_kv_heads; /* key/value heads n_kv (groups) */
   int32_t head_dim;   /* d: 64, 128, 192 or 256 */
-  int32_t max_seq;    /* largest seq, a multiple of 64, at most 4096 */
+  int32_t max_seq;    /* largest seq, a multiple of 64, at most 4096 (TPATTN_FUSED_ONLY: 128, 32768) */
   int32_t max_t;      /* largest logical TP degree; must divide n_kv_heads */
   int32_t dtype;      /* TPMLP_BF16 */
-  int32_t reserved;   /* must be 0 */
+  int32_t flags;      /* 0, or TPATTN_FUSED_ONLY */
 } tpattn_config;
+
+/* flags: only the fused attention kernels run.  The workspace then holds no
+ * score square (batch * n_q * seq^2 * 6 bytes on the unfused path), which
+ * lets max_seq go up to 32768 (a multiple of 128); head_dim must be 128,
+ * every forward's seq a multiple of 128 (else TPMLP_ERR_SHAPE), and
+ * tpattn_set_fused(ctx, 0) returns TPMLP_ERR_UNSUPPORTED. */
+#define TPATTN_FUSED_ONLY 1
 
 TPMLP_API size_t tpattn_workspace_bytes(const tpattn_config* cfg);
 TPMLP_API tpmlp_status tpattn_create(const tpattn_config* cfg, void* cuda_stream, tpattn_ctx** out);

@@ -86,13 +86,20 @@ bool attn_config_error(const tpattn_config* c, std::string* why) {
   };
   if (!c) return fail("config is NULL");
   if (c->dtype != TPMLP_BF16) return fail("the attention sublayer runs in bf16");
-  if (c->reserved != 0) return fail("reserved field must be 0");
+  if (c->flags & ~TPATTN_FUSED_ONLY) return fail("unknown flags");
+  const bool fused_only = (c->flags & TPATTN_FUSED_ONLY) != 0;
   if (c->max_tokens < 0 || c->hidden <= 0 || c->hidden % 8 != 0 || c->hidden > 8192)
     return fail("hidden must be a positive multiple of 8, at most 8192");
   if (c->n_heads < 1 || c->n_kv_heads < 1 || c->n_heads % c->n_kv_heads != 0)
     return fail("n_heads must be a positive multiple of n_kv_heads");
   if (c->head_dim < 64 || c->head_dim % 64 != 0 || c->head_dim > 256) return fail("head_dim must be 64, 128, 192 or 256");
-  if (c->max_seq < 64 || c->max_seq % 64 != 0 || c->max_seq > 4096) return fail("max_seq must be a multiple of 64, at most 4096");
+  if (fused_only) {
+    if (c->head_dim != 128) return fail("TPATTN_FUSED_ONLY needs head_dim 128");
+    if (c->max_seq < 128 || c->max_seq % 128 != 0 || c->max_seq > 32768)
+      return fail("with TPATTN_FUSED_ONLY, max_seq must be a multiple of 128, at most 32768");
+  } else if (c->max_seq < 64 || c->max_seq % 64 != 0 || c->max_seq > 4096) {
+    return fail("max_seq must be a multiple of 64, at most 4096");
+  }
   if (c->max_t < 1 || c->n_kv_heads % c->max_t != 0) return fail("max_t must divide n_kv_heads");
   if (c->max_tokens > (int64_t)1 << 24) return fail("max_tokens too large");
   return false;
@@ -102,7 +109,8 @@ AttnLayout attn_layout(const tpattn_config& c) {
   AttnLayout L{};
   const size_t N = (size_t)c.max_tokens, H = (size_t)c.hidden, d = (size_t)c.head_dim;
   const size_t W = (size_t)(c.n_heads + 2 * c.n_kv_heads) * d, Z = (size_t)c.n_heads * d;
-  const size_t SS = N * (size_t)c.max_seq * (size_t)c.n_heads;  // score elements: batch * n_q * S * S
+  // score elements, batch * n_q * S * S (none when only the fused kernels run)
+  const size_t SS = (c.flags & TPATTN_FUSED_ONLY) ? 0 : N * (size_t)c.max_seq * (size_t)c.n_heads;
   size_t off = 0;
   auto take = [&](size_t bytes) {
     const size_t o = off;
@@ -465,6 +473,8 @@ tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const voi
   if (batch < 1 || seq < 64 || seq % 64 != 0 || seq > cf.max_seq || batch * seq > cf.max_tokens)
     return c->fail(TPMLP_ERR_SHAPE, "seq must be a multiple of 64 within max_seq, batch * seq within max_tokens");
   if (t < 1 || t > cf.max_t || cf.n_kv_heads % t != 0) return c->fail(TPMLP_ERR_SHAPE, "t must divide n_kv_heads");
+  if ((cf.flags & TPATTN_FUSED_ONLY) && seq % 128 != 0)
+    return c->fail(TPMLP_ERR_SHAPE, "a fused-only context needs seq to be a multiple of 128");
   if (!x || !norm_w || !w_qkv || !w_o || !b_o || !y) return c->fail(TPMLP_ERR_ARG, "NULL tensor");
   for (const void* p : {x, norm_w, w_qkv, w_o, b_o, (const void*)y})
     if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "tensor not 16-byte aligned");
@@ -663,6 +673,8 @@ tpmlp_status tpattn_bind_master(tpattn_ctx* c, float* norm_w, float* w_qkv, floa
 
 tpmlp_status tpattn_set_fused(tpattn_ctx* c, int32_t enable) {
   if (!c) return TPMLP_ERR_ARG;
+  if (!enable && (c->cfg.flags & TPATTN_FUSED_ONLY))
+    return c->fail(TPMLP_ERR_UNSUPPORTED, "a fused-only context has no workspace for the unfused path");
   c->fused = enable != 0;
   return TPMLP_OK;
 }

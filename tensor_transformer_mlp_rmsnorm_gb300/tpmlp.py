@@ -40,7 +40,7 @@ class AttnConfig(ctypes.Structure):
     """tpattn_config."""
     _fields_ = [("max_tokens", ctypes.c_int64), ("hidden", ctypes.c_int64), ("n_heads", ctypes.c_int32),
                 ("n_kv_heads", ctypes.c_int32), ("head_dim", ctypes.c_int32), ("max_seq", ctypes.c_int32),
-                ("max_t", ctypes.c_int32), ("dtype", ctypes.c_int32), ("reserved", ctypes.c_int32)]
+                ("max_t", ctypes.c_int32), ("dtype", ctypes.c_int32), ("flags", ctypes.c_int32)]
 
 
 class ParamSet(ctypes.Structure):
@@ -111,6 +111,7 @@ _SIGNATURES = {
     "tpmlp_fp8_quantize": (_i32, [_vp, _i64, _i64, _vp, _i64, _vp, _i64, _fp, _vp, _vp]),
     "tpmlp_fp8_gemm": (_i32, [_vp, _i64, _vp, _i64, _i64, _i64, _i64, _fp, _fp, _fp, _i64, _vp, _vp]),
 }
+TPATTN_FUSED_ONLY = 1  # tpattn_config.flags: only the fused attention kernels, no score square
 FP8_SCRATCH_BYTES = 4096
 NOALLOC_LOSS_MAX_BLOCKS = 65536
 
@@ -424,12 +425,13 @@ class TPAttn:
     bf16 tensors on one CUDA device; the workspace is a torch uint8 tensor."""
 
     def __init__(self, max_tokens: int, hidden: int, n_heads: int, n_kv_heads: int, head_dim: int,
-                 max_seq: int, max_t: int = 8, device=None, stream=None):
+                 max_seq: int, max_t: int = 8, device=None, stream=None, fused_only: bool = False):
         dev = torch.device(device) if device is not None else torch.device("cuda")
         if dev.index is None:
             dev = torch.device("cuda", torch.cuda.current_device())
         self.device = dev
-        self.cfg = AttnConfig(max_tokens, hidden, n_heads, n_kv_heads, head_dim, max_seq, max_t, BF16, 0)
+        self.cfg = AttnConfig(max_tokens, hidden, n_heads, n_kv_heads, head_dim, max_seq, max_t, BF16,
+                              TPATTN_FUSED_ONLY if fused_only else 0)
         self.H, self.nq, self.nkv, self.d = hidden, n_heads, n_kv_heads, head_dim
         self.W = (n_heads + 2 * n_kv_heads) * head_dim
         self.stream = stream if stream is not None else torch.cuda.current_stream(dev)

@@ -119,7 +119,7 @@ def test_fp8_and_attention_validation_without_gpu(T):
     good = tpmlp.AttnConfig(512, 256, 4, 2, 64, 128, 2, T.BF16, 0)
     assert L.tpattn_workspace_bytes(ctypes.byref(good)) > 0
     bad = [dict(n_heads=3), dict(head_dim=96), dict(max_seq=100), dict(max_t=4), dict(dtype=T.F32),
-           dict(hidden=12), dict(reserved=1)]
+           dict(hidden=12), dict(flags=2), dict(max_seq=8192)]
     for kw in bad:
         c = tpmlp.AttnConfig(512, 256, 4, 2, 64, 128, 2, T.BF16, 0)
         for k, v in kw.items():
@@ -128,6 +128,29 @@ def test_fp8_and_attention_validation_without_gpu(T):
         ctx = ctypes.c_void_p()
         assert L.tpattn_create(ctypes.byref(c), None, ctypes.byref(ctx)) == T.ERR_SHAPE, kw
         assert L.tpattn_last_error(None)
+
+
+def test_attention_fused_only_config_without_gpu(T):
+    """TPATTN_FUSED_ONLY drops the score square from the workspace and admits
+    sequences past 4096 (multiples of 128), for head_dim 128 only."""
+    from tensor_transformer_mlp_rmsnorm_gb300 import tpmlp
+    L = T.lib()
+    F = tpmlp.TPATTN_FUSED_ONLY
+
+    def ws(**kw):
+        c = tpmlp.AttnConfig(8192, 1024, 8, 2, 128, 2048, 2, T.BF16, 0)
+        for k, v in kw.items():
+            setattr(c, k, v)
+        return L.tpattn_workspace_bytes(ctypes.byref(c))
+
+    plain, fused = ws(), ws(flags=F)
+    square = 8192 * 2048 * 8 * (4 + 2)  # f32 scores and bf16 probabilities, batch * n_q * S^2
+    assert plain - fused >= square
+    assert ws(flags=F, max_seq=16384, max_tokens=16384) > 0
+    assert ws(max_seq=16384, max_tokens=16384) == 0      # only without the square
+    assert ws(flags=F, max_seq=1984) == 0                  # not a multiple of 128
+    assert ws(flags=F, head_dim=64) == 0                   # fused kernels need head_dim 128
+    assert ws(flags=F, max_seq=65536) == 0
 
 
 def test_traffic_record_lookup(tmp_path, monkeypatch):

@@ -27,11 +27,12 @@ def _dev(a):
     return torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
 
 
-def _run(cfg, t, inp, fused=True):
+def _run(cfg, t, inp, fused=True, fused_only=False):
     from tensor_transformer_mlp_rmsnorm_gb300 import TPAttn, tpmlp_create  # noqa: F401
     from tensor_transformer_mlp_rmsnorm_gb300.tpmlp import tpmlp_mse_loss_grad_noalloc
-    m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=max(t, 1))
-    m.set_fused(fused)
+    m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=max(t, 1), fused_only=fused_only)
+    if not fused_only:
+        m.set_fused(fused)
     p = {k: _dev(inp[k]) for k in NAMES}
     masters = {k: torch.from_numpy(np.asarray(inp[k], dtype=np.float32)).cuda() for k in NAMES}
     m.bind_master(masters)
@@ -63,11 +64,11 @@ CASES = [  # batch, seq, hidden, n_q, n_kv, d, t
 FUSABLE = [c for c in CASES if c[5] == 128 and c[1] % 128 == 0]
 
 
-def _case(B, S, H, nq, nkv, d, t, fused):
+def _case(B, S, H, nq, nkv, d, t, fused, fused_only=False):
     cfg = dataclasses.replace(synth.ATTN_CONFIGS["attn_small"], name="case", batch=B, seq=S, hidden=H, n_q=nq,
                               n_kv=nkv, d=d, w_std=0.05)
     inp = synth.make_attn_inputs(cfg, seed=B * 1000 + S)
-    return cfg, inp, _run(cfg, t, inp, fused)
+    return cfg, inp, _run(cfg, t, inp, fused, fused_only)
 
 
 @pytest.mark.parametrize("B,S,H,nq,nkv,d,t", CASES)
@@ -81,8 +82,8 @@ def test_attention_step_unfused_matches_oracle(B, S, H, nq, nkv, d, t):
     _check(B, S, H, nq, nkv, d, t, False)
 
 
-def _check(B, S, H, nq, nkv, d, t, fused):
-    cfg, inp, gpu = _case(B, S, H, nq, nkv, d, t, fused)
+def _check(B, S, H, nq, nkv, d, t, fused, fused_only=False):
+    cfg, inp, gpu = _case(B, S, H, nq, nkv, d, t, fused, fused_only)
     p = {k: inp[k] for k in NAMES}
     ora = O.attn_sharded_step(p, inp["x"], inp["target"], cfg.eps, LR, t, B, nq, nkv)
     compare("y", gpu["y"], ora["y"], "bf16")
@@ -94,6 +95,27 @@ def _check(B, S, H, nq, nkv, d, t, fused):
         w0 = np.asarray(inp[k], dtype=np.float32).astype(np.float64)
         compare("post_step_" + k, new, w0 - LR * ora["grads"][k], "bf16",
                 extra=0.5 * np.spacing(np.abs(new).astype(np.float32)).astype(np.float64))
+
+
+def test_attention_fused_only_long_sequence():
+    """A fused-only context (no score square in its workspace) on a sequence
+    longer than the unfused path admits: 4608 tokens, 36 key blocks."""
+    _check(1, 4608, 256, 2, 1, 128, 1, True, fused_only=True)
+
+
+def test_attention_fused_only_refuses_the_unfused_path():
+    from tensor_transformer_mlp_rmsnorm_gb300 import ERR_SHAPE, ERR_UNSUPPORTED, TPAttn, TPMLPError
+    m = TPAttn(512, 128, 2, 2, 128, 512, max_t=2, fused_only=True)
+    with pytest.raises(TPMLPError) as e:
+        m.set_fused(False)
+    assert e.value.status == ERR_UNSUPPORTED
+    z = torch.zeros(384, 128, dtype=torch.bfloat16, device="cuda")
+    w = torch.zeros(128, dtype=torch.bfloat16, device="cuda")
+    wqkv = torch.zeros(6 * 128, 128, dtype=torch.bfloat16, device="cuda")
+    wo = torch.zeros(128, 256, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(TPMLPError) as e:  # seq 192: a multiple of 64 but not of 128
+        m.forward(z, w, wqkv, wo, w, 1e-6, 1, 2, 192)
+    assert e.value.status == ERR_SHAPE
 
 
 def test_attention_errors():
