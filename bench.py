@@ -348,9 +348,12 @@ def ours_attn(args):
     tg_host = torch.from_numpy(np.ascontiguousarray(inp["target"], dtype=np.float32)).to(bf).pin_memory()
     del inp
     x, target = x_host.to(dev), tg_host.to(dev)
-    m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=t, device=dev)
+    # the fused path needs no score square in its workspace
+    fused_only = args.attn_path == "fused" and cfg.d == 128 and cfg.seq % 128 == 0
+    m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=t, device=dev, fused_only=fused_only)
     m.bind_master(masters)
-    m.set_fused(args.attn_path == "fused")
+    if not fused_only:
+        m.set_fused(args.attn_path == "fused")
     y, dy, dx = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
     grads = m.new_grads()
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
