@@ -432,14 +432,14 @@ constexpr uint32_t QT_BYTES = BQB * 64 * 2;   // [64 queries x 64 d] tile, 8 KB
 // shared memory
 constexpr uint32_t B_SK = 0;                          // K_j: two 16 KB tiles
 constexpr uint32_t B_SV = B_SK + 2 * KT_BYTES;        // V_j
-constexpr int QST = 3;                                // Q / dO / lse2 / D ring stages
+constexpr int QST = 4;                                // Q / dO / lse2 ring stages
 constexpr uint32_t B_SQ = B_SV + 2 * KT_BYTES;        // Q_i ring: QST stages x two 8 KB tiles
 constexpr uint32_t B_SDO = B_SQ + 2 * QST * QT_BYTES; // dO_i ring
 constexpr uint32_t B_SDS = B_SDO + 2 * QST * QT_BYTES; // dS^T: 2 slots x [128 keys x 64 queries], 16 KB each
-constexpr uint32_t B_SLD = B_SDS + 2 * KT_BYTES;      // lse2 / D ring: QST stages x 2 x 64 floats
-constexpr uint32_t BSMEM = B_SLD + QST * 2 * BQB * 4 + 1024;
+constexpr uint32_t B_SLD = B_SDS + 2 * KT_BYTES;      // lse2 ring: QST stages x 64 floats
+constexpr uint32_t BSMEM = B_SLD + QST * BQB * 4 + 1024;
 static_assert(BSMEM <= 232448 - 256, "shared memory budget");
-constexpr uint32_t IN_TX = 4 * QT_BYTES + 2 * BQB * 4;
+constexpr uint32_t IN_TX = 4 * QT_BYTES + BQB * 4;
 // tensor memory columns
 constexpr uint32_t T_S = 0;     // S^T: 2 slots x 64 (P^T over the first 32 columns of its slot)
 constexpr uint32_t T_PQ = 128;  // dP^T, then dQ^T: 2 slots x 64
@@ -558,8 +558,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
           tma_load_2d(smem + B_SDO + (2 * s + t) * QT_BYTES, &map_do, &in_full[s], h * FD + 64 * t, row_q);
         }
         const size_t li = ((size_t)(b * p.nq + h)) * p.S + (size_t)i * BQB;
-        bulk_load_1d(smem + B_SLD + s * 512, p.lse2 + li, BQB * 4, &in_full[s]);
-        bulk_load_1d(smem + B_SLD + s * 512 + 256, p.dsum + li, BQB * 4, &in_full[s]);
+        bulk_load_1d(smem + B_SLD + s * 256, p.lse2 + li, BQB * 4, &in_full[s]);
       }
       if (!ok || *abort_flag) {
         int no_abort = 0;
@@ -674,8 +673,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       if (!(ok = wait_all(&in_full[q3], (n / QST) & 1))) break;
       if (!(ok = wait_all(&s_full[grp], par))) break;
       tc_fence_after();
-      const float* lse2 = reinterpret_cast<const float*>(smem + B_SLD + q3 * 512);
-      const float* dsum = lse2 + 64;
+      const float* lse2 = reinterpret_cast<const float*>(smem + B_SLD + q3 * 256);
       {
         // P^T row (bf16 pairs) over the first 32 columns of the scores, read
         // in two 32-column halves; the half written (columns 0..15, then
@@ -703,6 +701,21 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       }
       tc_fence_before();
       arrive(&p_full[grp]);
+      // D of this step's 64 queries, from global memory (every lane reads the
+      // same values); the loads are in flight while dP^T is awaited
+      float dsum[64];
+      {
+        const float4* d4 = reinterpret_cast<const float4*>(
+            p.dsum + ((size_t)(b * p.nq + step_h(n))) * p.S + (size_t)i * BQB);
+#pragma unroll
+        for (int k = 0; k < 16; ++k) {
+          const float4 t4 = __ldg(d4 + k);
+          dsum[4 * k] = t4.x;
+          dsum[4 * k + 1] = t4.y;
+          dsum[4 * k + 2] = t4.z;
+          dsum[4 * k + 3] = t4.w;
+        }
+      }
       if (!(ok = wait_all(&dp_full[grp], par))) break;
       // dS^T row into the group's slot, once step n - 2's products have read it
       if (!(ok = wait_all(&ds_empty[grp], par ^ 1u))) break;
