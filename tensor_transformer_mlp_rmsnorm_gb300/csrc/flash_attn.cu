@@ -400,8 +400,9 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 //   dS^T = P^T o (dP^T - D_i) / sqrt(d)
 //   dV_j += P^T dO_i               dK_j += dS^T Q_i      dQ_i^T = K_j^T dS^T
 //
-//   warp 0      : TMA producer -- K_j, V_j once; Q_i, dO_i, lse2_i, D_i per
-//                 step into a three-stage ring.  Steps run over the query
+//   warp 0      : TMA producer -- K_j, V_j once; Q_i, dO_i, lse2_i per
+//                 step into a four-stage ring (the row warps read D_i from
+//                 global memory).  Steps run over the query
 //                 blocks from the last one down, the heads of the group
 //                 inner, so the CTAs of one (sequence, group) read the same
 //                 Q / dO blocks at about the same time.
