@@ -251,6 +251,9 @@ class AttnConfig:
 ATTN_CONFIGS = {
     "attn_small": AttnConfig("attn_small", 2, 128, 256, 4, 2, 64, (1, 2)),
     "attn_gpt_h4096": AttnConfig("attn_gpt_h4096", 4, 2048, 4096, 32, 8, 128, (8, 4)),
+    # the same sublayer on one long sequence (fused attention only)
+    "attn_gpt_h4096_s8k": AttnConfig("attn_gpt_h4096_s8k", 1, 8192, 4096, 32, 8, 128, (8, 4)),
+    "attn_gpt_h4096_s32k": AttnConfig("attn_gpt_h4096_s32k", 1, 32768, 4096, 32, 8, 128, (8, 4)),
 }
 
 
