@@ -359,12 +359,20 @@ def ours_attn(args):
     loss = torch.zeros(1, dtype=torch.float32, device=dev)
     loss_host = torch.zeros(1, dtype=torch.float32).pin_memory()
     stream = m.stream
+    adamw = args.optimizer == "adamw"
+    if adamw:
+        m.new_adam_state()
+    nstep = [0]
 
     def step(xb=x, tb=target):
         m.forward(xb, p["norm_w"], p["w_qkv"], p["w_o"], p["b_o"], cfg.eps, t, cfg.batch, cfg.seq, y=y)
         tpmlp_mse_loss_grad_noalloc(y, tb, dy, loss, stream=stream.cuda_stream)
         m.backward(dy, dx=dx, grads=grads)
-        m.sgd_step(cfg.lr)
+        if adamw:
+            nstep[0] += 1
+            m.adamw_step(step=nstep[0], **ADAMW)
+        else:
+            m.sgd_step(cfg.lr)
 
     def barrier():
         if world > 1:
@@ -443,12 +451,15 @@ def ours_attn(args):
                 "frac": ach / pk["hbm_gbs"] if ach else None, "traffic": None, "avg_launch_ms": per_launch}
     gemm_ms = sum(v[0] for k, v in ktimes.items() if k in kflops)
     line = {
-        "metric": "TP-attention fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak",
+        "metric": "TP-attention fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak".replace(
+            "SGD", "AdamW" if adamw else "SGD"),
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
         "config": {"workload": f"{cfg.name}: attention sublayer, {B}x{S} tokens, hidden={H}, {nq} query heads in "
-                               f"{nkv} KV groups, head dim {d}, causal, t={t} logical shards, lr={cfg.lr}",
+                               f"{nkv} KV groups, head dim {d}, causal, t={t} logical shards"
+                               + (f", AdamW {ADAMW}" if adamw else f", lr={cfg.lr}"),
+                   "optimizer": args.optimizer,
                    "attention_kernels": "fused (scores never stored)" if fused else "unfused (scores materialised)",
                    "global_batch": B * world, "seq_len": S, "tokens_per_gpu": N, "t": t,
                    "parallelism": f"replicas x{world}", "l2": "no flush: per-step working set >> 129 MB L2"},

@@ -363,6 +363,32 @@ TPMLP_API tpmlp_status tpattn_set_fused(tpattn_ctx* ctx, int32_t enable);
 /* 1 if the last tpattn_forward ran the fused kernels, 0 if not (or no forward yet). */
 TPMLP_API int32_t tpattn_fused_active(const tpattn_ctx* ctx);
 TPMLP_API tpmlp_status tpattn_sgd_step(tpattn_ctx* ctx, float lr);
+
+/* The attention sublayer's four parameters, one fp32 device tensor each
+ * (shapes as in tpattn_forward); used for the AdamW moments. */
+typedef struct {
+  float* norm_w; /* [H] */
+  float* w_qkv;  /* [(n_q + 2 n_kv) d, H] */
+  float* w_o;    /* [H, n_q d] */
+  float* b_o;    /* [H] */
+} tpattn_param_set;
+
+/* Bind the AdamW moments m and v of the attention parameters: caller-owned
+ * fp32 device tensors, zero before the first step, 16-byte aligned, valid
+ * while tpattn_adamw_step runs.  Two NULL sets unbind.  TPMLP_ERR_ARG on a
+ * missing or misaligned tensor. */
+TPMLP_API tpmlp_status tpattn_bind_adam_state(tpattn_ctx* ctx, const tpattn_param_set* m, const tpattn_param_set* v);
+
+/* One clipped AdamW update of the attention parameters with the gradients of
+ * the last tpattn_backward: the rule of tpmlp_adamw_step (global-norm
+ * clipping over all four gradients, bias-corrected moments, decoupled
+ * weight decay on w_qkv and w_o only).  bf16 parameters are updated through
+ * the bound fp32 masters (tpattn_bind_master) and re-rounded, or through
+ * float when none are bound.  `grad_norm`, if not NULL, is a device float
+ * that receives the norm before clipping.  Two kernels (norm pass, update).
+ * TPMLP_ERR_ORDER before a backward; TPMLP_ERR_ARG without bound moments or
+ * with hyperparameters out of range. */
+TPMLP_API tpmlp_status tpattn_adamw_step(tpattn_ctx* ctx, const tpmlp_adamw_params* hp, float* grad_norm);
 TPMLP_API tpmlp_status tpattn_sync(tpattn_ctx* ctx);
 TPMLP_API tpmlp_status tpattn_set_timing(tpattn_ctx* ctx, int32_t enable);
 TPMLP_API int32_t tpattn_read_kernel_times(tpattn_ctx* ctx, float* ms, int64_t* launches, int32_t n);

@@ -413,7 +413,7 @@ def shape_trace(S: int, B: int, H: int, F: int, t: int) -> dict:
 ADAMW_DEFAULTS = {"lr": 1.5e-4, "beta1": 0.9, "beta2": 0.999, "eps": 1e-8, "weight_decay": 0.1,
                   "max_grad_norm": 1.0}
 CLIP_EPS = 1e-6
-DECAYED = ("w_gate_up", "w_1", "w_down")
+DECAYED = ("w_gate_up", "w_1", "w_down", "w_qkv", "w_o")  # MLP and attention projection matrices
 REPLICATED = ("norm_w", "b_down")
 
 

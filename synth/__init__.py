@@ -269,3 +269,21 @@ def make_attn_inputs(cfg: AttnConfig, seed: int = 1234) -> dict:
             "norm_w": r(normal(seed, 42, (H,), 1.0, 0.1)), "w_qkv": r(normal(seed, 43, (W, H), 0.0, cfg.w_std)),
             "w_o": r(normal(seed, 44, (H, cfg.n_q * d), 0.0, cfg.w_std)),
             "b_o": r(normal(seed, 45, (H,), 0.0, 0.01))}
+
+
+def make_attn_optimizer_state(cfg: AttnConfig, seed: int = 1234, grad_std: float = 1e-4, m_std: float = 5e-5,
+                              v_std: float = 1e-4) -> dict:
+    """Seeded optimizer-step inputs for the attention parameters, drawn as in
+    ``make_optimizer_state``: g ~ N(0, grad_std), m ~ N(0, m_std), v =
+    |N(0, v_std)|^2, fp32-representable float64.  Streams 150 + 3k, 151 + 3k,
+    152 + 3k for the k-th of norm_w, w_qkv, w_o, b_o."""
+    H, d = cfg.hidden, cfg.d
+    shapes = {"norm_w": (H,), "w_qkv": ((cfg.n_q + 2 * cfg.n_kv) * d, H), "w_o": (H, cfg.n_q * d), "b_o": (H,)}
+    f32 = lambda a: a.astype(np.float32).astype(np.float64)
+    out = {"grad": {}, "m": {}, "v": {}}
+    for k, name in enumerate(("norm_w", "w_qkv", "w_o", "b_o")):
+        shp = shapes[name]
+        out["grad"][name] = f32(normal(seed, 150 + 3 * k, shp, 0.0, grad_std))
+        out["m"][name] = f32(normal(seed, 151 + 3 * k, shp, 0.0, m_std))
+        out["v"][name] = f32(np.square(normal(seed, 152 + 3 * k, shp, 0.0, v_std)))
+    return out

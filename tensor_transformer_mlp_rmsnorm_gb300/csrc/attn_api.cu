@@ -13,6 +13,7 @@
 //             gemm_dgrad_norm (every head's contribution summed on chip: the
 //             f all-reduce) -> rmsnorm_bwd_residual -> colsum_finalize
 //   sgd     : sgd_update
+//   adamw   : grad_sqnorm -> adamw_update
 // Fused path (head_dim 128, seq % 128 == 0; the default): gemm_scores ->
 // softmax_fwd -> gemm_pv become flash_attn_fwd (Z and each row's log-sum-exp),
 // and gemm_dp .. group_sum become flash_bwd_prep (D = rowsum(dZ o Z), dQ
@@ -60,6 +61,8 @@ enum AttnKernel {
   A_FLASH_BWD_PREP,
   A_FLASH_BWD,
   A_FLASH_DQ_CAST,
+  A_GRAD_NORM,
+  A_ADAMW,
   A_COUNT
 };
 const char* const kAttnNames[A_COUNT] = {
@@ -67,7 +70,8 @@ const char* const kAttnNames[A_COUNT] = {
     "gemm_out_proj",   "gemm_dz",         "gemm_wgrad_out",  "gemm_dp",          "gemm_dv",
     "group_sum",       "softmax_bwd",     "gemm_dq",         "gemm_dk",          "gemm_wgrad_qkv",
     "gemm_dgrad_norm", "rmsnorm_bwd_residual", "colsum_finalize", "sgd_update",
-    "flash_attn_fwd",  "flash_bwd_prep",  "flash_attn_bwd",  "flash_dq_cast"};
+    "flash_attn_fwd",  "flash_bwd_prep",  "flash_attn_bwd",  "flash_dq_cast",   "grad_sqnorm",
+    "adamw_update"};
 
 constexpr int MAX_PARTS = 1024;
 thread_local std::string g_attn_err;
@@ -76,7 +80,7 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnLayout {
-  size_t status, nrm, rstd, qkv, z, dz, dqkv, dnrm, scores, probs, dkv_head, lse2, dsum, part_dw, part_db, total;
+  size_t status, nrm, rstd, qkv, z, dz, dqkv, dnrm, scores, probs, dkv_head, lse2, dsum, part_dw, part_db, norm_part, total;
 };
 
 bool attn_config_error(const tpattn_config* c, std::string* why) {
@@ -132,6 +136,7 @@ AttnLayout attn_layout(const tpattn_config& c) {
   L.dsum = take(N * (size_t)c.n_heads * 4);  // fused path: rowsum(dZ o Z), same layout
   L.part_dw = take((size_t)MAX_PARTS * H * 4);
   L.part_db = take((size_t)MAX_PARTS * H * 4);
+  L.norm_part = take((size_t)MAX_NORM_PARTS * sizeof(double));  // AdamW: per-block partial sums of g^2
   L.total = off;
   return L;
 }
@@ -150,6 +155,8 @@ struct tpattn_ctx {
   const void *x = nullptr, *norm_w = nullptr, *w_qkv = nullptr, *w_o = nullptr, *b_o = nullptr;
   float *g_norm_w = nullptr, *g_w_qkv = nullptr, *g_w_o = nullptr, *g_b_o = nullptr;
   float *m_norm_w = nullptr, *m_w_qkv = nullptr, *m_w_o = nullptr, *m_b_o = nullptr;
+  tpattn_param_set adam_m{}, adam_v{};
+  bool adam_bound = false;
   bool timing = false;
   struct Rec {
     int id;
@@ -695,6 +702,67 @@ tpmlp_status tpattn_sgd_step(tpattn_ctx* c, float lr) {
   a.seg[a.nseg++] = SgdSeg{c->m_w_o, c->g_w_o, const_cast<void*>(c->w_o), H * Zc};
   a.seg[a.nseg++] = SgdSeg{c->m_b_o, c->g_b_o, const_cast<void*>(c->b_o), H};
   return c->run(A_SGD, [&] { return launch_sgd(1, a, c->num_sms, c->stream); });
+}
+
+tpmlp_status tpattn_bind_adam_state(tpattn_ctx* c, const tpattn_param_set* m, const tpattn_param_set* v) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!m && !v) {
+    c->adam_m = tpattn_param_set{};
+    c->adam_v = tpattn_param_set{};
+    c->adam_bound = false;
+    return TPMLP_OK;
+  }
+  if (!m || !v) return c->fail(TPMLP_ERR_ARG, "bind both moment sets or neither");
+  for (const tpattn_param_set* s : {m, v}) {
+    if (!s->norm_w || !s->w_qkv || !s->w_o || !s->b_o) return c->fail(TPMLP_ERR_ARG, "a moment tensor is missing");
+    for (const void* p : {(const void*)s->norm_w, (const void*)s->w_qkv, (const void*)s->w_o, (const void*)s->b_o})
+      if (!a16(p)) return c->fail(TPMLP_ERR_ARG, "moment tensor not 16-byte aligned");
+  }
+  c->adam_m = *m;
+  c->adam_v = *v;
+  c->adam_bound = true;
+  return TPMLP_OK;
+}
+
+// The MLP's clipped AdamW (norm pass over every gradient, then the update)
+// over the attention sublayer's four parameters; weight decay on the two
+// projection matrices only.
+tpmlp_status tpattn_adamw_step(tpattn_ctx* c, const tpmlp_adamw_params* hp, float* grad_norm) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (!hp) return c->fail(TPMLP_ERR_ARG, "hyperparameters are NULL");
+  if (!c->bwd_done) return c->fail(TPMLP_ERR_ORDER, "adamw_step before backward");
+  if (!c->adam_bound) return c->fail(TPMLP_ERR_ARG, "AdamW moments are not bound");
+  if (!std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay) || !std::isfinite(hp->max_grad_norm) ||
+      !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f) ||
+      !(hp->eps >= 0.f && std::isfinite(hp->eps)) || hp->step < 1)
+    return c->fail(TPMLP_ERR_ARG, "AdamW hyperparameter out of range");
+  if (grad_norm && (reinterpret_cast<uintptr_t>(grad_norm) & 3u))
+    return c->fail(TPMLP_ERR_ARG, "grad_norm not 4-byte aligned");
+  const tpattn_config& cf = c->cfg;
+  const int64_t H = cf.hidden, d = cf.head_dim, W = (int64_t)(cf.n_heads + 2 * cf.n_kv_heads) * d,
+                Zc = (int64_t)cf.n_heads * d;
+  const double bc1 = 1.0 - std::pow((double)hp->beta1, (double)hp->step);
+  const double bc2 = 1.0 - std::pow((double)hp->beta2, (double)hp->step);
+  AdamArgs a{};
+  a.beta1 = hp->beta1;
+  a.beta2 = hp->beta2;
+  a.one_m_beta1 = (float)(1.0 - (double)hp->beta1);
+  a.one_m_beta2 = (float)(1.0 - (double)hp->beta2);
+  a.step_size = (float)((double)hp->lr / bc1);
+  a.inv_sqrt_bc2 = (float)(1.0 / std::sqrt(bc2));
+  a.eps = hp->eps;
+  a.max_norm = hp->max_grad_norm;
+  a.part = c->wsp<double>(c->L.norm_part);
+  a.grad_norm = grad_norm;
+  const float lr_wd = (float)((double)hp->lr * (double)hp->weight_decay);
+  const tpattn_param_set &M = c->adam_m, &V = c->adam_v;
+  a.seg[a.nseg++] = AdamSeg{c->m_norm_w, c->g_norm_w, const_cast<void*>(c->norm_w), M.norm_w, V.norm_w, H, 0.0f};
+  a.seg[a.nseg++] = AdamSeg{c->m_w_qkv, c->g_w_qkv, const_cast<void*>(c->w_qkv), M.w_qkv, V.w_qkv, W * H, lr_wd};
+  a.seg[a.nseg++] = AdamSeg{c->m_w_o, c->g_w_o, const_cast<void*>(c->w_o), M.w_o, V.w_o, H * Zc, lr_wd};
+  a.seg[a.nseg++] = AdamSeg{c->m_b_o, c->g_b_o, const_cast<void*>(c->b_o), M.b_o, V.b_o, H, 0.0f};
+  const int nb = adam_blocks(a, c->num_sms);
+  ATTN_TRY(c->run(A_GRAD_NORM, [&] { return launch_grad_sqnorm(a, nb, c->stream); }));
+  return c->run(A_ADAMW, [&] { return launch_adamw(1, a, nb, c->stream); });
 }
 
 tpmlp_status tpattn_sync(tpattn_ctx* c) {

@@ -49,6 +49,12 @@ class ParamSet(ctypes.Structure):
                 ("w_down", ctypes.c_void_p), ("b_down", ctypes.c_void_p)]
 
 
+class AttnParamSet(ctypes.Structure):
+    """tpattn_param_set: one device float* per attention parameter."""
+    _fields_ = [("norm_w", ctypes.c_void_p), ("w_qkv", ctypes.c_void_p), ("w_o", ctypes.c_void_p),
+                ("b_o", ctypes.c_void_p)]
+
+
 class AdamWParams(ctypes.Structure):
     """tpmlp_adamw_params."""
     _fields_ = [("lr", ctypes.c_float), ("beta1", ctypes.c_float), ("beta2", ctypes.c_float),
@@ -98,6 +104,8 @@ _SIGNATURES = {
     "tpattn_backward": (_i32, [_vp, _vp, _vp, _fp, _fp, _fp, _fp]),
     "tpattn_bind_master": (_i32, [_vp, _fp, _fp, _fp, _fp]),
     "tpattn_sgd_step": (_i32, [_vp, _f32]),
+    "tpattn_bind_adam_state": (_i32, [_vp, ctypes.POINTER(AttnParamSet), ctypes.POINTER(AttnParamSet)]),
+    "tpattn_adamw_step": (_i32, [_vp, ctypes.POINTER(AdamWParams), _fp]),
     "tpattn_set_fused": (_i32, [_vp, _i32]),
     "tpattn_fused_active": (_i32, [_vp]),
     "tpattn_sync": (_i32, [_vp]),
@@ -506,6 +514,42 @@ class TPAttn:
 
     def sgd_step(self, lr: float):
         _acheck(lib().tpattn_sgd_step(self.ctx, float(lr)), self.ctx)
+
+    def _param_set(self, d: dict, what: str) -> AttnParamSet:
+        f32 = torch.float32
+        return AttnParamSet(self._t(d["norm_w"], (self.H,), f32, f"{what}.norm_w"),
+                            self._t(d["w_qkv"], (self.W, self.H), f32, f"{what}.w_qkv"),
+                            self._t(d["w_o"], (self.H, self.nq * self.d), f32, f"{what}.w_o"),
+                            self._t(d["b_o"], (self.H,), f32, f"{what}.b_o"))
+
+    def new_adam_state(self):
+        """Zeroed first and second moments shaped like the parameters (fp32), bound to this context."""
+        m = {k: torch.zeros_like(v) for k, v in self.new_grads().items()}
+        v = {k: torch.zeros_like(t) for k, t in m.items()}
+        self.bind_adam_state(m, v)
+        return m, v
+
+    def bind_adam_state(self, m: dict | None, v: dict | None):
+        if m is None and v is None:
+            _acheck(lib().tpattn_bind_adam_state(self.ctx, None, None), self.ctx)
+            self._adam = None
+            return
+        ms, vs = self._param_set(m, "m"), self._param_set(v, "v")
+        _acheck(lib().tpattn_bind_adam_state(self.ctx, ctypes.byref(ms), ctypes.byref(vs)), self.ctx)
+        self._adam = (m, v)  # keep the tensors alive while bound
+
+    def adamw_step(self, lr: float, step: int, beta1: float = 0.9, beta2: float = 0.999, eps: float = 1e-8,
+                   weight_decay: float = 0.1, max_grad_norm: float = 1.0, grad_norm=None):
+        """One clipped AdamW update; returns the device float holding the global gradient norm."""
+        if grad_norm is None:
+            if getattr(self, "_gn", None) is None:
+                self._gn = torch.zeros(1, dtype=torch.float32, device=self.device)
+            grad_norm = self._gn
+        hp = AdamWParams(float(lr), float(beta1), float(beta2), float(eps), float(weight_decay),
+                         float(max_grad_norm), int(step))
+        _acheck(lib().tpattn_adamw_step(self.ctx, ctypes.byref(hp),
+                                        self._t(grad_norm, (1,), torch.float32, "grad_norm")), self.ctx)
+        return grad_norm
 
     def sync(self):
         _acheck(lib().tpattn_sync(self.ctx), self.ctx)

@@ -28,7 +28,8 @@ def test_header_declares_the_entry_points():
     for must in ("tpmlp_forward", "tpmlp_backward", "tpmlp_sgd_step", "tpmlp_mse_loss_grad", "tpmlp_create",
                  "tpmlp_workspace_bytes", "tpmlp_bind_workspace", "tpmlp_sync", "tpmlp_destroy",
                  "tpmlp_adamw_step", "tpmlp_set_sequence_parallel", "tpmlp_set_precision", "tpmlp_fp8_quantize",
-                 "tpmlp_fp8_gemm", "tpattn_forward", "tpattn_backward", "tpattn_sgd_step"):
+                 "tpmlp_fp8_gemm", "tpattn_forward", "tpattn_backward", "tpattn_sgd_step",
+                 "tpattn_bind_adam_state", "tpattn_adamw_step"):
         assert must in names
 
 

@@ -114,6 +114,22 @@ def test_adamw_zero_gradient_is_pure_decay():
     assert out["grad_norm"] == 0.0 and out["clip"] == 1.0
 
 
+def test_adamw_attention_parameters_decay_like_the_mlp_ones():
+    # the attention sublayer's projection matrices (W_qkv, W_out) decay, its
+    # norm weight and output bias do not: zero gradient and moments leave
+    # exactly w (1 - lr wd) or w
+    rng = np.random.default_rng(5)
+    p = {"norm_w": rng.standard_normal(4), "w_qkv": rng.standard_normal((6, 4)),
+         "w_o": rng.standard_normal((4, 2)), "b_o": rng.standard_normal(4)}
+    z = {k: np.zeros_like(v) for k, v in p.items()}
+    out = O.adamw(p, z, dict(z), dict(z), 3, lr=0.05, beta1=0.9, beta2=0.999, eps=1e-8, weight_decay=0.4,
+                  max_grad_norm=1.0)
+    for k in ("w_qkv", "w_o"):
+        np.testing.assert_array_equal(out["params"][k], p[k] - 0.05 * 0.4 * p[k])
+    for k in ("norm_w", "b_o"):
+        np.testing.assert_array_equal(out["params"][k], p[k])
+
+
 def test_adam_step_is_scale_free_without_eps():
     rng = np.random.default_rng(11)
     w = rng.standard_normal(9)
