@@ -420,7 +420,7 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 // element-wise work runs under the products of the other group's step:
 // tensor memory holds S^T / P^T per slot, dP^T per slot (overwritten by the
 // step's dQ^T once the group has read dP^T), dV_j and dK_j.  Per step n the
-// MMA warp issues dV_n, dP^T_{n+1}, dK_n and dQ^T_n, then S^T_{n+2}.
+// MMA warp issues dV_n, dP^T_{n+1}, dQ^T_n and dK_n, then S^T_{n+2}.
 // The same shared-memory tile of Q, dO, K or dS^T serves as a K-major operand
 // of one product and an MN-major operand of another: a 128-byte swizzled tile
 // of 64-element rows is both.
@@ -633,19 +633,21 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       }
       __syncwarp();
       if (n + 1 < nsteps && !(ok = issue_dp(n + 1))) break;
-      // dK += dS^T Q_n ; dQ^T_n = K^T dS^T over the slot's dP^T, which the group has read
+      // dQ^T_n = K^T dS^T over the slot's dP^T, which the group has read; then
+      // dK += dS^T Q_n.  dQ^T goes first so that its slot, which dP^T_{n+2}
+      // needs next, is read out while dK_n and S^T_{n+2} keep the tensor core busy.
       if (!(ok = wait_all(&ds_full[s], par))) break;
       tc_fence_after();
       if (elect_one()) {
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)
-          tc_mma_f16(tmem_base + T_DK, desc_advance(sds_k, kk * 32), desc_advance(sq, kk * 2048), IDESC_KV,
-                     (n > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk)
           tc_mma_f16(tmem_base + T_PQ + s * BQB, desc_advance(k_mdesc, kk * 2048), desc_advance(sds_m, kk * 2048),
                      IDESC_DQ, kk > 0 ? 1u : 0u);
         tc_commit(&dq_full[s]);
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)
+          tc_mma_f16(tmem_base + T_DK, desc_advance(sds_k, kk * 32), desc_advance(sq, kk * 2048), IDESC_KV,
+                     (n > 0 || kk > 0) ? 1u : 0u);
         tc_commit(&ds_empty[s]);
         tc_commit(&in_empty[q]);
         if (n + 1 == nsteps) tc_commit(&acc_full);
