@@ -808,48 +808,79 @@ __global__ void __launch_bounds__(BTHREADS, 1)
   }
 }
 
-// D[(b nq + h) S + q] = sum_c dO[b S + q, h d + c] O[b S + q, h d + c] (one
-// warp per (token, head)); the f32 dQ accumulator is cleared alongside.
+// D[(b nq + h) S + q] = sum_c dO[b S + q, h d + c] O[b S + q, h d + c], and
+// the f32 dQ accumulator cleared alongside.  d = 128: a block walks whole
+// token rows (nq d contiguous elements); each half-warp takes one head of
+// the row, a lane 8 elements (16-byte loads), and sums the products with
+// four shuffles.  Two chunks per thread per pass keep four loads in flight.
 __global__ void __launch_bounds__(256) flash_bwd_prep_kernel(const __nv_bfloat16* __restrict__ dz,
                                                              const __nv_bfloat16* __restrict__ z,
                                                              float* __restrict__ dsum, float* __restrict__ dq_acc,
-                                                             int64_t N, int S, int nq, int d) {
-  const int lane = threadIdx.x & 31;
-  const int64_t nw = (int64_t)gridDim.x * (blockDim.x >> 5);
-  const int64_t Zc = (int64_t)nq * d;
-  for (int64_t w = (int64_t)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5); w < N * nq; w += nw) {
-    const int64_t tok = w / nq;
-    const int h = (int)(w % nq);
-    const int64_t base = tok * Zc + (int64_t)h * d;
-    float acc = 0.0f;
-    for (int c = 4 * lane; c < d; c += 128) {
-      float a[4], o[4];
-      load4(dz + base + c, a);
-      load4(z + base + c, o);
-      acc += a[0] * o[0] + a[1] * o[1] + a[2] * o[2] + a[3] * o[3];
+                                                             int64_t N, int S, int nq) {
+  const int chunks = nq * 16;  // 8-element chunks per token row
+  for (int64_t tok = blockIdx.x; tok < N; tok += gridDim.x) {
+    const int64_t row0 = tok * (int64_t)chunks * 8;
+    const int b = (int)(tok / S), qi = (int)(tok % S);
+    // the loop runs warp-uniformly (the shuffles need every lane); chunks is a
+    // multiple of 16, so each half-warp is wholly in or out of range
+    for (int base = threadIdx.x & ~31; base < chunks; base += 2 * blockDim.x) {
+      const int k0 = base + (threadIdx.x & 31), k1 = k0 + blockDim.x;
+      const bool has0 = k0 < chunks, has1 = k1 < chunks;
+      float a0[8], o0[8], a1[8], o1[8];
+      if (has0) {
+        Vec<__nv_bfloat16>::load(dz + row0 + 8 * k0, a0);
+        Vec<__nv_bfloat16>::load(z + row0 + 8 * k0, o0);
+      }
+      if (has1) {
+        Vec<__nv_bfloat16>::load(dz + row0 + 8 * k1, a1);
+        Vec<__nv_bfloat16>::load(z + row0 + 8 * k1, o1);
+      }
       const float zero[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-      store4(dq_acc + base + c, zero);
-    }
+      float s0 = 0.0f, s1 = 0.0f;
+      if (has0) {
+        store4(dq_acc + row0 + 8 * k0, zero);
+        store4(dq_acc + row0 + 8 * k0 + 4, zero);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
-    if (lane == 0) {
-      const int64_t b = tok / S, qi = tok % S;
-      dsum[(b * nq + h) * S + qi] = acc;
+        for (int i = 0; i < 8; ++i) s0 = fmaf(a0[i], o0[i], s0);
+      }
+      if (has1) {
+        store4(dq_acc + row0 + 8 * k1, zero);
+        store4(dq_acc + row0 + 8 * k1 + 4, zero);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) s1 = fmaf(a1[i], o1[i], s1);
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) {
+        s0 += __shfl_xor_sync(0xffffffffu, s0, o);
+        s1 += __shfl_xor_sync(0xffffffffu, s1, o);
+      }
+      if (has0 && (k0 & 15) == 0) dsum[((int64_t)b * nq + (k0 >> 4)) * S + qi] = s0;
+      if (has1 && (k1 & 15) == 0) dsum[((int64_t)b * nq + (k1 >> 4)) * S + qi] = s1;
     }
   }
 }
 
-// dqkv[:, 0 : nq d] = bf16(dQ accumulator).
+// dqkv[:, 0 : Zc] = bf16(dQ accumulator): a block walks whole rows, a
+// thread 8 floats (two 16-byte loads, one 16-byte store), two chunks per pass.
 __global__ void __launch_bounds__(256) flash_dq_cast_kernel(const float* __restrict__ dq_acc,
                                                             __nv_bfloat16* __restrict__ dqkv, int64_t N, int64_t Zc,
                                                             int64_t ld) {
-  const int64_t n4 = N * Zc / 4;
-  for (int64_t t = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; t < n4; t += (int64_t)gridDim.x * blockDim.x) {
-    const int64_t e = 4 * t;
-    const int64_t row = e / Zc, col = e % Zc;
-    float v[4];
-    load4(dq_acc + e, v);
-    store4(dqkv + row * ld + col, v);
+  const int chunks = (int)(Zc / 8);
+  for (int64_t row = blockIdx.x; row < N; row += gridDim.x) {
+    const float* src = dq_acc + row * Zc;
+    __nv_bfloat16* dst = dqkv + row * ld;
+    for (int k0 = threadIdx.x; k0 < chunks; k0 += 2 * blockDim.x) {
+      const int k1 = k0 + blockDim.x;
+      float v0[8], v1[8];
+      load4(src + 8 * k0, v0);
+      load4(src + 8 * k0 + 4, v0 + 4);
+      if (k1 < chunks) {
+        load4(src + 8 * k1, v1);
+        load4(src + 8 * k1 + 4, v1 + 4);
+      }
+      Vec<__nv_bfloat16>::store(dst + 8 * k0, v0);
+      if (k1 < chunks) Vec<__nv_bfloat16>::store(dst + 8 * k1, v1);
+    }
   }
 }
 
@@ -888,14 +919,13 @@ cudaError_t launch_flash_attn_fwd(const void* qkv, int batch, int S, int nq, int
 
 cudaError_t launch_flash_bwd_prep(const void* dz, const void* z, float* dsum, float* dq_acc, int batch, int S, int nq,
                                   int d, int num_sms, cudaStream_t st) {
-  if (d % 4 != 0 || d > 128) return cudaErrorInvalidValue;
-  const int64_t N = (int64_t)batch * S, warps = N * nq;
-  if (warps <= 0) return cudaSuccess;
-  int64_t blocks = (warps + 7) / 8;
-  if (blocks > 16LL * num_sms) blocks = 16LL * num_sms;
+  if (d != FD) return cudaErrorInvalidValue;
+  const int64_t N = (int64_t)batch * S;
+  if (N <= 0 || nq <= 0) return cudaSuccess;
+  const int64_t blocks = N < 8LL * num_sms ? N : 8LL * num_sms;
   flash_bwd_prep_kernel<<<(unsigned)blocks, 256, 0, st>>>(static_cast<const __nv_bfloat16*>(dz),
                                                           static_cast<const __nv_bfloat16*>(z), dsum, dq_acc, N, S,
-                                                          nq, d);
+                                                          nq);
   return cudaGetLastError();
 }
 
@@ -940,11 +970,9 @@ cudaError_t launch_flash_attn_bwd(const void* qkv, const void* dz, const float* 
 
 cudaError_t launch_flash_dq_cast(const float* dq_acc, void* dqkv, int64_t N, int64_t Zc, int64_t ld, int num_sms,
                                  cudaStream_t st) {
-  if (Zc % 4 != 0) return cudaErrorInvalidValue;
-  const int64_t n4 = N * Zc / 4;
-  if (n4 <= 0) return cudaSuccess;
-  int64_t blocks = (n4 + 255) / 256;
-  if (blocks > 8LL * num_sms) blocks = 8LL * num_sms;
+  if (Zc % 8 != 0 || ld % 8 != 0 || Zc / 8 > (1LL << 30)) return cudaErrorInvalidValue;
+  if (N <= 0 || Zc <= 0) return cudaSuccess;
+  const int64_t blocks = N < 8LL * num_sms ? N : 8LL * num_sms;
   flash_dq_cast_kernel<<<(unsigned)blocks, 256, 0, st>>>(dq_acc, static_cast<__nv_bfloat16*>(dqkv), N, Zc, ld);
   return cudaGetLastError();
 }

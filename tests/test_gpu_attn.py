@@ -60,6 +60,8 @@ CASES = [  # batch, seq, hidden, n_q, n_kv, d, t
     (3, 128, 256, 2, 2, 128, 2),
     (1, 384, 1024, 8, 4, 128, 4),
     (2, 256, 512, 4, 1, 128, 1),
+    # an odd number of query heads: a token row of dZ holds 3 x 16 chunks of 8
+    (1, 256, 384, 3, 1, 128, 1),
 ]
 FUSABLE = [c for c in CASES if c[5] == 128 and c[1] % 128 == 0]
 
