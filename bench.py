@@ -257,6 +257,26 @@ def cpu_oracle_tflops(cfg, inp, budget_s: float, min_tokens: int = 16, max_token
     return flops / dt / 1e12, n, dt
 
 
+def cpu_attn_oracle_tflops(cfg, inp, budget_s: float, min_seq: int = 128, max_seq: int = 2048):
+    """Time the attention oracle's dense step on the first tokens of sequence 0 (a causal prefix
+    is a complete smaller problem), doubling the prefix up to about budget_s."""
+    from oracle import tpmlp_oracle as O
+    p = {k: inp[k] for k in ("norm_w", "w_qkv", "w_o", "b_o")}
+
+    def run(n):
+        t0 = time.perf_counter()
+        O.attn_dense_step(p, inp["x"][:n], inp["target"][:n], cfg.eps, cfg.lr, 1, cfg.n_q, cfg.n_kv)
+        return time.perf_counter() - t0
+
+    n = min(min_seq, cfg.seq)
+    dt = run(n)
+    while dt < budget_s / 4 and n < min(max_seq, cfg.seq):
+        n = min(max_seq, cfg.seq, n * 2)
+        dt = run(n)
+    flops = dataclasses.replace(cfg, batch=1, seq=n).gemm_flops
+    return flops / dt / 1e12, n, dt
+
+
 def host_cores():
     try:
         return len(os.sched_getaffinity(0))
@@ -346,6 +366,7 @@ def ours_attn(args):
     masters = {k: torch.from_numpy(np.ascontiguousarray(inp[k], dtype=np.float32)).to(dev) for k in names}
     x_host = torch.from_numpy(np.ascontiguousarray(inp["x"], dtype=np.float32)).to(bf).pin_memory()
     tg_host = torch.from_numpy(np.ascontiguousarray(inp["target"], dtype=np.float32)).to(bf).pin_memory()
+    cpu_inp = inp if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     del inp
     x, target = x_host.to(dev), tg_host.to(dev)
     # the fused path needs no score square in its workspace
@@ -450,6 +471,12 @@ def ours_attn(args):
         roof = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": ach / pk["hbm_gbs"] if ach else None, "traffic": None, "avg_launch_ms": per_launch}
     gemm_ms = sum(v[0] for k, v in ktimes.items() if k in kflops)
+    cpu = None
+    if cpu_inp is not None:
+        v, n, dt = cpu_attn_oracle_tflops(cfg, cpu_inp, budget_s=args.cpu_budget)
+        cpu = {"value": v, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
+               "sample": f"dense fwd+loss+bwd+SGD of the first {n} tokens of sequence 0 (a causal prefix) "
+                         f"with the full weights, float64 numpy, {dt:.1f} s"}
     line = {
         "metric": "TP-attention fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak".replace(
             "SGD", "AdamW" if adamw else "SGD"),
@@ -467,7 +494,7 @@ def ours_attn(args):
                              "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"], "source": pk_src},
         "gemm_only_tflops": flops * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][0])},
-        "roofline": roof, "cpu_baseline": None,
+        "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": flops * e2e_steps * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 4, "steps": e2e_steps,
                 "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)"},
