@@ -198,28 +198,30 @@ __global__ void __launch_bounds__(FTHREADS, 1)
     auto wait_all = [&](uint64_t* bar, uint32_t par) -> int {
       return __all_sync(0xffffffffu, mbar_wait(bar, par, abort_flag, p.status, STATUS_TIMEOUT, FWAIT_NS));
     };
-    // S_x = Q_x K_j^T into tile x's score columns
-    auto issue_s = [&](int x, int j) {
+    // S_x = Q_x K_j^T into tile x's score columns (issued by the elected lane)
+    auto mma_s = [&](int x, int j) {
       const uint64_t qa = desc_advance(q_desc, x * OPND_BYTES), kb = desc_advance(k_desc, (j & 1) * OPND_BYTES);
-      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16(tmem_base + x * FB, desc_advance(qa, (kk >> 2) * TILE_BYTES + (kk & 3) * 32),
-                     desc_advance(kb, (kk >> 2) * TILE_BYTES + (kk & 3) * 32), IDESC_S, kk > 0 ? 1u : 0u);
-        tc_commit(&s_full[x]);
-      }
-      __syncwarp();
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_f16(tmem_base + x * FB, desc_advance(qa, (kk >> 2) * TILE_BYTES + (kk & 3) * 32),
+                   desc_advance(kb, (kk >> 2) * TILE_BYTES + (kk & 3) * 32), IDESC_S, kk > 0 ? 1u : 0u);
+      tc_commit(&s_full[x]);
     };
     // O_x += P_x V_j, P_x from tile x's score columns (bf16 pairs, 8 columns per K = 16)
-    auto issue_pv = [&](int x, int j, bool last) {
+    auto mma_pv = [&](int x, int j, bool last) {
       const uint64_t vb = desc_advance(v_desc, (j & 1) * OPND_BYTES);
-      if (elect_one()) {
 #pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-          tc_mma_f16_ts(tmem_base + 256 + x * FD, tmem_base + x * FB + kk * 8, desc_advance(vb, kk * 2048), IDESC_PV,
-                        (j > 0 || kk > 0) ? 1u : 0u);
-        if (last) tc_commit(&o_full[x]);
-      }
+      for (int kk = 0; kk < 8; ++kk)
+        tc_mma_f16_ts(tmem_base + 256 + x * FD, tmem_base + x * FB + kk * 8, desc_advance(vb, kk * 2048), IDESC_PV,
+                      (j > 0 || kk > 0) ? 1u : 0u);
+      if (last) tc_commit(&o_full[x]);
+    };
+    auto issue_s = [&](int x, int j) {
+      if (elect_one()) mma_s(x, j);
+      __syncwarp();
+    };
+    auto issue_pv = [&](int x, int j, bool last) {
+      if (elect_one()) mma_pv(x, j, last);
       __syncwarp();
     };
     int ok = wait_all(&q_full, 0) && wait_all(&k_full[0], 0);
@@ -245,10 +247,14 @@ __global__ void __launch_bounds__(FTHREADS, 1)
       if (has_b) {
         if (!(ok = wait_all(&p_full[1], j & 1))) break;
         tc_fence_after();
-        issue_pv(1, j, j + 1 == nk_b);
-        if (j + 1 < nk_b) issue_s(1, j + 1);
       }
+      // tile B's products and the ring releases in one elected issue (one
+      // issue point fewer per key block: 2% on the 2048-token workload)
       if (elect_one()) {
+        if (has_b) {
+          mma_pv(1, j, j + 1 == nk_b);
+          if (j + 1 < nk_b) mma_s(1, j + 1);
+        }
         tc_commit(&v_empty[s]);
         if (next) tc_commit(&k_empty[(j + 1) & 1]);
       }
