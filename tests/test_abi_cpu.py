@@ -173,3 +173,20 @@ def test_traffic_record_lookup(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w", 4, 16, "gemm_a") == (None, None)
     (csrc / "gemm_tc.cu").write_text("// changed")
     assert bench.recorded_traffic("w", 8, 16, "gemm_a") == (None, None)
+
+
+def test_cpu_baselines_time_the_oracle_on_a_bounded_sample():
+    # the bench's CPU legs: both report a positive rate on a sample no larger than asked for
+    import dataclasses
+    import bench
+    import synth
+    cfg = synth.CONFIGS["fp32_small"]
+    inp = synth.make_inputs(cfg, seed=3)
+    v, n, dt = bench.cpu_oracle_tflops(cfg, inp, budget_s=0.0, min_tokens=8, max_tokens=16)
+    assert v > 0 and n == 8 and dt > 0
+    acfg = dataclasses.replace(synth.ATTN_CONFIGS["attn_small"], batch=2, seq=256, hidden=128, n_q=2, n_kv=1, d=64)
+    ainp = synth.make_attn_inputs(acfg, seed=3)
+    v, n, dt = bench.cpu_attn_oracle_tflops(acfg, ainp, budget_s=0.0, min_seq=64, max_seq=128)
+    assert v > 0 and n == 64 and dt > 0
+    v, n, dt = bench.cpu_attn_oracle_tflops(acfg, ainp, budget_s=1e9, min_seq=64, max_seq=128)
+    assert n == 128  # doubled up to the cap, never past it
