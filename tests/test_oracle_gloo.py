@@ -228,3 +228,78 @@ def test_two_gloo_ranks_sequence_parallel(tmp_path, skip_sync):
         close(z["dbd"], s["grads"]["b_down"])
         synced = np.allclose(z["dnw"], d["grads"]["norm_w"], rtol=1e-12, atol=1e-15)
         assert synced == (not skip_sync)
+
+
+# --------------------------------------------------------------------------
+# The attention sublayer with real collectives: each rank owns complete KV
+# groups and their query heads (W_qkv split by heads, W_out by columns); the
+# partial outputs and the normed input's partial gradients are all-reduced.
+
+_AB, _AS, _AH, _ANQ, _ANKV, _AD = 2, 8, 16, 4, 2, 4
+
+
+def _attn_fixture():
+    rng = np.random.default_rng(4321)
+    W = (_ANQ + 2 * _ANKV) * _AD
+    p = {"norm_w": 1.0 + 0.1 * rng.standard_normal(_AH), "w_qkv": 0.4 * rng.standard_normal((W, _AH)),
+         "w_o": 0.3 * rng.standard_normal((_AH, _ANQ * _AD)), "b_o": 0.05 * rng.standard_normal(_AH)}
+    N = _AB * _AS
+    return p, rng.standard_normal((N, _AH)), rng.standard_normal((N, _AH))
+
+
+def _attn_rank_main(rank, world, port, mode, out_dir):
+    import sys
+    sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+    from oracle import tpmlp_oracle as O
+    os.environ["MASTER_ADDR"] = "127.0.0.1"
+    os.environ["MASTER_PORT"] = str(port)
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        p, x, tgt = _attn_fixture()
+        eps = 1e-6
+        nq, nkv = _ANQ // world, _ANKV // world
+        q = O.attn_local_params(p, world, rank, _ANQ, _ANKV)
+        n, rstd, xhat = O.rms_norm(x, p["norm_w"], eps)
+        wq, wk, wv, d = O.attn_split_heads(q, nq, nkv)
+        qq, kk, vv = O.linear(n, wq), O.linear(n, wk), O.linear(n, wv)
+        z, P = O.attention_heads(qq, kk, vv, _AB, nq, nkv, d)
+        y = x + _all_reduce(O.linear(z, q["w_o"])) + p["b_o"]
+        loss, dy = O.mse_loss(y, tgt)
+        c = {"n": n, "rstd": rstd, "xhat": xhat, "q": qq, "k": kk, "v": vv, "z": z, "P": P, "d": d,
+             "batch": _AB, "n_q": nq, "n_kv": nkv}
+        dq, dk, dv = O.attention_heads_backward(c, dy @ q["w_o"])
+        dqkv = np.concatenate([dq, dk, dv], axis=1)
+        dn_local = dqkv @ q["w_qkv"]
+        dn = dn_local if mode == "missing_backward_reduce" else _all_reduce(dn_local)
+        dxn, dnw = O.rms_norm_backward(dn, xhat, rstd, p["norm_w"])
+        np.savez(os.path.join(out_dir, f"t{rank}.npz"), y=y, dx=dy + dxn, dnorm_w=dnw, dwqkv=dqkv.T @ n,
+                 dwo=dy.T @ z)
+    finally:
+        dist.destroy_process_group()
+
+
+@pytest.mark.parametrize("mode", ["equivalence", "missing_backward_reduce"])
+def test_two_gloo_ranks_attention(tmp_path, mode):
+    from oracle import tpmlp_oracle as O
+    world = 2
+    mp.start_processes(_attn_rank_main, args=(world, _free_port(), mode, str(tmp_path)), nprocs=world,
+                       join=True, start_method="spawn")
+    p, x, tgt = _attn_fixture()
+    dense = O.attn_dense_step(p, x, tgt, 1e-6, 0.0, _AB, _ANQ, _ANKV)
+    g = dense["grads"]
+    close = lambda a, b: float(np.max(np.abs(a - b))) < 1e-12
+    gq, gk, d = _ANQ // world, _ANKV // world, _AD
+    for r in range(world):
+        z = np.load(tmp_path / f"t{r}.npz")
+        sq = slice(r * gq * d, (r + 1) * gq * d)
+        sk = slice(r * gk * d, (r + 1) * gk * d)
+        dense_rows = np.concatenate([g["w_qkv"][: _ANQ * d][sq], g["w_qkv"][_ANQ * d: (_ANQ + _ANKV) * d][sk],
+                                     g["w_qkv"][(_ANQ + _ANKV) * d:][sk]], axis=0)
+        # the forward, and the weight gradients of the rank's own heads, need no backward reduction
+        assert close(z["y"], dense["y"])
+        assert close(z["dwqkv"], dense_rows)
+        assert close(z["dwo"], g["w_o"][:, sq])
+        if mode == "equivalence":
+            assert close(z["dx"], g["x"]) and close(z["dnorm_w"], g["norm_w"])
+        else:
+            assert not close(z["dx"], g["x"]) and not close(z["dnorm_w"], g["norm_w"])
