@@ -90,6 +90,13 @@ def test_null_context_is_rejected(T):
     assert L.tpmlp_sync(None) == T.ERR_ARG
     assert L.tpmlp_launch_count(None) == 0
     L.tpmlp_destroy(None)
+    assert L.tpmlp_adamw_step(None, None, None) == T.ERR_ARG
+    assert L.tpattn_sgd_step(None, 0.1) == T.ERR_ARG
+    assert L.tpattn_bind_adam_state(None, None, None) == T.ERR_ARG
+    assert L.tpattn_adamw_step(None, None, None) == T.ERR_ARG
+    assert L.tpattn_sync(None) == T.ERR_ARG
+    assert L.tpattn_launch_count(None) == 0
+    L.tpattn_destroy(None)
 
 
 def test_missing_library_fails_loudly(tmp_path, monkeypatch):
