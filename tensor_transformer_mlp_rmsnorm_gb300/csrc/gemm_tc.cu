@@ -613,6 +613,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const bool want_max = p.ep.amax != nullptr;
     float amax_acc = 0.0f;
     // Input tiles of chunk [col, col+32) of this warp's 32 rows -> buffer n_in % NIN.
+    // Every lane must have executed fence.proxy.async after its last generic
+    // reads of that buffer before the refill is issued: with double buffers
+    // the staging fence of the chunk that read it lies in between; with a
+    // single buffer the chunk loop fences explicitly.
     auto issue_in = [&](int col, int row0) {
       if (!HAS_IN) return;
       const uint32_t b = NIN == 2 ? (n_in & 1u) : 0u;
@@ -664,6 +668,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           read_row_bf16(si + b * 4096, lane, in.a);
           if (EPI == EPI_DGRAD_SWIGLU) read_row_bf16(si + b * 4096 + 2048, lane, in.b);
           if (NIN == 1) {
+            // The refill is an async-proxy (TMA) write into the buffer these
+            // generic loads read.  __syncwarp orders memory only within the
+            // generic proxy, so without the proxy fence neither the compiler
+            // nor the hardware keeps the loads before the refill, and lanes
+            // could read some 16-byte granules of the next chunk's inputs.
+            fence_proxy_async_smem();
             __syncwarp();  // every lane has read its input row before the buffer is refilled
             if (more) issue_in(col + 32 + so.col, row0 + so.row);
           }
