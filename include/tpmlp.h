@@ -410,16 +410,19 @@ TPMLP_API void tpattn_destroy(tpattn_ctx* ctx);
  * with y, target, dy of `dtype` (TPMLP_F32 or TPMLP_BF16), n >= 0 a multiple
  * of 8, pointers 16-byte aligned, enqueued on `cuda_stream`.
  * Its per-block partial sums live in a fixed array inside the library
- * (TPMLP_NOALLOC_LOSS_MAX_BLOCKS doubles, 512 KiB, held by every GPU that
- * loads the library until the process exits), so n is limited to
- * TPMLP_NOALLOC_LOSS_MAX_BLOCKS * 2048 elements for bf16 and * 1024 for f32;
- * larger n returns TPMLP_ERR_SHAPE before anything is enqueued.
+ * (TPMLP_NOALLOC_LOSS_MAX_BLOCKS doubles, 8 KiB, held by every GPU that
+ * loads the library until the process exits).  The loss kernel's grid is
+ * capped at that many blocks, which stride over all n elements, so the array
+ * bounds the number of partial sums and no n is refused for its sake.
  * The first call on a device looks up that array's device address (with the
- * device current); make that first call before any stream capture.  All
- * calls share the array: calls whose kernels overlap on the GPU race on it.
- * Errors: TPMLP_ERR_UNSUPPORTED (dtype), TPMLP_ERR_SHAPE (n), TPMLP_ERR_ARG
- * (NULL / misaligned), TPMLP_ERR_CUDA; the message is in tpmlp_last_error(NULL). */
-#define TPMLP_NOALLOC_LOSS_MAX_BLOCKS 65536
+ * device current) and keeps it for the life of the process: make that first
+ * call before any stream capture, and do not use this entry point on a device
+ * after cudaDeviceReset.  All calls share the array: calls whose kernels
+ * overlap on the GPU race on it.  Each call writes every partial sum it reads.
+ * Errors: TPMLP_ERR_UNSUPPORTED (dtype), TPMLP_ERR_SHAPE (n < 0 or not a
+ * multiple of 8), TPMLP_ERR_ARG (NULL / misaligned), TPMLP_ERR_CUDA; the
+ * message is in tpmlp_last_error(NULL). */
+#define TPMLP_NOALLOC_LOSS_MAX_BLOCKS 1024
 TPMLP_API tpmlp_status tpmlp_mse_loss_grad_noalloc(int32_t dtype, int64_t n, const void* y, const void* target,
                                                    void* dy, float* loss_dev, void* cuda_stream);
 

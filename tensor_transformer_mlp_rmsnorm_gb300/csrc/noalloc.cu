@@ -12,7 +12,9 @@
 // exits.  All calls share it: two calls whose kernels overlap on the GPU
 // (different streams, or different host threads) race on it.  Each call
 // writes every partial it later reads, so nothing has to be cleared between
-// calls.
+// calls.  Its device address is looked up once per device and kept for the
+// life of the process, so the entry point must not be used on a device after
+// cudaDeviceReset.
 #include <cuda_runtime.h>
 
 #include <mutex>
@@ -23,8 +25,9 @@
 
 namespace {
 
-// One double per 256-thread block of 16-byte vectors; the size limit on n
-// stays that of one block per 256 vectors.
+// One double per block of the loss kernel's grid.  The grid is capped at
+// kMaxBlocks blocks that stride over all n elements, so the array bounds the
+// number of partial sums, not n.
 constexpr int64_t kMaxBlocks = TPMLP_NOALLOC_LOSS_MAX_BLOCKS;
 static __device__ __align__(256) double g_loss_partials[kMaxBlocks];
 
@@ -72,13 +75,11 @@ extern "C" tpmlp_status tpmlp_mse_loss_grad_noalloc(int32_t dtype, int64_t n, co
     tpmlp::set_thread_error("n must be >= 0 and a multiple of 8");
     return TPMLP_ERR_SHAPE;
   }
+  // One block per 256 vectors of 16 bytes, capped at the array's size; the
+  // loss kernel strides over the vectors, so the capped grid covers any n.
   const int64_t per_block = 256LL * (dtype == TPMLP_BF16 ? 8 : 4);
   const int64_t blocks = (n + per_block - 1) / per_block;
-  if (blocks > kMaxBlocks) {
-    tpmlp::set_thread_error("n exceeds the fixed scratch of tpmlp_mse_loss_grad_noalloc (max " +
-                            std::to_string(kMaxBlocks * per_block) + " elements for this dtype)");
-    return TPMLP_ERR_SHAPE;
-  }
+  const int grid = (int)(blocks < kMaxBlocks ? blocks : kMaxBlocks);
   if (!loss_dev || (n > 0 && (!y || !target || !dy))) {
     tpmlp::set_thread_error("NULL tensor");
     return TPMLP_ERR_ARG;
@@ -97,10 +98,6 @@ extern "C" tpmlp_status tpmlp_mse_loss_grad_noalloc(int32_t dtype, int64_t n, co
     const tpmlp_status s = partials_on_current_device(&part);
     if (s != TPMLP_OK) return s;
     const int dt = dtype == TPMLP_BF16 ? 1 : 0;
-    // The loss kernel strides over the vectors, so a grid of at most 1024
-    // blocks covers any n (one block per vector group would leave most of
-    // each block's time to launch and reduction overhead at large n).
-    const int grid = (int)(blocks < 1024 ? blocks : 1024);
     e = tpmlp::launch_mse_loss_grad(dt, y, target, dy, part, grid, n, (float)(1.0 / (double)n), st);
     if (e == cudaSuccess) e = tpmlp::launch_loss_finalize(part, grid, 0.5 / (double)n, loss_dev, st);
   }

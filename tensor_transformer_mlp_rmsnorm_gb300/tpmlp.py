@@ -121,7 +121,7 @@ _SIGNATURES = {
 }
 TPATTN_FUSED_ONLY = 1  # tpattn_config.flags: only the fused attention kernels, no score square
 FP8_SCRATCH_BYTES = 4096
-NOALLOC_LOSS_MAX_BLOCKS = 65536
+NOALLOC_LOSS_MAX_BLOCKS = 1024
 
 _LIB = None
 
