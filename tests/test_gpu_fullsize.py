@@ -1,21 +1,27 @@
 """Parity at the full workload sizes, in the launch configuration the
 benchmark times (same library calls, same t, same dtypes).
 
-The oracle cannot afford the whole step at these sizes (the Llama-3-8B-shaped
-step alone is 17.3 TFLOP), so:
-
-* sampled token rows are checked element by element: a token's output y and
-  input gradient dx depend only on that token's row (and the weights), so the
-  oracle computes them exactly, row by row;
-* the reductions over tokens (the weight gradients, the loss) are checked by
-  identities that hold at any size, evaluated in float64 on the GPU's outputs:
+* Element by element against the oracle's whole dense step in float64 (page
+  "Megatron tensor-parallel MLP", "Reproduce one dense training step": the
+  output, the loss, the input gradient, every parameter gradient and the
+  weights after one update), at the GeLU workload (8192 tokens, H 4096,
+  F 16384, t = 8), the Llama-3-8B-shaped benchmark workload (16384 tokens,
+  H 4096, F 14336, t = 8) and the 70B shape (H 8192, F 28672, t = 8) at 512,
+  2048 and 8192 tokens.  The oracle takes tens of seconds of host time for
+  each of these.
+* At the 70B shape's 32768 tokens the oracle cannot afford the whole step, so
+  sampled token rows are checked element by element (a token's output y and
+  input gradient dx depend only on that token's row and the weights), and the
+  reductions over tokens by identities that hold at any size, evaluated in
+  float64 on the GPU's outputs:
     sum(db_down)                    = sum over tokens of dy
     sum(dW_down * W_down)           = sum(dy * (y - x - b_down))
     sum(dW_gate_up * W_gate_up)     = sum(dnorm_w * norm_w)
                                       (G, U are linear in W_gate_up and n = xhat * norm_w)
     (dx - dy) . x = 0 for every row  (RMSNorm is scale invariant, up to eps)
     loss = 0.5 mean((y - target)^2)
-* the logical degree t only fixes where shard boundaries fall inside the
+  The identities are also checked at the other sizes, as extra checks.
+* The logical degree t only fixes where shard boundaries fall inside the
   accumulation order, which runs over the FFN axis in shard order either way,
   so t = 4 and t = 8 give bit-identical results.
 """
@@ -24,7 +30,7 @@ import pytest
 
 import synth
 from oracle import tpmlp_oracle as O
-from tests._util import compare, gpu_step
+from tests._util import compare, compare_step, gpu_step
 
 pytestmark = pytest.mark.gpu
 
@@ -75,6 +81,7 @@ def check_identities(cfg, inp, gpu, rel=2e-2):
 
 
 def run_case(cfg, t, lr):
+    """Sampled rows element by element plus the identities (sizes the oracle cannot do whole)."""
     inp = synth.make_inputs(cfg)
     gpu = gpu_step(cfg, inp, t, lr, with_params=False)
     rows = sampled_rows(cfg.tokens)
@@ -86,10 +93,25 @@ def run_case(cfg, t, lr):
     return inp, gpu
 
 
+def full_case(cfg, t, lr):
+    """The whole step element by element against the oracle's dense step in float64."""
+    inp = synth.make_inputs(cfg)
+    gpu = gpu_step(cfg, inp, t, lr)
+    del gpu["new_params"]  # the post-step check reads the fp32 masters
+    p = {k: inp[k] for k in synth.param_names(cfg.act)}
+    ora = O.dense_step(p, inp["x"], inp["target"], cfg.eps, lr, cfg.act)
+    del ora["cache"], ora["new_params"]  # the post-step check forms w - lr * g itself
+    report = {}
+    compare_step(cfg, gpu, ora, inp, lr, report=report)
+    compare("dy", gpu["dy"], ora["dy"], cfg.dtype)
+    check_identities(cfg, inp, gpu)
+    return inp, gpu
+
+
 def test_llama8b_shape_bench_configuration():
-    """The benchmark's workload: 16384 tokens, H 4096, F 14336, t = 8 (and t = 4)."""
+    """The benchmark's workload: 16384 tokens, H 4096, F 14336, t = 8 (and t = 4), whole step."""
     cfg = synth.CONFIGS["bf16_llama8b"]
-    inp, g8 = run_case(cfg, 8, cfg.lr)
+    inp, g8 = full_case(cfg, 8, cfg.lr)
     g4 = gpu_step(cfg, inp, 4, cfg.lr, with_params=False)
     for k in ("y", "dx"):
         np.testing.assert_array_equal(g8[k], g4[k])
@@ -99,10 +121,15 @@ def test_llama8b_shape_bench_configuration():
 
 def test_gelu_h4096_full():
     cfg = synth.CONFIGS["bf16_gelu_h4096"]
-    run_case(cfg, 8, cfg.lr)
+    full_case(cfg, 8, cfg.lr)
 
 
-@pytest.mark.parametrize("tokens", [512, 2048])
-def test_70b_shape_sampled(tokens):
+@pytest.mark.parametrize("tokens", [512, 2048, 8192])
+def test_70b_shape_full(tokens):
     cfg = synth.CONFIGS["bf16_70b_n2048"].with_tokens(tokens)
+    full_case(cfg, 8, cfg.lr)
+
+
+def test_70b_shape_32768_sampled():
+    cfg = synth.CONFIGS["bf16_70b_n2048"].with_tokens(32768)
     run_case(cfg, 8, cfg.lr)
