@@ -138,13 +138,6 @@ def choose_peak(pk: dict, clk, region_s: float, ratio: float = 1.0):
     return ratio * pk["bf16_tflops_sustained"], "sustained"
 
 
-def frac_at_clock(achieved: float, pk: dict, clk, ratio: float = 1.0):
-    """achieved / (burst peak scaled by median SM clock / maximum SM clock): the fraction of
-    what the tensor cores can do at the clock the run actually held."""
-    if not clk or not clk.get("sm_max_mhz"):
-        return None
-    return achieved / (ratio * pk["bf16_tflops"] * clk["sm_mhz"] / clk["sm_max_mhz"])
-
 
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
@@ -491,7 +484,6 @@ def ours_attn(args):
         roof = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
                 "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
                 "frac_of_burst": ach / pk["bf16_tflops"], "frac_of_sustained": ach / pk["bf16_tflops_sustained"],
-                "frac_at_median_clock": frac_at_clock(ach, pk, clk),
                 "peak_kind": f"bf16 {kind} ({pk_src})", "avg_launch_ms": per_launch,
                 "note": "attention products counted over the causal half of the score square"
                         + ("; the fused backward's score recomputation is not counted" if top == "flash_attn_bwd"
@@ -682,8 +674,7 @@ def ours(args):
                 "peak_kind": f"{pname} {kind} ({pk_src}): " + (
                     "timed region under 1 s at the maximum SM clock" if kind == "burst"
                     else "timed region long enough for the power cap, or SM clock below its maximum"),
-                "frac_of_burst": achieved / peak_b, "frac_of_sustained": achieved / peak_s,
-                "frac_at_median_clock": frac_at_clock(achieved, pk, clk, ratio), "traffic": traffic,
+                "frac_of_burst": achieved / peak_b, "frac_of_sustained": achieved / peak_s, "traffic": traffic,
                 "flops_per_launch": units[top] * N * H * F, "avg_launch_ms": per_launch_ms}
     else:
         nbytes = hbm_bytes(top, cfg, masters=True)

@@ -412,7 +412,12 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 //                 blocks from the last one down, the heads of the group
 //                 inner, so the CTAs of one (sequence, group) read the same
 //                 Q / dO blocks at about the same time.
-//   warp 1      : tensor memory owner and MMA issuer.
+//   warp 1      : tensor memory owner; issues the score-side products
+//                 S^T and dP^T.
+//   warp 14     : issues the accumulating products dV, dQ^T and dK.
+//                 Two issuers keep products queued while either one waits
+//                 on a barrier: each wait costs an issue gap, and with one
+//                 issuer every gap reached the tensor pipe.
 //   warps 2..5  : row group 0, the even steps; warps 6..9: row group 1, the
 //                 odd steps.  One key row per thread: P^T (bf16, written
 //                 over its scores in tensor memory, where the dV product
@@ -426,13 +431,18 @@ __global__ void __launch_bounds__(FTHREADS, 1)
 // element-wise work runs under the products of the other group's step:
 // tensor memory holds S^T / P^T per slot, dP^T per slot (overwritten by the
 // step's dQ^T once the group has read dP^T), dV_j and dK_j.  Per step n the
-// MMA warp issues dV_n, dP^T_{n+1}, dQ^T_n and dK_n, then S^T_{n+2}.
+// score issuer issues dP^T_{n+1} and S^T_{n+2}; the accumulating issuer
+// dV_n, dQ^T_n and dK_n.  Products of one issuer run in issue order; across
+// the two, every reuse of a buffer waits on a barrier: S^T_{n+2} overwrites
+// slot n & 1 only after dV_n has read P^T_n (pv_done) and the row group has
+// read it back for dS (ds_full).
 // The same shared-memory tile of Q, dO, K or dS^T serves as a K-major operand
 // of one product and an MN-major operand of another: a 128-byte swizzled tile
 // of 64-element rows is both.
 constexpr int BKB = 128;  // keys per CTA
 constexpr int BQB = 64;   // queries per step
-constexpr int BTHREADS = 448;
+constexpr int BTHREADS = 480;
+constexpr int B_ISSUER = 14;  // warp index of the second MMA issuer
 constexpr int GROUP_WARPS = 4;  // warps per row group: one per TMEM lane quarter
 constexpr uint32_t KT_BYTES = BKB * 64 * 2;   // [128 keys x 64 d] tile, 16 KB
 constexpr uint32_t QT_BYTES = BQB * 64 * 2;   // [64 queries x 64 d] tile, 8 KB
@@ -477,7 +487,7 @@ __global__ void __launch_bounds__(BTHREADS, 1)
                      const __grid_constant__ CUtensorMap map_do, const FbParams p, int batch) {
   extern __shared__ uint8_t smem_raw[];
   __shared__ __align__(8) uint64_t kv_full, in_full[QST], in_empty[QST], s_full[2], p_full[2], dp_full[2],
-      ds_full[2], ds_empty[2], dq_full[2], dq_empty[2], acc_full, drain_bar;
+      ds_full[2], ds_empty[2], dq_full[2], dq_empty[2], pv_done[2], acc_full, drain_bar, drain_b;
   __shared__ uint32_t tmem_base_sh;
   __shared__ int abort_sh;
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -511,9 +521,11 @@ __global__ void __launch_bounds__(BTHREADS, 1)
       mbar_init(&ds_empty[i], 1);
       mbar_init(&dq_full[i], 1);
       mbar_init(&dq_empty[i], 4);
+      mbar_init(&pv_done[i], 1);
     }
     mbar_init(&acc_full, 1);
     mbar_init(&drain_bar, 1);
+    mbar_init(&drain_b, 1);
     abort_sh = 0;
     fence_mbar_init();
   }
@@ -624,11 +636,37 @@ __global__ void __launch_bounds__(BTHREADS, 1)
     if (ok && nsteps > 1) ok = issue_s(1);
     if (ok) ok = issue_dp(0);
     for (int n = 0; ok && n < nsteps; ++n) {
+      if (n + 1 < nsteps && !(ok = issue_dp(n + 1))) break;
+      if (n + 2 < nsteps) {
+        // slot n & 1 holds P^T_n until dV_n has read it and the row group
+        // has read it back for dS_n
+        const uint32_t par = (uint32_t)((n >> 1) & 1);
+        if (!(ok = wait_all(&pv_done[n & 1], par))) break;
+        if (!(ok = wait_all(&ds_full[n & 1], par))) break;
+        if (!(ok = issue_s(n + 2))) break;
+      }
+    }
+    if (elect_one()) tc_commit(&drain_bar);
+    __syncwarp();
+    int no_abort = 0;
+    mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
+  } else if (warp == B_ISSUER) {
+    // ------------------------------------------------- accumulating issuer
+    constexpr uint32_t IDESC_KV = idesc_bf16_f32(BKB, FD, false, true);    // dV, dK
+    constexpr uint32_t IDESC_DQ = idesc_bf16_f32(FD, BQB, true, true);     // dQ^T
+    const uint64_t k_mdesc = sw128_desc(smem_u32(smem + B_SK), KT_BYTES, 1024);  // K^T, MN-major
+    const uint64_t q_mdesc = sw128_desc(smem_u32(smem + B_SQ), QT_BYTES, 1024);  // Q ring, MN-major
+    const uint64_t o_mdesc = sw128_desc(smem_u32(smem + B_SDO), QT_BYTES, 1024); // dO ring, MN-major
+    const uint64_t ds_kdesc = sw128_desc(smem_u32(smem + B_SDS), 16, 1024);      // dS^T slots, K-major
+    const uint64_t ds_mdesc = sw128_desc(smem_u32(smem + B_SDS), KT_BYTES, 1024);// dS^T slots, MN-major
+    int ok = 1;
+    for (int n = 0; ok && n < nsteps; ++n) {
       const int s = n & 1, q = n % QST;
       const uint32_t par = (uint32_t)((n >> 1) & 1);
       const uint64_t sq = desc_advance(q_mdesc, 2 * q * QT_BYTES), sdo = desc_advance(o_mdesc, 2 * q * QT_BYTES);
       const uint64_t sds_k = desc_advance(ds_kdesc, s * KT_BYTES), sds_m = desc_advance(ds_mdesc, s * KT_BYTES);
-      // dV += P^T dO_n, P^T from tensor memory (bf16 pairs, 8 columns per K = 16)
+      // dV += P^T dO_n, P^T from tensor memory (bf16 pairs, 8 columns per K = 16).
+      // p_full implies S^T_n, issued after dO_n landed, has been read.
       if (!(ok = wait_all(&p_full[s], par))) break;
       tc_fence_after();
       if (elect_one()) {
@@ -636,12 +674,12 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_f16_ts(tmem_base + T_DV, tmem_base + T_S + s * BQB + kk * 8, desc_advance(sdo, kk * 2048), IDESC_KV,
                         (n > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(&pv_done[s]);
       }
       __syncwarp();
-      if (n + 1 < nsteps && !(ok = issue_dp(n + 1))) break;
       // dQ^T_n = K^T dS^T over the slot's dP^T, which the group has read; then
       // dK += dS^T Q_n.  dQ^T goes first so that its slot, which dP^T_{n+2}
-      // needs next, is read out while dK_n and S^T_{n+2} keep the tensor core busy.
+      // needs next, is read out while dK_n keeps the tensor core busy.
       if (!(ok = wait_all(&ds_full[s], par))) break;
       tc_fence_after();
       if (elect_one()) {
@@ -654,17 +692,19 @@ __global__ void __launch_bounds__(BTHREADS, 1)
         for (int kk = 0; kk < 4; ++kk)
           tc_mma_f16(tmem_base + T_DK, desc_advance(sds_k, kk * 32), desc_advance(sq, kk * 2048), IDESC_KV,
                      (n > 0 || kk > 0) ? 1u : 0u);
+        // the stage's readers are done: S^T_n and dP^T_n (the score issuer's)
+        // were read by the row group before p_full and ds_full, dV_n and dK_n
+        // are this thread's
         tc_commit(&ds_empty[s]);
         tc_commit(&in_empty[q]);
         if (n + 1 == nsteps) tc_commit(&acc_full);
       }
       __syncwarp();
-      if (n + 2 < nsteps && !(ok = issue_s(n + 2))) break;
     }
-    if (elect_one()) tc_commit(&drain_bar);
+    if (elect_one()) tc_commit(&drain_b);
     __syncwarp();
     int no_abort = 0;
-    mbar_wait(&drain_bar, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
+    mbar_wait(&drain_b, 0, &no_abort, p.status, STATUS_TIMEOUT, FDRAIN_NS);
   } else if (warp < 2 + 2 * GROUP_WARPS) {
     // ------------------------------------------------------------ row groups
     const int grp = (warp - 2) / GROUP_WARPS;  // steps n with n & 1 == grp, slot grp
