@@ -215,6 +215,18 @@ def instrumented_pass(torch, m, step, stream, steps: int) -> float:
     return a.elapsed_time(b)
 
 
+def h2d_gbps(torch, host, dev, reps: int = 3) -> float:
+    """Host-to-device copy rate of one pinned buffer alone (GB/s), for reading the e2e figure."""
+    dev.copy_(host, non_blocking=True)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        dev.copy_(host, non_blocking=True)
+    b.record()
+    torch.cuda.synchronize()
+    return reps * host.numel() * host.element_size() / (a.elapsed_time(b) / 1e3) / 1e9
+
+
 def timed_e2e(torch, run_step, stream, x_host, tg_host, xbufs, tbufs, loss, loss_host, steps: int) -> float:
     """Milliseconds for `steps` training steps fed from pinned host memory.
 
@@ -462,6 +474,7 @@ def ours_attn(args):
         ms, ems = float(tt[0].item()), float(tt[1].item())
     flops = cfg.gemm_flops
     value = flops * args.steps * world / (ms / 1e3) / 1e12
+    h2d_rate = h2d_gbps(torch, x_host, y)
     if rank != 0:
         if world > 1:
             torch.distributed.destroy_process_group()
@@ -526,7 +539,8 @@ def ours_attn(args):
         "roofline": roof, "cpu_baseline": cpu,
         "e2e": {"value": flops * e2e_steps * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 4, "steps": e2e_steps,
-                "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)"},
+                "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)",
+                "h2d_gbps_alone": h2d_rate},
         "clocks": clk, "gpu_launches": launches, "loss": float(loss_host.item()),
     }
     print(json.dumps(line), flush=True)
@@ -649,6 +663,7 @@ def ours(args):
     ws_gb = (N * H * (5 * e + 4) + N * F * (5 * e if cfg.act == "swiglu" else 3 * e) + nP * (e + 8)) / 1e9
     value = flops_step * args.steps * world / (ms / 1e3) / 1e12
     e2e_value = flops_step * e2e_steps * world / (ems / 1e3) / 1e12
+    h2d_rate = h2d_gbps(torch, x_host, y)
 
     if rank != 0:
         if world > 1:
@@ -709,7 +724,8 @@ def ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * N * H * e,
                 "d2h_bytes_per_step": 4, "steps": e2e_steps,
-                "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)"},
+                "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)",
+                "h2d_gbps_alone": h2d_rate},
         "clocks": clk,
         "gpu_launches": launches,
         "loss": float(loss_host.item()),

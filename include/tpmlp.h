@@ -107,8 +107,10 @@ typedef struct {
 TPMLP_API tpmlp_status tpmlp_create(const tpmlp_config* cfg, void* cuda_stream, tpmlp_ctx** out);
 
 /* Bytes of device workspace a context with `cfg` needs (saved activations
- * n/rstd/G,U/A, the backward intermediates dGU and dN, reduction partials and
- * the device status word).  0 if `cfg` is invalid. */
+ * n/rstd/G,U/A, the backward intermediates dGU and dN, reduction partials,
+ * the device status word and, for bf16, 40 MB of scratch for the partial sums
+ * of GEMM tiles whose contraction is split along K in a launch's last wave).
+ * 0 if `cfg` is invalid. */
 TPMLP_API size_t tpmlp_workspace_bytes(const tpmlp_config* cfg);
 
 /* Hand the context `bytes` of device memory at `dev` (256-byte aligned).  The

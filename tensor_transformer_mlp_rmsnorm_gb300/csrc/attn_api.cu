@@ -80,7 +80,8 @@ size_t al256(size_t v) { return (v + 255) & ~size_t(255); }
 bool a16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 struct AttnLayout {
-  size_t status, nrm, rstd, qkv, z, dz, dqkv, dnrm, scores, probs, dkv_head, lse2, dsum, part_dw, part_db, norm_part, total;
+  size_t status, split_ctr, nrm, rstd, qkv, z, dz, dqkv, dnrm, scores, probs, dkv_head, lse2, dsum, part_dw, part_db,
+      norm_part, split_scratch, total;
 };
 
 bool attn_config_error(const tpattn_config* c, std::string* why) {
@@ -122,6 +123,7 @@ AttnLayout attn_layout(const tpattn_config& c) {
     return o;
   };
   L.status = take(256);
+  L.split_ctr = take(SPLIT_COUNTER_WORDS * sizeof(uint32_t));  // zeroed before each split GEMM
   L.nrm = take(N * H * 2);
   L.rstd = take(N * 4);
   L.qkv = take(N * W * 2);
@@ -137,6 +139,7 @@ AttnLayout attn_layout(const tpattn_config& c) {
   L.part_dw = take((size_t)MAX_PARTS * H * 4);
   L.part_db = take((size_t)MAX_PARTS * H * 4);
   L.norm_part = take((size_t)MAX_NORM_PARTS * sizeof(double));  // AdamW: per-block partial sums of g^2
+  L.split_scratch = take(SPLIT_SCRATCH_BYTES);  // tail-split partial accumulators of the GEMMs
   L.total = off;
   return L;
 }
@@ -202,7 +205,12 @@ struct tpattn_ctx {
     if (e != cudaSuccess) return fail(TPMLP_ERR_CUDA, std::string(kAttnNames[id]) + ": " + cudaGetErrorString(e));
     return TPMLP_OK;
   }
-  tpmlp_status gemm(int id, const GemmDesc& g) {
+  tpmlp_status gemm(int id, const GemmDesc& desc) {
+    GemmDesc g = desc;
+    g.split_scratch = wsp<float>(L.split_scratch);
+    g.split_scratch_bytes = SPLIT_SCRATCH_BYTES;
+    g.split_counters = wsp<uint32_t>(L.split_ctr);
+    g.split_counter_words = SPLIT_COUNTER_WORDS;
     return run(id, [&] { return launch_gemm_tc(g, stream, num_sms, wsp<uint32_t>(L.status), 0); });
   }
 };
@@ -468,7 +476,7 @@ tpmlp_status tpattn_bind_workspace(tpattn_ctx* c, void* dev, size_t bytes) {
   if (!dev || (reinterpret_cast<uintptr_t>(dev) & 255u)) return c->fail(TPMLP_ERR_ARG, "workspace must be 256-byte aligned");
   if (bytes < c->L.total) return c->fail(TPMLP_ERR_ARG, "workspace too small");
   c->ws = static_cast<uint8_t*>(dev);
-  const cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
+  cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
   return e == cudaSuccess ? TPMLP_OK : c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
 }
 

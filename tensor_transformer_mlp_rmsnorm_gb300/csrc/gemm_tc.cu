@@ -61,6 +61,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s per wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s for draining after an abort
 constexpr uint64_t PEER_DRAIN_NS = 5000000ull;      // 5 ms: a CTA-pair peer's loads land long before this
 constexpr uint64_t FORCED_LIMIT_NS = 2000000ull;    // 2 ms for the forced-timeout debug wait
+constexpr int SPLIT_MIN_KBLOCKS = 192;              // shortest contraction whose tail is split
 
 // Epilogues that read global inputs (the residual x, or G and U, or Z) bring
 // them into shared memory with TMA as well.
@@ -118,7 +119,56 @@ struct TcParams {
   int tiles_per_batch;  // num_m_blk * num_n_blk
   BatchDesc batch;
   int causal;  // CAUSAL_* restriction for attention problems
+  // Work units: tiles [0, split_first) whole, then `split` K parts of each
+  // tile in [split_first, num_tiles); num_units in all.  kb_total is the
+  // k-blocks of one tile's contraction (both segments).
+  int num_units, split_first, split, kb_total;
+  float* scratch;      // partial accumulators of the parts after the first
+  uint32_t* counters;  // per split tile, CTA of the pair and epilogue warp
+  size_t scratch_bytes;
+  int counter_words;
 };
+
+// One work unit: a tile, which of its K parts, and the range [vb, ve) of
+// k-blocks it contracts, counted over the tile's segments in order.
+struct Unit {
+  int tile, part, vb, ve;
+};
+__device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
+  Unit w;
+  if (u < p.split_first) {
+    w.tile = u;
+    w.part = 0;
+    w.vb = 0;
+    w.ve = 0x7fffffff;
+    return w;
+  }
+  const int i = u - p.split_first;
+  w.tile = p.split_first + i / p.split;
+  w.part = i % p.split;
+  w.vb = (int)((int64_t)w.part * p.kb_total / p.split);
+  w.ve = (int)((int64_t)(w.part + 1) * p.kb_total / p.split);
+  return w;
+}
+
+// Bounded wait until *ctr >= target (acquire at GPU scope).  On a timeout it
+// raises the CTA's abort flag and ORs `code` into the status word.
+__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, volatile int* abort,
+                                           uint32_t* status, uint32_t code, uint64_t limit_ns) {
+  const uint64_t t0 = global_timer_ns();
+  for (;;) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
+    if (v >= target) return true;
+    if (*abort) return false;
+    if (global_timer_ns() - t0 > limit_ns) {
+      *abort = 1;
+      atomicOr(status, code);
+      return false;
+    }
+    __nanosleep(256);
+  }
+}
 
 // Causal restrictions of attention problems (M = queries or keys of one
 // sequence): tiles wholly above the diagonal skipped (score GEMMs), or the
@@ -132,6 +182,19 @@ __device__ __forceinline__ void seg_range(const TcParams& p, int mb, int seg, in
   hi = p.kb[2 * seg + 1];
   if (p.causal == CAUSAL_K_UPTO) hi = min(hi, ((mb + 1) * tile_m + bke - 1) / bke);
   if (p.causal == CAUSAL_K_FROM) lo = max(lo, (mb * tile_m) / bke);
+}
+
+// The k-blocks of segment `seg` of tile row block mb that unit `un` contracts:
+// [lo, hi), with v0 the count of the tile's k-blocks in earlier segments
+// (advanced past this segment on return).
+__device__ __forceinline__ void unit_seg_range(const TcParams& p, const Unit& un, int mb, int seg, int tile_m, int bke,
+                                               int& v0, int& lo, int& hi) {
+  int a, b;
+  seg_range(p, mb, seg, tile_m, bke, a, b);
+  const int n = b > a ? b - a : 0;
+  lo = a + max(0, min(n, un.vb - v0));
+  hi = a + max(0, min(n, un.ve - v0));
+  v0 += n;
 }
 
 // Coordinate shift of one operand for batch index z.
@@ -181,6 +244,20 @@ __device__ __forceinline__ void unpack8_bf16(uint4 v, float* f) {
     float2 t = __bfloat1622float2(h);
     f[2 * i] = t.x;
     f[2 * i + 1] = t.y;
+  }
+}
+
+// r[i] += src[i] for 32 consecutive floats of a scratch row (read past L1:
+// other CTAs wrote them during this launch).
+__device__ __forceinline__ void add32_from(uint32_t (&r)[32], const float* src) {
+  const float4* s4 = reinterpret_cast<const float4*>(src);
+#pragma unroll
+  for (int k = 0; k < 8; ++k) {
+    const float4 v = __ldcg(s4 + k);
+    r[4 * k] = __float_as_uint(__uint_as_float(r[4 * k]) + v.x);
+    r[4 * k + 1] = __float_as_uint(__uint_as_float(r[4 * k + 1]) + v.y);
+    r[4 * k + 2] = __float_as_uint(__uint_as_float(r[4 * k + 2]) + v.z);
+    r[4 * k + 3] = __float_as_uint(__uint_as_float(r[4 * k + 3]) + v.w);
   }
 }
 
@@ -412,9 +489,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       uint32_t stage = 0, phase = 0;
       uint32_t armed = 0, armed_par = 0;
       bool ok = true;
-      for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
+      for (int u = worker; ok && u < p.num_units; u += num_workers) {
+        const Unit un = unit_of(p, u);
         int mb, nb, z;
-        tile_coords(p, tile, mb, nb, z);
+        tile_coords(p, un.tile, mb, nb, z);
         if (!tile_active(p, mb, nb, C::TILE_M)) continue;
         const Shift sa = batch_shift(p.batch, p.batch.a, z), sbt = batch_shift(p.batch, p.batch.b, z);
         const int m0 = mb * C::TILE_M + (int)rank * BM + (A_MN ? sa.col : sa.row);
@@ -429,9 +507,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (PAIR) brow0 = rank ? brow1 : brow0;  // each CTA of the pair holds one half
         brow0 += B_MN ? sbt.col : sbt.row;
         brow1 += B_MN ? sbt.col : sbt.row;
+        int v0 = 0;
         for (int seg = 0; ok && seg < 2; ++seg) {
           int kb_lo, kb_hi;
-          seg_range(p, mb, seg, C::TILE_M, KDepth<F8>::STAGE, kb_lo, kb_hi);
+          unit_seg_range(p, un, mb, seg, C::TILE_M, KDepth<F8>::STAGE, v0, kb_lo, kb_hi);
           for (int kb = kb_lo; kb < kb_hi; ++kb) {
             if (!mbar_wait(&empty_bar[stage], phase ^ 1u, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS)) {
               ok = false;
@@ -513,9 +592,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // tcgen05.mma well below the 128 cycles it keeps the tensor core busy.
       uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
       int ok = !*abort_flag;
-      for (int tile = worker; ok && tile < p.num_tiles; tile += num_workers) {
+      for (int u = worker; ok && u < p.num_units; u += num_workers) {
+        const Unit un = unit_of(p, u);
         int mb, nb, z;
-        tile_coords(p, tile, mb, nb, z);
+        tile_coords(p, un.tile, mb, nb, z);
         if (!tile_active(p, mb, nb, C::TILE_M)) continue;
         ok = __all_sync(0xffffffffu, mbar_wait(&tempty_bar[acc], acc_phase ^ 1u, abort_flag, p.status,
                                                STATUS_TIMEOUT, WAIT_LIMIT_NS));
@@ -523,9 +603,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_after();
         const uint32_t d_tmem = tmem_base + acc * BN;
         uint32_t accumulate = 0;
+        int v0 = 0;
         for (int seg = 0; ok && seg < 2; ++seg) {
           int kb_lo, kb_hi;
-          seg_range(p, mb, seg, C::TILE_M, KDepth<F8>::STAGE, kb_lo, kb_hi);
+          unit_seg_range(p, un, mb, seg, C::TILE_M, KDepth<F8>::STAGE, v0, kb_lo, kb_hi);
           for (int kb = kb_lo; kb < kb_hi; ++kb) {
             ok = __all_sync(0xffffffffu, mbar_wait(&full_bar[stage], phase, abort_flag, p.status, STATUS_TIMEOUT,
                                                    WAIT_LIMIT_NS));
@@ -627,14 +708,59 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       }
       ++n_in;
     };
-    for (int tile = worker; tile < p.num_tiles; tile += num_workers) {
+    for (int u = worker; u < p.num_units; u += num_workers) {
+      const Unit un = unit_of(p, u);
       int mb, nb, z;
-      tile_coords(p, tile, mb, nb, z);
+      tile_coords(p, un.tile, mb, nb, z);
       if (!tile_active(p, mb, nb, C::TILE_M)) continue;
       const Shift so = batch_shift(p.batch, p.batch.o, z);  // output / input coordinate shift
       const int row0 = mb * C::TILE_M + (int)rank * BM + q * 32;  // first row of this warp
       constexpr int CHUNKS = EPI == EPI_GATEUP_SWIGLU ? BN / 2 / 32 : BN / 32;
       const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
+      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      // Split tiles: this warp's arrival counter, and this lane's row in a
+      // scratch slot (one slot of TILE_M x BN floats per later part).
+      const bool split = un.tile >= p.split_first;
+      const int ti = un.tile - p.split_first;
+      uint32_t* ctr = split ? p.counters + ((size_t)ti * 2 + rank) * 4 + q : nullptr;
+      const float* slots =
+          split ? p.scratch + ((size_t)ti * (p.split - 1) * C::TILE_M + (size_t)rank * BM + q * 32 + lane) * BN
+                : nullptr;
+      if (split && un.part > 0) {
+        // A later K part: leave the raw accumulator rows of this warp in its
+        // slot, then count this warp's arrival (release) for the first part.
+        int ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status,
+                                                   STATUS_TIMEOUT, WAIT_LIMIT_NS));
+        if (!ok) break;
+        tc_fence_after();
+        if (row0 < p.M) {
+          float* dst = const_cast<float*>(slots) + (size_t)(un.part - 1) * C::TILE_M * BN;
+#pragma unroll 1
+          for (int c = 0; c < BN / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld_32x32b_x32(tbase + c * 32, r);
+            tmem_ld_wait();
+            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
+#pragma unroll
+            for (int k = 0; k < 8; ++k)
+              __stcg(d4 + k, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                         __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
+          }
+        }
+        __threadfence();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+          if (PAIR)
+            mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
+          else
+            mbar_arrive(&tempty_bar[acc]);
+        }
+        acc ^= 1u;
+        if (acc == 0) acc_phase ^= 1u;
+        continue;
+      }
       // The first chunk's inputs are fetched while the tile's main loop runs,
       // each later chunk's while the previous one is computed.
       if (col_base < p.N && row0 < p.M) issue_in(col_base + so.col, row0 + so.row);
@@ -642,7 +768,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
       tc_fence_after();
-      const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
+      if (split) {
+        // The first K part of a split tile: wait for the later parts of this
+        // warp's rows.
+        int wok = 1;
+        if (lane == 0)
+          wok = wait_count(ctr, (uint32_t)(p.split - 1), abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+        ok = __all_sync(0xffffffffu, wok);
+        if (!ok) break;
+      }
       uint32_t r0[32], r1[32];
 #pragma unroll 1
       for (int c = 0; c < CHUNKS; ++c) {
@@ -690,6 +824,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();  // also: every lane has read its input row before the buffer is refilled
         tmem_ld_wait();
+        if (split) {
+          // the later parts' partial sums, added in part order
+#pragma unroll 1
+          for (int part = 1; part < p.split; ++part) {
+            const float* src = slots + (size_t)(part - 1) * C::TILE_M * BN;
+            add32_from(r0, src + c * 32);
+            if (EPI == EPI_GATEUP_SWIGLU) add32_from(r1, src + BN / 2 + c * 32);
+          }
+        }
         if (F8) {
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
@@ -790,9 +933,39 @@ cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStre
   });
   if (attr_err != cudaSuccess) return attr_err;
   if (max_workers <= 0) return cudaErrorInvalidConfiguration;
-  const int workers = p.num_tiles < max_workers ? p.num_tiles : max_workers;
+  // Tail split: the r tiles of the last, partial round of the persistent grid
+  // (r of W workers busy) are cut into S = min(W / r, 4) contiguous K parts,
+  // so that the round takes about 1/S of a tile's time.  The tail units
+  // [T - r, T - r + r S) all fall in the last round (T - r is a multiple of
+  // W), one per worker and after its whole tiles, so a first part only ever
+  // waits on workers that wait on nobody.  Only long contractions are split:
+  // the first part reads the others' partial rows back at one round trip per
+  // part and chunk (a few microseconds), which a tile of 64 k-blocks (about
+  // 20 us) does not win back (measured: K = 4096 GEMMs 7-14% slower split
+  // four ways, K = 28672 ones faster).
+  TcParams q = p;
+  const int W = max_workers;
+  if (q.scratch && q.counters && q.causal == CAUSAL_NONE && q.tiles_per_batch == q.num_tiles &&
+      q.kb_total >= SPLIT_MIN_KBLOCKS) {
+    const int r = q.num_tiles % W;
+    int S = r > 0 ? W / r : 1;
+    if (S > 4) S = 4;
+    if (S > q.kb_total) S = q.kb_total;
+    while (S > 1 && ((size_t)r * (S - 1) * C::TILE_M * BN * sizeof(float) > q.scratch_bytes ||
+                     (size_t)r * 8 > (size_t)q.counter_words))
+      --S;
+    if (S >= 2) {
+      q.split = S;
+      q.split_first = q.num_tiles - r;
+      q.num_units = q.split_first + r * S;
+      // the arrival counters start from zero in every launch
+      const cudaError_t e = cudaMemsetAsync(q.counters, 0, (size_t)r * 8 * sizeof(uint32_t), st);
+      if (e != cudaSuccess) return e;
+    }
+  }
+  const int workers = q.num_units < W ? q.num_units : W;
   if (!PAIR) {
-    kfn<<<workers, NUM_THREADS, C::SMEM_BYTES, st>>>(mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], mp.i[0], mp.i[1], p);
+    kfn<<<workers, NUM_THREADS, C::SMEM_BYTES, st>>>(mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], mp.i[0], mp.i[1], q);
     return cudaGetLastError();
   }
   cudaLaunchConfig_t cfg = {};
@@ -807,7 +980,7 @@ cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStre
   cfg.stream = st;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kfn, mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], mp.i[0], mp.i[1], p);
+  return cudaLaunchKernelEx(&cfg, kfn, mp.a, mp.b, mp.o[0], mp.o[1], mp.o[2], mp.i[0], mp.i[1], q);
 }
 
 template <bool PAIR>
@@ -848,6 +1021,14 @@ cudaError_t launch_shape(const GemmDesc& g, cudaStream_t st, int num_sms, uint32
     p.kb[2 * s + 1] = (int)((k1 + BKE - 1) / BKE);
   }
   if (p.kb[1] - p.kb[0] + p.kb[3] - p.kb[2] <= 0) return cudaErrorInvalidValue;
+  p.kb_total = p.kb[1] - p.kb[0] + p.kb[3] - p.kb[2];
+  p.num_units = p.num_tiles;  // whole tiles unless the launch splits the tail
+  p.split_first = p.num_tiles;
+  p.split = 1;
+  p.scratch = g.split_scratch;
+  p.scratch_bytes = g.split_scratch_bytes;
+  p.counters = g.split_counters;
+  p.counter_words = g.split_counter_words;
   p.paired = g.paired ? 1 : 0;
   p.pair_off = (int)g.pair_off;
   p.ep = g.ep;

@@ -69,7 +69,8 @@ thread_local std::string g_thread_err;
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 struct Layout {
-  size_t status, loss_part, norm_part, nrm, rstd, gu, act, dgu, dnrm, part_dw, part_db, part_b1, shard_sums, total;
+  size_t status, split_ctr, loss_part, norm_part, nrm, rstd, gu, act, dgu, dnrm, part_dw, part_db, part_b1, shard_sums,
+      split_scratch, total;
 };
 
 bool config_error(const tpmlp_config* c, std::string* why, tpmlp_status* st) {
@@ -104,6 +105,7 @@ Layout make_layout(const tpmlp_config& c) {
     return o;
   };
   L.status = take(256);
+  L.split_ctr = take(SPLIT_COUNTER_WORDS * sizeof(uint32_t));  // zeroed before each split GEMM
   L.loss_part = take(MAX_LOSS_PARTS * sizeof(double));
   L.norm_part = take(MAX_NORM_PARTS * sizeof(double));
   L.nrm = take(N * H * E);
@@ -116,6 +118,7 @@ Layout make_layout(const tpmlp_config& c) {
   L.part_db = take((size_t)MAX_BWD_PARTS * H * 4);
   L.part_b1 = c.act == TPMLP_GELU ? take((size_t)MAX_B1_PARTS * F * 4) : off;
   L.shard_sums = take((size_t)2 * (c.max_t < MAX_SP_SHARDS ? c.max_t : MAX_SP_SHARDS) * H * 4);
+  L.split_scratch = c.dtype == TPMLP_BF16 ? take(SPLIT_SCRATCH_BYTES) : off;  // tensor-core GEMMs only
   L.total = off;
   return L;
 }
@@ -248,6 +251,10 @@ tpmlp_status run_gemm(tpmlp_ctx* c, int id, const GemmDesc& desc, int force_time
   if (c->cfg.dtype == TPMLP_BF16) {
     GemmDesc g = desc;
     if (c->dbg_flags & TPMLP_DBG_GEMM_SINGLE_CTA) g.tile_mode = 1;
+    g.split_scratch = c->wsp<float>(c->L.split_scratch);
+    g.split_scratch_bytes = SPLIT_SCRATCH_BYTES;
+    g.split_counters = c->wsp<uint32_t>(c->L.split_ctr);
+    g.split_counter_words = SPLIT_COUNTER_WORDS;
     return c->run(id, [&] { return launch_gemm_tc(g, c->stream, c->num_sms, c->status(), force_timeout); });
   }
   const GemmDesc& g = desc;
@@ -378,7 +385,7 @@ tpmlp_status tpmlp_bind_workspace(tpmlp_ctx* c, void* dev, size_t bytes) {
   if (bytes < c->L.total) return c->fail(TPMLP_ERR_ARG, "workspace too small");
   c->ws = static_cast<uint8_t*>(dev);
   c->ws_bytes = bytes;
-  const cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
+  cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
   if (e != cudaSuccess) return c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
   return TPMLP_OK;
 }

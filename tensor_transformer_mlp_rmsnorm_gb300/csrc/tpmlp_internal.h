@@ -72,7 +72,24 @@ struct GemmDesc {
   // K >= the tile's first row (all at tile granularity; the entries beyond
   // the causal boundary inside a tile must be zero in A).
   int causal = CAUSAL_NONE;
+  // Tail split along K (tensor-core path): the tiles of the last, partial
+  // wave of the persistent grid are cut into up to four contiguous K parts
+  // run by otherwise idle CTAs; the parts after the first leave their f32
+  // accumulators in `split_scratch` and count their arrival in
+  // `split_counters` (zeroed on the stream before each split launch), and
+  // the first part adds the partials in part order.  NULL disables the split.
+  float* split_scratch = nullptr;
+  size_t split_scratch_bytes = 0;
+  uint32_t* split_counters = nullptr;
+  int split_counter_words = 0;
 };
+
+// Workspace regions for the tail split: partial accumulators of up to
+// SPLIT_SLOTS tiles of 256 x 256 f32, and 8 counters (two CTAs of a pair x
+// four epilogue warps) per split tile.
+constexpr int SPLIT_SLOTS = 160;
+constexpr size_t SPLIT_SCRATCH_BYTES = (size_t)SPLIT_SLOTS * 256 * 256 * 4;
+constexpr int SPLIT_COUNTER_WORDS = SPLIT_SLOTS * 8;
 
 // tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory), or
 // E4M3 operands with f8 set.  Segment boundaries must be multiples of 64
