@@ -9,10 +9,10 @@ identities that hold at any size:
   output for y); the MLP identities with the tolerance widened to the FP8
   band, because the two sides of each identity quantise different tensors
   (dy against Q(dy), W against Q(W));
-* attention (4 x 2048 tokens, hidden 4096, 32/8 heads of 128, t = 8): y of
-  sampled rows of two sequences at the bf16 tolerance (a row needs the keys
-  and values of its sequence's prefix, computed here in full for those two
-  sequences), and
+* attention (4 x 2048 tokens, hidden 4096, 32/8 heads of 128, t = 8): the
+  whole step element by element against the oracle's float64 dense step
+  (about 15 s of host time); and, as an independent check, y of sampled rows
+  of two sequences computed here row by row over each causal prefix, and
     sum(db_o)             = sum over tokens of dy
     sum(dW_o * W_o)       = sum(dy * (y - x - b_o))
     sum(dW_qkv * W_qkv)   = sum(dnorm_w * norm_w)   (qkv is linear in W_qkv, n = xhat * norm_w)
@@ -112,3 +112,45 @@ def test_attention_gpt_h4096():
     num = np.abs(np.sum(dxn * inp["x"], axis=1))
     den = np.sum(np.abs(dxn) * np.abs(inp["x"]), axis=1) + 1e-300
     assert np.max(num / den) < 1e-2, float(np.max(num / den))
+
+
+def test_attention_gpt_h4096_whole_step():
+    """The attention workload's whole step (4 x 2048 tokens, hidden 4096, 32 query heads in 8
+    KV groups of 128, t = 8, the fused kernels on a fused-only context as the benchmark runs
+    it) element by element against the oracle's dense step in float64: y, the loss, dy, dx,
+    every parameter gradient and the post-step fp32 masters."""
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPAttn
+    from tensor_transformer_mlp_rmsnorm_gb300.tpmlp import tpmlp_mse_loss_grad_noalloc
+    cfg = synth.ATTN_CONFIGS["attn_gpt_h4096"]
+    inp = synth.make_attn_inputs(cfg)
+    names = ("norm_w", "w_qkv", "w_o", "b_o")
+    dev = lambda a: torch.from_numpy(np.ascontiguousarray(a, dtype=np.float32)).to(torch.bfloat16).cuda()
+    p = {k: dev(inp[k]) for k in names}
+    masters = {k: torch.from_numpy(np.asarray(inp[k], dtype=np.float32)).cuda() for k in names}
+    m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=8, fused_only=True)
+    m.bind_master(masters)
+    x, tgt = dev(inp["x"]), dev(inp["target"])
+    y = m.forward(x, p["norm_w"], p["w_qkv"], p["w_o"], p["b_o"], cfg.eps, 8, cfg.batch, cfg.seq)
+    dy = torch.empty_like(y)
+    loss = torch.zeros(1, dtype=torch.float32, device="cuda")
+    tpmlp_mse_loss_grad_noalloc(y, tgt, dy, loss)
+    dx, g = m.backward(dy)
+    m.sgd_step(cfg.lr)
+    m.sync()
+    assert m.fused_active()
+    gpu = {"y": to_np(y), "loss": float(loss.item()), "dy": to_np(dy), "dx": to_np(dx),
+           "grads": {k: to_np(v) for k, v in g.items()}, "master": {k: to_np(v) for k, v in masters.items()}}
+    ora = O.attn_dense_step({k: inp[k] for k in names}, inp["x"], inp["target"], cfg.eps, cfg.lr, cfg.batch,
+                            cfg.n_q, cfg.n_kv)
+    del ora["cache"], ora["new_params"]
+    compare("y", gpu["y"], ora["y"], "bf16")
+    assert abs(gpu["loss"] - ora["loss"]) <= 2e-2 * abs(ora["loss"]), (gpu["loss"], ora["loss"])
+    compare("dy", gpu["dy"], ora["dy"], "bf16")
+    compare("dx", gpu["dx"], ora["grads"]["x"], "bf16")
+    for k in names:
+        compare("d" + k, gpu["grads"][k], ora["grads"][k], "bf16")
+        new = gpu["master"][k]
+        w0 = np.asarray(inp[k], dtype=np.float32).astype(np.float64)
+        ex = 0.5 * np.spacing(np.abs(new).astype(np.float32)).astype(np.float64)
+        compare("post_step_" + k, new, w0 - cfg.lr * ora["grads"][k], "bf16", extra=ex)
+        compare("update_" + k, new - w0, -cfg.lr * ora["grads"][k], "bf16", extra=ex)
