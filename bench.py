@@ -699,6 +699,18 @@ def ours(args):
                 "traffic": traffic, "bytes_per_launch": nbytes, "avg_launch_ms": per_launch_ms}
     roof["traffic_source"] = traffic_src if traffic is not None else \
         "null: no ncu DRAM record for this workload on the current kernel sources"
+    # every kernel against its own roofline: GEMMs' algorithmic flops against the bf16 peak the
+    # dominant kernel uses, memory-bound kernels' algorithmic bytes against the measured copy rate
+    tpeak, _ = choose_peak(pk, clk, (ms + ems + kms) / 1e3, ratio)
+    kfrac = {}
+    for kname, (kms_tot, kn) in ktimes.items():
+        per = kms_tot / max(1, kn) / 1e3
+        if kname in units:
+            kfrac[kname] = units[kname] * N * H * F / per / 1e12 / tpeak
+        else:
+            nb = hbm_bytes(kname, cfg, masters=True)
+            if nb:
+                kfrac[kname] = nb / per / 1e9 / pk["hbm_gbs"]
     cpu = None
     if cpu_inp is not None:
         v, n, dt = cpu_oracle_tflops(cfg, cpu_inp, budget_s=args.cpu_budget)
@@ -720,6 +732,7 @@ def ours(args):
         "gemm_only_tflops": flops_step * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None,
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][0])},
         "instrumented_ms_per_step": kms / args.steps,
+        "kernel_frac_of_roofline": {k: round(v, 3) for k, v in sorted(kfrac.items(), key=lambda kv: -kv[1])},
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "TFLOP/s", "h2d_bytes_per_step": 2 * N * H * e,

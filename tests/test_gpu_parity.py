@@ -94,15 +94,17 @@ def test_bf16_config_h2048_full_every_t():
         compare_step(cfg, gpu, ora, inp, 0.1)
 
 
-def test_bf16_tail_split_long_contraction():
-    """Contractions long enough for the tail split along K (F = 12288, 2F = 24576) on two and
-    four row blocks: the down and dN GEMMs run each tile in four K parts whose partial sums the
-    first part adds, for CTA pairs and single-CTA tiles, against the oracle, and bit-identical
-    on a repeat."""
+@pytest.mark.parametrize("N,H,ts", [(512, 256, ((1, 0), (4, 0), (4, 8))), (300, 328, ((3, 0), (3, 8)))])
+def test_bf16_tail_split_long_contraction(N, H, ts):
+    """Contractions long enough for the tail split along K (F = 12288, 2F = 24576) on a few
+    tiles: the down and dN GEMMs run each tile in four K parts whose partial sums the first
+    part adds, for CTA pairs and single-CTA tiles (flag 8), on whole and on ragged tiles
+    (300 tokens, H = 328), against the oracle, and bit-identical on a repeat."""
     from tensor_transformer_mlp_rmsnorm_gb300 import DBG_GEMM_SINGLE_CTA
-    cfg = synth.CONFIGS["bf16_h2048"].with_shape(512, 256, 12288)
+    assert DBG_GEMM_SINGLE_CTA == 8
+    cfg = synth.CONFIGS["bf16_h2048"].with_shape(N, H, 12288)
     inp = synth.make_inputs(cfg, seed=21)
-    for t, flags in ((1, 0), (4, 0), (4, DBG_GEMM_SINGLE_CTA)):
+    for t, flags in ts:
         ora = oracle_step(cfg, inp, t, 0.1)
         gpu = gpu_step(cfg, inp, t, 0.1, flags=flags)
         compare_step(cfg, gpu, ora, inp, 0.1)
