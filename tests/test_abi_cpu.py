@@ -197,3 +197,16 @@ def test_cpu_baselines_time_the_oracle_on_a_bounded_sample():
     assert v > 0 and n == 64 and dt > 0
     v, n, dt = bench.cpu_attn_oracle_tflops(acfg, ainp, budget_s=1e9, min_seq=64, max_seq=128)
     assert n == 128  # doubled up to the cap, never past it
+
+
+def test_peak_choice_follows_clock_and_region_length():
+    # burst only for a short region at near-maximum clock; the contraction-dtype ratio scales both
+    import bench
+    pk = {"bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+    hot = {"sm_mhz": 2000, "sm_max_mhz": 2070}
+    slow = {"sm_mhz": 1700, "sm_max_mhz": 2070}
+    assert bench.choose_peak(pk, hot, 0.5) == (1900.0, "burst")
+    assert bench.choose_peak(pk, hot, 3.0) == (1700.0, "sustained")
+    assert bench.choose_peak(pk, slow, 0.5) == (1700.0, "sustained")
+    assert bench.choose_peak(pk, None, 0.5) == (1700.0, "sustained")
+    assert bench.choose_peak(pk, hot, 0.5, ratio=2.0) == (3800.0, "burst")
