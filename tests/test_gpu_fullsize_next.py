@@ -8,7 +8,10 @@ identities that hold at any size:
   the exact step inside the FP8 band (normwise per row, relative to the MLP
   output for y); the MLP identities with the tolerance widened to the FP8
   band, because the two sides of each identity quantise different tensors
-  (dy against Q(dy), W against Q(W));
+  (dy against Q(dy), W against Q(W)); and the whole E4M3 step element by
+  element against the oracle's float64 E4M3 step on the same stored bf16
+  operands (y, loss, dx, every gradient, the post-step masters; about 3.5
+  minutes of host time);
 * attention (4 x 2048 tokens, hidden 4096, 32/8 heads of 128, t = 8): the
   whole step element by element against the oracle's float64 dense step
   (about 15 s of host time); and, as an independent check, y of sampled rows
@@ -154,3 +157,23 @@ def test_attention_gpt_h4096_whole_step():
         ex = 0.5 * np.spacing(np.abs(new).astype(np.float32)).astype(np.float64)
         compare("post_step_" + k, new, w0 - cfg.lr * ora["grads"][k], "bf16", extra=ex)
         compare("update_" + k, new - w0, -cfg.lr * ora["grads"][k], "bf16", extra=ex)
+
+
+def test_fp8_step_llama8b_whole_step():
+    """The E4M3 step at the benchmark size (16384 x 4096 x 14336, t = 8) element by element
+    against the oracle's E4M3 step in float64 (every GEMM on E4M3 codes of the stored bf16
+    operands with per-tensor scales): y, the loss, dx, every parameter gradient and the
+    post-step masters, at the FP8 tolerance of tests/_util.py."""
+    from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP
+    from tests._util import compare_step
+    cfg = synth.CONFIGS["bf16_llama8b"]
+    inp = synth.make_inputs(cfg)
+    m = TPMLP(cfg.tokens, cfg.hidden, cfg.ffn, max_t=8, dtype="bf16", act="swiglu")
+    m.set_precision("fp8")
+    gpu = gpu_step(cfg, inp, 8, cfg.lr, mod=m)
+    del gpu["new_params"]
+    m.close()
+    p = {k: inp[k] for k in synth.param_names(cfg.act)}
+    ora = O.dense_step_fp8(p, inp["x"], inp["target"], cfg.eps, cfg.lr, cfg.act, store=synth.round_to_bf16)
+    del ora["new_params"]
+    compare_step(cfg, gpu, ora, inp, cfg.lr, tol="fp8")
