@@ -61,7 +61,7 @@ constexpr uint64_t WAIT_LIMIT_NS = 1000000000ull;   // 1 s per wait
 constexpr uint64_t DRAIN_LIMIT_NS = 200000000ull;   // 0.2 s for draining after an abort
 constexpr uint64_t PEER_DRAIN_NS = 5000000ull;      // 5 ms: a CTA-pair peer's loads land long before this
 constexpr uint64_t FORCED_LIMIT_NS = 2000000ull;    // 2 ms for the forced-timeout debug wait
-constexpr int SPLIT_MIN_KBLOCKS = 192;              // shortest contraction whose tail is split
+constexpr int SPLIT_MIN_KBLOCKS = 64;               // shortest contraction whose tail is split
 
 // Epilogues that read global inputs (the residual x, or G and U, or Z) bring
 // them into shared memory with TMA as well.
@@ -247,17 +247,44 @@ __device__ __forceinline__ void unpack8_bf16(uint4 v, float* f) {
   }
 }
 
-// r[i] += src[i] for 32 consecutive floats of a scratch row (read past L1:
-// other CTAs wrote them during this launch).
-__device__ __forceinline__ void add32_from(uint32_t (&r)[32], const float* src) {
-  const float4* s4 = reinterpret_cast<const float4*>(src);
+// Partial accumulators of a split tile.  A warp's 32 rows x BN columns of one
+// later K part are one 32 KB block, laid out lane-minor so that every warp
+// access covers 512 contiguous bytes: float4 number (cc * 8 + k) * 32 + lane
+// holds columns cc * 32 + 4 k .. + 3 of the lane's row.  The same thread
+// (same CTA rank, warp quarter and lane) writes a block and reads it back.
+__device__ __forceinline__ void dump32_to(float4* blk, int cc, int lane, const uint32_t (&r)[32]) {
 #pragma unroll
-  for (int k = 0; k < 8; ++k) {
-    const float4 v = __ldcg(s4 + k);
-    r[4 * k] = __float_as_uint(__uint_as_float(r[4 * k]) + v.x);
-    r[4 * k + 1] = __float_as_uint(__uint_as_float(r[4 * k + 1]) + v.y);
-    r[4 * k + 2] = __float_as_uint(__uint_as_float(r[4 * k + 2]) + v.z);
-    r[4 * k + 3] = __float_as_uint(__uint_as_float(r[4 * k + 3]) + v.w);
+  for (int k = 0; k < 8; ++k)
+    __stcg(blk + (cc * 8 + k) * 32 + lane, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
+                                                       __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
+}
+
+// r += the later parts' columns cc * 32 .. + 31 of this lane's row, added in
+// part order (read past L1: other CTAs wrote them during this launch).  Two
+// parts' loads are in flight at a time.
+__device__ __forceinline__ void add_parts(uint32_t (&r)[32], const float4* blk1, size_t part_stride4, int split,
+                                          int cc, int lane) {
+#pragma unroll 1
+  for (int p0 = 1; p0 < split; p0 += 2) {
+    float4 v[2][8];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (p0 + j < split) {
+        const float4* b = blk1 + (size_t)(p0 + j - 1) * part_stride4 + cc * 256 + lane;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) v[j][k] = __ldcg(b + k * 32);
+      }
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (p0 + j < split) {
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          r[4 * k] = __float_as_uint(__uint_as_float(r[4 * k]) + v[j][k].x);
+          r[4 * k + 1] = __float_as_uint(__uint_as_float(r[4 * k + 1]) + v[j][k].y);
+          r[4 * k + 2] = __float_as_uint(__uint_as_float(r[4 * k + 2]) + v[j][k].z);
+          r[4 * k + 3] = __float_as_uint(__uint_as_float(r[4 * k + 3]) + v[j][k].w);
+        }
+      }
   }
 }
 
@@ -718,14 +745,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr int CHUNKS = EPI == EPI_GATEUP_SWIGLU ? BN / 2 / 32 : BN / 32;
       const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      // Split tiles: this warp's arrival counter, and this lane's row in a
-      // scratch slot (one slot of TILE_M x BN floats per later part).
+      // Split tiles: this warp's arrival counter, and its block in the first
+      // later part's scratch slot (one slot of TILE_M x BN floats per later
+      // part, part_stride4 float4s apart).
       const bool split = un.tile >= p.split_first;
       const int ti = un.tile - p.split_first;
       uint32_t* ctr = split ? p.counters + ((size_t)ti * 2 + rank) * 4 + q : nullptr;
-      const float* slots =
-          split ? p.scratch + ((size_t)ti * (p.split - 1) * C::TILE_M + (size_t)rank * BM + q * 32 + lane) * BN
-                : nullptr;
+      constexpr size_t part_stride4 = (size_t)C::TILE_M * BN / 4;
+      float4* blk1 = split ? reinterpret_cast<float4*>(p.scratch) +
+                                 ((size_t)ti * (p.split - 1) * C::TILE_M + (size_t)rank * BM + q * 32) * (BN / 4)
+                           : nullptr;
       if (split && un.part > 0) {
         // A later K part: leave the raw accumulator rows of this warp in its
         // slot, then count this warp's arrival (release) for the first part.
@@ -734,17 +763,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (!ok) break;
         tc_fence_after();
         if (row0 < p.M) {
-          float* dst = const_cast<float*>(slots) + (size_t)(un.part - 1) * C::TILE_M * BN;
+          float4* blk = blk1 + (size_t)(un.part - 1) * part_stride4;
 #pragma unroll 1
           for (int c = 0; c < BN / 32; ++c) {
             uint32_t r[32];
             tmem_ld_32x32b_x32(tbase + c * 32, r);
             tmem_ld_wait();
-            float4* d4 = reinterpret_cast<float4*>(dst + c * 32);
-#pragma unroll
-            for (int k = 0; k < 8; ++k)
-              __stcg(d4 + k, make_float4(__uint_as_float(r[4 * k]), __uint_as_float(r[4 * k + 1]),
-                                         __uint_as_float(r[4 * k + 2]), __uint_as_float(r[4 * k + 3])));
+            dump32_to(blk, c, lane, r);
           }
         }
         __threadfence();
@@ -826,12 +851,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tmem_ld_wait();
         if (split) {
           // the later parts' partial sums, added in part order
-#pragma unroll 1
-          for (int part = 1; part < p.split; ++part) {
-            const float* src = slots + (size_t)(part - 1) * C::TILE_M * BN;
-            add32_from(r0, src + c * 32);
-            if (EPI == EPI_GATEUP_SWIGLU) add32_from(r1, src + BN / 2 + c * 32);
-          }
+          add_parts(r0, blk1, part_stride4, p.split, c, lane);
+          if (EPI == EPI_GATEUP_SWIGLU) add_parts(r1, blk1, part_stride4, p.split, BN / 64 + c, lane);
         }
         if (F8) {
 #pragma unroll
@@ -938,11 +959,10 @@ cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStre
   // so that the round takes about 1/S of a tile's time.  The tail units
   // [T - r, T - r + r S) all fall in the last round (T - r is a multiple of
   // W), one per worker and after its whole tiles, so a first part only ever
-  // waits on workers that wait on nobody.  Only long contractions are split:
-  // the first part reads the others' partial rows back at one round trip per
-  // part and chunk (a few microseconds), which a tile of 64 k-blocks (about
-  // 20 us) does not win back (measured: K = 4096 GEMMs 7-14% slower split
-  // four ways, K = 28672 ones faster).
+  // waits on workers that wait on nobody.  Contractions shorter than 64
+  // k-blocks are not split: there the partial sums' round trip through L2
+  // and the counter reset cost more than the shorter round saves (measured:
+  // K = 2048 GEMMs 5% slower split three ways; K >= 4096 ones 1-5% faster).
   TcParams q = p;
   const int W = max_workers;
   if (q.scratch && q.counters && q.causal == CAUSAL_NONE && q.tiles_per_batch == q.num_tiles &&
