@@ -402,7 +402,7 @@ TPMLP_API void tpattn_destroy(tpattn_ctx* ctx);
 
 /* Loss and loss gradient without any device allocation or workspace.
  *
- * The paper has no counterpart: this entry point exists for callers that
+ * The method itself has no such call: this entry point exists for callers that
  * cannot call cudaMalloc -- code whose device memory is owned by a host
  * framework's pool and budget, or a latency-bound loop where an allocation
  * (which may synchronise the device) is not acceptable.  It computes the same

@@ -123,7 +123,7 @@ AttnLayout attn_layout(const tpattn_config& c) {
     return o;
   };
   L.status = take(256);
-  L.split_ctr = take(SPLIT_COUNTER_WORDS * sizeof(uint32_t));  // zeroed before each split GEMM
+  L.split_ctr = take(SPLIT_COUNTER_WORDS * sizeof(uint32_t));  // split GEMMs' arrival flags (epoch-tagged)
   L.nrm = take(N * H * 2);
   L.rstd = take(N * 4);
   L.qkv = take(N * W * 2);

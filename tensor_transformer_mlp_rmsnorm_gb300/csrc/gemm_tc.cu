@@ -38,6 +38,8 @@
 
 #include <mutex>
 
+#include <atomic>
+
 #include "epilogue.cuh"
 #include "ptx_sm103.cuh"
 #include "tma_maps.cuh"
@@ -124,9 +126,10 @@ struct TcParams {
   // k-blocks of one tile's contraction (both segments).
   int num_units, split_first, split, kb_total;
   float* scratch;      // partial accumulators of the parts after the first
-  uint32_t* counters;  // per split tile, CTA of the pair and epilogue warp
+  uint32_t* counters;  // arrival flags: per split tile, CTA of the pair, epilogue warp and later part
   size_t scratch_bytes;
   int counter_words;
+  uint32_t epoch;  // value a later part's flag takes in this launch (never 0, unique per launch)
 };
 
 // One work unit: a tile, which of its K parts, and the range [vb, ve) of
@@ -151,15 +154,15 @@ __device__ __forceinline__ Unit unit_of(const TcParams& p, int u) {
   return w;
 }
 
-// Bounded wait until *ctr >= target (acquire at GPU scope).  On a timeout it
+// Bounded wait until *flag == epoch (acquire at GPU scope).  On a timeout it
 // raises the CTA's abort flag and ORs `code` into the status word.
-__device__ __forceinline__ bool wait_count(const uint32_t* ctr, uint32_t target, volatile int* abort,
-                                           uint32_t* status, uint32_t code, uint64_t limit_ns) {
+__device__ __forceinline__ bool wait_flag(const uint32_t* flag, uint32_t epoch, volatile int* abort,
+                                          uint32_t* status, uint32_t code, uint64_t limit_ns) {
   const uint64_t t0 = global_timer_ns();
   for (;;) {
     uint32_t v;
-    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(ctr) : "memory");
-    if (v >= target) return true;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(flag) : "memory");
+    if (v == epoch) return true;
     if (*abort) return false;
     if (global_timer_ns() - t0 > limit_ns) {
       *abort = 1;
@@ -745,19 +748,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       constexpr int CHUNKS = EPI == EPI_GATEUP_SWIGLU ? BN / 2 / 32 : BN / 32;
       const int col_base = EPI == EPI_GATEUP_SWIGLU ? nb * (BN / 2) : nb * BN;
       const uint32_t tbase = tmem_base + ((uint32_t)(q * 32) << 16) + acc * BN;
-      // Split tiles: this warp's arrival counter, and its block in the first
-      // later part's scratch slot (one slot of TILE_M x BN floats per later
-      // part, part_stride4 float4s apart).
+      // Split tiles: this warp's arrival flags (one per later part), and its
+      // block in the first later part's scratch slot (one slot of TILE_M x BN
+      // floats per later part, part_stride4 float4s apart).
       const bool split = un.tile >= p.split_first;
       const int ti = un.tile - p.split_first;
-      uint32_t* ctr = split ? p.counters + ((size_t)ti * 2 + rank) * 4 + q : nullptr;
+      uint32_t* flags = split ? p.counters + (((size_t)ti * 2 + rank) * 4 + q) * (p.split - 1) : nullptr;
       constexpr size_t part_stride4 = (size_t)C::TILE_M * BN / 4;
       float4* blk1 = split ? reinterpret_cast<float4*>(p.scratch) +
                                  ((size_t)ti * (p.split - 1) * C::TILE_M + (size_t)rank * BM + q * 32) * (BN / 4)
                            : nullptr;
       if (split && un.part > 0) {
         // A later K part: leave the raw accumulator rows of this warp in its
-        // slot, then count this warp's arrival (release) for the first part.
+        // slot, then raise this warp's flag (release) for the first part.
         int ok = __all_sync(0xffffffffu, mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status,
                                                    STATUS_TIMEOUT, WAIT_LIMIT_NS));
         if (!ok) break;
@@ -776,7 +779,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         tc_fence_before();
         __syncwarp();
         if (lane == 0) {
-          asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(ctr) : "memory");
+          asm volatile("st.release.gpu.global.u32 [%0], %1;" ::"l"(flags + un.part - 1), "r"(p.epoch) : "memory");
           if (PAIR)
             mbar_arrive_cluster(mapa_shared(smem_u32(&tempty_bar[acc]), 0));
           else
@@ -798,7 +801,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // warp's rows.
         int wok = 1;
         if (lane == 0)
-          wok = wait_count(ctr, (uint32_t)(p.split - 1), abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
+          for (int part = 1; part < p.split && wok; ++part)
+            wok = wait_flag(flags + part - 1, p.epoch, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
         ok = __all_sync(0xffffffffu, wok);
         if (!ok) break;
       }
@@ -925,6 +929,15 @@ struct Maps {
   CUtensorMap a, b, o[3], i[2];
 };
 
+// Epoch of a split launch: unique within the process (every context's GEMMs
+// draw from it), never 0.
+uint32_t next_split_epoch() {
+  static std::atomic<uint32_t> last{0};
+  uint32_t e = last.fetch_add(1, std::memory_order_relaxed) + 1;
+  while (e == 0) e = last.fetch_add(1, std::memory_order_relaxed) + 1;
+  return e;
+}
+
 template <bool PAIR, bool A_MN, bool B_MN, int EPI, bool F8 = false>
 cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStream_t st) {
   using C = TileCfg<PAIR, epi_has_in<EPI>(), epi_single<EPI>()>;
@@ -972,15 +985,15 @@ cudaError_t launch_inst(const Maps& mp, const TcParams& p, int num_sms, cudaStre
     if (S > 4) S = 4;
     if (S > q.kb_total) S = q.kb_total;
     while (S > 1 && ((size_t)r * (S - 1) * C::TILE_M * BN * sizeof(float) > q.scratch_bytes ||
-                     (size_t)r * 8 > (size_t)q.counter_words))
+                     (size_t)r * 8 * (S - 1) > (size_t)q.counter_words))
       --S;
     if (S >= 2) {
       q.split = S;
       q.split_first = q.num_tiles - r;
       q.num_units = q.split_first + r * S;
-      // the arrival counters start from zero in every launch
-      const cudaError_t e = cudaMemsetAsync(q.counters, 0, (size_t)r * 8 * sizeof(uint32_t), st);
-      if (e != cudaSuccess) return e;
+      // Arrival flags are not reset: a flag counts only when it holds this
+      // launch's epoch, which no earlier launch wrote.
+      q.epoch = next_split_epoch();
     }
   }
   const int workers = q.num_units < W ? q.num_units : W;

@@ -105,7 +105,7 @@ Layout make_layout(const tpmlp_config& c) {
     return o;
   };
   L.status = take(256);
-  L.split_ctr = take(SPLIT_COUNTER_WORDS * sizeof(uint32_t));  // zeroed before each split GEMM
+  L.split_ctr = take(SPLIT_COUNTER_WORDS * sizeof(uint32_t));  // split GEMMs' arrival flags (epoch-tagged)
   L.loss_part = take(MAX_LOSS_PARTS * sizeof(double));
   L.norm_part = take(MAX_NORM_PARTS * sizeof(double));
   L.nrm = take(N * H * E);

@@ -85,11 +85,12 @@ struct GemmDesc {
 };
 
 // Workspace regions for the tail split: partial accumulators of up to
-// SPLIT_SLOTS tiles of 256 x 256 f32, and 8 counters (two CTAs of a pair x
-// four epilogue warps) per split tile.
+// SPLIT_SLOTS tiles of 256 x 256 f32 (or twice as many 128 x 256 single-CTA
+// tiles), and an arrival flag per later part of a split tile, CTA of the pair
+// and epilogue warp (8 per slot, 16 per slot for single-CTA tiles).
 constexpr int SPLIT_SLOTS = 160;
 constexpr size_t SPLIT_SCRATCH_BYTES = (size_t)SPLIT_SLOTS * 256 * 256 * 4;
-constexpr int SPLIT_COUNTER_WORDS = SPLIT_SLOTS * 8;
+constexpr int SPLIT_COUNTER_WORDS = SPLIT_SLOTS * 16;
 
 // tcgen05/TMA GEMM for bf16 operands (f32 accumulation in tensor memory), or
 // E4M3 operands with f8 set.  Segment boundaries must be multiples of 64
