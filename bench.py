@@ -459,7 +459,8 @@ def ours_attn(args):
     launches = m.launch_count() - l0 + 2 * args.steps
     ms = e0.elapsed_time(e1)
     barrier()
-    e2e_steps = max(3, args.steps // 2)
+    time.sleep(0.3)  # the same idle pause as before the device-resident loop
+    e2e_steps = max(3, args.steps)
     ems = timed_e2e(torch, step, stream, x_host, tg_host, (x, torch.empty_like(x)),
                     (target, torch.empty_like(target)), loss, loss_host, e2e_steps)
     kms = instrumented_pass(torch, m, step, stream, args.steps)
@@ -637,10 +638,11 @@ def ours(args):
     launches = m.launch_count() - launches0
     ms = e0.elapsed_time(e1)
     # ---------------------------------------------------------- end-to-end through the public API
-    # (right after the device-resident loop, so that both run at the same point of the power cap's
-    # averaging window)
+    # The same number of steps, started like the device-resident loop: after the same idle pause,
+    # so that both begin at the same point of the power cap's averaging window.
     barrier()
-    e2e_steps = max(3, args.steps // 2)
+    time.sleep(0.3)
+    e2e_steps = max(3, args.steps)
     ems = timed_e2e(torch, step, stream, x_host, tg_host, (x, torch.empty_like(x)),
                     (target, torch.empty_like(target)), loss, loss_host, e2e_steps)
     # Per-kernel times come from a third pass of the same steps with the library's CUDA events
