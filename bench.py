@@ -333,29 +333,136 @@ def workload_config(cfg, t: int, world: int) -> dict:
             "parallelism": f"replicas x{world}"}
 
 
+def mlp_config(cfg, t: int, world: int, args, n_params: int) -> dict:
+    """The MLP run's `config`, identical in both arms."""
+    N, H, F = cfg.tokens, cfg.hidden, cfg.ffn
+    e = 2 if cfg.dtype == "bf16" else 4
+    # activations saved and produced per step (x, y, dy, dx, n, G|U, A, dGU, dN) + parameters,
+    # fp32 masters and fp32 gradients
+    ws_gb = (N * H * (5 * e + 4) + N * F * (5 * e if cfg.act == "swiglu" else 3 * e) + n_params * (e + 8)) / 1e9
+    return dict(workload_config(cfg, t, world), optimizer=args.optimizer, gemm_operands=args.precision,
+                sequence_parallel=bool(args.sequence_parallel),
+                l2=f"no flush: per-step working set ~{ws_gb:.1f} GB >> 129 MB L2")
+
+
+def attn_run(args):
+    """The attention workload of this run: (config object, t, whether the fused kernels run)."""
+    cfg = synth.ATTN_CONFIGS[args.workload]
+    if args.tokens:
+        cfg = dataclasses.replace(cfg, batch=max(1, args.tokens // cfg.seq))
+    t = args.t if cfg.n_kv % args.t == 0 else cfg.t_list[0]
+    fused = args.attn_path == "fused" and cfg.d == 128 and cfg.seq % 128 == 0
+    return cfg, t, fused
+
+
+def attn_config(cfg, t: int, world: int, args, fused: bool) -> dict:
+    """The attention run's `config`, identical in both arms."""
+    return {"workload": f"{cfg.name}: attention sublayer, {cfg.batch}x{cfg.seq} tokens, hidden={cfg.hidden}, "
+                        f"{cfg.n_q} query heads in {cfg.n_kv} KV groups, head dim {cfg.d}, causal, t={t} logical shards"
+                        + (f", AdamW {ADAMW}" if args.optimizer == "adamw" else f", lr={cfg.lr}"),
+            "optimizer": args.optimizer,
+            "attention_kernels": "fused (scores never stored)" if fused else "unfused (scores materialised)",
+            "global_batch": cfg.batch * world, "seq_len": cfg.seq, "tokens_per_gpu": cfg.tokens, "t": t,
+            "parallelism": f"replicas x{world}", "l2": "no flush: per-step working set >> 129 MB L2"}
+
+
+def metric_name(args, attention: bool) -> str:
+    m = METRIC if not attention else "TP-attention fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak"
+    return m.replace("SGD", "AdamW") if args.optimizer == "adamw" else m
+
+
 def reference_arm(args):
+    """The oracle, as it stands, on this run's workload and options, timed on the host cores.
+
+    Each step is the oracle's step for the same options (dense SGD step, the AdamW step, the
+    E4M3 step, the sequence-parallel rank decomposition, or the attention sublayer's step) on
+    a bounded token sample with the full weights; the sample is halved until warm-up plus timed
+    steps fit in about 150 s.  The line carries the same metric and config as this run's GPU
+    arm."""
     world, rank, _ = dist_env()
     if rank != 0:
         return 0
-    cfg = synth.CONFIGS[args.workload]
-    if args.tokens:
-        cfg = cfg.with_tokens(args.tokens)
-    # the oracle needs the full weights but only a token sample
-    sample = max(16, args.ref_tokens)
-    inp = synth.make_inputs(cfg.with_tokens(sample), seed=1234)
     from oracle import tpmlp_oracle as O
-    p = {k: inp[k] for k in synth.param_names(cfg.act)}
+    attention = args.workload in synth.ATTN_CONFIGS
     budget = 150.0  # seconds for warmup + timed steps
+    nstep = [0]
+    if attention:
+        if args.precision != "bf16" or args.sequence_parallel:
+            print(json.dumps({"impl": "reference", "unavailable": "the attention sublayer has neither E4M3 "
+                                                                  "operands nor a sequence-parallel form"}))
+            return 0
+        cfg, t, fused = attn_run(args)
+        config = attn_config(cfg, t, world, args, fused)
+        inp = synth.make_attn_inputs(cfg, seed=1234)
+        p = {k: inp[k] for k in ("norm_w", "w_qkv", "w_o", "b_o")}
+        mom = {k: np.zeros_like(v) for k, v in p.items()}
+        vel = {k: np.zeros_like(v) for k, v in p.items()}
+        sample = min(cfg.seq, max(64, args.ref_tokens))
 
-    def step(n):
-        O.dense_step(p, inp["x"][:n], inp["target"][:n], cfg.eps, cfg.lr, cfg.act)
+        def step(n):
+            # a causal prefix of sequence 0 is a complete smaller problem
+            x, tg = inp["x"][:n], inp["target"][:n]
+            if args.optimizer == "adamw":
+                nstep[0] += 1
+                y, c = O.attn_dense_forward(p, x, cfg.eps, 1, cfg.n_q, cfg.n_kv)
+                _, dy = O.mse_loss(y, tg)
+                g = O.attn_dense_backward(p, c, dy)
+                O.adamw(p, {k: g[k] for k in p}, mom, vel, nstep[0], **ADAMW)
+            else:
+                O.attn_dense_step(p, x, tg, cfg.eps, cfg.lr, 1, cfg.n_q, cfg.n_kv)
 
+        def flops_of(n):
+            return dataclasses.replace(cfg, batch=1, seq=n).gemm_flops
+
+        def halve(n):
+            return max(16, n // 2)
+
+        what = "tokens of sequence 0 (a causal prefix)"
+    else:
+        cfg = synth.CONFIGS[args.workload]
+        if args.tokens:
+            cfg = cfg.with_tokens(args.tokens)
+        t = args.t
+        options = (args.optimizer == "adamw") + (args.precision == "fp8") + bool(args.sequence_parallel)
+        if options > 1:
+            print(json.dumps({"impl": "reference", "unavailable": "the oracle has no step combining AdamW, E4M3 "
+                                                                  "operands and the sequence-parallel form"}))
+            return 0
+        # the oracle needs the full weights but only a token sample
+        sample = max(16, args.ref_tokens)
+        if args.sequence_parallel:
+            sample = max(t, sample // t * t)
+        inp = synth.make_inputs(cfg.with_tokens(sample), seed=1234)
+        p = {k: inp[k] for k in synth.param_names(cfg.act)}
+        config = mlp_config(cfg, t, world, args, sum(int(v.size) for v in p.values()))
+        mom = {k: np.zeros_like(v) for k, v in p.items()}
+        vel = {k: np.zeros_like(v) for k, v in p.items()}
+
+        def step(n):
+            x, tg = inp["x"][:n], inp["target"][:n]
+            if args.optimizer == "adamw":
+                nstep[0] += 1
+                O.dense_step_adamw(p, x, tg, cfg.eps, mom, vel, nstep[0], ADAMW, cfg.act)
+            elif args.precision == "fp8":
+                O.dense_step_fp8(p, x, tg, cfg.eps, cfg.lr, cfg.act, store=synth.round_to_bf16)
+            elif args.sequence_parallel:
+                O.sp_step(p, x, tg, cfg.eps, cfg.lr, t, cfg.act)
+            else:
+                O.dense_step(p, x, tg, cfg.eps, cfg.lr, cfg.act)
+
+        def flops_of(n):
+            return cfg.gemm_flops * n / cfg.tokens
+
+        def halve(n):
+            return max(t, n // 2 // t * t) if args.sequence_parallel else max(1, n // 2)
+
+        what = f"of {cfg.tokens} tokens"
     n = sample
     t0 = time.perf_counter()
     step(n)
     one = time.perf_counter() - t0
-    while one * (args.steps + args.warmup) > budget and n > 1:
-        n = max(1, n // 2)
+    while one * (args.steps + args.warmup) > budget and halve(n) < n:
+        n = halve(n)
         t0 = time.perf_counter()
         step(n)
         one = time.perf_counter() - t0
@@ -365,16 +472,15 @@ def reference_arm(args):
     for _ in range(args.steps):
         step(n)
     el = time.perf_counter() - t0
-    flops = cfg.gemm_flops * n / cfg.tokens
-    val = flops * args.steps / el / 1e12
+    val = flops_of(n) * args.steps / el / 1e12
     cores = host_cores()
     line = {
-        "impl": "reference", "metric": METRIC, "value": val, "unit": "TFLOP/s", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
+        "impl": "reference", "metric": metric_name(args, attention), "value": val, "unit": "TFLOP/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": el / args.steps * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": dict(workload_config(cfg, args.t, world), tokens_per_step_sampled=n),
+        "config": config,
         "cpu_baseline": {"value": val, "unit": "TFLOP/s", "cores": cores, "kind": "oracle",
-                         "sample": f"first {n} of {cfg.tokens} tokens per step, full weights, float64 numpy"},
+                         "sample": f"first {n} {what} per step, full weights, float64 numpy"},
         "e2e": {"value": val, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line), flush=True)
@@ -395,10 +501,7 @@ def ours_attn(args):
     from tensor_transformer_mlp_rmsnorm_gb300 import TPAttn, build
     from tensor_transformer_mlp_rmsnorm_gb300.tpmlp import tpmlp_mse_loss_grad_noalloc
     build.build()
-    cfg = synth.ATTN_CONFIGS[args.workload]
-    if args.tokens:
-        cfg = dataclasses.replace(cfg, batch=max(1, args.tokens // cfg.seq))
-    t = args.t if cfg.n_kv % args.t == 0 else cfg.t_list[0]
+    cfg, t, fused_only = attn_run(args)
     inp = synth.make_attn_inputs(cfg, seed=1234 + rank)
     names = ("norm_w", "w_qkv", "w_o", "b_o")
     bf = torch.bfloat16
@@ -410,7 +513,6 @@ def ours_attn(args):
     del inp
     x, target = x_host.to(dev), tg_host.to(dev)
     # the fused path needs no score square in its workspace
-    fused_only = args.attn_path == "fused" and cfg.d == 128 and cfg.seq % 128 == 0
     m = TPAttn(cfg.tokens, cfg.hidden, cfg.n_q, cfg.n_kv, cfg.d, cfg.seq, max_t=t, device=dev, fused_only=fused_only)
     m.bind_master(masters)
     if not fused_only:
@@ -443,6 +545,8 @@ def ours_attn(args):
         step()
     m.sync()
     fused = m.fused_active()
+    if fused != fused_only:
+        raise RuntimeError(f"fused attention active={fused}, expected {fused_only}")
     clocks = ClockSampler(local)
     barrier()
     torch.cuda.synchronize()
@@ -520,18 +624,11 @@ def ours_attn(args):
                "sample": f"dense fwd+loss+bwd+SGD of the first {n} tokens of sequence 0 (a causal prefix) "
                          f"with the full weights, float64 numpy, {dt:.1f} s"}
     line = {
-        "metric": "TP-attention fwd+bwd+SGD TFLOP/s at 1 GB300 and % of BF16 dense tensor peak".replace(
-            "SGD", "AdamW" if adamw else "SGD"),
+        "metric": metric_name(args, True),
         "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps, "warmup": max(3, args.warmup),
         "ms_per_step": ms / args.steps, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": f"{cfg.name}: attention sublayer, {B}x{S} tokens, hidden={H}, {nq} query heads in "
-                               f"{nkv} KV groups, head dim {d}, causal, t={t} logical shards"
-                               + (f", AdamW {ADAMW}" if adamw else f", lr={cfg.lr}"),
-                   "optimizer": args.optimizer,
-                   "attention_kernels": "fused (scores never stored)" if fused else "unfused (scores materialised)",
-                   "global_batch": B * world, "seq_len": S, "tokens_per_gpu": N, "t": t,
-                   "parallelism": f"replicas x{world}", "l2": "no flush: per-step working set >> 129 MB L2"},
+        "config": attn_config(cfg, t, world, args, fused),
         "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
                              "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"], "source": pk_src},
         "gemm_only_tflops": flops * args.steps / (gemm_ms / 1e3) / 1e12 if gemm_ms > 0 else None,
@@ -660,9 +757,6 @@ def ours(args):
     flops_step = cfg.gemm_flops
     e = 2 if cfg.dtype == "bf16" else 4
     nP = sum(v.numel() for v in params.values())
-    # activations saved and produced per step (x, y, dy, dx, n, G|U, A, dGU, dN) + parameters,
-    # fp32 masters and fp32 gradients
-    ws_gb = (N * H * (5 * e + 4) + N * F * (5 * e if cfg.act == "swiglu" else 3 * e) + nP * (e + 8)) / 1e9
     value = flops_step * args.steps * world / (ms / 1e3) / 1e12
     e2e_value = flops_step * e2e_steps * world / (ems / 1e3) / 1e12
     h2d_rate = h2d_gbps(torch, x_host, y)
@@ -719,15 +813,13 @@ def ours(args):
         cpu = {"value": v, "unit": "TFLOP/s", "cores": host_cores(), "kind": "oracle",
                "sample": f"dense fwd+loss+bwd+SGD of the first {n} of {N} tokens with the full weights, "
                          f"float64 numpy, {dt:.1f} s"}
-    metric = METRIC if not adamw else METRIC.replace("SGD", "AdamW")
+    metric = metric_name(args, False)
     line = {
         "metric": metric, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
         "warmup": max(3, args.warmup), "ms_per_step": ms / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "e4m3" if args.precision == "fp8" else cfg.dtype,
         "data": "synthetic",
-        "config": dict(workload_config(cfg, t, world), optimizer=args.optimizer, gemm_operands=args.precision,
-                       sequence_parallel=bool(args.sequence_parallel),
-                       l2=f"no flush: per-step working set ~{ws_gb:.1f} GB >> 129 MB L2"),
+        "config": mlp_config(cfg, t, world, args, nP),
         "pct_of_bf16_peak": {"of_burst": 100.0 * value / world / pk["bf16_tflops"],
                              "of_sustained": 100.0 * value / world / pk["bf16_tflops_sustained"],
                              "source": pk_src},
@@ -772,10 +864,6 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     if args.impl == "reference":
-        if args.workload in synth.ATTN_CONFIGS:
-            print(json.dumps({"impl": "reference", "unavailable": "the reference arm times the MLP oracle; "
-                                                                  "run the attention oracle through the tests"}))
-            return 0
         return reference_arm(args)
     if args.workload in synth.ATTN_CONFIGS:
         return ours_attn(args)

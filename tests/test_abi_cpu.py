@@ -1,6 +1,7 @@
 """The C-ABI library builds, loads and exports every entry point its header
 declares; host-side validation rejects bad configurations without a GPU."""
 import ctypes
+import json
 import os
 import re
 
@@ -210,3 +211,29 @@ def test_peak_choice_follows_clock_and_region_length():
     assert bench.choose_peak(pk, slow, 0.5) == (1700.0, "sustained")
     assert bench.choose_peak(pk, None, 0.5) == (1700.0, "sustained")
     assert bench.choose_peak(pk, hot, 0.5, ratio=2.0) == (3800.0, "burst")
+
+
+def test_reference_arm_prints_the_gpu_arms_config(capsys, monkeypatch):
+    # the reference line carries the metric and config the GPU arm builds for the same options
+    import argparse
+    import bench
+    import synth
+    monkeypatch.delenv("RANK", raising=False)
+    monkeypatch.delenv("WORLD_SIZE", raising=False)
+    base = dict(steps=1, warmup=0, ref_tokens=16, t=8, tokens=0, optimizer="sgd", precision="bf16",
+                sequence_parallel=False, attn_path="fused")
+    args = argparse.Namespace(workload="bf16_llama8b", **base)
+    assert bench.reference_arm(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    cfg = synth.CONFIGS["bf16_llama8b"]
+    n_params = sum(int(v.size) for k, v in synth.make_inputs(cfg.with_tokens(16), seed=1234).items()
+                   if k in synth.param_names(cfg.act))
+    assert line["config"] == json.loads(json.dumps(bench.mlp_config(cfg, 8, 1, args, n_params)))
+    assert line["metric"] == bench.metric_name(args, False) and line["impl"] == "reference"
+    assert line["value"] > 0 and line["e2e"]["h2d_bytes_per_step"] == 0
+    args = argparse.Namespace(workload="attn_gpt_h4096", **dict(base, ref_tokens=64))
+    assert bench.reference_arm(args) == 0
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    acfg, t, fused = bench.attn_run(args)
+    assert fused and line["config"] == json.loads(json.dumps(bench.attn_config(acfg, t, 1, args, fused)))
+    assert line["metric"] == bench.metric_name(args, True)
