@@ -1,6 +1,8 @@
 """GPU parity: the CUDA path through the C ABI against the CPU oracle on the
 same seeded inputs, element by element, for every logical t, both
 activations, ragged shapes, the broken variants and the edge cases."""
+import dataclasses
+
 import numpy as np
 import pytest
 
@@ -92,6 +94,28 @@ def test_bf16_config_h2048_full_every_t():
     for t in cfg.t_list:
         gpu = gpu_step(cfg, inp, t, 0.1)
         compare_step(cfg, gpu, ora, inp, 0.1)
+
+
+@pytest.mark.parametrize("dtype,act", [("bf16", "swiglu"), ("bf16", "gelu"), ("f32", "swiglu")])
+def test_uncommon_t(dtype, act):
+    """Degrees other than the powers of two: t = 3, 12 and 48 on F = 1536 (shards of 512, 128
+    and 32 channels; 32 is below one 64-wide k-block, so shard boundaries fall inside k-blocks).
+    The step must match the oracle's t-rank decomposition, and, since the on-chip sum runs over
+    the FFN axis in one order whatever t is, be bit-identical to t = 1."""
+    base = synth.CONFIGS["bf16_h2048" if dtype == "bf16" else "fp32_small"]
+    N, H = (300, 512) if dtype == "bf16" else (40, 128)
+    cfg = dataclasses.replace(base.with_shape(N, H, 1536), act=act)
+    if act == "gelu":
+        cfg = dataclasses.replace(cfg, b_1_std=0.01)
+    inp = synth.make_inputs(cfg, seed=41)
+    one = gpu_step(cfg, inp, 1, 0.1)
+    for t in (3, 12, 48):
+        gpu = gpu_step(cfg, inp, t, 0.1)
+        compare_step(cfg, gpu, oracle_step(cfg, inp, t, 0.1), inp, 0.1)
+        for k in ("y", "dx"):
+            np.testing.assert_array_equal(gpu[k], one[k], err_msg=(t, k))
+        for k in gpu["grads"]:
+            np.testing.assert_array_equal(gpu["grads"][k], one["grads"][k], err_msg=(t, k))
 
 
 @pytest.mark.parametrize("N,H,ts", [(512, 256, ((1, 0), (4, 0), (4, 8))), (300, 328, ((3, 0), (3, 8)))])
