@@ -173,6 +173,19 @@ def test_skip_reductions_match_oracle(dtype):
 
 
 # ------------------------------------------------------------ edge cases
+@pytest.mark.parametrize("dtype,act,N", [("bf16", "swiglu", 1), ("bf16", "gelu", 2), ("f32", "swiglu", 1)])
+def test_one_or_two_tokens(dtype, act, N):
+    """A one- or two-token batch: one ragged row tile in every GEMM, and weight-gradient
+    contractions of one or two tokens."""
+    base = synth.CONFIGS["bf16_h2048" if dtype == "bf16" else "fp32_small"]
+    cfg = dataclasses.replace(base.with_shape(N, 256, 512), act=act)
+    if act == "gelu":
+        cfg = dataclasses.replace(cfg, b_1_std=0.01)
+    inp = synth.make_inputs(cfg, seed=43)
+    for t in (1, 2):
+        compare_step(cfg, gpu_step(cfg, inp, t, 0.1), oracle_step(cfg, inp, t, 0.1), inp, 0.1)
+
+
 def test_zero_tokens():
     import torch
     from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP
