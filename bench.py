@@ -103,15 +103,17 @@ def recorded_traffic(workload: str, t: int, tokens: int, kernel: str, precision:
     return None, None
 
 
-def hbm_bytes(kernel: str, cfg, masters: bool):
-    """Algorithmic HBM bytes of one launch of a memory-bound kernel."""
+def hbm_bytes(kernel: str, cfg, masters: bool, update_in_backward: bool = False):
+    """Algorithmic HBM bytes of one launch of a memory-bound kernel.  With the update in backward
+    the SGD kernel updates only the vectors (the matrices are updated in their GEMMs' epilogues)."""
     N, H, F = cfg.tokens, cfg.hidden, cfg.ffn
     e = 2 if cfg.dtype == "bf16" else 4
     P = 3 * F * H + 2 * H if cfg.act == "swiglu" else 2 * F * H + F + 2 * H
+    Pu = (2 * H if cfg.act == "swiglu" else F + 2 * H) if update_in_backward else P
     return {"rmsnorm_fwd": 2 * N * H * e + 4 * N + H * e,
             "mse_loss_grad": 3 * N * H * e,
             "rmsnorm_bwd_residual": N * H * 4 + 3 * N * H * e + 4 * N + H * e,
-            "sgd_update": P * (12 + e) if masters else P * (4 + 2 * e),
+            "sgd_update": Pu * (12 + e) if masters else Pu * (4 + 2 * e),
             "grad_sqnorm": 4 * P,
             "adamw_update": P * (28 + e) if masters else P * (20 + 2 * e)}.get(kernel)
 
@@ -697,6 +699,11 @@ def ours(args):
     adamw = args.optimizer == "adamw"
     if adamw:
         m.new_adam_state()
+    # SGD: backward applies the update to the weight matrices where their gradients are produced
+    # (bit-identical to a separate sgd_step), unless --separate-update asks for the separate kernel
+    fused_update = not adamw and not args.separate_update
+    if fused_update:
+        m.set_update_in_backward(True, cfg.lr)
     nstep = [0]
 
     def step(xb=x, tb=target):
@@ -707,7 +714,7 @@ def ours(args):
         if adamw:
             nstep[0] += 1
             m.adamw_step(step=nstep[0], **ADAMW)
-        else:
+        elif not fused_update:
             m.sgd_step(cfg.lr)
 
     def barrier():
@@ -788,7 +795,7 @@ def ours(args):
                 "frac_of_burst": achieved / peak_b, "frac_of_sustained": achieved / peak_s, "traffic": traffic,
                 "flops_per_launch": units[top] * N * H * F, "avg_launch_ms": per_launch_ms}
     else:
-        nbytes = hbm_bytes(top, cfg, masters=True)
+        nbytes = hbm_bytes(top, cfg, masters=True, update_in_backward=fused_update)
         achieved = nbytes / (per_launch_ms / 1e3) / 1e9 if nbytes else None
         roof = {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"] if achieved else None, "peak_kind": f"hbm_gbs ({pk_src})",
@@ -804,7 +811,7 @@ def ours(args):
         if kname in units:
             kfrac[kname] = units[kname] * N * H * F / per / 1e12 / tpeak
         else:
-            nb = hbm_bytes(kname, cfg, masters=True)
+            nb = hbm_bytes(kname, cfg, masters=True, update_in_backward=fused_update)
             if nb:
                 kfrac[kname] = nb / per / 1e9 / pk["hbm_gbs"]
     cpu = None
@@ -862,6 +869,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=20.0)
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--separate-update", action="store_true",
+                    help="MLP with SGD: run the update as its own kernel after backward instead of in backward")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)

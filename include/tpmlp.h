@@ -241,6 +241,25 @@ TPMLP_API tpmlp_status tpmlp_set_precision(tpmlp_ctx* ctx, int32_t precision);
  * requires a new forward. */
 TPMLP_API tpmlp_status tpmlp_set_sequence_parallel(tpmlp_ctx* ctx, int32_t enable);
 
+/* The SGD update applied by backward (bf16 dtype with fp32 masters bound;
+ * "Megatron-LM walkthrough", "Stage 8: the optimizer step").  While enabled,
+ * tpmlp_backward still writes every gradient, and also applies
+ * w <- w - lr * g to the fp32 masters and bf16 copies of the parameters of
+ * the last forward.  With at least 8192 tokens, W_gate_up (W_1) and W_down
+ * are updated inside the epilogues of the GEMMs that produce their
+ * gradients (their contraction over the tokens then hides the masters' reads
+ * and writes); with fewer, and for the other parameters, the update kernel
+ * runs at the end of backward.  The arithmetic is tpmlp_sgd_step's, so
+ * masters and copies are bit-identical to backward followed by
+ * tpmlp_sgd_step(lr).  The data-gradient GEMM into the normed input runs
+ * before the gate/up weight gradient, so every read of a weight precedes its
+ * update.  After such a
+ * backward, tpmlp_sgd_step and tpmlp_adamw_step return TPMLP_ERR_ORDER until
+ * the next forward.  Errors: TPMLP_ERR_UNSUPPORTED for the fp32 dtype,
+ * TPMLP_ERR_ARG for a non-finite lr, and TPMLP_ERR_ORDER from backward when
+ * no masters are bound.  enable = 0 turns it off (lr is then ignored). */
+TPMLP_API tpmlp_status tpmlp_set_update_in_backward(tpmlp_ctx* ctx, int32_t enable, float lr);
+
 /* Debug flags (TPMLP_DBG_*) and the shard whose view the SKIP flags take. */
 TPMLP_API tpmlp_status tpmlp_set_debug(tpmlp_ctx* ctx, uint32_t flags, int32_t shard);
 

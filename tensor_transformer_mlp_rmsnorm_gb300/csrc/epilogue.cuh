@@ -48,6 +48,15 @@ struct EpiParams {
   // output (A, or dG and dU, or dZ) after bf16 rounding, as float bits,
   // combined with atomicMax (the caller zeroes it first).
   uint32_t* amax;
+  // Optional (tensor-core STORE_F32 of a weight gradient): the SGD update
+  // applied where the gradient is produced.  Each output element g also sets
+  // master = fmaf(-sgd_lr, g, master) and writes the new master rounded to
+  // bf16 (nearest even) into sgd_w; both are row-major with leading dimension
+  // sgd_ld and indexed like the output.
+  float* sgd_master;
+  __nv_bfloat16* sgd_w;
+  int64_t sgd_ld;
+  float sgd_lr;
 };
 
 __device__ __forceinline__ float to_f(float v) { return v; }

@@ -291,6 +291,51 @@ __device__ __forceinline__ void add_parts(uint32_t (&r)[32], const float4* blk1,
   }
 }
 
+// The SGD update of 32 consecutive parameters of one row (nv of them valid),
+// where their gradient g is produced, in two halves so that the masters'
+// loads are issued a chunk ahead: sgd_load reads the fp32 masters into
+// registers; sgd_apply forms the separate update kernel's
+// master = fmaf(-lr, g, master), stores it, and stores its bf16 rounding
+// (nearest even) into the parameter copy.  Loops are fully unrolled so that
+// the chunk stays in registers.
+__device__ __forceinline__ void sgd_load(const EpiParams& e, int row, int col, int nv, float (&v)[32]) {
+  const float* m = e.sgd_master + (size_t)row * e.sgd_ld + col;
+  if (nv >= 32) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+      const float4 t = reinterpret_cast<const float4*>(m)[k];
+      v[4 * k] = t.x;
+      v[4 * k + 1] = t.y;
+      v[4 * k + 2] = t.z;
+      v[4 * k + 3] = t.w;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) v[i] = i < nv ? m[i] : 0.0f;
+  }
+}
+__device__ __forceinline__ void sgd_apply(const EpiParams& e, int row, int col, int nv, const float* g,
+                                          float (&v)[32]) {
+  float* m = e.sgd_master + (size_t)row * e.sgd_ld + col;
+  __nv_bfloat16* w = e.sgd_w + (size_t)row * e.sgd_ld + col;
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = fmaf(-e.sgd_lr, g[i], v[i]);
+  if (nv >= 32) {
+#pragma unroll
+    for (int k = 0; k < 8; ++k)
+      reinterpret_cast<float4*>(m)[k] = make_float4(v[4 * k], v[4 * k + 1], v[4 * k + 2], v[4 * k + 3]);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) reinterpret_cast<uint4*>(w)[k] = pack8_bf16(v + 8 * k);
+  } else {
+#pragma unroll
+    for (int i = 0; i < 32; ++i)
+      if (i < nv) {
+        m[i] = v[i];
+        w[i] = __float2bfloat16_rn(v[i]);
+      }
+  }
+}
+
 // Raw bf16 inputs of one epilogue chunk (32 consecutive values of one row,
 // two tensors at most), loaded ahead of the math that uses them.
 struct EpiIn {
@@ -792,6 +837,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
       // The first chunk's inputs are fetched while the tile's main loop runs,
       // each later chunk's while the previous one is computed.
       if (col_base < p.N && row0 < p.M) issue_in(col_base + so.col, row0 + so.row);
+      // Weight gradients with the update applied here: the first chunk's
+      // masters are read while the tile's main loop runs.
+      const bool sgd = EPI == EPI_STORE_F32 && p.ep.sgd_master && row0 + lane < p.M && col_base < p.N;
+      float sgdm[32];
+      if (sgd) sgd_load(p.ep, row0 + lane, col_base, p.N - col_base, sgdm);
       int ok = mbar_wait(&tfull_bar[acc], acc_phase, abort_flag, p.status, STATUS_TIMEOUT, WAIT_LIMIT_NS);
       ok = __all_sync(0xffffffffu, ok);
       if (!ok) break;
@@ -875,6 +925,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
           if (EpiOut<EPI>::N > 1) tma_store_2d(&map_o1, sb + 2048, col + so.col, row0 + so.row);
           if (EpiOut<EPI>::N > 2) tma_store_2d(&map_o2, sb + 4096, col + so.col, row0 + so.row);
           bulk_commit_group();
+        }
+        if (EPI == EPI_STORE_F32 && sgd) {
+          // the next chunk's masters are requested before this chunk's are written
+          float nxt[32];
+          if (more) sgd_load(p.ep, row0 + lane, col + 32, p.N - col - 32, nxt);
+          sgd_apply(p.ep, row0 + lane, col, p.N - col, reinterpret_cast<const float*>(r0), sgdm);
+          if (more) {
+#pragma unroll
+            for (int i = 0; i < 32; ++i) sgdm[i] = nxt[i];
+          }
         }
         ++n_stored;
       }

@@ -180,6 +180,10 @@ struct tpmlp_ctx {
   float *m_norm_w = nullptr, *m_w_gu = nullptr, *m_b_1 = nullptr, *m_w_down = nullptr, *m_b_down = nullptr;
   bool sp = false;  // sequence-parallel form: token shards of N / t rows
   bool fp8 = false;  // E4M3 GEMM operands (needs the FP8 workspace)
+  // SGD applied by backward (tpmlp_set_update_in_backward), and whether the
+  // last backward did so (sgd_step / adamw_step are then refused)
+  bool upd_in_bwd = false, upd_done = false;
+  float upd_lr = 0.0f;
   uint8_t* ws8 = nullptr;
   Fp8Layout L8{};
   tpmlp_param_set adam_m{}, adam_v{};
@@ -557,6 +561,7 @@ tpmlp_status tpmlp_forward(tpmlp_ctx* c, int64_t tokens, const void* x, const vo
     TPMLP_TRY(run_gemm(c, K_GEMM_DOWN, d));
   }
   c->fwd_done = true;
+  c->upd_done = false;
   return TPMLP_OK;
 }
 
@@ -579,6 +584,27 @@ tpmlp_status tpmlp_mse_loss_grad(tpmlp_ctx* c, const void* y, const void* target
   return TPMLP_OK;
 }
 
+// SGD w <- w - lr g over the parameters of the last forward with the gradients
+// of the last backward; the two projection matrices only when `matrices`.
+constexpr int64_t UPDATE_IN_EPILOGUE_MIN_TOKENS = 8192;
+
+static tpmlp_status run_sgd(tpmlp_ctx* c, float lr, bool matrices) {
+  const int64_t H = c->cfg.hidden, F = c->cfg.ffn;
+  const bool sw = c->swiglu();
+  SgdArgs a{};
+  a.lr = lr;
+  auto add = [&](float* m, const float* g, const void* w, int64_t n) {
+    a.seg[a.nseg++] = SgdSeg{m, g, const_cast<void*>(w), n};
+  };
+  add(c->m_norm_w, c->g_norm_w, c->norm_w, H);
+  if (matrices) add(c->m_w_gu, c->g_w_gu, c->w_gu, (sw ? 2 * F : F) * H);
+  if (!sw) add(c->m_b_1, c->g_b_1, c->b_1, F);
+  if (matrices) add(c->m_w_down, c->g_w_down, c->w_down, H * F);
+  add(c->m_b_down, c->g_b_down, c->b_down, H);
+  const int dt = c->cfg.dtype == TPMLP_BF16 ? 1 : 0;
+  return c->run(K_SGD, [&] { return launch_sgd(dt, a, c->num_sms, c->stream); });
+}
+
 tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm_w, float* dw_gate_up, float* db_1,
                             float* dw_down, float* db_down) {
   if (!c) return TPMLP_ERR_ARG;
@@ -596,7 +622,17 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   const bool sw = c->swiglu();
   const int64_t guw = sw ? 2 * F : F;
   const int dt = cf.dtype == TPMLP_BF16 ? 1 : 0;
+  const bool upd = c->upd_in_bwd;
+  if (upd && (!c->m_norm_w || !c->m_w_gu || !c->m_w_down || !c->m_b_down))
+    return c->fail(TPMLP_ERR_ORDER, "the update in backward needs bound fp32 masters");
+  // The weight matrices are updated in their gradient GEMMs' epilogues when
+  // the contraction over tokens is long enough to hide the masters' extra
+  // reads and writes there (measured: K = 8192 and 16384 steps 1.5-2.2%
+  // faster, K = 4096 even, K = 512 19% slower, where the epilogue's stores
+  // already set the pace); otherwise by the update kernel after backward.
+  const bool fuse = upd && N >= UPDATE_IN_EPILOGUE_MIN_TOKENS;
   c->bwd_done = false;
+  c->upd_done = false;
   c->g_norm_w = dnorm_w;
   c->g_w_gu = dw_gate_up;
   c->g_b_1 = db_1;
@@ -611,6 +647,10 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
     if (e == cudaSuccess && db_1) e = cudaMemsetAsync(db_1, 0, (size_t)F * 4, c->stream);
     if (e != cudaSuccess) return c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
     c->bwd_done = true;
+    if (upd) {
+      TPMLP_TRY(run_sgd(c, c->upd_lr, true));
+      c->upd_done = true;
+    }
     return TPMLP_OK;
   }
   void* gu = c->wsp<void>(c->L.gu);
@@ -659,38 +699,18 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   wd.epi = EPI_STORE_F32;
   wd.ep.out0 = dw_down;
   wd.ep.ld_out0 = F;
+  if (fuse) {  // W_down was last read by the dA GEMM above
+    wd.ep.sgd_master = c->m_w_down;
+    wd.ep.sgd_w = static_cast<__nv_bfloat16*>(const_cast<void*>(c->w_down));
+    wd.ep.sgd_ld = F;
+    wd.ep.sgd_lr = c->upd_lr;
+  }
   if (c->fp8) use_fp8(c, wd, F8_DY, true, pitch16(N), F8_ACT, true, pitch16(N), F);
   TPMLP_TRY(run_gemm(c, K_GEMM_WGRAD_DOWN, wd));
 
-  // dW_gate_up = dGU^T n  ([2F, H]; GeLU: dW_1 [F, H]).
-  GemmDesc wg;
-  wg.M = (int)guw;
-  wg.N = (int)H;
-  wg.k_extent = N;
-  wg.a = dgu;
-  wg.lda = guw;
-  wg.a_mn = true;
-  wg.b = nrm;
-  wg.ldb = H;
-  wg.b_mn = true;
-  wg.kseg[1] = N;
-  wg.epi = EPI_STORE_F32;
-  wg.ep.out0 = dw_gate_up;
-  wg.ep.ld_out0 = H;
-  if (c->fp8) {
-    TPMLP_TRY(fp8_cast(c, F8_DGU, dgu, N, guw, true));
-    use_fp8(c, wg, F8_DGU, true, pitch16(N), F8_NRM, true, pitch16(N), H);
-  }
-  TPMLP_TRY(run_gemm(c, K_GEMM_WGRAD_GATEUP, wg));
-
-  if (!sw) {
-    const int nb = colsum_blocks(N, c->num_sms);
-    float* part = c->wsp<float>(c->L.part_b1);
-    TPMLP_TRY(c->run(K_COLSUM_B1, [&] { return launch_colsum_partials(dt, dgu, F, part, N, F, nb, c->stream); }));
-    TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(part, db_1, nullptr, nullptr, nb, F, c->stream); }));
-  }
-
+  if (c->fp8) TPMLP_TRY(fp8_cast(c, F8_DGU, dgu, N, guw, true));
   // dN = sum over shards of dGU_s W_gu,s -- the f all-reduce, summed on chip.
+  // It runs before the gate/up weight gradient, which may update W_gate_up.
   GemmDesc dn;
   dn.M = (int)N;
   dn.N = (int)H;
@@ -714,6 +734,37 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   dn.ep.ld_out0 = H;
   if (c->fp8) use_fp8(c, dn, F8_DGU, false, pitch16(guw), F8_WGU, true, pitch16(guw), H);
   TPMLP_TRY(run_gemm(c, K_GEMM_DGRAD_NORM, dn));
+
+  // dW_gate_up = dGU^T n  ([2F, H]; GeLU: dW_1 [F, H]).
+  GemmDesc wg;
+  wg.M = (int)guw;
+  wg.N = (int)H;
+  wg.k_extent = N;
+  wg.a = dgu;
+  wg.lda = guw;
+  wg.a_mn = true;
+  wg.b = nrm;
+  wg.ldb = H;
+  wg.b_mn = true;
+  wg.kseg[1] = N;
+  wg.epi = EPI_STORE_F32;
+  wg.ep.out0 = dw_gate_up;
+  wg.ep.ld_out0 = H;
+  if (fuse) {  // W_gate_up was last read by the dN GEMM above
+    wg.ep.sgd_master = c->m_w_gu;
+    wg.ep.sgd_w = static_cast<__nv_bfloat16*>(const_cast<void*>(c->w_gu));
+    wg.ep.sgd_ld = H;
+    wg.ep.sgd_lr = c->upd_lr;
+  }
+  if (c->fp8) use_fp8(c, wg, F8_DGU, true, pitch16(N), F8_NRM, true, pitch16(N), H);
+  TPMLP_TRY(run_gemm(c, K_GEMM_WGRAD_GATEUP, wg));
+
+  if (!sw) {
+    const int nb = colsum_blocks(N, c->num_sms);
+    float* part = c->wsp<float>(c->L.part_b1);
+    TPMLP_TRY(c->run(K_COLSUM_B1, [&] { return launch_colsum_partials(dt, dgu, F, part, N, F, nb, c->stream); }));
+    TPMLP_TRY(c->run(K_COLSUM_FINAL, [&] { return launch_colsum_finalize(part, db_1, nullptr, nullptr, nb, F, c->stream); }));
+  }
 
   const int shards = c->sp ? c->t : 1;
   const int nb = rmsnorm_bwd_blocks(N, c->num_sms, shards);
@@ -742,6 +793,11 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
     }));
   }
   c->bwd_done = true;
+  if (upd) {
+    // the matrices too unless their weight-gradient epilogues updated them
+    TPMLP_TRY(run_sgd(c, c->upd_lr, !fuse));
+    c->upd_done = true;
+  }
   return TPMLP_OK;
 }
 
@@ -770,21 +826,19 @@ tpmlp_status tpmlp_bind_master(tpmlp_ctx* c, float* norm_w, float* w_gate_up, fl
 tpmlp_status tpmlp_sgd_step(tpmlp_ctx* c, float lr) {
   if (!c) return TPMLP_ERR_ARG;
   if (!c->bwd_done) return c->fail(TPMLP_ERR_ORDER, "sgd_step before backward");
+  if (c->upd_done) return c->fail(TPMLP_ERR_ORDER, "the last backward already applied the update");
   if (!std::isfinite(lr)) return c->fail(TPMLP_ERR_ARG, "lr must be finite");
-  const int64_t H = c->cfg.hidden, F = c->cfg.ffn;
-  const bool sw = c->swiglu();
-  SgdArgs a{};
-  a.lr = lr;
-  auto add = [&](float* m, const float* g, const void* w, int64_t n) {
-    a.seg[a.nseg++] = SgdSeg{m, g, const_cast<void*>(w), n};
-  };
-  add(c->m_norm_w, c->g_norm_w, c->norm_w, H);
-  add(c->m_w_gu, c->g_w_gu, c->w_gu, (sw ? 2 * F : F) * H);
-  if (!sw) add(c->m_b_1, c->g_b_1, c->b_1, F);
-  add(c->m_w_down, c->g_w_down, c->w_down, H * F);
-  add(c->m_b_down, c->g_b_down, c->b_down, H);
-  const int dt = c->cfg.dtype == TPMLP_BF16 ? 1 : 0;
-  return c->run(K_SGD, [&] { return launch_sgd(dt, a, c->num_sms, c->stream); });
+  return run_sgd(c, lr, true);
+}
+
+tpmlp_status tpmlp_set_update_in_backward(tpmlp_ctx* c, int32_t enable, float lr) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (enable && c->cfg.dtype != TPMLP_BF16)
+    return c->fail(TPMLP_ERR_UNSUPPORTED, "the update in backward is for the bf16 dtype with fp32 masters");
+  if (enable && !std::isfinite(lr)) return c->fail(TPMLP_ERR_ARG, "lr must be finite");
+  c->upd_in_bwd = enable != 0;
+  c->upd_lr = enable ? lr : 0.0f;
+  return TPMLP_OK;
 }
 
 tpmlp_status tpmlp_bind_adam_state(tpmlp_ctx* c, const tpmlp_param_set* m, const tpmlp_param_set* v) {
@@ -813,6 +867,7 @@ tpmlp_status tpmlp_adamw_step(tpmlp_ctx* c, const tpmlp_adamw_params* hp, float*
   if (!c) return TPMLP_ERR_ARG;
   if (!hp) return c->fail(TPMLP_ERR_ARG, "hyperparameters are NULL");
   if (!c->bwd_done) return c->fail(TPMLP_ERR_ORDER, "adamw_step before backward");
+  if (c->upd_done) return c->fail(TPMLP_ERR_ORDER, "the last backward already applied the update");
   if (!c->adam_bound) return c->fail(TPMLP_ERR_ARG, "AdamW moments are not bound");
   if (!std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay) || !std::isfinite(hp->max_grad_norm) ||
       !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f) ||

@@ -84,9 +84,10 @@ def device_inputs(cfg: synth.Config, inp: dict):
 
 
 def gpu_step(cfg: synth.Config, inp: dict, t: int, lr: float, flags: int = 0, shard: int = 0,
-             masters: bool = True, mod=None, with_params: bool = True):
+             masters: bool = True, mod=None, with_params: bool = True, update_in_backward: bool = False):
     """Forward, loss, backward and SGD through the binding; numpy results
-    (the updated parameters only when ``with_params``)."""
+    (the updated parameters only when ``with_params``).  With
+    ``update_in_backward`` the backward applies the SGD update itself."""
     from tensor_transformer_mlp_rmsnorm_gb300 import TPMLP
     m = mod or TPMLP(max(cfg.tokens, 1), cfg.hidden, cfg.ffn, max_t=max(8, t), dtype=cfg.dtype, act=cfg.act)
     d = device_inputs(cfg, inp)
@@ -98,13 +99,18 @@ def gpu_step(cfg: synth.Config, inp: dict, t: int, lr: float, flags: int = 0, sh
               for k in synth.param_names(cfg.act)}
         m.bind_master(ms)
     m.set_debug(flags, shard)
+    if update_in_backward:
+        m.set_update_in_backward(True, lr)
     y = m.forward(d["x"], d["norm_w"], d[gu_key], d["w_down"], d["b_down"], cfg.eps, t,
                   b_1=d.get("b_1"))
     loss, dy = m.mse_loss_grad(y, d["target"])
     dx, g = m.backward(dy)
     grads = {k: to_np(v) for k, v in g.items()}
     out = {"y": to_np(y), "loss": float(loss.item()), "dy": to_np(dy), "dx": to_np(dx), "grads": grads}
-    m.sgd_step(lr)
+    if update_in_backward:
+        m.set_update_in_backward(False)
+    else:
+        m.sgd_step(lr)
     m.sync()
     if with_params:
         if ms is not None:
