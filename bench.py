@@ -724,6 +724,7 @@ def ours(args):
     for _ in range(max(3, args.warmup)):
         step()
     m.sync()
+    matrices_in_epilogue = fused_update and m.update_in_epilogue()
     stream = m.stream
     # ---------------------------------------------------------- device-resident timing
     clocks = ClockSampler(local)
@@ -795,7 +796,7 @@ def ours(args):
                 "frac_of_burst": achieved / peak_b, "frac_of_sustained": achieved / peak_s, "traffic": traffic,
                 "flops_per_launch": units[top] * N * H * F, "avg_launch_ms": per_launch_ms}
     else:
-        nbytes = hbm_bytes(top, cfg, masters=True, update_in_backward=fused_update)
+        nbytes = hbm_bytes(top, cfg, masters=True, update_in_backward=matrices_in_epilogue)
         achieved = nbytes / (per_launch_ms / 1e3) / 1e9 if nbytes else None
         roof = {"kernel": top, "bound": "hbm", "achieved": achieved, "peak": pk["hbm_gbs"], "unit": "GB/s",
                 "frac": achieved / pk["hbm_gbs"] if achieved else None, "peak_kind": f"hbm_gbs ({pk_src})",
@@ -811,7 +812,7 @@ def ours(args):
         if kname in units:
             kfrac[kname] = units[kname] * N * H * F / per / 1e12 / tpeak
         else:
-            nb = hbm_bytes(kname, cfg, masters=True, update_in_backward=fused_update)
+            nb = hbm_bytes(kname, cfg, masters=True, update_in_backward=matrices_in_epilogue)
             if nb:
                 kfrac[kname] = nb / per / 1e9 / pk["hbm_gbs"]
     cpu = None

@@ -260,6 +260,11 @@ TPMLP_API tpmlp_status tpmlp_set_sequence_parallel(tpmlp_ctx* ctx, int32_t enabl
  * no masters are bound.  enable = 0 turns it off (lr is then ignored). */
 TPMLP_API tpmlp_status tpmlp_set_update_in_backward(tpmlp_ctx* ctx, int32_t enable, float lr);
 
+/* 1 if the last backward updated W_gate_up (W_1) and W_down inside their
+ * weight-gradient epilogues, 0 otherwise (no update in backward, fewer than
+ * 8192 tokens, or a NULL context).  Never fails. */
+TPMLP_API int32_t tpmlp_update_in_epilogue(const tpmlp_ctx* ctx);
+
 /* Debug flags (TPMLP_DBG_*) and the shard whose view the SKIP flags take. */
 TPMLP_API tpmlp_status tpmlp_set_debug(tpmlp_ctx* ctx, uint32_t flags, int32_t shard);
 

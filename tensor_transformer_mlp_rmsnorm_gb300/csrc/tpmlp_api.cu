@@ -182,7 +182,7 @@ struct tpmlp_ctx {
   bool fp8 = false;  // E4M3 GEMM operands (needs the FP8 workspace)
   // SGD applied by backward (tpmlp_set_update_in_backward), and whether the
   // last backward did so (sgd_step / adamw_step are then refused)
-  bool upd_in_bwd = false, upd_done = false;
+  bool upd_in_bwd = false, upd_done = false, upd_epi = false;
   float upd_lr = 0.0f;
   uint8_t* ws8 = nullptr;
   Fp8Layout L8{};
@@ -633,6 +633,7 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
   const bool fuse = upd && N >= UPDATE_IN_EPILOGUE_MIN_TOKENS;
   c->bwd_done = false;
   c->upd_done = false;
+  c->upd_epi = false;
   c->g_norm_w = dnorm_w;
   c->g_w_gu = dw_gate_up;
   c->g_b_1 = db_1;
@@ -797,6 +798,7 @@ tpmlp_status tpmlp_backward(tpmlp_ctx* c, const void* dy, void* dx, float* dnorm
     // the matrices too unless their weight-gradient epilogues updated them
     TPMLP_TRY(run_sgd(c, c->upd_lr, !fuse));
     c->upd_done = true;
+    c->upd_epi = fuse;
   }
   return TPMLP_OK;
 }
@@ -830,6 +832,8 @@ tpmlp_status tpmlp_sgd_step(tpmlp_ctx* c, float lr) {
   if (!std::isfinite(lr)) return c->fail(TPMLP_ERR_ARG, "lr must be finite");
   return run_sgd(c, lr, true);
 }
+
+int32_t tpmlp_update_in_epilogue(const tpmlp_ctx* c) { return c && c->upd_done && c->upd_epi ? 1 : 0; }
 
 tpmlp_status tpmlp_set_update_in_backward(tpmlp_ctx* c, int32_t enable, float lr) {
   if (!c) return TPMLP_ERR_ARG;

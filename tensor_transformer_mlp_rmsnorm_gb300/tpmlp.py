@@ -85,6 +85,7 @@ _SIGNATURES = {
     "tpmlp_set_debug": (_i32, [_vp, _u32, _i32]),
     "tpmlp_set_sequence_parallel": (_i32, [_vp, _i32]),
     "tpmlp_set_update_in_backward": (_i32, [_vp, _i32, _f32]),
+    "tpmlp_update_in_epilogue": (_i32, [_vp]),
     "tpmlp_fp8_workspace_bytes": (ctypes.c_size_t, [ctypes.POINTER(Config)]),
     "tpmlp_bind_fp8_workspace": (_i32, [_vp, _vp, ctypes.c_size_t]),
     "tpmlp_set_precision": (_i32, [_vp, _i32]),
@@ -353,6 +354,10 @@ class TPMLP:
     def set_update_in_backward(self, enable: bool, lr: float = 0.0):
         """Have backward apply the SGD update itself (bf16 with bound masters); sgd_step is then not called."""
         _check(lib().tpmlp_set_update_in_backward(self.ctx, int(bool(enable)), float(lr)), self.ctx)
+
+    def update_in_epilogue(self) -> bool:
+        """Whether the last backward updated the weight matrices inside their gradient GEMMs' epilogues."""
+        return bool(lib().tpmlp_update_in_epilogue(self.ctx))
 
     def _param_set(self, d: dict, what: str) -> ParamSet:
         f32 = torch.float32

@@ -64,7 +64,9 @@ def test_bit_identical_to_separate_update(act, N, H, F, t, fp8, sp):
     cfg = _cfg(act, N, H, F)
     inp = synth.make_inputs(cfg, seed=51)
     sep = gpu_step(cfg, inp, t, LR, mod=_module(cfg, t, fp8, sp))
-    fused = gpu_step(cfg, inp, t, LR, mod=_module(cfg, t, fp8, sp), update_in_backward=True)
+    m = _module(cfg, t, fp8, sp)
+    fused = gpu_step(cfg, inp, t, LR, mod=m, update_in_backward=True)
+    assert m.update_in_epilogue() == (N >= 8192)
     _same(fused, sep)
 
 
