@@ -118,6 +118,16 @@ def hbm_bytes(kernel: str, cfg, masters: bool, update_in_backward: bool = False)
             "adamw_update": P * (28 + e) if masters else P * (20 + 2 * e)}.get(kernel)
 
 
+def update_placement(adamw: bool, in_backward: bool, matrices_in_epilogue: bool) -> str:
+    """Where the timed step applies its parameter update."""
+    if adamw:
+        return "AdamW: norm pass and update kernel after backward"
+    if not in_backward:
+        return "SGD: update kernel after backward"
+    return ("SGD in backward: weight matrices in their gradient GEMMs' epilogues, vectors by the update kernel"
+            if matrices_in_epilogue else "SGD in backward: update kernel at the end of backward")
+
+
 def peaks():
     p = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -527,6 +537,11 @@ def ours_attn(args):
     adamw = args.optimizer == "adamw"
     if adamw:
         m.new_adam_state()
+    # SGD: backward applies the update (W_qkv and W_o in their gradient GEMMs' epilogues), as for
+    # the MLP, unless --separate-update asks for the separate kernel
+    fused_update = not adamw and not args.separate_update
+    if fused_update:
+        m.set_update_in_backward(True, cfg.lr)
     nstep = [0]
 
     def step(xb=x, tb=target):
@@ -536,7 +551,7 @@ def ours_attn(args):
         if adamw:
             nstep[0] += 1
             m.adamw_step(step=nstep[0], **ADAMW)
-        else:
+        elif not fused_update:
             m.sgd_step(cfg.lr)
 
     def barrier():
@@ -546,6 +561,7 @@ def ours_attn(args):
     for _ in range(max(3, args.warmup)):
         step()
     m.sync()
+    matrices_in_epilogue = fused_update and m.update_in_epilogue()
     fused = m.fused_active()
     if fused != fused_only:
         raise RuntimeError(f"fused attention active={fused}, expected {fused_only}")
@@ -642,6 +658,7 @@ def ours_attn(args):
                 "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)",
                 "h2d_gbps_alone": h2d_rate},
         "clocks": clk, "gpu_launches": launches, "loss": float(loss_host.item()),
+        "update": update_placement(adamw, fused_update, matrices_in_epilogue),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -844,6 +861,7 @@ def ours(args):
         "clocks": clk,
         "gpu_launches": launches,
         "loss": float(loss_host.item()),
+        "update": update_placement(adamw, fused_update, matrices_in_epilogue),
     }
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -871,7 +889,7 @@ def main():
     ap.add_argument("--ref-tokens", type=int, default=256)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--separate-update", action="store_true",
-                    help="MLP with SGD: run the update as its own kernel after backward instead of in backward")
+                    help="SGD: run the update as its own kernel after backward instead of in backward")
     args = ap.parse_args()
     if args.impl == "reference":
         return reference_arm(args)

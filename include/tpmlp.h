@@ -127,7 +127,8 @@ TPMLP_API tpmlp_status tpmlp_set_stream(tpmlp_ctx* ctx, void* cuda_stream);
  *  eps: RMSNorm epsilon, inside the square root.  t: logical TP degree,
  *  1 <= t <= max_t and F % t == 0 (the fixture's divisibility assertion).
  * The pointers of x and of the parameters are remembered: backward reads x,
- * and sgd_step updates the parameters in place. */
+ * and the updates write the parameters in place, so they must stay valid
+ * until then. */
 TPMLP_API tpmlp_status tpmlp_forward(tpmlp_ctx* ctx, int64_t tokens, const void* x, const void* norm_w,
                            const void* w_gate_up, const void* b_1, const void* w_down,
                            const void* b_down, float eps, int32_t t, void* y);
@@ -373,7 +374,10 @@ TPMLP_API size_t tpattn_workspace_bytes(const tpattn_config* cfg);
 TPMLP_API tpmlp_status tpattn_create(const tpattn_config* cfg, void* cuda_stream, tpattn_ctx** out);
 TPMLP_API tpmlp_status tpattn_bind_workspace(tpattn_ctx* ctx, void* dev, size_t bytes);
 /* batch sequences of seq tokens (seq % 64 == 0, seq <= max_seq); t divides n_kv_heads.
- * x [batch*seq, H], norm_w [H], w_qkv [(n_q+2n_kv) d, H], w_o [H, n_q d], b_o [H] -> y. */
+ * x [batch*seq, H], norm_w [H], w_qkv [(n_q+2n_kv) d, H], w_o [H, n_q d], b_o [H] -> y.
+ * The pointers of x and of the parameters are remembered: backward reads x,
+ * and the updates write the parameters in place, so they must stay valid
+ * until then. */
 TPMLP_API tpmlp_status tpattn_forward(tpattn_ctx* ctx, int64_t batch, int64_t seq, const void* x, const void* norm_w,
                                       const void* w_qkv, const void* w_o, const void* b_o, float eps, int32_t t,
                                       void* y);
@@ -389,6 +393,28 @@ TPMLP_API tpmlp_status tpattn_set_fused(tpattn_ctx* ctx, int32_t enable);
 /* 1 if the last tpattn_forward ran the fused kernels, 0 if not (or no forward yet). */
 TPMLP_API int32_t tpattn_fused_active(const tpattn_ctx* ctx);
 TPMLP_API tpmlp_status tpattn_sgd_step(tpattn_ctx* ctx, float lr);
+
+/* Have tpattn_backward apply the SGD update itself, as tpmlp_set_update_in_backward
+ * does for the MLP ("Megatron-LM walkthrough", "Stage 8: the optimizer step").
+ * While enabled, tpattn_backward still writes every gradient, and also applies
+ * w <- w - lr * g to the bound fp32 masters and bf16 copies of the parameters
+ * of the last forward.  With at least 8192 tokens (batch * seq), W_qkv and W_o
+ * are updated inside the epilogues of the GEMMs that produce their gradients;
+ * with fewer, and for norm_w and b_o, the update kernel runs at the end of
+ * backward.  Masters and copies are bit-identical to backward followed by
+ * tpattn_sgd_step(lr).  The data-gradient GEMM into the normed input runs
+ * before the QKV weight gradient, and dZ = dy W_o before the output
+ * projection's weight gradient, so every read of a weight precedes its
+ * update.  After such a backward, tpattn_sgd_step and tpattn_adamw_step
+ * return TPMLP_ERR_ORDER until the next forward.  Errors: TPMLP_ERR_ARG for a
+ * non-finite lr, and TPMLP_ERR_ORDER from backward when no masters are bound.
+ * enable = 0 turns it off (lr is then ignored). */
+TPMLP_API tpmlp_status tpattn_set_update_in_backward(tpattn_ctx* ctx, int32_t enable, float lr);
+
+/* 1 if the last tpattn_backward updated W_qkv and W_o inside their
+ * weight-gradient epilogues, 0 otherwise (no update in backward, fewer than
+ * 8192 tokens, or a NULL context).  Never fails. */
+TPMLP_API int32_t tpattn_update_in_epilogue(const tpattn_ctx* ctx);
 
 /* The attention sublayer's four parameters, one fp32 device tensor each
  * (shapes as in tpattn_forward); used for the AdamW moments. */

@@ -153,6 +153,9 @@ struct tpattn_ctx {
   uint8_t* ws = nullptr;
   AttnLayout L{};
   bool fwd_done = false, bwd_done = false;
+  // SGD applied by backward (tpattn_set_update_in_backward) and what the last backward did
+  bool upd_in_bwd = false, upd_done = false, upd_epi = false;
+  float upd_lr = 0.0f;
   bool fused = true, fwd_fused = false;
   int64_t batch = 0, seq = 0;
   const void *x = nullptr, *norm_w = nullptr, *w_qkv = nullptr, *w_o = nullptr, *b_o = nullptr;
@@ -556,9 +559,29 @@ tpmlp_status tpattn_forward(tpattn_ctx* c, int64_t batch, int64_t seq, const voi
   o.ep.vec = b_o;
   ATTN_TRY(c->gemm(A_GEMM_OUT, o));
   c->fwd_done = true;
+  c->upd_done = false;
   return TPMLP_OK;
 }
 
+
+constexpr int64_t ATTN_UPDATE_IN_EPILOGUE_MIN_TOKENS = 8192;
+
+// SGD w <- w - lr g over the parameters of the last forward with the gradients
+// of the last backward; the two projection matrices only when `matrices`.
+static tpmlp_status attn_run_sgd(tpattn_ctx* c, float lr, bool matrices) {
+  const tpattn_config& cf = c->cfg;
+  const int64_t H = cf.hidden, d = cf.head_dim, W = (int64_t)(cf.n_heads + 2 * cf.n_kv_heads) * d,
+                Zc = (int64_t)cf.n_heads * d;
+  SgdArgs a{};
+  a.lr = lr;
+  a.seg[a.nseg++] = SgdSeg{c->m_norm_w, c->g_norm_w, const_cast<void*>(c->norm_w), H};
+  if (matrices) {
+    a.seg[a.nseg++] = SgdSeg{c->m_w_qkv, c->g_w_qkv, const_cast<void*>(c->w_qkv), W * H};
+    a.seg[a.nseg++] = SgdSeg{c->m_w_o, c->g_w_o, const_cast<void*>(c->w_o), H * Zc};
+  }
+  a.seg[a.nseg++] = SgdSeg{c->m_b_o, c->g_b_o, const_cast<void*>(c->b_o), H};
+  return c->run(A_SGD, [&] { return launch_sgd(1, a, c->num_sms, c->stream); });
+}
 
 tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dnorm_w, float* dw_qkv, float* dw_o,
                              float* db_o) {
@@ -571,7 +594,15 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   const tpattn_config& cf = c->cfg;
   const int B = (int)c->batch, S = (int)c->seq, N = B * S, H = (int)cf.hidden, d = cf.head_dim;
   const int nq = cf.n_heads, nkv = cf.n_kv_heads, W = (nq + 2 * nkv) * d, Zc = nq * d;
+  const bool upd = c->upd_in_bwd;
+  if (upd && (!c->m_norm_w || !c->m_w_qkv || !c->m_w_o || !c->m_b_o))
+    return c->fail(TPMLP_ERR_ORDER, "the update in backward needs bound fp32 masters");
+  // W_qkv and W_o are updated in their weight-gradient epilogues from 8192
+  // tokens (as in the MLP), otherwise by the update kernel after backward
+  const bool fuse = upd && N >= ATTN_UPDATE_IN_EPILOGUE_MIN_TOKENS;
   c->bwd_done = false;
+  c->upd_done = false;
+  c->upd_epi = false;
   c->g_norm_w = dnorm_w;
   c->g_w_qkv = dw_qkv;
   c->g_w_o = dw_o;
@@ -615,6 +646,12 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   wo.epi = EPI_STORE_F32;
   wo.ep.out0 = dw_o;
   wo.ep.ld_out0 = Zc;
+  if (fuse) {  // W_o was last read by the dZ GEMM above
+    wo.ep.sgd_master = c->m_w_o;
+    wo.ep.sgd_w = static_cast<__nv_bfloat16*>(const_cast<void*>(c->w_o));
+    wo.ep.sgd_ld = Zc;
+    wo.ep.sgd_lr = c->upd_lr;
+  }
   ATTN_TRY(c->gemm(A_GEMM_WGRAD_OUT, wo));
   if (c->fwd_fused) {
     float* dq_acc = c->wsp<float>(c->L.dkv_head);
@@ -630,6 +667,22 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   } else {
     ATTN_TRY(attn_core_bwd_unfused(c, B, S, qkv, dz, dqkv, dp, pr, dkv));
   }
+  // dN = dqkv W_qkv: every head's contribution summed on chip (the f all-reduce);
+  // it runs before the QKV weight gradient, which may update W_qkv
+  GemmDesc dn;
+  dn.M = N;
+  dn.N = H;
+  dn.k_extent = W;
+  dn.a = dqkv;
+  dn.lda = W;
+  dn.b = c->w_qkv;
+  dn.ldb = H;
+  dn.b_mn = true;
+  dn.kseg[1] = W;
+  dn.epi = EPI_STORE_F32;
+  dn.ep.out0 = dnrm;
+  dn.ep.ld_out0 = H;
+  ATTN_TRY(c->gemm(A_GEMM_DGRAD_NORM, dn));
   // dW_qkv = dqkv^T n
   GemmDesc wq;
   wq.M = W;
@@ -645,22 +698,13 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   wq.epi = EPI_STORE_F32;
   wq.ep.out0 = dw_qkv;
   wq.ep.ld_out0 = H;
+  if (fuse) {  // W_qkv was last read by the dN GEMM above
+    wq.ep.sgd_master = c->m_w_qkv;
+    wq.ep.sgd_w = static_cast<__nv_bfloat16*>(const_cast<void*>(c->w_qkv));
+    wq.ep.sgd_ld = H;
+    wq.ep.sgd_lr = c->upd_lr;
+  }
   ATTN_TRY(c->gemm(A_GEMM_WGRAD_QKV, wq));
-  // dN = dqkv W_qkv: every head's contribution summed on chip (the f all-reduce)
-  GemmDesc dn;
-  dn.M = N;
-  dn.N = H;
-  dn.k_extent = W;
-  dn.a = dqkv;
-  dn.lda = W;
-  dn.b = c->w_qkv;
-  dn.ldb = H;
-  dn.b_mn = true;
-  dn.kseg[1] = W;
-  dn.epi = EPI_STORE_F32;
-  dn.ep.out0 = dnrm;
-  dn.ep.ld_out0 = H;
-  ATTN_TRY(c->gemm(A_GEMM_DGRAD_NORM, dn));
   const int nb = rmsnorm_bwd_blocks(N, c->num_sms, 1);
   float* pdw = c->wsp<float>(c->L.part_dw);
   float* pdb = c->wsp<float>(c->L.part_db);
@@ -670,6 +714,12 @@ tpmlp_status tpattn_backward(tpattn_ctx* c, const void* dy, void* dx, float* dno
   }));
   ATTN_TRY(c->run(A_COLSUM, [&] { return launch_colsum_finalize(pdw, dnorm_w, pdb, db_o, nb, H, c->stream); }));
   c->bwd_done = true;
+  if (upd) {
+    // the matrices too unless their weight-gradient epilogues updated them
+    ATTN_TRY(attn_run_sgd(c, c->upd_lr, !fuse));
+    c->upd_done = true;
+    c->upd_epi = fuse;
+  }
   return TPMLP_OK;
 }
 
@@ -699,18 +749,20 @@ int32_t tpattn_fused_active(const tpattn_ctx* c) { return c && c->fwd_done && c-
 tpmlp_status tpattn_sgd_step(tpattn_ctx* c, float lr) {
   if (!c) return TPMLP_ERR_ARG;
   if (!c->bwd_done) return c->fail(TPMLP_ERR_ORDER, "sgd_step before backward");
+  if (c->upd_done) return c->fail(TPMLP_ERR_ORDER, "the last backward already applied the update");
   if (!std::isfinite(lr)) return c->fail(TPMLP_ERR_ARG, "lr must be finite");
-  const tpattn_config& cf = c->cfg;
-  const int64_t H = cf.hidden, d = cf.head_dim, W = (int64_t)(cf.n_heads + 2 * cf.n_kv_heads) * d,
-                Zc = (int64_t)cf.n_heads * d;
-  SgdArgs a{};
-  a.lr = lr;
-  a.seg[a.nseg++] = SgdSeg{c->m_norm_w, c->g_norm_w, const_cast<void*>(c->norm_w), H};
-  a.seg[a.nseg++] = SgdSeg{c->m_w_qkv, c->g_w_qkv, const_cast<void*>(c->w_qkv), W * H};
-  a.seg[a.nseg++] = SgdSeg{c->m_w_o, c->g_w_o, const_cast<void*>(c->w_o), H * Zc};
-  a.seg[a.nseg++] = SgdSeg{c->m_b_o, c->g_b_o, const_cast<void*>(c->b_o), H};
-  return c->run(A_SGD, [&] { return launch_sgd(1, a, c->num_sms, c->stream); });
+  return attn_run_sgd(c, lr, true);
 }
+
+tpmlp_status tpattn_set_update_in_backward(tpattn_ctx* c, int32_t enable, float lr) {
+  if (!c) return TPMLP_ERR_ARG;
+  if (enable && !std::isfinite(lr)) return c->fail(TPMLP_ERR_ARG, "lr must be finite");
+  c->upd_in_bwd = enable != 0;
+  c->upd_lr = enable ? lr : 0.0f;
+  return TPMLP_OK;
+}
+
+int32_t tpattn_update_in_epilogue(const tpattn_ctx* c) { return c && c->upd_done && c->upd_epi ? 1 : 0; }
 
 tpmlp_status tpattn_bind_adam_state(tpattn_ctx* c, const tpattn_param_set* m, const tpattn_param_set* v) {
   if (!c) return TPMLP_ERR_ARG;
@@ -739,6 +791,7 @@ tpmlp_status tpattn_adamw_step(tpattn_ctx* c, const tpmlp_adamw_params* hp, floa
   if (!c) return TPMLP_ERR_ARG;
   if (!hp) return c->fail(TPMLP_ERR_ARG, "hyperparameters are NULL");
   if (!c->bwd_done) return c->fail(TPMLP_ERR_ORDER, "adamw_step before backward");
+  if (c->upd_done) return c->fail(TPMLP_ERR_ORDER, "the last backward already applied the update");
   if (!c->adam_bound) return c->fail(TPMLP_ERR_ARG, "AdamW moments are not bound");
   if (!std::isfinite(hp->lr) || !std::isfinite(hp->weight_decay) || !std::isfinite(hp->max_grad_norm) ||
       !(hp->beta1 >= 0.f && hp->beta1 < 1.f) || !(hp->beta2 >= 0.f && hp->beta2 < 1.f) ||

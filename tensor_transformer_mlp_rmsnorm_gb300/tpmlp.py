@@ -106,6 +106,8 @@ _SIGNATURES = {
     "tpattn_backward": (_i32, [_vp, _vp, _vp, _fp, _fp, _fp, _fp]),
     "tpattn_bind_master": (_i32, [_vp, _fp, _fp, _fp, _fp]),
     "tpattn_sgd_step": (_i32, [_vp, _f32]),
+    "tpattn_set_update_in_backward": (_i32, [_vp, _i32, _f32]),
+    "tpattn_update_in_epilogue": (_i32, [_vp]),
     "tpattn_bind_adam_state": (_i32, [_vp, ctypes.POINTER(AttnParamSet), ctypes.POINTER(AttnParamSet)]),
     "tpattn_adamw_step": (_i32, [_vp, ctypes.POINTER(AdamWParams), _fp]),
     "tpattn_set_fused": (_i32, [_vp, _i32]),
@@ -295,6 +297,9 @@ class TPMLP:
         yp = self._t(y, (n, self.H), name="y")
         self._fwd = False
         _check(lib().tpmlp_forward(self.ctx, n, *args, float(eps), int(t), yp), self.ctx)
+        # the library keeps these pointers (backward reads x; the updates write the parameters):
+        # hold the tensors until the next forward so that a temporary argument is not freed
+        self._fwd_tensors = (x, norm_w, w_gate_up, b_1, w_down, b_down)
         self.tokens = n
         self._fwd = True
         return y
@@ -488,6 +493,9 @@ class TPAttn:
                                      self._t(w_o, (self.H, self.nq * self.d), name="w_o"),
                                      self._t(b_o, (self.H,), name="b_o"), float(eps), int(t),
                                      self._t(y, (n, self.H), name="y")), self.ctx)
+        # the library keeps these pointers (backward reads x; the updates write the parameters):
+        # hold the tensors until the next forward so that a temporary argument is not freed
+        self._fwd_tensors = (x, norm_w, w_qkv, w_o, b_o)
         self.params = (norm_w, w_qkv, w_o, b_o)
         self.tokens = n
         return y
@@ -524,6 +532,14 @@ class TPAttn:
 
     def sgd_step(self, lr: float):
         _acheck(lib().tpattn_sgd_step(self.ctx, float(lr)), self.ctx)
+
+    def set_update_in_backward(self, enable: bool, lr: float = 0.0):
+        """Have backward apply the SGD update itself (needs bound masters); sgd_step is then not called."""
+        _acheck(lib().tpattn_set_update_in_backward(self.ctx, int(bool(enable)), float(lr)), self.ctx)
+
+    def update_in_epilogue(self) -> bool:
+        """Whether the last backward updated W_qkv and W_o inside their gradient GEMMs' epilogues."""
+        return bool(lib().tpattn_update_in_epilogue(self.ctx))
 
     def _param_set(self, d: dict, what: str) -> AttnParamSet:
         f32 = torch.float32

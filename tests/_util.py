@@ -48,6 +48,28 @@ def to_dev(a, dtype: str, device="cuda"):
     return t.to(device)
 
 
+def fma_f32(a, b, c):
+    """a * b + c over float32 arrays with one rounding to float32 (nearest even), as fmaf does.
+
+    The product of two float32 values is exact in float64; the sum is formed in
+    float64 with its exact error (two-sum), and where the float64 sum lies on a
+    float32 midpoint the error decides the side, so the result never suffers
+    double rounding.  Finite inputs whose result stays finite and normal."""
+    a, b, c = (np.asarray(v, dtype=np.float32) for v in (a, b, c))
+    p = a.astype(np.float64) * b.astype(np.float64)
+    q = c.astype(np.float64)
+    s = p + q
+    bv = s - p
+    err = (p - (s - bv)) + (q - bv)
+    r = s.astype(np.float32)
+    r64 = r.astype(np.float64)
+    up = np.nextafter(r, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(r, np.float32(-np.inf)).astype(np.float64)
+    r = np.where((s == (r64 + up) / 2) & (err > 0), up.astype(np.float32), r)
+    r = np.where((s == (r64 + dn) / 2) & (err < 0), dn.astype(np.float32), r)
+    return r
+
+
 def to_np(t):
     return t.detach().float().cpu().numpy().astype(np.float64)
 

@@ -92,7 +92,11 @@ def test_null_context_is_rejected(T):
     assert L.tpmlp_launch_count(None) == 0
     L.tpmlp_destroy(None)
     assert L.tpmlp_adamw_step(None, None, None) == T.ERR_ARG
+    assert L.tpmlp_set_update_in_backward(None, 1, 0.1) == T.ERR_ARG
+    assert L.tpmlp_update_in_epilogue(None) == 0
     assert L.tpattn_sgd_step(None, 0.1) == T.ERR_ARG
+    assert L.tpattn_set_update_in_backward(None, 1, 0.1) == T.ERR_ARG
+    assert L.tpattn_update_in_epilogue(None) == 0
     assert L.tpattn_bind_adam_state(None, None, None) == T.ERR_ARG
     assert L.tpattn_adamw_step(None, None, None) == T.ERR_ARG
     assert L.tpattn_sync(None) == T.ERR_ARG
