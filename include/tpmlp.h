@@ -114,8 +114,9 @@ TPMLP_API tpmlp_status tpmlp_create(const tpmlp_config* cfg, void* cuda_stream, 
 TPMLP_API size_t tpmlp_workspace_bytes(const tpmlp_config* cfg);
 
 /* Hand the context `bytes` of device memory at `dev` (256-byte aligned).  The
- * caller owns it and keeps it alive until tpmlp_destroy. Zeroes the status
- * word (enqueued on the stream). */
+ * caller owns it and keeps it alive until tpmlp_destroy.  Zeroes the status
+ * word and the split GEMMs' arrival flags (enqueued on the stream); the rest
+ * of the workspace needs no initial contents. */
 TPMLP_API tpmlp_status tpmlp_bind_workspace(tpmlp_ctx* ctx, void* dev, size_t bytes);
 
 /* Change the stream later calls enqueue on. */
@@ -372,6 +373,7 @@ typedef struct {
 
 TPMLP_API size_t tpattn_workspace_bytes(const tpattn_config* cfg);
 TPMLP_API tpmlp_status tpattn_create(const tpattn_config* cfg, void* cuda_stream, tpattn_ctx** out);
+/* As tpmlp_bind_workspace, for the attention context (tpattn_workspace_bytes). */
 TPMLP_API tpmlp_status tpattn_bind_workspace(tpattn_ctx* ctx, void* dev, size_t bytes);
 /* batch sequences of seq tokens (seq % 64 == 0, seq <= max_seq); t divides n_kv_heads.
  * x [batch*seq, H], norm_w [H], w_qkv [(n_q+2n_kv) d, H], w_o [H, n_q d], b_o [H] -> y.

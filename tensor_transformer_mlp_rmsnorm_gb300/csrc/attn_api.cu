@@ -479,7 +479,9 @@ tpmlp_status tpattn_bind_workspace(tpattn_ctx* c, void* dev, size_t bytes) {
   if (!dev || (reinterpret_cast<uintptr_t>(dev) & 255u)) return c->fail(TPMLP_ERR_ARG, "workspace must be 256-byte aligned");
   if (bytes < c->L.total) return c->fail(TPMLP_ERR_ARG, "workspace too small");
   c->ws = static_cast<uint8_t*>(dev);
+  // the status word and the split GEMMs' arrival flags (epoch-tagged: stale values must not match)
   cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + c->L.split_ctr, 0, SPLIT_COUNTER_WORDS * sizeof(uint32_t), c->stream);
   return e == cudaSuccess ? TPMLP_OK : c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
 }
 

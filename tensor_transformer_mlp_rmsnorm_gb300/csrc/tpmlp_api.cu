@@ -389,7 +389,10 @@ tpmlp_status tpmlp_bind_workspace(tpmlp_ctx* c, void* dev, size_t bytes) {
   if (bytes < c->L.total) return c->fail(TPMLP_ERR_ARG, "workspace too small");
   c->ws = static_cast<uint8_t*>(dev);
   c->ws_bytes = bytes;
+  // the status word, and the split GEMMs' arrival flags: a flag counts when it
+  // holds its launch's epoch, so whatever the memory held before must not
   cudaError_t e = cudaMemsetAsync(c->ws + c->L.status, 0, 256, c->stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(c->ws + c->L.split_ctr, 0, SPLIT_COUNTER_WORDS * sizeof(uint32_t), c->stream);
   if (e != cudaSuccess) return c->fail(TPMLP_ERR_CUDA, cudaGetErrorString(e));
   return TPMLP_OK;
 }

@@ -76,8 +76,12 @@ struct GemmDesc {
   // wave of the persistent grid are cut into up to four contiguous K parts
   // run by otherwise idle CTAs; the parts after the first leave their f32
   // accumulators in `split_scratch` and count their arrival in
-  // `split_counters` (zeroed on the stream before each split launch), and
-  // the first part adds the partials in part order.  NULL disables the split.
+  // `split_counters` by writing the launch's epoch there, and the first
+  // part adds the partials in part order.  NULL disables the split.  The
+  // flags are zeroed when the workspace is bound and epochs are unique in
+  // the process (so workspaces shared between contexts stay safe); a 32-bit
+  // epoch repeats after 2^32 - 1 split launches, and a stale flag could then
+  // match only if its slot had gone unwritten for all of them.
   float* split_scratch = nullptr;
   size_t split_scratch_bytes = 0;
   uint32_t* split_counters = nullptr;
