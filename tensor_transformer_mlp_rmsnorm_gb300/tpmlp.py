@@ -339,12 +339,15 @@ class TPMLP:
             self._t(g["b_1"], (self.F,), f32, "db_1") if self.act == "gelu" else None,
             self._t(g["w_down"], (self.H, self.F), f32, "dw_down"), self._t(g["b_down"], (self.H,), f32, "db_down")),
             self.ctx)
+        # the updates read these gradients later: hold them until the next backward
+        self._grads = g
         return dx, g
 
     def bind_master(self, masters: dict | None):
         f32 = torch.float32
         if masters is None:
             _check(lib().tpmlp_bind_master(self.ctx, None, None, None, None, None), self.ctx)
+            self._masters = None
             return
         _check(lib().tpmlp_bind_master(
             self.ctx, self._t(masters["norm_w"], (self.H,), f32, "norm_w"),
@@ -352,6 +355,7 @@ class TPMLP:
             self._t(masters["b_1"], (self.F,), f32, "b_1") if self.act == "gelu" else None,
             self._t(masters["w_down"], (self.H, self.F), f32, "w_down"),
             self._t(masters["b_down"], (self.H,), f32, "b_down")), self.ctx)
+        self._masters = masters  # keep the tensors alive while bound
 
     def sgd_step(self, lr: float):
         _check(lib().tpmlp_sgd_step(self.ctx, float(lr)), self.ctx)
@@ -516,6 +520,8 @@ class TPAttn:
                                       self._t(g["w_qkv"], (self.W, self.H), f32, "dw_qkv"),
                                       self._t(g["w_o"], (self.H, self.nq * self.d), f32, "dw_o"),
                                       self._t(g["b_o"], (self.H,), f32, "db_o")), self.ctx)
+        # the updates read these gradients later: hold them until the next backward
+        self._grads = g
         return dx, g
 
     def bind_master(self, m: dict | None):
