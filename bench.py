@@ -151,6 +151,20 @@ def choose_peak(pk: dict, clk, region_s: float, ratio: float = 1.0):
 
 
 
+def max_over_ranks(torch, times, dev, world: int):
+    """Each timing as its maximum over the ranks (an all-reduce on `dev`; unchanged at one rank)."""
+    if world <= 1:
+        return list(times)
+    tt = torch.tensor([float(v) for v in times], dtype=torch.float64, device=dev)
+    torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
+    return [float(v) for v in tt.tolist()]
+
+
+def job_tflops(flops_per_rank_step: float, steps: int, world: int, ms: float) -> float:
+    """Whole-job throughput: the work of all ranks over the slowest rank's time."""
+    return flops_per_rank_step * steps * world / (ms / 1e3) / 1e12
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -591,12 +605,9 @@ def ours_attn(args):
     clk = clocks.stop()
     barrier()
     m.sync()
-    if world > 1:
-        tt = torch.tensor([ms, ems], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, ems = float(tt[0].item()), float(tt[1].item())
+    ms, ems = max_over_ranks(torch, [ms, ems], dev, world)
     flops = cfg.gemm_flops
-    value = flops * args.steps * world / (ms / 1e3) / 1e12
+    value = job_tflops(flops, args.steps, world, ms)
     h2d_rate = h2d_gbps(torch, x_host, y)
     if rank != 0:
         if world > 1:
@@ -653,7 +664,7 @@ def ours_attn(args):
         "kernels_ms_per_step": {k: v[0] / args.steps for k, v in sorted(ktimes.items(), key=lambda kv: -kv[1][0])},
         "instrumented_ms_per_step": kms / args.steps,
         "roofline": roof, "cpu_baseline": cpu,
-        "e2e": {"value": flops * e2e_steps * world / (ems / 1e3) / 1e12, "unit": "TFLOP/s",
+        "e2e": {"value": job_tflops(flops, e2e_steps, world, ems), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": 2 * N * H * 2, "d2h_bytes_per_step": 4, "steps": e2e_steps,
                 "h2d": "pinned host -> device on a copy stream, double-buffered (step i+1's copy overlaps step i)",
                 "h2d_gbps_alone": h2d_rate},
@@ -775,15 +786,12 @@ def ours(args):
     clk = clocks.stop()
     barrier()
     m.sync()
-    if world > 1:
-        tt = torch.tensor([ms, ems], device=dev)
-        torch.distributed.all_reduce(tt, op=torch.distributed.ReduceOp.MAX)
-        ms, ems = float(tt[0].item()), float(tt[1].item())
+    ms, ems = max_over_ranks(torch, [ms, ems], dev, world)
     flops_step = cfg.gemm_flops
     e = 2 if cfg.dtype == "bf16" else 4
     nP = sum(v.numel() for v in params.values())
-    value = flops_step * args.steps * world / (ms / 1e3) / 1e12
-    e2e_value = flops_step * e2e_steps * world / (ems / 1e3) / 1e12
+    value = job_tflops(flops_step, args.steps, world, ms)
+    e2e_value = job_tflops(flops_step, e2e_steps, world, ems)
     h2d_rate = h2d_gbps(torch, x_host, y)
 
     if rank != 0:
