@@ -58,12 +58,15 @@ KERNEL_FAMILIES = {
     "rowwise": ("rowwise.cu", "vec.cuh", "epilogue.cuh"),
     "optim": ("optim.cu", "vec.cuh"),
     "fp8": ("fp8.cu",),
+    "flash": ("flash_attn.cu", "ptx_sm103.cuh", "f32x2.cuh", "tma_maps.cuh", "vec.cuh"),
 }
 
 
 def kernel_family(kernel: str) -> str:
     if kernel.startswith("gemm_"):
         return "gemm"
+    if kernel.startswith("flash_"):
+        return "flash"
     if kernel in ("fp8_amax", "fp8_cast"):
         return "fp8"
     return "optim" if kernel in ("grad_sqnorm", "adamw_update") else "rowwise"
@@ -625,11 +628,13 @@ def ours_attn(args):
               "flash_attn_fwd": 2 * causal, "flash_attn_bwd": 4 * causal}
     top = max(ktimes, key=lambda k: ktimes[k][0])
     per_launch = ktimes[top][0] / max(1, ktimes[top][1])
+    # DRAM bytes per launch from a one-launch ncu capture on the current sources (attention GEMMs: none)
+    traffic, traffic_src = recorded_traffic(cfg.name, t, N, top) if top.startswith("flash_") else (None, None)
     if top in kflops:
         ach = kflops[top] / (per_launch / 1e3) / 1e12
         peak, kind = choose_peak(pk, clk, (ms + ems + kms) / 1e3)
         roof = {"kernel": top, "bound": "tensor", "achieved": ach, "peak": peak,
-                "unit": "TFLOP/s", "frac": ach / peak, "traffic": None,
+                "unit": "TFLOP/s", "frac": ach / peak, "traffic": traffic, "traffic_source": traffic_src,
                 "frac_of_burst": ach / pk["bf16_tflops"], "frac_of_sustained": ach / pk["bf16_tflops_sustained"],
                 "peak_kind": f"bf16 {kind} ({pk_src})", "avg_launch_ms": per_launch,
                 "note": "attention products counted over the causal half of the score square"
@@ -644,7 +649,8 @@ def ours_attn(args):
                   "flash_dq_cast": N * nq * d * (4.0 + 2.0)}.get(top)
         ach = nbytes / (per_launch / 1e3) / 1e9 if nbytes else None
         roof = {"kernel": top, "bound": "hbm", "achieved": ach, "peak": pk["hbm_gbs"], "unit": "GB/s",
-                "frac": ach / pk["hbm_gbs"] if ach else None, "traffic": None, "avg_launch_ms": per_launch}
+                "frac": ach / pk["hbm_gbs"] if ach else None, "traffic": traffic, "traffic_source": traffic_src,
+                "avg_launch_ms": per_launch}
     gemm_ms = sum(v[0] for k, v in ktimes.items() if k in kflops)
     cpu = None
     if cpu_inp is not None:

@@ -183,8 +183,15 @@ def test_traffic_record_lookup(tmp_path, monkeypatch):
     assert bench.recorded_traffic("w", 8, 16, "gemm_a", "fp8") == (55.0, "profiles/x.md")
     assert bench.recorded_traffic("w", 8, 16, "sgd_update") == (None, None)  # rowwise digest does not match
     assert bench.recorded_traffic("w", 4, 16, "gemm_a") == (None, None)
+    (tmp_path / "profiles" / "y.md").write_text(
+        "traffic-record: workload=a t=8 tokens=32 digest=flash:%s flash_attn_bwd=99\n" % dg["flash"])
+    assert bench.kernel_family("flash_attn_bwd") == "flash"
+    assert bench.recorded_traffic("a", 8, 32, "flash_attn_bwd") == (99.0, "profiles/y.md")
     (csrc / "gemm_tc.cu").write_text("// changed")
     assert bench.recorded_traffic("w", 8, 16, "gemm_a") == (None, None)
+    assert bench.recorded_traffic("a", 8, 32, "flash_attn_bwd") == (99.0, "profiles/y.md")
+    (csrc / "flash_attn.cu").write_text("// changed")
+    assert bench.recorded_traffic("a", 8, 32, "flash_attn_bwd") == (None, None)
 
 
 def test_cpu_baselines_time_the_oracle_on_a_bounded_sample():
